@@ -1,0 +1,317 @@
+"""Pins of the fp64 oracle to facts outside itself (CPU only).
+
+Each test checks one oracle function against something it does not compute
+itself: a closed form, a hand-worked case, a library routine, an invariant of
+the definitions, or brute force on tiny inputs.  Definitions followed: page
+"MiniCPM4: Ultra-Efficient LLMs on End Devices" (paper-graph-ui digest),
+section "InfLLM v2".
+"""
+
+import itertools
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synthetic_inputs as S
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- kernels ----
+
+@pytest.mark.parametrize("L,expect", [(0, 0), (31, 0), (32, 1), (47, 1), (48, 2), (4096, 255),
+                                      (32768, 2047), (131072, 8191), (131080, 8191)])
+def test_kernel_count_closed_form(L, expect):
+    # S_j = K[j s : j s + p] must fit in L keys: j s + p <= L.
+    assert O.n_complete_kernels(L, 32, 16) == expect
+    assert expect == sum(1 for j in range(L) if j * 16 + 32 <= L)
+
+
+def test_compress_keys_prefix_sum_closed_form():
+    rng = np.random.default_rng(5)
+    for (L, p, s) in [(200, 32, 16), (97, 8, 3), (64, 64, 64), (31, 32, 16)]:
+        K = rng.standard_normal((L, 6))
+        Kc = O.compress_keys(K, p, s)
+        P = np.concatenate([np.zeros((1, 6)), np.cumsum(K, axis=0)])
+        n = O.n_complete_kernels(L, p, s)
+        ref = np.array([(P[j * s + p] - P[j * s]) / p for j in range(n)]).reshape(n, 6)
+        assert Kc.shape == (n, 6)
+        np.testing.assert_allclose(Kc, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_compress_keys_arithmetic_ramp():
+    # K[t] = t: the mean of t = js .. js+p-1 is js + (p-1)/2.
+    L, p, s = 300, 32, 16
+    K = np.arange(L, dtype=np.float64)[:, None]
+    Kc = O.compress_keys(K, p, s)
+    assert np.array_equal(Kc[:, 0], np.array([j * s + (p - 1) / 2 for j in range(Kc.shape[0])]))
+
+
+# ------------------------------------------------------ kernel softmax ----
+
+def test_kernel_softmax_matches_torch_softmax():
+    rng = np.random.default_rng(1)
+    z = rng.standard_normal((16, 300)) * 7.0
+    ref = torch.softmax(torch.from_numpy(z), dim=1).numpy()
+    np.testing.assert_allclose(O.kernel_softmax(z), ref, rtol=1e-13, atol=0)
+
+
+def test_group_relevance_is_head_mean_and_sums_to_one():
+    rng = np.random.default_rng(2)
+    z = rng.standard_normal((16, 77))
+    g = O.group_relevance(z)
+    ref = torch.softmax(torch.from_numpy(z), dim=1).mean(dim=0).numpy()
+    np.testing.assert_allclose(g, ref, rtol=1e-13)
+    assert abs(g.sum() - 1.0) < 1e-12
+
+
+# ------------------------------------------------------- block relevance ----
+
+def _block_relevance_brute(g, i, m, p, s):
+    """Max over kernels whose key set meets the block's key set (set intersection)."""
+    c = i // m
+    r = []
+    for j in range(c + 1):
+        bkeys = set(range(j * m, (j + 1) * m))
+        vals = [g[k] for k in range(len(g)) if bkeys & set(range(k * s, k * s + p))]
+        r.append(max(vals) if vals else -math.inf)
+    return np.array(r)
+
+
+@pytest.mark.parametrize("m,p,s", [(64, 32, 16), (16, 8, 4), (32, 32, 16), (8, 12, 5)])
+def test_block_relevance_brute_force(m, p, s):
+    rng = np.random.default_rng(m * 100 + p + s)
+    for i in [0, 5, p - 1, p, m - 1, m, 3 * m + 7, 6 * m - 1, 400]:
+        nv = O.visible_kernel_count(i, p, s)
+        g = rng.random(nv)
+        np.testing.assert_array_equal(O.block_relevance(g, i, m, p, s),
+                                      _block_relevance_brute(g, i, m, p, s))
+
+
+def test_block_relevance_recommended_shape_uses_kernels_4j_minus_1_to_4j_plus_3():
+    i = 64 * 20 + 40
+    nv = O.visible_kernel_count(i, 32, 16)
+    g = np.random.default_rng(3).random(nv)
+    r = O.block_relevance(g, i, 64, 32, 16)
+    for j in range(r.shape[0]):
+        ks = [k for k in range(4 * j - 1, 4 * j + 4) if 0 <= k < nv]
+        expect = max(g[k] for k in ks) if ks else -math.inf
+        assert r[j] == expect
+
+
+# --------------------------------------------------------- forced blocks ----
+
+@pytest.mark.parametrize("i,expect", [(0, [0]), (63, [0]), (64, [0, 1]), (127, [0, 1]),
+                                      (128, [0, 1, 2]), (1000, [0, 14, 15]),
+                                      (131071, [0, 2046, 2047])])
+def test_forced_blocks_hand_cases(i, expect):
+    assert O.forced_blocks(i, 64, 1, 2) == expect
+
+
+# ----------------------------------------------------------------- top-k ----
+
+def _topk_brute(r, forced, topk, includes_forced):
+    """Enumerate every subset of candidates; keep those that dominate the rest."""
+    fset = set(forced)
+    cand = [j for j in range(len(r)) if j not in fset and np.isfinite(r[j])]
+    n = max(0, (topk - len(forced)) if includes_forced else topk)
+    n = min(n, len(cand))
+    key = {j: (r[j], -j) for j in cand}
+    good = []
+    for sub in itertools.combinations(cand, n):
+        rest = [j for j in cand if j not in sub]
+        if all(key[a] > key[b] for a in sub for b in rest):
+            good.append(sorted(fset | set(sub)))
+    assert len(good) == 1
+    return good[0]
+
+
+def test_topk_brute_force_with_ties():
+    rng = np.random.default_rng(11)
+    for trial in range(60):
+        nb = int(rng.integers(1, 11))
+        r = rng.integers(0, 4, nb).astype(np.float64) / 4.0   # many exact ties
+        r[rng.random(nb) < 0.15] = -np.inf
+        i = nb * 64 - 1
+        forced = O.forced_blocks(i, 64, 1, 2)
+        for topk in (3, 4, 6):
+            for inc in (True, False):
+                got = O.top_k_blocks(r, forced, topk, inc).tolist()
+                assert got == _topk_brute(r, forced, topk, inc)
+
+
+def test_hand_worked_selections():
+    spec = json.load(open(os.path.join(GOLDEN, "hand_selection.json")))
+    st_ = spec["settings"]
+    for case in spec["cases"]:
+        K = np.zeros((st_["L"], st_["d"]))
+        for a, b in case["spans"]:
+            K[a:b, 0] = math.log(4.0)
+        q = np.array(case["q_heads"], dtype=np.float64)
+        Kc = O.compress_keys(K, st_["kernel"], st_["stride"])
+        for topk_s, expect in case["select"].items():
+            st = O.Settings(block=st_["block"], kernel=st_["kernel"], stride=st_["stride"],
+                            topk=int(topk_s), n_init=st_["n_init"], n_local=st_["n_local"],
+                            includes_forced=True, score_scale=st_["score_scale"])
+            sel = O.select_for_query(q, Kc, st_["i"], st)
+            want = [float(Fraction(a, b)) for a, b in zip(case["r_block_num"], case["r_block_den"])]
+            np.testing.assert_allclose(sel.r, want, rtol=1e-14)
+            assert sel.blocks.tolist() == expect, (case["name"], topk_s)
+
+
+# --------------------------------------------------- selection invariants ----
+
+def _rand_case(seed, L=1500, G=16, d=8):
+    rng = np.random.default_rng(seed)
+    return rng.standard_normal((G, d)), rng.standard_normal((L, d))
+
+
+def test_selection_key_shift_invariance():
+    q, K = _rand_case(4)
+    st = O.Settings(topk=8, score_scale=1.0)
+    i = K.shape[0] - 1
+    base = O.select_for_query(q, O.compress_keys(K, 32, 16), i, st)
+    shifted = O.select_for_query(q, O.compress_keys(K + np.array([0.5, -1.25, 2.0, 0, 0, 1, 0, -3.0]), 32, 16), i, st)
+    np.testing.assert_allclose(shifted.r, base.r, rtol=1e-9)
+    assert shifted.blocks.tolist() == base.blocks.tolist()
+
+
+def test_selection_head_permutation_invariance():
+    q, K = _rand_case(5)
+    st = O.Settings(topk=8)
+    Kc = O.compress_keys(K, 32, 16)
+    i = K.shape[0] - 1
+    base = O.select_for_query(q, Kc, i, st)
+    perm = O.select_for_query(q[np.random.default_rng(0).permutation(16)], Kc, i, st)
+    np.testing.assert_allclose(perm.r, base.r, rtol=1e-12)
+    assert perm.blocks.tolist() == base.blocks.tolist()
+
+
+def test_selection_structural_invariants():
+    q, K = _rand_case(6, L=2000)
+    Kc = O.compress_keys(K, 32, 16)
+    for inc in (True, False):
+        st = O.Settings(topk=10, includes_forced=inc)
+        for i in [0, 20, 31, 63, 64, 100, 640, 1999]:
+            sel = O.select_for_query(q, Kc, i, st)
+            c = i // 64
+            forced = O.forced_blocks(i, 64, 1, 2)
+            assert set(forced) <= set(sel.blocks.tolist())
+            assert sel.blocks.max() <= c and sel.blocks.tolist() == sorted(set(sel.blocks.tolist()))
+            n_vis_blocks = c + 1
+            want = min(10, n_vis_blocks) if inc else min(10 + len(forced), n_vis_blocks)
+            assert len(sel.blocks) == want, (i, inc)
+
+
+def test_planted_blocks_are_selected_on_4k_decode_workload():
+    inp = S.make_inputs(S.WORKLOADS["decode_4k"])
+    st = O.Settings(topk=16)
+    sel = O.run_selection(inp, st)[(0, 0, 0)]
+    assert set(inp.planted[0, 0].tolist()) <= set(sel.blocks.tolist())
+    assert len(sel.blocks) == 16
+
+
+# ------------------------------------------------------------- attention ----
+
+def test_attention_dense_degeneracy_matches_torch_sdpa():
+    # With every visible block selected the method is exact dense causal
+    # attention ("Initial and local tokens always selected": l <= k m).
+    rng = np.random.default_rng(8)
+    G, d, L = 16, 128, 300
+    q_all = rng.standard_normal((L, G, d))
+    K = rng.standard_normal((L, d))
+    V = rng.standard_normal((L, d))
+    qt = torch.from_numpy(q_all).permute(1, 0, 2)[None]            # [1, G, L, d]
+    kt = torch.from_numpy(K)[None, None].expand(1, G, L, d)
+    vt = torch.from_numpy(V)[None, None].expand(1, G, L, d)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, is_causal=True)[0]  # [G, L, d]
+    for i in [0, 1, 63, 64, 150, 299]:
+        blocks = np.arange(i // 64 + 1)
+        out, lse = O.sparse_attention(q_all[i], K, V, blocks, i, 64, 1 / math.sqrt(d))
+        np.testing.assert_allclose(out, ref[:, i].numpy(), rtol=1e-10, atol=1e-12)
+        sc = (q_all[i] @ K[: i + 1].T) / math.sqrt(d)
+        np.testing.assert_allclose(lse, torch.logsumexp(torch.from_numpy(sc), dim=1).numpy(), rtol=1e-13)
+
+
+def test_attention_block_mask_matches_torch_sdpa_with_mask():
+    rng = np.random.default_rng(9)
+    G, d, L = 16, 32, 640
+    q = rng.standard_normal((G, d))
+    K = rng.standard_normal((L, d))
+    V = rng.standard_normal((L, d))
+    i = 600
+    blocks = np.array([0, 3, 5, 8, 9])
+    mask = np.zeros(L, dtype=bool)
+    for j in blocks:
+        mask[j * 64:(j + 1) * 64] = True
+    mask[i + 1:] = False
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q)[None, :, None], torch.from_numpy(K)[None, None].expand(1, G, L, d),
+        torch.from_numpy(V)[None, None].expand(1, G, L, d),
+        attn_mask=torch.from_numpy(mask)[None, None, None], scale=0.3)[0, :, 0]
+    out, _ = O.sparse_attention(q, K, V, blocks, i, 64, 0.3)
+    np.testing.assert_allclose(out, ref.numpy(), rtol=1e-11, atol=1e-13)
+
+
+def test_attention_split_merge_identity():
+    # Softmax over a union equals the lse-weighted merge of its parts: the
+    # identity the split-KV combine relies on.
+    rng = np.random.default_rng(10)
+    G, d, L = 16, 16, 1024
+    q, K, V = rng.standard_normal((G, d)), rng.standard_normal((L, d)), rng.standard_normal((L, d))
+    i = L - 1
+    all_b = np.array([0, 2, 3, 7, 11, 12, 15])
+    o_all, l_all = O.sparse_attention(q, K, V, all_b, i, 64, 0.25)
+    parts = [all_b[:3], all_b[3:5], all_b[5:]]
+    res = [O.sparse_attention(q, K, V, p_, i, 64, 0.25) for p_ in parts]
+    M = np.max([r[1] for r in res], axis=0)
+    w = [np.exp(r[1] - M) for r in res]
+    merged = sum(wi[:, None] * r[0] for wi, r in zip(w, res)) / sum(w)[:, None]
+    np.testing.assert_allclose(merged, o_all, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(M + np.log(sum(w)), l_all, rtol=1e-13)
+
+
+# ------------------------------------------------ the pins catch mistakes ----
+
+def _planted_mistakes():
+    orig_br = O.block_relevance
+
+    def br_off_by_one(g, i, m, p, s):                  # kernel range shifted by one
+        r = orig_br(np.roll(g, 1), i, m, p, s)
+        return r
+
+    def gr_max_not_mean(z):                            # max over heads instead of mean
+        return O.kernel_softmax(z).max(axis=0)
+
+    def ks_no_norm(z):                                 # dropped normaliser
+        return np.exp(z - z.max(axis=1, keepdims=True))
+
+    def forced_no_prev(i, m, n_init, n_local):         # local window of one block
+        c = i // m
+        return sorted({0, c})
+
+    return [("block_relevance", br_off_by_one), ("group_relevance", gr_max_not_mean),
+            ("kernel_softmax", ks_no_norm), ("forced_blocks", forced_no_prev)]
+
+
+@pytest.mark.parametrize("name,bad", _planted_mistakes())
+def test_planted_oracle_mistakes_are_caught(monkeypatch, name, bad):
+    monkeypatch.setattr(O.infllmv2_oracle, name, bad)
+    monkeypatch.setattr(O, name, bad)
+    checks = [test_hand_worked_selections, test_group_relevance_is_head_mean_and_sums_to_one,
+              test_selection_structural_invariants,
+              lambda: test_block_relevance_brute_force(64, 32, 16),
+              lambda: test_forced_blocks_hand_cases(1000, [0, 14, 15])]
+    failed = 0
+    for chk in checks:
+        try:
+            chk()
+        except AssertionError:
+            failed += 1
+    assert failed > 0, f"planted mistake in {name} went unnoticed"
