@@ -1,0 +1,181 @@
+/*
+ * infllmv2.h -- C ABI of the InfLLM v2 block-sparse attention library (sm_103a).
+ *
+ * The method is the trainable sparse attention of the MiniCPM4 technical
+ * report ("MiniCPM4: Ultra-Efficient LLMs on End Devices", section "InfLLM v2:
+ * Trainable Sparse Attention for Both Prefilling and Decoding"; cited below as
+ * [InfLLM v2 > paragraph, equation]).  Three stages:
+ *
+ *   1. infllmv2_compress_keys       semantic-kernel key means
+ *                                   [InfLLM v2 > Semantic kernels, eq. S_j]
+ *   2. infllmv2_select_blocks       per-head kernel softmax, GQA group mean,
+ *                                   block max, forced blocks, top-k
+ *                                   [InfLLM v2 > Semantic kernels, eqs. r_kernel,
+ *                                   r_block; > Query group sharing, eq. r_group;
+ *                                   > Top-K implementation and the LSE bottleneck;
+ *                                   > Initial and local tokens always selected]
+ *   3. infllmv2_sparse_attn_decode  exact softmax attention over the selected
+ *      infllmv2_sparse_attn_prefill KV blocks [InfLLM v2 > Block-level key-value
+ *                                   partitioning, eq. B_j; > Complexity analysis]
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every tensor argument is a DEVICE pointer owned by the caller.  The
+ *   library never allocates, frees or synchronises in these calls; all work
+ *   is enqueued on `stream` (a cudaStream_t passed as void*, NULL = legacy
+ *   default stream) and the calls return before it runs.
+ * - Shapes (row-major, innermost last; d = head_dim, G = group_size,
+ *   Hq = n_kv_heads * G, n_c(L) = floor((L - p)/s) + 1 complete kernels,
+ *   n_b(L) = ceil(L / m) blocks):
+ *       q          bf16  [batch, n_q, Hq, d]        (heads h*G .. h*G+G-1 share KV head h)
+ *       k_cache    bf16  [batch, n_kv_heads, max_kv_len, d]
+ *       v_cache    bf16  [batch, n_kv_heads, max_kv_len, d]
+ *       kv_lens    int32 [batch]                    (L_b, including the n_q query tokens)
+ *       kc         bf16  [batch, n_kv_heads, 2, n_c(max_kv_len), d]
+ *                  plane 0 holds hi = bf16(mean), plane 1 lo = bf16(mean - hi):
+ *                  hi + lo is the fp32 kernel mean to 16 significant bits.
+ *       block_idx  int32 [batch, n_kv_heads, n_q, k_max]   ascending, padded with -1
+ *       n_selected int32 [batch, n_kv_heads, n_q]
+ *       out        bf16  [batch, n_q, Hq, d]
+ *       lse        fp32  [batch, n_q, Hq]           natural-log sum of exp of the
+ *                                                   scaled scores of the attended keys
+ * - Query t (0 <= t < n_q) of sequence b sits at position i = L_b - n_q + t; it
+ *   attends keys 0..i of its selected blocks (inclusive causal mask).  The
+ *   same rule serves decode (n_q = 1), speculative verification (small n_q)
+ *   and causal prefill (n_q = L_b).
+ * - Pointers must be 16-byte aligned.  Supported shape: head_dim 128,
+ *   group_size 16, block_size 64, kernel_size 32, kernel_stride 16;
+ *   anything else returns INFLLMV2_UNSUPPORTED.
+ * - Return codes are INFLLMV2_* below; on failure nothing was launched and
+ *   infllmv2_last_error() describes why (thread-local string).  Problems only
+ *   the device can see (a kv_len outside [n_q, max_kv_len], a bounded wait
+ *   that gave up) are recorded in a device status word read by
+ *   infllmv2_get_device_status(); the affected unit writes zeros / an empty
+ *   selection instead of reading out of bounds.
+ * - No C++ exception crosses this boundary.
+ */
+#ifndef INFLLMV2_H
+#define INFLLMV2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define INFLLMV2_OK                  0
+#define INFLLMV2_INVALID_ARGUMENT    1  /* null pointer, bad size, topk < forced count, ... */
+#define INFLLMV2_UNSUPPORTED         2  /* shape outside the supported set, misaligned pointer */
+#define INFLLMV2_WORKSPACE_TOO_SMALL 3
+#define INFLLMV2_CUDA_ERROR          4  /* launch failed; message from the CUDA runtime */
+
+/* Device status bits (infllmv2_get_device_status). */
+#define INFLLMV2_DEVICE_BAD_KV_LEN   0x1u  /* kv_lens[b] < n_q or > max_kv_len */
+#define INFLLMV2_DEVICE_TIMEOUT      0x2u  /* a bounded mbarrier wait expired */
+
+/* Workspace kinds for infllmv2_workspace_size. */
+#define INFLLMV2_OP_SELECT  1
+#define INFLLMV2_OP_DECODE  2
+#define INFLLMV2_OP_PREFILL 3
+
+typedef struct infllmv2_params {
+  int32_t batch;                 /* B */
+  int32_t n_kv_heads;            /* Hkv */
+  int32_t group_size;            /* G, query heads per KV head (16) */
+  int32_t head_dim;              /* d (128) */
+  int32_t block_size;            /* m (64)  [InfLLM v2 > Block-level key-value partitioning] */
+  int32_t kernel_size;           /* p (32)  [InfLLM v2 > Semantic kernels] */
+  int32_t kernel_stride;         /* s (16)  [InfLLM v2 > Semantic kernels] */
+  int32_t topk;                  /* k, blocks per query group */
+  int32_t n_init_blocks;         /* forced initial blocks (1) [InfLLM v2 > Initial and local tokens] */
+  int32_t n_local_blocks;        /* forced local blocks ending at the query's block (2) */
+  int32_t topk_includes_forced;  /* 1: forced blocks count toward k; 0: k scored blocks on top */
+  int32_t max_kv_len;            /* cache capacity per (b, h) in tokens */
+  float score_scale;             /* scale inside the kernel softmax (default 1/sqrt(d)) */
+  float attn_scale;              /* attention softmax scale (default 1/sqrt(d)) */
+} infllmv2_params;
+
+/* Fill `p` with the recommended shape (d 128, G 16, m 64, p 32, s 16, one
+ * initial and two local blocks, both scales 1/sqrt(128)). */
+void infllmv2_default_params(infllmv2_params* p, int32_t batch, int32_t n_kv_heads,
+                             int32_t max_kv_len, int32_t topk, int32_t topk_includes_forced);
+
+/* Width of a block_idx row: topk if forced blocks are included, else
+ * topk + n_init_blocks + n_local_blocks.  Negative on invalid params. */
+int32_t infllmv2_max_selected(const infllmv2_params* p);
+
+/* n_c(max_kv_len): rows of each kc plane. */
+int32_t infllmv2_num_kernels(const infllmv2_params* p);
+
+/* Bytes of scratch that `op` (INFLLMV2_OP_*) needs for n_q query tokens per
+ * sequence.  0 on invalid arguments. */
+size_t infllmv2_workspace_size(const infllmv2_params* p, int32_t n_q, int32_t op);
+
+/*
+ * Stage 1: kc[b, h, :, j, :] = split(Mean(k_cache[b, h, j s : j s + p, :])) for
+ * complete kernels j in [kernel_begin, kernel_end) of each sequence.
+ * [InfLLM v2 > Semantic kernels for block relevance scoring, eqs. S_j, r_kernel]
+ *   kernel_begin >= 0 : absolute first kernel;  < 0 : n_c(L_b) + kernel_begin
+ *                       (so -1 recomputes only the newest complete kernel).
+ *   kernel_end   >= 0 : absolute end (clipped to n_c(L_b));  < 0 : n_c(L_b).
+ * Kernels outside the range are left untouched.  The mean is an fp32 sum of
+ * the 32 bf16 keys times 1/32.
+ */
+int infllmv2_compress_keys(const infllmv2_params* p, const void* k_cache, const int32_t* kv_lens,
+                           int32_t kernel_begin, int32_t kernel_end, void* kc, void* stream);
+
+/*
+ * Stage 2: choose the KV blocks of every (b, h_kv, t).
+ *   z[h, j]  = score_scale * q_h . Mean_j            for kernels j visible to i
+ *   g[j]     = (1/G) sum_h softmax_j(z[h, :])         (exact two-pass LSE)
+ *   r[blk]   = max of g over visible kernels meeting the block, -inf if none
+ *   selected = forced blocks (first n_init, the n_local ending at floor(i/m))
+ *              + the best other finite-score blocks ordered by (r desc, index asc):
+ *              topk - |forced| of them if topk_includes_forced, else topk.
+ * block_scores (nullable) receives r as fp32 [B, Hkv, n_q, n_b(max_kv_len)]
+ * (-inf past floor(i/m)).  n_q >= 1; workspace from
+ * infllmv2_workspace_size(p, n_q, INFLLMV2_OP_SELECT).
+ */
+int infllmv2_select_blocks(const infllmv2_params* p, const void* q, int32_t n_q, const void* kc,
+                           const int32_t* kv_lens, int32_t* block_idx, int32_t* n_selected,
+                           float* block_scores, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/*
+ * Stage 3, few queries per sequence (decode n_q = 1, speculative verification
+ * n_q <= 16): the selected blocks of each (b, h_kv, t) are split over CTAs,
+ * each computes an online-softmax partial, and the last CTA of the unit
+ * merges them.  out/lse as documented above (lse nullable).  Only the first
+ * n_selected[b, h, t] entries of block_idx are read; each must lie in
+ * [0, floor(i/m)] (entries outside are skipped).
+ */
+int infllmv2_sparse_attn_decode(const infllmv2_params* p, const void* q, int32_t n_q,
+                                const void* k_cache, const void* v_cache, const int32_t* kv_lens,
+                                const int32_t* block_idx, const int32_t* n_selected, void* out,
+                                float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Stage 3, many queries per sequence (chunked or full causal prefill): same
+ * arguments and result as the decode entry point, any n_q up to max_kv_len.
+ */
+int infllmv2_sparse_attn_prefill(const infllmv2_params* p, const void* q, int32_t n_q,
+                                 const void* k_cache, const void* v_cache, const int32_t* kv_lens,
+                                 const int32_t* block_idx, const int32_t* n_selected, void* out,
+                                 float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Human-readable name of an INFLLMV2_* return code. */
+const char* infllmv2_status_string(int status);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* infllmv2_last_error(void);
+
+/* Read (and if `clear` is nonzero, reset) the device status word of the
+ * current device.  Synchronises the device; not for the hot path. */
+int infllmv2_get_device_status(uint32_t* status_out, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* INFLLMV2_H */

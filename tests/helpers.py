@@ -1,0 +1,159 @@
+"""Shared helpers of the parity tests: device upload, running the CUDA path
+through the binding, and the comparison rules.
+
+Tolerances (fixed by the acceptance rule of the benchmark configurations):
+  * selection: block sets equal, except blocks whose oracle score lies within
+    1e-4 relative of the oracle's boundary score (the last scored block taken);
+  * attention: max |O_gpu - O_ref| <= 2e-3 and mean |O_gpu - O_ref| <= 2e-4
+    over all outputs, O_ref computed by the fp64 oracle on the same selection;
+  * block scores r: relative error <= 1e-4 where the oracle's r is finite
+    (the kernel means carry 16 significant bits, the dot products fp32);
+  * lse: absolute error <= 1e-3 (fp32 accumulation of a natural log).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+SEL_REL = 1e-4
+ATT_MAX = 2e-3
+ATT_MEAN = 2e-4
+R_REL = 1e-4
+LSE_ABS = 1e-3
+
+
+def dev_bf16(bits: np.ndarray, dev):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+
+def kc_to_f64(kc) -> np.ndarray:
+    """bf16 [B, Hkv, 2, n_c, d] hi/lo planes -> fp64 [B, Hkv, n_c, d] (hi + lo)."""
+    import torch
+    a = kc.view(torch.int16).cpu().numpy().view(np.uint16)
+    f = (a.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    return f[:, :, 0] + f[:, :, 1]
+
+
+class GpuRun:
+    """Uploads one input set and runs the three stages on the device."""
+
+    def __init__(self, inp, dev, score_scale=None, attn_scale=None):
+        import torch
+        import trainable_block_sparse_infllm_gb300 as T
+        self.T = T
+        self.inp = inp
+        wl = inp.wl
+        self.dev = dev
+        self.p = T.make_params(wl.batch, wl.n_kv_heads, wl.kv_len, wl.topk, wl.topk_includes_forced,
+                               n_init=wl.n_init, n_local=wl.n_local, score_scale=score_scale,
+                               attn_scale=attn_scale)
+        self.q = dev_bf16(inp.q, dev)
+        self.k = dev_bf16(inp.k, dev)
+        self.v = dev_bf16(inp.v, dev)
+        self.lens = torch.from_numpy(inp.kv_lens.astype(np.int32)).to(dev)
+        self.kmax = T.max_selected(self.p)
+        self.nq = wl.n_q
+        B, H = wl.batch, wl.n_kv_heads
+        self.kc = T.alloc_kc(self.p, dev)
+        self.idx = torch.full((B, H, self.nq, self.kmax), -7, dtype=torch.int32, device=dev)
+        self.nsel = torch.full((B, H, self.nq), -7, dtype=torch.int32, device=dev)
+        self.nbmax = -(-wl.kv_len // wl.block)
+        self.scores = torch.empty((B, H, self.nq, self.nbmax), dtype=torch.float32, device=dev)
+        self.out = torch.full_like(self.q, float("nan"))
+        self.lse = torch.full((B, self.nq, wl.n_heads), float("nan"), dtype=torch.float32, device=dev)
+
+    def compress(self, begin=0, end=-1):
+        self.T.compress_keys(self.p, self.k, self.lens, self.kc, begin, end)
+
+    def select(self, with_scores=True):
+        ws = self.T.alloc_workspace(self.p, self.nq, self.T.OP_SELECT, self.dev)
+        self.T.select_blocks(self.p, self.q, self.kc, self.lens, self.idx, self.nsel,
+                             self.scores if with_scores else None, ws)
+
+    def attend(self, idx=None, nsel=None, prefill=None):
+        idx = self.idx if idx is None else idx
+        nsel = self.nsel if nsel is None else nsel
+        if prefill is None:
+            prefill = self.nq > self.T.DECODE_MAX_NQ
+        op = self.T.OP_PREFILL if prefill else self.T.OP_DECODE
+        ws = self.T.alloc_workspace(self.p, self.nq, op, self.dev)
+        fn = self.T.sparse_attn_prefill if prefill else self.T.sparse_attn_decode
+        fn(self.p, self.q, self.k, self.v, self.lens, idx, nsel, self.out, self.lse, ws)
+
+    def upload_selection(self, sels):
+        """Oracle selections {(b,h,t): Selection} -> device idx/nsel tensors."""
+        import torch
+        B, H = self.inp.wl.batch, self.inp.wl.n_kv_heads
+        idx = np.full((B, H, self.nq, self.kmax), -1, dtype=np.int32)
+        nsel = np.zeros((B, H, self.nq), dtype=np.int32)
+        for (b, h, t), s in sels.items():
+            idx[b, h, t, :len(s.blocks)] = s.blocks
+            nsel[b, h, t] = len(s.blocks)
+        return torch.from_numpy(idx).to(self.dev), torch.from_numpy(nsel).to(self.dev)
+
+
+def selection_mismatch(gpu_blocks, sel, rel=SEL_REL):
+    """None if the GPU set is acceptable for oracle selection `sel`, else a message."""
+    g = set(int(x) for x in gpu_blocks)
+    o = set(int(x) for x in sel.blocks)
+    if len(g) != len(gpu_blocks):
+        return f"duplicate blocks {sorted(gpu_blocks)}"
+    if g == o:
+        return None
+    if len(g) != len(o):
+        return f"size {len(g)} != {len(o)}"
+    rK = sel.boundary
+    for j in g ^ o:
+        if j < 0 or j >= sel.r.shape[0] or not np.isfinite(sel.r[j]) or not np.isfinite(rK):
+            return f"block {j} outside the candidates"
+        if abs(sel.r[j] - rK) > rel * abs(rK):
+            return f"block {j} score {sel.r[j]:.8g} vs boundary {rK:.8g}"
+    return None
+
+
+def check_selections(run, sels, check_scores=True):
+    idx = run.idx.cpu().numpy()
+    nsel = run.nsel.cpu().numpy()
+    scores = run.scores.cpu().numpy() if check_scores else None
+    bad, ties = [], 0
+    for (b, h, t), s in sels.items():
+        n = int(nsel[b, h, t])
+        row = idx[b, h, t]
+        assert 0 <= n <= run.kmax, ((b, h, t), n)
+        assert np.all(row[n:] == -1), ((b, h, t), row)
+        blocks = row[:n]
+        assert np.all(np.diff(blocks) > 0), ((b, h, t), blocks)
+        msg = selection_mismatch(blocks, s)
+        if msg:
+            bad.append(((b, h, t), msg))
+        elif set(blocks.tolist()) != set(s.blocks.tolist()):
+            ties += 1
+        if scores is not None:
+            r_gpu = scores[b, h, t, :s.r.shape[0]]
+            fin = np.isfinite(s.r)
+            assert np.array_equal(np.isfinite(r_gpu), fin), ((b, h, t), "finite pattern")
+            if fin.any():
+                err = np.abs(r_gpu[fin] - s.r[fin]) / np.abs(s.r[fin])
+                assert err.max() <= R_REL, ((b, h, t), float(err.max()))
+            assert np.all(np.isneginf(scores[b, h, t, s.r.shape[0]:])), ((b, h, t), "tail")
+    assert not bad, bad[:5]
+    return ties
+
+
+def check_attention(run, refs, units=None):
+    """refs: {(b,h,t): (O [16, d], lse [16])}.  Returns (max, mean) abs error."""
+    out = run.out.float().cpu().numpy()
+    lse = run.lse.cpu().numpy()
+    errs, total, count, lse_err = [], 0.0, 0, 0.0
+    for (b, h, t), (o_ref, l_ref) in refs.items():
+        o = out[b, t, h * 16:(h + 1) * 16]
+        e = np.abs(o - o_ref)
+        errs.append(e.max())
+        total += e.sum()
+        count += e.size
+        lse_err = max(lse_err, float(np.abs(lse[b, t, h * 16:(h + 1) * 16] - l_ref).max()))
+    mx, mean = float(max(errs)), total / count
+    assert mx <= ATT_MAX and mean <= ATT_MEAN, (mx, mean)
+    assert lse_err <= LSE_ABS, lse_err
+    return mx, mean

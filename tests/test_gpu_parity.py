@@ -1,0 +1,242 @@
+"""GPU parity of the CUDA path (through the C ABI) against the fp64 oracle.
+
+Every test here needs an sm_103a GPU and the built library.  Small cases span
+several tiles of every kernel and ragged tails; the workload tests run the
+benchmark's own launch configuration at full size and compare every decode
+unit (prefill: a stratified sample of query tokens).
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle as O
+import synthetic_inputs as S
+from helpers import (GpuRun, check_attention, check_selections, kc_to_f64)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    d = torch.device("cuda:0")
+    torch.cuda.set_device(d)
+    import trainable_block_sparse_infllm_gb300 as T
+    T.get_device_status(clear=True)
+    yield d
+    torch.cuda.synchronize()
+    assert T.get_device_status(clear=True) == 0
+
+
+def _settings(wl, score_scale=None, attn_scale=None):
+    return O.Settings(topk=wl.topk, n_init=wl.n_init, n_local=wl.n_local,
+                      includes_forced=wl.topk_includes_forced, score_scale=score_scale,
+                      attn_scale=attn_scale)
+
+
+# ------------------------------------------------------------- stage 1 ----
+
+def test_compress_keys_ragged(dev):
+    import torch
+    inp = S.make_random(batch=3, n_kv_heads=2, kv_len=5000, n_q=1, topk=8, seed=21,
+                        kv_lens=[5000, 4093, 31])
+    run = GpuRun(inp, dev)
+    run.kc.view(torch.int16).fill_(0x7FC0)       # NaN sentinel: untouched rows stay NaN
+    run.compress()
+    torch.cuda.synchronize()
+    got = kc_to_f64(run.kc)
+    st = O.Settings()
+    for b in range(3):
+        for h in range(2):
+            ref = O.kc_for(inp, b, h, st)
+            n = ref.shape[0]
+            err = np.abs(got[b, h, :n] - ref)
+            assert np.all(err <= 2.0 ** -16 * np.abs(ref) + 1e-9), (b, h, float(err.max()))
+            assert np.all(np.isnan(got[b, h, n:])), (b, h)
+
+
+def test_compress_keys_incremental_ranges(dev):
+    import torch
+    inp = S.make_random(batch=2, n_kv_heads=1, kv_len=3000, n_q=1, topk=8, seed=22, kv_lens=[3000, 2222])
+    run = GpuRun(inp, dev)
+    run.compress()
+    full = run.kc.clone()
+    run.kc.view(torch.int16).fill_(0x7FC0)
+    run.compress(0, 50)
+    run.compress(50, 100)
+    run.compress(100, -1)
+    assert torch.equal(run.kc.view(torch.int16)[:, :, :, :137], full.view(torch.int16)[:, :, :, :137])
+    # -1: only the newest complete kernel of each sequence
+    run.kc.view(torch.int16).fill_(0x7FC0)
+    run.compress(-1, -1)
+    for b, L in enumerate(inp.kv_lens):
+        n = O.n_complete_kernels(int(L), 32, 16)
+        assert torch.equal(run.kc[b, :, :, n - 1], full[b, :, :, n - 1])
+        assert torch.isnan(run.kc[b, :, :, : n - 1].float()).all()
+
+
+# ------------------------------------------------------------- stage 2 ----
+
+SELECT_CASES = [
+    # batch, hkv, cap, lens, n_q, topk, includes_forced, score_scale
+    (2, 2, 5000, [5000, 3333], 1, 16, True, None),
+    (1, 2, 9000, [9000], 1, 64, True, None),
+    (2, 1, 4100, [4100, 2000], 3, 12, True, 1.0),
+    (1, 2, 6000, [6000], 8, 24, True, None),
+    (2, 1, 3000, [3000, 1500], 16, 10, False, None),
+    (1, 2, 2600, [2600], 17, 16, True, None),          # smallest prefill-path n_q
+    (2, 1, 2000, [2000, 1234], 130, 8, False, None),
+    (1, 1, 700, [700], 700, 4, True, None),             # whole sequence from position 0
+    (3, 1, 300, [300, 40, 20], 20, 4, True, 1.0),       # tiny contexts, no visible kernel
+    (2, 1, 200, [64, 33], 1, 3, True, None),
+]
+
+
+@pytest.mark.parametrize("case", SELECT_CASES, ids=[f"sel{i}" for i in range(len(SELECT_CASES))])
+def test_select_blocks_parity(dev, case):
+    import torch
+    B, H, cap, lens, nq, topk, inc, sscale = case
+    inp = S.make_random(batch=B, n_kv_heads=H, kv_len=cap, n_q=nq, topk=topk, includes_forced=inc,
+                        seed=100 + sum(lens) + nq, kv_lens=lens)
+    run = GpuRun(inp, dev, score_scale=sscale)
+    run.compress()
+    run.select()
+    torch.cuda.synchronize()
+    sels = O.run_selection(inp, _settings(inp.wl, score_scale=sscale))
+    check_selections(run, sels)
+
+
+def test_select_blocks_dense_when_context_short(dev):
+    import torch
+    inp = S.make_random(batch=1, n_kv_heads=2, kv_len=1024, n_q=4, topk=16, seed=5)
+    run = GpuRun(inp, dev)
+    run.compress()
+    run.select()
+    torch.cuda.synchronize()
+    nsel = run.nsel.cpu().numpy()
+    idx = run.idx.cpu().numpy()
+    for t in range(4):
+        assert np.all(nsel[0, :, t] == 16)
+        assert np.array_equal(idx[0, 0, t], np.arange(16))
+
+
+# ------------------------------------------------------------- stage 3 ----
+
+ATTN_CASES = [
+    # batch, hkv, cap, lens, n_q, topk, includes_forced, prefill
+    (2, 2, 5000, [5000, 3333], 1, 16, True, False),
+    (1, 2, 9000, [9000], 1, 64, True, False),
+    (2, 1, 4100, [4100, 2100], 5, 12, True, False),
+    (1, 2, 6000, [6000], 16, 24, True, False),
+    (2, 1, 3000, [3000, 1500], 16, 10, False, True),
+    (2, 1, 2000, [2000, 1234], 130, 8, False, True),
+    (1, 1, 700, [700], 700, 4, True, True),
+    (3, 1, 300, [300, 40, 20], 20, 4, True, True),
+]
+
+
+@pytest.mark.parametrize("case", ATTN_CASES, ids=[f"att{i}" for i in range(len(ATTN_CASES))])
+def test_sparse_attention_parity(dev, case):
+    import torch
+    B, H, cap, lens, nq, topk, inc, prefill = case
+    inp = S.make_random(batch=B, n_kv_heads=H, kv_len=cap, n_q=nq, topk=topk, includes_forced=inc,
+                        seed=200 + sum(lens) + nq, kv_lens=lens)
+    st = _settings(inp.wl)
+    sels = O.run_selection(inp, st)
+    run = GpuRun(inp, dev)
+    idx, nsel = run.upload_selection(sels)
+    run.attend(idx, nsel, prefill=prefill)
+    torch.cuda.synchronize()
+    refs = O.run_attention(inp, st, {u: s.blocks for u, s in sels.items()})
+    check_attention(run, refs)
+
+
+def test_attention_dense_degeneracy_matches_sdpa(dev):
+    # topk covering every block: the output is plain causal attention.
+    import torch
+    inp = S.make_random(batch=1, n_kv_heads=1, kv_len=900, n_q=900, topk=15, seed=7)
+    run = GpuRun(inp, dev)
+    run.compress()
+    run.select()
+    run.attend()
+    torch.cuda.synchronize()
+    q = torch.from_numpy(S.bf16_bits_to_f32(inp.q[0])).double().permute(1, 0, 2)[None]
+    k = torch.from_numpy(S.bf16_bits_to_f32(inp.k[0, 0])).double()[None, None].expand(1, 16, 900, 128)
+    v = torch.from_numpy(S.bf16_bits_to_f32(inp.v[0, 0])).double()[None, None].expand(1, 16, 900, 128)
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True)[0].permute(1, 0, 2)
+    err = (run.out[0].double().cpu() - ref).abs()
+    assert err.max().item() <= 2e-3 and err.mean().item() <= 2e-4
+
+
+def test_split_count_does_not_change_decode_result(dev):
+    # Same unit through the decode (split + merge) and prefill (single CTA)
+    # entry points: the merge identity makes them agree to rounding.
+    import torch
+    inp = S.make_random(batch=2, n_kv_heads=2, kv_len=8000, n_q=4, topk=48, seed=9)
+    st = _settings(inp.wl)
+    sels = O.run_selection(inp, st)
+    run = GpuRun(inp, dev)
+    idx, nsel = run.upload_selection(sels)
+    run.attend(idx, nsel, prefill=False)
+    a = run.out.float().clone()
+    run.attend(idx, nsel, prefill=True)
+    torch.cuda.synchronize()
+    assert (a - run.out.float()).abs().max().item() <= 2e-3
+
+
+def test_bad_kv_len_sets_device_status(dev):
+    import torch
+    import trainable_block_sparse_infllm_gb300 as T
+    inp = S.make_random(batch=2, n_kv_heads=1, kv_len=1000, n_q=2, topk=4, seed=3, kv_lens=[1000, 1])
+    run = GpuRun(inp, dev)
+    run.compress()
+    run.select()
+    run.attend()
+    torch.cuda.synchronize()
+    assert T.get_device_status(clear=True) & T.DEVICE_BAD_KV_LEN
+    assert run.nsel[1].eq(0).all().item()
+    assert run.out[1].float().eq(0).all().item()
+
+
+# --------------------------------------------------------- full workloads ----
+
+def _workload_units(wl, rng, n_sample):
+    if wl.n_q <= 16:
+        return [(b, h, t) for b in range(wl.batch) for h in range(wl.n_kv_heads) for t in range(wl.n_q)]
+    toks = set(range(0, 256)) | set(range(wl.n_q - 256, wl.n_q))
+    toks |= set(rng.choice(wl.n_q, size=n_sample, replace=False).tolist())
+    return [(b, h, t) for b in range(wl.batch) for h in range(wl.n_kv_heads) for t in sorted(toks)]
+
+
+@pytest.mark.parametrize("name", ["decode_4k", "decode_32k", "decode_128k", "verify_128k", "prefill_32k"])
+def test_workload_parity(dev, name):
+    import torch
+    wl = S.WORKLOADS[name]
+    inp = S.make_inputs(wl)
+    st = _settings(wl)
+    run = GpuRun(inp, dev)
+    run.compress()
+    run.select()
+    run.attend()
+    torch.cuda.synchronize()
+    units = _workload_units(wl, np.random.default_rng(0), 512)
+    kc_cache = {}
+    sels = O.run_selection(inp, st, units=units, kc_cache=kc_cache)
+    ties = check_selections(run, sels, check_scores=False)
+    if name in ("decode_4k", "decode_32k"):
+        # Free slots >= planted blocks: every planted block is selected.
+        idx = run.idx.cpu().numpy()
+        for (b, h, t) in units:
+            assert set(inp.planted[b, h].tolist()) <= set(idx[b, h, t].tolist())
+    # Attention on the oracle's selection.
+    idx, nsel = run.upload_selection(sels)
+    run.out.fill_(float("nan"))
+    run.attend(idx, nsel)
+    torch.cuda.synchronize()
+    refs = O.run_attention(inp, st, {u: s.blocks for u, s in sels.items()}, units=units)
+    mx, mean = check_attention(run, refs)
+    print(f"{name}: units={len(units)} tie-band differences={ties} max|dO|={mx:.2e} mean={mean:.2e}")

@@ -1,0 +1,142 @@
+"""InfLLM v2 block-sparse attention for GB300 (sm_103a): Python binding.
+
+The compute path is the CUDA library ``libinfllmv2.so`` behind the C ABI in
+``include/infllmv2.h``; this module only passes torch tensors' device
+pointers, sizes and the current stream to it.  PyTorch provides device
+memory and streams.  Entry points mirror the C names:
+
+    compress_keys        stage 1, semantic-kernel key means
+    select_blocks        stage 2, block relevance and top-k
+    sparse_attn_decode   stage 3 for decode / speculative verification
+    sparse_attn_prefill  stage 3 for prefill
+
+Method: "MiniCPM4: Ultra-Efficient LLMs on End Devices", section "InfLLM v2:
+Trainable Sparse Attention for Both Prefilling and Decoding".
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+
+import torch
+
+from . import _lib
+from ._lib import (InfLLMv2Error, OP_DECODE, OP_PREFILL, OP_SELECT, Params,  # noqa: F401
+                   DEVICE_BAD_KV_LEN, DEVICE_TIMEOUT)
+
+__all__ = [
+    "Params", "InfLLMv2Error", "make_params", "num_kernels", "max_selected", "workspace_size",
+    "alloc_kc", "alloc_workspace", "compress_keys", "select_blocks", "sparse_attn_decode",
+    "sparse_attn_prefill", "get_device_status", "OP_SELECT", "OP_DECODE", "OP_PREFILL",
+    "DECODE_MAX_NQ",
+]
+
+DECODE_MAX_NQ = 16
+
+
+def make_params(batch: int, n_kv_heads: int, max_kv_len: int, topk: int,
+                includes_forced: bool = True, n_init: int = 1, n_local: int = 2,
+                score_scale: float | None = None, attn_scale: float | None = None) -> Params:
+    p = Params()
+    _lib.lib.infllmv2_default_params(ctypes.byref(p), batch, n_kv_heads, max_kv_len, topk,
+                                     1 if includes_forced else 0)
+    p.n_init_blocks = n_init
+    p.n_local_blocks = n_local
+    if score_scale is not None:
+        p.score_scale = score_scale
+    if attn_scale is not None:
+        p.attn_scale = attn_scale
+    return p
+
+
+def num_kernels(p: Params) -> int:
+    return int(_lib.lib.infllmv2_num_kernels(ctypes.byref(p)))
+
+
+def max_selected(p: Params) -> int:
+    k = int(_lib.lib.infllmv2_max_selected(ctypes.byref(p)))
+    if k < 0:
+        raise InfLLMv2Error(_lib.INVALID_ARGUMENT, _lib.lib.infllmv2_last_error().decode())
+    return k
+
+
+def workspace_size(p: Params, n_q: int, op: int) -> int:
+    return int(_lib.lib.infllmv2_workspace_size(ctypes.byref(p), n_q, op))
+
+
+def _ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise InfLLMv2Error(_lib.INVALID_ARGUMENT, "tensors must live on a CUDA device")
+    if not t.is_contiguous():
+        raise InfLLMv2Error(_lib.INVALID_ARGUMENT, "tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def alloc_kc(p: Params, device=None) -> torch.Tensor:
+    """Compressed-key buffer bf16 [B, Hkv, 2, n_c(max_kv_len), 128] (hi and lo planes)."""
+    return torch.empty((p.batch, p.n_kv_heads, 2, max(num_kernels(p), 0), p.head_dim),
+                       dtype=torch.bfloat16, device=device)
+
+
+def alloc_workspace(p: Params, n_q: int, op: int, device=None) -> torch.Tensor | None:
+    n = workspace_size(p, n_q, op)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n > 0 else None
+
+
+def compress_keys(p: Params, k_cache: torch.Tensor, kv_lens: torch.Tensor, kc: torch.Tensor,
+                  kernel_begin: int = 0, kernel_end: int = -1, stream=None) -> torch.Tensor:
+    _lib.check(_lib.lib.infllmv2_compress_keys(ctypes.byref(p), _ptr(k_cache), _ptr(kv_lens),
+                                               kernel_begin, kernel_end, _ptr(kc), _stream(stream)))
+    return kc
+
+
+def select_blocks(p: Params, q: torch.Tensor, kc: torch.Tensor, kv_lens: torch.Tensor,
+                  block_idx: torch.Tensor, n_selected: torch.Tensor,
+                  block_scores: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                  stream=None):
+    n_q = q.shape[1]
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    _lib.check(_lib.lib.infllmv2_select_blocks(ctypes.byref(p), _ptr(q), n_q, _ptr(kc), _ptr(kv_lens),
+                                               _ptr(block_idx), _ptr(n_selected), _ptr(block_scores),
+                                               _ptr(workspace), ws_bytes, _stream(stream)))
+    return block_idx, n_selected
+
+
+def _attn(fn, p, q, k_cache, v_cache, kv_lens, block_idx, n_selected, out, lse, workspace, stream):
+    n_q = q.shape[1]
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    _lib.check(fn(ctypes.byref(p), _ptr(q), n_q, _ptr(k_cache), _ptr(v_cache), _ptr(kv_lens),
+                  _ptr(block_idx), _ptr(n_selected), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
+                  _stream(stream)))
+    return out, lse
+
+
+def sparse_attn_decode(p: Params, q, k_cache, v_cache, kv_lens, block_idx, n_selected, out,
+                       lse=None, workspace=None, stream=None):
+    return _attn(_lib.lib.infllmv2_sparse_attn_decode, p, q, k_cache, v_cache, kv_lens, block_idx,
+                 n_selected, out, lse, workspace, stream)
+
+
+def sparse_attn_prefill(p: Params, q, k_cache, v_cache, kv_lens, block_idx, n_selected, out,
+                        lse=None, workspace=None, stream=None):
+    return _attn(_lib.lib.infllmv2_sparse_attn_prefill, p, q, k_cache, v_cache, kv_lens, block_idx,
+                 n_selected, out, lse, workspace, stream)
+
+
+def get_device_status(clear: bool = True) -> int:
+    v = ctypes.c_uint32(0)
+    _lib.check(_lib.lib.infllmv2_get_device_status(ctypes.byref(v), 1 if clear else 0))
+    return int(v.value)
+
+
+def default_scale(head_dim: int = 128) -> float:
+    return 1.0 / math.sqrt(head_dim)

@@ -1,0 +1,110 @@
+// Stage 1 of InfLLM v2: semantic-kernel key compression.
+//
+// [InfLLM v2 > Semantic kernels for block relevance scoring, eq. S_j]: kernel
+// j covers keys [j s, j s + p) (p = 32, s = 16, adjacent kernels overlap by
+// half) and is represented by the mean of its keys, eq. r_kernel.
+//
+// With s = p / 2 every kernel is the union of two consecutive 16-key chunks,
+// so a CTA streams its chunk range once (one fp32 sum per chunk and dim) and
+// writes Mean_j = (C_j + C_{j+1}) / 32.  The fp32 mean is stored as two bf16
+// planes, hi = bf16(mean) and lo = bf16(mean - hi), so that the selection
+// stage can feed both straight to the tensor cores.  HBM-bound: one read of
+// the keys, one write of 512 bytes per kernel.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace infllmv2 {
+
+namespace {
+
+constexpr int kKernelsPerCta = 32;
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4& w) {
+  const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc[2 * i] += __uint_as_float(v[i] << 16);
+    acc[2 * i + 1] += __uint_as_float(v[i] & 0xffff0000u);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads)
+    compress_kernel(const __nv_bfloat16* __restrict__ k, const int32_t* __restrict__ kv_lens,
+                    int Hkv, int Lmax, int ncmax, int kbegin, int kend,
+                    __nv_bfloat16* __restrict__ kc, uint32_t* status) {
+  __shared__ __align__(16) float csum[kKernelsPerCta + 1][kHeadDim];
+  const int b = blockIdx.z, h = blockIdx.y;
+  const int L = kv_lens[b];
+  if (L < 0 || L > Lmax) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && h == 0) atomicOr(status, kStatusBadKvLen);
+    return;
+  }
+  const int nc = n_complete_kernels(L);
+  const int begin = kbegin >= 0 ? kbegin : max(0, nc + kbegin);
+  const int end = kend >= 0 ? min(kend, nc) : nc;
+  const int j0 = begin + blockIdx.x * kKernelsPerCta;
+  const int j1 = min(j0 + kKernelsPerCta, end);
+  if (j0 >= j1) return;
+
+  const size_t bh = static_cast<size_t>(b) * Hkv + h;
+  const __nv_bfloat16* kbh = k + bh * Lmax * kHeadDim;
+  const int nchunk = j1 - j0 + 1;  // chunks j0 .. j1 of 16 keys
+  const int sub = threadIdx.x & 15;
+  for (int cc = threadIdx.x >> 4; cc < nchunk; cc += kThreads / 16) {
+    const int tok0 = (j0 + cc) * kStride;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int t = 0; t < kStride; ++t) {
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(kbh + static_cast<size_t>(tok0 + t) * kHeadDim) + sub);
+      add_bf16x8(acc, w);
+    }
+    float4* dst = reinterpret_cast<float4*>(&csum[cc][sub * 8]);
+    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+  __syncthreads();
+
+  __nv_bfloat16* hi_plane = kc + (bh * 2 + 0) * ncmax * kHeadDim;
+  __nv_bfloat16* lo_plane = kc + (bh * 2 + 1) * ncmax * kHeadDim;
+  for (int idx = threadIdx.x; idx < (j1 - j0) * 32; idx += kThreads) {
+    const int jj = idx >> 5, q4 = idx & 31;
+    const float4 a = *reinterpret_cast<const float4*>(&csum[jj][q4 * 4]);
+    const float4 c = *reinterpret_cast<const float4*>(&csum[jj + 1][q4 * 4]);
+    const float m[4] = {(a.x + c.x) * (1.0f / kKernel), (a.y + c.y) * (1.0f / kKernel),
+                        (a.z + c.z) * (1.0f / kKernel), (a.w + c.w) * (1.0f / kKernel)};
+    uint32_t hw[2], lw[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const __nv_bfloat162 hv = __floats2bfloat162_rn(m[2 * e], m[2 * e + 1]);
+      const float h0 = __bfloat162float(hv.x), h1 = __bfloat162float(hv.y);
+      const __nv_bfloat162 lv = __floats2bfloat162_rn(m[2 * e] - h0, m[2 * e + 1] - h1);
+      hw[e] = *reinterpret_cast<const uint32_t*>(&hv);
+      lw[e] = *reinterpret_cast<const uint32_t*>(&lv);
+    }
+    const size_t off = static_cast<size_t>(j0 + jj) * kHeadDim + q4 * 4;
+    *reinterpret_cast<uint2*>(hi_plane + off) = make_uint2(hw[0], hw[1]);
+    *reinterpret_cast<uint2*>(lo_plane + off) = make_uint2(lw[0], lw[1]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_compress(const Shape& s, const void* k, const int32_t* kv_lens, int kbegin,
+                            int kend, void* kc, uint32_t* status, cudaStream_t st) {
+  int count;
+  if (kbegin < 0) {
+    count = min(-kbegin, s.ncmax);
+  } else {
+    const int e = kend >= 0 ? min(kend, s.ncmax) : s.ncmax;
+    count = e - kbegin;
+  }
+  if (count <= 0) return cudaSuccess;
+  dim3 grid((count + kKernelsPerCta - 1) / kKernelsPerCta, s.Hkv, s.B);
+  compress_kernel<<<grid, kThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(k), kv_lens, s.Hkv,
+                                             s.Lmax, s.ncmax, kbegin, kend,
+                                             static_cast<__nv_bfloat16*>(kc), status);
+  return cudaGetLastError();
+}
+
+}  // namespace infllmv2

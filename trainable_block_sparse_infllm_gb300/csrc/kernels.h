@@ -1,0 +1,43 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernel
+// translation units.  Host-side only; every pointer is a device pointer.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace infllmv2 {
+
+struct Shape {
+  int B, Hkv, Lmax, nq;
+  int ncmax;   // complete kernels of a full cache
+  int nbmax;   // ceil(Lmax / 64)
+  int kmax;    // width of a block_idx row
+  int topk, n_init, n_local, inc_forced;
+  float score_scale2;  // score_scale * log2(e)
+  float attn_scale2;   // attn_scale * log2(e)
+};
+
+// ---- stage 1 ---------------------------------------------------------------
+cudaError_t launch_compress(const Shape& s, const void* k, const int32_t* kv_lens, int kbegin,
+                            int kend, void* kc, uint32_t* status, cudaStream_t st);
+
+// ---- stage 2 ---------------------------------------------------------------
+constexpr int kSelChunk = 128;        // kernels per scoring CTA (decode path)
+constexpr int kSelReduceBlocks = 64;  // blocks per reduction CTA (decode path)
+constexpr int kSelDecodeMaxNq = 16;   // n_q at or below this uses the decode path
+
+size_t select_workspace_bytes(const Shape& s);
+cudaError_t launch_select(const Shape& s, const CUtensorMap& kc_map, const CUtensorMap& q_map,
+                          const void* q, const int32_t* kv_lens, int32_t* block_idx,
+                          int32_t* n_sel, float* block_scores, void* ws, uint32_t* status,
+                          cudaStream_t st);
+
+// ---- stage 3 ---------------------------------------------------------------
+size_t attn_workspace_bytes(const Shape& s, bool prefill);
+cudaError_t launch_attn(const Shape& s, bool prefill, const CUtensorMap& q_map,
+                        const CUtensorMap& k_map, const CUtensorMap& v_map,
+                        const int32_t* kv_lens, const int32_t* block_idx, const int32_t* n_sel,
+                        void* out, float* lse, void* ws, uint32_t* status, cudaStream_t st);
+
+}  // namespace infllmv2

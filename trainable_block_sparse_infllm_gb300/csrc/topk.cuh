@@ -1,0 +1,174 @@
+// Top-k block choice shared by the selection kernels.
+//
+// [InfLLM v2 > Top-K implementation and the LSE bottleneck, step (3)] and
+// [InfLLM v2 > Initial and local tokens always selected]: forced blocks (the
+// first n_init blocks and the n_local blocks ending at the query's block c)
+// are always taken; among the other blocks with a finite score the best are
+// taken in order (score descending, index ascending).  The result is written
+// ascending by block index and padded with -1.
+//
+// The threshold score is found exactly with a 4-pass radix select over the
+// order-preserving 32-bit image of the fp32 scores (8-bit digits, one
+// shared-memory histogram per pass); ties at the threshold go to the lowest
+// indices through a prefix count in index order.  The routine is written for
+// a cooperating group of NT threads: a whole CTA (NT = blockDim.x, WARP =
+// false) or a single warp (NT = 32, WARP = true).
+#pragma once
+
+#include "common.cuh"
+
+namespace infllmv2 {
+
+template <int NT>
+struct TopkScratch {
+  uint32_t hist[256];
+  int ctrl[4];
+  int warp_tot[NT / 32 > 0 ? NT / 32 : 1];
+};
+
+template <bool WARP>
+__device__ __forceinline__ void group_sync() {
+  if (WARP) {
+    __syncwarp();
+  } else {
+    __syncthreads();
+  }
+}
+
+// Exclusive prefix sum of `v` over the group; `total` receives the sum.
+template <int NT, bool WARP>
+__device__ __forceinline__ int group_exclusive_scan(int v, int& total, TopkScratch<NT>& sm,
+                                                    int tid) {
+  const int lane = tid & 31;
+  int incl = warp_inclusive_scan(v);
+  if (WARP) {
+    total = __shfl_sync(0xffffffffu, incl, 31);
+    return incl - v;
+  }
+  const int warp = tid >> 5;
+  constexpr int NWARP = NT / 32;
+  if (lane == 31) sm.warp_tot[warp] = incl;
+  __syncthreads();
+  int base = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < NWARP; ++w) {
+    const int x = sm.warp_tot[w];
+    base += (w < warp) ? x : 0;
+    tot += x;
+  }
+  __syncthreads();
+  total = tot;
+  return base + incl - v;
+}
+
+template <int NT, bool WARP>
+__device__ __forceinline__ int group_sum(int v, TopkScratch<NT>& sm, int tid) {
+  int total;
+  group_exclusive_scan<NT, WARP>(v, total, sm, tid);
+  return total;
+}
+
+// r[0..nb) : block scores of blocks 0..c (c = nb - 1), in shared memory.
+// flag[0..nb) : shared scratch (bytes).  Writes out_idx[0..k_max) and *out_n.
+template <int NT, bool WARP>
+__device__ void select_topk(const float* r, uint8_t* flag, int nb, int n_init, int n_local,
+                            int topk, bool includes_forced, int k_max, int32_t* out_idx,
+                            int32_t* out_n, TopkScratch<NT>& sm, int tid) {
+  const int c = nb - 1;
+  const int local_lo = c - n_local + 1;
+  int my_cand = 0, my_forced = 0;
+  for (int j = tid; j < nb; j += NT) {
+    const bool forced = (j < n_init) || (j >= local_lo);
+    const bool cand = !forced && (r[j] > -INFINITY);
+    flag[j] = forced ? 2 : (cand ? 1 : 0);
+    my_cand += cand ? 1 : 0;
+    my_forced += forced ? 1 : 0;
+  }
+  group_sync<WARP>();
+  const int n_cand = group_sum<NT, WARP>(my_cand, sm, tid);
+  const int n_forced = group_sum<NT, WARP>(my_forced, sm, tid);
+  int n_take = includes_forced ? topk - n_forced : topk;
+  if (n_take < 0) n_take = 0;
+
+  const int per = (nb + NT - 1) / NT;
+  const int lo = tid * per;
+  const int hi = min(nb, lo + per);
+
+  if (n_take > 0 && n_cand <= n_take) {
+    for (int j = tid; j < nb; j += NT)
+      if (flag[j] == 1) flag[j] = 3;
+  } else if (n_take > 0) {
+    uint32_t prefix = 0, pmask = 0;
+    int remaining = n_take;
+#pragma unroll 1
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      for (int b = tid; b < 256; b += NT) sm.hist[b] = 0;
+      group_sync<WARP>();
+      for (int j = tid; j < nb; j += NT) {
+        if (flag[j] == 1) {
+          const uint32_t key = float_to_ordered(r[j]);
+          if ((key & pmask) == prefix) atomicAdd(&sm.hist[(key >> shift) & 255u], 1u);
+        }
+      }
+      group_sync<WARP>();
+      if (tid < 32) {
+        // Lane l owns digits 255-8l .. 255-8l-7 (descending).
+        int cnt[8];
+        int tot = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          cnt[k] = static_cast<int>(sm.hist[255 - 8 * tid - k]);
+          tot += cnt[k];
+        }
+        int run = warp_inclusive_scan(tot) - tot;  // elements with a larger digit
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (run < remaining && run + cnt[k] >= remaining) {
+            sm.ctrl[0] = 255 - 8 * tid - k;
+            sm.ctrl[1] = remaining - run;
+          }
+          run += cnt[k];
+        }
+      }
+      group_sync<WARP>();
+      prefix |= static_cast<uint32_t>(sm.ctrl[0]) << shift;
+      pmask |= 255u << shift;
+      remaining = sm.ctrl[1];
+      group_sync<WARP>();
+    }
+    // prefix = exact key of the last element taken; `remaining` of the
+    // elements equal to it are taken, lowest indices first.
+    int my_eq = 0;
+    for (int j = lo; j < hi; ++j)
+      if (flag[j] == 1 && float_to_ordered(r[j]) == prefix) ++my_eq;
+    int tot_eq;
+    int rank = group_exclusive_scan<NT, WARP>(my_eq, tot_eq, sm, tid);
+    for (int j = lo; j < hi; ++j) {
+      if (flag[j] != 1) continue;
+      const uint32_t key = float_to_ordered(r[j]);
+      if (key > prefix) {
+        flag[j] = 3;
+      } else if (key == prefix) {
+        if (rank < remaining) flag[j] = 3;
+        ++rank;
+      }
+    }
+  }
+  group_sync<WARP>();
+
+  int my_sel = 0;
+  for (int j = lo; j < hi; ++j) my_sel += (flag[j] >= 2) ? 1 : 0;
+  int total;
+  int pos = group_exclusive_scan<NT, WARP>(my_sel, total, sm, tid);
+  for (int j = lo; j < hi; ++j) {
+    if (flag[j] >= 2) {
+      if (pos < k_max) out_idx[pos] = j;
+      ++pos;
+    }
+  }
+  for (int p = total + tid; p < k_max; p += NT) out_idx[p] = -1;
+  if (tid == 0) *out_n = min(total, k_max);
+}
+
+}  // namespace infllmv2
