@@ -1,0 +1,520 @@
+"""Benchmark of the InfLLM v2 hot path on GB300.
+
+Headline: decode tokens/s at 128K context (batch 4, 32 query / 2 KV heads,
+top-64 blocks).  One step = the whole decode path for one new token per
+sequence: compress_keys for the newest complete kernel, select_blocks
+(scores, LSE, group mean, block max, top-k) and sparse_attn_decode
+(split-KV attention + merge), captured in a CUDA graph.  A prefill line
+(32K causal prefill, 32 query / 2 KV heads) is reported alongside.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+N > 1 runs under torch.distributed (one process per GPU); every rank decodes
+its own batch (weak scaling) and the time is the max over ranks.
+`--impl reference` times the fp64 CPU oracle on the same workload.
+"""
+
+from __future__ import annotations
+
+import os
+
+# The CPU legs (input generation, the oracle) run single-threaded so that the
+# reported core count is exact.
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import hashlib
+import json
+import math
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthetic_inputs as S  # noqa: E402
+
+DECODE = "decode_128k"
+PREFILL = "prefill_32k"
+METRIC = "decode tokens/s and prefill tokens/s at 128K ctx; % of HBM / bf16 TC roofline"
+REPLICAS = 8          # rotating input copies: 8 x 0.57 GB >> L2 (129 MB)
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _src_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "trainable_block_sparse_infllm_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, fn), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if the source is unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        d = json.load(open(path))
+        e = d[f"{kernel}@{workload}"]
+        if e.get("src_hash") == _src_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ----------------------------------------------------------------- decode ---
+
+class DecodeBench:
+    def __init__(self, dev, seed_offset=0):
+        import torch
+        import trainable_block_sparse_infllm_gb300 as T
+        self.T, self.torch, self.dev = T, torch, dev
+        wl = S.WORKLOADS[DECODE]
+        if seed_offset:
+            wl = wl.scaled(seed=wl.seed + 1000 * seed_offset)
+        self.wl = wl
+        inp = S.make_inputs(wl)
+        self.inp = inp
+        self.p = T.make_params(wl.batch, wl.n_kv_heads, wl.kv_len, wl.topk, wl.topk_includes_forced)
+        B, H, L, nq = wl.batch, wl.n_kv_heads, wl.kv_len, wl.n_q
+
+        def up(bits):
+            return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+
+        q0, k0, v0 = up(inp.q), up(inp.k), up(inp.v)
+        self.lens = torch.from_numpy(inp.kv_lens).to(dev)
+        self.kmax = T.max_selected(self.p)
+        self.reps = []
+        for r in range(REPLICAS):
+            rep = {"q": q0.clone(), "k": k0.clone(), "v": v0.clone(), "kc": T.alloc_kc(self.p, dev),
+                   "idx": torch.empty((B, H, nq, self.kmax), dtype=torch.int32, device=dev),
+                   "nsel": torch.empty((B, H, nq), dtype=torch.int32, device=dev),
+                   "out": torch.empty_like(q0),
+                   "lse": torch.empty((B, nq, wl.n_heads), dtype=torch.float32, device=dev),
+                   "ws_sel": T.alloc_workspace(self.p, nq, T.OP_SELECT, dev),
+                   "ws_att": T.alloc_workspace(self.p, nq, T.OP_DECODE, dev)}
+            T.compress_keys(self.p, rep["k"], self.lens, rep["kc"])      # full cache, once
+            self.reps.append(rep)
+        del q0, k0, v0
+        torch.cuda.synchronize()
+
+    # the three stages of one decode step on replica r
+    def compress_newest(self, r):
+        rep = self.reps[r]
+        self.T.compress_keys(self.p, rep["k"], self.lens, rep["kc"], -1, -1)
+
+    def select(self, r):
+        rep = self.reps[r]
+        self.T.select_blocks(self.p, rep["q"], rep["kc"], self.lens, rep["idx"], rep["nsel"], None,
+                             rep["ws_sel"])
+
+    def attend(self, r):
+        rep = self.reps[r]
+        self.T.sparse_attn_decode(self.p, rep["q"], rep["k"], rep["v"], self.lens, rep["idx"], rep["nsel"],
+                                  rep["out"], rep["lse"], rep["ws_att"])
+
+    def step(self, r):
+        self.compress_newest(r)
+        self.select(r)
+        self.attend(r)
+
+    def capture(self):
+        torch = self.torch
+        for r in range(REPLICAS):
+            self.step(r)                        # warm: module load, attributes, symbols
+        torch.cuda.synchronize()
+        self.graphs = []
+        for r in range(REPLICAS):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self.step(r)
+            self.graphs.append(g)
+        torch.cuda.synchronize()
+
+    def time_fn(self, fn, n, warm=3):
+        torch = self.torch
+        for i in range(warm):
+            fn(i % REPLICAS)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(n):
+            fn(i % REPLICAS)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n * 1e-3     # seconds per call
+
+    def algorithmic_bytes(self):
+        """Bytes a decode step must move (SURVEY-style accounting, per launch)."""
+        wl = self.wl
+        B, H, nq, d = wl.batch, wl.n_kv_heads, wl.n_q, wl.head_dim
+        n_c = S_n_c(wl.kv_len)
+        nsel = self.reps[0]["nsel"].cpu().numpy()
+        q_b = B * nq * wl.n_heads * d * 2
+        kc_b = B * H * n_c * d * 4                      # hi + lo planes
+        kv_b = int(nsel.sum()) * wl.block * d * 2 * 2   # selected K and V tiles
+        out_b = q_b
+        idx_b = B * H * nq * (self.kmax + 1) * 4
+        comp_b = B * H * (wl.kernel * d * 2 + d * 4)    # newest kernel: 32 keys in, 512 B out
+        return {"compress": comp_b, "select": kc_b + q_b + idx_b,
+                "attend": kv_b + q_b + out_b + idx_b + B * nq * wl.n_heads * 4,
+                "step": comp_b + kc_b + q_b * 2 + kv_b + idx_b}
+
+
+def S_n_c(L, p=32, s=16):
+    return (L - p) // s + 1 if L >= p else 0
+
+
+# ---------------------------------------------------------------- prefill ---
+
+def prefill_line(dev, steps, warmup, peaks):
+    import torch
+    import trainable_block_sparse_infllm_gb300 as T
+    wl = S.WORKLOADS[PREFILL]
+    inp = S.make_inputs(wl)
+    p = T.make_params(wl.batch, wl.n_kv_heads, wl.kv_len, wl.topk, wl.topk_includes_forced)
+
+    def up(bits):
+        return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    q, k, v = up(inp.q), up(inp.k), up(inp.v)
+    lens = torch.from_numpy(inp.kv_lens).to(dev)
+    kmax = T.max_selected(p)
+    B, H, nq = wl.batch, wl.n_kv_heads, wl.n_q
+    kc = T.alloc_kc(p, dev)
+    idx = torch.empty((B, H, nq, kmax), dtype=torch.int32, device=dev)
+    nsel = torch.empty((B, H, nq), dtype=torch.int32, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, nq, wl.n_heads), dtype=torch.float32, device=dev)
+    ws_sel = T.alloc_workspace(p, nq, T.OP_SELECT, dev)
+    ws_att = T.alloc_workspace(p, nq, T.OP_PREFILL, dev)
+
+    stages = {
+        "compress": lambda: T.compress_keys(p, k, lens, kc),
+        "select": lambda: T.select_blocks(p, q, kc, lens, idx, nsel, None, ws_sel),
+        "attend": lambda: T.sparse_attn_prefill(p, q, k, v, lens, idx, nsel, out, lse, ws_att),
+    }
+
+    def timed(fn, n):
+        for _ in range(max(warmup, 1)):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n * 1e-3
+
+    def full():
+        for f in stages.values():
+            f()
+
+    t_step = timed(full, steps)
+    t_stage = {name: timed(f, steps) for name, f in stages.items()}
+    # Algorithmic attention FLOPs from the selection actually made:
+    # 4 d per (query head, attended key) pair.
+    idx_h, nsel_h = idx.cpu().numpy(), nsel.cpu().numpy()
+    pairs = 0
+    m = wl.block
+    for b in range(B):
+        L = int(inp.kv_lens[b])
+        pos = L - nq + np.arange(nq)
+        for h in range(H):
+            rows = idx_h[b, h]
+            valid = rows >= 0
+            keys = np.where(valid, np.minimum(m, pos[:, None] - rows * m + 1), 0)
+            pairs += int(keys.clip(min=0).sum())
+    flops = 4.0 * wl.head_dim * pairs * wl.group
+    achieved = flops / t_stage["attend"] / 1e12
+    return {
+        "workload": f"{PREFILL}: batch 1, 32 q / 2 kv heads, causal 32768 x 32768, top-64 + init + local",
+        "tokens_per_s": B * nq / t_step,
+        "ms_per_step": t_step * 1e3,
+        "stage_ms": {k_: v_ * 1e3 for k_, v_ in t_stage.items()},
+        "roofline": {"kernel": "attn_kernel (sparse_attn_prefill)", "bound": "tensor",
+                     "achieved": achieved, "peak": peaks[1], "unit": "TFLOP/s",
+                     "frac": achieved / peaks[1], "peak_kind": peaks[3] + " burst bf16",
+                     "algorithmic_flop_per_launch": flops, "traffic": _traffic("attn_kernel", PREFILL)},
+    }
+
+
+# ----------------------------------------------------------- CPU baseline ---
+
+def cpu_baseline(budget_s=15.0):
+    """The fp64 oracle, as it stands, on a bounded sample of the decode workload."""
+    import oracle as O
+    wl = S.WORKLOADS[DECODE]
+    inp = S.make_inputs(wl)
+    st = O.Settings(topk=wl.topk, includes_forced=wl.topk_includes_forced)
+    t0 = time.perf_counter()
+    seqs = 0
+    for b in range(wl.batch):
+        units = [(b, h, t) for h in range(wl.n_kv_heads) for t in range(wl.n_q)]
+        sels = O.run_selection(inp, st, units=units)
+        O.run_attention(inp, st, {u: s.blocks for u, s in sels.items()}, units=units)
+        seqs += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": seqs * wl.n_q / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{seqs} of {wl.batch} sequences of {DECODE} (both KV heads: kernel means, "
+                      f"selection, attention), single-threaded numpy fp64"}
+
+
+def reference_arm(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle as O
+    wl = S.WORKLOADS[DECODE]
+    inp = S.make_inputs(wl)
+    st = O.Settings(topk=wl.topk, includes_forced=wl.topk_includes_forced)
+
+    def one_step(i):
+        b = i % wl.batch
+        units = [(b, h, t) for h in range(wl.n_kv_heads) for t in range(wl.n_q)]
+        sels = O.run_selection(inp, st, units=units)
+        O.run_attention(inp, st, {u: s.blocks for u, s in sels.items()}, units=units)
+
+    for i in range(args.warmup):
+        one_step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        one_step(i)
+    dt = time.perf_counter() - t0
+    value = args.steps * wl.n_q / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": f"{DECODE} (one sequence per step)"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": "one sequence (both KV heads) of decode_128k per step, "
+                                       "single-threaded numpy fp64"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------------- main ---
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    import torch
+    import __graft_entry__
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        if rank != 0:
+            __graft_entry__.build()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    import trainable_block_sparse_infllm_gb300 as T
+    peaks = _peaks()
+
+    bench = DecodeBench(dev, seed_offset=rank)
+    bench.capture()
+    wl = bench.wl
+    tokens_per_step = wl.batch * wl.n_q
+
+    # Per-stage durations (each stage alone, rotating replicas).
+    stage_t = {"compress": bench.time_fn(bench.compress_newest, args.steps),
+               "select": bench.time_fn(bench.select, args.steps),
+               "attend": bench.time_fn(bench.attend, args.steps)}
+
+    # Timed region: K graph replays of the whole step.
+    for i in range(args.warmup):
+        bench.graphs[i % REPLICAS].replay()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = Clocks(local)
+    clocks.start()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0 = time.perf_counter()
+    e0.record()
+    for i in range(args.steps):
+        bench.graphs[i % REPLICAS].replay()
+    e1.record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - w0
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    t = e0.elapsed_time(e1) * 1e-3
+    if dist:
+        tt = torch.tensor([t], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t = float(tt.item())
+    assert T.get_device_status(clear=True) == 0, "device status flagged during the bench"
+
+    # End to end through the public API with host buffers: per step the new
+    # token's q, k, v come from pinned host memory (k, v appended to the
+    # cache) and the attention output goes back to pinned host memory.
+    B, H, nq, d = wl.batch, wl.n_kv_heads, wl.n_q, wl.head_dim
+    q_h = torch.empty((REPLICAS,) + tuple(bench.reps[0]["q"].shape), dtype=torch.bfloat16).pin_memory()
+    kv_h = torch.empty((REPLICAS, 2, B, H, d), dtype=torch.bfloat16).pin_memory()
+    out_h = torch.empty((REPLICAS,) + tuple(bench.reps[0]["out"].shape), dtype=torch.bfloat16).pin_memory()
+    for r in range(REPLICAS):
+        q_h[r].copy_(bench.reps[r]["q"])
+        kv_h[r, 0].copy_(bench.reps[r]["k"][:, :, wl.kv_len - 1])
+        kv_h[r, 1].copy_(bench.reps[r]["v"][:, :, wl.kv_len - 1])
+    torch.cuda.synchronize()
+
+    def e2e_step(i):
+        r = i % REPLICAS
+        rep = bench.reps[r]
+        rep["q"].copy_(q_h[r], non_blocking=True)
+        rep["k"][:, :, wl.kv_len - 1].copy_(kv_h[r, 0], non_blocking=True)
+        rep["v"][:, :, wl.kv_len - 1].copy_(kv_h[r, 1], non_blocking=True)
+        bench.graphs[r].replay()
+        out_h[r].copy_(rep["out"], non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record()
+    for i in range(args.steps):
+        e2e_step(i)
+    f1.record()
+    torch.cuda.synchronize()
+    t_e2e = f0.elapsed_time(f1) * 1e-3
+    if dist:
+        tt = torch.tensor([t_e2e], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_e2e = float(tt.item())
+
+    prefill = None
+    if not args.no_prefill and rank == 0:
+        prefill = prefill_line(dev, max(3, min(10, args.steps // 20)), 3, peaks)
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    ab = bench.algorithmic_bytes()
+    dom = max(stage_t, key=stage_t.get)
+    dom_kernel = {"compress": "compress_kernel", "select": "sel_score_kernel + sel_reduce_kernel",
+                  "attend": "attn_kernel"}[dom]
+    achieved = ab[dom] / stage_t[dom] / 1e9
+    value = world * tokens_per_step * args.steps / t
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": t / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{DECODE}: batch 4, 32 q / 2 kv heads, head_dim 128, 131072-token bf16 "
+                               f"KV cache, block 64, kernel 32/16, top-64 incl. block 0 + 2 local, 1 query/seq",
+                   "global_batch": world * wl.batch, "seq_len": wl.kv_len, "parallelism": f"dp{world}",
+                   "l2": f"{REPLICAS} rotating input replicas ({REPLICAS * 0.57:.1f} GB) > L2",
+                   "graph": "one CUDA graph per step: compress(newest) + select + attention"},
+        "clocks": clk,
+        "gpu_launches": 4 * args.steps,
+        "stage_ms": {k_: v_ * 1e3 for k_, v_ in stage_t.items()},
+        "roofline": {"kernel": dom_kernel, "bound": "hbm", "achieved": achieved, "peak": peaks[0],
+                     "unit": "GB/s", "frac": achieved / peaks[0], "peak_kind": peaks[3],
+                     "algorithmic_bytes_per_launch": ab[dom], "traffic": _traffic(dom_kernel, DECODE)},
+        "step_roofline": {"achieved": ab["step"] / (t / args.steps) / 1e9, "unit": "GB/s",
+                          "frac": ab["step"] / (t / args.steps) / 1e9 / peaks[0],
+                          "algorithmic_bytes_per_step": ab["step"]},
+        "e2e": {"value": world * tokens_per_step * args.steps / t_e2e, "unit": "tokens/s",
+                "h2d_bytes_per_step": int(q_h[0].numel() * 2 + kv_h[0].numel() * 2),
+                "d2h_bytes_per_step": int(out_h[0].numel() * 2), "wall_s": wall},
+        "prefill": prefill,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
