@@ -145,30 +145,38 @@ def check_attention(run, refs, strict=False):
     """refs: {(b,h,t): (O [16, d], lse [16])}.  Returns (max, mean) abs error.
 
     strict: the workload acceptance rule (max 2e-3, mean 2e-4 absolute).
-    Otherwise (short contexts, where |O| reaches several units because a
-    query averages only a few values) the bound derived from the arithmetic:
-    the output is bf16 (half an ulp is 2^-9 |O|) and the probabilities enter
-    the P.V product as bf16 (2^-9 relative each), so per element
-    |err| <= 2e-3 + 2^-8 |O_ref|, and the mean of |err| / max(1, |O_ref|)
-    stays <= 2e-4.
+    Otherwise (short contexts, where a query averages only a few values and
+    |O| approaches |V|) the bound derived from the two bf16 roundings the
+    path may make: the output store (half an ulp, <= 2^-9 |O|) and, in the
+    prefill tensor-core kernel, the probabilities entering P.V (2^-9
+    relative each, so <= 2^-9 max|V| on the output).  Per element
+    |err| <= 2e-3 + 2^-8 (|O_ref| + vmax), and the mean |err| stays within
+    2e-4 + 2^-9 mean|O_ref| + 2^-11 vmax, vmax = max |V| of the sequence.
     """
+    from synthetic_inputs import bf16_bits_to_f32
     out = run.out.float().cpu().numpy()
     lse = run.lse.cpu().numpy()
-    errs, total, total_n, count, lse_err = [], 0.0, 0.0, 0, 0.0
+    vmax_bh = {}
+    errs, total, total_ref, count, lse_err, vmax_all = [], 0.0, 0.0, 0, 0.0, 0.0
     for (b, h, t), (o_ref, l_ref) in refs.items():
+        if (b, h) not in vmax_bh:
+            L = int(run.inp.kv_lens[b])
+            vmax_bh[(b, h)] = float(np.abs(bf16_bits_to_f32(run.inp.v[b, h, :L])).max())
+        vmax = vmax_bh[(b, h)]
+        vmax_all = max(vmax_all, vmax)
         o = out[b, t, h * 16:(h + 1) * 16]
         e = np.abs(o - o_ref)
         if not strict:
-            assert np.all(e <= ATT_MAX + 2.0 ** -8 * np.abs(o_ref)), ((b, h, t), float(e.max()))
+            assert np.all(e <= ATT_MAX + 2.0 ** -8 * (np.abs(o_ref) + vmax)), ((b, h, t), float(e.max()))
         errs.append(e.max())
         total += e.sum()
-        total_n += (e / np.maximum(1.0, np.abs(o_ref))).sum()
+        total_ref += np.abs(o_ref).sum()
         count += e.size
         lse_err = max(lse_err, float(np.abs(lse[b, t, h * 16:(h + 1) * 16] - l_ref).max()))
     mx, mean = float(max(errs)), total / count
     if strict:
         assert mx <= ATT_MAX and mean <= ATT_MEAN, (mx, mean)
     else:
-        assert total_n / count <= ATT_MEAN, total_n / count
+        assert mean <= ATT_MEAN + 2.0 ** -9 * total_ref / count + 2.0 ** -11 * vmax_all, mean
     assert lse_err <= LSE_ABS, lse_err
     return mx, mean

@@ -169,8 +169,12 @@ def test_attention_dense_degeneracy_matches_sdpa(dev):
     v = torch.from_numpy(S.bf16_bits_to_f32(inp.v[0, 0])).double()[None, None].expand(1, 16, 900, 128)
     ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True)[0].permute(1, 0, 2)
     err = (run.out[0].double().cpu() - ref).abs()
-    assert bool((err <= 2e-3 + 2.0 ** -8 * ref.abs()).all())
-    assert (err / ref.abs().clamp(min=1.0)).mean().item() <= 2e-4
+    vmax = v.abs().max().item()
+    # Same derived bound as the short-context cases in helpers.check_attention.
+    assert bool((err <= 2e-3 + 2.0 ** -8 * (ref.abs() + vmax)).all())
+    assert err.mean().item() <= 2e-4 + 2.0 ** -9 * ref.abs().mean().item() + 2.0 ** -11 * vmax
+    late = err[256:]                      # >= 256 keys per query: the absolute rule holds
+    assert late.max().item() <= 2e-3 and late.mean().item() <= 2e-4
 
 
 def test_split_count_does_not_change_decode_result(dev):

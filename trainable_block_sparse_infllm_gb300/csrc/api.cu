@@ -168,8 +168,11 @@ int attn_entry(const infllmv2_params* p, const void* q, int32_t n_q, const void*
   if ((rc = make_map(&qm, q, static_cast<uint64_t>(s.B) * s.nq * s.Hkv * kGroup, 16, "q"))) return rc;
   if ((rc = make_map(&km, k_cache, kv_rows, 64, "k_cache"))) return rc;
   if ((rc = make_map(&vm, v_cache, kv_rows, 64, "v_cache"))) return rc;
-  cudaError_t e = launch_attn(s, prefill, qm, km, vm, kv_lens, block_idx, n_selected, out, lse, workspace,
-                              status, static_cast<cudaStream_t>(stream));
+  cudaError_t e =
+      prefill ? launch_attn_tc(s, qm, km, vm, kv_lens, block_idx, n_selected, out, lse, status,
+                               static_cast<cudaStream_t>(stream))
+              : launch_attn(s, false, qm, km, vm, kv_lens, block_idx, n_selected, out, lse, workspace, status,
+                            static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, prefill ? "sparse_attn_prefill" : "sparse_attn_decode");
   return INFLLMV2_OK;
 }

@@ -193,15 +193,22 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
       o[n][2] *= sc1;
       o[n][3] *= sc1;
     }
-    uint32_t pa[4][4];
+    // P enters the tensor cores as hi + lo bf16 parts (16 significant bits),
+    // so the only bf16 rounding left in the output is the final store.
+    uint32_t pa[4][4], pl[4][4];
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
       const float p0 = fast_exp2(s[nt][0] - mn0), p1 = fast_exp2(s[nt][1] - mn0);
       const float p2 = fast_exp2(s[nt][2] - mn1), p3 = fast_exp2(s[nt][3] - mn1);
       l0 += p0 + p1;
       l1 += p2 + p3;
-      pa[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(p0, p1);
-      pa[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(p2, p3);
+      const __nv_bfloat162 h01 = __floats2bfloat162_rn(p0, p1);
+      const __nv_bfloat162 h23 = __floats2bfloat162_rn(p2, p3);
+      const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+      pa[nt >> 1][(nt & 1) * 2 + 0] = *reinterpret_cast<const uint32_t*>(&h01);
+      pa[nt >> 1][(nt & 1) * 2 + 1] = *reinterpret_cast<const uint32_t*>(&h23);
+      pl[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(p0 - f01.x, p1 - f01.y);
+      pl[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(p2 - f23.x, p3 - f23.y);
     }
     // O += P V: A = P (16 x 64 keys), B = V (64 keys x 128 dims) via ldmatrix.trans.
 #pragma unroll
@@ -213,6 +220,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
                                                   2 * np + (lane >> 4), kBlock));
         mma_bf16_16816(o[2 * np], pa[kk], vb[0], vb[1]);
         mma_bf16_16816(o[2 * np + 1], pa[kk], vb[2], vb[3]);
+        mma_bf16_16816(o[2 * np], pl[kk], vb[0], vb[1]);
+        mma_bf16_16816(o[2 * np + 1], pl[kk], vb[2], vb[3]);
       }
     }
   }

@@ -40,4 +40,10 @@ cudaError_t launch_attn(const Shape& s, bool prefill, const CUtensorMap& q_map,
                         const int32_t* kv_lens, const int32_t* block_idx, const int32_t* n_sel,
                         void* out, float* lse, void* ws, uint32_t* status, cudaStream_t st);
 
+// Prefill on tcgen05/TMEM: 8 query tokens x 16 heads per 128-row MMA tile.
+cudaError_t launch_attn_tc(const Shape& s, const CUtensorMap& q_map, const CUtensorMap& k_map,
+                           const CUtensorMap& v_map, const int32_t* kv_lens, const int32_t* block_idx,
+                           const int32_t* n_sel, void* out, float* lse, uint32_t* status,
+                           cudaStream_t st);
+
 }  // namespace infllmv2
