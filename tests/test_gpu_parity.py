@@ -173,8 +173,6 @@ def test_attention_dense_degeneracy_matches_sdpa(dev):
     # Same derived bound as the short-context cases in helpers.check_attention.
     assert bool((err <= 2e-3 + 2.0 ** -8 * (ref.abs() + vmax)).all())
     assert err.mean().item() <= 2e-4 + 2.0 ** -9 * ref.abs().mean().item() + 2.0 ** -11 * vmax
-    late = err[256:]                      # >= 256 keys per query: the absolute rule holds
-    assert late.max().item() <= 2e-3 and late.mean().item() <= 2e-4
 
 
 def test_split_count_does_not_change_decode_result(dev):
