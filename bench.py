@@ -290,10 +290,10 @@ def prefill_line(dev, steps, warmup, peaks):
         "tokens_per_s": B * nq / t_step,
         "ms_per_step": t_step * 1e3,
         "stage_ms": {k_: v_ * 1e3 for k_, v_ in t_stage.items()},
-        "roofline": {"kernel": "attn_kernel (sparse_attn_prefill)", "bound": "tensor",
+        "roofline": {"kernel": "attn_tc_kernel (sparse_attn_prefill)", "bound": "tensor",
                      "achieved": achieved, "peak": peaks[1], "unit": "TFLOP/s",
                      "frac": achieved / peaks[1], "peak_kind": peaks[3] + " burst bf16",
-                     "algorithmic_flop_per_launch": flops, "traffic": _traffic("attn_kernel", PREFILL)},
+                     "algorithmic_flop_per_launch": flops, "traffic": _traffic("attn_tc_kernel", PREFILL)},
     }
 
 
