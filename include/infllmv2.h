@@ -144,11 +144,13 @@ int infllmv2_select_blocks(const infllmv2_params* p, const void* q, int32_t n_q,
 
 /*
  * Stage 3, few queries per sequence (decode n_q = 1, speculative verification
- * n_q <= 16): the selected blocks of each (b, h_kv, t) are split over CTAs,
- * each computes an online-softmax partial, and the last CTA of the unit
- * merges them.  out/lse as documented above (lse nullable).  Only the first
- * n_selected[b, h, t] entries of block_idx are read; each must lie in
- * [0, floor(i/m)] (entries outside are skipped).
+ * n_q <= 16): the selected blocks of each (b, h_kv, t) are dealt to the CTAs
+ * of a thread-block cluster; each CTA computes an online-softmax partial and
+ * the partials are merged through distributed shared memory.  out/lse as
+ * documented above (lse nullable).  Only the first n_selected[b, h, t]
+ * entries of block_idx are read; each must lie in [0, floor(i/m)] (entries
+ * outside are skipped).  Needs no workspace (infllmv2_workspace_size
+ * returns 0; workspace may be NULL).
  */
 int infllmv2_sparse_attn_decode(const infllmv2_params* p, const void* q, int32_t n_q,
                                 const void* k_cache, const void* v_cache, const int32_t* kv_lens,

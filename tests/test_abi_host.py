@@ -73,7 +73,7 @@ def test_default_params_and_sizes(L):
     ws8 = L.lib.infllmv2_workspace_size(ctypes.byref(p), 8, L.OP_SELECT)
     assert 0 < ws1 < ws8
     assert L.lib.infllmv2_workspace_size(ctypes.byref(p), 100, L.OP_SELECT) == 0
-    assert L.lib.infllmv2_workspace_size(ctypes.byref(p), 1, L.OP_DECODE) > 0
+    assert L.lib.infllmv2_workspace_size(ctypes.byref(p), 1, L.OP_DECODE) == 0   # merged on chip
     assert L.lib.infllmv2_workspace_size(ctypes.byref(p), 100, L.OP_PREFILL) == 0
     assert L.lib.infllmv2_workspace_size(ctypes.byref(p), 100, L.OP_DECODE) == 0
     assert L.lib.infllmv2_workspace_size(ctypes.byref(p), 1, 99) == 0
@@ -105,11 +105,11 @@ def test_argument_errors_return_codes(L):
     assert _attn(L, p, nq=17) == L.INVALID_ARGUMENT                      # decode takes n_q <= 16
     assert _attn(L, p, q=FAKE_ODD) == L.UNSUPPORTED
     assert _attn(L, p, out=None) == L.INVALID_ARGUMENT
-    assert _attn(L, p) == L.WORKSPACE_TOO_SMALL
-    assert b"workspace" in L.lib.infllmv2_last_error()
-    need = L.lib.infllmv2_workspace_size(ctypes.byref(p), 1, L.OP_DECODE)
-    assert _attn(L, p, ws=FAKE, ws_bytes=need - 1) == L.WORKSPACE_TOO_SMALL
     rc = L.lib.infllmv2_select_blocks(ctypes.byref(p), FAKE, 1, FAKE, FAKE, FAKE, FAKE, None, None, 0, None)
+    assert rc == L.WORKSPACE_TOO_SMALL
+    assert b"workspace" in L.lib.infllmv2_last_error()
+    need = L.lib.infllmv2_workspace_size(ctypes.byref(p), 1, L.OP_SELECT)
+    rc = L.lib.infllmv2_select_blocks(ctypes.byref(p), FAKE, 1, FAKE, FAKE, FAKE, FAKE, None, FAKE, need - 1, None)
     assert rc == L.WORKSPACE_TOO_SMALL
     rc = L.lib.infllmv2_select_blocks(ctypes.byref(p), FAKE, 1, None, FAKE, FAKE, FAKE, None, None, 0, None)
     assert rc == L.INVALID_ARGUMENT

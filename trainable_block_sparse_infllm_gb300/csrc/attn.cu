@@ -1,4 +1,5 @@
-// Stage 3 of InfLLM v2: exact softmax attention over the selected KV blocks.
+// Stage 3 of InfLLM v2 for decode and speculative verification: exact
+// softmax attention over the selected KV blocks of each query token.
 //
 // [InfLLM v2 > Block-level key-value partitioning, eq. B_j]: the cache is
 // split into 64-key blocks that are fetched whole; [> Query group sharing]:
@@ -7,13 +8,14 @@
 // of the tensor-core MMA ([> Query group sharing]: "at least 16 heads");
 // [> Complexity analysis, stage 2]: each query attends k*m keys.
 //
-// One CTA handles a contiguous slice ("split") of the selected blocks of one
-// (b, h_kv, t) unit.  Each warp owns one 32 KB shared-memory stage into which
-// TMA (128-byte swizzle) loads a block's K and V tiles; the warp computes
-// S = Q K^T (16 x 64) with bf16 m16n8k16 MMAs, an online softmax in fp32 base
-// 2, and O += P V with P rounded to bf16.  The warps of a CTA merge their
-// (max, sum, O) in shared memory; with several splits per unit the CTA writes
-// an fp32 partial and the last CTA of the unit (atomic ticket) merges them.
+// One thread-block cluster of C CTAs per (b, h_kv, t) unit; the unit's
+// selected blocks are dealt round-robin to the cluster's 4*C warps.  Each
+// warp TMA-loads a block's K and V tiles (128-byte swizzle) into its own
+// 32 KB stage, computes S = Q K^T (16 x 64, bf16 m16n8k16 MMAs, fp32), an
+// online softmax in base 2, and O += P V with P fed as bf16 hi + lo parts
+// (16 significant bits).  Warps merge in shared memory, CTAs merge through
+// distributed shared memory: CTA r produces heads [16 r / C, 16 (r+1) / C)
+// of the output from every CTA's (max, sum, O) partial.  No global scratch.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -22,25 +24,29 @@ namespace infllmv2 {
 namespace {
 
 constexpr int kAttnWarps = 4;
-constexpr int kMaxSplits = 64;
 constexpr int kStageBytes = 32768;  // K tile 16 KB + V tile 16 KB
 
 struct AttnParams {
-  int B, Hkv, Lmax, nq, kmax, n_splits, bps;
+  int B, Hkv, Lmax, nq, kmax;
   float scale2;  // attn_scale * log2(e)
   const int32_t* kv_lens;
   const int32_t* block_idx;
   const int32_t* n_sel;
   __nv_bfloat16* out;
   float* lse;
-  float* part_o;      // [units][n_splits][16][128]
-  float2* part_ml;    // [units][n_splits][16]
-  uint32_t* counters; // [units]
   uint32_t* status;
 };
 
-__device__ __forceinline__ void tma_kv(uint8_t* stage, const CUtensorMap* kmap,
-                                       const CUtensorMap* vmap, int row, uint64_t* bar) {
+constexpr int kQOff = kAttnWarps * kStageBytes;         // Q tile, 4 KB
+constexpr int kCtaOOff = kQOff + 4096;                   // CTA partial O [16][128] fp32
+constexpr int kCtaMlOff = kCtaOOff + kGroup * kHeadDim * 4;  // CTA (max, sum) [16]
+constexpr int kWarpMlOff = kCtaMlOff + kGroup * 8;       // per-warp (max, sum) [4][16]
+constexpr int kWgtOff = kWarpMlOff + kAttnWarps * kGroup * 8;  // per-warp weights [4][16]
+constexpr int kBarOff = kWgtOff + kAttnWarps * kGroup * 4;
+constexpr int kAttnSmem = 1024 + kBarOff + (1 + kAttnWarps) * 8;
+
+__device__ __forceinline__ void tma_kv(uint8_t* stage, const CUtensorMap* kmap, const CUtensorMap* vmap,
+                                       int row, uint64_t* bar) {
   mbar_arrive_expect_tx(bar, kStageBytes);
   tma_load_2d(stage, kmap, 0, row, bar);
   tma_load_2d(stage + 8192, kmap, 64, row, bar);
@@ -48,35 +54,47 @@ __device__ __forceinline__ void tma_kv(uint8_t* stage, const CUtensorMap* kmap,
   tma_load_2d(stage + 24576, vmap, 64, row, bar);
 }
 
-__global__ void __launch_bounds__(kAttnWarps * 32)
-    attn_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
-                const __grid_constant__ CUtensorMap v_map, AttnParams p) {
+template <int C>
+__global__ void __launch_bounds__(kAttnWarps * 32, 1)
+    attn_cluster_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
+                        const __grid_constant__ CUtensorMap v_map, AttnParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  uint8_t* stages = smem;                                   // kAttnWarps x 32 KB
-  uint8_t* q_t = smem + kAttnWarps * kStageBytes;           // 4 KB
-  float2* ml_s = reinterpret_cast<float2*>(q_t + 4096);     // [kAttnWarps][16]
-  float* wgt_s = reinterpret_cast<float*>(ml_s + kAttnWarps * kGroup);  // [kMaxSplits][16]
-  float* inv_s = wgt_s + kMaxSplits * kGroup;               // [16]
-  float* mtot_s = inv_s + kGroup;                           // [16]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(mtot_s + kGroup);  // qbar, kv[kAttnWarps]
-  __shared__ int is_last;
+  uint8_t* q_t = smem + kQOff;
+  float* cta_o = reinterpret_cast<float*>(smem + kCtaOOff);
+  float2* cta_ml = reinterpret_cast<float2*>(smem + kCtaMlOff);
+  float2* warp_ml = reinterpret_cast<float2*>(smem + kWarpMlOff);
+  float* wgt = reinterpret_cast<float*>(smem + kWgtOff);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, tq = lane & 3;
-  const int split = blockIdx.x % p.n_splits;
-  const int t = blockIdx.x / p.n_splits;
+  const int split = static_cast<int>(cluster_ctarank());
+  const int t = blockIdx.x / C;
   const int bh = blockIdx.y;
   const int b = bh / p.Hkv, h = bh % p.Hkv;
   const int Hq = p.Hkv * kGroup;
   const size_t u = static_cast<size_t>(bh) * p.nq + t;
   const size_t orow = (static_cast<size_t>(b) * p.nq + t) * Hq + static_cast<size_t>(h) * kGroup;
+  uint64_t* qbar = bars;
+  uint64_t* kvbar = bars + 1 + warp;
+
+  if (tid == 0) {
+    prefetch_tensormap(&q_map);
+    prefetch_tensormap(&k_map);
+    prefetch_tensormap(&v_map);
+    mbar_init(qbar, 1);
+    for (int w = 0; w < kAttnWarps; ++w) mbar_init(bars + 1 + w, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  pdl_wait();
+  pdl_trigger();
 
   const int L = p.kv_lens[b];
-  if (L < p.nq || L > p.Lmax) {
+  if (L < p.nq || L > p.Lmax) {      // same for every CTA of the cluster
     if (split == 0) {
-      for (int e = tid; e < kGroup * kHeadDim; e += kAttnWarps * 32)
-        p.out[orow * kHeadDim + e] = __float2bfloat16(0.f);
+      for (int e = tid; e < kGroup * kHeadDim; e += kAttnWarps * 32) p.out[orow * kHeadDim + e] = __float2bfloat16(0.f);
       if (tid < kGroup && p.lse) p.lse[orow + tid] = -INFINITY;
       if (tid == 0 && t == 0) atomicOr(p.status, kStatusBadKvLen);
     }
@@ -85,28 +103,24 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
   const int i = L - p.nq + t;
   const int c = i / kBlock;
   const int ns = min(p.n_sel[u], p.kmax);
-  const int lo = split * p.bps;
-  const int hi = min(ns, lo + p.bps);
   const int32_t* sel = p.block_idx + u * p.kmax;
   const size_t kv_row0 = static_cast<size_t>(bh) * p.Lmax;
+  constexpr int kStride = C * kAttnWarps;   // warps in the cluster
+  const int first = split * kAttnWarps + warp;
 
-  uint64_t* qbar = bars;
-  uint64_t* kvbar = bars + 1 + warp;
-  if (tid == 0) {
-    prefetch_tensormap(&k_map);
-    prefetch_tensormap(&v_map);
-    mbar_init(qbar, 1);
-    for (int w = 0; w < kAttnWarps; ++w) mbar_init(bars + 1 + w, 1);
-    fence_barrier_init();
-  }
-  __syncthreads();
   if (tid == 0) {
     mbar_arrive_expect_tx(qbar, 4096);
     tma_load_2d(q_t, &q_map, 0, static_cast<int>(orow), qbar);
     tma_load_2d(q_t + 2048, &q_map, 64, static_cast<int>(orow), qbar);
   }
-  bool ok = __all_sync(0xffffffffu, mbar_wait(qbar, 0, p.status));
+  uint8_t* stage = smem + warp * kStageBytes;
+  const uint32_t k_b = smem_u32(stage), v_b = k_b + 16384;
+  // Start this warp's first block load before waiting for Q.
+  int n = first;
+  while (n < ns && (sel[n] < 0 || sel[n] > c)) n += kStride;
+  if (lane == 0 && n < ns) tma_kv(stage, &k_map, &v_map, static_cast<int>(kv_row0 + static_cast<size_t>(sel[n]) * kBlock), kvbar);
 
+  bool ok = __all_sync(0xffffffffu, mbar_wait(qbar, 0, p.status));
   uint32_t qa[8][4];
   const uint32_t q_b = smem_u32(q_t);
 #pragma unroll
@@ -115,28 +129,16 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
 
   float o[16][4];
 #pragma unroll
-  for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  for (int x = 0; x < 16; ++x) o[x][0] = o[x][1] = o[x][2] = o[x][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
-  uint8_t* stage = stages + warp * kStageBytes;
-  const uint32_t k_b = smem_u32(stage), v_b = k_b + 16384;
   uint32_t phase = 0;
 
 #pragma unroll 1
-  for (int n = lo + warp; n < hi && ok; n += kAttnWarps) {
+  while (n < ns && ok) {
     const int j = sel[n];
-    if (j < 0 || j > c) continue;
-    // Order this warp's earlier generic writes to the stage (zeroed V rows)
-    // before the async-proxy (TMA) writes that refill it.
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) tma_kv(stage, &k_map, &v_map, static_cast<int>(kv_row0 + static_cast<size_t>(j) * kBlock), kvbar);
-    ok = mbar_wait(kvbar, phase, p.status);
+    ok = __all_sync(0xffffffffu, mbar_wait(kvbar, phase, p.status));
     phase ^= 1u;
-    if (!__all_sync(0xffffffffu, ok)) {
-      ok = false;
-      break;
-    }
+    if (!ok) break;
     const int key0 = j * kBlock;
     if (key0 + kBlock - 1 > i) {
       // Keys past i: zero their V rows so masked probabilities never meet
@@ -187,11 +189,11 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
     l0 *= sc0;
     l1 *= sc1;
 #pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      o[n][0] *= sc0;
-      o[n][1] *= sc0;
-      o[n][2] *= sc1;
-      o[n][3] *= sc1;
+    for (int x = 0; x < 16; ++x) {
+      o[x][0] *= sc0;
+      o[x][1] *= sc0;
+      o[x][2] *= sc1;
+      o[x][3] *= sc1;
     }
     // P enters the tensor cores as hi + lo bf16 parts (16 significant bits),
     // so the only bf16 rounding left in the output is the final store.
@@ -224,6 +226,16 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
         mma_bf16_16816(o[2 * np + 1], pl[kk], vb[2], vb[3]);
       }
     }
+    // Next block of this warp.
+    n += kStride;
+    while (n < ns && (sel[n] < 0 || sel[n] > c)) n += kStride;
+    if (n < ns) {
+      // Order the generic writes to the stage (zeroed V rows) before the
+      // async-proxy (TMA) writes that refill it.
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tma_kv(stage, &k_map, &v_map, static_cast<int>(kv_row0 + static_cast<size_t>(sel[n]) * kBlock), kvbar);
+    }
   }
   __syncwarp();
 #pragma unroll
@@ -231,122 +243,134 @@ __global__ void __launch_bounds__(kAttnWarps * 32)
     l0 += __shfl_xor_sync(0xffffffffu, l0, off);
     l1 += __shfl_xor_sync(0xffffffffu, l1, off);
   }
-  // Per-warp results into the warp's own stage (K half, 8 KB of fp32).
+  // Per-warp results into the warp's own stage (8 KB of fp32).
   float* o_w = reinterpret_cast<float*>(stage);
 #pragma unroll
-  for (int n = 0; n < 16; ++n) {
-    const int d0 = n * 8 + 2 * tq;
-    *reinterpret_cast<float2*>(o_w + g * kHeadDim + d0) = make_float2(o[n][0], o[n][1]);
-    *reinterpret_cast<float2*>(o_w + (g + 8) * kHeadDim + d0) = make_float2(o[n][2], o[n][3]);
+  for (int x = 0; x < 16; ++x) {
+    const int d0 = x * 8 + 2 * tq;
+    *reinterpret_cast<float2*>(o_w + g * kHeadDim + d0) = make_float2(o[x][0], o[x][1]);
+    *reinterpret_cast<float2*>(o_w + (g + 8) * kHeadDim + d0) = make_float2(o[x][2], o[x][3]);
   }
   if (tq == 0) {
-    ml_s[warp * kGroup + g] = make_float2(m0, l0);
-    ml_s[warp * kGroup + g + 8] = make_float2(m1, l1);
+    warp_ml[warp * kGroup + g] = make_float2(m0, l0);
+    warp_ml[warp * kGroup + g + 8] = make_float2(m1, l1);
   }
   __syncthreads();
   if (tid < kGroup) {
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, ml_s[w * kGroup + tid].x);
+    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, warp_ml[w * kGroup + tid].x);
     float lsum = 0.f;
 #pragma unroll
     for (int w = 0; w < kAttnWarps; ++w) {
-      const float2 v = ml_s[w * kGroup + tid];
+      const float2 v = warp_ml[w * kGroup + tid];
       const float wt = (M == -INFINITY) ? 0.f : fast_exp2(v.x - M);
-      wgt_s[w * kGroup + tid] = wt;
+      wgt[w * kGroup + tid] = wt;
       lsum += wt * v.y;
     }
-    mtot_s[tid] = M;
-    inv_s[tid] = lsum;
+    cta_ml[tid] = make_float2(M, lsum);
   }
   __syncthreads();
-
-  const bool single = p.n_splits == 1;
   for (int e = tid; e < kGroup * kHeadDim; e += kAttnWarps * 32) {
     const int hd = e >> 7;
     float acc = 0.f;
 #pragma unroll
     for (int w = 0; w < kAttnWarps; ++w)
-      acc += wgt_s[w * kGroup + hd] * reinterpret_cast<const float*>(stages + w * kStageBytes)[e];
-    if (single) {
-      const float lsum = inv_s[hd];
-      p.out[orow * kHeadDim + e] = __float2bfloat16(lsum > 0.f ? acc / lsum : 0.f);
-    } else {
-      p.part_o[(u * p.n_splits + split) * (kGroup * kHeadDim) + e] = acc;
-    }
+      acc += wgt[w * kGroup + hd] * reinterpret_cast<const float*>(smem + w * kStageBytes)[e];
+    cta_o[e] = acc;
   }
-  if (single) {
-    if (tid < kGroup && p.lse) {
-      const float lsum = inv_s[tid];
-      p.lse[orow + tid] = lsum > 0.f ? (mtot_s[tid] + fast_log2(lsum)) * 0.69314718055994531f : -INFINITY;
-    }
-    return;
-  }
-  if (tid < kGroup) p.part_ml[(u * p.n_splits + split) * kGroup + tid] = make_float2(mtot_s[tid], inv_s[tid]);
+  cluster_sync();
 
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const uint32_t prev = atomicAdd(&p.counters[u], 1u);
-    is_last = (prev == static_cast<uint32_t>(p.n_splits) - 1) ? 1 : 0;
-  }
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  if (tid == 0) p.counters[u] = 0;
-  if (tid < kGroup) {
+  // Heads [hpc * split, hpc * (split + 1)) of the output from all partials.
+  constexpr int hpc = kGroup / C;
+  for (int e = tid; e < hpc * kHeadDim; e += kAttnWarps * 32) {
+    const int hd = split * hpc + e / kHeadDim;
+    const int d = e % kHeadDim;
+    float2 ml[C];
+    float ov[C];
+#pragma unroll
+    for (int q = 0; q < C; ++q) {
+      ml[q] = ld_dsmem_f32x2(dsmem_addr(&cta_ml[hd], q));
+      ov[q] = ld_dsmem_f32(dsmem_addr(&cta_o[hd * kHeadDim + d], q));
+    }
     float M = -INFINITY;
-    for (int sp = 0; sp < p.n_splits; ++sp) M = fmaxf(M, __ldcg(&p.part_ml[(u * p.n_splits + sp) * kGroup + tid]).x);
-    float lsum = 0.f;
-    for (int sp = 0; sp < p.n_splits; ++sp) {
-      const float2 v = __ldcg(&p.part_ml[(u * p.n_splits + sp) * kGroup + tid]);
-      const float wt = (M == -INFINITY) ? 0.f : fast_exp2(v.x - M);
-      wgt_s[sp * kGroup + tid] = wt;
-      lsum += wt * v.y;
+#pragma unroll
+    for (int q = 0; q < C; ++q) M = fmaxf(M, ml[q].x);
+    float lsum = 0.f, acc = 0.f;
+#pragma unroll
+    for (int q = 0; q < C; ++q) {
+      const float wt = (M == -INFINITY) ? 0.f : fast_exp2(ml[q].x - M);
+      lsum += wt * ml[q].y;
+      acc += wt * ov[q];
     }
-    mtot_s[tid] = M;
-    inv_s[tid] = lsum;
+    p.out[(orow + hd) * kHeadDim + d] = __float2bfloat16(lsum > 0.f ? acc / lsum : 0.f);
+    if (d == 0 && p.lse)
+      p.lse[orow + hd] = lsum > 0.f ? (M + fast_log2(lsum)) * 0.69314718055994531f : -INFINITY;
   }
-  __syncthreads();
-  for (int e = tid; e < kGroup * kHeadDim; e += kAttnWarps * 32) {
-    const int hd = e >> 7;
-    float acc = 0.f;
-    for (int sp = 0; sp < p.n_splits; ++sp)
-      acc += wgt_s[sp * kGroup + hd] * __ldcg(&p.part_o[(u * p.n_splits + sp) * (kGroup * kHeadDim) + e]);
-    const float lsum = inv_s[hd];
-    p.out[orow * kHeadDim + e] = __float2bfloat16(lsum > 0.f ? acc / lsum : 0.f);
-  }
-  if (tid < kGroup && p.lse) {
-    const float lsum = inv_s[tid];
-    p.lse[orow + tid] = lsum > 0.f ? (mtot_s[tid] + fast_log2(lsum)) * 0.69314718055994531f : -INFINITY;
-  }
+  cluster_sync();
 }
 
-constexpr int kAttnSmem = 1024 + kAttnWarps * kStageBytes + 4096 + kAttnWarps * kGroup * 8 +
-                          kMaxSplits * kGroup * 4 + 2 * kGroup * 4 + (1 + kAttnWarps) * 8;
-
-int decode_splits(const Shape& s) {
-  // One block per warp per CTA: ceil(kmax / warps) splits.
-  int n = (s.kmax + kAttnWarps - 1) / kAttnWarps;
-  return n < 1 ? 1 : (n > kMaxSplits ? kMaxSplits : n);
+int device_sm_count() {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cache[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 148;
+  }
+  return cache[dev];
 }
 
-size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+template <int C>
+cudaError_t launch_cluster(const Shape& s, const CUtensorMap& q_map, const CUtensorMap& k_map,
+                           const CUtensorMap& v_map, const AttnParams& p, cudaStream_t st, bool* unsupported) {
+  *unsupported = false;
+  cudaError_t e = cudaFuncSetAttribute(attn_cluster_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+  if (e != cudaSuccess) return e;
+  if (C > 8) {
+    e = cudaFuncSetAttribute(attn_cluster_kernel<C>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C * s.nq, s.B * s.Hkv, 1);
+  cfg.blockDim = dim3(kAttnWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = kAttnSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = C;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, attn_cluster_kernel<C>, &cfg);
+  if (e != cudaSuccess || clusters < 1) {
+    cudaGetLastError();
+    *unsupported = true;
+    return cudaSuccess;
+  }
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<C>, q_map, k_map, v_map, p);
+}
 
 }  // namespace
 
 size_t attn_workspace_bytes(const Shape& s, bool prefill) {
-  if (prefill) return 0;
-  const size_t units = static_cast<size_t>(s.B) * s.Hkv * s.nq;
-  const int ns = decode_splits(s);
-  return align256(units * 4) + align256(units * ns * kGroup * sizeof(float2)) +
-         align256(units * ns * kGroup * kHeadDim * sizeof(float));
+  (void)s;
+  (void)prefill;
+  return 0;
 }
 
 cudaError_t launch_attn(const Shape& s, bool prefill, const CUtensorMap& q_map,
                         const CUtensorMap& k_map, const CUtensorMap& v_map,
                         const int32_t* kv_lens, const int32_t* block_idx, const int32_t* n_sel,
                         void* out, float* lse, void* ws, uint32_t* status, cudaStream_t st) {
+  (void)prefill;
+  (void)ws;
   AttnParams p{};
   p.B = s.B;
   p.Hkv = s.Hkv;
@@ -360,32 +384,22 @@ cudaError_t launch_attn(const Shape& s, bool prefill, const CUtensorMap& q_map,
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
   p.status = status;
-  const size_t units = static_cast<size_t>(s.B) * s.Hkv * s.nq;
+  // Cluster size: enough warps for one block each where the SM count allows.
+  const int want = (s.kmax + kAttnWarps - 1) / kAttnWarps;
+  const long long units = static_cast<long long>(s.B) * s.Hkv * s.nq;
+  bool unsupported = false;
   cudaError_t e;
-  if (prefill) {
-    p.n_splits = 1;
-    p.bps = s.kmax;
-  } else {
-    p.n_splits = decode_splits(s);
-    p.bps = kAttnWarps;
-    if (p.n_splits * p.bps < s.kmax) p.bps = (s.kmax + p.n_splits - 1) / p.n_splits;
-    uint8_t* base = static_cast<uint8_t*>(ws);
-    p.counters = reinterpret_cast<uint32_t*>(base);
-    p.part_ml = reinterpret_cast<float2*>(base + align256(units * 4));
-    p.part_o = reinterpret_cast<float*>(base + align256(units * 4) +
-                                        align256(units * p.n_splits * kGroup * sizeof(float2)));
-    if (p.n_splits > 1) {
-      e = cudaMemsetAsync(p.counters, 0, units * 4, st);
-      if (e != cudaSuccess) return e;
-    }
+  if (want > 8 && units * 16 <= device_sm_count()) {
+    e = launch_cluster<16>(s, q_map, k_map, v_map, p, st, &unsupported);
+    if (e != cudaSuccess || !unsupported) return e;
   }
-  e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
-  if (e != cudaSuccess) return e;
-  const size_t gx = static_cast<size_t>(p.n_splits) * s.nq;
-  if (gx > 0x7fffffffull || s.B * s.Hkv > 65535) return cudaErrorInvalidConfiguration;
-  attn_kernel<<<dim3(static_cast<unsigned>(gx), s.B * s.Hkv), kAttnWarps * 32, kAttnSmem, st>>>(
-      q_map, k_map, v_map, p);
-  return cudaGetLastError();
+  if (want > 4) {
+    e = launch_cluster<8>(s, q_map, k_map, v_map, p, st, &unsupported);
+    if (e != cudaSuccess || !unsupported) return e;
+  }
+  e = launch_cluster<4>(s, q_map, k_map, v_map, p, st, &unsupported);
+  if (e == cudaSuccess && unsupported) return cudaErrorInvalidConfiguration;
+  return e;
 }
 
 }  // namespace infllmv2

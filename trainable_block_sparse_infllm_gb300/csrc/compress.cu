@@ -35,6 +35,8 @@ __global__ void __launch_bounds__(kThreads)
                     __nv_bfloat16* __restrict__ kc, uint32_t* status) {
   __shared__ __align__(16) float csum[kKernelsPerCta + 1][kHeadDim];
   const int b = blockIdx.z, h = blockIdx.y;
+  pdl_wait();
+  pdl_trigger();
   const int L = kv_lens[b];
   if (L < 0 || L > Lmax) {
     if (threadIdx.x == 0 && blockIdx.x == 0 && h == 0) atomicOr(status, kStatusBadKvLen);
@@ -54,11 +56,12 @@ __global__ void __launch_bounds__(kThreads)
   for (int cc = threadIdx.x >> 4; cc < nchunk; cc += kThreads / 16) {
     const int tok0 = (j0 + cc) * kStride;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-    for (int t = 0; t < kStride; ++t) {
-      const uint4 w = __ldg(reinterpret_cast<const uint4*>(kbh + static_cast<size_t>(tok0 + t) * kHeadDim) + sub);
-      add_bf16x8(acc, w);
-    }
+    uint4 w[kStride];   // all 16 loads in flight before the first add
+#pragma unroll
+    for (int t = 0; t < kStride; ++t)
+      w[t] = __ldg(reinterpret_cast<const uint4*>(kbh + static_cast<size_t>(tok0 + t) * kHeadDim) + sub);
+#pragma unroll
+    for (int t = 0; t < kStride; ++t) add_bf16x8(acc, w[t]);
     float4* dst = reinterpret_cast<float4*>(&csum[cc][sub * 8]);
     dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
     dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
@@ -100,11 +103,17 @@ cudaError_t launch_compress(const Shape& s, const void* k, const int32_t* kv_len
     count = e - kbegin;
   }
   if (count <= 0) return cudaSuccess;
-  dim3 grid((count + kKernelsPerCta - 1) / kKernelsPerCta, s.Hkv, s.B);
-  compress_kernel<<<grid, kThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(k), kv_lens, s.Hkv,
-                                             s.Lmax, s.ncmax, kbegin, kend,
-                                             static_cast<__nv_bfloat16*>(kc), status);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((count + kKernelsPerCta - 1) / kKernelsPerCta, s.Hkv, s.B);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.stream = st;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, compress_kernel, static_cast<const __nv_bfloat16*>(k), kv_lens, s.Hkv, s.Lmax,
+                            s.ncmax, kbegin, kend, static_cast<__nv_bfloat16*>(kc), status);
 }
 
 }  // namespace infllmv2

@@ -16,12 +16,10 @@
 // planes, which keeps 16 significant bits of the fp32 mean.
 //
 // Two paths, same result:
-//  * decode / verify (n_q <= 16): few (b, h_kv, t) units and up to thousands
-//    of kernels each, so kernels are split over CTAs.  sel_score_kernel loads
-//    a 128-kernel hi/lo tile and the group's queries with TMA, writes z and
-//    per-chunk (max, sum) partials; sel_reduce_kernel merges the partials
-//    into lse, forms g and the block maxima for a 64-block range, and the last
-//    CTA of each unit (atomic ticket) runs the top-k.
+//  * decode / verify (n_q <= 16): few (b, h_kv) groups and thousands of
+//    kernels each, so each group's kernels are spread over a thread-block
+//    cluster that exchanges LSE partials and block scores through
+//    distributed shared memory (sel_cluster_kernel, one launch).
 //  * prefill (n_q > 16): one warp per query token, TT tokens per CTA sharing
 //    a TMA pipeline of 64-kernel hi/lo tiles, streamed twice (pass 1: LSE,
 //    pass 2: normalised group mean and block maxima), then a warp top-k.
@@ -34,17 +32,15 @@ namespace infllmv2 {
 namespace {
 
 struct SelParams {
-  int B, Hkv, Lmax, nq, ncmax, ncpad, nbmax, kmax, n_chunks;
+  int B, Hkv, Lmax, nq, ncmax, ncpad, nbmax, kmax;
   int topk, n_init, n_local, inc_forced;
   float scale2;
   const int32_t* kv_lens;
   int32_t* block_idx;  // [B*Hkv*nq][kmax]
   int32_t* n_sel;      // [B*Hkv*nq]
-  float* r_buf;        // [B*Hkv*nq][nbmax]
-  float* z;            // [B*Hkv*nq][16][ncpad]      (decode path)
-  float2* part;        // [B*Hkv*nq][16][n_chunks]   (decode path)
-  uint32_t* counters;  // [B*Hkv*nq]                 (decode path)
-  int write_r;         // prefill path: write r to r_buf
+  float* r_buf;        // [B*Hkv*nq][nbmax] block scores (written when write_r)
+  float* z;            // [B*Hkv*nq][16][ncpad] scratch  (decode path)
+  int write_r;
   int stages;          // prefill path: pipeline depth
   uint32_t* status;
 };
@@ -94,202 +90,266 @@ __device__ __forceinline__ void score_ntile(float (&acc)[4], const uint32_t (&a)
 }
 
 // ------------------------------------------------------------- decode path --
+//
+// One thread-block cluster of C CTAs per (b, h_kv) group; the group's n_q
+// query tokens (<= 16) are scored together.  The blocks 0 .. floor(i/m) are
+// cut into C contiguous ranges of 16-block groups; CTA r owns the matching
+// 64-kernel chunks (kernels of blocks [16k, 16k+16) are 64k-1 .. 64k+63).
+//   phase A  TMA-stream the CTA's hi/lo chunks, z = q.Mean (tensor cores),
+//            z to scratch (L2), per-row (max, sum) partials in shared memory.
+//   sync     partials of all CTAs read through distributed shared memory
+//            -> exact LSE per head.
+//   phase B  g = mean_h exp2(z - lse) and the block maxima of the CTA's range.
+//   sync     the CTA that owns token t (t mod C) gathers the token's block
+//            scores from every CTA and runs the radix top-k.
+// No global partials, tickets or memsets: the cluster barriers order it all.
 
-constexpr int kScoreThreads = 128;  // 4 warps x 32 kernels
-constexpr int kReduceThreads = 256;
+constexpr int kClThreads = 256;   // 8 warps: one 8-kernel n-tile each per chunk
+constexpr int kClChunk = 64;      // kernels per stage (= 16 blocks)
+constexpr int kClStages = 3;
+constexpr int kClStageBytes = 2 * kClChunk * 256;
 
-__global__ void __launch_bounds__(kScoreThreads)
-    sel_score_kernel(const __grid_constant__ CUtensorMap kc_map,
-                     const __grid_constant__ CUtensorMap q_map, SelParams p) {
+struct ClLayout {
+  int stage, q, wpart, cpart, lse, g, rsl, rfull, flag, tk, bar, total, rsl_stride;
+};
+
+__host__ __device__ inline ClLayout cl_layout(int C, int nq, int nbmax) {
+  ClLayout l;
+  const int groups = (nbmax + 15) / 16;
+  const int per_cta = (groups + C - 1) / C;     // 16-block groups per CTA (upper bound)
+  l.rsl_stride = per_cta * 16;
+  l.stage = 0;
+  l.q = kClStages * kClStageBytes;
+  l.wpart = l.q + nq * 4096;
+  l.cpart = l.wpart + 8 * nq * kGroup * 8;
+  l.lse = l.cpart + nq * kGroup * 8;
+  l.g = l.lse + nq * kGroup * 4;
+  l.rsl = l.g + (per_cta * kClChunk + 4) * 4;
+  l.rfull = l.rsl + nq * l.rsl_stride * 4;
+  l.flag = l.rfull + nbmax * 4;
+  l.tk = (l.flag + nbmax + 15) & ~15;
+  l.bar = (l.tk + static_cast<int>(sizeof(TopkScratch<kClThreads>)) + 15) & ~15;
+  l.total = l.bar + (2 * kClStages + 1) * 8;
+  return l;
+}
+
+// Which CTA of the cluster owns 16-block group `grp` (ranges are
+// [floor(r * groups / C), floor((r + 1) * groups / C))).
+__device__ __forceinline__ int cl_owner(int grp, int groups, int C) {
+  int q = (grp * C) / groups;
+  while (q + 1 < C && ((q + 1) * groups) / C <= grp) ++q;
+  while (q > 0 && (q * groups) / C > grp) --q;
+  return q;
+}
+
+template <int C>
+__global__ void __launch_bounds__(kClThreads, 1)
+    sel_cluster_kernel(const __grid_constant__ CUtensorMap kc_map, const __grid_constant__ CUtensorMap q_map,
+                       SelParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int nq = p.nq;
-  uint8_t* hi_t = smem;                 // 128 rows x 128 bf16, swizzled, 32 KB
-  uint8_t* lo_t = smem + 32768;
-  uint8_t* q_t = smem + 65536;          // nq tiles of 16 rows, 4 KB each
-  float2* part_s = reinterpret_cast<float2*>(q_t + nq * 4096);   // [4][nq*16]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(part_s + 4 * nq * 16);
+  const ClLayout lay = cl_layout(C, nq, p.nbmax);
+  float2* wpart = reinterpret_cast<float2*>(smem + lay.wpart);   // [8 warps][nq*16]
+  float2* cpart = reinterpret_cast<float2*>(smem + lay.cpart);   // [nq*16]
+  float* lse2 = reinterpret_cast<float*>(smem + lay.lse);        // [nq*16]
+  float* gbuf = reinterpret_cast<float*>(smem + lay.g);
+  float* rsl = reinterpret_cast<float*>(smem + lay.rsl);         // [nq][rsl_stride]
+  float* rfull = reinterpret_cast<float*>(smem + lay.rfull);
+  uint8_t* flag = smem + lay.flag;
+  TopkScratch<kClThreads>& tk = *reinterpret_cast<TopkScratch<kClThreads>*>(smem + lay.tk);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.bar);
+  uint64_t* empty = full + kClStages;
+  uint64_t* qbar = empty + kClStages;
 
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, tq = lane & 3;
+  const int rank = static_cast<int>(cluster_ctarank());
   const int bh = blockIdx.y;
   const int b = bh / p.Hkv, h = bh % p.Hkv;
-  const int L = p.kv_lens[b];
-  if (L < nq || L > p.Lmax) {
-    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(p.status, kStatusBadKvLen);
-    return;
-  }
-  const int nc = n_complete_kernels(L);
-  const int j0 = blockIdx.x * kSelChunk;
-  if (j0 >= nc) return;
-
-  if (threadIdx.x == 0) {
-    prefetch_tensormap(&kc_map);
-    prefetch_tensormap(&q_map);
-    mbar_init(bar, 1);
-    fence_barrier_init();
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    mbar_arrive_expect_tx(bar, 2 * kSelChunk * 256 + nq * 4096);
-    const int row_hi = (bh * 2 + 0) * p.ncmax + j0;
-    const int row_lo = (bh * 2 + 1) * p.ncmax + j0;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {      // column halves (64 dims)
-#pragma unroll
-      for (int rh = 0; rh < 2; ++rh) {          // row halves (64 kernels)
-        tma_load_2d(hi_t + half * 16384 + rh * 8192, &kc_map, half * 64, row_hi + rh * 64, bar);
-        tma_load_2d(lo_t + half * 16384 + rh * 8192, &kc_map, half * 64, row_lo + rh * 64, bar);
-      }
-    }
-    const int Hq = p.Hkv * kGroup;
-    for (int t = 0; t < nq; ++t) {
-      const int row = (b * nq + t) * Hq + h * kGroup;
-      tma_load_2d(q_t + t * 4096, &q_map, 0, row, bar);
-      tma_load_2d(q_t + t * 4096 + 2048, &q_map, 64, row, bar);
-    }
-  }
-  const bool ok = __syncthreads_and(mbar_wait(bar, 0, p.status));
-  if (!ok) return;
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, tq = lane & 3;
-  const uint32_t hi_b = smem_u32(hi_t), lo_b = smem_u32(lo_t), q_b = smem_u32(q_t);
   const size_t unit0 = static_cast<size_t>(bh) * nq;
 
-  for (int t = 0; t < nq; ++t) {
-    const int i = L - nq + t;
-    const int nvis = n_complete_kernels(i + 1);
-    uint32_t a[8][4];
-    load_q_frags(a, q_b + t * 4096, lane);
-    float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
-    float* zrow = p.z + ((unit0 + t) * kGroup + g) * static_cast<size_t>(p.ncpad);
+  if (tid == 0) {
+    prefetch_tensormap(&kc_map);
+    prefetch_tensormap(&q_map);
+    for (int s = 0; s < kClStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 8);
+    }
+    mbar_init(qbar, 1);
+    fence_barrier_init();
+  }
+  for (int e = tid; e < 8 * nq * kGroup; e += kClThreads) wpart[e] = make_float2(-INFINITY, 0.f);
+  __syncthreads();
+  pdl_wait();
+  pdl_trigger();
+
+  const int L = p.kv_lens[b];
+  if (L < nq || L > p.Lmax) {        // same for every CTA of the cluster
+    if (rank == 0) {
+      for (int e = tid; e < nq * p.kmax; e += kClThreads) p.block_idx[unit0 * p.kmax + e] = -1;
+      for (int e = tid; e < nq; e += kClThreads) p.n_sel[unit0 + e] = 0;
+      if (p.write_r)
+        for (int e = tid; e < nq * p.nbmax; e += kClThreads) p.r_buf[unit0 * p.nbmax + e] = -INFINITY;
+      if (tid == 0) atomicOr(p.status, kStatusBadKvLen);
+    }
+    return;
+  }
+  const int nbt = (L - 1) / kBlock + 1;            // blocks visible to the last token
+  const int groups = (nbt + 15) / 16;
+  const int k0 = (rank * groups) / C, k1 = ((rank + 1) * groups) / C;
+  const int nc = n_complete_kernels(L);
+  const int nmy = max(0, min(k1, (nc + kClChunk - 1) / kClChunk) - k0);   // chunks to stream
+
+  auto issue = [&](int it) {
+    const int st = it % kClStages;
+    const int row = (k0 + it) * kClChunk;
+    uint8_t* dst = smem + lay.stage + st * kClStageBytes;
+    mbar_arrive_expect_tx(&full[st], kClStageBytes);
+    tma_load_2d(dst, &kc_map, 0, (bh * 2 + 0) * p.ncmax + row, &full[st]);
+    tma_load_2d(dst + 8192, &kc_map, 64, (bh * 2 + 0) * p.ncmax + row, &full[st]);
+    tma_load_2d(dst + 16384, &kc_map, 0, (bh * 2 + 1) * p.ncmax + row, &full[st]);
+    tma_load_2d(dst + 24576, &kc_map, 64, (bh * 2 + 1) * p.ncmax + row, &full[st]);
+  };
+  if (tid == 0) {
+    if (nmy > 0) {
+      mbar_arrive_expect_tx(qbar, nq * 4096);
+      const int Hq = p.Hkv * kGroup;
+      for (int t = 0; t < nq; ++t) {
+        const int row = (b * nq + t) * Hq + h * kGroup;
+        tma_load_2d(smem + lay.q + t * 4096, &q_map, 0, row, qbar);
+        tma_load_2d(smem + lay.q + t * 4096 + 2048, &q_map, 64, row, qbar);
+      }
+    }
+    for (int it = 0; it < min(kClStages, nmy); ++it) issue(it);
+  }
+
+  // ------------------------------------------------------------ phase A --
+  bool ok = true;
+  if (nmy > 0) ok = __syncthreads_and(mbar_wait(qbar, 0, p.status));
+  const uint32_t q_b = smem_u32(smem + lay.q);
 #pragma unroll 1
-    for (int nt = 0; nt < 4; ++nt) {
-      const int n0 = warp * 32 + nt * 8;
+  for (int it = 0; it < nmy && ok; ++it) {
+    const int st = it % kClStages;
+    const uint32_t ph = static_cast<uint32_t>(it / kClStages) & 1u;
+    ok = __all_sync(0xffffffffu, mbar_wait(&full[st], ph, p.status));
+    if (!ok) break;
+    const int kbase = (k0 + it) * kClChunk;
+    const uint32_t hi_b = smem_u32(smem + lay.stage + st * kClStageBytes);
+    const int kj = kbase + warp * 8 + 2 * tq;
+#pragma unroll 1
+    for (int t = 0; t < nq; ++t) {
+      const int nvis = n_complete_kernels(L - nq + t + 1);
+      uint32_t a[8][4];
+      load_q_frags(a, q_b + t * 4096, lane);
       float acc[4];
-      score_ntile(acc, a, hi_b, lo_b, n0, kSelChunk, lane);
-      const int kj = j0 + n0 + 2 * tq;
+      score_ntile(acc, a, hi_b, hi_b + 16384, warp * 8, kClChunk, lane);
       const bool v0 = kj < nvis, v1 = kj + 1 < nvis;
       const float z0 = v0 ? acc[0] * p.scale2 : -INFINITY;
       const float z1 = v1 ? acc[1] * p.scale2 : -INFINITY;
       const float z2 = v0 ? acc[2] * p.scale2 : -INFINITY;
       const float z3 = v1 ? acc[3] * p.scale2 : -INFINITY;
+      float* zrow = p.z + ((unit0 + t) * kGroup + g) * static_cast<size_t>(p.ncpad);
       *reinterpret_cast<float2*>(zrow + kj) = make_float2(z0, z1);
       *reinterpret_cast<float2*>(zrow + 8 * static_cast<size_t>(p.ncpad) + kj) = make_float2(z2, z3);
+      float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
       lse_add2(m0, l0, z0, z1);
       lse_add2(m1, l1, z2, z3);
-    }
 #pragma unroll
-    for (int o = 1; o <= 2; o <<= 1) {
-      lse_merge(m0, l0, __shfl_xor_sync(0xffffffffu, m0, o), __shfl_xor_sync(0xffffffffu, l0, o));
-      lse_merge(m1, l1, __shfl_xor_sync(0xffffffffu, m1, o), __shfl_xor_sync(0xffffffffu, l1, o));
-    }
-    if (tq == 0) {
-      part_s[(warp * nq + t) * kGroup + g] = make_float2(m0, l0);
-      part_s[(warp * nq + t) * kGroup + g + 8] = make_float2(m1, l1);
-    }
-  }
-  __syncthreads();
-  for (int row = threadIdx.x; row < nq * kGroup; row += kScoreThreads) {
-    float m = -INFINITY, l = 0.f;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const float2 v = part_s[w * nq * kGroup + row];
-      lse_merge(m, l, v.x, v.y);
-    }
-    p.part[(unit0 * kGroup + row) * p.n_chunks + blockIdx.x] = make_float2(m, l);
-  }
-}
-
-__global__ void __launch_bounds__(kReduceThreads) sel_reduce_kernel(SelParams p) {
-  extern __shared__ __align__(16) uint8_t dsm[];
-  __shared__ float lse2[kGroup];
-  __shared__ float gs[4 * kSelReduceBlocks + 4];
-  __shared__ TopkScratch<kReduceThreads> tk;
-  __shared__ int is_last;
-  float* r_s = reinterpret_cast<float*>(dsm);
-  uint8_t* flag_s = reinterpret_cast<uint8_t*>(r_s + p.nbmax);
-
-  const int tid = threadIdx.x;
-  const int u = blockIdx.y;
-  const int bh = u / p.nq, t = u % p.nq;
-  const int b = bh / p.Hkv;
-  const int L = p.kv_lens[b];
-  int32_t* idx_out = p.block_idx + static_cast<size_t>(u) * p.kmax;
-  float* r_row = p.r_buf + static_cast<size_t>(u) * p.nbmax;
-  const int jb0 = blockIdx.x * kSelReduceBlocks;
-  const int jend = min(p.nbmax, jb0 + kSelReduceBlocks);
-
-  if (L < p.nq || L > p.Lmax) {
-    for (int j = jb0 + tid; j < jend; j += kReduceThreads) r_row[j] = -INFINITY;
-    if (blockIdx.x == 0) {
-      for (int k = tid; k < p.kmax; k += kReduceThreads) idx_out[k] = -1;
-      if (tid == 0) {
-        p.n_sel[u] = 0;
-        atomicOr(p.status, kStatusBadKvLen);
+      for (int o = 1; o <= 2; o <<= 1) {
+        lse_merge(m0, l0, __shfl_xor_sync(0xffffffffu, m0, o), __shfl_xor_sync(0xffffffffu, l0, o));
+        lse_merge(m1, l1, __shfl_xor_sync(0xffffffffu, m1, o), __shfl_xor_sync(0xffffffffu, l1, o));
+      }
+      if (tq == 0) {
+        float2* w0 = &wpart[warp * nq * kGroup + t * kGroup + g];
+        float2 v = *w0;
+        lse_merge(v.x, v.y, m0, l0);
+        *w0 = v;
+        float2* w1 = w0 + 8;
+        v = *w1;
+        lse_merge(v.x, v.y, m1, l1);
+        *w1 = v;
       }
     }
-    return;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+    if (tid == 0 && it + kClStages < nmy) {
+      if (mbar_wait(&empty[st], ph, p.status)) issue(it + kClStages);
+    }
+    __syncwarp();
   }
-  const int i = L - p.nq + t;
-  const int c = i / kBlock;
-  const int nb = c + 1;
-  const int nvis = n_complete_kernels(i + 1);
-  if (jb0 >= nb) {
-    for (int j = jb0 + tid; j < jend; j += kReduceThreads) r_row[j] = -INFINITY;
-    return;
-  }
-  const int jb1 = min(nb, jb0 + kSelReduceBlocks);
-
-  {  // lse of each head from the scoring CTAs' partials
-    const int head = tid >> 4, sub = tid & 15;
-    const int n_sc = (nvis + kSelChunk - 1) / kSelChunk;
+  __syncthreads();
+  for (int row = tid; row < nq * kGroup; row += kClThreads) {
     float m = -INFINITY, l = 0.f;
-    const float2* pp = p.part + (static_cast<size_t>(u) * kGroup + head) * p.n_chunks;
-    for (int ch = sub; ch < n_sc; ch += 16) {
-      const float2 v = __ldcg(pp + ch);
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const float2 v = wpart[w * nq * kGroup + row];
       lse_merge(m, l, v.x, v.y);
     }
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1)
-      lse_merge(m, l, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, l, o));
-    if (sub == 0) lse2[head] = (m == -INFINITY) ? -INFINITY : m + fast_log2(l);
+    cpart[row] = make_float2(m, l);
   }
-  __syncthreads();
+  cluster_sync();
 
-  const int klo = max(0, 4 * jb0 - 1);
-  const int khi = min(nvis, 4 * (jb1 - 1) + 4);
-  const float* zu = p.z + static_cast<size_t>(u) * kGroup * p.ncpad;
-  for (int k = klo + tid; k < khi; k += kReduceThreads) {
-    float s = 0.f;
+  // ---------------------------------------------- LSE over the cluster --
+  for (int row = tid; row < nq * kGroup; row += kClThreads) {
+    float m = -INFINITY, l = 0.f;
 #pragma unroll
-    for (int hh = 0; hh < kGroup; ++hh) s += fast_exp2(__ldcg(zu + static_cast<size_t>(hh) * p.ncpad + k) - lse2[hh]);
-    gs[k - klo] = s * (1.0f / kGroup);
-  }
-  __syncthreads();
-  for (int j = jb0 + tid; j < jend; j += kReduceThreads) {
-    float r = -INFINITY;
-    if (j < jb1) {
-      const int a = max(0, 4 * j - 1), e = min(nvis - 1, 4 * j + 3);
-      for (int k = a; k <= e; ++k) r = fmaxf(r, gs[k - klo]);
+    for (int q = 0; q < C; ++q) {
+      const float2 v = ld_dsmem_f32x2(dsmem_addr(&cpart[row], q));
+      lse_merge(m, l, v.x, v.y);
     }
-    r_row[j] = r;
+    lse2[row] = (m == -INFINITY) ? -INFINITY : m + fast_log2(l);
   }
+  __syncthreads();
 
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const uint32_t nparts = (nb + kSelReduceBlocks - 1) / kSelReduceBlocks;
-    const uint32_t prev = atomicAdd(&p.counters[u], 1u);
-    is_last = (prev == nparts - 1) ? 1 : 0;
+  // ------------------------------------------------------------ phase B --
+  for (int t = 0; t < nq; ++t) {
+    const int i = L - nq + t;
+    const int c = i / kBlock;
+    const int nvis = n_complete_kernels(i + 1);
+    const int jb0 = 16 * k0, jb1 = min(16 * k1, c + 1);
+    if (jb0 < jb1) {
+      const int klo = max(0, 4 * jb0 - 1);
+      const int khi = min(nvis, 4 * (jb1 - 1) + 4);
+      const float* zu = p.z + (unit0 + t) * kGroup * static_cast<size_t>(p.ncpad);
+      const float* lt = lse2 + t * kGroup;
+      for (int k = klo + tid; k < khi; k += kClThreads) {
+        float s = 0.f;
+#pragma unroll
+        for (int hh = 0; hh < kGroup; ++hh) s += fast_exp2(__ldcg(zu + static_cast<size_t>(hh) * p.ncpad + k) - lt[hh]);
+        gbuf[k - klo] = s * (1.0f / kGroup);
+      }
+      __syncthreads();
+      for (int j = jb0 + tid; j < jb1; j += kClThreads) {
+        const int a0 = max(0, 4 * j - 1), e0 = min(nvis - 1, 4 * j + 3);
+        float r = -INFINITY;
+        for (int k = a0; k <= e0; ++k) r = fmaxf(r, gbuf[k - klo]);
+        rsl[t * lay.rsl_stride + (j - jb0)] = r;
+        if (p.write_r) p.r_buf[(unit0 + t) * p.nbmax + j] = r;
+      }
+    }
+    __syncthreads();
   }
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  if (tid == 0) p.counters[u] = 0;
-  for (int j = tid; j < nb; j += kReduceThreads) r_s[j] = __ldcg(r_row + j);
-  __syncthreads();
-  select_topk<kReduceThreads, false>(r_s, flag_s, nb, p.n_init, p.n_local, p.topk, p.inc_forced != 0,
-                                     p.kmax, idx_out, p.n_sel + u, tk, tid);
+  cluster_sync();
+
+  // ------------------------------------------------------------- top-k --
+  for (int t = rank; t < nq; t += C) {
+    const int i = L - nq + t;
+    const int nb = i / kBlock + 1;
+    for (int j = tid; j < nb; j += kClThreads) {
+      const int grp = j >> 4;
+      const int q = cl_owner(grp, groups, C);
+      const int base = 16 * ((q * groups) / C);
+      rfull[j] = ld_dsmem_f32(dsmem_addr(&rsl[t * lay.rsl_stride + (j - base)], q));
+    }
+    if (p.write_r)
+      for (int j = nb + tid; j < p.nbmax; j += kClThreads) p.r_buf[(unit0 + t) * p.nbmax + j] = -INFINITY;
+    __syncthreads();
+    select_topk<kClThreads, false>(rfull, flag, nb, p.n_init, p.n_local, p.topk, p.inc_forced != 0, p.kmax,
+                                   p.block_idx + (unit0 + t) * p.kmax, p.n_sel + unit0 + t, tk, tid);
+    __syncthreads();
+  }
+  cluster_sync();
 }
 
 // ------------------------------------------------------------ prefill path --
@@ -482,27 +542,67 @@ __global__ void __launch_bounds__(kPrefTokens * 32)
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-struct DecodeWs {
-  size_t counters, part, z, r, total;
-};
+int device_sm_count() {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cache[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 148;
+  }
+  return cache[dev];
+}
 
-DecodeWs decode_ws(const Shape& s) {
-  const size_t units = static_cast<size_t>(s.B) * s.Hkv * s.nq;
-  const int n_chunks = (s.ncmax + kSelChunk - 1) / kSelChunk;
-  const size_t ncpad = static_cast<size_t>(n_chunks) * kSelChunk;
-  DecodeWs w;
-  w.counters = 0;
-  w.part = align256(units * 4);
-  w.z = w.part + align256(units * kGroup * n_chunks * sizeof(float2));
-  w.r = w.z + align256(units * kGroup * ncpad * sizeof(float));
-  w.total = w.r + align256(units * s.nbmax * sizeof(float));
-  return w;
+size_t decode_ncpad(const Shape& s) { return static_cast<size_t>((s.ncmax + kClChunk - 1) / kClChunk) * kClChunk; }
+
+template <int C>
+cudaError_t launch_cluster(const Shape& s, const CUtensorMap& kc_map, const CUtensorMap& q_map, const SelParams& p,
+                           cudaStream_t st, bool* unsupported) {
+  const int smem = cl_layout(C, s.nq, s.nbmax).total + 1024;
+  *unsupported = false;
+  if (smem > 227 * 1024) {
+    *unsupported = true;
+    return cudaSuccess;
+  }
+  cudaError_t e = cudaFuncSetAttribute(sel_cluster_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  if (C > 8) {
+    e = cudaFuncSetAttribute(sel_cluster_kernel<C>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C, s.B * s.Hkv, 1);
+  cfg.blockDim = dim3(kClThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = C;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, sel_cluster_kernel<C>, &cfg);
+  if (e != cudaSuccess || clusters < 1) {
+    cudaGetLastError();
+    *unsupported = true;
+    return cudaSuccess;
+  }
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, sel_cluster_kernel<C>, kc_map, q_map, p);
 }
 
 }  // namespace
 
 size_t select_workspace_bytes(const Shape& s) {
-  if (s.nq <= kSelDecodeMaxNq) return decode_ws(s).total;
+  if (s.nq <= kSelDecodeMaxNq) {
+    const size_t units = static_cast<size_t>(s.B) * s.Hkv * s.nq;
+    return align256(units * kGroup * decode_ncpad(s) * sizeof(float));
+  }
   return 0;  // the prefill path keeps everything on chip
 }
 
@@ -528,37 +628,23 @@ cudaError_t launch_select(const Shape& s, const CUtensorMap& kc_map, const CUten
   p.block_idx = block_idx;
   p.n_sel = n_sel;
   p.status = status;
-  uint8_t* base = static_cast<uint8_t*>(ws);
-
-  if (s.nq <= kSelDecodeMaxNq) {
-    const DecodeWs w = decode_ws(s);
-    p.n_chunks = (s.ncmax + kSelChunk - 1) / kSelChunk;
-    p.ncpad = p.n_chunks * kSelChunk;
-    p.counters = reinterpret_cast<uint32_t*>(base + w.counters);
-    p.part = reinterpret_cast<float2*>(base + w.part);
-    p.z = reinterpret_cast<float*>(base + w.z);
-    p.r_buf = block_scores ? block_scores : reinterpret_cast<float*>(base + w.r);
-    const size_t units = static_cast<size_t>(s.B) * s.Hkv * s.nq;
-    cudaError_t e = cudaMemsetAsync(p.counters, 0, units * 4, st);
-    if (e != cudaSuccess) return e;
-    if (p.n_chunks > 0) {
-      const int smem = 1024 + 65536 + s.nq * 4096 + 4 * s.nq * kGroup * 8 + 16;
-      e = cudaFuncSetAttribute(sel_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e != cudaSuccess) return e;
-      sel_score_kernel<<<dim3(p.n_chunks, s.B * s.Hkv), kScoreThreads, smem, st>>>(kc_map, q_map, p);
-      e = cudaGetLastError();
-      if (e != cudaSuccess) return e;
-    }
-    const int rsmem = s.nbmax * 5 + 16;
-    e = cudaFuncSetAttribute(sel_reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, rsmem);
-    if (e != cudaSuccess) return e;
-    const int nrc = (s.nbmax + kSelReduceBlocks - 1) / kSelReduceBlocks;
-    sel_reduce_kernel<<<dim3(nrc, static_cast<unsigned>(units)), kReduceThreads, rsmem, st>>>(p);
-    return cudaGetLastError();
-  }
-
   p.write_r = block_scores != nullptr;
   p.r_buf = block_scores;
+
+  if (s.nq <= kSelDecodeMaxNq) {
+    p.ncpad = static_cast<int>(decode_ncpad(s));
+    p.z = static_cast<float*>(ws);
+    bool unsupported = false;
+    cudaError_t e = cudaSuccess;
+    if (s.B * s.Hkv * 16 <= device_sm_count()) {
+      e = launch_cluster<16>(s, kc_map, q_map, p, st, &unsupported);
+      if (e != cudaSuccess || !unsupported) return e;
+    }
+    e = launch_cluster<8>(s, kc_map, q_map, p, st, &unsupported);
+    if (e == cudaSuccess && unsupported) return cudaErrorInvalidConfiguration;
+    return e;
+  }
+
   int stages = 3;
   PrefLayout lay = pref_layout(stages, s.nbmax);
   if (lay.total + 1024 > 227 * 1024) {
