@@ -23,7 +23,7 @@ namespace infllmv2 {
 
 namespace {
 
-constexpr int kAttnWarps = 4;
+constexpr int kAttnWarps = 3;      // 3 x 32 KB stages: two CTAs fit on one SM
 constexpr int kStageBytes = 32768;  // K tile 16 KB + V tile 16 KB
 
 struct AttnParams {
@@ -55,7 +55,7 @@ __device__ __forceinline__ void tma_kv(uint8_t* stage, const CUtensorMap* kmap, 
 }
 
 template <int C>
-__global__ void __launch_bounds__(kAttnWarps * 32, 1)
+__global__ void __launch_bounds__(kAttnWarps * 32, 2)
     attn_cluster_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
                         const __grid_constant__ CUtensorMap v_map, AttnParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -348,7 +348,9 @@ cudaError_t launch_cluster(const Shape& s, const CUtensorMap& q_map, const CUten
   cfg.numAttrs = 1;
   int clusters = 0;
   e = cudaOccupancyMaxActiveClusters(&clusters, attn_cluster_kernel<C>, &cfg);
-  if (e != cudaSuccess || clusters < 1) {
+  // The 16-CTA form only pays off when every unit's cluster is resident at once.
+  const long long need = (C > 8) ? static_cast<long long>(s.B) * s.Hkv * s.nq : 1;
+  if (e != cudaSuccess || clusters < need) {
     cudaGetLastError();
     *unsupported = true;
     return cudaSuccess;
@@ -389,7 +391,7 @@ cudaError_t launch_attn(const Shape& s, bool prefill, const CUtensorMap& q_map,
   const long long units = static_cast<long long>(s.B) * s.Hkv * s.nq;
   bool unsupported = false;
   cudaError_t e;
-  if (want > 8 && units * 16 <= device_sm_count()) {
+  if (want > 8 && units * 16 <= 2 * device_sm_count()) {
     e = launch_cluster<16>(s, q_map, k_map, v_map, p, st, &unsupported);
     if (e != cudaSuccess || !unsupported) return e;
   }

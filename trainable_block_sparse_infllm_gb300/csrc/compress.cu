@@ -56,12 +56,15 @@ __global__ void __launch_bounds__(kThreads)
   for (int cc = threadIdx.x >> 4; cc < nchunk; cc += kThreads / 16) {
     const int tok0 = (j0 + cc) * kStride;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    uint4 w[kStride];   // all 16 loads in flight before the first add
 #pragma unroll
-    for (int t = 0; t < kStride; ++t)
-      w[t] = __ldg(reinterpret_cast<const uint4*>(kbh + static_cast<size_t>(tok0 + t) * kHeadDim) + sub);
+    for (int half = 0; half < 2; ++half) {
+      uint4 w[kStride / 2];   // eight loads in flight before the first add
 #pragma unroll
-    for (int t = 0; t < kStride; ++t) add_bf16x8(acc, w[t]);
+      for (int t = 0; t < kStride / 2; ++t)
+        w[t] = __ldg(reinterpret_cast<const uint4*>(kbh + static_cast<size_t>(tok0 + half * 8 + t) * kHeadDim) + sub);
+#pragma unroll
+      for (int t = 0; t < kStride / 2; ++t) add_bf16x8(acc, w[t]);
+    }
     float4* dst = reinterpret_cast<float4*>(&csum[cc][sub * 8]);
     dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
     dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);

@@ -106,7 +106,7 @@ __device__ __forceinline__ void score_ntile(float (&acc)[4], const uint32_t (&a)
 
 constexpr int kClThreads = 256;   // 8 warps: one 8-kernel n-tile each per chunk
 constexpr int kClChunk = 64;      // kernels per stage (= 16 blocks)
-constexpr int kClStages = 3;
+constexpr int kClStages = 2;   // small enough for two CTAs per SM
 constexpr int kClStageBytes = 2 * kClChunk * 256;
 
 struct ClLayout {
@@ -143,7 +143,7 @@ __device__ __forceinline__ int cl_owner(int grp, int groups, int C) {
 }
 
 template <int C>
-__global__ void __launch_bounds__(kClThreads, 1)
+__global__ void __launch_bounds__(kClThreads, 2)
     sel_cluster_kernel(const __grid_constant__ CUtensorMap kc_map, const __grid_constant__ CUtensorMap q_map,
                        SelParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -336,11 +336,24 @@ __global__ void __launch_bounds__(kClThreads, 1)
   for (int t = rank; t < nq; t += C) {
     const int i = L - nq + t;
     const int nb = i / kBlock + 1;
-    for (int j = tid; j < nb; j += kClThreads) {
-      const int grp = j >> 4;
-      const int q = cl_owner(grp, groups, C);
-      const int base = 16 * ((q * groups) / C);
-      rfull[j] = ld_dsmem_f32(dsmem_addr(&rsl[t * lay.rsl_stride + (j - base)], q));
+    // Gather in batches: all remote loads of a batch are in flight together.
+    for (int j0 = 0; j0 < nb; j0 += 8 * kClThreads) {
+      float v[8];
+#pragma unroll
+      for (int x = 0; x < 8; ++x) {
+        const int j = j0 + x * kClThreads + tid;
+        v[x] = -INFINITY;
+        if (j < nb) {
+          const int q = cl_owner(j >> 4, groups, C);
+          const int base = 16 * ((q * groups) / C);
+          v[x] = ld_dsmem_f32(dsmem_addr(&rsl[t * lay.rsl_stride + (j - base)], q));
+        }
+      }
+#pragma unroll
+      for (int x = 0; x < 8; ++x) {
+        const int j = j0 + x * kClThreads + tid;
+        if (j < nb) rfull[j] = v[x];
+      }
     }
     if (p.write_r)
       for (int j = nb + tid; j < p.nbmax; j += kClThreads) p.r_buf[(unit0 + t) * p.nbmax + j] = -INFINITY;
@@ -587,7 +600,9 @@ cudaError_t launch_cluster(const Shape& s, const CUtensorMap& kc_map, const CUte
   cfg.numAttrs = 1;
   int clusters = 0;
   e = cudaOccupancyMaxActiveClusters(&clusters, sel_cluster_kernel<C>, &cfg);
-  if (e != cudaSuccess || clusters < 1) {
+  // The 16-CTA form only pays off when every group's cluster is resident at once.
+  const int need = (C > 8) ? s.B * s.Hkv : 1;
+  if (e != cudaSuccess || clusters < need) {
     cudaGetLastError();
     *unsupported = true;
     return cudaSuccess;
@@ -636,7 +651,8 @@ cudaError_t launch_select(const Shape& s, const CUtensorMap& kc_map, const CUten
     p.z = static_cast<float*>(ws);
     bool unsupported = false;
     cudaError_t e = cudaSuccess;
-    if (s.B * s.Hkv * 16 <= device_sm_count()) {
+    // 16-CTA clusters when every group's cluster can be resident at once.
+    if (s.B * s.Hkv * 16 <= 2 * device_sm_count()) {
       e = launch_cluster<16>(s, kc_map, q_map, p, st, &unsupported);
       if (e != cudaSuccess || !unsupported) return e;
     }

@@ -105,11 +105,17 @@ __device__ void select_topk(const float* r, uint8_t* flag, int nb, int n_init, i
       const int shift = 24 - 8 * pass;
       for (int b = tid; b < 256; b += NT) sm.hist[b] = 0;
       group_sync<WARP>();
-      for (int j = tid; j < nb; j += NT) {
-        if (flag[j] == 1) {
+      // Scores share their leading digits (same sign and exponent), so the
+      // lanes of a warp that hit the same bin add once, with their count.
+      for (int j0 = 0; j0 < nb; j0 += NT) {
+        const int j = j0 + tid;
+        int digit = -1;
+        if (j < nb && flag[j] == 1) {
           const uint32_t key = float_to_ordered(r[j]);
-          if ((key & pmask) == prefix) atomicAdd(&sm.hist[(key >> shift) & 255u], 1u);
+          if ((key & pmask) == prefix) digit = static_cast<int>((key >> shift) & 255u);
         }
+        const unsigned same = __match_any_sync(0xffffffffu, digit);
+        if (digit >= 0 && (tid & 31) == __ffs(same) - 1) atomicAdd(&sm.hist[digit], static_cast<unsigned>(__popc(same)));
       }
       group_sync<WARP>();
       if (tid < 32) {
