@@ -248,3 +248,28 @@ def test_workload_parity(dev, name):
         refs = {u: v for u, v in refs.items() if u[2] >= 1024}
     mx, mean = check_attention(run, refs, strict=True)
     print(f"{name}: units={len(units)} tie-band differences={ties} max|dO|={mx:.2e} mean={mean:.2e}")
+
+
+def test_select_exact_ties_break_to_lower_block(dev):
+    # The key sequence repeats after `half` keys, so block j and block
+    # j + half/64 see bit-identical kernel means and score exactly alike; both
+    # sides must keep the lower block of every tied pair (ties go to the lower
+    # index).  A second case makes every block identical, which exercises the
+    # many-way tie path of the top-k.
+    import torch
+    for period_blocks, L in ((40, 80 * 64), (1, 20000)):
+        inp = S.make_random(batch=1, n_kv_heads=2, kv_len=L, n_q=2, topk=12, seed=31)
+        half = period_blocks * 64
+        k = inp.k.copy()
+        for start in range(half, L, half):
+            n = min(half, L - start)
+            k[:, :, start:start + n] = inp.k[:, :, :n]
+        inp.k[...] = k
+        run = GpuRun(inp, dev)
+        run.compress()
+        run.select()
+        torch.cuda.synchronize()
+        sels = O.run_selection(inp, _settings(inp.wl))
+        idx, nsel = run.idx.cpu().numpy(), run.nsel.cpu().numpy()
+        for (b, h, t), s in sels.items():
+            assert idx[b, h, t, :nsel[b, h, t]].tolist() == s.blocks.tolist(), ((b, h, t), period_blocks)

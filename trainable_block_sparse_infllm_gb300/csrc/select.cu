@@ -128,7 +128,7 @@ __host__ __device__ inline ClLayout cl_layout(int C, int nq, int nbmax) {
   l.rfull = l.rsl + nq * l.rsl_stride * 4;
   l.flag = l.rfull + nbmax * 4;
   l.tk = (l.flag + nbmax + 15) & ~15;
-  l.bar = (l.tk + static_cast<int>(sizeof(TopkScratch<kClThreads>)) + 15) & ~15;
+  l.bar = (l.tk + static_cast<int>(sizeof(FastTopkScratch<kClThreads>)) + 15) & ~15;
   l.total = l.bar + (2 * kClStages + 1) * 8;
   return l;
 }
@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(kClThreads, 2)
   float* rsl = reinterpret_cast<float*>(smem + lay.rsl);         // [nq][rsl_stride]
   float* rfull = reinterpret_cast<float*>(smem + lay.rfull);
   uint8_t* flag = smem + lay.flag;
-  TopkScratch<kClThreads>& tk = *reinterpret_cast<TopkScratch<kClThreads>*>(smem + lay.tk);
+  FastTopkScratch<kClThreads>& tk = *reinterpret_cast<FastTopkScratch<kClThreads>*>(smem + lay.tk);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.bar);
   uint64_t* empty = full + kClStages;
   uint64_t* qbar = empty + kClStages;
@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(kClThreads, 2)
     if (p.write_r)
       for (int j = nb + tid; j < p.nbmax; j += kClThreads) p.r_buf[(unit0 + t) * p.nbmax + j] = -INFINITY;
     __syncthreads();
-    select_topk<kClThreads, false>(rfull, flag, nb, p.n_init, p.n_local, p.topk, p.inc_forced != 0, p.kmax,
+    select_topk_fast<kClThreads>(rfull, flag, nb, p.n_init, p.n_local, p.topk, p.inc_forced != 0, p.kmax,
                                    p.block_idx + (unit0 + t) * p.kmax, p.n_sel + unit0 + t, tk, tid);
     __syncthreads();
   }
