@@ -105,17 +105,11 @@ __device__ void select_topk(const float* r, uint8_t* flag, int nb, int n_init, i
       const int shift = 24 - 8 * pass;
       for (int b = tid; b < 256; b += NT) sm.hist[b] = 0;
       group_sync<WARP>();
-      // Scores share their leading digits (same sign and exponent), so the
-      // lanes of a warp that hit the same bin add once, with their count.
-      for (int j0 = 0; j0 < nb; j0 += NT) {
-        const int j = j0 + tid;
-        int digit = -1;
-        if (j < nb && flag[j] == 1) {
+      for (int j = tid; j < nb; j += NT) {
+        if (flag[j] == 1) {
           const uint32_t key = float_to_ordered(r[j]);
-          if ((key & pmask) == prefix) digit = static_cast<int>((key >> shift) & 255u);
+          if ((key & pmask) == prefix) atomicAdd(&sm.hist[(key >> shift) & 255u], 1u);
         }
-        const unsigned same = __match_any_sync(0xffffffffu, digit);
-        if (digit >= 0 && (tid & 31) == __ffs(same) - 1) atomicAdd(&sm.hist[digit], static_cast<unsigned>(__popc(same)));
       }
       group_sync<WARP>();
       if (tid < 32) {
@@ -178,19 +172,19 @@ __device__ void select_topk(const float* r, uint8_t* flag, int nb, int n_init, i
 }
 
 // Same contract as select_topk for a whole CTA (NT threads, NT % 32 == 0),
-// built for few syncs: one 256-bin histogram of the scores' leading bits
-// (sign, exponent, 4 mantissa bits, counted down from the largest score)
-// finds the bin holding the n_take-th best score; every candidate at or
-// above that bin survives, and each survivor's exact rank among the
-// survivors, by (score desc, index asc), decides whether it is taken.
-// Falls back to the radix select when the survivors exceed the scratch.
+// built for few barriers and no contended atomics: one 256-bin histogram of
+// the scores' leading bits (sign, exponent, 6 mantissa bits, counted down
+// from the best score; per-warp private copies) finds the bin holding the
+// n_take-th best score; every candidate at or above that bin survives, and
+// each survivor's exact rank among the survivors, by (score desc, index
+// asc), decides whether it is taken.  Falls back to the radix select when
+// the survivors exceed NT (many exactly tied or very close scores).
 template <int NT>
 struct FastTopkScratch {
-  uint32_t hist[256];
-  uint32_t skey[NT];     // survivors: ordered key
-  int sidx[NT];          // survivors: block index
+  uint32_t hist[NT / 32][256];  // per-warp histograms
+  unsigned long long surv[NT];  // survivors: (ordered key << 32) | ~index
   int ctrl[8];
-  int warp_tot[NT / 32];
+  int wcnt[NT / 32][3];
   TopkScratch<NT> radix;
 };
 
@@ -198,66 +192,65 @@ template <int NT>
 __device__ void select_topk_fast(const float* r, uint8_t* flag, int nb, int n_init, int n_local, int topk,
                                  bool includes_forced, int k_max, int32_t* out_idx, int32_t* out_n,
                                  FastTopkScratch<NT>& sm, int tid) {
+  constexpr int NWARP = NT / 32;
+  constexpr int kShift = 17;   // 1 sign + 8 exponent + 6 mantissa bits
   const int lane = tid & 31, warp = tid >> 5;
   const int c = nb - 1;
   const int local_lo = c - n_local + 1;
-  // 1. flags, candidate count, forced count, largest leading-bits bin.
+  const int per = (nb + NT - 1) / NT;
+  const int lo = tid * per;
+  const int hi = min(nb, lo + per);
+  // 1. flags (contiguous range per thread), counts, best leading bits.
   int my_cand = 0, my_forced = 0;
   uint32_t my_top = 0;
-  for (int j = tid; j < nb; j += NT) {
+  for (int j = lo; j < hi; ++j) {
     const bool forced = (j < n_init) || (j >= local_lo);
     const bool cand = !forced && (r[j] > -INFINITY);
     flag[j] = forced ? 2 : (cand ? 1 : 0);
     my_cand += cand ? 1 : 0;
     my_forced += forced ? 1 : 0;
-    if (cand) my_top = max(my_top, float_to_ordered(r[j]) >> 19);
+    if (cand) my_top = max(my_top, float_to_ordered(r[j]) >> kShift);
   }
-  for (int b = tid; b < 256; b += NT) sm.hist[b] = 0;
+  for (int b = lane; b < 256; b += 32) sm.hist[warp][b] = 0;
+  my_cand = __reduce_add_sync(0xffffffffu, my_cand);
+  my_forced = __reduce_add_sync(0xffffffffu, my_forced);
+  my_top = __reduce_max_sync(0xffffffffu, my_top);
+  if (lane == 0) {
+    sm.wcnt[warp][0] = my_cand;
+    sm.wcnt[warp][1] = my_forced;
+    sm.wcnt[warp][2] = static_cast<int>(my_top);
+  }
+  __syncthreads();
+  int n_cand = 0, n_forced = 0;
+  uint32_t top = 0;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    my_cand += __shfl_xor_sync(0xffffffffu, my_cand, o);
-    my_forced += __shfl_xor_sync(0xffffffffu, my_forced, o);
-    my_top = max(my_top, __shfl_xor_sync(0xffffffffu, my_top, o));
+  for (int w = 0; w < NWARP; ++w) {
+    n_cand += sm.wcnt[w][0];
+    n_forced += sm.wcnt[w][1];
+    top = max(top, static_cast<uint32_t>(sm.wcnt[w][2]));
   }
-  if (lane == 0) {
-    sm.ctrl[0] = 0;
-    sm.ctrl[1] = 0;
-    sm.ctrl[2] = 0;
-  }
-  __syncthreads();
-  if (lane == 0) {
-    atomicAdd(&sm.ctrl[0], my_cand);
-    atomicAdd(&sm.ctrl[1], my_forced);
-    atomicMax(&sm.ctrl[2], static_cast<int>(my_top));
-  }
-  __syncthreads();
-  const int n_cand = sm.ctrl[0];
-  const int n_forced = sm.ctrl[1];
-  const uint32_t top = static_cast<uint32_t>(sm.ctrl[2]);
   int n_take = includes_forced ? topk - n_forced : topk;
   if (n_take < 0) n_take = 0;
 
   bool use_radix = false;
   if (n_take > 0 && n_cand <= n_take) {
-    for (int j = tid; j < nb; j += NT)
+    for (int j = lo; j < hi; ++j)
       if (flag[j] == 1) flag[j] = 3;
   } else if (n_take > 0) {
-    // 2. histogram of bins (0 = the best bin), lanes of a bin add once.
-    for (int j0 = 0; j0 < nb; j0 += NT) {
-      const int j = j0 + tid;
-      int bin = -1;
-      if (j < nb && flag[j] == 1) bin = static_cast<int>(min(255u, top - (float_to_ordered(r[j]) >> 19)));
-      const unsigned same = __match_any_sync(0xffffffffu, bin);
-      if (bin >= 0 && lane == __ffs(same) - 1) atomicAdd(&sm.hist[bin], static_cast<unsigned>(__popc(same)));
-    }
+    // 2. per-warp histograms of bins (0 = the best bin).
+    for (int j = lo; j < hi; ++j)
+      if (flag[j] == 1) atomicAdd(&sm.hist[warp][min(255u, top - (float_to_ordered(r[j]) >> kShift))], 1u);
     __syncthreads();
     // 3. boundary bin: the first whose cumulative count reaches n_take.
     if (warp == 0) {
       int cnt[8], tot = 0;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        cnt[k] = static_cast<int>(sm.hist[8 * lane + k]);
-        tot += cnt[k];
+        int v = 0;
+#pragma unroll
+        for (int w = 0; w < NWARP; ++w) v += static_cast<int>(sm.hist[w][8 * lane + k]);
+        cnt[k] = v;
+        tot += v;
       }
       int run = warp_inclusive_scan(tot) - tot;
 #pragma unroll
@@ -275,38 +268,29 @@ __device__ void select_topk_fast(const float* r, uint8_t* flag, int nb, int n_in
     if (n_surv > NT) {
       use_radix = true;
     } else {
-      // 4. compact the survivors (any order) into shared memory.
-      if (tid == 0) sm.ctrl[5] = 0;
-      __syncthreads();
-      for (int j0 = 0; j0 < nb; j0 += NT) {
-        const int j = j0 + tid;
-        bool keep = false;
-        uint32_t key = 0;
-        if (j < nb && flag[j] == 1) {
-          key = float_to_ordered(r[j]);
-          keep = static_cast<int>(min(255u, top - (key >> 19))) <= bnd;
-        }
-        const unsigned ballot = __ballot_sync(0xffffffffu, keep);
-        int base = 0;
-        if (lane == 0 && ballot) base = atomicAdd(&sm.ctrl[5], __popc(ballot));
-        base = __shfl_sync(0xffffffffu, base, 0);
-        if (keep) {
-          const int pos = base + __popc(ballot & ((1u << lane) - 1u));
-          sm.skey[pos] = key;
-          sm.sidx[pos] = j;
-        }
+      // 4. survivors into shared memory, positions from a prefix count.
+      int my_keep = 0;
+      for (int j = lo; j < hi; ++j)
+        my_keep += (flag[j] == 1 && static_cast<int>(min(255u, top - (float_to_ordered(r[j]) >> kShift))) <= bnd) ? 1 : 0;
+      int tot_keep;
+      int pos = group_exclusive_scan<NT, false>(my_keep, tot_keep, sm.radix, tid);
+      for (int j = lo; j < hi; ++j) {
+        if (flag[j] != 1) continue;
+        const uint32_t key = float_to_ordered(r[j]);
+        if (static_cast<int>(min(255u, top - (key >> kShift))) <= bnd)
+          sm.surv[pos++] = (static_cast<unsigned long long>(key) << 32) | static_cast<uint32_t>(~j);
       }
       __syncthreads();
       // 5. exact rank among the survivors; the best n_take are taken.
       if (tid < n_surv) {
-        const uint32_t k0 = sm.skey[tid];
-        const int j0 = sm.sidx[tid];
+        const unsigned long long me = sm.surv[tid];
         int rank = 0;
-        for (int x = 0; x < n_surv; ++x) {
-          const uint32_t kx = sm.skey[x];
-          rank += (kx > k0 || (kx == k0 && sm.sidx[x] < j0)) ? 1 : 0;
+        int x = 0;
+        for (; x + 4 <= n_surv; x += 4) {
+          rank += (sm.surv[x] > me) + (sm.surv[x + 1] > me) + (sm.surv[x + 2] > me) + (sm.surv[x + 3] > me);
         }
-        if (rank < n_take) flag[j0] = 3;
+        for (; x < n_surv; ++x) rank += (sm.surv[x] > me) ? 1 : 0;
+        if (rank < n_take) flag[static_cast<int>(~static_cast<uint32_t>(me & 0xffffffffu))] = 3;
       }
     }
   }
@@ -318,9 +302,6 @@ __device__ void select_topk_fast(const float* r, uint8_t* flag, int nb, int n_in
   }
   __syncthreads();
   // 6. ascending output of forced + taken blocks.
-  const int per = (nb + NT - 1) / NT;
-  const int lo = tid * per;
-  const int hi = min(nb, lo + per);
   int my_sel = 0;
   for (int j = lo; j < hi; ++j) my_sel += (flag[j] >= 2) ? 1 : 0;
   int total;
