@@ -99,9 +99,14 @@ __device__ __forceinline__ void score_ntile(float (&acc)[4], const uint32_t (&a)
 //            z to scratch (L2), per-row (max, sum) partials in shared memory.
 //   sync     partials of all CTAs read through distributed shared memory
 //            -> exact LSE per head.
-//   phase B  g = mean_h exp2(z - lse) and the block maxima of the CTA's range.
-//   sync     the CTA that owns token t (t mod C) gathers the token's block
-//            scores from every CTA and runs the radix top-k.
+//   phase B  g = mean_h exp2(z - lse) and the block maxima of the CTA's range,
+//            with the range's candidate count and best score.
+//   top-k    (cluster-wide, three barriers) each CTA histograms its blocks'
+//            scores by leading bits against the cluster's best score; the
+//            summed histogram gives the bin holding the k-th best score;
+//            the few candidates at or above it are gathered by the CTA that
+//            owns token t (t mod C), ranked exactly by (score desc, index
+//            asc), and written ascending with the forced blocks.
 // No global partials, tickets or memsets: the cluster barriers order it all.
 
 constexpr int kClThreads = 256;   // 8 warps: one 8-kernel n-tile each per chunk
@@ -109,11 +114,17 @@ constexpr int kClChunk = 64;      // kernels per stage (= 16 blocks)
 constexpr int kClStages = 2;   // small enough for two CTAs per SM
 constexpr int kClStageBytes = 2 * kClChunk * 256;
 
-struct ClLayout {
-  int stage, q, wpart, cpart, lse, g, rsl, rfull, flag, tk, bar, total, rsl_stride;
+// Per-token top-k bookkeeping shared across the cluster.
+struct ClTok {
+  int n_cand, n_forced, top, n_take;   // local counts / max (then global in `glob`)
+  int bnd, n_surv, n_lsurv, pad;
 };
 
-__host__ __device__ inline ClLayout cl_layout(int C, int nq, int nbmax) {
+struct ClLayout {
+  int stage, q, wpart, cpart, lse, g, rsl, tok, glob, hist, ghist, lsurv, gsurv, sel, bar, total, rsl_stride;
+};
+
+__host__ __device__ inline ClLayout cl_layout(int C, int nq, int nbmax, int kmax) {
   ClLayout l;
   const int groups = (nbmax + 15) / 16;
   const int per_cta = (groups + C - 1) / C;     // 16-block groups per CTA (upper bound)
@@ -125,21 +136,30 @@ __host__ __device__ inline ClLayout cl_layout(int C, int nq, int nbmax) {
   l.lse = l.cpart + nq * kGroup * 8;
   l.g = l.lse + nq * kGroup * 4;
   l.rsl = l.g + (per_cta * kClChunk + 4) * 4;
-  l.rfull = l.rsl + nq * l.rsl_stride * 4;
-  l.flag = l.rfull + nbmax * 4;
-  l.tk = (l.flag + nbmax + 15) & ~15;
-  l.bar = (l.tk + static_cast<int>(sizeof(FastTopkScratch<kClThreads>)) + 15) & ~15;
+  l.tok = (l.rsl + nq * l.rsl_stride * 4 + 15) & ~15;       // local ClTok per token
+  l.glob = l.tok + nq * static_cast<int>(sizeof(ClTok));     // cluster-wide ClTok per token
+  l.hist = l.glob + nq * static_cast<int>(sizeof(ClTok));    // local histograms [nq][256]
+  l.ghist = l.hist + nq * 256 * 4;                           // cluster histograms [nq][256]
+  l.lsurv = (l.ghist + nq * 256 * 4 + 15) & ~15;             // local survivors [nq][rsl_stride]
+  l.gsurv = l.lsurv + nq * l.rsl_stride * 8;                 // gathered survivors [nbmax]
+  l.sel = l.gsurv + nbmax * 8;                               // chosen blocks [kmax]
+  l.bar = (l.sel + kmax * 4 + 15) & ~15;
   l.total = l.bar + (2 * kClStages + 1) * 8;
   return l;
 }
 
-// Which CTA of the cluster owns 16-block group `grp` (ranges are
-// [floor(r * groups / C), floor((r + 1) * groups / C))).
-__device__ __forceinline__ int cl_owner(int grp, int groups, int C) {
-  int q = (grp * C) / groups;
-  while (q + 1 < C && ((q + 1) * groups) / C <= grp) ++q;
-  while (q > 0 && (q * groups) / C > grp) --q;
-  return q;
+// Scores are binned by their leading bits (sign, exponent, 6 mantissa bits):
+// a bin spans about 1.1 % of the score.
+constexpr int kClBinShift = 17;
+
+// A block competes for the scored slots if it is not forced and some visible
+// kernel touches it.
+__device__ __forceinline__ bool cl_candidate(int j, int c, float r, int n_init, int n_local) {
+  return j >= n_init && j <= c - n_local && r > -INFINITY;
+}
+
+__device__ __forceinline__ int cl_bin(uint32_t top, float r) {
+  return static_cast<int>(min(255u, top - (float_to_ordered(r) >> kClBinShift)));
 }
 
 template <int C>
@@ -149,15 +169,19 @@ __global__ void __launch_bounds__(kClThreads, 2)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int nq = p.nq;
-  const ClLayout lay = cl_layout(C, nq, p.nbmax);
+  const ClLayout lay = cl_layout(C, nq, p.nbmax, p.kmax);
   float2* wpart = reinterpret_cast<float2*>(smem + lay.wpart);   // [8 warps][nq*16]
   float2* cpart = reinterpret_cast<float2*>(smem + lay.cpart);   // [nq*16]
   float* lse2 = reinterpret_cast<float*>(smem + lay.lse);        // [nq*16]
   float* gbuf = reinterpret_cast<float*>(smem + lay.g);
   float* rsl = reinterpret_cast<float*>(smem + lay.rsl);         // [nq][rsl_stride]
-  float* rfull = reinterpret_cast<float*>(smem + lay.rfull);
-  uint8_t* flag = smem + lay.flag;
-  FastTopkScratch<kClThreads>& tk = *reinterpret_cast<FastTopkScratch<kClThreads>*>(smem + lay.tk);
+  ClTok* tok = reinterpret_cast<ClTok*>(smem + lay.tok);         // [nq] this CTA's slice
+  ClTok* glob = reinterpret_cast<ClTok*>(smem + lay.glob);       // [nq] whole cluster
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem + lay.hist);    // [nq][256]
+  uint32_t* ghist = reinterpret_cast<uint32_t*>(smem + lay.ghist);  // [nq][256]
+  unsigned long long* lsurv = reinterpret_cast<unsigned long long*>(smem + lay.lsurv);  // [nq][rsl_stride]
+  unsigned long long* gsurv = reinterpret_cast<unsigned long long*>(smem + lay.gsurv);  // [nbmax]
+  int* selbuf = reinterpret_cast<int*>(smem + lay.sel);          // [kmax]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.bar);
   uint64_t* empty = full + kClStages;
   uint64_t* qbar = empty + kClStages;
@@ -180,6 +204,8 @@ __global__ void __launch_bounds__(kClThreads, 2)
     fence_barrier_init();
   }
   for (int e = tid; e < 8 * nq * kGroup; e += kClThreads) wpart[e] = make_float2(-INFINITY, 0.f);
+  for (int e = tid; e < nq * 256; e += kClThreads) hist[e] = 0u;
+  for (int e = tid; e < nq; e += kClThreads) tok[e] = ClTok{0, 0, 0, 0, 0, 0, 0, 0};
   __syncthreads();
   pdl_wait();
   pdl_trigger();
@@ -308,8 +334,8 @@ __global__ void __launch_bounds__(kClThreads, 2)
     const int c = i / kBlock;
     const int nvis = n_complete_kernels(i + 1);
     const int jb0 = 16 * k0, jb1 = min(16 * k1, c + 1);
+    const int klo = max(0, 4 * jb0 - 1);
     if (jb0 < jb1) {
-      const int klo = max(0, 4 * jb0 - 1);
       const int khi = min(nvis, 4 * (jb1 - 1) + 4);
       const float* zu = p.z + (unit0 + t) * kGroup * static_cast<size_t>(p.ncpad);
       const float* lt = lse2 + t * kGroup;
@@ -320,46 +346,159 @@ __global__ void __launch_bounds__(kClThreads, 2)
         gbuf[k - klo] = s * (1.0f / kGroup);
       }
       __syncthreads();
-      for (int j = jb0 + tid; j < jb1; j += kClThreads) {
-        const int a0 = max(0, 4 * j - 1), e0 = min(nvis - 1, 4 * j + 3);
-        float r = -INFINITY;
-        for (int k = a0; k <= e0; ++k) r = fmaxf(r, gbuf[k - klo]);
-        rsl[t * lay.rsl_stride + (j - jb0)] = r;
-        if (p.write_r) p.r_buf[(unit0 + t) * p.nbmax + j] = r;
+    }
+    int my_cand = 0;
+    uint32_t my_top = 0;
+    for (int j = jb0 + tid; j < jb1; j += kClThreads) {
+      const int a0 = max(0, 4 * j - 1), e0 = min(nvis - 1, 4 * j + 3);
+      float r = -INFINITY;
+      for (int k = a0; k <= e0; ++k) r = fmaxf(r, gbuf[k - klo]);
+      rsl[t * lay.rsl_stride + (j - jb0)] = r;
+      if (p.write_r) p.r_buf[(unit0 + t) * p.nbmax + j] = r;
+      if (cl_candidate(j, c, r, p.n_init, p.n_local)) {
+        ++my_cand;
+        my_top = max(my_top, float_to_ordered(r) >> kClBinShift);
       }
+    }
+    my_cand = __reduce_add_sync(0xffffffffu, my_cand);
+    my_top = __reduce_max_sync(0xffffffffu, my_top);
+    if (lane == 0 && my_cand > 0) {
+      atomicAdd(&tok[t].n_cand, my_cand);
+      atomicMax(&tok[t].top, static_cast<int>(my_top));
     }
     __syncthreads();
   }
   cluster_sync();
 
   // ------------------------------------------------------------- top-k --
-  for (int t = rank; t < nq; t += C) {
-    const int i = L - nq + t;
-    const int nb = i / kBlock + 1;
-    // Gather in batches: all remote loads of a batch are in flight together.
-    for (int j0 = 0; j0 < nb; j0 += 8 * kClThreads) {
-      float v[8];
+  // 1. cluster-wide candidate count and best leading bits; forced blocks are
+  //    known in closed form (first n_init, the n_local ending at block c).
+  for (int t = tid; t < nq; t += kClThreads) {
+    int ncand = 0, top = 0;
 #pragma unroll
-      for (int x = 0; x < 8; ++x) {
-        const int j = j0 + x * kClThreads + tid;
-        v[x] = -INFINITY;
-        if (j < nb) {
-          const int q = cl_owner(j >> 4, groups, C);
-          const int base = 16 * ((q * groups) / C);
-          v[x] = ld_dsmem_f32(dsmem_addr(&rsl[t * lay.rsl_stride + (j - base)], q));
-        }
-      }
-#pragma unroll
-      for (int x = 0; x < 8; ++x) {
-        const int j = j0 + x * kClThreads + tid;
-        if (j < nb) rfull[j] = v[x];
+    for (int q = 0; q < C; ++q) {
+      ncand += static_cast<int>(ld_dsmem_u32(dsmem_addr(&tok[t].n_cand, q)));
+      top = max(top, static_cast<int>(ld_dsmem_u32(dsmem_addr(&tok[t].top, q))));
+    }
+    const int c = (L - nq + t) / kBlock;
+    const int n_first = min(p.n_init, c + 1);
+    const int n_forced = n_first + max(0, c - max(n_first, c - p.n_local + 1) + 1);
+    const int n_take = max(0, p.inc_forced ? p.topk - n_forced : p.topk);
+    glob[t] = ClTok{ncand, n_forced, top, n_take, 255, 0, 0, 0};
+  }
+  __syncthreads();
+  // 2. local histograms of the bins (0 = best bin) where a threshold is needed.
+  for (int t = 0; t < nq; ++t) {
+    const ClTok gt = glob[t];
+    if (gt.n_take > 0 && gt.n_cand > gt.n_take) {
+      const int c = (L - nq + t) / kBlock;
+      const int jb0 = 16 * k0, jb1 = min(16 * k1, c + 1);
+      for (int j = jb0 + tid; j < jb1; j += kClThreads) {
+        const float r = rsl[t * lay.rsl_stride + (j - jb0)];
+        if (cl_candidate(j, c, r, p.n_init, p.n_local))
+          atomicAdd(&hist[t * 256 + cl_bin(static_cast<uint32_t>(gt.top), r)], 1u);
       }
     }
+  }
+  cluster_sync();
+  // 3. cluster histograms -> the bin holding the n_take-th best score; every
+  //    candidate at or above it survives.
+  for (int t = 0; t < nq; ++t) {
+    const ClTok gt = glob[t];
+    if (gt.n_take > 0 && gt.n_cand > gt.n_take) {
+      uint32_t v = 0;
+#pragma unroll
+      for (int q = 0; q < C; ++q) v += ld_dsmem_u32(dsmem_addr(&hist[t * 256 + tid], q));
+      ghist[t * 256 + tid] = v;
+    }
+  }
+  __syncthreads();
+  for (int t = warp; t < nq; t += kClThreads / 32) {
+    const ClTok gt = glob[t];
+    int bnd = gt.n_take > 0 ? 255 : -1;
+    if (gt.n_take > 0 && gt.n_cand > gt.n_take) {
+      int cnt[8], tot = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        cnt[k] = static_cast<int>(ghist[t * 256 + 8 * lane + k]);
+        tot += cnt[k];
+      }
+      int run = warp_inclusive_scan(tot) - tot;
+      int found = -1;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (run < gt.n_take && run + cnt[k] >= gt.n_take) found = 8 * lane + k;
+        run += cnt[k];
+      }
+      bnd = __reduce_max_sync(0xffffffffu, found);
+    }
+    if (lane == 0) glob[t].bnd = bnd;
+  }
+  __syncthreads();
+  for (int t = 0; t < nq; ++t) {
+    const ClTok gt = glob[t];
+    if (gt.bnd < 0) continue;
+    const int c = (L - nq + t) / kBlock;
+    const int jb0 = 16 * k0, jb1 = min(16 * k1, c + 1);
+    for (int j = jb0 + tid; j < jb1; j += kClThreads) {
+      const float r = rsl[t * lay.rsl_stride + (j - jb0)];
+      if (cl_candidate(j, c, r, p.n_init, p.n_local) && cl_bin(static_cast<uint32_t>(gt.top), r) <= gt.bnd) {
+        const int pos = atomicAdd(&tok[t].n_lsurv, 1);
+        lsurv[t * lay.rsl_stride + pos] =
+            (static_cast<unsigned long long>(float_to_ordered(r)) << 32) | static_cast<uint32_t>(~j);
+      }
+    }
+  }
+  cluster_sync();
+  // 4. the CTA that owns token t gathers the survivors, ranks them by
+  //    (score desc, index asc), and writes forced + best blocks ascending.
+  __shared__ int offs[C + 1];
+  for (int t = rank; t < nq; t += C) {
+    const ClTok gt = glob[t];
+    const int c = (L - nq + t) / kBlock;
+    const int nb = c + 1;
+    if (warp == 0) {
+      const int v = lane < C ? static_cast<int>(ld_dsmem_u32(dsmem_addr(&tok[t].n_lsurv, lane))) : 0;
+      const int incl = warp_inclusive_scan(v);
+      if (lane < C) offs[lane] = incl - v;
+      if (lane == C - 1) offs[C] = incl;
+    }
+    if (tid == 0) {   // forced blocks, ascending and without duplicates
+      const int n_first = min(p.n_init, nb);
+      int n = 0;
+      for (int j = 0; j < n_first; ++j) selbuf[n++] = j;
+      for (int j = max(n_first, c - p.n_local + 1); j <= c; ++j) selbuf[n++] = j;
+    }
+    __syncthreads();
+    const int n_surv = offs[C];
+    for (int q = 0; q < C; ++q) {
+      const int cnt = offs[q + 1] - offs[q];
+      for (int e = tid; e < cnt; e += kClThreads)
+        gsurv[offs[q] + e] = ld_dsmem_u64(dsmem_addr(&lsurv[t * lay.rsl_stride + e], q));
+    }
+    __syncthreads();
+    for (int x = tid; x < n_surv; x += kClThreads) {
+      const unsigned long long me = gsurv[x];
+      int rk = 0;
+      int y = 0;
+      for (; y + 4 <= n_surv; y += 4)
+        rk += (gsurv[y] > me) + (gsurv[y + 1] > me) + (gsurv[y + 2] > me) + (gsurv[y + 3] > me);
+      for (; y < n_surv; ++y) rk += (gsurv[y] > me) ? 1 : 0;
+      if (rk < gt.n_take) selbuf[gt.n_forced + rk] = static_cast<int>(~static_cast<uint32_t>(me & 0xffffffffu));
+    }
+    __syncthreads();
+    const int n_total = min(p.kmax, gt.n_forced + min(gt.n_take, n_surv));
+    int32_t* out = p.block_idx + (unit0 + t) * p.kmax;
+    for (int x = tid; x < n_total; x += kClThreads) {
+      const int v = selbuf[x];
+      int pos = 0;
+      for (int y = 0; y < n_total; ++y) pos += (selbuf[y] < v) ? 1 : 0;
+      out[pos] = v;
+    }
+    for (int x = n_total + tid; x < p.kmax; x += kClThreads) out[x] = -1;
+    if (tid == 0) p.n_sel[unit0 + t] = n_total;
     if (p.write_r)
       for (int j = nb + tid; j < p.nbmax; j += kClThreads) p.r_buf[(unit0 + t) * p.nbmax + j] = -INFINITY;
-    __syncthreads();
-    select_topk_fast<kClThreads>(rfull, flag, nb, p.n_init, p.n_local, p.topk, p.inc_forced != 0, p.kmax,
-                                   p.block_idx + (unit0 + t) * p.kmax, p.n_sel + unit0 + t, tk, tid);
     __syncthreads();
   }
   cluster_sync();
@@ -572,7 +711,7 @@ size_t decode_ncpad(const Shape& s) { return static_cast<size_t>((s.ncmax + kClC
 template <int C>
 cudaError_t launch_cluster(const Shape& s, const CUtensorMap& kc_map, const CUtensorMap& q_map, const SelParams& p,
                            cudaStream_t st, bool* unsupported) {
-  const int smem = cl_layout(C, s.nq, s.nbmax).total + 1024;
+  const int smem = cl_layout(C, s.nq, s.nbmax, s.kmax).total + 1024;
   *unsupported = false;
   if (smem > 227 * 1024) {
     *unsupported = true;
