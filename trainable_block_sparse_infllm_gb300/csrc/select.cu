@@ -318,12 +318,12 @@ __global__ void __launch_bounds__(kClThreads, 2)
 
   // ---------------------------------------------- LSE over the cluster --
   for (int row = tid; row < nq * kGroup; row += kClThreads) {
+    float2 v[C];   // all remote loads first, so their round trips overlap
+#pragma unroll
+    for (int q = 0; q < C; ++q) v[q] = ld_dsmem_f32x2(dsmem_addr(&cpart[row], q));
     float m = -INFINITY, l = 0.f;
 #pragma unroll
-    for (int q = 0; q < C; ++q) {
-      const float2 v = ld_dsmem_f32x2(dsmem_addr(&cpart[row], q));
-      lse_merge(m, l, v.x, v.y);
-    }
+    for (int q = 0; q < C; ++q) lse_merge(m, l, v[q].x, v[q].y);
     lse2[row] = (m == -INFINITY) ? -INFINITY : m + fast_log2(l);
   }
   __syncthreads();
@@ -374,11 +374,17 @@ __global__ void __launch_bounds__(kClThreads, 2)
   // 1. cluster-wide candidate count and best leading bits; forced blocks are
   //    known in closed form (first n_init, the n_local ending at block c).
   for (int t = tid; t < nq; t += kClThreads) {
+    uint32_t nc[C], tp[C];
+#pragma unroll
+    for (int q = 0; q < C; ++q) {
+      nc[q] = ld_dsmem_u32(dsmem_addr(&tok[t].n_cand, q));
+      tp[q] = ld_dsmem_u32(dsmem_addr(&tok[t].top, q));
+    }
     int ncand = 0, top = 0;
 #pragma unroll
     for (int q = 0; q < C; ++q) {
-      ncand += static_cast<int>(ld_dsmem_u32(dsmem_addr(&tok[t].n_cand, q)));
-      top = max(top, static_cast<int>(ld_dsmem_u32(dsmem_addr(&tok[t].top, q))));
+      ncand += static_cast<int>(nc[q]);
+      top = max(top, static_cast<int>(tp[q]));
     }
     const int c = (L - nq + t) / kBlock;
     const int n_first = min(p.n_init, c + 1);
@@ -406,9 +412,12 @@ __global__ void __launch_bounds__(kClThreads, 2)
   for (int t = 0; t < nq; ++t) {
     const ClTok gt = glob[t];
     if (gt.n_take > 0 && gt.n_cand > gt.n_take) {
+      uint32_t hv[C];
+#pragma unroll
+      for (int q = 0; q < C; ++q) hv[q] = ld_dsmem_u32(dsmem_addr(&hist[t * 256 + tid], q));
       uint32_t v = 0;
 #pragma unroll
-      for (int q = 0; q < C; ++q) v += ld_dsmem_u32(dsmem_addr(&hist[t * 256 + tid], q));
+      for (int q = 0; q < C; ++q) v += hv[q];
       ghist[t * 256 + tid] = v;
     }
   }
@@ -471,10 +480,11 @@ __global__ void __launch_bounds__(kClThreads, 2)
     }
     __syncthreads();
     const int n_surv = offs[C];
-    for (int q = 0; q < C; ++q) {
-      const int cnt = offs[q + 1] - offs[q];
-      for (int e = tid; e < cnt; e += kClThreads)
-        gsurv[offs[q] + e] = ld_dsmem_u64(dsmem_addr(&lsurv[t * lay.rsl_stride + e], q));
+    // One remote load per thread: survivor x lives in CTA q, slot x - offs[q].
+    for (int x = tid; x < n_surv; x += kClThreads) {
+      int q = 0;
+      while (q + 1 < C && offs[q + 1] <= x) ++q;
+      gsurv[x] = ld_dsmem_u64(dsmem_addr(&lsurv[t * lay.rsl_stride + (x - offs[q])], q));
     }
     __syncthreads();
     for (int x = tid; x < n_surv; x += kClThreads) {
