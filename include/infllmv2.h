@@ -143,6 +143,28 @@ int infllmv2_select_blocks(const infllmv2_params* p, const void* q, int32_t n_q,
                            void* stream);
 
 /*
+ * infllmv2_select_blocks without a caller workspace.  The MiniCPM4 pages have
+ * no counterpart of this entry point; it exists for embedders that cannot
+ * hand the library device scratch at the call site: inference engines whose
+ * device memory is laid out once at start-up, and plain C hosts that have no
+ * device allocator of their own.
+ *   Same arguments and result as infllmv2_select_blocks, minus the
+ *   workspace.  Scratch comes from a fixed 8 MiB array inside the library
+ *   (held by every device that loads it until the process exits); a
+ *   selection whose scratch (infllmv2_workspace_size(p, n_q,
+ *   INFLLMV2_OP_SELECT)) exceeds 8 MiB returns INFLLMV2_WORKSPACE_TOO_SMALL
+ *   and launches nothing.  It allocates and frees nothing.
+ *   The first call on a device looks up that device's address of the array
+ *   (once); make that first call before any stream capture.  Every call
+ *   shares the one array: calls whose work overlaps on the GPU (different
+ *   streams, no ordering) race.  Nothing in the array has to start at zero;
+ *   each call writes what it reads first.
+ */
+int infllmv2_select_blocks_static(const infllmv2_params* p, const void* q, int32_t n_q, const void* kc,
+                                  const int32_t* kv_lens, int32_t* block_idx, int32_t* n_selected,
+                                  float* block_scores, void* stream);
+
+/*
  * Stage 3, few queries per sequence (decode n_q = 1, speculative verification
  * n_q <= 16): the selected blocks of each (b, h_kv, t) are dealt to the CTAs
  * of a thread-block cluster; each CTA computes an online-softmax partial and

@@ -111,6 +111,22 @@ def select_blocks(p: Params, q: torch.Tensor, kc: torch.Tensor, kv_lens: torch.T
     return block_idx, n_selected
 
 
+def select_blocks_static(p: Params, q: torch.Tensor, kc: torch.Tensor, kv_lens: torch.Tensor,
+                         block_idx: torch.Tensor, n_selected: torch.Tensor,
+                         block_scores: torch.Tensor | None = None, stream=None):
+    """select_blocks with the library's built-in scratch instead of a workspace.
+
+    For embedders that cannot hand over device scratch at the call site
+    (start-up-planned device memory, C hosts without a device allocator).
+    At most 8 MiB of scratch; calls that overlap on the GPU share it.
+    """
+    n_q = q.shape[1]
+    _lib.check(_lib.lib.infllmv2_select_blocks_static(ctypes.byref(p), _ptr(q), n_q, _ptr(kc), _ptr(kv_lens),
+                                                      _ptr(block_idx), _ptr(n_selected), _ptr(block_scores),
+                                                      _stream(stream)))
+    return block_idx, n_selected
+
+
 def _attn(fn, p, q, k_cache, v_cache, kv_lens, block_idx, n_selected, out, lse, workspace, stream):
     n_q = q.shape[1]
     ws_bytes = workspace.numel() if workspace is not None else 0

@@ -78,6 +78,8 @@ lib.infllmv2_compress_keys.argtypes = [_P, _vp, _vp, _i32, _i32, _vp, _vp]
 lib.infllmv2_compress_keys.restype = ctypes.c_int
 lib.infllmv2_select_blocks.argtypes = [_P, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
 lib.infllmv2_select_blocks.restype = ctypes.c_int
+lib.infllmv2_select_blocks_static.argtypes = [_P, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp]
+lib.infllmv2_select_blocks_static.restype = ctypes.c_int
 for _name in ("infllmv2_sparse_attn_decode", "infllmv2_sparse_attn_prefill"):
     getattr(lib, _name).argtypes = [_P, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                     ctypes.c_size_t, _vp]
@@ -92,6 +94,7 @@ lib.infllmv2_get_device_status.restype = ctypes.c_int
 EXPORTED = (
     "infllmv2_default_params", "infllmv2_max_selected", "infllmv2_num_kernels",
     "infllmv2_workspace_size", "infllmv2_compress_keys", "infllmv2_select_blocks",
+    "infllmv2_select_blocks_static",
     "infllmv2_sparse_attn_decode", "infllmv2_sparse_attn_prefill", "infllmv2_status_string",
     "infllmv2_last_error", "infllmv2_get_device_status",
 )

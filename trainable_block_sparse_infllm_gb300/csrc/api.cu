@@ -17,6 +17,13 @@ using namespace infllmv2;
 // Device status word (INFLLMV2_DEVICE_* bits), one per device context.
 static __device__ uint32_t g_device_status;
 
+// Built-in scratch of infllmv2_select_blocks_static: 8 MiB that every device
+// which loads the library keeps until the process exits.  Each call overwrites
+// the part it reads before reading it (nothing has to start at zero); calls
+// that overlap on the GPU share it and race.
+static constexpr size_t kStaticSelectScratchBytes = static_cast<size_t>(8) << 20;
+static __device__ __align__(256) unsigned char g_select_scratch[kStaticSelectScratchBytes];
+
 namespace {
 
 thread_local std::string g_last_error;
@@ -62,6 +69,31 @@ uint32_t* status_ptr() {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
     ptrs[dev] = static_cast<uint32_t*>(p);
+  }
+  return ptrs[dev];
+}
+
+// Device address of the built-in selection scratch on the current device.  The
+// host name of a __device__ array is only a stand-in, so the address is asked
+// of the runtime once per device (on that device's first call) and cached.
+void* static_select_scratch(cudaError_t* err) {
+  static void* ptrs[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *err = (e != cudaSuccess) ? e : cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  if (!ptrs[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_select_scratch);
+    if (e != cudaSuccess) {
+      *err = e;
+      return nullptr;
+    }
+    ptrs[dev] = ptr;
   }
   return ptrs[dev];
 }
@@ -269,6 +301,44 @@ int infllmv2_select_blocks(const infllmv2_params* p, const void* q, int32_t n_q,
     cudaError_t e = launch_select(s, kcm, qm, q, kv_lens, block_idx, n_selected, block_scores, workspace,
                                   status, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "select_blocks");
+    return INFLLMV2_OK;
+  });
+}
+
+int infllmv2_select_blocks_static(const infllmv2_params* p, const void* q, int32_t n_q, const void* kc,
+                                  const int32_t* kv_lens, int32_t* block_idx, int32_t* n_selected,
+                                  float* block_scores, void* stream) {
+  INFLLMV2_GUARD({
+    Shape s;
+    int rc = check_params(p, n_q, &s);
+    if (rc) return rc;
+    if (!q || !kc || !kv_lens || !block_idx || !n_selected)
+      return fail(INFLLMV2_INVALID_ARGUMENT, "a required pointer is NULL");
+    if (!aligned16(q) || !aligned16(kc)) return fail(INFLLMV2_UNSUPPORTED, "q and kc must be 16-byte aligned");
+    const size_t need = select_workspace_bytes(s);
+    if (need > kStaticSelectScratchBytes)
+      return fail(INFLLMV2_WORKSPACE_TOO_SMALL,
+                  "this selection needs %zu bytes of scratch; the built-in scratch holds %zu bytes "
+                  "(use infllmv2_select_blocks with a caller workspace)",
+                  need, kStaticSelectScratchBytes);
+    void* scratch = nullptr;
+    if (need > 0) {
+      cudaError_t se = cudaSuccess;
+      scratch = static_select_scratch(&se);
+      if (!scratch) return cuda_fail(se, "select_blocks_static: address of the built-in scratch");
+    }
+    uint32_t* status = status_ptr();
+    if (!status) return fail(INFLLMV2_CUDA_ERROR, "no device status word (no current CUDA device?)");
+    CUtensorMap kcm, qm;
+    if ((rc = make_map(&qm, q, static_cast<uint64_t>(s.B) * s.nq * s.Hkv * kGroup, 16, "q"))) return rc;
+    if (s.ncmax > 0) {
+      if ((rc = make_map(&kcm, kc, static_cast<uint64_t>(s.B) * s.Hkv * 2 * s.ncmax, 64, "kc"))) return rc;
+    } else {
+      kcm = qm;
+    }
+    cudaError_t e = launch_select(s, kcm, qm, q, kv_lens, block_idx, n_selected, block_scores, scratch, status,
+                                  static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "select_blocks_static");
     return INFLLMV2_OK;
   });
 }
