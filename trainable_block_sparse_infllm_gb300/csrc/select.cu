@@ -73,20 +73,26 @@ __device__ __forceinline__ void load_q_frags(uint32_t (&a)[8][4], uint32_t tile,
 }
 
 // z for one n-tile (8 kernels at tile row n0) of a hi/lo tile with `rows` rows.
+// Four accumulators (hi/lo x even/odd k-step) keep the 16 MMAs in four short
+// dependency chains instead of one long one.
 __device__ __forceinline__ void score_ntile(float (&acc)[4], const uint32_t (&a)[8][4],
                                             uint32_t hi, uint32_t lo, int n0, int rows, int lane) {
-  acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+  float c[4][4];
+#pragma unroll
+  for (int x = 0; x < 4; ++x) c[x][0] = c[x][1] = c[x][2] = c[x][3] = 0.f;
 #pragma unroll
   for (int kk = 0; kk < 4; ++kk) {
     uint32_t bh[4], bl[4];
     const uint32_t off = swz128_offset(n0 + (lane & 7), 4 * kk + (lane >> 3), rows);
     ldmatrix_x4(bh, hi + off);
     ldmatrix_x4(bl, lo + off);
-    mma_bf16_16816(acc, a[2 * kk], bh[0], bh[1]);
-    mma_bf16_16816(acc, a[2 * kk], bl[0], bl[1]);
-    mma_bf16_16816(acc, a[2 * kk + 1], bh[2], bh[3]);
-    mma_bf16_16816(acc, a[2 * kk + 1], bl[2], bl[3]);
+    mma_bf16_16816(c[0], a[2 * kk], bh[0], bh[1]);
+    mma_bf16_16816(c[1], a[2 * kk], bl[0], bl[1]);
+    mma_bf16_16816(c[2], a[2 * kk + 1], bh[2], bh[3]);
+    mma_bf16_16816(c[3], a[2 * kk + 1], bl[2], bl[3]);
   }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) acc[e] = (c[0][e] + c[2][e]) + (c[1][e] + c[3][e]);
 }
 
 // ------------------------------------------------------------- decode path --
@@ -248,12 +254,23 @@ __global__ void __launch_bounds__(kClThreads, 2)
       }
     }
     for (int it = 0; it < min(kClStages, nmy); ++it) issue(it);
+    // The rest of this CTA's chunks go to L2 now, so HBM streams at full
+    // rate while the two shared-memory stages trail behind.
+    for (int it = kClStages; it < nmy; ++it) {
+      const int row = (k0 + it) * kClChunk;
+      tma_prefetch_2d(&kc_map, 0, (bh * 2 + 0) * p.ncmax + row);
+      tma_prefetch_2d(&kc_map, 64, (bh * 2 + 0) * p.ncmax + row);
+      tma_prefetch_2d(&kc_map, 0, (bh * 2 + 1) * p.ncmax + row);
+      tma_prefetch_2d(&kc_map, 64, (bh * 2 + 1) * p.ncmax + row);
+    }
   }
 
   // ------------------------------------------------------------ phase A --
   bool ok = true;
   if (nmy > 0) ok = __syncthreads_and(mbar_wait(qbar, 0, p.status));
   const uint32_t q_b = smem_u32(smem + lay.q);
+  uint32_t a[8][4];
+  if (nq == 1 && nmy > 0) load_q_frags(a, q_b, lane);   // one token: fragments stay in registers
 #pragma unroll 1
   for (int it = 0; it < nmy && ok; ++it) {
     const int st = it % kClStages;
@@ -266,8 +283,7 @@ __global__ void __launch_bounds__(kClThreads, 2)
 #pragma unroll 1
     for (int t = 0; t < nq; ++t) {
       const int nvis = n_complete_kernels(L - nq + t + 1);
-      uint32_t a[8][4];
-      load_q_frags(a, q_b + t * 4096, lane);
+      if (nq > 1) load_q_frags(a, q_b + t * 4096, lane);
       float acc[4];
       score_ntile(acc, a, hi_b, hi_b + 16384, warp * 8, kClChunk, lane);
       const bool v0 = kj < nvis, v1 = kj + 1 < nvis;
@@ -646,7 +662,7 @@ __global__ void __launch_bounds__(kPrefTokens * 32)
     if (active && kbase < nvis_t) {
       const uint32_t hi_b = smem_u32(smem + lay.stage_off + stage * kPrefStageBytes);
       const uint32_t lo_b = hi_b + 16384;
-#pragma unroll 1
+#pragma unroll 2
       for (int nt = 0; nt < 8; ++nt) {
         float acc[4];
         score_ntile(acc, a, hi_b, lo_b, nt * 8, kPrefChunk, lane);
