@@ -171,6 +171,137 @@ __device__ void select_topk(const float* r, uint8_t* flag, int nb, int n_init, i
   if (tid == 0) *out_n = min(total, k_max);
 }
 
+// Top-k over scores held in registers: thread tid holds the scores of blocks
+// j = tid + NT x (x < MAXR) in v[x].  Same selection rule and output as
+// select_topk.  One 256-bin histogram of the scores' leading bits (sign,
+// exponent, 6 mantissa bits, counted down from the best score) locates the
+// bin holding the n_take-th best score; candidates at or above it are
+// ranked exactly by (score desc, index asc).  Every step works on registers
+// with a handful of CTA barriers.  `surv` (shared, nb entries) takes the
+// survivors, so many-way exact ties are handled too; `sel` (shared, k_max
+// entries) collects the chosen blocks.  NT >= 256.
+template <int NT>
+struct RegTopkScratch {
+  uint32_t hist[NT / 32][256];
+  int wred[NT / 32][2];
+  int warp_tot[NT / 32];
+  int ctrl[4];
+};
+
+template <int NT, int MAXR>
+__device__ void select_topk_regs(const float (&v)[MAXR], int nb, int n_init, int n_local, int topk,
+                                 bool includes_forced, int k_max, int32_t* out_idx, int32_t* out_n,
+                                 RegTopkScratch<NT>& sm, unsigned long long* surv_buf, int* sel_buf,
+                                 int tid) {
+  static_assert(NT >= 256, "one thread per histogram bin");
+  constexpr int NWARP = NT / 32;
+  constexpr int kShift = 17;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int c = nb - 1;
+  // 1. candidates, their count and best leading bits.
+  bool cand[MAXR];
+  int my_cand = 0;
+  uint32_t my_top = 0;
+#pragma unroll
+  for (int x = 0; x < MAXR; ++x) {
+    const int j = tid + NT * x;
+    cand[x] = j < nb && j >= n_init && j <= c - n_local && v[x] > -INFINITY;
+    if (cand[x]) {
+      ++my_cand;
+      my_top = max(my_top, float_to_ordered(v[x]) >> kShift);
+    }
+  }
+  for (int b = lane; b < 256; b += 32) sm.hist[warp][b] = 0u;
+  my_cand = __reduce_add_sync(0xffffffffu, my_cand);
+  my_top = __reduce_max_sync(0xffffffffu, my_top);
+  if (lane == 0) {
+    sm.wred[warp][0] = my_cand;
+    sm.wred[warp][1] = static_cast<int>(my_top);
+  }
+  __syncthreads();
+  int n_cand = 0;
+  uint32_t top = 0;
+#pragma unroll
+  for (int w = 0; w < NWARP; ++w) {
+    n_cand += sm.wred[w][0];
+    top = max(top, static_cast<uint32_t>(sm.wred[w][1]));
+  }
+  const int n_first = min(n_init, nb);
+  const int n_forced = n_first + max(0, c - max(n_first, c - n_local + 1) + 1);
+  const int n_take = max(0, includes_forced ? topk - n_forced : topk);
+  // 2. boundary bin (255 = every candidate survives, -1 = none is taken).
+  int bnd = n_take > 0 ? 255 : -1;
+  if (n_take > 0 && n_cand > n_take) {
+#pragma unroll
+    for (int x = 0; x < MAXR; ++x)
+      if (cand[x]) atomicAdd(&sm.hist[warp][min(255u, top - (float_to_ordered(v[x]) >> kShift))], 1u);
+    __syncthreads();
+    int cnt = 0;
+    for (int b = tid; b < 256; b += NT) {
+#pragma unroll
+      for (int w = 0; w < NWARP; ++w) cnt += static_cast<int>(sm.hist[w][b]);
+    }
+    // tid < 256 holds bin tid (NT >= 256); inclusive scan in bin order.
+    const int incl = warp_inclusive_scan(cnt);
+    if (lane == 31) sm.warp_tot[warp] = incl;
+    __syncthreads();
+    int before = 0;
+#pragma unroll
+    for (int w = 0; w < NWARP; ++w) before += (w < warp) ? sm.warp_tot[w] : 0;
+    const int run = before + incl - cnt;
+    if (tid < 256 && run < n_take && run + cnt >= n_take) sm.ctrl[0] = tid;
+    __syncthreads();
+    bnd = sm.ctrl[0];
+  }
+  // 3. survivors (candidates at or above the boundary bin) into shared memory.
+  bool surv[MAXR];
+  int my_surv = 0;
+#pragma unroll
+  for (int x = 0; x < MAXR; ++x) {
+    surv[x] = cand[x] && static_cast<int>(min(255u, top - (float_to_ordered(v[x]) >> kShift))) <= bnd;
+    my_surv += surv[x] ? 1 : 0;
+  }
+  const int incl = warp_inclusive_scan(my_surv);
+  if (lane == 31) sm.warp_tot[warp] = incl;
+  __syncthreads();
+  int pos = incl - my_surv, n_surv = 0;
+#pragma unroll
+  for (int w = 0; w < NWARP; ++w) {
+    pos += (w < warp) ? sm.warp_tot[w] : 0;
+    n_surv += sm.warp_tot[w];
+  }
+#pragma unroll
+  for (int x = 0; x < MAXR; ++x)
+    if (surv[x]) surv_buf[pos++] = (static_cast<unsigned long long>(float_to_ordered(v[x])) << 32) |
+                                   static_cast<uint32_t>(~(tid + NT * x));
+  if (tid == 0) {   // forced blocks first, ascending
+    int n = 0;
+    for (int j = 0; j < n_first; ++j) sel_buf[n++] = j;
+    for (int j = max(n_first, c - n_local + 1); j <= c; ++j) sel_buf[n++] = j;
+  }
+  __syncthreads();
+  // 4. exact rank among survivors; the best n_take follow the forced blocks.
+  for (int x = tid; x < n_surv; x += NT) {
+    const unsigned long long me = surv_buf[x];
+    int rk = 0, y = 0;
+    for (; y + 4 <= n_surv; y += 4)
+      rk += (surv_buf[y] > me) + (surv_buf[y + 1] > me) + (surv_buf[y + 2] > me) + (surv_buf[y + 3] > me);
+    for (; y < n_surv; ++y) rk += (surv_buf[y] > me) ? 1 : 0;
+    if (rk < n_take) sel_buf[n_forced + rk] = static_cast<int>(~static_cast<uint32_t>(me & 0xffffffffu));
+  }
+  __syncthreads();
+  // 5. ascending output.
+  const int n_total = min(k_max, n_forced + min(n_take, n_surv));
+  for (int x = tid; x < n_total; x += NT) {
+    const int val = sel_buf[x];
+    int p = 0;
+    for (int y = 0; y < n_total; ++y) p += (sel_buf[y] < val) ? 1 : 0;
+    out_idx[p] = val;
+  }
+  for (int x = n_total + tid; x < k_max; x += NT) out_idx[x] = -1;
+  if (tid == 0) *out_n = n_total;
+}
+
 // Same contract as select_topk for a whole CTA (NT threads, NT % 32 == 0),
 // built for few barriers and no contended atomics: one 256-bin histogram of
 // the scores' leading bits (sign, exponent, 6 mantissa bits, counted down
