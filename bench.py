@@ -2,10 +2,12 @@
 
 Headline: decode tokens/s at 128K context (batch 4, 32 query / 2 KV heads,
 top-64 blocks).  One step = the whole decode path for one new token per
-sequence: compress_keys for the newest complete kernel, select_blocks
-(scores, LSE, group mean, block max, top-k) and sparse_attn_decode
-(split-KV attention + merge), captured in a CUDA graph.  A prefill line
-(32K causal prefill, 32 query / 2 KV heads) is reported alongside.
+sequence through infllmv2_decode_step: the newest complete kernel mean, block
+selection (scores, LSE, group mean, block max, top-k) and sparse attention
+with its merge, in one cluster launch.  Eight steps over eight input replicas
+form one CUDA graph.  The three separate stages (compress_keys,
+select_blocks, sparse_attn_decode) are timed alone as a breakdown.  A prefill
+line (32K causal prefill, 32 query / 2 KV heads) is reported alongside.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -149,7 +151,8 @@ class DecodeBench:
                    "out": torch.empty_like(q0),
                    "lse": torch.empty((B, nq, wl.n_heads), dtype=torch.float32, device=dev),
                    "ws_sel": T.alloc_workspace(self.p, nq, T.OP_SELECT, dev),
-                   "ws_att": T.alloc_workspace(self.p, nq, T.OP_DECODE, dev)}
+                   "ws_att": T.alloc_workspace(self.p, nq, T.OP_DECODE, dev),
+                   "ws_step": T.alloc_workspace(self.p, nq, T.OP_DECODE_STEP, dev)}
             T.compress_keys(self.p, rep["k"], self.lens, rep["kc"])      # full cache, once
             self.reps.append(rep)
         del q0, k0, v0
@@ -171,22 +174,34 @@ class DecodeBench:
                                   rep["out"], rep["lse"], rep["ws_att"])
 
     def step(self, r):
-        self.compress_newest(r)
-        self.select(r)
-        self.attend(r)
+        """One decode step on replica r: a single fused launch."""
+        rep = self.reps[r]
+        self.T.decode_step(self.p, rep["q"], rep["k"], rep["v"], self.lens, rep["kc"], rep["idx"], rep["nsel"],
+                           rep["out"], rep["lse"], rep["ws_step"])
 
     def capture(self):
         torch = self.torch
         for r in range(REPLICAS):
             self.step(r)                        # warm: module load, attributes, symbols
         torch.cuda.synchronize()
-        self.graphs = []
+        self.graphs = []                        # one step each (end-to-end leg, remainders)
         for r in range(REPLICAS):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 self.step(r)
             self.graphs.append(g)
+        self.round = torch.cuda.CUDAGraph()     # REPLICAS steps back to back
+        with torch.cuda.graph(self.round):
+            for r in range(REPLICAS):
+                self.step(r)
         torch.cuda.synchronize()
+
+    def run_steps(self, n):
+        """n steps: whole rounds of REPLICAS, then single steps."""
+        for _ in range(n // REPLICAS):
+            self.round.replay()
+        for r in range(n % REPLICAS):
+            self.graphs[r].replay()
 
     def time_fn(self, fn, n, warm=3):
         torch = self.torch
@@ -202,7 +217,8 @@ class DecodeBench:
         return e0.elapsed_time(e1) / n * 1e-3     # seconds per call
 
     def algorithmic_bytes(self):
-        """Bytes a decode step must move (SURVEY-style accounting, per launch)."""
+        """Bytes a decode step must move: queries, both kernel-mean planes, the
+        selected K and V tiles, outputs, indices and the newest kernel."""
         wl = self.wl
         B, H, nq, d = wl.batch, wl.n_kv_heads, wl.n_q, wl.head_dim
         n_c = S_n_c(wl.kv_len)
@@ -354,6 +370,52 @@ def reference_arm(args):
     return 0
 
 
+# ---------------------------------------------------------------- profile ---
+
+def profile_passes(path, n):
+    """n passes of one path on a single input copy, nothing timed: the decode
+    path is one decode_step launch per pass (decode_128k, 0.57 GB of inputs);
+    the prefill path is compress + select + attention (prefill_32k)."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import trainable_block_sparse_infllm_gb300 as T
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    wl = S.WORKLOADS[DECODE if path == "decode" else PREFILL]
+    inp = S.make_inputs(wl)
+    p = T.make_params(wl.batch, wl.n_kv_heads, wl.kv_len, wl.topk, wl.topk_includes_forced)
+
+    def up(bits):
+        return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    q, k, v = up(inp.q), up(inp.k), up(inp.v)
+    lens = torch.from_numpy(inp.kv_lens).to(dev)
+    B, H, nq = wl.batch, wl.n_kv_heads, wl.n_q
+    kmax = T.max_selected(p)
+    kc = T.alloc_kc(p, dev)
+    idx = torch.empty((B, H, nq, kmax), dtype=torch.int32, device=dev)
+    nsel = torch.empty((B, H, nq), dtype=torch.int32, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, nq, wl.n_heads), dtype=torch.float32, device=dev)
+    T.compress_keys(p, k, lens, kc)
+    if path == "decode":
+        ws = T.alloc_workspace(p, nq, T.OP_DECODE_STEP, dev)
+        for _ in range(n):
+            T.decode_step(p, q, k, v, lens, kc, idx, nsel, out, lse, ws)
+    else:
+        ws_sel = T.alloc_workspace(p, nq, T.OP_SELECT, dev)
+        ws_att = T.alloc_workspace(p, nq, T.OP_PREFILL, dev)
+        for _ in range(n):
+            T.compress_keys(p, k, lens, kc)
+            T.select_blocks(p, q, kc, lens, idx, nsel, None, ws_sel)
+            T.sparse_attn_prefill(p, q, k, v, lens, idx, nsel, out, lse, ws_att)
+    torch.cuda.synchronize()
+    assert T.get_device_status(clear=True) == 0
+    print(f"profile passes done: {path} x {n}")
+    return 0
+
+
 # ------------------------------------------------------------------- main ---
 
 def main():
@@ -364,7 +426,12 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["decode", "prefill"],
+                    help="run warmup + steps untimed passes of one path on one input copy and exit "
+                         "(a small, fixed launch sequence for ncu)")
     args = ap.parse_args()
+    if args.profile:
+        return profile_passes(args.profile, args.warmup + args.steps)
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
         return reference_arm(args)
@@ -397,9 +464,8 @@ def main():
                "select": bench.time_fn(bench.select, args.steps),
                "attend": bench.time_fn(bench.attend, args.steps)}
 
-    # Timed region: K graph replays of the whole step.
-    for i in range(args.warmup):
-        bench.graphs[i % REPLICAS].replay()
+    # Timed region: exactly K steps (graph replays).
+    bench.run_steps(max(args.warmup, REPLICAS))
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
@@ -409,8 +475,7 @@ def main():
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     w0 = time.perf_counter()
     e0.record()
-    for i in range(args.steps):
-        bench.graphs[i % REPLICAS].replay()
+    bench.run_steps(args.steps)
     e1.record()
     torch.cuda.synchronize()
     wall = time.perf_counter() - w0
@@ -471,10 +536,10 @@ def main():
         return 0
 
     ab = bench.algorithmic_bytes()
-    dom = max(stage_t, key=stage_t.get)
-    dom_kernel = {"compress": "compress_kernel", "select": "sel_score_kernel + sel_reduce_kernel",
-                  "attend": "attn_kernel"}[dom]
-    achieved = ab[dom] / stage_t[dom] / 1e9
+    # The step is one launch of decode_step_kernel: its average duration is
+    # the timed region over K.
+    t_launch = t / args.steps
+    achieved = ab["step"] / t_launch / 1e9
     value = world * tokens_per_step * args.steps / t
     line = {
         "metric": METRIC,
@@ -493,16 +558,15 @@ def main():
                                f"KV cache, block 64, kernel 32/16, top-64 incl. block 0 + 2 local, 1 query/seq",
                    "global_batch": world * wl.batch, "seq_len": wl.kv_len, "parallelism": f"dp{world}",
                    "l2": f"{REPLICAS} rotating input replicas ({REPLICAS * 0.57:.1f} GB) > L2",
-                   "graph": "one CUDA graph per step: compress(newest) + select + attention"},
+                   "graph": f"decode_step (newest kernel + select + attention, one launch per step), "
+                            f"{REPLICAS} steps per CUDA graph"},
         "clocks": clk,
-        "gpu_launches": 4 * args.steps,
-        "stage_ms": {k_: v_ * 1e3 for k_, v_ in stage_t.items()},
-        "roofline": {"kernel": dom_kernel, "bound": "hbm", "achieved": achieved, "peak": peaks[0],
+        "gpu_launches": args.steps,
+        "unfused_stage_ms": {k_: v_ * 1e3 for k_, v_ in stage_t.items()},
+        "roofline": {"kernel": "decode_step_kernel", "bound": "hbm", "achieved": achieved, "peak": peaks[0],
                      "unit": "GB/s", "frac": achieved / peaks[0], "peak_kind": peaks[3],
-                     "algorithmic_bytes_per_launch": ab[dom], "traffic": _traffic(dom_kernel, DECODE)},
-        "step_roofline": {"achieved": ab["step"] / (t / args.steps) / 1e9, "unit": "GB/s",
-                          "frac": ab["step"] / (t / args.steps) / 1e9 / peaks[0],
-                          "algorithmic_bytes_per_step": ab["step"]},
+                     "algorithmic_bytes_per_launch": ab["step"],
+                     "traffic": _traffic("decode_step_kernel", DECODE)},
         "e2e": {"value": world * tokens_per_step * args.steps / t_e2e, "unit": "tokens/s",
                 "h2d_bytes_per_step": int(q_h[0].numel() * 2 + kv_h[0].numel() * 2),
                 "d2h_bytes_per_step": int(out_h[0].numel() * 2), "wall_s": wall},

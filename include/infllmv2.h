@@ -78,6 +78,7 @@ extern "C" {
 #define INFLLMV2_OP_SELECT  1
 #define INFLLMV2_OP_DECODE  2
 #define INFLLMV2_OP_PREFILL 3
+#define INFLLMV2_OP_DECODE_STEP 4
 
 typedef struct infllmv2_params {
   int32_t batch;                 /* B */
@@ -187,6 +188,31 @@ int infllmv2_sparse_attn_prefill(const infllmv2_params* p, const void* q, int32_
                                  const void* k_cache, const void* v_cache, const int32_t* kv_lens,
                                  const int32_t* block_idx, const int32_t* n_selected, void* out,
                                  float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * One whole decode step: stages 1-3 for the newest n_q tokens of each
+ * sequence, whose keys and values the caller has already written to the
+ * caches (kv_lens counts them) [InfLLM v2 > Semantic kernels, eq. S_j;
+ * > Top-K implementation and the LSE bottleneck; > Block-level key-value
+ * partitioning; > Complexity analysis, stage 2].
+ *   kc      in/out: every kernel mean that ends before the step's tokens must
+ *           be present; the kernels that end inside them (for n_q = 1: the
+ *           newest complete kernel n_c(L) - 1) are recomputed from k_cache
+ *           and written back.
+ *   block_idx, n_selected, out, lse: as from infllmv2_select_blocks followed
+ *           by infllmv2_sparse_attn_decode (lse nullable).
+ *   n_q in [1, 16].  With n_q = 1 and a cache of at most 128 * 16 blocks
+ *   (131072 tokens; 65536 where only 8-CTA clusters fit) the step is one
+ *   launch of a thread-block cluster per (b, h_kv) that keeps every
+ *   intermediate on chip and needs no workspace; otherwise it enqueues the
+ *   three stages in order.  Workspace: infllmv2_workspace_size(p, n_q,
+ *   INFLLMV2_OP_DECODE_STEP) bytes (0 for the single-launch form; workspace
+ *   may then be NULL).
+ */
+int infllmv2_decode_step(const infllmv2_params* p, const void* q, int32_t n_q, const void* k_cache,
+                         const void* v_cache, const int32_t* kv_lens, void* kc, int32_t* block_idx,
+                         int32_t* n_selected, void* out, float* lse, void* workspace,
+                         size_t workspace_bytes, void* stream);
 
 /* Human-readable name of an INFLLMV2_* return code. */
 const char* infllmv2_status_string(int status);

@@ -14,7 +14,7 @@ abbreviated below as [InfLLM v2 › <paragraph>, <equation>].
 Every step is written the slow, obvious way, in float64, in the order the
 section gives it: kernel means -> per-head kernel softmax -> group mean ->
 block max -> forced blocks -> top-k -> exact softmax attention over the chosen
-blocks.  Readings of points the pages leave open (all listed in the design doc):
+blocks.  Readings of points the pages leave open:
 
 * R1  the kernel softmax is taken over ``score_scale * q . Mean(K)``; the
       section prints no scale, so the scale is a parameter (default 1/sqrt(d),

@@ -81,6 +81,31 @@ class GpuRun:
         fn = self.T.sparse_attn_prefill if prefill else self.T.sparse_attn_decode
         fn(self.p, self.q, self.k, self.v, self.lens, idx, nsel, self.out, self.lse, ws)
 
+    def step(self):
+        """The fused decode step (newest kernel + selection + attention)."""
+        ws = self.T.alloc_workspace(self.p, self.nq, self.T.OP_DECODE_STEP, self.dev)
+        self.T.decode_step(self.p, self.q, self.k, self.v, self.lens, self.kc, self.idx, self.nsel,
+                           self.out, self.lse, ws)
+
+    def blank_step_kernels(self):
+        """Compress everything, then NaN the kernel means a decode step must
+        recompute (those ending inside the last n_q tokens).  Returns the full
+        kernel-mean buffer for comparison."""
+        import torch
+        from oracle import n_complete_kernels
+        self.compress()
+        full = self.kc.clone()
+        for b, L in enumerate(self.inp.kv_lens):
+            lo = n_complete_kernels(max(int(L) - self.nq, 0), 32, 16)
+            hi = n_complete_kernels(int(L), 32, 16)
+            if hi > lo:
+                self.kc[b, :, :, lo:hi].view(torch.int16).fill_(0x7FC0)
+        return full
+
+    def gpu_blocks(self, units):
+        idx, nsel = self.idx.cpu().numpy(), self.nsel.cpu().numpy()
+        return {(b, h, t): idx[b, h, t, :nsel[b, h, t]].copy() for (b, h, t) in units}
+
     def upload_selection(self, sels):
         """Oracle selections {(b,h,t): Selection} -> device idx/nsel tensors."""
         import torch

@@ -205,6 +205,75 @@ def test_bad_kv_len_sets_device_status(dev):
     assert run.out[1].float().eq(0).all().item()
 
 
+# ------------------------------------------------------ fused decode step ----
+
+STEP_CASES = [
+    # batch, hkv, cap, lens, n_q, topk, includes_forced
+    (2, 2, 5000, [5000, 3333], 1, 16, True),
+    (1, 2, 9000, [9000], 1, 64, True),
+    (3, 1, 4200, [4192, 4177, 4100], 1, 16, True),    # 4192 completes a kernel
+    (2, 2, 20000, [20000, 17], 1, 32, False),          # second sequence has no kernel
+    (3, 1, 300, [300, 40, 33], 1, 4, True),
+    (2, 1, 200, [64, 1], 1, 3, True),                  # a one-token sequence
+    (1, 2, 6000, [6000], 8, 24, True),                 # n_q > 1: the three stages in order
+]
+
+
+@pytest.mark.parametrize("case", STEP_CASES, ids=[f"step{i}" for i in range(len(STEP_CASES))])
+def test_decode_step_parity(dev, case):
+    import torch
+    B, H, cap, lens, nq, topk, inc = case
+    inp = S.make_random(batch=B, n_kv_heads=H, kv_len=cap, n_q=nq, topk=topk, includes_forced=inc,
+                        seed=300 + sum(lens) + nq, kv_lens=lens)
+    st = _settings(inp.wl)
+    run = GpuRun(inp, dev)
+    full = run.blank_step_kernels()
+    run.step()
+    torch.cuda.synchronize()
+    # The recomputed kernel means are bit-identical to the compression kernel's.
+    assert torch.equal(run.kc.view(torch.int16), full.view(torch.int16))
+    sels = O.run_selection(inp, st)
+    check_selections(run, sels, check_scores=False)
+    refs = O.run_attention(inp, st, run.gpu_blocks(sels.keys()))
+    check_attention(run, refs)
+
+
+def test_decode_step_matches_separate_stages(dev):
+    # Same inputs through the single launch and through the three entry
+    # points: identical selections (no tie-band case here) and outputs equal
+    # to rounding.
+    import torch
+    inp = S.make_random(batch=2, n_kv_heads=2, kv_len=30000, n_q=1, topk=48, seed=41, kv_lens=[30000, 12345])
+    run = GpuRun(inp, dev)
+    run.compress()
+    run.select(with_scores=False)
+    run.attend()
+    idx_a, out_a, lse_a = run.idx.clone(), run.out.float().clone(), run.lse.clone()
+    run.idx.fill_(-7)
+    run.out.fill_(float("nan"))
+    run.step()
+    torch.cuda.synchronize()
+    assert torch.equal(idx_a, run.idx)
+    assert (out_a - run.out.float()).abs().max().item() <= 2e-3
+    assert (lse_a - run.lse).abs().max().item() <= 1e-3
+
+
+def test_decode_step_bad_kv_len(dev):
+    import torch
+    import trainable_block_sparse_infllm_gb300 as T
+    inp = S.make_random(batch=2, n_kv_heads=1, kv_len=1000, n_q=1, topk=4, seed=3, kv_lens=[1000, 900])
+    run = GpuRun(inp, dev)
+    run.compress()
+    run.lens[1] = 1001                      # beyond max_kv_len
+    run.step()
+    torch.cuda.synchronize()
+    assert T.get_device_status(clear=True) & T.DEVICE_BAD_KV_LEN
+    assert run.nsel[1].eq(0).all().item()
+    assert run.idx[1].eq(-1).all().item()
+    assert run.out[1].float().eq(0).all().item()
+    assert run.nsel[0].eq(4).all().item()
+
+
 # --------------------------------------------------------- full workloads ----
 
 def _workload_units(wl, rng, n_sample):
@@ -248,6 +317,22 @@ def test_workload_parity(dev, name):
         refs = {u: v for u, v in refs.items() if u[2] >= 1024}
     mx, mean = check_attention(run, refs, strict=True)
     print(f"{name}: units={len(units)} tie-band differences={ties} max|dO|={mx:.2e} mean={mean:.2e}")
+    if wl.n_q == 1:
+        # The fused decode step on the same inputs, in the benchmark's launch
+        # configuration: kernel means, selection and attention in one launch.
+        full = run.blank_step_kernels()
+        run.idx.fill_(-7)
+        run.out.fill_(float("nan"))
+        run.step()
+        torch.cuda.synchronize()
+        assert torch.equal(run.kc.view(torch.int16), full.view(torch.int16))
+        ties = check_selections(run, sels, check_scores=False)
+        got = run.gpu_blocks(units)
+        same = {u for u in units if np.array_equal(got[u], sels[u].blocks)}
+        refs = {u: refs[u] for u in same}
+        refs.update(O.run_attention(inp, st, got, units=[u for u in units if u not in same]))
+        mx, mean = check_attention(run, refs, strict=True)
+        print(f"{name} fused step: tie-band differences={ties} max|dO|={mx:.2e} mean={mean:.2e}")
 
 
 def test_select_exact_ties_break_to_lower_block(dev):

@@ -9,6 +9,7 @@ memory and streams.  Entry points mirror the C names:
     select_blocks        stage 2, block relevance and top-k
     sparse_attn_decode   stage 3 for decode / speculative verification
     sparse_attn_prefill  stage 3 for prefill
+    decode_step          stages 1-3 for the newest token(s), one launch when n_q = 1
 
 Method: "MiniCPM4: Ultra-Efficient LLMs on End Devices", section "InfLLM v2:
 Trainable Sparse Attention for Both Prefilling and Decoding".
@@ -22,14 +23,14 @@ import math
 import torch
 
 from . import _lib
-from ._lib import (InfLLMv2Error, OP_DECODE, OP_PREFILL, OP_SELECT, Params,  # noqa: F401
+from ._lib import (InfLLMv2Error, OP_DECODE, OP_DECODE_STEP, OP_PREFILL, OP_SELECT, Params,  # noqa: F401
                    DEVICE_BAD_KV_LEN, DEVICE_TIMEOUT)
 
 __all__ = [
     "Params", "InfLLMv2Error", "make_params", "num_kernels", "max_selected", "workspace_size",
     "alloc_kc", "alloc_workspace", "compress_keys", "select_blocks", "sparse_attn_decode",
-    "sparse_attn_prefill", "get_device_status", "OP_SELECT", "OP_DECODE", "OP_PREFILL",
-    "DECODE_MAX_NQ",
+    "sparse_attn_prefill", "decode_step", "get_device_status", "OP_SELECT", "OP_DECODE", "OP_PREFILL",
+    "OP_DECODE_STEP", "DECODE_MAX_NQ",
 ]
 
 DECODE_MAX_NQ = 16
@@ -146,6 +147,20 @@ def sparse_attn_prefill(p: Params, q, k_cache, v_cache, kv_lens, block_idx, n_se
                         lse=None, workspace=None, stream=None):
     return _attn(_lib.lib.infllmv2_sparse_attn_prefill, p, q, k_cache, v_cache, kv_lens, block_idx,
                  n_selected, out, lse, workspace, stream)
+
+
+def decode_step(p: Params, q, k_cache, v_cache, kv_lens, kc, block_idx, n_selected, out,
+                lse=None, workspace=None, stream=None):
+    """Newest kernel mean(s), selection and attention for the last n_q tokens.
+
+    ``kc`` must hold every kernel that ends before those tokens; the ones that
+    end inside them are recomputed and written back."""
+    n_q = q.shape[1]
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    _lib.check(_lib.lib.infllmv2_decode_step(ctypes.byref(p), _ptr(q), n_q, _ptr(k_cache), _ptr(v_cache),
+                                             _ptr(kv_lens), _ptr(kc), _ptr(block_idx), _ptr(n_selected),
+                                             _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream)))
+    return block_idx, n_selected, out, lse
 
 
 def get_device_status(clear: bool = True) -> int:

@@ -24,6 +24,7 @@ DEVICE_TIMEOUT = 0x2
 OP_SELECT = 1
 OP_DECODE = 2
 OP_PREFILL = 3
+OP_DECODE_STEP = 4
 
 
 class InfLLMv2Error(RuntimeError):
@@ -84,6 +85,9 @@ for _name in ("infllmv2_sparse_attn_decode", "infllmv2_sparse_attn_prefill"):
     getattr(lib, _name).argtypes = [_P, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                     ctypes.c_size_t, _vp]
     getattr(lib, _name).restype = ctypes.c_int
+lib.infllmv2_decode_step.argtypes = [_P, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                     ctypes.c_size_t, _vp]
+lib.infllmv2_decode_step.restype = ctypes.c_int
 lib.infllmv2_status_string.argtypes = [ctypes.c_int]
 lib.infllmv2_status_string.restype = ctypes.c_char_p
 lib.infllmv2_last_error.argtypes = []
@@ -95,7 +99,8 @@ EXPORTED = (
     "infllmv2_default_params", "infllmv2_max_selected", "infllmv2_num_kernels",
     "infllmv2_workspace_size", "infllmv2_compress_keys", "infllmv2_select_blocks",
     "infllmv2_select_blocks_static",
-    "infllmv2_sparse_attn_decode", "infllmv2_sparse_attn_prefill", "infllmv2_status_string",
+    "infllmv2_sparse_attn_decode", "infllmv2_sparse_attn_prefill", "infllmv2_decode_step",
+    "infllmv2_status_string",
     "infllmv2_last_error", "infllmv2_get_device_status",
 )
 

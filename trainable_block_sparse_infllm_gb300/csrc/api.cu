@@ -171,6 +171,8 @@ size_t workspace_for(const Shape& s, int op) {
       return attn_workspace_bytes(s, false);
     case INFLLMV2_OP_PREFILL:
       return attn_workspace_bytes(s, true);
+    case INFLLMV2_OP_DECODE_STEP:
+      return decode_step_cluster_size(s) ? 0 : select_workspace_bytes(s) + attn_workspace_bytes(s, false);
     default:
       return 0;
   }
@@ -253,7 +255,7 @@ int32_t infllmv2_num_kernels(const infllmv2_params* p) {
 size_t infllmv2_workspace_size(const infllmv2_params* p, int32_t n_q, int32_t op) {
   Shape s;
   if (check_params(p, n_q, &s)) return 0;
-  if (op == INFLLMV2_OP_DECODE && n_q > kSelDecodeMaxNq) return 0;
+  if ((op == INFLLMV2_OP_DECODE || op == INFLLMV2_OP_DECODE_STEP) && n_q > kSelDecodeMaxNq) return 0;
   return workspace_for(s, op);
 }
 
@@ -357,6 +359,55 @@ int infllmv2_sparse_attn_prefill(const infllmv2_params* p, const void* q, int32_
                                  size_t workspace_bytes, void* stream) {
   INFLLMV2_GUARD(return attn_entry(p, q, n_q, k_cache, v_cache, kv_lens, block_idx, n_selected, out, lse,
                                    workspace, workspace_bytes, stream, true));
+}
+
+int infllmv2_decode_step(const infllmv2_params* p, const void* q, int32_t n_q, const void* k_cache,
+                         const void* v_cache, const int32_t* kv_lens, void* kc, int32_t* block_idx,
+                         int32_t* n_selected, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  INFLLMV2_GUARD({
+    Shape s;
+    int rc = check_params(p, n_q, &s);
+    if (rc) return rc;
+    if (!q || !k_cache || !v_cache || !kv_lens || !kc || !block_idx || !n_selected || !out)
+      return fail(INFLLMV2_INVALID_ARGUMENT, "a required pointer is NULL");
+    if (n_q > kSelDecodeMaxNq)
+      return fail(INFLLMV2_INVALID_ARGUMENT, "decode_step takes n_q <= %d (got %d)", kSelDecodeMaxNq, n_q);
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(kc) || !aligned16(out))
+      return fail(INFLLMV2_UNSUPPORTED, "q, k_cache, v_cache, kc and out must be 16-byte aligned");
+    if (s.ncmax < 1) return fail(INFLLMV2_UNSUPPORTED, "max_kv_len must hold at least one semantic kernel");
+    const int cluster = decode_step_cluster_size(s);
+    const size_t need = cluster ? 0 : select_workspace_bytes(s) + attn_workspace_bytes(s, false);
+    if (need > 0 && (!workspace || workspace_bytes < need))
+      return fail(INFLLMV2_WORKSPACE_TOO_SMALL, "workspace needs %zu bytes (got %zu)", need, workspace_bytes);
+    if (need > 0 && !aligned16(workspace)) return fail(INFLLMV2_UNSUPPORTED, "workspace must be 16-byte aligned");
+    uint32_t* status = status_ptr();
+    if (!status) return fail(INFLLMV2_CUDA_ERROR, "no device status word (no current CUDA device?)");
+    CUtensorMap qm, kcm, km, vm;
+    const uint64_t kv_rows = static_cast<uint64_t>(s.B) * s.Hkv * s.Lmax;
+    if ((rc = make_map(&qm, q, static_cast<uint64_t>(s.B) * s.nq * s.Hkv * kGroup, 16, "q"))) return rc;
+    if ((rc = make_map(&kcm, kc, static_cast<uint64_t>(s.B) * s.Hkv * 2 * s.ncmax, 64, "kc"))) return rc;
+    if ((rc = make_map(&km, k_cache, kv_rows, 64, "k_cache"))) return rc;
+    if ((rc = make_map(&vm, v_cache, kv_rows, 64, "v_cache"))) return rc;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (cluster) {
+      e = launch_decode_step(s, cluster, kcm, qm, km, vm, k_cache, kv_lens, kc, block_idx, n_selected, out, lse,
+                             status, st);
+      if (e != cudaSuccess) return cuda_fail(e, "decode_step");
+      return INFLLMV2_OK;
+    }
+    // Kernels ending inside the last n_q tokens: at most n_q / 16 + 1 of them.
+    e = launch_compress(s, k_cache, kv_lens, -(n_q / kStride + 1), -1, kc, status, st);
+    if (e != cudaSuccess) return cuda_fail(e, "decode_step (compress)");
+    const size_t sel_ws = select_workspace_bytes(s);
+    e = launch_select(s, kcm, qm, q, kv_lens, block_idx, n_selected, nullptr, workspace, status, st);
+    if (e != cudaSuccess) return cuda_fail(e, "decode_step (select)");
+    e = launch_attn(s, false, qm, km, vm, kv_lens, block_idx, n_selected, out, lse,
+                    static_cast<unsigned char*>(workspace) + sel_ws, status, st);
+    if (e != cudaSuccess) return cuda_fail(e, "decode_step (attend)");
+    return INFLLMV2_OK;
+  });
 }
 
 const char* infllmv2_status_string(int status) {

@@ -10,7 +10,7 @@
 // planes, hi = bf16(mean) and lo = bf16(mean - hi), so that the selection
 // stage can feed both straight to the tensor cores.  HBM-bound: one read of
 // the keys, one write of 512 bytes per kernel.
-#include "common.cuh"
+#include "compress.cuh"
 #include "kernels.h"
 
 namespace infllmv2 {
@@ -19,15 +19,6 @@ namespace {
 
 constexpr int kKernelsPerCta = 32;
 constexpr int kThreads = 256;
-
-__device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4& w) {
-  const uint32_t v[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    acc[2 * i] += __uint_as_float(v[i] << 16);
-    acc[2 * i + 1] += __uint_as_float(v[i] & 0xffff0000u);
-  }
-}
 
 __global__ void __launch_bounds__(kThreads)
     compress_kernel(const __nv_bfloat16* __restrict__ k, const int32_t* __restrict__ kv_lens,
@@ -54,17 +45,8 @@ __global__ void __launch_bounds__(kThreads)
   const int nchunk = j1 - j0 + 1;  // chunks j0 .. j1 of 16 keys
   const int sub = threadIdx.x & 15;
   for (int cc = threadIdx.x >> 4; cc < nchunk; cc += kThreads / 16) {
-    const int tok0 = (j0 + cc) * kStride;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      uint4 w[kStride / 2];   // eight loads in flight before the first add
-#pragma unroll
-      for (int t = 0; t < kStride / 2; ++t)
-        w[t] = __ldg(reinterpret_cast<const uint4*>(kbh + static_cast<size_t>(tok0 + half * 8 + t) * kHeadDim) + sub);
-#pragma unroll
-      for (int t = 0; t < kStride / 2; ++t) add_bf16x8(acc, w[t]);
-    }
+    float acc[8];
+    chunk_sum16(acc, kbh, (j0 + cc) * kStride, sub);
     float4* dst = reinterpret_cast<float4*>(&csum[cc][sub * 8]);
     dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
     dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
@@ -77,17 +59,9 @@ __global__ void __launch_bounds__(kThreads)
     const int jj = idx >> 5, q4 = idx & 31;
     const float4 a = *reinterpret_cast<const float4*>(&csum[jj][q4 * 4]);
     const float4 c = *reinterpret_cast<const float4*>(&csum[jj + 1][q4 * 4]);
-    const float m[4] = {(a.x + c.x) * (1.0f / kKernel), (a.y + c.y) * (1.0f / kKernel),
-                        (a.z + c.z) * (1.0f / kKernel), (a.w + c.w) * (1.0f / kKernel)};
     uint32_t hw[2], lw[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const __nv_bfloat162 hv = __floats2bfloat162_rn(m[2 * e], m[2 * e + 1]);
-      const float h0 = __bfloat162float(hv.x), h1 = __bfloat162float(hv.y);
-      const __nv_bfloat162 lv = __floats2bfloat162_rn(m[2 * e] - h0, m[2 * e + 1] - h1);
-      hw[e] = *reinterpret_cast<const uint32_t*>(&hv);
-      lw[e] = *reinterpret_cast<const uint32_t*>(&lv);
-    }
+    kernel_mean_hilo(a.x, a.y, c.x, c.y, hw[0], lw[0]);
+    kernel_mean_hilo(a.z, a.w, c.z, c.w, hw[1], lw[1]);
     const size_t off = static_cast<size_t>(j0 + jj) * kHeadDim + q4 * 4;
     *reinterpret_cast<uint2*>(hi_plane + off) = make_uint2(hw[0], hw[1]);
     *reinterpret_cast<uint2*>(lo_plane + off) = make_uint2(lw[0], lw[1]);

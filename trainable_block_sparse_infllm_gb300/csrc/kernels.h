@@ -23,8 +23,6 @@ cudaError_t launch_compress(const Shape& s, const void* k, const int32_t* kv_len
                             int kend, void* kc, uint32_t* status, cudaStream_t st);
 
 // ---- stage 2 ---------------------------------------------------------------
-constexpr int kSelChunk = 128;        // kernels per scoring CTA (decode path)
-constexpr int kSelReduceBlocks = 64;  // blocks per reduction CTA (decode path)
 constexpr int kSelDecodeMaxNq = 16;   // n_q at or below this uses the decode path
 
 size_t select_workspace_bytes(const Shape& s);
@@ -45,5 +43,14 @@ cudaError_t launch_attn_tc(const Shape& s, const CUtensorMap& q_map, const CUten
                            const CUtensorMap& v_map, const int32_t* kv_lens, const int32_t* block_idx,
                            const int32_t* n_sel, void* out, float* lse, uint32_t* status,
                            cudaStream_t st);
+
+// ---- fused decode step (n_q = 1): newest kernel + selection + attention ----
+// Cluster size of the single-launch form on the current device (16 or 8),
+// or 0 when it does not apply to this shape.
+int decode_step_cluster_size(const Shape& s);
+cudaError_t launch_decode_step(const Shape& s, int cluster, const CUtensorMap& kc_map, const CUtensorMap& q_map,
+                               const CUtensorMap& k_map, const CUtensorMap& v_map, const void* k,
+                               const int32_t* kv_lens, void* kc, int32_t* block_idx, int32_t* n_sel, void* out,
+                               float* lse, uint32_t* status, cudaStream_t st);
 
 }  // namespace infllmv2

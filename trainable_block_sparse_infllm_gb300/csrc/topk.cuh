@@ -179,7 +179,8 @@ __device__ void select_topk(const float* r, uint8_t* flag, int nb, int n_init, i
 // ranked exactly by (score desc, index asc).  Every step works on registers
 // with a handful of CTA barriers.  `surv` (shared, nb entries) takes the
 // survivors, so many-way exact ties are handled too; `sel` (shared, k_max
-// entries) collects the chosen blocks.  NT >= 256.
+// entries) collects the chosen blocks; `sorted_copy` (optional, k_max
+// entries) receives the ascending output list too, padded with -1.  NT >= 256.
 template <int NT>
 struct RegTopkScratch {
   uint32_t hist[NT / 32][256];
@@ -192,7 +193,7 @@ template <int NT, int MAXR>
 __device__ void select_topk_regs(const float (&v)[MAXR], int nb, int n_init, int n_local, int topk,
                                  bool includes_forced, int k_max, int32_t* out_idx, int32_t* out_n,
                                  RegTopkScratch<NT>& sm, unsigned long long* surv_buf, int* sel_buf,
-                                 int tid) {
+                                 int tid, int32_t* sorted_copy = nullptr) {
   static_assert(NT >= 256, "one thread per histogram bin");
   constexpr int NWARP = NT / 32;
   constexpr int kShift = 17;
@@ -297,8 +298,12 @@ __device__ void select_topk_regs(const float (&v)[MAXR], int nb, int n_init, int
     int p = 0;
     for (int y = 0; y < n_total; ++y) p += (sel_buf[y] < val) ? 1 : 0;
     out_idx[p] = val;
+    if (sorted_copy) sorted_copy[p] = val;
   }
-  for (int x = n_total + tid; x < k_max; x += NT) out_idx[x] = -1;
+  for (int x = n_total + tid; x < k_max; x += NT) {
+    out_idx[x] = -1;
+    if (sorted_copy) sorted_copy[x] = -1;
+  }
   if (tid == 0) *out_n = n_total;
 }
 
