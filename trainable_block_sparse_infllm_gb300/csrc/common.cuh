@@ -193,6 +193,16 @@ __device__ __forceinline__ float2 ld_dsmem_f32x2(uint32_t addr) {
   return v;
 }
 
+// Remote stores: fire-and-forget; a following cluster_sync (release/acquire)
+// makes them visible to the owning CTA.
+__device__ __forceinline__ void st_dsmem_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_dsmem_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 // ------------------------------------------- programmatic dependent launch --
 
 // Block until the preceding kernel in the stream has completed and its memory

@@ -23,9 +23,10 @@
 //             memory -> exact lse per head.
 //   phase B   g = (1/16) sum_h exp2(z - lse_h) from the stored exponentials
 //             and one weight per (warp, head); block maxima of the CTA's
-//             blocks.  The kernel 64k - 1 shared with the previous CTA is
-//             merged in when CTA 0 gathers the block scores.
-//   top-k     CTA 0 holds all block scores in registers and selects.
+//             blocks, pushed to the group's owner CTA.  The kernel 64k - 1
+//             shared with the previous CTA is merged in by the owner.
+//   top-k     the owner holds all block scores in registers, selects
+//             (bitmask top-k) and pushes the list to every CTA.
 //   attend    the selected blocks are dealt round-robin to three warp pairs
 //             per CTA; a pair TMA-loads one block's K and V tiles (32 KB) and
 //             each warp of the pair takes 32 of its keys: S = Q K^T on the
@@ -46,8 +47,9 @@ constexpr int kDsStages = 2;          // phase-A stages
 constexpr int kDsMaxIt = 8;           // chunks per CTA (their z live in registers)
 constexpr int kDsPairs = 3;           // attention warp pairs, one 32 KB stage each
 constexpr int kDsStageBytes = 32768;  // 64 kernels hi + lo, or one block's K + V
-constexpr int kDsMaxR = 16;           // block scores per thread in the top-k
 constexpr int kDsCtaOOff = 16384;     // CTA partial O: stage 0's V half
+constexpr int kDsZOff = 2 * 32768;    // phase-A scores: the stage slot phase A leaves free
+static_assert(kDsMaxIt * kGroup * kDsChunk * 4 <= 32768, "phase-A scores fit one stage slot");
 
 struct DsParams {
   int B, Hkv, Lmax, ncmax, nbmax, kmax;
@@ -64,27 +66,31 @@ struct DsParams {
 };
 
 struct DsLayout {
-  int surv, selbuf, q, wpart, cpart, lse, gbuf, rsl, glast, sel, cta_ml, warp_ml, wgt, bar, total;
+  int bits, surv, rfull, glall, q, wpart, cpart, lse, gbuf, wtab, sel, cta_ml, warp_ml, wgt, items, bar, total;
 };
 
-// The stage area (kDsPairs x 32 KB) holds, in turn: the phase-A chunks, CTA
-// 0's top-k scratch, the attention K/V tiles, the per-warp O partials.
+// The stage area (kDsPairs x 32 KB) holds, in turn: the phase-A chunks; in
+// the owner CTA the gathered block scores and the top-k scratch (other CTAs
+// write the scores there only after every CTA's phase A); the attention K/V
+// tiles; the per-warp O partials.
 __host__ __device__ inline DsLayout ds_layout(int nbmax, int kmax) {
   DsLayout l;
-  l.surv = (static_cast<int>(sizeof(RegTopkScratch<kDsThreads>)) + 15) & ~15;
-  l.selbuf = l.surv + nbmax * 8;
+  l.bits = (static_cast<int>(sizeof(SmemTopkScratch<kDsThreads>)) + 15) & ~15;
+  l.surv = (l.bits + (nbmax + 31) / 32 * 4 + 15) & ~15;
+  l.rfull = l.surv + nbmax * 8;
+  l.glall = l.rfull + nbmax * 4;
   l.q = kDsPairs * kDsStageBytes;
   l.wpart = l.q + 4096;
   l.cpart = l.wpart + 8 * kGroup * 8;
   l.lse = l.cpart + kGroup * 8;
   l.gbuf = l.lse + kGroup * 4;
-  l.rsl = l.gbuf + kDsMaxIt * kDsChunk * 4;
-  l.glast = l.rsl + kDsMaxIt * 16 * 4;
-  l.sel = l.glast + 16;
+  l.wtab = l.gbuf + kDsMaxIt * kDsChunk * 4;
+  l.sel = l.wtab + 8 * kGroup * 4;
   l.cta_ml = (l.sel + kmax * 4 + 15) & ~15;
   l.warp_ml = l.cta_ml + kGroup * 8;
   l.wgt = l.warp_ml + 2 * kDsPairs * kGroup * 8;
-  l.bar = (l.wgt + 2 * kDsPairs * kGroup * 4 + 15) & ~15;
+  l.items = l.wgt + 2 * kDsPairs * kGroup * 4;   // item counter + two mailbox slots per pair
+  l.bar = (l.items + (1 + 2 * kDsPairs) * 4 + 15) & ~15;
   l.total = l.bar + (2 * kDsStages + 1 + kDsPairs) * 8;
   return l;
 }
@@ -94,6 +100,14 @@ __host__ __device__ inline int ds_per(int groups, int C) { return (groups + C - 
 // Barrier of the two warps of attention pair `pair` (ids 1..3; 0 is __syncthreads).
 __device__ __forceinline__ void pair_sync(int pair) {
   asm volatile("bar.sync %0, 64;" ::"r"(pair + 1) : "memory");
+}
+
+// K and V tiles of one block into L2 (no shared memory, no completion).
+__device__ __forceinline__ void prefetch_block(const CUtensorMap* kmap, const CUtensorMap* vmap, int row) {
+  tma_prefetch_2d(kmap, 0, row);
+  tma_prefetch_2d(kmap, 64, row);
+  tma_prefetch_2d(vmap, 0, row);
+  tma_prefetch_2d(vmap, 64, row);
 }
 
 __device__ __forceinline__ void tma_block(uint8_t* stage, const CUtensorMap* kmap, const CUtensorMap* vmap,
@@ -117,8 +131,11 @@ __global__ void __launch_bounds__(kDsThreads, 2)
   float2* cpart = reinterpret_cast<float2*>(smem + lay.cpart);   // [16]
   float* lse2 = reinterpret_cast<float*>(smem + lay.lse);        // [16]
   float* gbuf = reinterpret_cast<float*>(smem + lay.gbuf);       // [kDsMaxIt * 64]
-  float* rsl = reinterpret_cast<float*>(smem + lay.rsl);         // [kDsMaxIt * 16]
-  float* glast = reinterpret_cast<float*>(smem + lay.glast);
+  float* wtab = reinterpret_cast<float*>(smem + lay.wtab);       // [8 warps][16 heads] exponential weights
+  float* rfull = reinterpret_cast<float*>(smem + lay.rfull);     // owner: [nbmax] all block scores
+  float* glall = reinterpret_cast<float*>(smem + lay.glall);     // owner: [C] each CTA's last-kernel g
+  int* item_ctr = reinterpret_cast<int*>(smem + lay.items);      // next attention item of this CTA
+  int* pair_next = item_ctr + 1;                                 // [pairs][2] mailbox
   int32_t* selS = reinterpret_cast<int32_t*>(smem + lay.sel);    // [kmax] ascending, -1 padded
   float2* cta_ml = reinterpret_cast<float2*>(smem + lay.cta_ml);
   float2* warp_ml = reinterpret_cast<float2*>(smem + lay.warp_ml);
@@ -133,6 +150,10 @@ __global__ void __launch_bounds__(kDsThreads, 2)
   const int g = lane >> 2, tq = lane & 3;
   const int rank = static_cast<int>(cluster_ctarank());
   const int bh = blockIdx.y;
+  // The CTA that gathers the block scores and selects; it differs between
+  // neighbouring groups so that two clusters sharing SMs do not stack their
+  // selections on one SM.
+  const int owner = bh % C;
   const int b = bh / p.Hkv, h = bh % p.Hkv;
   const int Hq = p.Hkv * kGroup;
   const size_t orow = static_cast<size_t>(b) * Hq + static_cast<size_t>(h) * kGroup;
@@ -149,10 +170,16 @@ __global__ void __launch_bounds__(kDsThreads, 2)
     mbar_init(qbar, 1);
     for (int s = 0; s < kDsPairs; ++s) mbar_init(&kvfull[s], 1);
     fence_barrier_init();
+    *item_ctr = kDsPairs;
   }
   __syncthreads();
   pdl_wait();
   pdl_trigger();
+  if (tid == 0) {   // Q does not depend on the length: start it first
+    mbar_arrive_expect_tx(qbar, 4096);
+    tma_load_2d(smem + lay.q, &q_map, 0, static_cast<int>(orow), qbar);
+    tma_load_2d(smem + lay.q + 2048, &q_map, 64, static_cast<int>(orow), qbar);
+  }
 
   const int L = p.kv_lens[b];
   const int nbt = L >= 1 ? (L - 1) / kBlock + 1 : 0;
@@ -168,6 +195,7 @@ __global__ void __launch_bounds__(kDsThreads, 2)
         atomicOr(p.status, kStatusBadKvLen);
       }
     }
+    mbar_wait(qbar, 0, p.status);   // no copy may still be landing in this CTA's memory
     return;
   }
   const int i = L - 1, c = i / kBlock;
@@ -188,21 +216,35 @@ __global__ void __launch_bounds__(kDsThreads, 2)
     tma_load_2d(dst + 16384, &kc_map, 0, (bh * 2 + 1) * p.ncmax + row, &full[st]);
     tma_load_2d(dst + 24576, &kc_map, 64, (bh * 2 + 1) * p.ncmax + row, &full[st]);
   };
-  if (tid == 0) {
-    mbar_arrive_expect_tx(qbar, 4096);
-    tma_load_2d(smem + lay.q, &q_map, 0, static_cast<int>(orow), qbar);
-    tma_load_2d(smem + lay.q + 2048, &q_map, 64, static_cast<int>(orow), qbar);
+  const int kv_row0 = bh * p.Lmax;
+  if (rank == owner && warp == 2) {
+    // The forced blocks are known now: their K/V head for L2 at once.
+    const int n_first = min(p.n_init, c + 1);
+    const int lo = max(n_first, c - p.n_local + 1);
+    const int n_f = n_first + max(0, c - lo + 1);
+    for (int x = lane; x < n_f; x += 32)
+      prefetch_block(&k_map, &v_map, kv_row0 + (x < n_first ? x : lo + x - n_first) * kBlock);
+  }
+  if (it_new >= 0 && warp == 7) {
+    // The 32 keys of the newest kernel (8 KB): into L2 while Q and the first chunks load.
+    const char* kr = reinterpret_cast<const char*>(p.k + (static_cast<size_t>(bh) * p.Lmax + jn * kStride) * kHeadDim);
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(kr + lane * 256));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(kr + lane * 256 + 128));
+  }
+  if (tid == 0)
     for (int it = 0; it < min(kDsStages, nmy); ++it) issue(it);
-    for (int it = kDsStages; it < nmy; ++it) {
-      const int row = (k0 + it) * kDsChunk;
-      tma_prefetch_2d(&kc_map, 0, (bh * 2 + 0) * p.ncmax + row);
-      tma_prefetch_2d(&kc_map, 64, (bh * 2 + 0) * p.ncmax + row);
-      tma_prefetch_2d(&kc_map, 0, (bh * 2 + 1) * p.ncmax + row);
-      tma_prefetch_2d(&kc_map, 64, (bh * 2 + 1) * p.ncmax + row);
+  if (warp == 1) {
+    // The rest of this CTA's chunks go to L2 now (one box per lane), so HBM
+    // streams at full rate while the two shared-memory stages trail behind.
+    for (int x = lane; x < 4 * (nmy - kDsStages); x += 32) {
+      const int row = (k0 + kDsStages + (x >> 2)) * kDsChunk;
+      tma_prefetch_2d(&kc_map, (x & 1) * 64, (bh * 2 + ((x >> 1) & 1)) * p.ncmax + row);
     }
   }
 
-  // ---------------------------------------------------- newest kernel --
+  // ------------------------------------------------------------ phase A --
+  bool ok = __syncthreads_and(mbar_wait(qbar, 0, p.status));
+  // Newest kernel, by warp 7 while the other warps start on the chunks.
   // Warp 7: lane = 16 * half + sub sums chunk jn + half over dims [8 sub, 8 sub + 8).
   uint4 new_hi = make_uint4(0, 0, 0, 0), new_lo = make_uint4(0, 0, 0, 0);
   if (it_new >= 0 && warp == 7) {
@@ -224,73 +266,78 @@ __global__ void __launch_bounds__(kDsThreads, 2)
     }
   }
 
-  // ------------------------------------------------------------ phase A --
-  bool ok = __syncthreads_and(mbar_wait(qbar, 0, p.status));
   const uint32_t q_b = smem_u32(smem + lay.q);
-  float zr[kDsMaxIt][4];
-  float mx0 = -INFINITY, mx1 = -INFINITY;
+  // z (then exp2(z - warp max)) of chunk it, head h, kernel x of the chunk:
+  // zs[(it * 16 + h) * 64 + x], in the stage slot phase A leaves free.
+  float* zs = reinterpret_cast<float*>(smem + kDsZOff);
+  float mx0 = -INFINITY, mx1 = -INFINITY;   // this warp's max of heads g and g + 8
   {
     uint32_t a[8][4];
     load_q_frags(a, q_b, lane);
-#pragma unroll
-    for (int it = 0; it < kDsMaxIt; ++it) {
-      zr[it][0] = zr[it][1] = zr[it][2] = zr[it][3] = -INFINITY;
-      if (it < nmy) {
-        const int st = it % kDsStages;
-        const uint32_t ph = static_cast<uint32_t>(it / kDsStages) & 1u;
-        bool got = ok && mbar_wait(&full[st], ph, p.status);
-        ok = __all_sync(0xffffffffu, got);
-        if (it == it_new) {   // the same iteration in every warp of the CTA
-          ok = __syncthreads_and(ok);
-          if (ok && warp == 7 && lane < 16) {
-            uint8_t* stg = smem + st * kDsStageBytes;
-            const uint32_t off = swz128_offset(jn - (k0 + it) * kDsChunk, lane, kDsChunk);
-            *reinterpret_cast<uint4*>(stg + off) = new_hi;
-            *reinterpret_cast<uint4*>(stg + 16384 + off) = new_lo;
-          }
-          __syncthreads();
+#pragma unroll 1
+    for (int it = 0; it < nmy; ++it) {
+      const int st = it % kDsStages;
+      const uint32_t ph = static_cast<uint32_t>(it / kDsStages) & 1u;
+      bool got = ok && mbar_wait(&full[st], ph, p.status);
+      ok = __all_sync(0xffffffffu, got);
+      if (it == it_new) {   // the same iteration in every warp of the CTA
+        ok = __syncthreads_and(ok);
+        if (ok && warp == 7 && lane < 16) {
+          uint8_t* stg = smem + st * kDsStageBytes;
+          const uint32_t off = swz128_offset(jn - (k0 + it) * kDsChunk, lane, kDsChunk);
+          *reinterpret_cast<uint4*>(stg + off) = new_hi;
+          *reinterpret_cast<uint4*>(stg + 16384 + off) = new_lo;
         }
-        if (ok) {
-          const uint32_t hi_b = smem_u32(smem + st * kDsStageBytes);
-          const int kj = (k0 + it) * kDsChunk + warp * 8 + 2 * tq;
-          float acc[4];
-          score_ntile(acc, a, hi_b, hi_b + 16384, warp * 8, kDsChunk, lane);
-          const bool v0 = kj < nc, v1 = kj + 1 < nc;
-          zr[it][0] = v0 ? acc[0] * p.score_scale2 : -INFINITY;
-          zr[it][1] = v1 ? acc[1] * p.score_scale2 : -INFINITY;
-          zr[it][2] = v0 ? acc[2] * p.score_scale2 : -INFINITY;
-          zr[it][3] = v1 ? acc[3] * p.score_scale2 : -INFINITY;
-          mx0 = fmaxf(mx0, fmaxf(zr[it][0], zr[it][1]));
-          mx1 = fmaxf(mx1, fmaxf(zr[it][2], zr[it][3]));
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
-        if (tid == 0 && ok && it + kDsStages < nmy) {
-          if (mbar_wait(&empty[st], ph, p.status)) issue(it + kDsStages);
-        }
-        __syncwarp();
+        __syncthreads();
       }
+      float z0 = -INFINITY, z1 = -INFINITY, z2 = -INFINITY, z3 = -INFINITY;
+      if (ok) {
+        const uint32_t hi_b = smem_u32(smem + st * kDsStageBytes);
+        const int kj = (k0 + it) * kDsChunk + warp * 8 + 2 * tq;
+        float acc[4];
+        score_ntile(acc, a, hi_b, hi_b + 16384, warp * 8, kDsChunk, lane);
+        const bool v0 = kj < nc, v1 = kj + 1 < nc;
+        z0 = v0 ? acc[0] * p.score_scale2 : -INFINITY;
+        z1 = v1 ? acc[1] * p.score_scale2 : -INFINITY;
+        z2 = v0 ? acc[2] * p.score_scale2 : -INFINITY;
+        z3 = v1 ? acc[3] * p.score_scale2 : -INFINITY;
+        mx0 = fmaxf(mx0, fmaxf(z0, z1));
+        mx1 = fmaxf(mx1, fmaxf(z2, z3));
+      }
+      float* zrow = zs + (it * kGroup + g) * kDsChunk + warp * 8 + 2 * tq;
+      *reinterpret_cast<float2*>(zrow) = make_float2(z0, z1);
+      *reinterpret_cast<float2*>(zrow + 8 * kDsChunk) = make_float2(z2, z3);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+      if (tid == 0 && ok && it + kDsStages < nmy) {
+        if (mbar_wait(&empty[st], ph, p.status)) issue(it + kDsStages);
+      }
+      __syncwarp();
     }
   }
 
   // --------------------------------------------------- LSE over the cluster --
   // Row g holds head g, row g + 8 head g + 8; the four tq lanes share a row.
+  // Each thread turns its own z into exp2(z - warp max) in place.
 #pragma unroll
   for (int o = 1; o <= 2; o <<= 1) {
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
   }
   float l0 = 0.f, l1 = 0.f;
-#pragma unroll
-  for (int it = 0; it < kDsMaxIt; ++it) {
-    if (it < nmy) {
-      zr[it][0] = (mx0 == -INFINITY) ? 0.f : fast_exp2(zr[it][0] - mx0);
-      zr[it][1] = (mx0 == -INFINITY) ? 0.f : fast_exp2(zr[it][1] - mx0);
-      zr[it][2] = (mx1 == -INFINITY) ? 0.f : fast_exp2(zr[it][2] - mx1);
-      zr[it][3] = (mx1 == -INFINITY) ? 0.f : fast_exp2(zr[it][3] - mx1);
-      l0 += zr[it][0] + zr[it][1];
-      l1 += zr[it][2] + zr[it][3];
-    }
+#pragma unroll 4
+  for (int it = 0; it < nmy; ++it) {
+    float2* z01 = reinterpret_cast<float2*>(zs + (it * kGroup + g) * kDsChunk + warp * 8 + 2 * tq);
+    float2* z23 = reinterpret_cast<float2*>(reinterpret_cast<float*>(z01) + 8 * kDsChunk);
+    float2 u = *z01, w = *z23;
+    u.x = (mx0 == -INFINITY) ? 0.f : fast_exp2(u.x - mx0);
+    u.y = (mx0 == -INFINITY) ? 0.f : fast_exp2(u.y - mx0);
+    w.x = (mx1 == -INFINITY) ? 0.f : fast_exp2(w.x - mx1);
+    w.y = (mx1 == -INFINITY) ? 0.f : fast_exp2(w.y - mx1);
+    *z01 = u;
+    *z23 = w;
+    l0 += u.x + u.y;
+    l1 += w.x + w.y;
   }
 #pragma unroll
   for (int o = 1; o <= 2; o <<= 1) {
@@ -302,97 +349,96 @@ __global__ void __launch_bounds__(kDsThreads, 2)
     wpart[warp * kGroup + g + 8] = make_float2(mx1, l1);
   }
   __syncthreads();
-  if (tid < kGroup) {
-    float m = -INFINITY, l = 0.f;
+  if (tid < 8 * kGroup) {   // head tid / 8, warp tid % 8: a shuffle tree over the 8 warps
+    const float2 v = wpart[(tid & 7) * kGroup + (tid >> 3)];
+    float m = v.x, l = v.y;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
-      const float2 v = wpart[w * kGroup + tid];
-      lse_merge(m, l, v.x, v.y);
-    }
-    cpart[tid] = make_float2(m, l);
+    for (int o = 1; o < 8; o <<= 1)
+      lse_merge(m, l, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, l, o));
+    if ((tid & 7) == 0) cpart[tid >> 3] = make_float2(m, l);
   }
   cluster_sync();
-  if (tid < kGroup) {
-    float2 v[C];
+  if (tid < C * kGroup) {   // head tid / C, CTA tid % C: one remote load each, then a shuffle tree
+    const float2 v = ld_dsmem_f32x2(dsmem_addr(&cpart[tid / C], tid % C));
+    float m = v.x, l = v.y;
 #pragma unroll
-    for (int q = 0; q < C; ++q) v[q] = ld_dsmem_f32x2(dsmem_addr(&cpart[tid], q));
-    float m = -INFINITY, l = 0.f;
-#pragma unroll
-    for (int q = 0; q < C; ++q) lse_merge(m, l, v[q].x, v[q].y);
-    lse2[tid] = (m == -INFINITY) ? -INFINITY : m + fast_log2(l);
+    for (int o = 1; o < C; o <<= 1)
+      lse_merge(m, l, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, l, o));
+    if (tid % C == 0) lse2[tid / C] = (m == -INFINITY) ? -INFINITY : m + fast_log2(l);
   }
   __syncthreads();
 
   // ------------------------------------------------------------ phase B --
-  {
-    const float w0 = (mx0 == -INFINITY) ? 0.f : fast_exp2(mx0 - lse2[g]) * (1.0f / kGroup);
-    const float w1 = (mx1 == -INFINITY) ? 0.f : fast_exp2(mx1 - lse2[g + 8]) * (1.0f / kGroup);
+  // Weight of warp w's exponentials of head h: exp2(max_wh - lse_h) / 16.
+  if (tq == 0) {
+    wtab[warp * kGroup + g] = (mx0 == -INFINITY) ? 0.f : fast_exp2(mx0 - lse2[g]) * (1.0f / kGroup);
+    wtab[warp * kGroup + g + 8] = (mx1 == -INFINITY) ? 0.f : fast_exp2(mx1 - lse2[g + 8]) * (1.0f / kGroup);
+  }
+  __syncthreads();
+  // g of every kernel of this CTA's chunks (kernel x of a chunk came from warp x / 8).
+#pragma unroll 1
+  for (int k = tid; k < nmy * kDsChunk; k += kDsThreads) {
+    const int it = k / kDsChunk, x = k % kDsChunk;
+    const float* zc = zs + it * kGroup * kDsChunk + x;
+    const float* wt = wtab + (x >> 3) * kGroup;
+    float acc = 0.f;
 #pragma unroll
-    for (int it = 0; it < kDsMaxIt; ++it) {
-      if (it < nmy) {
-        float se = zr[it][0] * w0 + zr[it][2] * w1;   // kernel kj, heads g and g + 8
-        float so = zr[it][1] * w0 + zr[it][3] * w1;   // kernel kj + 1
-#pragma unroll
-        for (int o = 4; o <= 16; o <<= 1) {
-          se += __shfl_xor_sync(0xffffffffu, se, o);
-          so += __shfl_xor_sync(0xffffffffu, so, o);
-        }
-        if (g == 0) *reinterpret_cast<float2*>(&gbuf[it * kDsChunk + warp * 8 + 2 * tq]) = make_float2(se, so);
-      }
-    }
+    for (int h = 0; h < kGroup; ++h) acc += zc[h * kDsChunk] * wt[h];
+    gbuf[k] = acc;
   }
   __syncthreads();
   {
     const int jb0 = 16 * k0, jb1 = min(16 * k1, nbt);
     const int kb0 = kDsChunk * k0;
+#pragma unroll 1
     for (int j = jb0 + tid; j < jb1; j += kDsThreads) {
       const int a0 = max(4 * j - 1, kb0), e0 = min(nc - 1, 4 * j + 3);
       float r = -INFINITY;
       for (int k = a0; k <= e0; ++k) r = fmaxf(r, gbuf[k - kb0]);
-      rsl[j - jb0] = r;
+      st_dsmem_f32(dsmem_addr(rfull + j, owner), r);   // the owner gathers every block score
     }
-    if (tid == 0) *glast = (k1 > k0 && kDsChunk * k1 - 1 < nc) ? gbuf[kDsChunk * (k1 - k0) - 1] : -INFINITY;
+    if (tid == 0) {
+      const float gl = (k1 > k0 && kDsChunk * k1 - 1 < nc) ? gbuf[kDsChunk * (k1 - k0) - 1] : -INFINITY;
+      st_dsmem_f32(dsmem_addr(glall + rank, owner), gl);
+    }
   }
   cluster_sync();
 
   // ------------------------------------------------------------- top-k --
-  if (rank == 0) {
-    float v[kDsMaxR];   // block j = tid + 256 x, scored by CTA (j / 16) / per
-#pragma unroll
-    for (int x = 0; x < kDsMaxR; ++x) {
-      const int j = tid + kDsThreads * x;
-      v[x] = -INFINITY;
-      if (j < nbt) {
-        const int q = (j >> 4) / per;
-        const int base = 16 * per * q;
-        float r = ld_dsmem_f32(dsmem_addr(&rsl[j - base], q));
-        if (j == base && q > 0) r = fmaxf(r, ld_dsmem_f32(dsmem_addr(glast, q - 1)));
-        v[x] = r;
-      }
+  if (rank == owner) {
+    // Block 16 per q starts CTA q's range; its kernel 64 per q - 1 was scored by CTA q - 1.
+    if (tid > 0 && tid < C && 16 * per * tid < nbt)
+      rfull[16 * per * tid] = fmaxf(rfull[16 * per * tid], glall[tid - 1]);
+    __syncthreads();
+    SmemTopkScratch<kDsThreads>& tk = *reinterpret_cast<SmemTopkScratch<kDsThreads>*>(smem);
+    select_topk_smem<kDsThreads>(rfull, nbt, p.n_init, p.n_local, p.topk, p.inc_forced != 0, p.kmax,
+                                 p.block_idx + static_cast<size_t>(bh) * p.kmax, p.n_sel + bh, tk,
+                                 reinterpret_cast<uint32_t*>(smem + lay.bits),
+                                 reinterpret_cast<unsigned long long*>(smem + lay.surv), tid, selS);
+    __syncthreads();
+    // Every CTA gets the list in its own shared memory.
+#pragma unroll 1
+    for (int e = tid; e < C * p.kmax; e += kDsThreads) {
+      const int q = e / p.kmax, x = e % p.kmax;
+      if (q != owner) st_dsmem_u32(dsmem_addr(selS + x, q), static_cast<uint32_t>(selS[x]));
     }
-    RegTopkScratch<kDsThreads>& tk = *reinterpret_cast<RegTopkScratch<kDsThreads>*>(smem);
-    select_topk_regs<kDsThreads, kDsMaxR>(
-        v, nbt, p.n_init, p.n_local, p.topk, p.inc_forced != 0, p.kmax, p.block_idx + static_cast<size_t>(bh) * p.kmax,
-        p.n_sel + bh, tk, reinterpret_cast<unsigned long long*>(smem + lay.surv),
-        reinterpret_cast<int*>(smem + lay.selbuf), tid, selS);
   }
   cluster_sync();
 
   // ------------------------------------------------------------ attend --
-  if (rank != 0)
-    for (int x = tid; x < p.kmax; x += kDsThreads)
-      selS[x] = static_cast<int32_t>(ld_dsmem_u32(dsmem_addr(&selS[x], 0)));
-  __syncthreads();
-
   const int pair = warp >> 1, half = warp & 1;
   if (pair < kDsPairs) {
     uint8_t* stage = smem + pair * kDsStageBytes;
     const uint32_t k_b = smem_u32(stage), v_b = k_b + 16384;
-    const int kv_row0 = bh * p.Lmax;
     const int rbase = 32 * half;
-    int n = rank + C * pair;
-    int j = n < p.kmax ? selS[n] : -1;
-    if (j > c) j = -1;
+    // Item x of this CTA is list entry rank + C x: items 0..2 go to pairs
+    // 0..2, each later one to whichever pair frees its stage first.
+    auto block_of = [&](int item) {
+      const int n = rank + C * item;
+      const int j = n < p.kmax ? selS[n] : -1;
+      return j > c ? -1 : j;
+    };
+    int j = block_of(pair);
     if (half == 0 && lane == 0 && j >= 0) tma_block(stage, &k_map, &v_map, kv_row0 + j * kBlock, &kvfull[pair]);
 
     float o[16][4];
@@ -402,6 +448,7 @@ __global__ void __launch_bounds__(kDsThreads, 2)
     l0 = 0.f;
     l1 = 0.f;
     uint32_t phase = 0;
+    int iter = 0;
 #pragma unroll 1
     while (j >= 0) {
       bool got = ok && mbar_wait(&kvfull[pair], phase, p.status);
@@ -500,21 +547,18 @@ __global__ void __launch_bounds__(kDsThreads, 2)
           }
         }
       }
-      // Next block of this pair (the same sequence in both warps).
-      n += C * kDsPairs;
-      int jnext = n < p.kmax ? selS[n] : -1;
-      if (jnext > c) jnext = -1;
-      if (jnext >= 0) {
-        // Both warps are done with the stage; order the zeroed V rows
-        // (generic writes) before the TMA refill (async proxy).
-        fence_proxy_async_smem();
-        pair_sync(pair);
-        if (half == 0 && lane == 0 && ok)
-          tma_block(stage, &k_map, &v_map, kv_row0 + jnext * kBlock, &kvfull[pair]);
-      }
-      j = jnext;
+      // Next item of this pair: drawn by the even warp, shared through a
+      // two-slot mailbox (a slot is rewritten only two pair barriers later).
+      if (half == 0 && lane == 0) pair_next[pair * 2 + (iter & 1)] = atomicAdd(item_ctr, 1);
+      // Both warps are done with the stage; order the zeroed V rows
+      // (generic writes) before the TMA refill (async proxy).
+      fence_proxy_async_smem();
+      pair_sync(pair);
+      j = block_of(pair_next[pair * 2 + (iter & 1)]);
+      ++iter;
+      if (j >= 0 && half == 0 && lane == 0 && ok)
+        tma_block(stage, &k_map, &v_map, kv_row0 + j * kBlock, &kvfull[pair]);
     }
-    pair_sync(pair);   // the partner has finished reading the stage
 #pragma unroll
     for (int off = 1; off <= 2; off <<= 1) {
       l0 += __shfl_xor_sync(0xffffffffu, l0, off);
@@ -562,6 +606,7 @@ __global__ void __launch_bounds__(kDsThreads, 2)
 
   // Heads [hpc * rank, hpc * (rank + 1)) of the output from all partials.
   constexpr int hpc = kGroup / C;
+#pragma unroll 1
   for (int e = tid; e < hpc * kHeadDim; e += kDsThreads) {
     const int hd = rank * hpc + e / kHeadDim;
     const int d = e % kHeadDim;
@@ -593,8 +638,8 @@ template <int C>
 bool ds_fits(const Shape& s) {
   const int groups = (s.nbmax + 15) / 16;
   const DsLayout l = ds_layout(s.nbmax, s.kmax);
-  return s.nq == 1 && ds_per(groups, C) <= kDsMaxIt && s.nbmax <= kDsThreads * kDsMaxR &&
-         l.selbuf + s.kmax * 4 <= kDsPairs * kDsStageBytes && l.total + 1024 <= 113 * 1024;
+  return s.nq == 1 && ds_per(groups, C) <= kDsMaxIt &&
+         l.glall + 16 * 4 <= kDsZOff && l.total + 1024 <= 113 * 1024;
 }
 
 template <int C>

@@ -20,7 +20,7 @@
 //            -> exact LSE per head.
 //   phase B  g and the block maxima r of the CTA's blocks.
 //   sync     the CTA that owns token t (t mod C) pulls the token's block
-//            scores into registers and runs a register-resident top-k.
+//            scores into registers and selects (bitmask top-k).
 // No global partials, tickets or memsets: cluster barriers order it all.
 #include "select_common.cuh"
 
@@ -35,7 +35,7 @@ constexpr int kClStageBytes = 2 * kClChunk * 256;
 constexpr int kClMaxR = 16;       // block scores per thread in the top-k (nbmax <= 4096)
 
 struct ClLayout {
-  int stage, q, wpart, cpart, lse, g, rsl, tk, surv, sel, bar, total, rsl_stride;
+  int stage, q, wpart, cpart, lse, g, rsl, tk, surv, bar, total, rsl_stride;
 };
 
 __host__ __device__ inline int cl_per(int groups, int C) { return (groups + C - 1) / C; }
@@ -52,9 +52,8 @@ __host__ __device__ inline ClLayout cl_layout(int C, int nq, int nbmax, int kmax
   l.g = l.lse + nq * kGroup * 4;
   l.rsl = l.g + (per * kClChunk + 4) * 4;
   l.tk = (l.rsl + nq * l.rsl_stride * 4 + 15) & ~15;
-  l.surv = (l.tk + static_cast<int>(sizeof(RegTopkScratch<kClThreads>)) + 15) & ~15;
-  l.sel = l.surv + nbmax * 8;
-  l.bar = (l.sel + kmax * 4 + 15) & ~15;
+  l.surv = (l.tk + static_cast<int>(sizeof(BitTopkScratch<kClThreads, kClMaxR>)) + 15) & ~15;
+  l.bar = (l.surv + nbmax * 8 + 15) & ~15;
   l.total = l.bar + (2 * kClStages + 1) * 8;
   return l;
 }
@@ -72,9 +71,8 @@ __global__ void __launch_bounds__(kClThreads, 2)
   float* lse2 = reinterpret_cast<float*>(smem + lay.lse);        // [nq*16]
   float* gbuf = reinterpret_cast<float*>(smem + lay.g);
   float* rsl = reinterpret_cast<float*>(smem + lay.rsl);         // [nq][rsl_stride]
-  RegTopkScratch<kClThreads>& tk = *reinterpret_cast<RegTopkScratch<kClThreads>*>(smem + lay.tk);
+  BitTopkScratch<kClThreads, kClMaxR>& tk = *reinterpret_cast<BitTopkScratch<kClThreads, kClMaxR>*>(smem + lay.tk);
   unsigned long long* surv = reinterpret_cast<unsigned long long*>(smem + lay.surv);   // [nbmax]
-  int* selbuf = reinterpret_cast<int*>(smem + lay.sel);          // [kmax]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.bar);
   uint64_t* empty = full + kClStages;
   uint64_t* qbar = empty + kClStages;
@@ -278,9 +276,8 @@ __global__ void __launch_bounds__(kClThreads, 2)
     }
     if (p.write_r)
       for (int j = nb + tid; j < p.nbmax; j += kClThreads) p.r_buf[(unit0 + t) * p.nbmax + j] = -INFINITY;
-    select_topk_regs<kClThreads, kClMaxR>(v, nb, p.n_init, p.n_local, p.topk, p.inc_forced != 0, p.kmax,
-                                          p.block_idx + (unit0 + t) * p.kmax, p.n_sel + unit0 + t, tk, surv,
-                                          selbuf, tid);
+    select_topk_bits<kClThreads, kClMaxR>(v, nb, p.n_init, p.n_local, p.topk, p.inc_forced != 0, p.kmax,
+                                          p.block_idx + (unit0 + t) * p.kmax, p.n_sel + unit0 + t, tk, surv, tid);
     __syncthreads();
   }
   cluster_sync();   // keeps this CTA's shared memory alive for remote readers

@@ -173,46 +173,91 @@ __device__ void select_topk(const float* r, uint8_t* flag, int nb, int n_init, i
 
 // Top-k over scores held in registers: thread tid holds the scores of blocks
 // j = tid + NT x (x < MAXR) in v[x].  Same selection rule and output as
-// select_topk.  One 256-bin histogram of the scores' leading bits (sign,
-// exponent, 6 mantissa bits, counted down from the best score) locates the
-// bin holding the n_take-th best score; candidates at or above it are
-// ranked exactly by (score desc, index asc).  Every step works on registers
-// with a handful of CTA barriers.  `surv` (shared, nb entries) takes the
-// survivors, so many-way exact ties are handled too; `sel` (shared, k_max
-// entries) collects the chosen blocks; `sorted_copy` (optional, k_max
-// entries) receives the ascending output list too, padded with -1.  NT >= 256.
-template <int NT>
-struct RegTopkScratch {
+// select_topk.  The chosen blocks are marked in a bitmask whose ascending
+// scan is the output, so no step sorts or ranks more than the few scores
+// tied for the last places:
+//   1. a 256-bin histogram of the candidates' leading bits (sign, exponent,
+//      6 mantissa bits) counted down from the best score locates the bin
+//      holding the n_take-th best; when that is the catch-all last bin and
+//      it holds more than NT scores, a second histogram over that bin (16
+//      times coarser, reaching 68 octaves below the best) narrows it;
+//   2. candidates in better bins are marked, those in the boundary bin are
+//      ranked exactly by (score desc, index asc) among themselves;
+//   3. forced blocks are marked too, and one warp writes the set bits in
+//      ascending order.
+// `surv` (shared, nb entries) holds the boundary bin; `sorted_copy`
+// (optional, k_max entries) receives the output list too, padded with -1.
+// NT >= 256; the caller synchronises before reading sorted_copy.
+template <int NT, int MAXR>
+struct BitTopkScratch {
+  static constexpr int kWords = (NT * MAXR + 31) / 32;
   uint32_t hist[NT / 32][256];
+  uint32_t bits[kWords];
   int wred[NT / 32][2];
   int warp_tot[NT / 32];
-  int ctrl[4];
+  int ctrl[4];   // boundary bin, count in better bins, boundary-list length
 };
 
+// Bin holding the need-th best entry of the per-warp histograms (bin 0 =
+// best); *above = entries in better bins.  Zeroes the histograms for reuse.
+// Two barriers.
 template <int NT, int MAXR>
-__device__ void select_topk_regs(const float (&v)[MAXR], int nb, int n_init, int n_local, int topk,
+__device__ __forceinline__ int topk_boundary_bin(BitTopkScratch<NT, MAXR>& sm, int need, int tid, int* above) {
+  constexpr int NWARP = NT / 32;
+  const int lane = tid & 31, warp = tid >> 5;
+  int cnt = 0;
+  if (tid < 256) {
+#pragma unroll
+    for (int w = 0; w < NWARP; ++w) cnt += static_cast<int>(sm.hist[w][tid]);
+  }
+  const int incl = warp_inclusive_scan(cnt);
+  if (lane == 31) sm.warp_tot[warp] = incl;
+  __syncthreads();
+  for (int b = lane; b < 256; b += 32) sm.hist[warp][b] = 0u;
+  int before = 0;
+#pragma unroll
+  for (int w = 0; w < NWARP; ++w) before += (w < warp) ? sm.warp_tot[w] : 0;
+  const int run = before + incl - cnt;
+  if (tid < 256 && run < need && run + cnt >= need) {
+    sm.ctrl[0] = tid;
+    sm.ctrl[1] = run;
+  }
+  __syncthreads();
+  *above = sm.ctrl[1];
+  return sm.ctrl[0];
+}
+
+template <int NT, int MAXR>
+__device__ void select_topk_bits(const float (&v)[MAXR], int nb, int n_init, int n_local, int topk,
                                  bool includes_forced, int k_max, int32_t* out_idx, int32_t* out_n,
-                                 RegTopkScratch<NT>& sm, unsigned long long* surv_buf, int* sel_buf,
-                                 int tid, int32_t* sorted_copy = nullptr) {
+                                 BitTopkScratch<NT, MAXR>& sm, unsigned long long* surv, int tid,
+                                 int32_t* sorted_copy = nullptr) {
   static_assert(NT >= 256, "one thread per histogram bin");
   constexpr int NWARP = NT / 32;
   constexpr int kShift = 17;
+  constexpr int kWords = BitTopkScratch<NT, MAXR>::kWords;
   const int lane = tid & 31, warp = tid >> 5;
   const int c = nb - 1;
-  // 1. candidates, their count and best leading bits.
+  const int n_first = min(n_init, nb);
+  const int local_lo = max(n_first, c - n_local + 1);
+  // 1. candidates, their count and the best leading bits; clear the scratch.
   bool cand[MAXR];
+  uint32_t key[MAXR];
   int my_cand = 0;
   uint32_t my_top = 0;
 #pragma unroll
   for (int x = 0; x < MAXR; ++x) {
     const int j = tid + NT * x;
-    cand[x] = j < nb && j >= n_init && j <= c - n_local && v[x] > -INFINITY;
+    key[x] = float_to_ordered(v[x]);
+    cand[x] = j < nb && j >= n_first && j < local_lo && v[x] > -INFINITY;
     if (cand[x]) {
       ++my_cand;
-      my_top = max(my_top, float_to_ordered(v[x]) >> kShift);
+      my_top = max(my_top, key[x] >> kShift);
     }
   }
   for (int b = lane; b < 256; b += 32) sm.hist[warp][b] = 0u;
+  for (int w = tid; w < kWords; w += NT) sm.bits[w] = 0u;
+  if (tid == 0) sm.ctrl[2] = 0;
   my_cand = __reduce_add_sync(0xffffffffu, my_cand);
   my_top = __reduce_max_sync(0xffffffffu, my_top);
   if (lane == 0) {
@@ -227,229 +272,274 @@ __device__ void select_topk_regs(const float (&v)[MAXR], int nb, int n_init, int
     n_cand += sm.wred[w][0];
     top = max(top, static_cast<uint32_t>(sm.wred[w][1]));
   }
-  const int n_first = min(n_init, nb);
-  const int n_forced = n_first + max(0, c - max(n_first, c - n_local + 1) + 1);
+  const int n_forced = n_first + max(0, c - local_lo + 1);
   const int n_take = max(0, includes_forced ? topk - n_forced : topk);
-  // 2. boundary bin (255 = every candidate survives, -1 = none is taken).
-  int bnd = n_take > 0 ? 255 : -1;
-  if (n_take > 0 && n_cand > n_take) {
+
+  // 2. thresholds: candidates with d < d_sel are taken, d in [d_sel, d_bnd]
+  //    (and, at the second level, coarse bin == bnd2) are ranked.
+  //    d = distance of a score's leading bits from the best one.
+  bool take_all = n_take >= n_cand, take_none = n_take == 0;
+  int lvl = 0, bnd = 0, above = 0;
+  if (!take_all && !take_none) {
 #pragma unroll
     for (int x = 0; x < MAXR; ++x)
-      if (cand[x]) atomicAdd(&sm.hist[warp][min(255u, top - (float_to_ordered(v[x]) >> kShift))], 1u);
+      if (cand[x]) atomicAdd(&sm.hist[warp][min(255u, top - (key[x] >> kShift))], 1u);
     __syncthreads();
-    int cnt = 0;
-    for (int b = tid; b < 256; b += NT) {
+    bnd = topk_boundary_bin(sm, n_take, tid, &above);
+    lvl = 1;
+    if (bnd == 255 && n_cand - above > NT) {
 #pragma unroll
-      for (int w = 0; w < NWARP; ++w) cnt += static_cast<int>(sm.hist[w][b]);
+      for (int x = 0; x < MAXR; ++x) {
+        const uint32_t d = top - (key[x] >> kShift);
+        if (cand[x] && d >= 255u) atomicAdd(&sm.hist[warp][min(255u, (d - 255u) >> 4)], 1u);
+      }
+      __syncthreads();
+      int above2 = 0;
+      bnd = topk_boundary_bin(sm, n_take - above, tid, &above2);
+      above += above2;
+      lvl = 2;
     }
-    // tid < 256 holds bin tid (NT >= 256); inclusive scan in bin order.
-    const int incl = warp_inclusive_scan(cnt);
-    if (lane == 31) sm.warp_tot[warp] = incl;
-    __syncthreads();
-    int before = 0;
-#pragma unroll
-    for (int w = 0; w < NWARP; ++w) before += (w < warp) ? sm.warp_tot[w] : 0;
-    const int run = before + incl - cnt;
-    if (tid < 256 && run < n_take && run + cnt >= n_take) sm.ctrl[0] = tid;
-    __syncthreads();
-    bnd = sm.ctrl[0];
   }
-  // 3. survivors (candidates at or above the boundary bin) into shared memory.
-  bool surv[MAXR];
-  int my_surv = 0;
+  // 3. mark the taken candidates and the forced blocks; collect the boundary.
 #pragma unroll
   for (int x = 0; x < MAXR; ++x) {
-    surv[x] = cand[x] && static_cast<int>(min(255u, top - (float_to_ordered(v[x]) >> kShift))) <= bnd;
-    my_surv += surv[x] ? 1 : 0;
+    if (!cand[x] || take_none) continue;
+    const int j = tid + NT * x;
+    const uint32_t d = top - (key[x] >> kShift);
+    bool sel = take_all, tie = false;
+    if (lvl == 1) {
+      sel = static_cast<int>(min(255u, d)) < bnd;
+      tie = static_cast<int>(min(255u, d)) == bnd;
+    } else if (lvl == 2) {
+      const int d2 = d < 255u ? -1 : static_cast<int>(min(255u, (d - 255u) >> 4));
+      sel = d2 < bnd;
+      tie = d2 == bnd;
+    }
+    if (sel) atomicOr(&sm.bits[j >> 5], 1u << (j & 31));
+    if (tie) surv[atomicAdd(&sm.ctrl[2], 1)] = (static_cast<unsigned long long>(key[x]) << 32) |
+                                              static_cast<uint32_t>(~j);
   }
-  const int incl = warp_inclusive_scan(my_surv);
-  if (lane == 31) sm.warp_tot[warp] = incl;
+  for (int j = tid; j < n_first; j += NT) atomicOr(&sm.bits[j >> 5], 1u << (j & 31));
+  for (int j = local_lo + tid; j <= c; j += NT) atomicOr(&sm.bits[j >> 5], 1u << (j & 31));
   __syncthreads();
-  int pos = incl - my_surv, n_surv = 0;
+  // 4. the boundary entries that still fit, by exact rank among themselves.
+  if (lvl > 0) {
+    const int m = sm.ctrl[2];
+    const int need = n_take - above;
+    for (int x = tid; x < m; x += NT) {
+      const unsigned long long me = surv[x];
+      int rk = 0;
+      for (int y = 0; y < m; ++y) rk += (surv[y] > me) ? 1 : 0;
+      if (rk < need) {
+        const int j = static_cast<int>(~static_cast<uint32_t>(me & 0xffffffffu));
+        atomicOr(&sm.bits[j >> 5], 1u << (j & 31));
+      }
+    }
+    __syncthreads();
+  }
+  // 5. ascending output from the bitmask (one warp).
+  if (warp == 0) {
+    constexpr int WPL = (kWords + 31) / 32;
+    uint32_t w[WPL];
+    int cnt = 0;
 #pragma unroll
-  for (int w = 0; w < NWARP; ++w) {
-    pos += (w < warp) ? sm.warp_tot[w] : 0;
-    n_surv += sm.warp_tot[w];
-  }
+    for (int i = 0; i < WPL; ++i) {
+      const int wi = lane * WPL + i;
+      w[i] = wi < kWords ? sm.bits[wi] : 0u;
+      cnt += __popc(w[i]);
+    }
+    const int incl = warp_inclusive_scan(cnt);
+    const int total = min(__shfl_sync(0xffffffffu, incl, 31), k_max);
+    int pos = incl - cnt;
 #pragma unroll
-  for (int x = 0; x < MAXR; ++x)
-    if (surv[x]) surv_buf[pos++] = (static_cast<unsigned long long>(float_to_ordered(v[x])) << 32) |
-                                   static_cast<uint32_t>(~(tid + NT * x));
-  if (tid == 0) {   // forced blocks first, ascending
-    int n = 0;
-    for (int j = 0; j < n_first; ++j) sel_buf[n++] = j;
-    for (int j = max(n_first, c - n_local + 1); j <= c; ++j) sel_buf[n++] = j;
+    for (int i = 0; i < WPL; ++i) {
+      uint32_t bw = w[i];
+      while (bw) {
+        const int j = (lane * WPL + i) * 32 + __ffs(bw) - 1;
+        bw &= bw - 1u;
+        if (pos < k_max) {
+          out_idx[pos] = j;
+          if (sorted_copy) sorted_copy[pos] = j;
+        }
+        ++pos;
+      }
+    }
+    for (int x = total + lane; x < k_max; x += 32) {
+      out_idx[x] = -1;
+      if (sorted_copy) sorted_copy[x] = -1;
+    }
+    if (lane == 0) *out_n = total;
   }
-  __syncthreads();
-  // 4. exact rank among survivors; the best n_take follow the forced blocks.
-  for (int x = tid; x < n_surv; x += NT) {
-    const unsigned long long me = surv_buf[x];
-    int rk = 0, y = 0;
-    for (; y + 4 <= n_surv; y += 4)
-      rk += (surv_buf[y] > me) + (surv_buf[y + 1] > me) + (surv_buf[y + 2] > me) + (surv_buf[y + 3] > me);
-    for (; y < n_surv; ++y) rk += (surv_buf[y] > me) ? 1 : 0;
-    if (rk < n_take) sel_buf[n_forced + rk] = static_cast<int>(~static_cast<uint32_t>(me & 0xffffffffu));
-  }
-  __syncthreads();
-  // 5. ascending output.
-  const int n_total = min(k_max, n_forced + min(n_take, n_surv));
-  for (int x = tid; x < n_total; x += NT) {
-    const int val = sel_buf[x];
-    int p = 0;
-    for (int y = 0; y < n_total; ++y) p += (sel_buf[y] < val) ? 1 : 0;
-    out_idx[p] = val;
-    if (sorted_copy) sorted_copy[p] = val;
-  }
-  for (int x = n_total + tid; x < k_max; x += NT) {
-    out_idx[x] = -1;
-    if (sorted_copy) sorted_copy[x] = -1;
-  }
-  if (tid == 0) *out_n = n_total;
 }
 
-// Same contract as select_topk for a whole CTA (NT threads, NT % 32 == 0),
-// built for few barriers and no contended atomics: one 256-bin histogram of
-// the scores' leading bits (sign, exponent, 6 mantissa bits, counted down
-// from the best score; per-warp private copies) finds the bin holding the
-// n_take-th best score; every candidate at or above that bin survives, and
-// each survivor's exact rank among the survivors, by (score desc, index
-// asc), decides whether it is taken.  Falls back to the radix select when
-// the survivors exceed NT (many exactly tied or very close scores).
+// Same selection as select_topk_bits for scores held in shared memory
+// (r[0..nb)), with every pass a short rolled loop: on this path the code
+// fetched once per launch costs more than the arithmetic, so the routine is
+// kept small.  `bits` needs (nb + 31) / 32 words of shared scratch.
 template <int NT>
-struct FastTopkScratch {
-  uint32_t hist[NT / 32][256];  // per-warp histograms
-  unsigned long long surv[NT];  // survivors: (ordered key << 32) | ~index
-  int ctrl[8];
-  int wcnt[NT / 32][3];
-  TopkScratch<NT> radix;
+struct SmemTopkScratch {
+  uint32_t hist[NT / 32][256];
+  int wred[NT / 32][2];
+  int warp_tot[NT / 32];
+  int ctrl[4];   // boundary bin, count in better bins, boundary-list length
 };
 
 template <int NT>
-__device__ void select_topk_fast(const float* r, uint8_t* flag, int nb, int n_init, int n_local, int topk,
-                                 bool includes_forced, int k_max, int32_t* out_idx, int32_t* out_n,
-                                 FastTopkScratch<NT>& sm, int tid) {
+__device__ __forceinline__ int smem_topk_boundary(SmemTopkScratch<NT>& sm, int need, int tid, int* above) {
   constexpr int NWARP = NT / 32;
-  constexpr int kShift = 17;   // 1 sign + 8 exponent + 6 mantissa bits
+  const int lane = tid & 31, warp = tid >> 5;
+  int cnt = 0;
+  if (tid < 256)
+    for (int w = 0; w < NWARP; ++w) cnt += static_cast<int>(sm.hist[w][tid]);
+  const int incl = warp_inclusive_scan(cnt);
+  if (lane == 31) sm.warp_tot[warp] = incl;
+  __syncthreads();
+  for (int b = lane; b < 256; b += 32) sm.hist[warp][b] = 0u;
+  int before = 0;
+  for (int w = 0; w < warp; ++w) before += sm.warp_tot[w];
+  const int run = before + incl - cnt;
+  if (tid < 256 && run < need && run + cnt >= need) {
+    sm.ctrl[0] = tid;
+    sm.ctrl[1] = run;
+  }
+  __syncthreads();
+  *above = sm.ctrl[1];
+  return sm.ctrl[0];
+}
+
+template <int NT>
+__device__ void select_topk_smem(const float* r, int nb, int n_init, int n_local, int topk, bool includes_forced,
+                                 int k_max, int32_t* out_idx, int32_t* out_n, SmemTopkScratch<NT>& sm,
+                                 uint32_t* bits, unsigned long long* surv, int tid, int32_t* sorted_copy = nullptr) {
+  static_assert(NT >= 256, "one thread per histogram bin");
+  constexpr int NWARP = NT / 32;
+  constexpr int kShift = 17;
   const int lane = tid & 31, warp = tid >> 5;
   const int c = nb - 1;
-  const int local_lo = c - n_local + 1;
-  const int per = (nb + NT - 1) / NT;
-  const int lo = tid * per;
-  const int hi = min(nb, lo + per);
-  // 1. flags (contiguous range per thread), counts, best leading bits.
-  int my_cand = 0, my_forced = 0;
+  const int n_first = min(n_init, nb);
+  const int local_lo = max(n_first, c - n_local + 1);
+  const int n_words = (nb + 31) / 32;
+  auto is_cand = [&](int j, float x) { return j >= n_first && j < local_lo && x > -INFINITY; };
+  // 1. candidates, their count and the best leading bits; clear the scratch.
+  int my_cand = 0;
   uint32_t my_top = 0;
-  for (int j = lo; j < hi; ++j) {
-    const bool forced = (j < n_init) || (j >= local_lo);
-    const bool cand = !forced && (r[j] > -INFINITY);
-    flag[j] = forced ? 2 : (cand ? 1 : 0);
-    my_cand += cand ? 1 : 0;
-    my_forced += forced ? 1 : 0;
-    if (cand) my_top = max(my_top, float_to_ordered(r[j]) >> kShift);
+#pragma unroll 1
+  for (int j = tid; j < nb; j += NT) {
+    const float x = r[j];
+    if (is_cand(j, x)) {
+      ++my_cand;
+      my_top = max(my_top, float_to_ordered(x) >> kShift);
+    }
   }
-  for (int b = lane; b < 256; b += 32) sm.hist[warp][b] = 0;
+  for (int b = lane; b < 256; b += 32) sm.hist[warp][b] = 0u;
+  for (int w = tid; w < n_words; w += NT) bits[w] = 0u;
+  if (tid == 0) sm.ctrl[2] = 0;
   my_cand = __reduce_add_sync(0xffffffffu, my_cand);
-  my_forced = __reduce_add_sync(0xffffffffu, my_forced);
   my_top = __reduce_max_sync(0xffffffffu, my_top);
   if (lane == 0) {
-    sm.wcnt[warp][0] = my_cand;
-    sm.wcnt[warp][1] = my_forced;
-    sm.wcnt[warp][2] = static_cast<int>(my_top);
+    sm.wred[warp][0] = my_cand;
+    sm.wred[warp][1] = static_cast<int>(my_top);
   }
   __syncthreads();
-  int n_cand = 0, n_forced = 0;
+  int n_cand = 0;
   uint32_t top = 0;
-#pragma unroll
   for (int w = 0; w < NWARP; ++w) {
-    n_cand += sm.wcnt[w][0];
-    n_forced += sm.wcnt[w][1];
-    top = max(top, static_cast<uint32_t>(sm.wcnt[w][2]));
+    n_cand += sm.wred[w][0];
+    top = max(top, static_cast<uint32_t>(sm.wred[w][1]));
   }
-  int n_take = includes_forced ? topk - n_forced : topk;
-  if (n_take < 0) n_take = 0;
-
-  bool use_radix = false;
-  if (n_take > 0 && n_cand <= n_take) {
-    for (int j = lo; j < hi; ++j)
-      if (flag[j] == 1) flag[j] = 3;
-  } else if (n_take > 0) {
-    // 2. per-warp histograms of bins (0 = the best bin).
-    for (int j = lo; j < hi; ++j)
-      if (flag[j] == 1) atomicAdd(&sm.hist[warp][min(255u, top - (float_to_ordered(r[j]) >> kShift))], 1u);
-    __syncthreads();
-    // 3. boundary bin: the first whose cumulative count reaches n_take.
-    if (warp == 0) {
-      int cnt[8], tot = 0;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        int v = 0;
-#pragma unroll
-        for (int w = 0; w < NWARP; ++w) v += static_cast<int>(sm.hist[w][8 * lane + k]);
-        cnt[k] = v;
-        tot += v;
-      }
-      int run = warp_inclusive_scan(tot) - tot;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        if (run < n_take && run + cnt[k] >= n_take) {
-          sm.ctrl[3] = 8 * lane + k;      // boundary bin
-          sm.ctrl[4] = run + cnt[k];      // survivors
-        }
-        run += cnt[k];
-      }
+  const int n_forced = n_first + max(0, c - local_lo + 1);
+  const int n_take = max(0, includes_forced ? topk - n_forced : topk);
+  const bool take_all = n_take >= n_cand, take_none = n_take == 0;
+  // 2. thresholds over d = distance of the leading bits from the best (see
+  //    select_topk_bits): level 1 bins min(d, 255), level 2 splits bin 255.
+  int lvl = 0, bnd = 0, above = 0;
+  if (!take_all && !take_none) {
+#pragma unroll 1
+    for (int j = tid; j < nb; j += NT) {
+      const float x = r[j];
+      if (is_cand(j, x)) atomicAdd(&sm.hist[warp][min(255u, top - (float_to_ordered(x) >> kShift))], 1u);
     }
     __syncthreads();
-    const int bnd = sm.ctrl[3];
-    const int n_surv = sm.ctrl[4];
-    if (n_surv > NT) {
-      use_radix = true;
-    } else {
-      // 4. survivors into shared memory, positions from a prefix count.
-      int my_keep = 0;
-      for (int j = lo; j < hi; ++j)
-        my_keep += (flag[j] == 1 && static_cast<int>(min(255u, top - (float_to_ordered(r[j]) >> kShift))) <= bnd) ? 1 : 0;
-      int tot_keep;
-      int pos = group_exclusive_scan<NT, false>(my_keep, tot_keep, sm.radix, tid);
-      for (int j = lo; j < hi; ++j) {
-        if (flag[j] != 1) continue;
-        const uint32_t key = float_to_ordered(r[j]);
-        if (static_cast<int>(min(255u, top - (key >> kShift))) <= bnd)
-          sm.surv[pos++] = (static_cast<unsigned long long>(key) << 32) | static_cast<uint32_t>(~j);
+    bnd = smem_topk_boundary(sm, n_take, tid, &above);
+    lvl = 1;
+    if (bnd == 255 && n_cand - above > NT) {
+#pragma unroll 1
+      for (int j = tid; j < nb; j += NT) {
+        const float x = r[j];
+        const uint32_t d = top - (float_to_ordered(x) >> kShift);
+        if (is_cand(j, x) && d >= 255u) atomicAdd(&sm.hist[warp][min(255u, (d - 255u) >> 4)], 1u);
       }
       __syncthreads();
-      // 5. exact rank among the survivors; the best n_take are taken.
-      if (tid < n_surv) {
-        const unsigned long long me = sm.surv[tid];
-        int rank = 0;
-        int x = 0;
-        for (; x + 4 <= n_surv; x += 4) {
-          rank += (sm.surv[x] > me) + (sm.surv[x + 1] > me) + (sm.surv[x + 2] > me) + (sm.surv[x + 3] > me);
-        }
-        for (; x < n_surv; ++x) rank += (sm.surv[x] > me) ? 1 : 0;
-        if (rank < n_take) flag[static_cast<int>(~static_cast<uint32_t>(me & 0xffffffffu))] = 3;
+      int above2 = 0;
+      bnd = smem_topk_boundary(sm, n_take - above, tid, &above2);
+      above += above2;
+      lvl = 2;
+    }
+  }
+  // 3. mark the taken candidates and the forced blocks; collect the boundary.
+  if (!take_none) {
+#pragma unroll 1
+    for (int j = tid; j < nb; j += NT) {
+      const float x = r[j];
+      if (!is_cand(j, x)) continue;
+      const uint32_t key = float_to_ordered(x);
+      const uint32_t d = top - (key >> kShift);
+      int dd = static_cast<int>(min(255u, d));
+      if (lvl == 2) dd = d < 255u ? -1 : static_cast<int>(min(255u, (d - 255u) >> 4));
+      if (lvl == 0 || dd < bnd) {
+        atomicOr(&bits[j >> 5], 1u << (j & 31));
+      } else if (dd == bnd) {
+        surv[atomicAdd(&sm.ctrl[2], 1)] = (static_cast<unsigned long long>(key) << 32) | static_cast<uint32_t>(~j);
       }
     }
   }
-  if (use_radix) {   // uniform: every thread saw the same n_surv
-    __syncthreads();
-    select_topk<NT, false>(r, flag, nb, n_init, n_local, topk, includes_forced, k_max, out_idx, out_n, sm.radix,
-                           tid);
-    return;
-  }
+  for (int j = tid; j < n_first; j += NT) atomicOr(&bits[j >> 5], 1u << (j & 31));
+  for (int j = local_lo + tid; j <= c; j += NT) atomicOr(&bits[j >> 5], 1u << (j & 31));
   __syncthreads();
-  // 6. ascending output of forced + taken blocks.
-  int my_sel = 0;
-  for (int j = lo; j < hi; ++j) my_sel += (flag[j] >= 2) ? 1 : 0;
-  int total;
-  int pos = group_exclusive_scan<NT, false>(my_sel, total, sm.radix, tid);
-  for (int j = lo; j < hi; ++j) {
-    if (flag[j] >= 2) {
-      if (pos < k_max) out_idx[pos] = j;
-      ++pos;
+  // 4. the boundary entries that still fit, by exact rank among themselves.
+  if (lvl > 0) {
+    const int m = sm.ctrl[2];
+    const int need = n_take - above;
+#pragma unroll 1
+    for (int x = tid; x < m; x += NT) {
+      const unsigned long long me = surv[x];
+      int rk = 0;
+#pragma unroll 1
+      for (int y = 0; y < m; ++y) rk += (surv[y] > me) ? 1 : 0;
+      if (rk < need) {
+        const int j = static_cast<int>(~static_cast<uint32_t>(me & 0xffffffffu));
+        atomicOr(&bits[j >> 5], 1u << (j & 31));
+      }
     }
+    __syncthreads();
   }
-  for (int p = total + tid; p < k_max; p += NT) out_idx[p] = -1;
-  if (tid == 0) *out_n = min(total, k_max);
+  // 5. ascending output from the bitmask (one warp, one 32-word slice per pass).
+  if (warp == 0) {
+    int base = 0;
+#pragma unroll 1
+    for (int w0 = 0; w0 < n_words; w0 += 32) {
+      uint32_t bw = (w0 + lane < n_words) ? bits[w0 + lane] : 0u;
+      const int cnt = __popc(bw);
+      const int incl = warp_inclusive_scan(cnt);
+      int pos = base + incl - cnt;
+      while (bw) {
+        const int j = (w0 + lane) * 32 + __ffs(bw) - 1;
+        bw &= bw - 1u;
+        if (pos < k_max) {
+          out_idx[pos] = j;
+          if (sorted_copy) sorted_copy[pos] = j;
+        }
+        ++pos;
+      }
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    const int total = min(base, k_max);
+    for (int x = total + lane; x < k_max; x += 32) {
+      out_idx[x] = -1;
+      if (sorted_copy) sorted_copy[x] = -1;
+    }
+    if (lane == 0) *out_n = total;
+  }
 }
 
 }  // namespace infllmv2
