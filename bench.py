@@ -234,6 +234,16 @@ class DecodeBench:
                 "step": comp_b + kc_b + q_b * 2 + kv_b + idx_b}
 
 
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """The largest of every rank's value (the job's time is its slowest rank's)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def S_n_c(L, p=32, s=16):
     return (L - p) // s + 1 if L >= p else 0
 
@@ -482,11 +492,7 @@ def main():
     if dist:
         dist.barrier()
     clk = clocks.stop()
-    t = e0.elapsed_time(e1) * 1e-3
-    if dist:
-        tt = torch.tensor([t], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t = float(tt.item())
+    t = max_over_ranks(e0.elapsed_time(e1) * 1e-3, dist, dev)
     assert T.get_device_status(clear=True) == 0, "device status flagged during the bench"
 
     # End to end through the public API with host buffers: per step the new
@@ -520,11 +526,7 @@ def main():
         e2e_step(i)
     f1.record()
     torch.cuda.synchronize()
-    t_e2e = f0.elapsed_time(f1) * 1e-3
-    if dist:
-        tt = torch.tensor([t_e2e], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_e2e = float(tt.item())
+    t_e2e = max_over_ranks(f0.elapsed_time(f1) * 1e-3, dist, dev)
 
     prefill = None
     if not args.no_prefill and rank == 0:
