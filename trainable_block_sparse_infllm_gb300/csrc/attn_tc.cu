@@ -8,19 +8,32 @@
 // token did not select a block get probability 0 for it, so every row's
 // result is exactly its own block-sparse attention.
 //
-// Roles (192 threads):
-//   warps 0-3  softmax: thread r owns row r (token r / 16, head r % 16);
-//              reads S from TMEM, online softmax in fp32 base 2 with a lazy
-//              rescale (the running max only moves when it grows by more
-//              than 2^8, which keeps exp2(s - m) <= 256), writes P (bf16,
-//              128-byte swizzled, K-major) to shared memory, rescales its O
-//              row in TMEM when needed, and finally writes out / lse.
-//   warp 4     TMA producer: Q tile once, then K and V tiles of each union
-//              block into a 3-stage ring.
-//   warp 5     MMA issuer (one thread): S_n = Q K_n^T (M 128, N 64, K 128)
-//              into one of two TMEM S buffers, then O += P_{n-1} V_{n-1}
-//              (M 128, N 128, K 64) with V as an MN-major operand.
-// TMEM: columns [0,128) two S buffers, [128,256) the O accumulator.
+// The union is walked two blocks (128 keys) per item: S = Q K^T is one
+// N = 128 product per item and O += P V one K = 128 product, which halves
+// the serial work of the issuing thread per key.
+//
+// Roles (352 threads):
+//   warps 0-7  softmax: row r = 32 (w % 4) + lane (token r / 16, head r % 16)
+//              is shared by warps w % 4 and w % 4 + 4, which take the
+//              item's first and second block (S columns 0-63 / 64-127) and
+//              O columns 0-63 / 64-127; they agree on the row's running max
+//              through shared memory.  Online softmax in fp32 base 2 with a
+//              lazy rescale (the running max only moves when it grows by
+//              more than 2^8, which keeps exp2(s - m) <= 256); P (bf16
+//              pairs) goes to TMEM; O rows are rescaled in TMEM when needed.
+//              Probabilities are computed while the previous P V product
+//              runs; a warp whose two tokens both skipped its block only
+//              writes zeros.
+//   warp 8     MMA issuer (one thread): S_i = Q K_i^T (M 128, N 128, K 128,
+//              both operands in shared memory) into one of two TMEM S
+//              buffers, then O += P_{i-1} V_{i-1} (M 128, N 128, K 128; P
+//              from TMEM, V an MN-major shared operand).
+//   warp 9     TMA producer: the Q tile, then each item's two K tiles into a
+//              3-stage ring (a stage frees once S is computed).
+//   warp 10    TMA producer: each item's two V tiles into a 2-stage ring (a
+//              stage frees once its P V product is done).
+// TMEM: columns [0,256) two S buffers, [256,384) the O accumulator,
+// [384,512) two P buffers.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -30,9 +43,16 @@ namespace infllmv2 {
 namespace {
 
 constexpr int kTcTokens = 8;
-constexpr int kTcStages = 3;
-constexpr int kTcThreads = 192;
-constexpr uint32_t kTmemCols = 256;
+constexpr int kTcKStages = 3;   // K tiles of an item (32 KB): freed as soon as S = Q K^T is done
+constexpr int kTcVStages = 2;   // V tiles of an item (32 KB): freed when O += P V is done
+constexpr int kTcItemBytes = 32768;
+constexpr int kTcSoftmaxWarps = 8;   // two per TMEM lane quadrant, 32 of the 64 S columns each
+constexpr int kTcThreads = (kTcSoftmaxWarps + 3) * 32;
+constexpr int kTcMmaWarp = kTcSoftmaxWarps, kTcTmaWarp = kTcSoftmaxWarps + 1, kTcVWarp = kTcSoftmaxWarps + 2;
+constexpr uint32_t kTmemCols = 512;
+// TMEM columns: two S buffers (128 keys each), the O accumulator and two P
+// buffers (bf16 pairs, one row per lane: the A operand of O += P V).
+constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
 constexpr float kLazyRescale = 8.0f;
 
 struct TcParams {
@@ -47,26 +67,56 @@ struct TcParams {
 };
 
 struct TcLayout {
-  int q, kv, p, bars, slot, bits, ulist, umask, scan, total;
+  int q, kv, vv, bars, slot, bits, ulist, umask, scan, xch, total;
 };
 
 __host__ __device__ inline TcLayout tc_layout(int nbmax) {
   TcLayout l;
   l.q = 0;                                   // 2 boxes x 128 rows x 128 B
-  l.kv = 32768;                              // stages x (K 16 KB + V 16 KB)
-  l.p = l.kv + kTcStages * 32768;            // 2 x 16 KB
-  l.bars = l.p + 2 * 16384;                  // 32 mbarriers max
+  l.kv = 32768;                              // K ring
+  l.vv = l.kv + kTcKStages * kTcItemBytes;   // V ring
+  l.bars = l.vv + kTcVStages * kTcItemBytes; // 32 mbarriers max
   l.slot = l.bars + 32 * 8;
   l.bits = l.slot + 16;
   l.ulist = l.bits + ((nbmax + 15) & ~15);
   l.umask = l.ulist + nbmax * 4;
   l.scan = l.umask + ((nbmax + 15) & ~15);
-  l.total = l.scan + 64;
+  l.xch = l.scan + 64;                       // [2 column halves][128 rows] fp32 exchange
+  l.total = l.xch + 2 * 128 * 4;
   return l;
 }
 
-enum Bar { kQFull = 0, kKvFull = 1, kKvEmpty = kKvFull + kTcStages, kSFull = kKvEmpty + kTcStages,
-           kSFree = kSFull + 2, kPFull = kSFree + 2, kODone = kPFull + 2, kNumBars = kODone + 1 };
+// kODone + (m & 1) completes when O += P_m V_m has finished, so the softmax
+// warps can wait for the P-V product two blocks back (whose P buffer they
+// reuse) without waiting for the one in flight.
+// Barrier of the two softmax warps of TMEM lane quadrant q (ids 1..4).
+__device__ __forceinline__ void pair_sync(int q) {
+  asm volatile("bar.sync %0, 64;" ::"r"(q + 1) : "memory");
+}
+
+// 2^x on the FMA pipe, for x <= 9 (probabilities after the lazy rescale):
+// x = n + f with n = rint(x), |f| <= 1/2, and 2^f = e^(f ln 2) by its Taylor
+// series to degree 5 (relative error below 4e-6 for |f| <= 1/2), scaled by 2^n
+// through the exponent field; x < -125 (and x = -inf) gives 0.
+__device__ __forceinline__ float exp2_fma(float x) {
+  x = fmaxf(x, -127.f);
+  const float n = rintf(x);
+  const float f = x - n;
+  constexpr float c1 = 0.6931471805599453f, c2 = 0.2402265069591007f, c3 = 0.05550410866482158f;
+  constexpr float c4 = 0.009618129107628477f, c5 = 0.0013333558146428443f;
+  float y = fmaf(c5, f, c4);
+  y = fmaf(y, f, c3);
+  y = fmaf(y, f, c2);
+  y = fmaf(y, f, c1);
+  y = fmaf(y, f, 1.0f);
+  const int e = static_cast<int>(n);
+  return e < -125 ? 0.f : __int_as_float(__float_as_int(y) + (e << 23));
+}
+
+enum Bar { kQFull = 0, kKFull = 1, kKEmpty = kKFull + kTcKStages, kVFull = kKEmpty + kTcKStages,
+           kVEmpty = kVFull + kTcVStages, kSFull = kVEmpty + kTcVStages, kSFree = kSFull + 2,
+           kPFull = kSFree + 2, kODone = kPFull + 2, kNumBars = kODone + 2 };
+static_assert(kNumBars <= 32, "barrier area holds 32");
 
 __global__ void __launch_bounds__(kTcThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
@@ -141,7 +191,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
     __syncthreads();
-    if (tid == 0) scan[8] = tot;
+    if (tid == 0) scan[15] = tot;
   }
 
   if (tid == 0) {
@@ -149,19 +199,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     prefetch_tensormap(&k_map);
     prefetch_tensormap(&v_map);
     mbar_init(&bars[kQFull], 1);
-    for (int s = 0; s < kTcStages; ++s) {
-      mbar_init(&bars[kKvFull + s], 1);
-      mbar_init(&bars[kKvEmpty + s], 1);
+    for (int s = 0; s < kTcKStages; ++s) {
+      mbar_init(&bars[kKFull + s], 1);
+      mbar_init(&bars[kKEmpty + s], 1);
+    }
+    for (int s = 0; s < kTcVStages; ++s) {
+      mbar_init(&bars[kVFull + s], 1);
+      mbar_init(&bars[kVEmpty + s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars[kSFull + s], 1);
-      mbar_init(&bars[kSFree + s], 4);
-      mbar_init(&bars[kPFull + s], 4);
+      mbar_init(&bars[kSFree + s], kTcSoftmaxWarps);
+      mbar_init(&bars[kPFull + s], kTcSoftmaxWarps);
     }
     mbar_init(&bars[kODone], 1);
+    mbar_init(&bars[kODone + 1], 1);
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == kTcMmaWarp) {
     tc::tmem_alloc(tmem_slot, kTmemCols);
     tc::tmem_relinquish();
   }
@@ -169,13 +224,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  const int nu = scan[8];
+  const int nu = scan[15];
+  const int nit = (nu + 1) / 2;   // items of two union blocks (the last may hold one)
   const uint32_t q_s = smem_u32(smem + lay.q);
   const uint32_t kv_s = smem_u32(smem + lay.kv);
-  const uint32_t p_s = smem_u32(smem + lay.p);
+  const uint32_t vv_s = smem_u32(smem + lay.vv);
+  // Block of slot `half` of item `it` (a missing second block repeats the
+  // first one's tiles and is masked out).
+  auto item_block = [&](int it, int half) { return ulist[min(2 * it + half, nu - 1)]; };
 
-  if (warp == 4) {
+  if (warp == kTcTmaWarp) {
     // ------------------------------------------------------- TMA producer
+    // Q and the K ring here; the V ring has a warp of its own, so neither
+    // producer's waits hold up the other.  An item's stage holds, per
+    // 64-column box, 128 rows: the first block's keys then the second's.
     if (lane == 0 && nu > 0) {
       mbar_arrive_expect_tx(&bars[kQFull], n_act * 4096);
       for (int tok = 0; tok < n_act; ++tok) {
@@ -183,106 +245,159 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tma_load_2d(smem + lay.q + tok * 2048, &q_map, 0, row, &bars[kQFull]);
         tma_load_2d(smem + lay.q + 16384 + tok * 2048, &q_map, 64, row, &bars[kQFull]);
       }
-      for (int n = 0; n < nu; ++n) {
-        const int st = n % kTcStages;
-        if (n >= kTcStages && !mbar_wait(&bars[kKvEmpty + st], ((n / kTcStages) - 1) & 1, p.status)) break;
-        const int row = bh * p.Lmax + ulist[n] * kBlock;
-        uint8_t* dst = smem + lay.kv + st * 32768;
-        mbar_arrive_expect_tx(&bars[kKvFull + st], 32768);
-        tma_load_2d(dst, &k_map, 0, row, &bars[kKvFull + st]);
-        tma_load_2d(dst + 8192, &k_map, 64, row, &bars[kKvFull + st]);
-        tma_load_2d(dst + 16384, &v_map, 0, row, &bars[kKvFull + st]);
-        tma_load_2d(dst + 24576, &v_map, 64, row, &bars[kKvFull + st]);
+      for (int it = 0; it < nit; ++it) {
+        const int st = it % kTcKStages;
+        if (it >= kTcKStages && !mbar_wait(&bars[kKEmpty + st], ((it / kTcKStages) - 1) & 1, p.status)) break;
+        uint8_t* dst = smem + lay.kv + st * kTcItemBytes;
+        mbar_arrive_expect_tx(&bars[kKFull + st], kTcItemBytes);
+        for (int hf = 0; hf < 2; ++hf) {
+          const int row = bh * p.Lmax + item_block(it, hf) * kBlock;
+          tma_load_2d(dst + hf * 8192, &k_map, 0, row, &bars[kKFull + st]);
+          tma_load_2d(dst + 16384 + hf * 8192, &k_map, 64, row, &bars[kKFull + st]);
+        }
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == kTcVWarp) {
+    // ------------------------------------------------------- V producer
+    if (lane == 0 && nu > 0) {
+      for (int it = 0; it < nit; ++it) {
+        const int st = it % kTcVStages;
+        if (it >= kTcVStages && !mbar_wait(&bars[kVEmpty + st], ((it / kTcVStages) - 1) & 1, p.status)) break;
+        uint8_t* dst = smem + lay.vv + st * kTcItemBytes;
+        mbar_arrive_expect_tx(&bars[kVFull + st], kTcItemBytes);
+        for (int hf = 0; hf < 2; ++hf) {
+          const int row = bh * p.Lmax + item_block(it, hf) * kBlock;
+          tma_load_2d(dst + hf * 8192, &v_map, 0, row, &bars[kVFull + st]);
+          tma_load_2d(dst + 16384 + hf * 8192, &v_map, 64, row, &bars[kVFull + st]);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kTcMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0 && nu > 0) {
-      constexpr uint32_t kIdS = tc::idesc_bf16(128, 64, 0, 0);
+      constexpr uint32_t kIdS = tc::idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t kIdO = tc::idesc_bf16(128, 128, 0, 1);
+      // Base descriptors; a tile offset is added to the 16-byte address field.
+      const uint64_t q_desc0 = tc::sdesc_sw128(q_s, 16, 1024);
+      const uint64_t k_desc0 = tc::sdesc_sw128(kv_s, 16, 1024);
+      const uint64_t v_desc0 = tc::sdesc_sw128(vv_s, 16384, 1024);
       bool ok = mbar_wait(&bars[kQFull], 0, p.status);
-      for (int n = 0; n <= nu && ok; ++n) {
-        if (n < nu) {
-          const int st = n % kTcStages, sb = n & 1;
-          ok = mbar_wait(&bars[kKvFull + st], (n / kTcStages) & 1, p.status);
-          if (ok && n >= 2) ok = mbar_wait(&bars[kSFree + sb], ((n >> 1) - 1) & 1, p.status);
+      for (int it = 0; it <= nit && ok; ++it) {
+        if (it < nit) {
+          const int st = it % kTcKStages, sb = it & 1;
+          ok = mbar_wait(&bars[kKFull + st], (it / kTcKStages) & 1, p.status);
+          if (ok && it >= 2) ok = mbar_wait(&bars[kSFree + sb], ((it >> 1) - 1) & 1, p.status);
           if (!ok) break;
           tc::fence_after_sync();
-          const uint32_t kb = kv_s + st * 32768;
+          const uint64_t kd = k_desc0 + static_cast<uint64_t>(st * (kTcItemBytes >> 4));
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const uint64_t ad = tc::sdesc_sw128(q_s + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
-            const uint64_t bd = tc::sdesc_sw128(kb + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024);
-            tc::mma_ss(tmem + sb * 64, ad, bd, kIdS, k > 0 ? 1u : 0u);
+            const uint64_t off = static_cast<uint64_t>(((k >> 2) * 16384 + (k & 3) * 32) >> 4);
+            tc::mma_ss(tmem + kColS + sb * 128, q_desc0 + off, kd + off, kIdS, k > 0 ? 1u : 0u);
           }
           tc::commit(&bars[kSFull + sb]);
+          tc::commit(&bars[kKEmpty + st]);
         }
-        if (n >= 1) {
-          const int m = n - 1, pb = m & 1, st = m % kTcStages;
+        if (it >= 1) {
+          const int m = it - 1, pb = m & 1, st = m % kTcVStages;
           if (!mbar_wait(&bars[kPFull + pb], (m >> 1) & 1, p.status)) break;
+          if (!mbar_wait(&bars[kVFull + st], (m / kTcVStages) & 1, p.status)) break;
           tc::fence_after_sync();
-          const uint32_t vb = kv_s + st * 32768 + 16384;
+          const uint64_t vd = v_desc0 + static_cast<uint64_t>(st * (kTcItemBytes >> 4));
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t ad = tc::sdesc_sw128(p_s + pb * 16384 + k * 32, 16, 1024);
-            const uint64_t bd = tc::sdesc_sw128(vb + k * 2048, 8192, 1024);
-            tc::mma_ss(tmem + 128, ad, bd, kIdO, (m > 0 || k > 0) ? 1u : 0u);
-          }
-          tc::commit(&bars[kODone]);
-          tc::commit(&bars[kKvEmpty + st]);
+          for (int k = 0; k < 8; ++k)
+            tc::mma_ts(tmem + kColO, tmem + kColP + pb * 64 + 8 * k, vd + static_cast<uint64_t>((k * 2048) >> 4),
+                       kIdO, (m > 0 || k > 0) ? 1u : 0u);
+          tc::commit(&bars[kODone + (m & 1)]);
+          tc::commit(&bars[kVEmpty + st]);
         }
       }
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
-    const int r = tid;              // TMEM lane == MMA row
+    // Warp w: TMEM lane quadrant w % 4 (rows 32 (w % 4) + lane); slot
+    // `half` = w / 4 of each item (S columns [64 half, 64 half + 64)) and O
+    // columns [64 half, 64 half + 64).  The two warps of a quadrant agree
+    // on each row's running max through shared memory; each keeps its own
+    // partial row sum.
+    const int quad = warp & 3, half = warp >> 2;
+    const int r = quad * 32 + lane;   // TMEM lane == MMA row
     const int tok = r >> 4;
     const bool active = tok < n_act;
     const int i_row = L - p.nq + t0 + tok;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    float* xch = reinterpret_cast<float*>(smem + lay.xch);   // [half][row]
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    uint8_t* prow_base = smem + lay.p + (r >> 3) * 1024 + (r & 7) * 128;
-    for (int n = 0; n < nu; ++n) {
-      const int sb = n & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars[kSFull + sb], (n >> 1) & 1, p.status));
-      if (!ok) break;
+    for (int it = 0; it < nit; ++it) {
+      const int sb = it & 1;
+      const int u = 2 * it + half;            // this warp's union slot
+      const bool present = u < nu;
+      const bool sel = present && active && ((umask[u] >> tok) & 1);
+      const bool warp_sel = __any_sync(0xffffffffu, sel);
+      // No early exit from this loop: both warps of a quadrant must meet the
+      // same pair barriers, so after a failed (timed-out) wait the warp keeps
+      // going without waiting and the status word carries the error.
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars[kSFull + sb], (it >> 1) & 1, p.status));
       tc::fence_after_sync();
       uint32_t s[64];
-      tc::ld32(lane_addr + sb * 64, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-      tc::ld32(lane_addr + sb * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-      tc::wait_ld();
+      if (warp_sel) {   // a warp none of whose tokens picked its block skips its scores
+        tc::ld32(lane_addr + kColS + sb * 128 + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+        tc::ld32(lane_addr + kColS + sb * 128 + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+        tc::wait_ld();
+      }
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kSFree + sb]);
 
-      const bool sel = active && ((umask[n] >> tok) & 1);
-      const int key0 = ulist[n] * kBlock;
+      // The stage slot holds this block's tiles (a repeat of the item's
+      // first block when the item has only one).
+      const int key0 = item_block(it, half) * kBlock;
       if (key0 + kBlock > L) {
         // The block holds cache rows past kv_len: clear their V rows so a
         // zero probability never multiplies a non-finite value.
-        const int st = n % kTcStages;
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars[kKvFull + st], (n / kTcStages) & 1, p.status));
-        if (!ok) break;
-        uint8_t* vt = smem + lay.kv + st * 32768 + 16384;
+        const int st = it % kTcVStages;
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars[kVFull + st], (it / kTcVStages) & 1, p.status));
+        uint8_t* vt = smem + lay.vv + st * kTcItemBytes + half * 8192;
         const int r0 = L - key0;
-        for (int e = tid; e < (kBlock - r0) * 16; e += 128) {
+        for (int e = lane; e < (kBlock - r0) * 16; e += 32) {
           const int row = r0 + (e >> 4), q16 = e & 15;
-          *reinterpret_cast<uint4*>(vt + (q16 >> 3) * 8192 + row * 128 + (q16 & 7) * 16) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vt + (q16 >> 3) * 16384 + row * 128 + (q16 & 7) * 16) = make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
       }
-      const int nvalid = sel ? min(kBlock, i_row - key0 + 1) : 0;   // keys key0 .. key0+nvalid-1
+      const int nv = sel ? min(kBlock, i_row - key0 + 1) : 0;   // keys key0 .. key0 + nv - 1
+      // Rows see the whole block or none of it except on a token's own
+      // diagonal block; the common case needs no per-key mask.
+      const bool whole = __all_sync(0xffffffffu, nv == 0 || nv == kBlock);
       float mx = -INFINITY;
+      if (warp_sel) {
+        if (whole) {
+          float m0 = __uint_as_float(s[0]), m1 = __uint_as_float(s[1]);
 #pragma unroll
-      for (int x = 0; x < 64; ++x)
-        if (x < nvalid) mx = fmaxf(mx, __uint_as_float(s[x]) * p.scale2);
+          for (int x = 2; x < 64; x += 2) {
+            m0 = fmaxf(m0, __uint_as_float(s[x]));
+            m1 = fmaxf(m1, __uint_as_float(s[x + 1]));
+          }
+          if (sel) mx = fmaxf(m0, m1) * p.scale2;
+        } else {
+#pragma unroll
+          for (int x = 0; x < 64; ++x)
+            if (x < nv) mx = fmaxf(mx, __uint_as_float(s[x]) * p.scale2);
+        }
+      }
+      xch[half * 128 + r] = mx;
+      pair_sync(quad);
+      mx = fmaxf(mx, xch[(half ^ 1) * 128 + r]);
+      // Either warp may have selected; both follow the row's combined max.
+      const bool row_sel = mx > -INFINITY;
       bool need = false;
       float alpha = 1.f;
       float m_use = m_run;
-      if (sel) {
+      if (row_sel) {
         if (m_run == -INFINITY) {
           m_use = mx;
         } else if (mx > m_run + kLazyRescale) {
@@ -291,81 +406,110 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           m_use = mx;
         }
       }
-      if (n >= 1) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars[kODone], (n - 1) & 1, p.status));
-        if (!ok) break;
-        tc::fence_after_sync();
+      uint32_t w[32];   // this warp's 64 probabilities of the row, bf16 pairs
+      float lsum = 0.f;
+      if (warp_sel) {
+        // Probabilities before waiting on the tensor core: only the P store
+        // and an O rescale depend on earlier products.  Three in eight go
+        // through the FMA pipe to share the load with the MUFU unit.
+        if (whole) {
+          // A row that skipped the block subtracts +inf: every exp2 is 0.
+          const float m_eff = sel ? m_use : INFINITY;
+          float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+          for (int x = 0; x < 32; ++x) {
+            const float a0 = fmaf(__uint_as_float(s[2 * x]), p.scale2, -m_eff);
+            const float a1 = fmaf(__uint_as_float(s[2 * x + 1]), p.scale2, -m_eff);
+            const float p0 = ((x & 3) == 3) ? exp2_fma(a0) : fast_exp2(a0);
+            const float p1 = ((x & 3) != 0) ? exp2_fma(a1) : fast_exp2(a1);
+            ls0 += p0;
+            ls1 += p1;
+            w[x] = pack_bf16x2(p0, p1);
+          }
+          lsum = ls0 + ls1;
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) {
+            const float a0 = __uint_as_float(s[2 * x]) * p.scale2 - m_use;
+            const float a1 = __uint_as_float(s[2 * x + 1]) * p.scale2 - m_use;
+            const float p0 = (2 * x < nv) ? fast_exp2(a0) : 0.f;
+            const float p1 = (2 * x + 1 < nv) ? fast_exp2(a1) : 0.f;
+            lsum += p0 + p1;
+            w[x] = pack_bf16x2(p0, p1);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int x = 0; x < 32; ++x) w[x] = 0u;
       }
+      // P buffer it & 1 was last read by the product of item it - 2.
+      if (it >= 2 && ok)
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars[kODone + (it & 1)], ((it - 2) >> 1) & 1, p.status));
       if (__any_sync(0xffffffffu, need)) {
+        // A rescale touches O: the product of item it - 1 must be done too.
+        if (it >= 1 && ok)
+          ok = __all_sync(0xffffffffu, mbar_wait(&bars[kODone + ((it - 1) & 1)], ((it - 1) >> 1) & 1, p.status));
+        tc::fence_after_sync();
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t o[32];
-          tc::ld32(lane_addr + 128 + c * 32, o);
+          tc::ld32(lane_addr + kColO + half * 64 + c * 32, o);
           tc::wait_ld();
 #pragma unroll
           for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
-          tc::st32(lane_addr + 128 + c * 32, o);
+          tc::st32(lane_addr + kColO + half * 64 + c * 32, o);
         }
         tc::wait_st();
       }
-      l_run *= alpha;
+      l_run = l_run * alpha + lsum;
       m_run = m_use;
-      // P row (bf16) into the swizzled K-major tile of this block's buffer.
-      uint8_t* prow = prow_base + (n & 1) * 16384;
-      float lsum = 0.f;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int x0 = c * 8 + 2 * e;
-          const float p0 = (x0 < nvalid) ? fast_exp2(__uint_as_float(s[x0]) * p.scale2 - m_run) : 0.f;
-          const float p1 = (x0 + 1 < nvalid) ? fast_exp2(__uint_as_float(s[x0 + 1]) * p.scale2 - m_run) : 0.f;
-          lsum += p0 + p1;
-          w[e] = pack_bf16x2(p0, p1);
-        }
-        *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-      l_run += lsum;
-      fence_proxy_async_smem();
+      // This warp's 64 probabilities (32 bf16 pairs) into the row's lane of
+      // this item's P buffer in TMEM (keys 64 half .. 64 half + 63).
+      tc::st32(lane_addr + kColP + (it & 1) * 64 + 32 * half, w);
+      tc::wait_st();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kPFull + (n & 1)]);
+      if (lane == 0) mbar_arrive(&bars[kPFull + (it & 1)]);
     }
     // ---- epilogue: O / l -> bf16 out, lse ----
-    if (nu > 0 && ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars[kODone], (nu - 1) & 1, p.status));
+    if (nit > 0 && ok)
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars[kODone + ((nit - 1) & 1)], ((nit - 1) >> 1) & 1, p.status));
     tc::fence_after_sync();
-    const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+    xch[half * 128 + r] = l_run;
+    pair_sync(quad);
+    const float l_row = l_run + xch[(half ^ 1) * 128 + r];
+    const float inv = (l_row > 0.f) ? 1.f / l_row : 0.f;
     __nv_bfloat16* orow = p.out + ((static_cast<size_t>(b) * p.nq + t0 + tok) * Hq + h * kGroup + (r & 15)) * kHeadDim;
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < 2; ++c) {
+      const int col = half * 64 + c * 32;
       uint32_t o[32];
-      if (nu > 0) {
-        tc::ld32(lane_addr + 128 + c * 32, o);
+      if (nit > 0) {
+        tc::ld32(lane_addr + kColO + col, o);
         tc::wait_ld();
       } else {
 #pragma unroll
         for (int x = 0; x < 32; ++x) o[x] = 0u;
       }
       if (active) {
-        uint32_t w[16];
+        uint32_t wo[16];
 #pragma unroll
         for (int x = 0; x < 16; ++x)
-          w[x] = pack_bf16x2(__uint_as_float(o[2 * x]) * inv, __uint_as_float(o[2 * x + 1]) * inv);
-        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+          wo[x] = pack_bf16x2(__uint_as_float(o[2 * x]) * inv, __uint_as_float(o[2 * x + 1]) * inv);
+        uint4* dst = reinterpret_cast<uint4*>(orow + col);
 #pragma unroll
-        for (int x = 0; x < 4; ++x) dst[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+        for (int x = 0; x < 4; ++x) dst[x] = make_uint4(wo[4 * x], wo[4 * x + 1], wo[4 * x + 2], wo[4 * x + 3]);
       }
     }
-    if (active && p.lse) {
+    if (active && half == 0 && p.lse) {
       p.lse[(static_cast<size_t>(b) * p.nq + t0 + tok) * Hq + h * kGroup + (r & 15)] =
-          (l_run > 0.f) ? (m_run + fast_log2(l_run)) * 0.69314718055994531f : -INFINITY;
+          (l_row > 0.f) ? (m_run + fast_log2(l_row)) * 0.69314718055994531f : -INFINITY;
     }
   }
 
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kTcMmaWarp) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
