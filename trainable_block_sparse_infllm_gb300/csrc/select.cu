@@ -171,20 +171,52 @@ __global__ void __launch_bounds__(kPrefTokens * 32)
     if (active && kbase < nvis_t) {
       const uint32_t hi_b = smem_u32(smem + lay.stage_off + stage * kPrefStageBytes);
       const uint32_t lo_b = hi_b + 16384;
-#pragma unroll 2
+      // All eight n-tiles' scores first (independent MMA chains), then the
+      // exponentials; only the chunk holding the last visible kernel masks.
+      float x[8][4];
+#pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
         float acc[4];
         score_ntile(acc, a, hi_b, lo_b, nt * 8, kPrefChunk, lane);
-        const int kj = kbase + nt * 8 + 2 * tq;
-        const bool v0 = kj < nvis_t, v1 = kj + 1 < nvis_t;
-        const float x0 = acc[0] * p.scale2, x1 = acc[1] * p.scale2;
-        const float x2 = acc[2] * p.scale2, x3 = acc[3] * p.scale2;
-        if (pass == 0) {
-          lse_add2(m0, l0, v0 ? x0 : -INFINITY, v1 ? x1 : -INFINITY);
-          lse_add2(m1, l1, v0 ? x2 : -INFINITY, v1 ? x3 : -INFINITY);
-        } else {
-          float s0 = (v0 ? fast_exp2(x0 - lse_g) : 0.f) + (v0 ? fast_exp2(x2 - lse_g8) : 0.f);
-          float s1 = (v1 ? fast_exp2(x1 - lse_g) : 0.f) + (v1 ? fast_exp2(x3 - lse_g8) : 0.f);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[nt][e] = acc[e] * p.scale2;
+      }
+      if (kbase + kPrefChunk > nvis_t) {
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+          const int kj = kbase + nt * 8 + 2 * tq;
+          if (kj >= nvis_t) x[nt][0] = x[nt][2] = -INFINITY;
+          if (kj + 1 >= nvis_t) x[nt][1] = x[nt][3] = -INFINITY;
+        }
+      }
+      if (pass == 0) {
+        // Chunk maxima, then one rescale of the running sums per chunk.
+        float c0 = x[0][0], c1 = x[0][2];
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+          c0 = fmaxf(c0, fmaxf(x[nt][0], x[nt][1]));
+          c1 = fmaxf(c1, fmaxf(x[nt][2], x[nt][3]));
+        }
+        const float M0 = fmaxf(m0, c0), M1 = fmaxf(m1, c1);
+        if (M0 > -INFINITY) {
+          float s0 = l0 * fast_exp2(m0 - M0);
+#pragma unroll
+          for (int nt = 0; nt < 8; ++nt) s0 += fast_exp2(x[nt][0] - M0) + fast_exp2(x[nt][1] - M0);
+          l0 = s0;
+          m0 = M0;
+        }
+        if (M1 > -INFINITY) {
+          float s1 = l1 * fast_exp2(m1 - M1);
+#pragma unroll
+          for (int nt = 0; nt < 8; ++nt) s1 += fast_exp2(x[nt][2] - M1) + fast_exp2(x[nt][3] - M1);
+          l1 = s1;
+          m1 = M1;
+        }
+      } else {
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+          float s0 = fast_exp2(x[nt][0] - lse_g) + fast_exp2(x[nt][2] - lse_g8);
+          float s1 = fast_exp2(x[nt][1] - lse_g) + fast_exp2(x[nt][3] - lse_g8);
 #pragma unroll
           for (int o = 4; o <= 16; o <<= 1) {
             s0 += __shfl_xor_sync(0xffffffffu, s0, o);
