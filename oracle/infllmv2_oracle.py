@@ -31,6 +31,12 @@ blocks.  Readings of points the pages leave open:
 * R6  equal scores are ordered by the lower block index.
 * R7  the query at position i attends key i itself (inclusive causal mask);
       query t of n_q sits at position L - n_q + t.
+* R10 (approximation, off by default) the coarse kernels of the LSE
+      approximation are the means of non-overlapping windows of s_c keys;
+      one is visible to query i once all its keys are <= i; their LSE
+      replaces the fine one as each head's normaliser (a count correction
+      would shift every head by the same constant and change no selection);
+      before the first coarse kernel is complete the exact LSE is kept.
 """
 
 from __future__ import annotations
@@ -54,6 +60,8 @@ class Settings:
     includes_forced: bool = True
     score_scale: float | None = None   # None -> 1/sqrt(d)
     attn_scale: float | None = None    # None -> 1/sqrt(d)
+    coarse: int = 0          # s_c: 0 = exact LSE; else the LSE over coarse kernels of
+                             # s_c keys [InfLLM v2 › Efficient LSE approximation]
 
     def sscale(self, d: int) -> float:
         return 1.0 / math.sqrt(d) if self.score_scale is None else float(self.score_scale)
@@ -92,6 +100,20 @@ def compress_keys(K: np.ndarray, p: int, s: int) -> np.ndarray:
 # Stage 1b: relevance scores
 # --------------------------------------------------------------------------
 
+def window_means(K: np.ndarray, size: int, stride: int) -> np.ndarray:
+    """Mean of K[j stride : j stride + size] for every complete window j.
+
+    With (size, stride) = (p, s) these are the semantic kernels; with
+    size = stride = s_c the coarse kernels of the LSE approximation.
+    """
+    L, d = K.shape
+    n = n_complete_kernels(L, size, stride)
+    out = np.zeros((n, d), dtype=np.float64)
+    for j in range(n):
+        out[j] = K[j * stride: j * stride + size].astype(np.float64).mean(axis=0)
+    return out
+
+
 def kernel_logits(q: np.ndarray, Kc: np.ndarray, scale: float) -> np.ndarray:
     """scale * q_h . Mean(K_j) for every head h and kernel j.  q: [G, d]."""
     return scale * (q @ Kc.T)
@@ -115,6 +137,18 @@ def group_relevance(z: np.ndarray) -> np.ndarray:
     [InfLLM v2 › Query group sharing for memory efficiency, eq. r_group]
     """
     return kernel_softmax(z).mean(axis=0)
+
+
+def log_sum_exp(z: np.ndarray) -> np.ndarray:
+    """Per-row log-sum-exp (pass 1 of [InfLLM v2 › Top-K implementation and
+    the LSE bottleneck]).  z: [G, n], n >= 1."""
+    zmax = z.max(axis=1, keepdims=True)
+    return (zmax + np.log(np.exp(z - zmax).sum(axis=1, keepdims=True)))[:, 0]
+
+
+def group_relevance_given_lse(z: np.ndarray, lse: np.ndarray) -> np.ndarray:
+    """r_group with a given per-head normaliser: mean_h exp(z_h - lse_h)."""
+    return np.exp(z - lse[:, None]).mean(axis=0)
 
 
 def block_relevance(g: np.ndarray, i: int, m: int, p: int, s: int) -> np.ndarray:
@@ -174,13 +208,28 @@ class Selection:
     boundary: float      # score of the lowest-ranked scored block taken (nan if none)
 
 
-def select_for_query(q: np.ndarray, Kc: np.ndarray, i: int, st: Settings) -> Selection:
-    """Stage 1 for one query token of one GQA group.  q: [G, d]; Kc: [n_c, d]."""
+def select_for_query(q: np.ndarray, Kc: np.ndarray, i: int, st: Settings,
+                     Kcc: np.ndarray | None = None) -> Selection:
+    """Stage 1 for one query token of one GQA group.  q: [G, d]; Kc: [n_c, d].
+
+    With st.coarse, the normaliser of every head's kernel softmax is the LSE
+    over the visible coarse kernels Kcc (means of s_c keys, stride s_c)
+    instead of over the fine kernels [InfLLM v2 › Efficient LSE
+    approximation]; before the first coarse kernel is complete the exact LSE
+    is kept.
+    """
     d = q.shape[1]
     n_vis = min(visible_kernel_count(i, st.kernel, st.stride), Kc.shape[0])
     if n_vis > 0:
         z = kernel_logits(q, Kc[:n_vis], st.sscale(d))
-        g = group_relevance(z)
+        n_vis_c = 0
+        if st.coarse:
+            n_vis_c = min(visible_kernel_count(i, st.coarse, st.coarse), Kcc.shape[0])
+        if n_vis_c > 0:
+            lse = log_sum_exp(kernel_logits(q, Kcc[:n_vis_c], st.sscale(d)))
+            g = group_relevance_given_lse(z, lse)
+        else:
+            g = group_relevance(z)
     else:
         g = np.zeros(0)
     r = block_relevance(g, i, st.block, st.kernel, st.stride)
@@ -242,6 +291,7 @@ def run_selection(inputs, st: Settings, units=None, kc_cache=None):
 
     Returns {(b, h, t): Selection}.
     """
+    kcc_cache = {}
     wl = inputs.wl
     G = wl.group
     if units is None:
@@ -255,7 +305,12 @@ def run_selection(inputs, st: Settings, units=None, kc_cache=None):
         L = int(inputs.kv_lens[b])
         i = query_position(L, wl.n_q, t)
         q = _f64(inputs.q[b, t, h * G:(h + 1) * G])
-        out[(b, h, t)] = select_for_query(q, kc_cache[(b, h)], i, st)
+        Kcc = None
+        if st.coarse:
+            if (b, h) not in kcc_cache:
+                kcc_cache[(b, h)] = window_means(_f64(inputs.k[b, h, :L]), st.coarse, st.coarse)
+            Kcc = kcc_cache[(b, h)]
+        out[(b, h, t)] = select_for_query(q, kc_cache[(b, h)], i, st, Kcc)
     return out
 
 

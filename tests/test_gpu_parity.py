@@ -335,6 +335,34 @@ def test_workload_parity(dev, name):
         print(f"{name} fused step: tie-band differences={ties} max|dO|={mx:.2e} mean={mean:.2e}")
 
 
+def test_chunked_prefill_on_a_cache(dev):
+    # A 2048-token chunk appended to caches of different lengths (the query
+    # position rule i = L - n_q + t): selection over each token's visible
+    # kernels and the tcgen05 attention, on a stratified sample of tokens.
+    import torch
+    nq = 2048
+    inp = S.make_random(batch=2, n_kv_heads=2, kv_len=20000, n_q=nq, topk=32, includes_forced=False,
+                        seed=77, kv_lens=[20000, 9000])
+    st = _settings(inp.wl)
+    run = GpuRun(inp, dev)
+    run.compress()
+    run.select(with_scores=False)
+    run.attend()
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(5)
+    toks = sorted(set(range(0, 64)) | set(range(nq - 64, nq)) | set(rng.choice(nq, 128, replace=False).tolist()))
+    units = [(b, h, t) for b in range(2) for h in range(2) for t in toks]
+    sels = O.run_selection(inp, st, units=units)
+    check_selections(run, sels, check_scores=False)
+    idx, nsel = run.upload_selection(sels)
+    run.out.fill_(float("nan"))
+    run.attend(idx, nsel)
+    torch.cuda.synchronize()
+    refs = O.run_attention(inp, st, {u: s.blocks for u, s in sels.items()}, units=units)
+    mx, mean = check_attention(run, refs, strict=True)
+    print(f"chunked prefill: units={len(units)} max|dO|={mx:.2e} mean={mean:.2e}")
+
+
 def test_select_exact_ties_break_to_lower_block(dev):
     # The key sequence repeats after `half` keys, so block j and block
     # j + half/64 see bit-identical kernel means and score exactly alike; both

@@ -209,6 +209,78 @@ def test_selection_structural_invariants():
             assert len(sel.blocks) == want, (i, inc)
 
 
+# ------------------------------------------- coarse-LSE approximation ----
+
+def test_window_means_prefix_sum_and_ramp():
+    # Coarse kernels: means of non-overlapping windows of s_c keys.
+    rng = np.random.default_rng(11)
+    K = rng.standard_normal((300, 5))
+    P = np.concatenate([np.zeros((1, 5)), np.cumsum(K, axis=0)])
+    for size in (64, 128):
+        W = O.window_means(K, size, size)
+        n = 300 // size
+        ref = np.array([(P[(j + 1) * size] - P[j * size]) / size for j in range(n)]).reshape(n, 5)
+        np.testing.assert_allclose(W, ref, rtol=1e-12, atol=1e-12)
+    ramp = O.window_means(np.arange(256, dtype=np.float64)[:, None], 64, 64)[:, 0]
+    assert ramp.tolist() == [31.5, 95.5, 159.5, 223.5]
+    # (p, s) windows are exactly the semantic kernels.
+    np.testing.assert_array_equal(O.window_means(K, 32, 16), O.compress_keys(K, 32, 16))
+
+
+def test_log_sum_exp_against_torch():
+    z = np.random.default_rng(12).standard_normal((16, 77)) * 9.0
+    ref = torch.logsumexp(torch.from_numpy(z), dim=1).numpy()
+    np.testing.assert_allclose(O.log_sum_exp(z), ref, rtol=1e-13)
+
+
+def test_coarse_lse_with_fine_kernels_is_the_exact_selection():
+    # Feeding the fine kernels as the "coarse" set (their LSE is the exact
+    # one) must reproduce the exact path bit for bit.
+    q, K = _rand_case(13, L=1200)
+    Kc = O.compress_keys(K, 32, 16)
+    i = 1199
+    exact = O.select_for_query(q, Kc, i, O.Settings(topk=8))
+    st = O.Settings(topk=8, coarse=16)   # visible-window rule of 16-key windows
+    n16 = O.visible_kernel_count(i, 16, 16)
+    assert n16 >= Kc.shape[0]
+    fine_as_coarse = O.select_for_query(q, Kc, i, st, Kcc=Kc)
+    np.testing.assert_allclose(fine_as_coarse.r, exact.r, rtol=1e-12)
+    assert fine_as_coarse.blocks.tolist() == exact.blocks.tolist()
+
+
+def test_coarse_lse_is_a_common_per_head_normaliser():
+    # g = mean_h exp(z_h - lse_h): the coarse path equals the definition with
+    # lse from the coarse windows, and a constant added to every head's lse
+    # scales g uniformly, leaving the block order unchanged.
+    q, K = _rand_case(14, L=2000)
+    Kc = O.compress_keys(K, 32, 16)
+    Kcc = O.window_means(K, 64, 64)
+    i, d = 1999, q.shape[1]
+    st = O.Settings(topk=10, coarse=64)
+    sel = O.select_for_query(q, Kc, i, st, Kcc=Kcc)
+    n_vis = O.visible_kernel_count(i, 32, 16)
+    z = O.kernel_logits(q, Kc[:n_vis], st.sscale(d))
+    zc = O.kernel_logits(q, Kcc[:O.visible_kernel_count(i, 64, 64)], st.sscale(d))
+    lse = torch.logsumexp(torch.from_numpy(zc), dim=1).numpy()
+    g = (np.exp(z - lse[:, None])).mean(axis=0)
+    np.testing.assert_allclose(sel.g, g, rtol=1e-12)
+    g_shift = O.group_relevance_given_lse(z, lse + 3.7)
+    np.testing.assert_allclose(g_shift, g * math.exp(-3.7), rtol=1e-12)
+    r_shift = O.block_relevance(g_shift, i, 64, 32, 16)
+    blocks_shift = O.top_k_blocks(r_shift, O.forced_blocks(i, 64, 1, 2), 10, True)
+    assert blocks_shift.tolist() == sel.blocks.tolist()
+
+
+def test_coarse_lse_keeps_exact_lse_before_first_coarse_window():
+    q, K = _rand_case(15, L=200)
+    Kc = O.compress_keys(K, 32, 16)
+    Kcc = O.window_means(K, 64, 64)
+    for i in (31, 40, 62):
+        a = O.select_for_query(q, Kc, i, O.Settings(topk=4))
+        b = O.select_for_query(q, Kc, i, O.Settings(topk=4, coarse=64), Kcc=Kcc)
+        np.testing.assert_array_equal(a.r, b.r)
+
+
 def test_planted_blocks_are_selected_on_4k_decode_workload():
     inp = S.make_inputs(S.WORKLOADS["decode_4k"])
     st = O.Settings(topk=16)
@@ -296,8 +368,17 @@ def _planted_mistakes():
         c = i // m
         return sorted({0, c})
 
+    orig_wm = O.window_means
+
+    def wm_half_stride(K, size, stride):               # overlapping coarse windows
+        return orig_wm(K, size, max(1, stride // 2) if size == stride else stride)
+
+    def lse_plain_max(z):                              # max instead of log-sum-exp
+        return z.max(axis=1)
+
     return [("block_relevance", br_off_by_one), ("group_relevance", gr_max_not_mean),
-            ("kernel_softmax", ks_no_norm), ("forced_blocks", forced_no_prev)]
+            ("kernel_softmax", ks_no_norm), ("forced_blocks", forced_no_prev),
+            ("window_means", wm_half_stride), ("log_sum_exp", lse_plain_max)]
 
 
 @pytest.mark.parametrize("name,bad", _planted_mistakes())
@@ -307,7 +388,8 @@ def test_planted_oracle_mistakes_are_caught(monkeypatch, name, bad):
     checks = [test_hand_worked_selections, test_group_relevance_is_head_mean_and_sums_to_one,
               test_selection_structural_invariants,
               lambda: test_block_relevance_brute_force(64, 32, 16),
-              lambda: test_forced_blocks_hand_cases(1000, [0, 14, 15])]
+              lambda: test_forced_blocks_hand_cases(1000, [0, 14, 15]),
+              test_window_means_prefix_sum_and_ramp, test_log_sum_exp_against_torch]
     failed = 0
     for chk in checks:
         try:
