@@ -311,6 +311,27 @@ def prefill_line(dev, steps, warmup, peaks):
             pairs += int(keys.clip(min=0).sum())
     flops = 4.0 * wl.head_dim * pairs * wl.group
     achieved = flops / t_stage["attend"] / 1e12
+
+    # The coarse-kernel LSE approximation of the selection (windows of 64
+    # keys): its time against the exact selection's, and how many of the
+    # exact selection's blocks it keeps.
+    sc = 64
+    kcc = T.alloc_kcc(p, sc, dev)
+    idx_c = torch.empty_like(idx)
+    nsel_c = torch.empty_like(nsel)
+    t_cmeans = timed(lambda: T.coarse_means(p, k, lens, sc, kcc), steps)
+    t_csel = timed(lambda: T.select_blocks_coarse_lse(p, q, kc, sc, kcc, lens, idx_c, nsel_c), steps)
+    idx_ch, nsel_ch = idx_c.cpu().numpy(), nsel_c.cpu().numpy()
+    kept = total = 0
+    for b in range(B):
+        for h in range(H):
+            for t_ in range(nq):
+                e = set(idx_h[b, h, t_, :nsel_h[b, h, t_]].tolist())
+                c = set(idx_ch[b, h, t_, :nsel_ch[b, h, t_]].tolist())
+                kept += len(e & c)
+                total += len(e)
+    coarse = {"window": sc, "select_ms": t_csel * 1e3, "coarse_means_ms": t_cmeans * 1e3,
+              "select_speedup": t_stage["select"] / t_csel, "selection_overlap": kept / max(total, 1)}
     return {
         "workload": f"{PREFILL}: batch 1, 32 q / 2 kv heads, causal 32768 x 32768, top-64 + init + local",
         "tokens_per_s": B * nq / t_step,
@@ -320,6 +341,7 @@ def prefill_line(dev, steps, warmup, peaks):
                      "achieved": achieved, "peak": peaks[1], "unit": "TFLOP/s",
                      "frac": achieved / peaks[1], "peak_kind": peaks[3] + " burst bf16",
                      "algorithmic_flop_per_launch": flops, "traffic": _traffic("attn_tc_kernel", PREFILL)},
+        "coarse_lse": coarse,
     }
 
 

@@ -166,6 +166,32 @@ int infllmv2_select_blocks_static(const infllmv2_params* p, const void* q, int32
                                   float* block_scores, void* stream);
 
 /*
+ * Coarse-grained LSE approximation [InfLLM v2 > Efficient LSE approximation]
+ * (off the default path; the exact LSE is the reference selection).
+ *
+ * infllmv2_coarse_means: kcc[b, h, 0 / 1, j, :] = hi / lo bf16 planes of the
+ * mean of keys [j coarse, (j + 1) coarse) for every complete window of
+ * sequence b (j < kv_lens[b] / coarse); kcc is bf16
+ * [batch, n_kv_heads, 2, max_kv_len / coarse, d].  `coarse` is a multiple of
+ * 16 in [32, 4096].
+ *
+ * infllmv2_select_blocks_coarse_lse: infllmv2_select_blocks for the prefill
+ * path (n_q > 16) with each head's kernel-softmax normaliser taken over the
+ * visible coarse windows (all keys <= i) instead of the fine kernels; a query
+ * with no complete window keeps the exact LSE.  This cuts the first pass over
+ * the kernel means by coarse / kernel_stride.  The decode path (n_q <= 16)
+ * already computes the exact LSE without a second pass over memory, so it
+ * has no coarse form (n_q <= 16 returns INFLLMV2_UNSUPPORTED).  Needs no
+ * workspace.
+ */
+int infllmv2_coarse_means(const infllmv2_params* p, const void* k_cache, const int32_t* kv_lens, int32_t coarse,
+                          void* kcc, void* stream);
+int infllmv2_select_blocks_coarse_lse(const infllmv2_params* p, const void* q, int32_t n_q, const void* kc,
+                                      int32_t coarse, const void* kcc, const int32_t* kv_lens,
+                                      int32_t* block_idx, int32_t* n_selected, float* block_scores,
+                                      void* stream);
+
+/*
  * Stage 3, few queries per sequence (decode n_q = 1, speculative verification
  * n_q <= 16): the selected blocks of each (b, h_kv, t) are dealt to the CTAs
  * of a thread-block cluster; each CTA computes an online-softmax partial and

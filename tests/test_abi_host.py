@@ -124,3 +124,16 @@ def test_python_binding_rejects_cpu_tensors(L):
     k = torch.zeros((1, 1, 256, 128), dtype=torch.bfloat16)
     with pytest.raises(T.InfLLMv2Error):
         T.compress_keys(p, k, torch.zeros(1, dtype=torch.int32), T.alloc_kc(p))
+
+
+def test_coarse_lse_entry_points_validate_first(L):
+    p = _params(L)
+    sel = L.lib.infllmv2_select_blocks_coarse_lse
+    # The decode path (n_q <= 16) has no coarse form.
+    assert sel(ctypes.byref(p), FAKE, 1, FAKE, 64, FAKE, FAKE, FAKE, FAKE, None, None) == L.UNSUPPORTED
+    assert b"prefill path" in L.lib.infllmv2_last_error()
+    for bad in (0, 16, 33, 8192):
+        assert sel(ctypes.byref(p), FAKE, 100, FAKE, bad, FAKE, FAKE, FAKE, FAKE, None, None) == L.INVALID_ARGUMENT
+        assert L.lib.infllmv2_coarse_means(ctypes.byref(p), FAKE, FAKE, bad, FAKE, None) == L.INVALID_ARGUMENT
+    assert sel(ctypes.byref(p), FAKE, 100, FAKE, 64, None, FAKE, FAKE, FAKE, None, None) == L.INVALID_ARGUMENT
+    assert L.lib.infllmv2_coarse_means(ctypes.byref(p), FAKE_ODD, FAKE, 64, FAKE, None) == L.UNSUPPORTED

@@ -363,6 +363,54 @@ def test_chunked_prefill_on_a_cache(dev):
     print(f"chunked prefill: units={len(units)} max|dO|={mx:.2e} mean={mean:.2e}")
 
 
+# ------------------------------------------- coarse-LSE approximation ----
+
+@pytest.mark.parametrize("sc", [64, 128])
+def test_coarse_means_match_oracle(dev, sc):
+    import torch
+    inp = S.make_random(batch=2, n_kv_heads=2, kv_len=5000, n_q=1, topk=8, seed=61, kv_lens=[5000, 1111])
+    run = GpuRun(inp, dev)
+    kcc = run.T.alloc_kcc(run.p, sc, dev)
+    kcc.view(torch.int16).fill_(0x7FC0)
+    run.T.coarse_means(run.p, run.k, run.lens, sc, kcc)
+    torch.cuda.synchronize()
+    got = kc_to_f64(kcc)
+    for b in range(2):
+        for h in range(2):
+            L = int(inp.kv_lens[b])
+            ref = O.window_means(S.bf16_bits_to_f32(inp.k[b, h, :L]).astype(np.float64), sc, sc)
+            n = ref.shape[0]
+            err = np.abs(got[b, h, :n] - ref)
+            assert np.all(err <= 2.0 ** -16 * np.abs(ref) + 1e-7), (b, h, float(err.max()))
+            assert np.all(np.isnan(got[b, h, n:])), (b, h)
+
+
+COARSE_CASES = [
+    # batch, hkv, cap, lens, n_q, topk, includes_forced, sc
+    (2, 2, 5000, [5000, 3333], 100, 16, True, 64),
+    (1, 2, 4000, [4000], 300, 24, False, 128),
+    (1, 1, 700, [700], 700, 4, True, 64),        # from position 0: the first tokens keep the exact LSE
+    (2, 1, 2000, [2000, 90], 90, 6, True, 64),   # a sequence barely past its first window
+]
+
+
+@pytest.mark.parametrize("case", COARSE_CASES, ids=[f"coarse{i}" for i in range(len(COARSE_CASES))])
+def test_select_coarse_lse_parity(dev, case):
+    import torch
+    B, H, cap, lens, nq, topk, inc, sc = case
+    inp = S.make_random(batch=B, n_kv_heads=H, kv_len=cap, n_q=nq, topk=topk, includes_forced=inc,
+                        seed=400 + sum(lens) + nq, kv_lens=lens)
+    run = GpuRun(inp, dev)
+    run.compress()
+    kcc = run.T.alloc_kcc(run.p, sc, dev)
+    run.T.coarse_means(run.p, run.k, run.lens, sc, kcc)
+    run.T.select_blocks_coarse_lse(run.p, run.q, run.kc, sc, kcc, run.lens, run.idx, run.nsel, run.scores)
+    torch.cuda.synchronize()
+    st = O.Settings(topk=topk, includes_forced=inc, coarse=sc)
+    sels = O.run_selection(inp, st)
+    check_selections(run, sels)
+
+
 def test_select_exact_ties_break_to_lower_block(dev):
     # The key sequence repeats after `half` keys, so block j and block
     # j + half/64 see bit-identical kernel means and score exactly alike; both

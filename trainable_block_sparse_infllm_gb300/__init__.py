@@ -10,6 +10,8 @@ memory and streams.  Entry points mirror the C names:
     sparse_attn_decode   stage 3 for decode / speculative verification
     sparse_attn_prefill  stage 3 for prefill
     decode_step          stages 1-3 for the newest token(s), one launch when n_q = 1
+    coarse_means, select_blocks_coarse_lse
+                         the coarse-kernel LSE approximation (prefill path)
 
 Method: "MiniCPM4: Ultra-Efficient LLMs on End Devices", section "InfLLM v2:
 Trainable Sparse Attention for Both Prefilling and Decoding".
@@ -29,7 +31,8 @@ from ._lib import (InfLLMv2Error, OP_DECODE, OP_DECODE_STEP, OP_PREFILL, OP_SELE
 __all__ = [
     "Params", "InfLLMv2Error", "make_params", "num_kernels", "max_selected", "workspace_size",
     "alloc_kc", "alloc_workspace", "compress_keys", "select_blocks", "sparse_attn_decode",
-    "sparse_attn_prefill", "decode_step", "get_device_status", "OP_SELECT", "OP_DECODE", "OP_PREFILL",
+    "sparse_attn_prefill", "decode_step", "coarse_means", "alloc_kcc", "select_blocks_coarse_lse",
+    "get_device_status", "OP_SELECT", "OP_DECODE", "OP_PREFILL",
     "OP_DECODE_STEP", "DECODE_MAX_NQ",
 ]
 
@@ -147,6 +150,30 @@ def sparse_attn_prefill(p: Params, q, k_cache, v_cache, kv_lens, block_idx, n_se
                         lse=None, workspace=None, stream=None):
     return _attn(_lib.lib.infllmv2_sparse_attn_prefill, p, q, k_cache, v_cache, kv_lens, block_idx,
                  n_selected, out, lse, workspace, stream)
+
+
+def alloc_kcc(p: Params, coarse: int, device=None) -> torch.Tensor:
+    """Coarse-window means bf16 [B, Hkv, 2, max_kv_len // coarse, 128] (hi and lo planes)."""
+    return torch.empty((p.batch, p.n_kv_heads, 2, p.max_kv_len // coarse, p.head_dim),
+                       dtype=torch.bfloat16, device=device)
+
+
+def coarse_means(p: Params, k_cache: torch.Tensor, kv_lens: torch.Tensor, coarse: int, kcc: torch.Tensor,
+                 stream=None) -> torch.Tensor:
+    _lib.check(_lib.lib.infllmv2_coarse_means(ctypes.byref(p), _ptr(k_cache), _ptr(kv_lens), coarse, _ptr(kcc),
+                                              _stream(stream)))
+    return kcc
+
+
+def select_blocks_coarse_lse(p: Params, q: torch.Tensor, kc: torch.Tensor, coarse: int, kcc: torch.Tensor,
+                             kv_lens: torch.Tensor, block_idx: torch.Tensor, n_selected: torch.Tensor,
+                             block_scores: torch.Tensor | None = None, stream=None):
+    """select_blocks (prefill path) with the LSE over coarse windows of `coarse` keys."""
+    n_q = q.shape[1]
+    _lib.check(_lib.lib.infllmv2_select_blocks_coarse_lse(ctypes.byref(p), _ptr(q), n_q, _ptr(kc), coarse, _ptr(kcc),
+                                                          _ptr(kv_lens), _ptr(block_idx), _ptr(n_selected),
+                                                          _ptr(block_scores), _stream(stream)))
+    return block_idx, n_selected
 
 
 def decode_step(p: Params, q, k_cache, v_cache, kv_lens, kc, block_idx, n_selected, out,

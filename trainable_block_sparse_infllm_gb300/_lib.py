@@ -85,6 +85,10 @@ for _name in ("infllmv2_sparse_attn_decode", "infllmv2_sparse_attn_prefill"):
     getattr(lib, _name).argtypes = [_P, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                     ctypes.c_size_t, _vp]
     getattr(lib, _name).restype = ctypes.c_int
+lib.infllmv2_coarse_means.argtypes = [_P, _vp, _vp, _i32, _vp, _vp]
+lib.infllmv2_coarse_means.restype = ctypes.c_int
+lib.infllmv2_select_blocks_coarse_lse.argtypes = [_P, _vp, _i32, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp]
+lib.infllmv2_select_blocks_coarse_lse.restype = ctypes.c_int
 lib.infllmv2_decode_step.argtypes = [_P, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                      ctypes.c_size_t, _vp]
 lib.infllmv2_decode_step.restype = ctypes.c_int
@@ -100,6 +104,7 @@ EXPORTED = (
     "infllmv2_workspace_size", "infllmv2_compress_keys", "infllmv2_select_blocks",
     "infllmv2_select_blocks_static",
     "infllmv2_sparse_attn_decode", "infllmv2_sparse_attn_prefill", "infllmv2_decode_step",
+    "infllmv2_coarse_means", "infllmv2_select_blocks_coarse_lse",
     "infllmv2_status_string",
     "infllmv2_last_error", "infllmv2_get_device_status",
 )

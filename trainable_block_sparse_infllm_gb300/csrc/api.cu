@@ -345,6 +345,60 @@ int infllmv2_select_blocks_static(const infllmv2_params* p, const void* q, int32
   });
 }
 
+int infllmv2_coarse_means(const infllmv2_params* p, const void* k_cache, const int32_t* kv_lens, int32_t coarse,
+                          void* kcc, void* stream) {
+  INFLLMV2_GUARD({
+    Shape s;
+    int rc = check_params(p, 1, &s);
+    if (rc) return rc;
+    if (!k_cache || !kv_lens || !kcc) return fail(INFLLMV2_INVALID_ARGUMENT, "a required pointer is NULL");
+    if (coarse < 32 || coarse > 4096 || coarse % kStride != 0)
+      return fail(INFLLMV2_INVALID_ARGUMENT, "coarse window %d: a multiple of 16 in [32, 4096]", coarse);
+    if (!aligned16(k_cache) || !aligned16(kcc))
+      return fail(INFLLMV2_UNSUPPORTED, "k_cache and kcc must be 16-byte aligned");
+    uint32_t* status = status_ptr();
+    if (!status) return fail(INFLLMV2_CUDA_ERROR, "no device status word (no current CUDA device?)");
+    cudaError_t e = launch_coarse(s, k_cache, kv_lens, coarse, kcc, status, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "coarse_means");
+    return INFLLMV2_OK;
+  });
+}
+
+int infllmv2_select_blocks_coarse_lse(const infllmv2_params* p, const void* q, int32_t n_q, const void* kc,
+                                      int32_t coarse, const void* kcc, const int32_t* kv_lens,
+                                      int32_t* block_idx, int32_t* n_selected, float* block_scores,
+                                      void* stream) {
+  INFLLMV2_GUARD({
+    Shape s;
+    int rc = check_params(p, n_q, &s);
+    if (rc) return rc;
+    if (!q || !kc || !kcc || !kv_lens || !block_idx || !n_selected)
+      return fail(INFLLMV2_INVALID_ARGUMENT, "a required pointer is NULL");
+    if (coarse < 32 || coarse > 4096 || coarse % kStride != 0)
+      return fail(INFLLMV2_INVALID_ARGUMENT, "coarse window %d: a multiple of 16 in [32, 4096]", coarse);
+    if (n_q <= kSelDecodeMaxNq)
+      return fail(INFLLMV2_UNSUPPORTED,
+                  "the coarse LSE applies to the prefill path (n_q > %d); the decode path already "
+                  "computes the exact LSE in one pass",
+                  kSelDecodeMaxNq);
+    if (!aligned16(q) || !aligned16(kc) || !aligned16(kcc))
+      return fail(INFLLMV2_UNSUPPORTED, "q, kc and kcc must be 16-byte aligned");
+    if (s.ncmax < 1 || s.Lmax / coarse < 1)
+      return fail(INFLLMV2_UNSUPPORTED, "max_kv_len must hold a kernel and a coarse window");
+    uint32_t* status = status_ptr();
+    if (!status) return fail(INFLLMV2_CUDA_ERROR, "no device status word (no current CUDA device?)");
+    CUtensorMap kcm, kccm, qm;
+    if ((rc = make_map(&qm, q, static_cast<uint64_t>(s.B) * s.nq * s.Hkv * kGroup, 16, "q"))) return rc;
+    if ((rc = make_map(&kcm, kc, static_cast<uint64_t>(s.B) * s.Hkv * 2 * s.ncmax, 64, "kc"))) return rc;
+    if ((rc = make_map(&kccm, kcc, static_cast<uint64_t>(s.B) * s.Hkv * 2 * (s.Lmax / coarse), 64, "kcc")))
+      return rc;
+    cudaError_t e = launch_select_coarse(s, kcm, kccm, coarse, qm, kv_lens, block_idx, n_selected, block_scores,
+                                         status, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "select_blocks_coarse_lse");
+    return INFLLMV2_OK;
+  });
+}
+
 int infllmv2_sparse_attn_decode(const infllmv2_params* p, const void* q, int32_t n_q, const void* k_cache,
                                 const void* v_cache, const int32_t* kv_lens, const int32_t* block_idx,
                                 const int32_t* n_selected, void* out, float* lse, void* workspace,

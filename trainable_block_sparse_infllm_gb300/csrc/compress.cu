@@ -68,7 +68,69 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// Coarse kernels of the LSE approximation ([InfLLM v2 > Efficient LSE
+// approximation]): the mean of each complete window of sc keys (stride sc,
+// sc a multiple of 16), as hi/lo bf16 planes like the fine kernels.  Sixteen
+// threads per window, 8 dims each, summing its 16-key chunks in order.
+__global__ void __launch_bounds__(kThreads)
+    coarse_kernel(const __nv_bfloat16* __restrict__ k, const int32_t* __restrict__ kv_lens, int Hkv, int Lmax,
+                  int nccmax, int sc, __nv_bfloat16* __restrict__ kcc, uint32_t* status) {
+  const int b = blockIdx.z, h = blockIdx.y;
+  pdl_wait();
+  pdl_trigger();
+  const int L = kv_lens[b];
+  if (L < 0 || L > Lmax) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && h == 0) atomicOr(status, kStatusBadKvLen);
+    return;
+  }
+  const int ncc = L / sc;
+  const int j = blockIdx.x * (kThreads / 16) + (threadIdx.x >> 4);
+  if (j >= ncc) return;
+  const int sub = threadIdx.x & 15;
+  const size_t bh = static_cast<size_t>(b) * Hkv + h;
+  const __nv_bfloat16* kbh = k + bh * Lmax * kHeadDim;
+  float tot[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+  for (int c = 0; c < sc / kStride; ++c) {
+    float acc[8];
+    chunk_sum16(acc, kbh, j * sc + c * kStride, sub);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) tot[e] += acc[e];
+  }
+  const float inv = 1.0f / static_cast<float>(sc);
+  uint32_t hw[4], lw[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float m0 = tot[2 * e] * inv, m1 = tot[2 * e + 1] * inv;
+    const __nv_bfloat162 hv = __floats2bfloat162_rn(m0, m1);
+    const __nv_bfloat162 lv = __floats2bfloat162_rn(m0 - __bfloat162float(hv.x), m1 - __bfloat162float(hv.y));
+    hw[e] = *reinterpret_cast<const uint32_t*>(&hv);
+    lw[e] = *reinterpret_cast<const uint32_t*>(&lv);
+  }
+  const size_t plane = static_cast<size_t>(nccmax) * kHeadDim;
+  const size_t off = bh * 2 * plane + static_cast<size_t>(j) * kHeadDim + sub * 8;
+  *reinterpret_cast<uint4*>(kcc + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  *reinterpret_cast<uint4*>(kcc + off + plane) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+}
+
 }  // namespace
+
+cudaError_t launch_coarse(const Shape& s, const void* k, const int32_t* kv_lens, int sc, void* kcc,
+                          uint32_t* status, cudaStream_t st) {
+  const int nccmax = s.Lmax / sc;
+  if (nccmax <= 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((nccmax + kThreads / 16 - 1) / (kThreads / 16), s.Hkv, s.B);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.stream = st;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, coarse_kernel, static_cast<const __nv_bfloat16*>(k), kv_lens, s.Hkv, s.Lmax,
+                            nccmax, sc, static_cast<__nv_bfloat16*>(kcc), status);
+}
 
 cudaError_t launch_compress(const Shape& s, const void* k, const int32_t* kv_lens, int kbegin,
                             int kend, void* kc, uint32_t* status, cudaStream_t st) {

@@ -22,6 +22,10 @@ struct Shape {
 cudaError_t launch_compress(const Shape& s, const void* k, const int32_t* kv_lens, int kbegin,
                             int kend, void* kc, uint32_t* status, cudaStream_t st);
 
+// Coarse kernels (means of sc-key windows) for the LSE approximation.
+cudaError_t launch_coarse(const Shape& s, const void* k, const int32_t* kv_lens, int sc, void* kcc,
+                          uint32_t* status, cudaStream_t st);
+
 // ---- stage 2 ---------------------------------------------------------------
 constexpr int kSelDecodeMaxNq = 16;   // n_q at or below this uses the decode path
 
@@ -30,6 +34,11 @@ cudaError_t launch_select(const Shape& s, const CUtensorMap& kc_map, const CUten
                           const void* q, const int32_t* kv_lens, int32_t* block_idx,
                           int32_t* n_sel, float* block_scores, void* ws, uint32_t* status,
                           cudaStream_t st);
+// Prefill path (n_q > 16) with the per-head LSE taken over coarse kernels of
+// sc keys (kcc_map over [B, Hkv, 2, Lmax / sc, 128]).
+cudaError_t launch_select_coarse(const Shape& s, const CUtensorMap& kc_map, const CUtensorMap& kcc_map, int sc,
+                                 const CUtensorMap& q_map, const int32_t* kv_lens, int32_t* block_idx,
+                                 int32_t* n_sel, float* block_scores, uint32_t* status, cudaStream_t st);
 
 // ---- stage 3 ---------------------------------------------------------------
 size_t attn_workspace_bytes(const Shape& s, bool prefill);

@@ -63,7 +63,7 @@ __host__ __device__ inline PrefLayout pref_layout(int stages, int nbmax) {
 }
 
 __global__ void __launch_bounds__(kPrefTokens * 32)
-    sel_prefill_kernel(const __grid_constant__ CUtensorMap kc_map,
+    sel_prefill_kernel(const __grid_constant__ CUtensorMap kc_map, const __grid_constant__ CUtensorMap kcc_map,
                        const __grid_constant__ CUtensorMap q_map, SelParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -99,17 +99,30 @@ __global__ void __launch_bounds__(kPrefTokens * 32)
     }
     return;
   }
-  const int t_last = min(nq - 1, static_cast<int>(blockIdx.x) * kPrefTokens + kPrefTokens - 1);
+  const int t_first = static_cast<int>(blockIdx.x) * kPrefTokens;
+  const int t_last = min(nq - 1, t_first + kPrefTokens - 1);
   const int nvis_max = n_complete_kernels(L - nq + t_last + 1);
   const int nch = (nvis_max + kPrefChunk - 1) / kPrefChunk;
-  const int total = 2 * nch;
   const int i_t = L - nq + (active ? t : t_last);
   const int c_t = i_t / kBlock;
   const int nvis_t = n_complete_kernels(i_t + 1);
+  // LSE pass over coarse windows ([InfLLM v2 > Efficient LSE approximation])
+  // for tokens that have a complete one, over the fine kernels otherwise.
+  // The stream of 64-row tiles: coarse pass (A), fine LSE pass (B), fine
+  // normalise pass (C); A and B only when some token of the CTA needs them.
+  const int nvis_c_t = p.sc ? (i_t + 1) / p.sc : 0;
+  const bool coarse_t = nvis_c_t > 0;
+  const int nvis_c_max = p.sc ? (L - nq + t_last + 1) / p.sc : 0;
+  const bool need_b = p.sc == 0 || (L - nq + t_first + 1) / p.sc == 0;
+  const int nch_a = (nvis_c_max + kPrefChunk - 1) / kPrefChunk;
+  const int nch_b = need_b ? nch : 0;
+  const int seg_c = nch_a + nch_b;
+  const int total = seg_c + nch;
 
   for (int j = lane; j < p.nbmax; j += 32) r_w[j] = -INFINITY;
   if (threadIdx.x == 0) {
     prefetch_tensormap(&kc_map);
+    prefetch_tensormap(&kcc_map);
     prefetch_tensormap(&q_map);
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -121,15 +134,19 @@ __global__ void __launch_bounds__(kPrefTokens * 32)
   __syncthreads();
 
   auto issue = [&](int it) {
-    const int ch = it % nch, stage = it % S;
+    const int stage = it % S;
+    const bool coarse_seg = it < nch_a;
+    const int ch = coarse_seg ? it : (it < seg_c ? it - nch_a : it - seg_c);
+    const CUtensorMap* map = coarse_seg ? &kcc_map : &kc_map;
+    const int rows = coarse_seg ? p.nccmax : p.ncmax;
     uint8_t* dst = smem + lay.stage_off + stage * kPrefStageBytes;
     mbar_arrive_expect_tx(&full[stage], kPrefStageBytes);
-    const int row_hi = (bh * 2 + 0) * p.ncmax + ch * kPrefChunk;
-    const int row_lo = (bh * 2 + 1) * p.ncmax + ch * kPrefChunk;
-    tma_load_2d(dst, &kc_map, 0, row_hi, &full[stage]);
-    tma_load_2d(dst + 8192, &kc_map, 64, row_hi, &full[stage]);
-    tma_load_2d(dst + 16384, &kc_map, 0, row_lo, &full[stage]);
-    tma_load_2d(dst + 24576, &kc_map, 64, row_lo, &full[stage]);
+    const int row_hi = (bh * 2 + 0) * rows + ch * kPrefChunk;
+    const int row_lo = (bh * 2 + 1) * rows + ch * kPrefChunk;
+    tma_load_2d(dst, map, 0, row_hi, &full[stage]);
+    tma_load_2d(dst + 8192, map, 64, row_hi, &full[stage]);
+    tma_load_2d(dst + 16384, map, 0, row_lo, &full[stage]);
+    tma_load_2d(dst + 24576, map, 64, row_lo, &full[stage]);
   };
 
   if (threadIdx.x == 0) {
@@ -155,9 +172,12 @@ __global__ void __launch_bounds__(kPrefTokens * 32)
   for (int it = 0; it < total; ++it) {
     const int stage = it % S;
     const uint32_t ph = static_cast<uint32_t>(it / S) & 1u;
-    const int pass = it / nch, ch = it % nch;
+    const int pass = it < seg_c ? 0 : 1;
+    const int ch = it < nch_a ? it : (it < seg_c ? it - nch_a : it - seg_c);
     const int kbase = ch * kPrefChunk;
-    if (pass == 1 && ch == 0) {
+    // This token's visible rows of the current tile (0: nothing to do).
+    const int nvv = it < nch_a ? (coarse_t ? nvis_c_t : 0) : (it < seg_c ? (coarse_t ? 0 : nvis_t) : nvis_t);
+    if (it == seg_c) {
 #pragma unroll
       for (int o = 1; o <= 2; o <<= 1) {
         lse_merge(m0, l0, __shfl_xor_sync(0xffffffffu, m0, o), __shfl_xor_sync(0xffffffffu, l0, o));
@@ -168,7 +188,7 @@ __global__ void __launch_bounds__(kPrefTokens * 32)
     }
     ok = mbar_wait(&full[stage], ph, p.status);
     if (!__all_sync(0xffffffffu, ok)) break;
-    if (active && kbase < nvis_t) {
+    if (active && kbase < nvv) {
       const uint32_t hi_b = smem_u32(smem + lay.stage_off + stage * kPrefStageBytes);
       const uint32_t lo_b = hi_b + 16384;
       // All eight n-tiles' scores first (independent MMA chains), then the
@@ -181,12 +201,12 @@ __global__ void __launch_bounds__(kPrefTokens * 32)
 #pragma unroll
         for (int e = 0; e < 4; ++e) x[nt][e] = acc[e] * p.scale2;
       }
-      if (kbase + kPrefChunk > nvis_t) {
+      if (kbase + kPrefChunk > nvv) {
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) {
           const int kj = kbase + nt * 8 + 2 * tq;
-          if (kj >= nvis_t) x[nt][0] = x[nt][2] = -INFINITY;
-          if (kj + 1 >= nvis_t) x[nt][1] = x[nt][3] = -INFINITY;
+          if (kj >= nvv) x[nt][0] = x[nt][2] = -INFINITY;
+          if (kj + 1 >= nvv) x[nt][1] = x[nt][3] = -INFINITY;
         }
       }
       if (pass == 0) {
@@ -261,6 +281,25 @@ __global__ void __launch_bounds__(kPrefTokens * 32)
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+cudaError_t launch_prefill_select(const Shape& s, const CUtensorMap& kc_map, const CUtensorMap& kcc_map,
+                                  const CUtensorMap& q_map, SelParams p, cudaStream_t st) {
+  int stages = 3;
+  PrefLayout lay = pref_layout(stages, s.nbmax);
+  if (lay.total + 1024 > 227 * 1024) {
+    stages = 2;
+    lay = pref_layout(stages, s.nbmax);
+  }
+  if (lay.total + 1024 > 227 * 1024) return cudaErrorInvalidConfiguration;
+  p.stages = stages;
+  const int psmem = lay.total + 1024;
+  cudaError_t e = cudaFuncSetAttribute(sel_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       psmem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((s.nq + kPrefTokens - 1) / kPrefTokens, s.Hkv, s.B);
+  sel_prefill_kernel<<<grid, kPrefTokens * 32, psmem, st>>>(kc_map, kcc_map, q_map, p);
+  return cudaGetLastError();
+}
+
 bool use_decode_path(const Shape& s) { return s.nq <= kSelDecodeMaxNq && select_decode_supported(s); }
 
 }  // namespace
@@ -304,21 +343,34 @@ cudaError_t launch_select(const Shape& s, const CUtensorMap& kc_map, const CUten
     return launch_select_decode(s, kc_map, q_map, p, st);
   }
 
-  int stages = 3;
-  PrefLayout lay = pref_layout(stages, s.nbmax);
-  if (lay.total + 1024 > 227 * 1024) {
-    stages = 2;
-    lay = pref_layout(stages, s.nbmax);
-  }
-  if (lay.total + 1024 > 227 * 1024) return cudaErrorInvalidConfiguration;
-  p.stages = stages;
-  const int psmem = lay.total + 1024;
-  cudaError_t e = cudaFuncSetAttribute(sel_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       psmem);
-  if (e != cudaSuccess) return e;
-  dim3 grid((s.nq + kPrefTokens - 1) / kPrefTokens, s.Hkv, s.B);
-  sel_prefill_kernel<<<grid, kPrefTokens * 32, psmem, st>>>(kc_map, q_map, p);
-  return cudaGetLastError();
+  return launch_prefill_select(s, kc_map, kc_map, q_map, p, st);
+}
+
+cudaError_t launch_select_coarse(const Shape& s, const CUtensorMap& kc_map, const CUtensorMap& kcc_map, int sc,
+                                 const CUtensorMap& q_map, const int32_t* kv_lens, int32_t* block_idx,
+                                 int32_t* n_sel, float* block_scores, uint32_t* status, cudaStream_t st) {
+  SelParams p{};
+  p.B = s.B;
+  p.Hkv = s.Hkv;
+  p.Lmax = s.Lmax;
+  p.nq = s.nq;
+  p.ncmax = s.ncmax;
+  p.nbmax = s.nbmax;
+  p.kmax = s.kmax;
+  p.topk = s.topk;
+  p.n_init = s.n_init;
+  p.n_local = s.n_local;
+  p.inc_forced = s.inc_forced;
+  p.scale2 = s.score_scale2;
+  p.kv_lens = kv_lens;
+  p.block_idx = block_idx;
+  p.n_sel = n_sel;
+  p.status = status;
+  p.write_r = block_scores != nullptr;
+  p.r_buf = block_scores;
+  p.sc = sc;
+  p.nccmax = s.Lmax / sc;
+  return launch_prefill_select(s, kc_map, kcc_map, q_map, p, st);
 }
 
 }  // namespace infllmv2

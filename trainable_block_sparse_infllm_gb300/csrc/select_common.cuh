@@ -25,6 +25,7 @@ struct SelParams {
   float* z;            // [B*Hkv*nq][16][ncpad] scratch  (decode path)
   int write_r;
   int stages;          // prefill path: pipeline depth
+  int sc, nccmax;      // prefill path: coarse-LSE window (0 = exact LSE) and windows per cache
   uint32_t* status;
 };
 
