@@ -349,6 +349,57 @@ def test_attention_split_merge_identity():
     np.testing.assert_allclose(M + np.log(sum(w)), l_all, rtol=1e-13)
 
 
+# ------------------------------------------------- attention backward ----
+
+def _grad_case(seed=20, G=4, d=6, L=300):
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((G, d)), rng.standard_normal((L, d)), rng.standard_normal((L, d)),
+            rng.standard_normal((G, d)))
+
+
+def test_attention_grad_matches_torch_autograd(grad_fn=None):
+    q, K, V, dO = _grad_case()
+    blocks, i, m, scale = np.array([0, 2, 4]), 290, 64, 0.37
+    dq, dK, dV = (grad_fn or O.sparse_attention_grad)(q, K, V, blocks, i, m, scale, dO)
+    qt = torch.from_numpy(q).requires_grad_()
+    Kt = torch.from_numpy(K).requires_grad_()
+    Vt = torch.from_numpy(V).requires_grad_()
+    mask = torch.zeros(K.shape[0], dtype=torch.bool)
+    for j in blocks:
+        mask[j * m:(j + 1) * m] = True
+    mask[i + 1:] = False
+    s = scale * (qt @ Kt.T)
+    s = s.masked_fill(~mask[None, :], float("-inf"))
+    out = torch.softmax(s, dim=1) @ Vt
+    out.backward(torch.from_numpy(dO))
+    np.testing.assert_allclose(dq, qt.grad.numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dK, Kt.grad.numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dV, Vt.grad.numpy(), rtol=1e-11, atol=1e-12)
+
+
+def test_attention_grad_finite_differences():
+    q, K, V, dO = _grad_case(seed=21, G=2, d=3, L=140)
+    blocks, i, m, scale = np.array([0, 2]), 135, 64, 0.5
+    dq, dK, dV = O.sparse_attention_grad(q, K, V, blocks, i, m, scale, dO)
+
+    def f(q_, K_, V_):
+        return float((O.sparse_attention(q_, K_, V_, blocks, i, m, scale)[0] * dO).sum())
+
+    eps = 1e-6
+    for (arr, grad, idxs) in ((q, dq, [(0, 0), (1, 2)]), (K, dK, [(3, 1), (130, 0), (70, 2)]),
+                              (V, dV, [(5, 0), (135, 2), (100, 1)])):
+        for ix in idxs:
+            plus, minus = arr.copy(), arr.copy()
+            plus[ix] += eps
+            minus[ix] -= eps
+            args_p = [plus if arr is x else x for x in (q, K, V)]
+            args_m = [minus if arr is x else x for x in (q, K, V)]
+            num = (f(*args_p) - f(*args_m)) / (2 * eps)
+            assert abs(num - grad[ix]) <= 1e-6 * (1 + abs(num)), (ix, num, grad[ix])
+    # keys outside the attended set get no gradient
+    assert np.all(dK[64:128] == 0) and np.all(dV[136:] == 0)
+
+
 # ------------------------------------------------ the pins catch mistakes ----
 
 def _planted_mistakes():
@@ -397,3 +448,39 @@ def test_planted_oracle_mistakes_are_caught(monkeypatch, name, bad):
         except AssertionError:
             failed += 1
     assert failed > 0, f"planted mistake in {name} went unnoticed"
+
+
+def _planted_grad_mistakes():
+    good = O.sparse_attention_grad
+
+    def no_scale_dq(q, K, V, b, i, m, s, dO):          # dropped softmax scale on dq
+        dq, dK, dV = good(q, K, V, b, i, m, s, dO)
+        return dq / s, dK, dV
+
+    def no_d_term(q, K, V, b, i, m, s, dO):            # dS = P * dP, the row term dropped
+        dq, dK, dV = good(q, K, V, b, i, m, s, dO)
+        _, lse = O.sparse_attention(q, K, V, b, i, m, s)
+        mask = np.zeros(K.shape[0], dtype=bool)
+        for j in b:
+            mask[j * m:(j + 1) * m] = True
+        mask[i + 1:] = False
+        P = np.exp(s * (q @ K[mask].T) - lse[:, None])
+        dS = P * (dO @ V[mask].T)
+        dq = s * (dS @ K[mask])
+        return dq, dK, dV
+
+    def shifted_dk(q, K, V, b, i, m, s, dO):           # gradient credited to the wrong key
+        dq, dK, dV = good(q, K, V, b, i, m, s, dO)
+        return dq, np.roll(dK, 1, axis=0), dV
+
+    def dv_uses_ds(q, K, V, b, i, m, s, dO):           # dV built from the wrong factor
+        dq, dK, dV = good(q, K, V, b, i, m, s, dO)
+        return dq, dK, dK / s
+
+    return [no_scale_dq, no_d_term, shifted_dk, dv_uses_ds]
+
+
+@pytest.mark.parametrize("bad", _planted_grad_mistakes())
+def test_planted_grad_mistakes_are_caught(bad):
+    with pytest.raises(AssertionError):
+        test_attention_grad_matches_torch_autograd(bad)
