@@ -79,6 +79,7 @@ extern "C" {
 #define INFLLMV2_OP_DECODE  2
 #define INFLLMV2_OP_PREFILL 3
 #define INFLLMV2_OP_DECODE_STEP 4
+#define INFLLMV2_OP_BACKWARD 5
 
 typedef struct infllmv2_params {
   int32_t batch;                 /* B */
@@ -239,6 +240,32 @@ int infllmv2_decode_step(const infllmv2_params* p, const void* q, int32_t n_q, c
                          const void* v_cache, const int32_t* kv_lens, void* kc, int32_t* block_idx,
                          int32_t* n_selected, void* out, float* lse, void* workspace,
                          size_t workspace_bytes, void* stream);
+
+/*
+ * Backward of stage 3 with the selection held fixed [InfLLM v2 >
+ * Training-time considerations: top-k passes no gradient, the keys learn
+ * through the gradient of the sparse attention]: for an upstream gradient
+ * dout of `out`,
+ *     P = exp(attn_scale q.k - lse) over each query's attended keys,
+ *     D = rowsum(dout * out),  dS = P * (dout . v - D),
+ *     dq = attn_scale sum_k dS k,  dk = attn_scale sum_q dS q,  dv = sum_q P dout.
+ *   q, k_cache, v_cache, kv_lens, block_idx, n_selected: as given to the
+ *           forward call; out (bf16) and lse (fp32, required) are its results.
+ *   dout    bf16 [batch, n_q, Hq, d].
+ *   dq      fp32 [batch, n_q, Hq, d], every row written.
+ *   dk, dv  fp32 [batch, n_kv_heads, max_kv_len, d], every row written: keys
+ *           no query attends get 0 (the call zeroes both, then adds the
+ *           contributions of all queries of all heads of the group).
+ * The contributions to one key row are added in an order that depends on
+ * scheduling, so dk and dv may differ in the last bits from run to run.
+ * Workspace: infllmv2_workspace_size(p, n_q, INFLLMV2_OP_BACKWARD) bytes
+ * (an inverse block -> query index, D, work lists).
+ */
+int infllmv2_sparse_attn_backward(const infllmv2_params* p, const void* q, int32_t n_q, const void* k_cache,
+                                  const void* v_cache, const int32_t* kv_lens, const int32_t* block_idx,
+                                  const int32_t* n_selected, const void* out, const float* lse, const void* dout,
+                                  float* dq, float* dk, float* dv, void* workspace, size_t workspace_bytes,
+                                  void* stream);
 
 /* Human-readable name of an INFLLMV2_* return code. */
 const char* infllmv2_status_string(int status);

@@ -267,8 +267,18 @@ def sparse_attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, blocks: np.nda
     return out, lse
 
 
-def sparse_attention_grad(q: np.ndarray, K: np.ndarray, V: np.ndarray, blocks: np.ndarray, i: int, m: int,
-                          scale: float, dO: np.ndarray):
+def attended_keys(n_keys: int, blocks: np.ndarray, i: int, m: int) -> np.ndarray:
+    """Indices (ascending) of the keys a query at position i attends: those of
+    its selected blocks with x <= i."""
+    mask = np.zeros(n_keys, dtype=bool)
+    for j in blocks:
+        mask[j * m:(j + 1) * m] = True
+    mask[i + 1:] = False
+    return np.nonzero(mask)[0]
+
+
+def sparse_attention_grad_selected(q: np.ndarray, K: np.ndarray, V: np.ndarray, blocks: np.ndarray, i: int,
+                                   m: int, scale: float, dO: np.ndarray):
     """Gradients of sparse_attention's O with respect to q, K and V for an
     upstream gradient dO [G, d], with the selection held fixed (there is no
     gradient through the top-k; [InfLLM v2 › Training-time considerations]:
@@ -276,13 +286,11 @@ def sparse_attention_grad(q: np.ndarray, K: np.ndarray, V: np.ndarray, blocks: n
         P = softmax(scale q K_sel^T),  dP = dO V_sel^T,
         D = rowsum(dO * O),  dS = P * (dP - D),
         dq = scale dS K_sel,  dK_sel = scale dS^T q,  dV_sel = P^T dO.
-    Returns (dq [G, d], dK [L, d], dV [L, d]) with zeros for keys not attended.
+    Returns (dq [G, d], keys [n], dK_sel [n, d], dV_sel [n, d]) for the n
+    attended keys.
     """
-    mask = np.zeros(K.shape[0], dtype=bool)
-    for j in blocks:
-        mask[j * m:(j + 1) * m] = True
-    mask[i + 1:] = False
-    Ks, Vs = K[mask], V[mask]
+    keys = attended_keys(K.shape[0], blocks, i, m)
+    Ks, Vs = K[keys], V[keys]
     sc = scale * (q @ Ks.T)
     P = np.exp(sc - sc.max(axis=1, keepdims=True))
     P /= P.sum(axis=1, keepdims=True)
@@ -290,11 +298,18 @@ def sparse_attention_grad(q: np.ndarray, K: np.ndarray, V: np.ndarray, blocks: n
     dP = dO @ Vs.T
     D = (dO * O).sum(axis=1, keepdims=True)
     dS = P * (dP - D)
-    dq = scale * (dS @ Ks)
-    dK = np.zeros_like(K, dtype=np.float64)
-    dV = np.zeros_like(V, dtype=np.float64)
-    dK[mask] = scale * (dS.T @ q)
-    dV[mask] = P.T @ dO
+    return scale * (dS @ Ks), keys, scale * (dS.T @ q), P.T @ dO
+
+
+def sparse_attention_grad(q: np.ndarray, K: np.ndarray, V: np.ndarray, blocks: np.ndarray, i: int, m: int,
+                          scale: float, dO: np.ndarray):
+    """sparse_attention_grad_selected scattered to full size: returns
+    (dq [G, d], dK [L, d], dV [L, d]) with zeros for keys not attended."""
+    dq, keys, dKs, dVs = sparse_attention_grad_selected(q, K, V, blocks, i, m, scale, dO)
+    dK = np.zeros(K.shape, dtype=np.float64)
+    dV = np.zeros(V.shape, dtype=np.float64)
+    dK[keys] = dKs
+    dV[keys] = dVs
     return dq, dK, dV
 
 
@@ -370,26 +385,16 @@ def run_attention(inputs, st: Settings, blocks_of, units=None):
     return out
 
 
-def run_attention_grad(inputs, st: Settings, blocks_of, dO_all: np.ndarray):
-    """Gradients for every unit of one input set with upstream dO_all
-    [B, n_q, Hq, d] (float64): returns (dq [B, n_q, Hq, d], dK [B, Hkv, L_max, d],
-    dV [B, Hkv, L_max, d]); dK and dV sum the contributions of all queries."""
+def unit_attention_grad(inputs, st: Settings, blocks_of, dO_all: np.ndarray, unit, K=None, V=None):
+    """Gradient contributions of one (b, h, t) unit: (dq [G, d], keys, dK_sel,
+    dV_sel) as from sparse_attention_grad_selected."""
     wl = inputs.wl
     G, d = wl.group, wl.head_dim
-    B, H, nq, cap = wl.batch, wl.n_kv_heads, wl.n_q, wl.kv_len
-    dq = np.zeros((B, nq, H * G, d))
-    dK = np.zeros((B, H, cap, d))
-    dV = np.zeros((B, H, cap, d))
-    for b in range(B):
-        L = int(inputs.kv_lens[b])
-        for h in range(H):
-            K, V = _f64(inputs.k[b, h, :L]), _f64(inputs.v[b, h, :L])
-            for t in range(nq):
-                i = query_position(L, nq, t)
-                q = _f64(inputs.q[b, t, h * G:(h + 1) * G])
-                gq, gk, gv = sparse_attention_grad(q, K, V, np.asarray(blocks_of[(b, h, t)]), i, st.block,
-                                                   st.ascale(d), dO_all[b, t, h * G:(h + 1) * G])
-                dq[b, t, h * G:(h + 1) * G] = gq
-                dK[b, h, :L] += gk
-                dV[b, h, :L] += gv
-    return dq, dK, dV
+    b, h, t = unit
+    L = int(inputs.kv_lens[b])
+    if K is None:
+        K, V = _f64(inputs.k[b, h, :L]), _f64(inputs.v[b, h, :L])
+    i = query_position(L, wl.n_q, t)
+    q = _f64(inputs.q[b, t, h * G:(h + 1) * G])
+    return sparse_attention_grad_selected(q, K, V, np.asarray(blocks_of[unit]), i, st.block, st.ascale(d),
+                                          np.asarray(dO_all[b, t, h * G:(h + 1) * G], dtype=np.float64))

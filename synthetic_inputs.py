@@ -230,3 +230,38 @@ def make_random(batch: int, n_kv_heads: int, kv_len: int, n_q: int, topk: int,
         v32[b, :, lens[b]:, :] = -1.0e4
     return Inputs(wl=wl, q=q, k=bf16_bits_from_f32(k32), v=bf16_bits_from_f32(v32),
                   kv_lens=lens, planted=np.zeros((batch, n_kv_heads, 0), dtype=np.int64))
+
+
+def make_grad_out(wl: Workload, seed: int) -> np.ndarray:
+    """Upstream gradient for the backward pass: bf16 bits of float32
+    ``standard_normal`` [B, n_q, Hq, d] from its own PCG64(seed)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return bf16_bits_from_f32(rng.standard_normal((wl.batch, wl.n_q, wl.n_heads, wl.head_dim), dtype=np.float32))
+
+
+def make_block_sets(wl: Workload, kv_lens: np.ndarray, seed: int):
+    """A fixed, valid block selection for backward tests at sizes where the
+    selection itself is not recomputed: per (b, h_kv, t) with query position
+    i = L - n_q + t and c = i // block, min(k_max, c + 1) distinct blocks in
+    [0, c] that always include 0 and c, the rest drawn uniformly without
+    replacement from [1, c - 1] by PCG64(seed), ascending.
+    Returns (block_idx int32 [B, Hkv, n_q, k_max] padded with -1,
+    n_selected int32 [B, Hkv, n_q])."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    B, H, nq, km = wl.batch, wl.n_kv_heads, wl.n_q, wl.k_max
+    idx = np.full((B, H, nq, km), -1, dtype=np.int32)
+    nsel = np.zeros((B, H, nq), dtype=np.int32)
+    for b in range(B):
+        L = int(kv_lens[b])
+        for h in range(H):
+            for t in range(nq):
+                c = (L - nq + t) // wl.block
+                n = min(km, c + 1)
+                if n == c + 1:
+                    chosen = np.arange(c + 1)
+                else:
+                    rest = rng.choice(np.arange(1, c), size=n - 2, replace=False)
+                    chosen = np.sort(np.concatenate(([0, c], rest)))
+                idx[b, h, t, :n] = chosen
+                nsel[b, h, t] = n
+    return idx, nsel

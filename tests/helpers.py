@@ -8,7 +8,19 @@ Tolerances (fixed by the acceptance rule of the benchmark configurations):
     over all outputs, O_ref computed by the fp64 oracle on the same selection;
   * block scores r: relative error <= 1e-4 where the oracle's r is finite
     (the kernel means carry 16 significant bits, the dot products fp32);
-  * lse: absolute error <= 1e-3 (fp32 accumulation of a natural log).
+  * lse: absolute error <= 1e-3 (fp32 accumulation of a natural log);
+  * gradients dq, dk, dv (backward with the selection fixed): the attention
+    rule relative to each tensor's scale, max |g_gpu - g_ref| <= 2e-3 max|g_ref|
+    and mean |g_gpu - g_ref| <= 2e-4 max|g_ref| over the rows that receive a
+    gradient; rows of keys no query attends are exactly 0.  The kernels carry
+    P and dS at 16 significant bits (error near 4e-4 of the scale).  D =
+    rowsum(dO * O) is formed from the forward output the call is given, which
+    is bf16: its error dD_r = sum_d dO_rd (O_gpu - O_ref)_rd moves dq_r by
+    -scale dD_r sum_j P_rj k_j and dk_j by -scale sum_r P_rj dD_r q_r.  Both
+    rules widen by those terms' magnitudes, bounded with the oracle's own
+    probabilities: scale |dD_r| sum_j P_rj |k_j| for dq and
+    scale sum_r P_rj |dD_r| |q_r| for dk (dv does not involve D).  The term
+    only matters for queries that attend a handful of keys, where |O| ~ |V|.
 """
 
 from __future__ import annotations
@@ -20,6 +32,8 @@ ATT_MAX = 2e-3
 ATT_MEAN = 2e-4
 R_REL = 1e-4
 LSE_ABS = 1e-3
+GRAD_MAX = 2e-3
+GRAD_MEAN = 2e-4
 
 
 def dev_bf16(bits: np.ndarray, dev):
@@ -101,6 +115,22 @@ class GpuRun:
             if hi > lo:
                 self.kc[b, :, :, lo:hi].view(torch.int16).fill_(0x7FC0)
         return full
+
+    def backward(self, idx, nsel, dout_bits):
+        """Gradients of the attention last run by ``attend`` (out, lse) for
+        upstream ``dout_bits``: returns fp32 (dq, dk, dv) device tensors."""
+        import torch
+        wl = self.inp.wl
+        dout = dev_bf16(dout_bits, self.dev)
+        dq = torch.full((wl.batch, self.nq, wl.n_heads, wl.head_dim), float("nan"), dtype=torch.float32,
+                        device=self.dev)
+        dk = torch.full((wl.batch, wl.n_kv_heads, wl.kv_len, wl.head_dim), float("nan"), dtype=torch.float32,
+                        device=self.dev)
+        dv = torch.full_like(dk, float("nan"))
+        ws = self.T.alloc_workspace(self.p, self.nq, self.T.OP_BACKWARD, self.dev)
+        self.T.sparse_attn_backward(self.p, self.q, self.k, self.v, self.lens, idx, nsel, self.out, self.lse, dout,
+                                    dq, dk, dv, ws)
+        return dq, dk, dv
 
     def gpu_blocks(self, units):
         idx, nsel = self.idx.cpu().numpy(), self.nsel.cpu().numpy()
@@ -205,3 +235,26 @@ def check_attention(run, refs, strict=False):
         assert mean <= ATT_MEAN + 2.0 ** -9 * total_ref / count + 2.0 ** -11 * vmax_all, mean
     assert lse_err <= LSE_ABS, lse_err
     return mx, mean
+
+
+def check_grad(name, got, ref, rows_used=None, allow=None):
+    """got, ref: arrays of the same shape [..., d].  rows_used (bool over the
+    leading dims, optional): rows that receive a gradient; the others must be
+    exactly 0 in ``got``.  allow (same shape as ref, optional): a per-element
+    bound on the error the kernel's inputs carry by themselves (the bf16
+    forward output inside D); it widens both rules.  Returns
+    (max err / scale, mean err / scale)."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    allow = np.zeros_like(ref) if allow is None else np.asarray(allow, dtype=np.float64)
+    assert np.all(np.isfinite(got)), (name, "non-finite")
+    scale = float(np.abs(ref).max())
+    assert scale > 0, (name, "zero reference")
+    err = np.abs(got - ref)
+    if rows_used is not None:
+        assert np.all(got[~rows_used] == 0), (name, "gradient on a key no query attends")
+        err, allow = err[rows_used], allow[rows_used]
+    over = err - 1.001 * allow
+    assert over.max() <= GRAD_MAX * scale, (name, float(over.max()) / scale, float(err.max()) / scale)
+    assert err.mean() <= GRAD_MEAN * scale + allow.mean(), (name, float(err.mean()) / scale)
+    return float(err.max()) / scale, float(err.mean()) / scale

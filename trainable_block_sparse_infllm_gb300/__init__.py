@@ -12,6 +12,7 @@ memory and streams.  Entry points mirror the C names:
     decode_step          stages 1-3 for the newest token(s), one launch when n_q = 1
     coarse_means, select_blocks_coarse_lse
                          the coarse-kernel LSE approximation (prefill path)
+    sparse_attn_backward dq, dk, dv of stage 3 with the selection held fixed
 
 Method: "MiniCPM4: Ultra-Efficient LLMs on End Devices", section "InfLLM v2:
 Trainable Sparse Attention for Both Prefilling and Decoding".
@@ -25,15 +26,15 @@ import math
 import torch
 
 from . import _lib
-from ._lib import (InfLLMv2Error, OP_DECODE, OP_DECODE_STEP, OP_PREFILL, OP_SELECT, Params,  # noqa: F401
-                   DEVICE_BAD_KV_LEN, DEVICE_TIMEOUT)
+from ._lib import (InfLLMv2Error, OP_BACKWARD, OP_DECODE, OP_DECODE_STEP, OP_PREFILL, OP_SELECT,  # noqa: F401
+                   Params, DEVICE_BAD_KV_LEN, DEVICE_TIMEOUT)
 
 __all__ = [
     "Params", "InfLLMv2Error", "make_params", "num_kernels", "max_selected", "workspace_size",
     "alloc_kc", "alloc_workspace", "compress_keys", "select_blocks", "sparse_attn_decode",
     "sparse_attn_prefill", "decode_step", "coarse_means", "alloc_kcc", "select_blocks_coarse_lse",
-    "get_device_status", "OP_SELECT", "OP_DECODE", "OP_PREFILL",
-    "OP_DECODE_STEP", "DECODE_MAX_NQ",
+    "sparse_attn_backward", "get_device_status", "OP_SELECT", "OP_DECODE", "OP_PREFILL",
+    "OP_DECODE_STEP", "OP_BACKWARD", "DECODE_MAX_NQ",
 ]
 
 DECODE_MAX_NQ = 16
@@ -188,6 +189,19 @@ def decode_step(p: Params, q, k_cache, v_cache, kv_lens, kc, block_idx, n_select
                                              _ptr(kv_lens), _ptr(kc), _ptr(block_idx), _ptr(n_selected),
                                              _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream)))
     return block_idx, n_selected, out, lse
+
+
+def sparse_attn_backward(p: Params, q, k_cache, v_cache, kv_lens, block_idx, n_selected, out, lse, dout,
+                         dq, dk, dv, workspace, stream=None):
+    """dq, dk, dv (fp32) of the block-sparse attention for upstream ``dout``,
+    with ``out`` and ``lse`` from the forward call on the same inputs."""
+    n_q = q.shape[1]
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    _lib.check(_lib.lib.infllmv2_sparse_attn_backward(
+        ctypes.byref(p), _ptr(q), n_q, _ptr(k_cache), _ptr(v_cache), _ptr(kv_lens), _ptr(block_idx),
+        _ptr(n_selected), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+        ws_bytes, _stream(stream)))
+    return dq, dk, dv
 
 
 def get_device_status(clear: bool = True) -> int:

@@ -25,6 +25,7 @@ OP_SELECT = 1
 OP_DECODE = 2
 OP_PREFILL = 3
 OP_DECODE_STEP = 4
+OP_BACKWARD = 5
 
 
 class InfLLMv2Error(RuntimeError):
@@ -92,6 +93,9 @@ lib.infllmv2_select_blocks_coarse_lse.restype = ctypes.c_int
 lib.infllmv2_decode_step.argtypes = [_P, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                      ctypes.c_size_t, _vp]
 lib.infllmv2_decode_step.restype = ctypes.c_int
+lib.infllmv2_sparse_attn_backward.argtypes = [_P, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                              _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+lib.infllmv2_sparse_attn_backward.restype = ctypes.c_int
 lib.infllmv2_status_string.argtypes = [ctypes.c_int]
 lib.infllmv2_status_string.restype = ctypes.c_char_p
 lib.infllmv2_last_error.argtypes = []
@@ -104,7 +108,7 @@ EXPORTED = (
     "infllmv2_workspace_size", "infllmv2_compress_keys", "infllmv2_select_blocks",
     "infllmv2_select_blocks_static",
     "infllmv2_sparse_attn_decode", "infllmv2_sparse_attn_prefill", "infllmv2_decode_step",
-    "infllmv2_coarse_means", "infllmv2_select_blocks_coarse_lse",
+    "infllmv2_coarse_means", "infllmv2_select_blocks_coarse_lse", "infllmv2_sparse_attn_backward",
     "infllmv2_status_string",
     "infllmv2_last_error", "infllmv2_get_device_status",
 )

@@ -160,6 +160,7 @@ int check_params(const infllmv2_params* p, int32_t n_q, Shape* s) {
   s->inc_forced = p->topk_includes_forced;
   s->score_scale2 = p->score_scale * 1.4426950408889634f;
   s->attn_scale2 = p->attn_scale * 1.4426950408889634f;
+  s->attn_scale = p->attn_scale;
   return INFLLMV2_OK;
 }
 
@@ -173,6 +174,8 @@ size_t workspace_for(const Shape& s, int op) {
       return attn_workspace_bytes(s, true);
     case INFLLMV2_OP_DECODE_STEP:
       return decode_step_cluster_size(s) ? 0 : select_workspace_bytes(s) + attn_workspace_bytes(s, false);
+    case INFLLMV2_OP_BACKWARD:
+      return attn_bwd_supported(s) ? attn_bwd_workspace_bytes(s) : 0;
     default:
       return 0;
   }
@@ -460,6 +463,44 @@ int infllmv2_decode_step(const infllmv2_params* p, const void* q, int32_t n_q, c
     e = launch_attn(s, false, qm, km, vm, kv_lens, block_idx, n_selected, out, lse,
                     static_cast<unsigned char*>(workspace) + sel_ws, status, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode_step (attend)");
+    return INFLLMV2_OK;
+  });
+}
+
+int infllmv2_sparse_attn_backward(const infllmv2_params* p, const void* q, int32_t n_q, const void* k_cache,
+                                  const void* v_cache, const int32_t* kv_lens, const int32_t* block_idx,
+                                  const int32_t* n_selected, const void* out, const float* lse, const void* dout,
+                                  float* dq, float* dk, float* dv, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+  INFLLMV2_GUARD({
+    Shape s;
+    int rc = check_params(p, n_q, &s);
+    if (rc) return rc;
+    if (!q || !k_cache || !v_cache || !kv_lens || !block_idx || !n_selected || !out || !lse || !dout || !dq ||
+        !dk || !dv)
+      return fail(INFLLMV2_INVALID_ARGUMENT, "a required pointer is NULL");
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(dout) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(lse))
+      return fail(INFLLMV2_UNSUPPORTED, "tensor pointers must be 16-byte aligned");
+    if (!attn_bwd_supported(s)) return fail(INFLLMV2_UNSUPPORTED, "too many (query, block) pairs for the index");
+    const size_t need = attn_bwd_workspace_bytes(s);
+    if (!workspace || workspace_bytes < need)
+      return fail(INFLLMV2_WORKSPACE_TOO_SMALL, "workspace needs %zu bytes (got %zu)", need, workspace_bytes);
+    if (!aligned16(workspace)) return fail(INFLLMV2_UNSUPPORTED, "workspace must be 16-byte aligned");
+    uint32_t* status = status_ptr();
+    if (!status) return fail(INFLLMV2_CUDA_ERROR, "no device status word (no current CUDA device?)");
+    CUtensorMap qm, dom, km, vm, km32, vm32;
+    const uint64_t kv_rows = static_cast<uint64_t>(s.B) * s.Hkv * s.Lmax;
+    const uint64_t q_rows = static_cast<uint64_t>(s.B) * s.nq * s.Hkv * kGroup;
+    if ((rc = make_map(&qm, q, q_rows, 16, "q"))) return rc;
+    if ((rc = make_map(&dom, dout, q_rows, 16, "dout"))) return rc;
+    if ((rc = make_map(&km, k_cache, kv_rows, 64, "k_cache"))) return rc;
+    if ((rc = make_map(&vm, v_cache, kv_rows, 64, "v_cache"))) return rc;
+    if ((rc = make_map(&km32, k_cache, kv_rows, 32, "k_cache"))) return rc;
+    if ((rc = make_map(&vm32, v_cache, kv_rows, 32, "v_cache"))) return rc;
+    cudaError_t e = launch_attn_bwd(s, qm, dom, km, vm, km32, vm32, q, kv_lens, block_idx, n_selected, out, lse,
+                                    dout, dq, dk, dv, workspace, status, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "sparse_attn_backward");
     return INFLLMV2_OK;
   });
 }

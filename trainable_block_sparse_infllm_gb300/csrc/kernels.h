@@ -16,6 +16,7 @@ struct Shape {
   int topk, n_init, n_local, inc_forced;
   float score_scale2;  // score_scale * log2(e)
   float attn_scale2;   // attn_scale * log2(e)
+  float attn_scale;
 };
 
 // ---- stage 1 ---------------------------------------------------------------
@@ -61,5 +62,17 @@ cudaError_t launch_decode_step(const Shape& s, int cluster, const CUtensorMap& k
                                const CUtensorMap& k_map, const CUtensorMap& v_map, const void* k,
                                const int32_t* kv_lens, void* kc, int32_t* block_idx, int32_t* n_sel, void* out,
                                float* lse, uint32_t* status, cudaStream_t st);
+
+// ---- backward of stage 3 (fixed selection) --------------------------------
+size_t attn_bwd_workspace_bytes(const Shape& s);
+bool attn_bwd_supported(const Shape& s);
+// q_map / do_map: 16-row boxes over q / dout; k_map / v_map: 64-row boxes;
+// k_map32 / v_map32: 32-row boxes over the caches.
+cudaError_t launch_attn_bwd(const Shape& s, const CUtensorMap& q_map, const CUtensorMap& do_map,
+                            const CUtensorMap& k_map, const CUtensorMap& v_map, const CUtensorMap& k_map32,
+                            const CUtensorMap& v_map32, const void* q, const int32_t* kv_lens,
+                            const int32_t* block_idx, const int32_t* n_sel, const void* out, const float* lse,
+                            const void* dout, float* dq, float* dk, float* dv, void* ws, uint32_t* status,
+                            cudaStream_t st);
 
 }  // namespace infllmv2
