@@ -332,6 +332,25 @@ def prefill_line(dev, steps, warmup, peaks):
                 total += len(e)
     coarse = {"window": sc, "select_ms": t_csel * 1e3, "coarse_means_ms": t_cmeans * 1e3,
               "select_speedup": t_stage["select"] / t_csel, "selection_overlap": kept / max(total, 1)}
+
+    # Backward of the attention with this selection held fixed (dq, dk, dv in
+    # fp32 for a seeded upstream gradient).  Algorithmic FLOPs: five products
+    # of 2 d per (query head, attended key) pair (q K^T, dO V^T, dS K, dS^T q,
+    # P^T dO); the kernels recompute q K^T and dO V^T once more each.
+    dout = up(S.make_grad_out(wl, seed=wl.seed + 2000))
+    dq = torch.empty((B, nq, wl.n_heads, wl.head_dim), dtype=torch.float32, device=dev)
+    dk = torch.empty((B, H, wl.kv_len, wl.head_dim), dtype=torch.float32, device=dev)
+    dv = torch.empty_like(dk)
+    ws_bwd = T.alloc_workspace(p, nq, T.OP_BACKWARD, dev)
+    t_bwd = timed(lambda: T.sparse_attn_backward(p, q, k, v, lens, idx, nsel, out, lse, dout, dq, dk, dv, ws_bwd),
+                  steps)
+    bflops = 10.0 * wl.head_dim * pairs * wl.group
+    b_achieved = bflops / t_bwd / 1e12
+    backward = {"ms": t_bwd * 1e3, "tokens_per_s": B * nq / t_bwd,
+                "kernels": "index (count, scan, fill), bwd_dq_kernel (mma.sync), bwd_dkdv_kernel (tcgen05)",
+                "roofline": {"bound": "tensor", "achieved": b_achieved, "peak": peaks[1], "unit": "TFLOP/s",
+                             "frac": b_achieved / peaks[1], "peak_kind": peaks[3] + " burst bf16",
+                             "algorithmic_flop_per_call": bflops}}
     return {
         "workload": f"{PREFILL}: batch 1, 32 q / 2 kv heads, causal 32768 x 32768, top-64 + init + local",
         "tokens_per_s": B * nq / t_step,
@@ -342,6 +361,7 @@ def prefill_line(dev, steps, warmup, peaks):
                      "frac": achieved / peaks[1], "peak_kind": peaks[3] + " burst bf16",
                      "algorithmic_flop_per_launch": flops, "traffic": _traffic("attn_tc_kernel", PREFILL)},
         "coarse_lse": coarse,
+        "backward": backward,
     }
 
 
@@ -407,7 +427,8 @@ def reference_arm(args):
 def profile_passes(path, n):
     """n passes of one path on a single input copy, nothing timed: the decode
     path is one decode_step launch per pass (decode_128k, 0.57 GB of inputs);
-    the prefill path is compress + select + attention (prefill_32k)."""
+    the prefill path is compress + select + attention (prefill_32k); the
+    backward path is one forward, then n backward calls (prefill_32k)."""
     import torch
     import __graft_entry__
     __graft_entry__.build()
@@ -435,6 +456,18 @@ def profile_passes(path, n):
         ws = T.alloc_workspace(p, nq, T.OP_DECODE_STEP, dev)
         for _ in range(n):
             T.decode_step(p, q, k, v, lens, kc, idx, nsel, out, lse, ws)
+    elif path == "backward":
+        ws_sel = T.alloc_workspace(p, nq, T.OP_SELECT, dev)
+        ws_att = T.alloc_workspace(p, nq, T.OP_PREFILL, dev)
+        T.select_blocks(p, q, kc, lens, idx, nsel, None, ws_sel)
+        T.sparse_attn_prefill(p, q, k, v, lens, idx, nsel, out, lse, ws_att)
+        dout = up(S.make_grad_out(wl, seed=wl.seed + 2000))
+        dq = torch.empty((B, nq, wl.n_heads, wl.head_dim), dtype=torch.float32, device=dev)
+        dk = torch.empty((B, H, wl.kv_len, wl.head_dim), dtype=torch.float32, device=dev)
+        dv = torch.empty_like(dk)
+        ws_bwd = T.alloc_workspace(p, nq, T.OP_BACKWARD, dev)
+        for _ in range(n):
+            T.sparse_attn_backward(p, q, k, v, lens, idx, nsel, out, lse, dout, dq, dk, dv, ws_bwd)
     else:
         ws_sel = T.alloc_workspace(p, nq, T.OP_SELECT, dev)
         ws_att = T.alloc_workspace(p, nq, T.OP_PREFILL, dev)
@@ -458,7 +491,7 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["decode", "prefill"],
+    ap.add_argument("--profile", choices=["decode", "prefill", "backward"],
                     help="run warmup + steps untimed passes of one path on one input copy and exit "
                          "(a small, fixed launch sequence for ncu)")
     args = ap.parse_args()

@@ -489,16 +489,16 @@ int infllmv2_sparse_attn_backward(const infllmv2_params* p, const void* q, int32
     if (!aligned16(workspace)) return fail(INFLLMV2_UNSUPPORTED, "workspace must be 16-byte aligned");
     uint32_t* status = status_ptr();
     if (!status) return fail(INFLLMV2_CUDA_ERROR, "no device status word (no current CUDA device?)");
-    CUtensorMap qm, dom, km, vm, km32, vm32;
+    CUtensorMap qm, dom, km, vm, km16, vm16;
     const uint64_t kv_rows = static_cast<uint64_t>(s.B) * s.Hkv * s.Lmax;
     const uint64_t q_rows = static_cast<uint64_t>(s.B) * s.nq * s.Hkv * kGroup;
     if ((rc = make_map(&qm, q, q_rows, 16, "q"))) return rc;
     if ((rc = make_map(&dom, dout, q_rows, 16, "dout"))) return rc;
     if ((rc = make_map(&km, k_cache, kv_rows, 64, "k_cache"))) return rc;
     if ((rc = make_map(&vm, v_cache, kv_rows, 64, "v_cache"))) return rc;
-    if ((rc = make_map(&km32, k_cache, kv_rows, 32, "k_cache"))) return rc;
-    if ((rc = make_map(&vm32, v_cache, kv_rows, 32, "v_cache"))) return rc;
-    cudaError_t e = launch_attn_bwd(s, qm, dom, km, vm, km32, vm32, q, kv_lens, block_idx, n_selected, out, lse,
+    if ((rc = make_map(&km16, k_cache, kv_rows, 16, "k_cache"))) return rc;
+    if ((rc = make_map(&vm16, v_cache, kv_rows, 16, "v_cache"))) return rc;
+    cudaError_t e = launch_attn_bwd(s, qm, dom, km, vm, km16, vm16, q, kv_lens, block_idx, n_selected, out, lse,
                                     dout, dq, dk, dv, workspace, status, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "sparse_attn_backward");
     return INFLLMV2_OK;

@@ -16,7 +16,7 @@
 //     kBkChunk tokens.
 //   * bwd_dq_kernel, query-centric on the warp-level tensor cores: one warp
 //     per (b, h_kv, t) unit (its 16 heads are the 16 MMA rows, [InfLLM v2 >
-//     Query group sharing]) walks the unit's selected blocks in 32-key halves
+//     Query group sharing]) walks the unit's selected blocks in 16-key quarters
 //     (K and V TMA-staged in a per-warp ring) and accumulates dq in
 //     registers; it also writes D for the second kernel.
 //   * bwd_dkdv_kernel, key-centric on tcgen05/TMEM: one CTA per work item
@@ -176,28 +176,29 @@ __global__ void __launch_bounds__(kScanThreads) bwd_scan_kernel(BwdParams p) {
 
 // -------------------------------------------------------------------- dq --
 
-constexpr int kBqWarps = 4;
-constexpr int kBqStages = 3;            // 32-key halves in flight per warp
-constexpr int kBqStageBytes = 16384;    // K then V, 32 rows x 128 bf16 each
+constexpr int kBqWarps = 8;
+constexpr int kBqStages = 3;            // 16-key quarters of a block in flight per warp
+constexpr int kBqRows = 16;
+constexpr int kBqStageBytes = 8192;     // K then V, 16 rows x 128 bf16 each
 constexpr int kBqSmem = 1024 + kBqWarps * kBqStages * kBqStageBytes + kBqWarps * kBqStages * 8;
 
-// First valid half-block position (2 n + half) at or after `pos`: entry n
-// must name a block in [0, c]; its second half must start at or before i.
-__device__ __forceinline__ int next_half(const int32_t* sel, int ns, int c, int i, int pos) {
-  while (pos < 2 * ns) {
-    const int n = pos >> 1;
+// First valid quarter position (4 n + part) at or after `pos`: entry n must
+// name a block in [0, c]; a quarter must start at or before i.
+__device__ __forceinline__ int next_part(const int32_t* sel, int ns, int c, int i, int pos) {
+  while (pos < 4 * ns) {
+    const int n = pos >> 2;
     const int j = sel[n];
-    if (j < 0 || j > c || ((pos & 1) && j * kBlock + 32 > i)) {
-      pos = 2 * (n + 1);
+    if (j < 0 || j > c || j * kBlock + (pos & 3) * kBqRows > i) {
+      pos = 4 * (n + 1);
       continue;
     }
     return pos;
   }
-  return 2 * ns;
+  return 4 * ns;
 }
 
 __global__ void __launch_bounds__(kBqWarps * 32, 1)
-    bwd_dq_kernel(const __grid_constant__ CUtensorMap k_map32, const __grid_constant__ CUtensorMap v_map32,
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap k_map16, const __grid_constant__ CUtensorMap v_map16,
                   BwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -205,8 +206,8 @@ __global__ void __launch_bounds__(kBqWarps * 32, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, tq = lane & 3;
   if (tid == 0) {
-    prefetch_tensormap(&k_map32);
-    prefetch_tensormap(&v_map32);
+    prefetch_tensormap(&k_map16);
+    prefetch_tensormap(&v_map16);
     for (int s = 0; s < kBqWarps * kBqStages; ++s) mbar_init(&bars[s], 1);
     fence_barrier_init();
   }
@@ -236,19 +237,19 @@ __global__ void __launch_bounds__(kBqWarps * 32, 1)
   const size_t kv_row0 = static_cast<size_t>(bh) * p.Lmax;
 
   auto issue = [&](int pos, int st) {
-    const int row = static_cast<int>(kv_row0 + static_cast<size_t>(sel[pos >> 1]) * kBlock + (pos & 1) * 32);
+    const int row = static_cast<int>(kv_row0 + static_cast<size_t>(sel[pos >> 2]) * kBlock + (pos & 3) * kBqRows);
     uint8_t* dst = ring + st * kBqStageBytes;
     mbar_arrive_expect_tx(&full[st], kBqStageBytes);
-    tma_load_2d(dst, &k_map32, 0, row, &full[st]);
-    tma_load_2d(dst + 4096, &k_map32, 64, row, &full[st]);
-    tma_load_2d(dst + 8192, &v_map32, 0, row, &full[st]);
-    tma_load_2d(dst + 12288, &v_map32, 64, row, &full[st]);
+    tma_load_2d(dst, &k_map16, 0, row, &full[st]);
+    tma_load_2d(dst + 2048, &k_map16, 64, row, &full[st]);
+    tma_load_2d(dst + 4096, &v_map16, 0, row, &full[st]);
+    tma_load_2d(dst + 6144, &v_map16, 64, row, &full[st]);
   };
-  // Prologue: the first kBqStages halves.
-  int pi = next_half(sel, ns, c, i, 0);
-  for (int s = 0; s < kBqStages && pi < 2 * ns; ++s) {
+  // Prologue: the first kBqStages quarters.
+  int pi = next_part(sel, ns, c, i, 0);
+  for (int s = 0; s < kBqStages && pi < 4 * ns; ++s) {
     if (lane == 0) issue(pi, s);
-    pi = next_half(sel, ns, c, i, pi + 1);
+    pi = next_part(sel, ns, c, i, pi + 1);
   }
 
   // q, dO and O rows of the unit straight from global memory into A
@@ -300,46 +301,56 @@ __global__ void __launch_bounds__(kBqWarps * 32, 1)
   for (int x = 0; x < 16; ++x) acc[x][0] = acc[x][1] = acc[x][2] = acc[x][3] = 0.f;
 
   bool ok = true;
-  int pc = next_half(sel, ns, c, i, 0);
-  for (int n = 0; pc < 2 * ns; ++n) {
+  int pc = next_part(sel, ns, c, i, 0);
+  for (int n = 0; pc < 4 * ns; ++n) {
     const int st = n % kBqStages;
     ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (n / kBqStages) & 1, p.status));
     if (!ok) break;
     uint8_t* stage = ring + st * kBqStageBytes;
-    const uint32_t k_b = smem_u32(stage), v_b = k_b + 8192;
-    const int key0 = sel[pc >> 1] * kBlock + (pc & 1) * 32;
-    if (key0 + 31 > i) {
+    const uint32_t k_b = smem_u32(stage), v_b = k_b + 4096;
+    const int key0 = sel[pc >> 2] * kBlock + (pc & 3) * kBqRows;
+    if (key0 + kBqRows - 1 > i) {
       // Keys past i: zero their K rows (dS is 0 there; the cache rows past
       // kv_len may hold non-finite values).
       const int r0 = i - key0 + 1;
-      for (int e = lane; e < (32 - r0) * 16; e += 32) {
+      for (int e = lane; e < (kBqRows - r0) * 16; e += 32) {
         const int row = r0 + (e >> 4), q16 = e & 15;
-        *reinterpret_cast<uint4*>(stage + (q16 >> 3) * 4096 + row * 128 + (q16 & 7) * 16) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(stage + (q16 >> 3) * 2048 + row * 128 + (q16 & 7) * 16) = make_uint4(0, 0, 0, 0);
       }
       __syncwarp();
     }
-    // S = q K^T and dP = dO V^T for 32 keys (4 n-tiles of 8).
-    float s[4][4], dp[4][4];
+    // S = q K^T and dP = dO V^T for 16 keys (2 n-tiles of 8); the four
+    // accumulators advance together over the 8 k-steps.
+    float s[2][4], dp[2][4];
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
+    for (int nt = 0; nt < 2; ++nt) {
       s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
       dp[nt][0] = dp[nt][1] = dp[nt][2] = dp[nt][3] = 0.f;
+    }
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        uint32_t kb[4], vb[4];
-        const uint32_t o = swz128_offset(nt * 8 + (lane & 7), 4 * kk + (lane >> 3), 32);
-        ldmatrix_x4(kb, k_b + o);
-        ldmatrix_x4(vb, v_b + o);
-        mma_bf16_16816(s[nt], qa[2 * kk], kb[0], kb[1]);
-        mma_bf16_16816(s[nt], qa[2 * kk + 1], kb[2], kb[3]);
-        mma_bf16_16816(dp[nt], da[2 * kk], vb[0], vb[1]);
-        mma_bf16_16816(dp[nt], da[2 * kk + 1], vb[2], vb[3]);
+    for (int kk = 0; kk < 4; ++kk) {
+      uint32_t kb[2][4], vb[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const uint32_t o = swz128_offset(nt * 8 + (lane & 7), 4 * kk + (lane >> 3), kBqRows);
+        ldmatrix_x4(kb[nt], k_b + o);
+        ldmatrix_x4(vb[nt], v_b + o);
+      }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        mma_bf16_16816(s[nt], qa[2 * kk], kb[nt][0], kb[nt][1]);
+        mma_bf16_16816(dp[nt], da[2 * kk], vb[nt][0], vb[nt][1]);
+      }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        mma_bf16_16816(s[nt], qa[2 * kk + 1], kb[nt][2], kb[nt][3]);
+        mma_bf16_16816(dp[nt], da[2 * kk + 1], vb[nt][2], vb[nt][3]);
       }
     }
     // dS = P (dP - D) with P = 2^(s scale2 - lse2); 0 past i.
-    uint32_t ah[2][4], al[2][4];
+    uint32_t ah[4], al[4];
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
+    for (int nt = 0; nt < 2; ++nt) {
       const int x = key0 + nt * 8 + 2 * tq;
       const bool v0 = x <= i, v1 = x + 1 <= i;
       const float p0 = (v0 && ok0) ? fast_exp2(fmaf(s[nt][0], p.scale2, -m0)) : 0.f;
@@ -353,33 +364,29 @@ __global__ void __launch_bounds__(kBqWarps * 32, 1)
       const __nv_bfloat162 h01 = __floats2bfloat162_rn(e0, e1);
       const __nv_bfloat162 h23 = __floats2bfloat162_rn(e2, e3);
       const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
-      ah[nt >> 1][(nt & 1) * 2 + 0] = *reinterpret_cast<const uint32_t*>(&h01);
-      ah[nt >> 1][(nt & 1) * 2 + 1] = *reinterpret_cast<const uint32_t*>(&h23);
-      al[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(e0 - f01.x, e1 - f01.y);
-      al[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(e2 - f23.x, e3 - f23.y);
+      ah[nt * 2 + 0] = *reinterpret_cast<const uint32_t*>(&h01);
+      ah[nt * 2 + 1] = *reinterpret_cast<const uint32_t*>(&h23);
+      al[nt * 2 + 0] = pack_bf16x2(e0 - f01.x, e1 - f01.y);
+      al[nt * 2 + 1] = pack_bf16x2(e2 - f23.x, e3 - f23.y);
     }
-    // dq += dS K: B = K (32 keys x 128 dims) through ldmatrix.trans.
+    // dq += dS K: B = K (16 keys x 128 dims) through ldmatrix.trans.
 #pragma unroll
     for (int np = 0; np < 8; ++np) {
-#pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        uint32_t kb[4];
-        ldmatrix_x4_trans(kb, k_b + swz128_offset(kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8,
-                                                  2 * np + (lane >> 4), 32));
-        mma_bf16_16816(acc[2 * np], ah[kk], kb[0], kb[1]);
-        mma_bf16_16816(acc[2 * np + 1], ah[kk], kb[2], kb[3]);
-        mma_bf16_16816(acc[2 * np], al[kk], kb[0], kb[1]);
-        mma_bf16_16816(acc[2 * np + 1], al[kk], kb[2], kb[3]);
-      }
+      uint32_t kb[4];
+      ldmatrix_x4_trans(kb, k_b + swz128_offset((lane & 7) + ((lane >> 3) & 1) * 8, 2 * np + (lane >> 4), kBqRows));
+      mma_bf16_16816(acc[2 * np], ah, kb[0], kb[1]);
+      mma_bf16_16816(acc[2 * np + 1], ah, kb[2], kb[3]);
+      mma_bf16_16816(acc[2 * np], al, kb[0], kb[1]);
+      mma_bf16_16816(acc[2 * np + 1], al, kb[2], kb[3]);
     }
-    pc = next_half(sel, ns, c, i, pc + 1);
-    if (pi < 2 * ns) {
+    pc = next_part(sel, ns, c, i, pc + 1);
+    if (pi < 4 * ns) {
       // The stage is free again (its reads are done); order any zeroed rows
       // before the TMA refill.
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) issue(pi, st);
-      pi = next_half(sel, ns, c, i, pi + 1);
+      pi = next_part(sel, ns, c, i, pi + 1);
     }
   }
   __syncwarp();
@@ -498,15 +505,15 @@ __global__ void __launch_bounds__(kBkThreads, 1)
         fence_proxy_async_smem();
       }
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bars[kBTFull + st], nt_tok * 8192);
-        for (int tt = 0; tt < nt_tok; ++tt) {
-          const int row = (b * p.nq + toks[n * kBkTokens + tt]) * Hq + h * kGroup;
-          tma_load_2d(tile + tt * 2048, &q_map, 0, row, &bars[kBTFull + st]);
-          tma_load_2d(tile + 16384 + tt * 2048, &q_map, 64, row, &bars[kBTFull + st]);
-          tma_load_2d(tile + 32768 + tt * 2048, &do_map, 0, row, &bars[kBTFull + st]);
-          tma_load_2d(tile + 49152 + tt * 2048, &do_map, 64, row, &bars[kBTFull + st]);
-        }
+      // One box per lane (token tt = lane / 4; q / dO, column half), after
+      // lane 0 has set the transaction count.
+      if (lane == 0) mbar_arrive_expect_tx(&bars[kBTFull + st], nt_tok * 8192);
+      __syncwarp();
+      if (lane < nt_tok * 4) {
+        const int tt = lane >> 2, part = lane & 3;
+        const int row = (b * p.nq + toks[n * kBkTokens + tt]) * Hq + h * kGroup;
+        tma_load_2d(tile + part * 16384 + tt * 2048, (part & 2) ? &do_map : &q_map, (part & 1) * 64, row,
+                    &bars[kBTFull + st]);
       }
       __syncwarp();
     }
@@ -519,12 +526,18 @@ __global__ void __launch_bounds__(kBkThreads, 1)
       const uint64_t v_desc = tc::sdesc_sw128(base_s + kOffKV + 16384, 16, 1024);
       const uint32_t ps = base_s + kOffPS;
       bool ok = mbar_wait(&bars[kBKv], 0, p.status);
-      for (int n = 0; n <= ntile && ok; ++n) {
-        if (n < ntile) {
-          const int st = n % kBkStages, sb = n & 1;
-          ok = mbar_wait(&bars[kBTFull + st], (n / kBkStages) & 1, p.status);
-          if (ok && n >= 2) ok = mbar_wait(&bars[kBSFree + sb], ((n >> 1) - 1) & 1, p.status);
-          if (!ok) break;
+      // Two in-order streams, issued as their inputs arrive: S and dP of tile
+      // n_s (its q / dO stage loaded, its S / dP buffer read out by the rows
+      // two tiles back) and the dV / dK products of tile n_g (its P and dS
+      // written).  Neither waits behind the other: the dV / dK products free
+      // a stage for the next load, S feeds the row warps.
+      int n_s = 0, n_g = 0;
+      uint32_t idle = 0;
+      while (ok && n_g < ntile) {
+        bool progressed = false;
+        if (n_s < ntile && mbar_try_wait(&bars[kBTFull + n_s % kBkStages], (n_s / kBkStages) & 1) &&
+            (n_s < 2 || mbar_try_wait(&bars[kBSFree + (n_s & 1)], ((n_s >> 1) - 1) & 1))) {
+          const int st = n_s % kBkStages, sb = n_s & 1;
           tc::fence_after_sync();
           const uint32_t tile = base_s + kOffTile + st * kBkTileBytes;
           const uint64_t q_desc = tc::sdesc_sw128(tile, 16, 1024);
@@ -537,10 +550,11 @@ __global__ void __launch_bounds__(kBkThreads, 1)
             tc::mma_ss(tmem + kColDP + sb * 64, o_desc + ta, v_desc + tb, kIdS, k > 0 ? 1u : 0u);
           }
           tc::commit(&bars[kBSFull + sb]);
+          ++n_s;
+          progressed = true;
         }
-        if (n >= 1) {
-          const int m = n - 1, st = m % kBkStages;
-          if (!mbar_wait(&bars[kBPFull], m & 1, p.status)) break;
+        if (n_g < n_s && mbar_try_wait(&bars[kBPFull], n_g & 1)) {
+          const int m = n_g, st = m % kBkStages;
           tc::fence_after_sync();
           const uint32_t tile = base_s + kOffTile + st * kBkTileBytes;
           // dO^T and q^T: M = 128 dims in two 64-column boxes (16 KB apart),
@@ -563,6 +577,14 @@ __global__ void __launch_bounds__(kBkThreads, 1)
           tc::commit(&bars[kBTEmpty + st]);
           tc::commit(&bars[kBPFree]);
           if (m == ntile - 1) tc::commit(&bars[kBAcc]);
+          ++n_g;
+          progressed = true;
+        }
+        if (progressed) {
+          idle = 0;
+        } else if (++idle > 4 * kSpinLimit) {
+          atomicOr(p.status, kStatusTimeout);
+          ok = false;
         }
       }
     }
@@ -576,22 +598,32 @@ __global__ void __launch_bounds__(kBkThreads, 1)
     uint8_t* ps = smem + kOffPS;
     const int key0 = j * kBlock;
     bool ok = true;
+    // The row's lse and D, loaded one tile ahead.
+    auto row_inputs = [&](int n, float& lse, float& dsum, int& t) {
+      const int slot = n * kBkTokens + (r >> 4);
+      lse = -INFINITY;
+      dsum = 0.f;
+      t = 0;
+      if (n < ntile && slot < ntok) {
+        t = toks[slot];
+        const size_t grow = (static_cast<size_t>(b) * p.nq + t) * Hq + h * kGroup + (r & 15);
+        lse = p.lse[grow];
+        dsum = p.dsum[grow];
+      }
+    };
+    float lse_n, dsum_n;
+    int t_n;
+    row_inputs(0, lse_n, dsum_n, t_n);
     for (int n = 0; n < ntile; ++n) {
       const int sb = n & 1;
-      const int slot = n * kBkTokens + (r >> 4);
-      const bool active = slot < ntok;
-      float m2 = 0.f, dsum = 0.f;
+      float m2 = 0.f;
+      const float dsum = dsum_n;
       int nv = 0;
-      if (active) {
-        const int t = toks[slot];
-        const size_t grow = (static_cast<size_t>(b) * p.nq + t) * Hq + h * kGroup + (r & 15);
-        const float lse = p.lse[grow];
-        dsum = p.dsum[grow];
-        if (lse > -INFINITY) {
-          m2 = lse * kLog2e;
-          nv = min(kBlock, L - p.nq + t - key0 + 1);   // keys key0 .. key0 + nv - 1 are <= i
-        }
+      if (lse_n > -INFINITY) {
+        m2 = lse_n * kLog2e;
+        nv = min(kBlock, L - p.nq + t_n - key0 + 1);   // keys key0 .. key0 + nv - 1 are <= i
       }
+      row_inputs(n + 1, lse_n, dsum_n, t_n);
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars[kBSFull + sb], (n >> 1) & 1, p.status));
       tc::fence_after_sync();
       uint32_t sv[64], dpv[64];
@@ -714,8 +746,8 @@ bool attn_bwd_supported(const Shape& s) {
 }
 
 cudaError_t launch_attn_bwd(const Shape& s, const CUtensorMap& q_map, const CUtensorMap& do_map,
-                            const CUtensorMap& k_map, const CUtensorMap& v_map, const CUtensorMap& k_map32,
-                            const CUtensorMap& v_map32, const void* q, const int32_t* kv_lens,
+                            const CUtensorMap& k_map, const CUtensorMap& v_map, const CUtensorMap& k_map16,
+                            const CUtensorMap& v_map16, const void* q, const int32_t* kv_lens,
                             const int32_t* block_idx, const int32_t* n_sel, const void* out, const float* lse,
                             const void* dout, float* dq, float* dk, float* dv, void* ws, uint32_t* status,
                             cudaStream_t st) {
@@ -777,7 +809,7 @@ cudaError_t launch_attn_bwd(const Shape& s, const CUtensorMap& q_map, const CUte
   if (e != cudaSuccess) return e;
   const long long units = static_cast<long long>(s.B) * s.Hkv * s.nq;
   bwd_dq_kernel<<<static_cast<unsigned>((units + kBqWarps - 1) / kBqWarps), kBqWarps * 32, kBqSmem, st>>>(
-      k_map32, v_map32, p);
+      k_map16, v_map16, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   e = cudaFuncSetAttribute(bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBkSmem);

@@ -67,10 +67,10 @@ cudaError_t launch_decode_step(const Shape& s, int cluster, const CUtensorMap& k
 size_t attn_bwd_workspace_bytes(const Shape& s);
 bool attn_bwd_supported(const Shape& s);
 // q_map / do_map: 16-row boxes over q / dout; k_map / v_map: 64-row boxes;
-// k_map32 / v_map32: 32-row boxes over the caches.
+// k_map16 / v_map16: 16-row boxes over the caches.
 cudaError_t launch_attn_bwd(const Shape& s, const CUtensorMap& q_map, const CUtensorMap& do_map,
-                            const CUtensorMap& k_map, const CUtensorMap& v_map, const CUtensorMap& k_map32,
-                            const CUtensorMap& v_map32, const void* q, const int32_t* kv_lens,
+                            const CUtensorMap& k_map, const CUtensorMap& v_map, const CUtensorMap& k_map16,
+                            const CUtensorMap& v_map16, const void* q, const int32_t* kv_lens,
                             const int32_t* block_idx, const int32_t* n_sel, const void* out, const float* lse,
                             const void* dout, float* dq, float* dk, float* dv, void* ws, uint32_t* status,
                             cudaStream_t st);
