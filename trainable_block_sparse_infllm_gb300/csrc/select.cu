@@ -13,9 +13,13 @@
 // Two paths, same result:
 //  * decode / verify (n_q <= 16): select_decode.cu, one thread-block cluster
 //    per (b, h_kv) group.
-//  * prefill (n_q > 16): one warp per query token, TT tokens per CTA sharing
-//    a TMA pipeline of 64-kernel hi/lo tiles, streamed twice (pass 1: LSE,
-//    pass 2: normalised group mean and block maxima), then a warp top-k.
+//  * prefill (n_q > 16): select_tc.cu on tcgen05 (8 tokens x 16 heads per
+//    128-row tile); here, the mma.sync form of the same two passes, used for
+//    the coarse-LSE approximation and for caches whose block scores do not
+//    fit the tcgen05 kernel's shared memory: one warp per query token, TT
+//    tokens per CTA sharing a TMA pipeline of 64-kernel hi/lo tiles, streamed
+//    twice (pass 1: LSE, pass 2: normalised group mean and block maxima),
+//    then a warp top-k.
 #include "select_common.cuh"
 
 namespace infllmv2 {
@@ -32,6 +36,9 @@ int device_sm_count() {
   return cache[dev];
 }
 
+bool select_tc_supported(const Shape& s);
+cudaError_t launch_select_tc(const Shape& s, const CUtensorMap& kc_map, const CUtensorMap& q_map, const SelParams& p,
+                             cudaStream_t st);
 size_t select_decode_ncpad(const Shape& s);
 bool select_decode_supported(const Shape& s);
 cudaError_t launch_select_decode(const Shape& s, const CUtensorMap& kc_map, const CUtensorMap& q_map,
@@ -342,7 +349,9 @@ cudaError_t launch_select(const Shape& s, const CUtensorMap& kc_map, const CUten
     p.z = static_cast<float*>(ws);
     return launch_select_decode(s, kc_map, q_map, p, st);
   }
-
+  // Prefill: the tcgen05 kernel where its shared memory holds the block
+  // scores of 8 tokens, the mma.sync kernel otherwise.
+  if (select_tc_supported(s)) return launch_select_tc(s, kc_map, q_map, p, st);
   return launch_prefill_select(s, kc_map, kc_map, q_map, p, st);
 }
 

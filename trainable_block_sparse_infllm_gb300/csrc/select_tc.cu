@@ -1,0 +1,306 @@
+// Stage 2 of InfLLM v2 for prefill on the 5th-generation tensor cores.
+//
+// [InfLLM v2 > Semantic kernels, eqs. r_kernel, r_block], [> Query group
+// sharing, eq. r_group], [> Top-K implementation and the LSE bottleneck]:
+// for each query token of a GQA group,
+//   z[h, j] = score_scale * q_h . Mean_j        (visible kernels j)
+//   g[j]    = (1/16) sum_h 2^(z[h, j] - lse_h)  (exact two-pass LSE, base 2)
+//   r[blk]  = max of g over the kernels meeting the block,
+// then the top-k with forced blocks ([> Initial and local tokens always
+// selected]).
+//
+// One CTA per 8 consecutive tokens of one (b, h_kv): their 8 x 16 heads are
+// the 128 rows of the tcgen05 tile and share every 64-kernel chunk of kernel
+// means (causality gives the 8 tokens the same kernels but for the last one
+// or two).  z = q . hi + q . lo accumulates in TMEM (M 128, N 64, K 128, hi and
+// lo as two products into one accumulator).  The chunks are streamed twice:
+//   pass 1: each row thread keeps its head's running (max, sum of 2^z);
+//   pass 2: each row thread forms 2^(z - lse) for its head, and the 16 lanes
+//           of a token reduce-scatter the 64 kernels so that lane x ends with
+//           the group sums of kernels 4x .. 4x + 3 of the chunk, which with
+//           kernel 4x - 1 from its neighbour are exactly the kernels meeting
+//           block (chunk / 4 + x): one block maximum per lane.
+// Roles (192 threads): warps 0-3 rows (row r = 32 w + lane: token r / 16,
+// head r % 16), warp 4 MMA issuer (one thread), warp 5 TMA producer.  The
+// row warps end with the warp top-k of their own two tokens.
+#include "select_common.cuh"
+#include "tc.cuh"
+
+namespace infllmv2 {
+
+namespace {
+
+constexpr int kStTokens = 8;
+constexpr int kStChunk = 64;               // kernels per chunk
+constexpr int kStStages = 3;
+constexpr int kStChunkBytes = 32768;       // hi then lo: 64 rows x 256 B each
+constexpr int kStThreads = 192;
+constexpr int kStMmaWarp = 4, kStTmaWarp = 5;
+constexpr uint32_t kStTmemCols = 128;      // two z buffers of 64 columns
+
+struct StLayout {
+  int ring, q, r, flag, tk, bars, slot, total;
+};
+
+__host__ __device__ inline StLayout st_layout(int nbmax) {
+  StLayout l;
+  l.ring = 0;
+  l.q = kStStages * kStChunkBytes;                      // two 64-column boxes x 128 rows
+  l.r = l.q + 32768;                                    // [8 tokens][nbmax] block scores
+  l.flag = l.r + kStTokens * nbmax * 4;                 // [8 tokens][nbmax] top-k flags
+  l.tk = (l.flag + kStTokens * nbmax + 15) & ~15;       // 4 warp top-k scratches
+  l.bars = (l.tk + 4 * static_cast<int>(sizeof(TopkScratch<32>)) + 15) & ~15;
+  l.slot = l.bars + 16 * 8;
+  l.total = l.slot + 16;
+  return l;
+}
+
+enum StBar { kFull = 0, kEmpty = kFull + kStStages, kQ = kEmpty + kStStages, kZFull = kQ + 1, kZFree = kZFull + 2,
+             kStNumBars = kZFree + 2 };
+static_assert(kStNumBars <= 16, "barrier area holds 16");
+
+__global__ void __launch_bounds__(kStThreads, 1)
+    sel_tc_kernel(const __grid_constant__ CUtensorMap kc_map, const __grid_constant__ CUtensorMap q_map, SelParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const StLayout lay = st_layout(p.nbmax);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + lay.bars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + lay.slot);
+  float* r_all = reinterpret_cast<float*>(smem + lay.r);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int bh = b * p.Hkv + h;
+  const int nq = p.nq;
+  const int t0 = blockIdx.x * kStTokens;
+  const int n_act = min(kStTokens, nq - t0);
+  const int L = p.kv_lens[b];
+
+  if (L < nq || L > p.Lmax) {
+    for (int e = tid; e < n_act * p.kmax; e += kStThreads) {
+      const size_t u = static_cast<size_t>(bh) * nq + t0 + e / p.kmax;
+      p.block_idx[u * p.kmax + e % p.kmax] = -1;
+    }
+    if (p.write_r)
+      for (int e = tid; e < n_act * p.nbmax; e += kStThreads)
+        p.r_buf[(static_cast<size_t>(bh) * nq + t0 + e / p.nbmax) * p.nbmax + e % p.nbmax] = -INFINITY;
+    if (tid < n_act) p.n_sel[static_cast<size_t>(bh) * nq + t0 + tid] = 0;
+    if (tid == 0) atomicOr(p.status, kStatusBadKvLen);
+    return;
+  }
+  const int nvis_max = n_complete_kernels(L - nq + t0 + n_act);
+  const int nch = (nvis_max + kStChunk - 1) / kStChunk;
+  const int total = 2 * nch;
+
+  for (int e = tid; e < kStTokens * p.nbmax; e += kStThreads) r_all[e] = -INFINITY;
+  if (tid == 0) {
+    prefetch_tensormap(&kc_map);
+    prefetch_tensormap(&q_map);
+    for (int s = 0; s < kStStages; ++s) {
+      mbar_init(&bars[kFull + s], 1);
+      mbar_init(&bars[kEmpty + s], 1);
+    }
+    mbar_init(&bars[kQ], 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars[kZFull + s], 1);
+      mbar_init(&bars[kZFree + s], 4);
+    }
+    fence_barrier_init();
+  }
+  if (warp == kStMmaWarp) {
+    tc::tmem_alloc(tmem_slot, kStTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t base_s = smem_u32(smem);
+
+  if (warp == kStTmaWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && total > 0) {
+      const int Hq = p.Hkv * kGroup;
+      mbar_arrive_expect_tx(&bars[kQ], n_act * 4096);
+      for (int tt = 0; tt < n_act; ++tt) {
+        const int row = (b * nq + t0 + tt) * Hq + h * kGroup;
+        tma_load_2d(smem + lay.q + tt * 2048, &q_map, 0, row, &bars[kQ]);
+        tma_load_2d(smem + lay.q + 16384 + tt * 2048, &q_map, 64, row, &bars[kQ]);
+      }
+      for (int it = 0; it < total; ++it) {
+        const int st = it % kStStages;
+        if (it >= kStStages && !mbar_wait(&bars[kEmpty + st], ((it / kStStages) - 1) & 1, p.status)) break;
+        const int ch = it < nch ? it : it - nch;
+        uint8_t* dst = smem + lay.ring + st * kStChunkBytes;
+        const int row_hi = (bh * 2 + 0) * p.ncmax + ch * kStChunk;
+        const int row_lo = (bh * 2 + 1) * p.ncmax + ch * kStChunk;
+        mbar_arrive_expect_tx(&bars[kFull + st], kStChunkBytes);
+        tma_load_2d(dst, &kc_map, 0, row_hi, &bars[kFull + st]);
+        tma_load_2d(dst + 8192, &kc_map, 64, row_hi, &bars[kFull + st]);
+        tma_load_2d(dst + 16384, &kc_map, 0, row_lo, &bars[kFull + st]);
+        tma_load_2d(dst + 24576, &kc_map, 64, row_lo, &bars[kFull + st]);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kStMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0 && total > 0) {
+      constexpr uint32_t kId = tc::idesc_bf16(128, 64, 0, 0);
+      const uint64_t q_desc = tc::sdesc_sw128(base_s + lay.q, 16, 1024);
+      bool ok = mbar_wait(&bars[kQ], 0, p.status);
+      for (int it = 0; it < total && ok; ++it) {
+        const int st = it % kStStages, zb = it & 1;
+        ok = mbar_wait(&bars[kFull + st], (it / kStStages) & 1, p.status);
+        if (ok && it >= 2) ok = mbar_wait(&bars[kZFree + zb], ((it >> 1) - 1) & 1, p.status);
+        if (!ok) break;
+        tc::fence_after_sync();
+        const uint32_t stage = base_s + lay.ring + st * kStChunkBytes;
+        const uint64_t hi_desc = tc::sdesc_sw128(stage, 16, 1024);
+        const uint64_t lo_desc = tc::sdesc_sw128(stage + 16384, 16, 1024);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t ta = static_cast<uint64_t>(((k >> 2) * 16384 + (k & 3) * 32) >> 4);
+          const uint64_t tb = static_cast<uint64_t>(((k >> 2) * 8192 + (k & 3) * 32) >> 4);
+          tc::mma_ss(tmem + zb * 64, q_desc + ta, hi_desc + tb, kId, k > 0 ? 1u : 0u);
+          tc::mma_ss(tmem + zb * 64, q_desc + ta, lo_desc + tb, kId, 1u);
+        }
+        tc::commit(&bars[kZFull + zb]);
+        tc::commit(&bars[kEmpty + st]);
+      }
+    }
+    __syncwarp();
+  } else {
+    // --------------------------------------------------------------- rows
+    const int r = warp * 32 + lane;
+    const int tok = r >> 4, x = r & 15;
+    const bool active = tok < n_act;
+    const int i_t = L - nq + t0 + (active ? tok : n_act - 1);
+    const int c_t = i_t / kBlock;
+    const int nvis_t = active ? n_complete_kernels(i_t + 1) : 0;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    float* r_tok = r_all + tok * p.nbmax;
+    float m = -INFINITY, l = 0.f, lse2 = -INFINITY;
+    float carry = -INFINITY;   // group value of the last kernel of the previous chunk
+    bool ok = true;
+    for (int it = 0; it < total; ++it) {
+      const int zb = it & 1;
+      const bool pass2 = it >= nch;
+      const int kbase = (pass2 ? it - nch : it) * kStChunk;
+      if (it == nch) lse2 = (m == -INFINITY) ? -INFINITY : m + fast_log2(l);
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars[kZFull + zb], (it >> 1) & 1, p.status));
+      tc::fence_after_sync();
+      uint32_t v[64];
+      tc::ld32(lane_addr + zb * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+      tc::ld32(lane_addr + zb * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      tc::wait_ld();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kZFree + zb]);
+      const int nv = max(0, min(kStChunk, nvis_t - kbase));   // this row's visible kernels of the chunk
+      if (!pass2) {
+        if (nv > 0) {
+          float cm = -INFINITY;
+#pragma unroll
+          for (int k = 0; k < 64; ++k)
+            if (k < nv) cm = fmaxf(cm, __uint_as_float(v[k]));
+          const float M = fmaxf(m, cm * p.scale2);
+          float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+          for (int k = 0; k < 64; k += 2) {
+            s0 += (k < nv) ? fast_exp2(fmaf(__uint_as_float(v[k]), p.scale2, -M)) : 0.f;
+            s1 += (k + 1 < nv) ? fast_exp2(fmaf(__uint_as_float(v[k + 1]), p.scale2, -M)) : 0.f;
+          }
+          l = l * fast_exp2(m - M) + (s0 + s1);
+          m = M;
+        }
+      } else {
+        float e[64];
+#pragma unroll
+        for (int k = 0; k < 64; ++k)
+          e[k] = (k < nv) ? fast_exp2(fmaf(__uint_as_float(v[k]), p.scale2, -lse2)) : 0.f;
+        // Reduce-scatter over the token's 16 lanes (xor 8, 4, 2, 1): lane x
+        // keeps the half of its range selected by bit 3, 2, 1, 0 of x and adds
+        // the partner's copy of that half.
+        const bool b3 = x & 8, b2 = x & 4, b1 = x & 2, b0 = x & 1;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float send = b3 ? e[k] : e[k + 32];
+          const float keep = b3 ? e[k + 32] : e[k];
+          e[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float send = b2 ? e[k] : e[k + 16];
+          const float keep = b2 ? e[k + 16] : e[k];
+          e[k] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float send = b1 ? e[k] : e[k + 8];
+          const float keep = b1 ? e[k + 8] : e[k];
+          e[k] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float send = b0 ? e[k] : e[k + 4];
+          const float keep = b0 ? e[k + 4] : e[k];
+          e[k] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+        }
+        // Lane x: group sums of kernels kbase + 4x .. kbase + 4x + 3.
+        const float g0 = e[0] * (1.0f / kGroup), g1 = e[1] * (1.0f / kGroup);
+        const float g2 = e[2] * (1.0f / kGroup), g3 = e[3] * (1.0f / kGroup);
+        const float left = __shfl_sync(0xffffffffu, g3, (lane & 16) | ((x + 15) & 15));
+        const float prev = x == 0 ? carry : left;
+        carry = __shfl_sync(0xffffffffu, g3, lane | 15);
+        const int j = kbase / 4 + x;
+        if (active && j <= c_t && j < p.nbmax) {
+          const bool has = max(0, 4 * j - 1) < nvis_t;
+          r_tok[j] = has ? fmaxf(fmaxf(prev, fmaxf(g0, g1)), fmaxf(g2, g3)) : -INFINITY;
+        }
+      }
+    }
+    // The block after the last chunk meets one kernel of it (4 j - 1).
+    if (nch > 0 && x == 0 && active) {
+      const int j = nch * (kStChunk / 4);
+      if (j <= c_t && j < p.nbmax && 4 * j - 1 < nvis_t) r_tok[j] = carry;
+    }
+    __syncwarp();
+    // Top-k of this warp's two tokens (rows 32 w .. 32 w + 31).
+    TopkScratch<32>& tk = reinterpret_cast<TopkScratch<32>*>(smem + lay.tk)[warp];
+#pragma unroll 1
+    for (int k = 0; k < 2; ++k) {
+      const int tt = 2 * warp + k;
+      if (tt >= n_act) break;
+      const size_t u = static_cast<size_t>(bh) * nq + t0 + tt;
+      const float* rw = r_all + tt * p.nbmax;
+      if (p.write_r)
+        for (int jj = lane; jj < p.nbmax; jj += 32) p.r_buf[u * p.nbmax + jj] = rw[jj];
+      const int c = (L - nq + t0 + tt) / kBlock;
+      select_topk<32, true>(rw, smem + lay.flag + tt * p.nbmax, c + 1, p.n_init, p.n_local, p.topk,
+                            p.inc_forced != 0, p.kmax, p.block_idx + u * p.kmax, p.n_sel + u, tk, lane);
+      __syncwarp();
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == kStMmaWarp) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kStTmemCols);
+  }
+}
+
+}  // namespace
+
+bool select_tc_supported(const Shape& s) { return st_layout(s.nbmax).total + 1024 <= 227 * 1024; }
+
+cudaError_t launch_select_tc(const Shape& s, const CUtensorMap& kc_map, const CUtensorMap& q_map, const SelParams& p,
+                             cudaStream_t st) {
+  const int smem = st_layout(s.nbmax).total + 1024;
+  cudaError_t e = cudaFuncSetAttribute(sel_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((s.nq + kStTokens - 1) / kStTokens, s.Hkv, s.B);
+  sel_tc_kernel<<<grid, kStThreads, smem, st>>>(kc_map, q_map, p);
+  return cudaGetLastError();
+}
+
+}  // namespace infllmv2
