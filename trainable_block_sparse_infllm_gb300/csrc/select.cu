@@ -15,8 +15,8 @@
 //    per (b, h_kv) group.
 //  * prefill (n_q > 16): select_tc.cu on tcgen05 (8 tokens x 16 heads per
 //    128-row tile); here, the mma.sync form of the same two passes, used for
-//    the coarse-LSE approximation and for caches whose block scores do not
-//    fit the tcgen05 kernel's shared memory: one warp per query token, TT
+//    caches whose block scores do not fit the tcgen05 kernel's shared
+//    memory: one warp per query token, TT
 //    tokens per CTA sharing a TMA pipeline of 64-kernel hi/lo tiles, streamed
 //    twice (pass 1: LSE, pass 2: normalised group mean and block maxima),
 //    then a warp top-k.
@@ -37,8 +37,8 @@ int device_sm_count() {
 }
 
 bool select_tc_supported(const Shape& s);
-cudaError_t launch_select_tc(const Shape& s, const CUtensorMap& kc_map, const CUtensorMap& q_map, const SelParams& p,
-                             cudaStream_t st);
+cudaError_t launch_select_tc(const Shape& s, const CUtensorMap& kc_map, const CUtensorMap& kcc_map,
+                             const CUtensorMap& q_map, const SelParams& p, cudaStream_t st);
 size_t select_decode_ncpad(const Shape& s);
 bool select_decode_supported(const Shape& s);
 cudaError_t launch_select_decode(const Shape& s, const CUtensorMap& kc_map, const CUtensorMap& q_map,
@@ -64,7 +64,7 @@ __host__ __device__ inline PrefLayout pref_layout(int stages, int nbmax) {
   l.flag_off = l.r_off + kPrefTokens * nbmax * 4;
   l.gbuf_off = (l.flag_off + kPrefTokens * nbmax + 15) & ~15;
   l.tk_off = l.gbuf_off + kPrefTokens * 68 * 4;
-  l.bar_off = (l.tk_off + kPrefTokens * static_cast<int>(sizeof(TopkScratch<32>)) + 15) & ~15;
+  l.bar_off = (l.tk_off + kPrefTokens * static_cast<int>(sizeof(WarpTopkScratch)) + 15) & ~15;
   l.total = l.bar_off + (2 * stages + 1) * 8;
   return l;
 }
@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(kPrefTokens * 32)
   float* r_w = reinterpret_cast<float*>(smem + lay.r_off) + warp * p.nbmax;
   uint8_t* flag_w = smem + lay.flag_off + warp * p.nbmax;
   float* gbuf = reinterpret_cast<float*>(smem + lay.gbuf_off) + warp * 68;
-  TopkScratch<32>& tk = reinterpret_cast<TopkScratch<32>*>(smem + lay.tk_off)[warp];
+  WarpTopkScratch& tk = reinterpret_cast<WarpTopkScratch*>(smem + lay.tk_off)[warp];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.bar_off);
   uint64_t* empty = full + S;
   uint64_t* qbar = empty + S;
@@ -282,8 +282,8 @@ __global__ void __launch_bounds__(kPrefTokens * 32)
   __syncwarp();
   if (p.write_r)
     for (int j = lane; j < p.nbmax; j += 32) p.r_buf[u * p.nbmax + j] = r_w[j];
-  select_topk<32, true>(r_w, flag_w, c_t + 1, p.n_init, p.n_local, p.topk, p.inc_forced != 0,
-                        p.kmax, p.block_idx + u * p.kmax, p.n_sel + u, tk, lane);
+  select_topk_warp(r_w, flag_w, c_t + 1, p.n_init, p.n_local, p.topk, p.inc_forced != 0, p.kmax,
+                   p.block_idx + u * p.kmax, p.n_sel + u, tk, lane);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -351,7 +351,7 @@ cudaError_t launch_select(const Shape& s, const CUtensorMap& kc_map, const CUten
   }
   // Prefill: the tcgen05 kernel where its shared memory holds the block
   // scores of 8 tokens, the mma.sync kernel otherwise.
-  if (select_tc_supported(s)) return launch_select_tc(s, kc_map, q_map, p, st);
+  if (select_tc_supported(s)) return launch_select_tc(s, kc_map, kc_map, q_map, p, st);
   return launch_prefill_select(s, kc_map, kc_map, q_map, p, st);
 }
 
@@ -379,6 +379,7 @@ cudaError_t launch_select_coarse(const Shape& s, const CUtensorMap& kc_map, cons
   p.r_buf = block_scores;
   p.sc = sc;
   p.nccmax = s.Lmax / sc;
+  if (select_tc_supported(s)) return launch_select_tc(s, kc_map, kcc_map, q_map, p, st);
   return launch_prefill_select(s, kc_map, kcc_map, q_map, p, st);
 }
 

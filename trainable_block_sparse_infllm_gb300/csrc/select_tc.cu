@@ -14,7 +14,8 @@
 // means (causality gives the 8 tokens the same kernels but for the last one
 // or two).  z = q . hi + q . lo accumulates in TMEM (M 128, N 64, K 128, hi and
 // lo as two products into one accumulator).  The chunks are streamed twice:
-//   pass 1: each row thread keeps its head's running (max, sum of 2^z);
+//   pass 1: each row thread keeps its head's running (max, sum of 2^z)
+//           (over coarse windows instead, for the LSE approximation);
 //   pass 2: each row thread forms 2^(z - lse) for its head, and the 16 lanes
 //           of a token reduce-scatter the 64 kernels so that lane x ends with
 //           the group sums of kernels 4x .. 4x + 3 of the chunk, which with
@@ -49,7 +50,7 @@ __host__ __device__ inline StLayout st_layout(int nbmax) {
   l.r = l.q + 32768;                                    // [8 tokens][nbmax] block scores
   l.flag = l.r + kStTokens * nbmax * 4;                 // [8 tokens][nbmax] top-k flags
   l.tk = (l.flag + kStTokens * nbmax + 15) & ~15;       // 4 warp top-k scratches
-  l.bars = (l.tk + 4 * static_cast<int>(sizeof(TopkScratch<32>)) + 15) & ~15;
+  l.bars = (l.tk + 4 * static_cast<int>(sizeof(WarpTopkScratch)) + 15) & ~15;
   l.slot = l.bars + 16 * 8;
   l.total = l.slot + 16;
   return l;
@@ -60,7 +61,8 @@ enum StBar { kFull = 0, kEmpty = kFull + kStStages, kQ = kEmpty + kStStages, kZF
 static_assert(kStNumBars <= 16, "barrier area holds 16");
 
 __global__ void __launch_bounds__(kStThreads, 1)
-    sel_tc_kernel(const __grid_constant__ CUtensorMap kc_map, const __grid_constant__ CUtensorMap q_map, SelParams p) {
+    sel_tc_kernel(const __grid_constant__ CUtensorMap kc_map, const __grid_constant__ CUtensorMap kcc_map,
+                  const __grid_constant__ CUtensorMap q_map, SelParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const StLayout lay = st_layout(p.nbmax);
@@ -89,11 +91,20 @@ __global__ void __launch_bounds__(kStThreads, 1)
   }
   const int nvis_max = n_complete_kernels(L - nq + t0 + n_act);
   const int nch = (nvis_max + kStChunk - 1) / kStChunk;
-  const int total = 2 * nch;
+  // Stream of chunks: A (coarse windows, the LSE approximation [InfLLM v2 >
+  // Efficient LSE approximation]; only with p.sc > 0), B (fine LSE, for the
+  // tokens without a complete window; skipped when every token has one), C
+  // (fine, normalise and block maxima).  p.sc = 0: B and C only.
+  const int nvis_c_max = p.sc ? (L - nq + t0 + n_act) / p.sc : 0;
+  const int nch_a = (nvis_c_max + kStChunk - 1) / kStChunk;
+  const bool need_b = p.sc == 0 || (L - nq + t0 + 1) / p.sc == 0;
+  const int seg_c = nch_a + (need_b ? nch : 0);
+  const int total = nch > 0 ? seg_c + nch : 0;
 
   for (int e = tid; e < kStTokens * p.nbmax; e += kStThreads) r_all[e] = -INFINITY;
   if (tid == 0) {
     prefetch_tensormap(&kc_map);
+    if (p.sc) prefetch_tensormap(&kcc_map);
     prefetch_tensormap(&q_map);
     for (int s = 0; s < kStStages; ++s) {
       mbar_init(&bars[kFull + s], 1);
@@ -129,15 +140,18 @@ __global__ void __launch_bounds__(kStThreads, 1)
       for (int it = 0; it < total; ++it) {
         const int st = it % kStStages;
         if (it >= kStStages && !mbar_wait(&bars[kEmpty + st], ((it / kStStages) - 1) & 1, p.status)) break;
-        const int ch = it < nch ? it : it - nch;
+        const bool coarse_seg = it < nch_a;
+        const int ch = coarse_seg ? it : (it < seg_c ? it - nch_a : it - seg_c);
+        const CUtensorMap* map = coarse_seg ? &kcc_map : &kc_map;
+        const int rows = coarse_seg ? p.nccmax : p.ncmax;
         uint8_t* dst = smem + lay.ring + st * kStChunkBytes;
-        const int row_hi = (bh * 2 + 0) * p.ncmax + ch * kStChunk;
-        const int row_lo = (bh * 2 + 1) * p.ncmax + ch * kStChunk;
+        const int row_hi = (bh * 2 + 0) * rows + ch * kStChunk;
+        const int row_lo = (bh * 2 + 1) * rows + ch * kStChunk;
         mbar_arrive_expect_tx(&bars[kFull + st], kStChunkBytes);
-        tma_load_2d(dst, &kc_map, 0, row_hi, &bars[kFull + st]);
-        tma_load_2d(dst + 8192, &kc_map, 64, row_hi, &bars[kFull + st]);
-        tma_load_2d(dst + 16384, &kc_map, 0, row_lo, &bars[kFull + st]);
-        tma_load_2d(dst + 24576, &kc_map, 64, row_lo, &bars[kFull + st]);
+        tma_load_2d(dst, map, 0, row_hi, &bars[kFull + st]);
+        tma_load_2d(dst + 8192, map, 64, row_hi, &bars[kFull + st]);
+        tma_load_2d(dst + 16384, map, 0, row_lo, &bars[kFull + st]);
+        tma_load_2d(dst + 24576, map, 64, row_lo, &bars[kFull + st]);
       }
     }
     __syncwarp();
@@ -176,6 +190,8 @@ __global__ void __launch_bounds__(kStThreads, 1)
     const int i_t = L - nq + t0 + (active ? tok : n_act - 1);
     const int c_t = i_t / kBlock;
     const int nvis_t = active ? n_complete_kernels(i_t + 1) : 0;
+    const int nvis_c_t = (active && p.sc) ? (i_t + 1) / p.sc : 0;   // complete coarse windows
+    const bool coarse_t = nvis_c_t > 0;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     float* r_tok = r_all + tok * p.nbmax;
     float m = -INFINITY, l = 0.f, lse2 = -INFINITY;
@@ -183,9 +199,9 @@ __global__ void __launch_bounds__(kStThreads, 1)
     bool ok = true;
     for (int it = 0; it < total; ++it) {
       const int zb = it & 1;
-      const bool pass2 = it >= nch;
-      const int kbase = (pass2 ? it - nch : it) * kStChunk;
-      if (it == nch) lse2 = (m == -INFINITY) ? -INFINITY : m + fast_log2(l);
+      const bool pass2 = it >= seg_c;
+      const int kbase = (it < nch_a ? it : (pass2 ? it - seg_c : it - nch_a)) * kStChunk;
+      if (it == seg_c) lse2 = (m == -INFINITY) ? -INFINITY : m + fast_log2(l);
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars[kZFull + zb], (it >> 1) & 1, p.status));
       tc::fence_after_sync();
       uint32_t v[64];
@@ -195,7 +211,11 @@ __global__ void __launch_bounds__(kStThreads, 1)
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kZFree + zb]);
-      const int nv = max(0, min(kStChunk, nvis_t - kbase));   // this row's visible kernels of the chunk
+      // This row's visible rows of the chunk: coarse windows in segment A for
+      // a token that has one, fine kernels in B for a token that has none,
+      // fine kernels in C.
+      const int nvis_seg = it < nch_a ? (coarse_t ? nvis_c_t : 0) : (pass2 ? nvis_t : (coarse_t ? 0 : nvis_t));
+      const int nv = max(0, min(kStChunk, nvis_seg - kbase));
       if (!pass2) {
         if (nv > 0) {
           float cm = -INFINITY;
@@ -265,7 +285,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
     }
     __syncwarp();
     // Top-k of this warp's two tokens (rows 32 w .. 32 w + 31).
-    TopkScratch<32>& tk = reinterpret_cast<TopkScratch<32>*>(smem + lay.tk)[warp];
+    WarpTopkScratch& tk = reinterpret_cast<WarpTopkScratch*>(smem + lay.tk)[warp];
 #pragma unroll 1
     for (int k = 0; k < 2; ++k) {
       const int tt = 2 * warp + k;
@@ -275,8 +295,8 @@ __global__ void __launch_bounds__(kStThreads, 1)
       if (p.write_r)
         for (int jj = lane; jj < p.nbmax; jj += 32) p.r_buf[u * p.nbmax + jj] = rw[jj];
       const int c = (L - nq + t0 + tt) / kBlock;
-      select_topk<32, true>(rw, smem + lay.flag + tt * p.nbmax, c + 1, p.n_init, p.n_local, p.topk,
-                            p.inc_forced != 0, p.kmax, p.block_idx + u * p.kmax, p.n_sel + u, tk, lane);
+      select_topk_warp(rw, smem + lay.flag + tt * p.nbmax, c + 1, p.n_init, p.n_local, p.topk, p.inc_forced != 0,
+                       p.kmax, p.block_idx + u * p.kmax, p.n_sel + u, tk, lane);
       __syncwarp();
     }
   }
@@ -293,13 +313,14 @@ __global__ void __launch_bounds__(kStThreads, 1)
 
 bool select_tc_supported(const Shape& s) { return st_layout(s.nbmax).total + 1024 <= 227 * 1024; }
 
-cudaError_t launch_select_tc(const Shape& s, const CUtensorMap& kc_map, const CUtensorMap& q_map, const SelParams& p,
-                             cudaStream_t st) {
+// p.sc > 0: coarse-window LSE from kcc_map (else kcc_map is not read).
+cudaError_t launch_select_tc(const Shape& s, const CUtensorMap& kc_map, const CUtensorMap& kcc_map,
+                             const CUtensorMap& q_map, const SelParams& p, cudaStream_t st) {
   const int smem = st_layout(s.nbmax).total + 1024;
   cudaError_t e = cudaFuncSetAttribute(sel_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid((s.nq + kStTokens - 1) / kStTokens, s.Hkv, s.B);
-  sel_tc_kernel<<<grid, kStThreads, smem, st>>>(kc_map, q_map, p);
+  sel_tc_kernel<<<grid, kStThreads, smem, st>>>(kc_map, kcc_map, q_map, p);
   return cudaGetLastError();
 }
 

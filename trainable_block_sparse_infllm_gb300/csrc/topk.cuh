@@ -171,6 +171,118 @@ __device__ void select_topk(const float* r, uint8_t* flag, int nb, int n_init, i
   if (tid == 0) *out_n = min(total, k_max);
 }
 
+// One warp, scores in shared memory, same rule and output as select_topk
+// with one histogram pass instead of four radix passes: a 256-bin histogram
+// of the candidates' leading bits (sign, exponent, 6 mantissa bits) counted
+// down from the best score locates the bin of the n_take-th best; better bins
+// are taken and the boundary bin (at most kWarpTopkSurv scores) is ranked
+// exactly by (score desc, index asc).  A boundary bin that is the catch-all
+// last bin, or holds more scores than that, goes to select_topk.
+constexpr int kWarpTopkSurv = 64;
+
+struct WarpTopkScratch {
+  uint32_t hist[256];
+  unsigned long long surv[kWarpTopkSurv];
+  int n_surv;
+  TopkScratch<32> radix;
+};
+
+__device__ inline void select_topk_warp(const float* r, uint8_t* flag, int nb, int n_init, int n_local, int topk,
+                                 bool includes_forced, int k_max, int32_t* out_idx, int32_t* out_n,
+                                 WarpTopkScratch& sm, int lane) {
+  constexpr int kShift = 17;
+  const int c = nb - 1;
+  const int local_lo = c - n_local + 1;
+  int my_cand = 0, my_forced = 0;
+  uint32_t my_top = 0;
+  for (int j = lane; j < nb; j += 32) {
+    const bool forced = (j < n_init) || (j >= local_lo);
+    const bool cand = !forced && (r[j] > -INFINITY);
+    flag[j] = forced ? 2 : (cand ? 1 : 0);
+    my_cand += cand ? 1 : 0;
+    my_forced += forced ? 1 : 0;
+    if (cand) my_top = max(my_top, float_to_ordered(r[j]) >> kShift);
+  }
+  for (int b = lane; b < 256; b += 32) sm.hist[b] = 0u;
+  if (lane == 0) sm.n_surv = 0;
+  const int n_cand = __reduce_add_sync(0xffffffffu, my_cand);
+  const int n_forced = __reduce_add_sync(0xffffffffu, my_forced);
+  const uint32_t top = __reduce_max_sync(0xffffffffu, my_top);
+  int n_take = includes_forced ? topk - n_forced : topk;
+  if (n_take < 0) n_take = 0;
+  __syncwarp();
+  if (n_take > 0 && n_cand <= n_take) {
+    for (int j = lane; j < nb; j += 32)
+      if (flag[j] == 1) flag[j] = 3;
+  } else if (n_take > 0) {
+    for (int j = lane; j < nb; j += 32)
+      if (flag[j] == 1) atomicAdd(&sm.hist[min(255u, top - (float_to_ordered(r[j]) >> kShift))], 1u);
+    __syncwarp();
+    // Lane l owns bins 8 l .. 8 l + 7 (bin 0 = best).
+    int cnt[8], tot = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      cnt[k] = static_cast<int>(sm.hist[8 * lane + k]);
+      tot += cnt[k];
+    }
+    int run = warp_inclusive_scan(tot) - tot;
+    int my_bnd = -1, my_above = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (run < n_take && run + cnt[k] >= n_take) {
+        my_bnd = 8 * lane + k;
+        my_above = run;
+      }
+      run += cnt[k];
+    }
+    const int src = __ffs(__ballot_sync(0xffffffffu, my_bnd >= 0)) - 1;
+    const int bnd = __shfl_sync(0xffffffffu, my_bnd, src);
+    const int above = __shfl_sync(0xffffffffu, my_above, src);
+    const int in_bnd = static_cast<int>(sm.hist[bnd]);
+    if (bnd == 255 || in_bnd > kWarpTopkSurv) {
+      __syncwarp();
+      select_topk<32, true>(r, flag, nb, n_init, n_local, topk, includes_forced, k_max, out_idx, out_n, sm.radix,
+                            lane);
+      return;
+    }
+    for (int j = lane; j < nb; j += 32) {
+      if (flag[j] != 1) continue;
+      const uint32_t key = float_to_ordered(r[j]);
+      const int d = static_cast<int>(min(255u, top - (key >> kShift)));
+      if (d < bnd) {
+        flag[j] = 3;
+      } else if (d == bnd) {
+        sm.surv[atomicAdd(&sm.n_surv, 1)] = (static_cast<unsigned long long>(key) << 32) |
+                                            static_cast<uint32_t>(~j);
+      }
+    }
+    __syncwarp();
+    const int m = sm.n_surv, need = n_take - above;
+    for (int x = lane; x < m; x += 32) {
+      const unsigned long long me = sm.surv[x];
+      int rk = 0;
+      for (int y = 0; y < m; ++y) rk += (sm.surv[y] > me) ? 1 : 0;
+      if (rk < need) flag[~static_cast<uint32_t>(me & 0xffffffffu)] = 3;
+    }
+  }
+  __syncwarp();
+  const int per = (nb + 31) / 32;
+  const int lo = lane * per, hi = min(nb, lo + per);
+  int my_sel = 0;
+  for (int j = lo; j < hi; ++j) my_sel += (flag[j] >= 2) ? 1 : 0;
+  const int incl = warp_inclusive_scan(my_sel);
+  const int total = __shfl_sync(0xffffffffu, incl, 31);
+  int pos = incl - my_sel;
+  for (int j = lo; j < hi; ++j) {
+    if (flag[j] >= 2) {
+      if (pos < k_max) out_idx[pos] = j;
+      ++pos;
+    }
+  }
+  for (int q = total + lane; q < k_max; q += 32) out_idx[q] = -1;
+  if (lane == 0) *out_n = min(total, k_max);
+}
+
 // Top-k over scores held in registers: thread tid holds the scores of blocks
 // j = tid + NT x (x < MAXR) in v[x].  Same selection rule and output as
 // select_topk.  The chosen blocks are marked in a bitmask whose ascending
