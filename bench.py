@@ -144,8 +144,20 @@ class DecodeBench:
         self.lens = torch.from_numpy(inp.kv_lens).to(dev)
         self.kmax = T.max_selected(self.p)
         self.reps = []
+        d = wl.head_dim
+        nq_el, kv_el = q0.numel(), B * H * nq * d
         for r in range(REPLICAS):
-            rep = {"q": q0.clone(), "k": k0.clone(), "v": v0.clone(), "kc": T.alloc_kc(self.p, dev),
+            # One device buffer per replica holds a step's inputs back to back
+            # (q, then the new tokens' keys and values), so that the end-to-end
+            # leg moves them with one host-to-device copy.
+            packed = torch.empty(nq_el + 2 * kv_el, dtype=torch.bfloat16, device=dev)
+            packed[:nq_el].copy_(q0.reshape(-1))
+            k_new = packed[nq_el:nq_el + kv_el].view(B, H, nq, d)
+            v_new = packed[nq_el + kv_el:].view(B, H, nq, d)
+            k_new.copy_(k0[:, :, L - nq:L])
+            v_new.copy_(v0[:, :, L - nq:L])
+            rep = {"q": packed[:nq_el].view(q0.shape), "packed": packed, "k_new": k_new, "v_new": v_new,
+                   "k": k0.clone(), "v": v0.clone(), "kc": T.alloc_kc(self.p, dev),
                    "idx": torch.empty((B, H, nq, self.kmax), dtype=torch.int32, device=dev),
                    "nsel": torch.empty((B, H, nq), dtype=torch.int32, device=dev),
                    "out": torch.empty_like(q0),
@@ -190,6 +202,14 @@ class DecodeBench:
             with torch.cuda.graph(g):
                 self.step(r)
             self.graphs.append(g)
+        self.graphs_e2e = []                    # cache append + step (end-to-end leg)
+        for r in range(REPLICAS):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                rep = self.reps[r]
+                self.T.append_kv(self.p, rep["k_new"], rep["v_new"], self.lens, rep["k"], rep["v"])
+                self.step(r)
+            self.graphs_e2e.append(g)
         self.round = torch.cuda.CUDAGraph()     # REPLICAS steps back to back
         with torch.cuda.graph(self.round):
             for r in range(REPLICAS):
@@ -554,22 +574,20 @@ def main():
     # token's q, k, v come from pinned host memory (k, v appended to the
     # cache) and the attention output goes back to pinned host memory.
     B, H, nq, d = wl.batch, wl.n_kv_heads, wl.n_q, wl.head_dim
-    q_h = torch.empty((REPLICAS,) + tuple(bench.reps[0]["q"].shape), dtype=torch.bfloat16).pin_memory()
-    kv_h = torch.empty((REPLICAS, 2, B, H, d), dtype=torch.bfloat16).pin_memory()
+    # Each step's inputs (q and the new token's key and value per sequence)
+    # sit back to back in pinned host memory: one copy in, the cache append and
+    # the step as one graph, one copy of the output back.
+    in_h = torch.empty((REPLICAS, bench.reps[0]["packed"].numel()), dtype=torch.bfloat16).pin_memory()
     out_h = torch.empty((REPLICAS,) + tuple(bench.reps[0]["out"].shape), dtype=torch.bfloat16).pin_memory()
     for r in range(REPLICAS):
-        q_h[r].copy_(bench.reps[r]["q"])
-        kv_h[r, 0].copy_(bench.reps[r]["k"][:, :, wl.kv_len - 1])
-        kv_h[r, 1].copy_(bench.reps[r]["v"][:, :, wl.kv_len - 1])
+        in_h[r].copy_(bench.reps[r]["packed"])
     torch.cuda.synchronize()
 
     def e2e_step(i):
         r = i % REPLICAS
         rep = bench.reps[r]
-        rep["q"].copy_(q_h[r], non_blocking=True)
-        rep["k"][:, :, wl.kv_len - 1].copy_(kv_h[r, 0], non_blocking=True)
-        rep["v"][:, :, wl.kv_len - 1].copy_(kv_h[r, 1], non_blocking=True)
-        bench.graphs[r].replay()
+        rep["packed"].copy_(in_h[r], non_blocking=True)
+        bench.graphs_e2e[r].replay()
         out_h[r].copy_(rep["out"], non_blocking=True)
 
     for i in range(args.warmup):
@@ -625,7 +643,7 @@ def main():
                      "algorithmic_bytes_per_launch": ab["step"],
                      "traffic": _traffic("decode_step_kernel", DECODE)},
         "e2e": {"value": world * tokens_per_step * args.steps / t_e2e, "unit": "tokens/s",
-                "h2d_bytes_per_step": int(q_h[0].numel() * 2 + kv_h[0].numel() * 2),
+                "h2d_bytes_per_step": int(in_h[0].numel() * 2),
                 "d2h_bytes_per_step": int(out_h[0].numel() * 2), "wall_s": wall},
         "prefill": prefill,
     }

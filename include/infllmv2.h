@@ -217,6 +217,20 @@ int infllmv2_sparse_attn_prefill(const infllmv2_params* p, const void* q, int32_
                                  float* lse, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Cache append of a decode step: k_new / v_new (bf16 [batch, n_kv_heads, n_q,
+ * d], the keys and values of each sequence's n_q newest tokens) are written
+ * to cache rows kv_lens[b] - n_q .. kv_lens[b] - 1 of (b, h), so that kv_lens
+ * already counts them [InfLLM v2 > Block-level key-value partitioning: the
+ * cache grows by the decoded tokens].  A sequence whose kv_lens[b] lies
+ * outside [n_q, max_kv_len] is left untouched and sets
+ * INFLLMV2_DEVICE_BAD_KV_LEN.  The launch may start while the previous kernel
+ * of the stream drains; it writes only after that kernel has finished, and
+ * infllmv2_decode_step on the same stream reads the rows it wrote.
+ */
+int infllmv2_append_kv(const infllmv2_params* p, int32_t n_q, const void* k_new, const void* v_new,
+                       const int32_t* kv_lens, void* k_cache, void* v_cache, void* stream);
+
+/*
  * One whole decode step: stages 1-3 for the newest n_q tokens of each
  * sequence, whose keys and values the caller has already written to the
  * caches (kv_lens counts them) [InfLLM v2 > Semantic kernels, eq. S_j;

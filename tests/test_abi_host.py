@@ -137,3 +137,22 @@ def test_coarse_lse_entry_points_validate_first(L):
         assert L.lib.infllmv2_coarse_means(ctypes.byref(p), FAKE, FAKE, bad, FAKE, None) == L.INVALID_ARGUMENT
     assert sel(ctypes.byref(p), FAKE, 100, FAKE, 64, None, FAKE, FAKE, FAKE, None, None) == L.INVALID_ARGUMENT
     assert L.lib.infllmv2_coarse_means(ctypes.byref(p), FAKE_ODD, FAKE, 64, FAKE, None) == L.UNSUPPORTED
+
+
+def test_append_and_backward_entry_points_validate_first(L):
+    p = _params(L)
+    app = L.lib.infllmv2_append_kv
+    assert app(ctypes.byref(p), 1, None, FAKE, FAKE, FAKE, FAKE, None) == L.INVALID_ARGUMENT
+    assert app(ctypes.byref(p), 1, FAKE_ODD, FAKE, FAKE, FAKE, FAKE, None) == L.UNSUPPORTED
+    assert app(ctypes.byref(p), 0, FAKE, FAKE, FAKE, FAKE, FAKE, None) == L.INVALID_ARGUMENT
+    bwd = L.lib.infllmv2_sparse_attn_backward
+    # q, n_q, then k_cache, v_cache, kv_lens, block_idx, n_selected, out, lse, dout, dq, dk, dv
+    ptrs = [FAKE] * 11
+    no_lse = list(ptrs)
+    no_lse[6] = None
+    assert bwd(ctypes.byref(p), FAKE, 4, *no_lse, FAKE, 1 << 30, None) == L.INVALID_ARGUMENT
+    assert bwd(ctypes.byref(p), FAKE, 4, *ptrs, None, 0, None) == L.WORKSPACE_TOO_SMALL
+    need = L.lib.infllmv2_workspace_size(ctypes.byref(p), 4, 5)
+    assert need > 0
+    assert bwd(ctypes.byref(p), FAKE, 4, *ptrs, FAKE, need - 1, None) == L.WORKSPACE_TOO_SMALL
+    assert bwd(ctypes.byref(p), FAKE_ODD, 4, *ptrs, FAKE, need, None) == L.UNSUPPORTED

@@ -434,3 +434,49 @@ def test_select_exact_ties_break_to_lower_block(dev):
         idx, nsel = run.idx.cpu().numpy(), run.nsel.cpu().numpy()
         for (b, h, t), s in sels.items():
             assert idx[b, h, t, :nsel[b, h, t]].tolist() == s.blocks.tolist(), ((b, h, t), period_blocks)
+
+
+@pytest.mark.parametrize("nq", [1, 3])
+def test_append_kv_then_decode_step(dev, nq):
+    # The append writes the newest rows bit-exactly, leaves every other row
+    # alone, and append + decode step gives the step on a cache that already
+    # held those rows.
+    import torch
+    import trainable_block_sparse_infllm_gb300 as T
+    inp = S.make_random(batch=2, n_kv_heads=2, kv_len=3000, n_q=nq, topk=16, seed=31 + nq, kv_lens=[3000, 2100])
+    run = GpuRun(inp, dev)
+    run.compress()
+    full_k, full_v = run.k.clone(), run.v.clone()
+    run.blank_step_kernels()
+    run.step()
+    out_ref, idx_ref = run.out.clone(), run.idx.clone()
+    k_new = torch.stack([full_k[b, :, int(L) - nq:int(L)] for b, L in enumerate(inp.kv_lens)]).contiguous()
+    v_new = torch.stack([full_v[b, :, int(L) - nq:int(L)] for b, L in enumerate(inp.kv_lens)]).contiguous()
+    for b, L in enumerate(inp.kv_lens):
+        run.k[b, :, int(L) - nq:int(L)].view(torch.int16).fill_(0x7FC0)
+        run.v[b, :, int(L) - nq:int(L)].view(torch.int16).fill_(0x7FC0)
+    T.append_kv(run.p, k_new, v_new, run.lens, run.k, run.v)
+    run.blank_step_kernels()
+    run.idx.fill_(-7)
+    run.out.fill_(float("nan"))
+    run.step()
+    torch.cuda.synchronize()
+    assert torch.equal(run.k.view(torch.int16), full_k.view(torch.int16))
+    assert torch.equal(run.v.view(torch.int16), full_v.view(torch.int16))
+    assert torch.equal(run.idx, idx_ref)
+    assert torch.equal(run.out.view(torch.int16), out_ref.view(torch.int16))
+
+
+def test_append_kv_bad_kv_len(dev):
+    import torch
+    import trainable_block_sparse_infllm_gb300 as T
+    inp = S.make_random(batch=2, n_kv_heads=1, kv_len=500, n_q=2, topk=4, seed=6, kv_lens=[500, 1])
+    run = GpuRun(inp, dev)
+    before_k, before_v = run.k.clone(), run.v.clone()
+    k_new = torch.zeros((2, 1, 2, 128), dtype=torch.bfloat16, device=dev)
+    T.append_kv(run.p, k_new, k_new, run.lens, run.k, run.v)
+    torch.cuda.synchronize()
+    assert T.get_device_status(clear=True) & T.DEVICE_BAD_KV_LEN
+    assert torch.equal(run.k[1].view(torch.int16), before_k[1].view(torch.int16))
+    assert bool((run.k[0, 0, 498:500] == 0).all()) and bool((run.v[0, 0, 498:500] == 0).all())
+    assert torch.equal(run.k[0, 0, :498].view(torch.int16), before_k[0, 0, :498].view(torch.int16))

@@ -9,6 +9,7 @@ memory and streams.  Entry points mirror the C names:
     select_blocks        stage 2, block relevance and top-k
     sparse_attn_decode   stage 3 for decode / speculative verification
     sparse_attn_prefill  stage 3 for prefill
+    append_kv            write the newest tokens' keys and values to the caches
     decode_step          stages 1-3 for the newest token(s), one launch when n_q = 1
     coarse_means, select_blocks_coarse_lse
                          the coarse-kernel LSE approximation (prefill path)
@@ -33,7 +34,7 @@ __all__ = [
     "Params", "InfLLMv2Error", "make_params", "num_kernels", "max_selected", "workspace_size",
     "alloc_kc", "alloc_workspace", "compress_keys", "select_blocks", "sparse_attn_decode",
     "sparse_attn_prefill", "decode_step", "coarse_means", "alloc_kcc", "select_blocks_coarse_lse",
-    "sparse_attn_backward", "get_device_status", "OP_SELECT", "OP_DECODE", "OP_PREFILL",
+    "sparse_attn_backward", "append_kv", "get_device_status", "OP_SELECT", "OP_DECODE", "OP_PREFILL",
     "OP_DECODE_STEP", "OP_BACKWARD", "DECODE_MAX_NQ",
 ]
 
@@ -189,6 +190,14 @@ def decode_step(p: Params, q, k_cache, v_cache, kv_lens, kc, block_idx, n_select
                                              _ptr(kv_lens), _ptr(kc), _ptr(block_idx), _ptr(n_selected),
                                              _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream)))
     return block_idx, n_selected, out, lse
+
+
+def append_kv(p: Params, k_new, v_new, kv_lens, k_cache, v_cache, stream=None):
+    """Write k_new / v_new [B, Hkv, n_q, d] to cache rows kv_lens - n_q .. kv_lens - 1."""
+    n_q = k_new.shape[2]
+    _lib.check(_lib.lib.infllmv2_append_kv(ctypes.byref(p), n_q, _ptr(k_new), _ptr(v_new), _ptr(kv_lens),
+                                           _ptr(k_cache), _ptr(v_cache), _stream(stream)))
+    return k_cache, v_cache
 
 
 def sparse_attn_backward(p: Params, q, k_cache, v_cache, kv_lens, block_idx, n_selected, out, lse, dout,

@@ -54,6 +54,10 @@ cudaError_t launch_attn_tc(const Shape& s, const CUtensorMap& q_map, const CUten
                            const int32_t* n_sel, void* out, float* lse, uint32_t* status,
                            cudaStream_t st);
 
+// ---- cache append of a decode step (rows kv_lens[b] - n_q .. kv_lens[b] - 1)
+cudaError_t launch_append(const Shape& s, const void* k_new, const void* v_new, const int32_t* kv_lens, void* k_cache,
+                          void* v_cache, uint32_t* status, cudaStream_t st);
+
 // ---- fused decode step (n_q = 1): newest kernel + selection + attention ----
 // Cluster size of the single-launch form on the current device (16 or 8),
 // or 0 when it does not apply to this shape.
