@@ -202,14 +202,6 @@ class DecodeBench:
             with torch.cuda.graph(g):
                 self.step(r)
             self.graphs.append(g)
-        self.graphs_e2e = []                    # cache append + step (end-to-end leg)
-        for r in range(REPLICAS):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                rep = self.reps[r]
-                self.T.append_kv(self.p, rep["k_new"], rep["v_new"], self.lens, rep["k"], rep["v"])
-                self.step(r)
-            self.graphs_e2e.append(g)
         self.round = torch.cuda.CUDAGraph()     # REPLICAS steps back to back
         with torch.cuda.graph(self.round):
             for r in range(REPLICAS):
@@ -577,18 +569,27 @@ def main():
     # Each step's inputs (q and the new token's key and value per sequence)
     # sit back to back in pinned host memory: one copy in, the cache append and
     # the step as one graph, one copy of the output back.
+    # Each step is one graph: the copy in, the cache append, the decode step
+    # and the copy of the output back to pinned host memory.
     in_h = torch.empty((REPLICAS, bench.reps[0]["packed"].numel()), dtype=torch.bfloat16).pin_memory()
     out_h = torch.empty((REPLICAS,) + tuple(bench.reps[0]["out"].shape), dtype=torch.bfloat16).pin_memory()
     for r in range(REPLICAS):
         in_h[r].copy_(bench.reps[r]["packed"])
     torch.cuda.synchronize()
+    graphs_e2e = []
+    for r in range(REPLICAS):
+        rep = bench.reps[r]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            rep["packed"].copy_(in_h[r], non_blocking=True)
+            T.append_kv(bench.p, rep["k_new"], rep["v_new"], bench.lens, rep["k"], rep["v"])
+            bench.step(r)
+            out_h[r].copy_(rep["out"], non_blocking=True)
+        graphs_e2e.append(g)
+    torch.cuda.synchronize()
 
     def e2e_step(i):
-        r = i % REPLICAS
-        rep = bench.reps[r]
-        rep["packed"].copy_(in_h[r], non_blocking=True)
-        bench.graphs_e2e[r].replay()
-        out_h[r].copy_(rep["out"], non_blocking=True)
+        graphs_e2e[i % REPLICAS].replay()
 
     for i in range(args.warmup):
         e2e_step(i)
