@@ -17,13 +17,14 @@
 //   pass 1: each row thread keeps its head's running (max, sum of 2^z)
 //           (over coarse windows instead, for the LSE approximation);
 //   pass 2: each row thread forms 2^(z - lse) for its head, and the 16 lanes
-//           of a token reduce-scatter the 64 kernels so that lane x ends with
-//           the group sums of kernels 4x .. 4x + 3 of the chunk, which with
-//           kernel 4x - 1 from its neighbour are exactly the kernels meeting
-//           block (chunk / 4 + x): one block maximum per lane.
-// Roles (192 threads): warps 0-3 rows (row r = 32 w + lane: token r / 16,
-// head r % 16), warp 4 MMA issuer (one thread), warp 5 TMA producer.  The
-// row warps end with the warp top-k of their own two tokens.
+//           of a token reduce-scatter the warp's 32 kernels so that lane x
+//           ends with the group sums of kernels 2x, 2x + 1; two neighbouring
+//           lanes and the kernel left of them are exactly the kernels meeting
+//           one block.
+// Roles (320 threads): warps 0-7 rows (two per TMEM lane quadrant, each with
+// 32 of a chunk's 64 kernels; row r = 32 (w % 4) + lane: token r / 16, head
+// r % 16), warp 8 MMA issuer (one thread), warp 9 TMA producer.  The row
+// warps end with one token's warp top-k each.
 #include "select_common.cuh"
 #include "tc.cuh"
 
@@ -33,31 +34,38 @@ namespace {
 
 constexpr int kStTokens = 8;
 constexpr int kStChunk = 64;               // kernels per chunk
-constexpr int kStStages = 3;
+constexpr int kStMaxStages = 3;            // fewer when the block scores of a long cache need the room
 constexpr int kStChunkBytes = 32768;       // hi then lo: 64 rows x 256 B each
-constexpr int kStThreads = 192;
-constexpr int kStMmaWarp = 4, kStTmaWarp = 5;
+constexpr int kStRowWarps = 8;             // two per TMEM lane quadrant, 32 of a chunk's 64 kernels each
+constexpr int kStThreads = (kStRowWarps + 2) * 32;
+constexpr int kStMmaWarp = kStRowWarps, kStTmaWarp = kStRowWarps + 1;
 constexpr uint32_t kStTmemCols = 128;      // two z buffers of 64 columns
 
 struct StLayout {
-  int ring, q, r, flag, tk, bars, slot, total;
+  int ring, q, r, flag, tk, xch, bars, slot, total;
 };
 
-__host__ __device__ inline StLayout st_layout(int nbmax) {
+__host__ __device__ inline StLayout st_layout(int nbmax, int stages) {
   StLayout l;
   l.ring = 0;
-  l.q = kStStages * kStChunkBytes;                      // two 64-column boxes x 128 rows
+  l.q = stages * kStChunkBytes;                         // two 64-column boxes x 128 rows
   l.r = l.q + 32768;                                    // [8 tokens][nbmax] block scores
   l.flag = l.r + kStTokens * nbmax * 4;                 // [8 tokens][nbmax] top-k flags
-  l.tk = (l.flag + kStTokens * nbmax + 15) & ~15;       // 4 warp top-k scratches
-  l.bars = (l.tk + 4 * static_cast<int>(sizeof(WarpTopkScratch)) + 15) & ~15;
+  l.tk = (l.flag + kStTokens * nbmax + 15) & ~15;       // one warp top-k scratch per token
+  l.xch = (l.tk + kStTokens * static_cast<int>(sizeof(WarpTopkScratch)) + 15) & ~15;   // [2][128] (max, sum)
+  l.bars = l.xch + 2 * 128 * 8;
   l.slot = l.bars + 16 * 8;
   l.total = l.slot + 16;
   return l;
 }
 
-enum StBar { kFull = 0, kEmpty = kFull + kStStages, kQ = kEmpty + kStStages, kZFull = kQ + 1, kZFree = kZFull + 2,
-             kStNumBars = kZFree + 2 };
+enum StBar { kFull = 0, kEmpty = kFull + kStMaxStages, kQ = kEmpty + kStMaxStages, kZFull = kQ + 1,
+             kZFree = kZFull + 2, kStNumBars = kZFree + 2 };
+
+// Barrier of the two row warps of TMEM lane quadrant q (ids 1..4).
+__device__ __forceinline__ void quad_pair_sync(int q) {
+  asm volatile("bar.sync %0, 64;" ::"r"(q + 1) : "memory");
+}
 static_assert(kStNumBars <= 16, "barrier area holds 16");
 
 __global__ void __launch_bounds__(kStThreads, 1)
@@ -65,7 +73,8 @@ __global__ void __launch_bounds__(kStThreads, 1)
                   const __grid_constant__ CUtensorMap q_map, SelParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  const StLayout lay = st_layout(p.nbmax);
+  const int S = p.stages;
+  const StLayout lay = st_layout(p.nbmax, S);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + lay.bars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + lay.slot);
   float* r_all = reinterpret_cast<float*>(smem + lay.r);
@@ -106,14 +115,14 @@ __global__ void __launch_bounds__(kStThreads, 1)
     prefetch_tensormap(&kc_map);
     if (p.sc) prefetch_tensormap(&kcc_map);
     prefetch_tensormap(&q_map);
-    for (int s = 0; s < kStStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&bars[kFull + s], 1);
       mbar_init(&bars[kEmpty + s], 1);
     }
     mbar_init(&bars[kQ], 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars[kZFull + s], 1);
-      mbar_init(&bars[kZFree + s], 4);
+      mbar_init(&bars[kZFree + s], kStRowWarps);
     }
     fence_barrier_init();
   }
@@ -138,8 +147,8 @@ __global__ void __launch_bounds__(kStThreads, 1)
         tma_load_2d(smem + lay.q + 16384 + tt * 2048, &q_map, 64, row, &bars[kQ]);
       }
       for (int it = 0; it < total; ++it) {
-        const int st = it % kStStages;
-        if (it >= kStStages && !mbar_wait(&bars[kEmpty + st], ((it / kStStages) - 1) & 1, p.status)) break;
+        const int st = it % S;
+        if (it >= S && !mbar_wait(&bars[kEmpty + st], ((it / S) - 1) & 1, p.status)) break;
         const bool coarse_seg = it < nch_a;
         const int ch = coarse_seg ? it : (it < seg_c ? it - nch_a : it - seg_c);
         const CUtensorMap* map = coarse_seg ? &kcc_map : &kc_map;
@@ -162,8 +171,8 @@ __global__ void __launch_bounds__(kStThreads, 1)
       const uint64_t q_desc = tc::sdesc_sw128(base_s + lay.q, 16, 1024);
       bool ok = mbar_wait(&bars[kQ], 0, p.status);
       for (int it = 0; it < total && ok; ++it) {
-        const int st = it % kStStages, zb = it & 1;
-        ok = mbar_wait(&bars[kFull + st], (it / kStStages) & 1, p.status);
+        const int st = it % S, zb = it & 1;
+        ok = mbar_wait(&bars[kFull + st], (it / S) & 1, p.status);
         if (ok && it >= 2) ok = mbar_wait(&bars[kZFree + zb], ((it >> 1) - 1) & 1, p.status);
         if (!ok) break;
         tc::fence_after_sync();
@@ -184,7 +193,11 @@ __global__ void __launch_bounds__(kStThreads, 1)
     __syncwarp();
   } else {
     // --------------------------------------------------------------- rows
-    const int r = warp * 32 + lane;
+    // Warp w: TMEM lane quadrant q = w % 4 (rows 32 q .. 32 q + 31: tokens
+    // 2 q and 2 q + 1, lanes 0-15 and 16-31), kernels 32 hf .. 32 hf + 31 of
+    // each chunk with hf = w / 4.
+    const int q4 = warp & 3, hf = warp >> 2;
+    const int r = q4 * 32 + lane;
     const int tok = r >> 4, x = r & 15;
     const bool active = tok < n_act;
     const int i_t = L - nq + t0 + (active ? tok : n_act - 1);
@@ -192,21 +205,34 @@ __global__ void __launch_bounds__(kStThreads, 1)
     const int nvis_t = active ? n_complete_kernels(i_t + 1) : 0;
     const int nvis_c_t = (active && p.sc) ? (i_t + 1) / p.sc : 0;   // complete coarse windows
     const bool coarse_t = nvis_c_t > 0;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
+    float2* xch = reinterpret_cast<float2*>(smem + lay.xch);
     float* r_tok = r_all + tok * p.nbmax;
+    const int col0 = 32 * hf;
+    // The kernel left of this half's first block: column 31 of the same
+    // chunk for the upper half; for the lower half, column 63 of the
+    // previous chunk, carried.
+    const int xcol = hf ? 31 : 63;
     float m = -INFINITY, l = 0.f, lse2 = -INFINITY;
-    float carry = -INFINITY;   // group value of the last kernel of the previous chunk
+    float carry = -INFINITY;
     bool ok = true;
     for (int it = 0; it < total; ++it) {
       const int zb = it & 1;
       const bool pass2 = it >= seg_c;
       const int kbase = (it < nch_a ? it : (pass2 ? it - seg_c : it - nch_a)) * kStChunk;
-      if (it == seg_c) lse2 = (m == -INFINITY) ? -INFINITY : m + fast_log2(l);
+      if (it == seg_c) {
+        // Merge the two halves' (max, sum) of each row.
+        xch[hf * 128 + r] = make_float2(m, l);
+        quad_pair_sync(q4);
+        const float2 o = xch[(hf ^ 1) * 128 + r];
+        lse_merge(m, l, o.x, o.y);
+        lse2 = (m == -INFINITY) ? -INFINITY : m + fast_log2(l);
+      }
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars[kZFull + zb], (it >> 1) & 1, p.status));
       tc::fence_after_sync();
-      uint32_t v[64];
-      tc::ld32(lane_addr + zb * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-      tc::ld32(lane_addr + zb * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      uint32_t v[32];
+      tc::ld32(lane_addr + zb * 64 + col0, v);
+      const uint32_t vx = pass2 ? tc::ld1(lane_addr + zb * 64 + xcol) : 0u;
       tc::wait_ld();
       tc::fence_before_sync();
       __syncwarp();
@@ -215,17 +241,17 @@ __global__ void __launch_bounds__(kStThreads, 1)
       // a token that has one, fine kernels in B for a token that has none,
       // fine kernels in C.
       const int nvis_seg = it < nch_a ? (coarse_t ? nvis_c_t : 0) : (pass2 ? nvis_t : (coarse_t ? 0 : nvis_t));
-      const int nv = max(0, min(kStChunk, nvis_seg - kbase));
+      const int nv = max(0, min(kStChunk, nvis_seg - kbase)) - col0;   // visible among this half's 32
       if (!pass2) {
         if (nv > 0) {
           float cm = -INFINITY;
 #pragma unroll
-          for (int k = 0; k < 64; ++k)
+          for (int k = 0; k < 32; ++k)
             if (k < nv) cm = fmaxf(cm, __uint_as_float(v[k]));
           const float M = fmaxf(m, cm * p.scale2);
           float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-          for (int k = 0; k < 64; k += 2) {
+          for (int k = 0; k < 32; k += 2) {
             s0 += (k < nv) ? fast_exp2(fmaf(__uint_as_float(v[k]), p.scale2, -M)) : 0.f;
             s1 += (k + 1 < nv) ? fast_exp2(fmaf(__uint_as_float(v[k + 1]), p.scale2, -M)) : 0.f;
           }
@@ -233,71 +259,86 @@ __global__ void __launch_bounds__(kStThreads, 1)
           m = M;
         }
       } else {
-        float e[64];
+        float e[32];
 #pragma unroll
-        for (int k = 0; k < 64; ++k)
+        for (int k = 0; k < 32; ++k)
           e[k] = (k < nv) ? fast_exp2(fmaf(__uint_as_float(v[k]), p.scale2, -lse2)) : 0.f;
+        // The extra kernel (xcol), summed over the token's 16 heads.
+        const int nvx = max(0, min(kStChunk, nvis_seg - kbase));
+        float ex = (xcol < nvx) ? fast_exp2(fmaf(__uint_as_float(vx), p.scale2, -lse2)) : 0.f;
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) ex += __shfl_xor_sync(0xffffffffu, ex, o);
+        ex *= 1.0f / kGroup;
         // Reduce-scatter over the token's 16 lanes (xor 8, 4, 2, 1): lane x
         // keeps the half of its range selected by bit 3, 2, 1, 0 of x and adds
-        // the partner's copy of that half.
+        // the partner's copy of that half; it ends with kernels 2x, 2x + 1 of
+        // this warp's 32.
         const bool b3 = x & 8, b2 = x & 4, b1 = x & 2, b0 = x & 1;
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float send = b3 ? e[k] : e[k + 32];
-          const float keep = b3 ? e[k + 32] : e[k];
+        for (int k = 0; k < 16; ++k) {
+          const float send = b3 ? e[k] : e[k + 16];
+          const float keep = b3 ? e[k + 16] : e[k];
           e[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
         }
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const float send = b2 ? e[k] : e[k + 16];
-          const float keep = b2 ? e[k + 16] : e[k];
+        for (int k = 0; k < 8; ++k) {
+          const float send = b2 ? e[k] : e[k + 8];
+          const float keep = b2 ? e[k + 8] : e[k];
           e[k] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
         }
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float send = b1 ? e[k] : e[k + 8];
-          const float keep = b1 ? e[k + 8] : e[k];
+        for (int k = 0; k < 4; ++k) {
+          const float send = b1 ? e[k] : e[k + 4];
+          const float keep = b1 ? e[k + 4] : e[k];
           e[k] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
         }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float send = b0 ? e[k] : e[k + 4];
-          const float keep = b0 ? e[k + 4] : e[k];
+        for (int k = 0; k < 2; ++k) {
+          const float send = b0 ? e[k] : e[k + 2];
+          const float keep = b0 ? e[k + 2] : e[k];
           e[k] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
         }
-        // Lane x: group sums of kernels kbase + 4x .. kbase + 4x + 3.
+        // Lane x: group values of kernels kbase + col0 + 2x, + 2x + 1.  Block
+        // b = x / 2 of the half (kernels 4b .. 4b + 3) is finished by the odd
+        // lane, with kernel 4b - 1 from lane x - 2 (or the extra kernel).
         const float g0 = e[0] * (1.0f / kGroup), g1 = e[1] * (1.0f / kGroup);
-        const float g2 = e[2] * (1.0f / kGroup), g3 = e[3] * (1.0f / kGroup);
-        const float left = __shfl_sync(0xffffffffu, g3, (lane & 16) | ((x + 15) & 15));
-        const float prev = x == 0 ? carry : left;
-        carry = __shfl_sync(0xffffffffu, g3, lane | 15);
-        const int j = kbase / 4 + x;
-        if (active && j <= c_t && j < p.nbmax) {
-          const bool has = max(0, 4 * j - 1) < nvis_t;
-          r_tok[j] = has ? fmaxf(fmaxf(prev, fmaxf(g0, g1)), fmaxf(g2, g3)) : -INFINITY;
+        const int grp = lane & 16;
+        const float p0 = __shfl_sync(0xffffffffu, g0, grp | ((x + 15) & 15));
+        const float p1 = __shfl_sync(0xffffffffu, g1, grp | ((x + 15) & 15));
+        const float pl = __shfl_sync(0xffffffffu, g1, grp | ((x + 14) & 15));
+        const float left = hf ? ex : carry;
+        if (!hf) carry = ex;   // column 63 of this chunk, for the next chunk's first block
+        if (x & 1) {
+          const int j = (kbase + col0) / 4 + (x >> 1);
+          const float prev = x == 1 ? left : pl;
+          if (active && j <= c_t && j < p.nbmax) {
+            const bool has = max(0, 4 * j - 1) < nvis_t;
+            r_tok[j] = has ? fmaxf(fmaxf(prev, fmaxf(p0, p1)), fmaxf(g0, g1)) : -INFINITY;
+          }
         }
       }
     }
-    // The block after the last chunk meets one kernel of it (4 j - 1).
-    if (nch > 0 && x == 0 && active) {
+    // The block after the last chunk meets one kernel of it (4 j - 1): the
+    // lower-half warp carries it.
+    if (nch > 0 && hf == 0 && x == 0 && active) {
       const int j = nch * (kStChunk / 4);
       if (j <= c_t && j < p.nbmax && 4 * j - 1 < nvis_t) r_tok[j] = carry;
     }
-    __syncwarp();
-    // Top-k of this warp's two tokens (rows 32 w .. 32 w + 31).
-    WarpTopkScratch& tk = reinterpret_cast<WarpTopkScratch*>(smem + lay.tk)[warp];
-#pragma unroll 1
-    for (int k = 0; k < 2; ++k) {
-      const int tt = 2 * warp + k;
-      if (tt >= n_act) break;
-      const size_t u = static_cast<size_t>(bh) * nq + t0 + tt;
-      const float* rw = r_all + tt * p.nbmax;
-      if (p.write_r)
-        for (int jj = lane; jj < p.nbmax; jj += 32) p.r_buf[u * p.nbmax + jj] = rw[jj];
-      const int c = (L - nq + t0 + tt) / kBlock;
-      select_topk_warp(rw, smem + lay.flag + tt * p.nbmax, c + 1, p.n_init, p.n_local, p.topk, p.inc_forced != 0,
-                       p.kmax, p.block_idx + u * p.kmax, p.n_sel + u, tk, lane);
-      __syncwarp();
+    quad_pair_sync(q4);
+    // Top-k: warp (q, hf) takes token 2 q + hf, whose scores the two warps of
+    // the quadrant wrote.
+    {
+      const int tt = 2 * q4 + hf;
+      if (tt < n_act) {
+        WarpTopkScratch& tk = reinterpret_cast<WarpTopkScratch*>(smem + lay.tk)[tt];
+        const size_t u = static_cast<size_t>(bh) * nq + t0 + tt;
+        const float* rw = r_all + tt * p.nbmax;
+        if (p.write_r)
+          for (int jj = lane; jj < p.nbmax; jj += 32) p.r_buf[u * p.nbmax + jj] = rw[jj];
+        const int c = (L - nq + t0 + tt) / kBlock;
+        select_topk_warp(rw, smem + lay.flag + tt * p.nbmax, c + 1, p.n_init, p.n_local, p.topk,
+                         p.inc_forced != 0, p.kmax, p.block_idx + u * p.kmax, p.n_sel + u, tk, lane);
+      }
     }
   }
 
@@ -311,16 +352,25 @@ __global__ void __launch_bounds__(kStThreads, 1)
 
 }  // namespace
 
-bool select_tc_supported(const Shape& s) { return st_layout(s.nbmax).total + 1024 <= 227 * 1024; }
+int select_tc_stages(const Shape& s) {
+  for (int st = kStMaxStages; st >= 2; --st)
+    if (st_layout(s.nbmax, st).total + 1024 <= 227 * 1024) return st;
+  return 0;
+}
+
+bool select_tc_supported(const Shape& s) { return select_tc_stages(s) > 0; }
 
 // p.sc > 0: coarse-window LSE from kcc_map (else kcc_map is not read).
 cudaError_t launch_select_tc(const Shape& s, const CUtensorMap& kc_map, const CUtensorMap& kcc_map,
                              const CUtensorMap& q_map, const SelParams& p, cudaStream_t st) {
-  const int smem = st_layout(s.nbmax).total + 1024;
+  SelParams pp = p;
+  pp.stages = select_tc_stages(s);
+  if (pp.stages == 0) return cudaErrorInvalidConfiguration;
+  const int smem = st_layout(s.nbmax, pp.stages).total + 1024;
   cudaError_t e = cudaFuncSetAttribute(sel_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid((s.nq + kStTokens - 1) / kStTokens, s.Hkv, s.B);
-  sel_tc_kernel<<<grid, kStThreads, smem, st>>>(kc_map, kcc_map, q_map, p);
+  sel_tc_kernel<<<grid, kStThreads, smem, st>>>(kc_map, kcc_map, q_map, pp);
   return cudaGetLastError();
 }
 
