@@ -480,3 +480,23 @@ def test_append_kv_bad_kv_len(dev):
     assert torch.equal(run.k[1].view(torch.int16), before_k[1].view(torch.int16))
     assert bool((run.k[0, 0, 498:500] == 0).all()) and bool((run.v[0, 0, 498:500] == 0).all())
     assert torch.equal(run.k[0, 0, :498].view(torch.int16), before_k[0, 0, :498].view(torch.int16))
+
+
+@pytest.mark.parametrize("sc", [0, 64])
+def test_select_long_capacity_takes_the_mma_sync_kernel(dev, sc):
+    # A cache capacity of 200K tokens (3125 blocks): 8 tokens' block scores no
+    # longer fit the tcgen05 selection kernel's shared memory, so the prefill
+    # selection runs on the mma.sync kernel; the result rule is the same.
+    import torch
+    inp = S.make_random(batch=1, n_kv_heads=2, kv_len=3000, n_q=40, topk=16, seed=77, max_kv_len=200_000)
+    run = GpuRun(inp, dev)
+    run.compress()
+    if sc:
+        kcc = run.T.alloc_kcc(run.p, sc, dev)
+        run.T.coarse_means(run.p, run.k, run.lens, sc, kcc)
+        run.T.select_blocks_coarse_lse(run.p, run.q, run.kc, sc, kcc, run.lens, run.idx, run.nsel, run.scores)
+    else:
+        run.select()
+    torch.cuda.synchronize()
+    st = O.Settings(topk=16, coarse=sc)
+    check_selections(run, O.run_selection(inp, st))
