@@ -49,7 +49,7 @@ def kc_to_f64(kc) -> np.ndarray:
     return f[:, :, 0] + f[:, :, 1]
 
 
-class GpuRun:
+class DeviceRun:
     """Uploads one input set and runs the three stages on the device."""
 
     def __init__(self, inp, dev, score_scale=None, attn_scale=None):

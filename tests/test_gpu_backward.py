@@ -11,7 +11,7 @@ import pytest
 
 import oracle as O
 import synthetic_inputs as S
-from helpers import GpuRun, check_grad
+from helpers import DeviceRun, check_grad
 
 pytestmark = pytest.mark.gpu
 
@@ -104,7 +104,7 @@ def test_backward_parity(dev, case):
     st = _settings(wl)
     sels = O.run_selection(inp, st)
     blocks = {u: s.blocks for u, s in sels.items()}
-    run = GpuRun(inp, dev)
+    run = DeviceRun(inp, dev)
     idx, nsel = run.upload_selection(sels)
     run.attend(idx, nsel)
     dout = S.make_grad_out(wl, seed=900 + nq)
@@ -123,7 +123,7 @@ def test_backward_dense_degeneracy_matches_autograd(dev):
     # attention, here from torch autograd in float64 on the CPU.
     import torch
     inp = S.make_random(batch=1, n_kv_heads=1, kv_len=600, n_q=600, topk=10, seed=8)
-    run = GpuRun(inp, dev)
+    run = DeviceRun(inp, dev)
     run.compress()
     run.select()
     run.attend()
@@ -150,7 +150,7 @@ def test_backward_bad_kv_len(dev):
     import torch
     import trainable_block_sparse_infllm_gb300 as T
     inp = S.make_random(batch=2, n_kv_heads=1, kv_len=1000, n_q=2, topk=4, seed=4, kv_lens=[1000, 1])
-    run = GpuRun(inp, dev)
+    run = DeviceRun(inp, dev)
     idx = torch.zeros((2, 1, 2, run.kmax), dtype=torch.int32, device=dev)
     nsel = torch.ones((2, 1, 2), dtype=torch.int32, device=dev)
     run.attend(idx, nsel)
@@ -170,7 +170,7 @@ def test_backward_prefill_32k_workload(dev):
     inp = S.make_inputs(wl)
     st = _settings(wl)
     idx_np, nsel_np = S.make_block_sets(wl, inp.kv_lens, seed=wl.seed + 1000)
-    run = GpuRun(inp, dev)
+    run = DeviceRun(inp, dev)
     idx = torch.from_numpy(idx_np).to(dev)
     nsel = torch.from_numpy(nsel_np).to(dev)
     run.attend(idx, nsel)

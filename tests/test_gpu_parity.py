@@ -13,7 +13,7 @@ import pytest
 
 import oracle as O
 import synthetic_inputs as S
-from helpers import (GpuRun, check_attention, check_selections, kc_to_f64)
+from helpers import (DeviceRun, check_attention, check_selections, kc_to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -44,7 +44,7 @@ def test_compress_keys_ragged(dev):
     import torch
     inp = S.make_random(batch=3, n_kv_heads=2, kv_len=5000, n_q=1, topk=8, seed=21,
                         kv_lens=[5000, 4093, 31])
-    run = GpuRun(inp, dev)
+    run = DeviceRun(inp, dev)
     run.kc.view(torch.int16).fill_(0x7FC0)       # NaN sentinel: untouched rows stay NaN
     run.compress()
     torch.cuda.synchronize()
@@ -62,7 +62,7 @@ def test_compress_keys_ragged(dev):
 def test_compress_keys_incremental_ranges(dev):
     import torch
     inp = S.make_random(batch=2, n_kv_heads=1, kv_len=3000, n_q=1, topk=8, seed=22, kv_lens=[3000, 2222])
-    run = GpuRun(inp, dev)
+    run = DeviceRun(inp, dev)
     run.compress()
     full = run.kc.clone()
     run.kc.view(torch.int16).fill_(0x7FC0)
@@ -102,7 +102,7 @@ def test_select_blocks_parity(dev, case):
     B, H, cap, lens, nq, topk, inc, sscale = case
     inp = S.make_random(batch=B, n_kv_heads=H, kv_len=cap, n_q=nq, topk=topk, includes_forced=inc,
                         seed=100 + sum(lens) + nq, kv_lens=lens)
-    run = GpuRun(inp, dev, score_scale=sscale)
+    run = DeviceRun(inp, dev, score_scale=sscale)
     run.compress()
     run.select()
     torch.cuda.synchronize()
@@ -113,7 +113,7 @@ def test_select_blocks_parity(dev, case):
 def test_select_blocks_dense_when_context_short(dev):
     import torch
     inp = S.make_random(batch=1, n_kv_heads=2, kv_len=1024, n_q=4, topk=16, seed=5)
-    run = GpuRun(inp, dev)
+    run = DeviceRun(inp, dev)
     run.compress()
     run.select()
     torch.cuda.synchronize()
@@ -147,7 +147,7 @@ def test_sparse_attention_parity(dev, case):
                         seed=200 + sum(lens) + nq, kv_lens=lens)
     st = _settings(inp.wl)
     sels = O.run_selection(inp, st)
-    run = GpuRun(inp, dev)
+    run = DeviceRun(inp, dev)
     idx, nsel = run.upload_selection(sels)
     run.attend(idx, nsel, prefill=prefill)
     torch.cuda.synchronize()
@@ -159,7 +159,7 @@ def test_attention_dense_degeneracy_matches_sdpa(dev):
     # topk covering every block: the output is plain causal attention.
     import torch
     inp = S.make_random(batch=1, n_kv_heads=1, kv_len=900, n_q=900, topk=15, seed=7)
-    run = GpuRun(inp, dev)
+    run = DeviceRun(inp, dev)
     run.compress()
     run.select()
     run.attend()
@@ -182,7 +182,7 @@ def test_split_count_does_not_change_decode_result(dev):
     inp = S.make_random(batch=2, n_kv_heads=2, kv_len=8000, n_q=4, topk=48, seed=9)
     st = _settings(inp.wl)
     sels = O.run_selection(inp, st)
-    run = GpuRun(inp, dev)
+    run = DeviceRun(inp, dev)
     idx, nsel = run.upload_selection(sels)
     run.attend(idx, nsel, prefill=False)
     a = run.out.float().clone()
@@ -195,7 +195,7 @@ def test_bad_kv_len_sets_device_status(dev):
     import torch
     import trainable_block_sparse_infllm_gb300 as T
     inp = S.make_random(batch=2, n_kv_heads=1, kv_len=1000, n_q=2, topk=4, seed=3, kv_lens=[1000, 1])
-    run = GpuRun(inp, dev)
+    run = DeviceRun(inp, dev)
     run.compress()
     run.select()
     run.attend()
@@ -226,7 +226,7 @@ def test_decode_step_parity(dev, case):
     inp = S.make_random(batch=B, n_kv_heads=H, kv_len=cap, n_q=nq, topk=topk, includes_forced=inc,
                         seed=300 + sum(lens) + nq, kv_lens=lens)
     st = _settings(inp.wl)
-    run = GpuRun(inp, dev)
+    run = DeviceRun(inp, dev)
     full = run.blank_step_kernels()
     run.step()
     torch.cuda.synchronize()
@@ -244,7 +244,7 @@ def test_decode_step_matches_separate_stages(dev):
     # to rounding.
     import torch
     inp = S.make_random(batch=2, n_kv_heads=2, kv_len=30000, n_q=1, topk=48, seed=41, kv_lens=[30000, 12345])
-    run = GpuRun(inp, dev)
+    run = DeviceRun(inp, dev)
     run.compress()
     run.select(with_scores=False)
     run.attend()
@@ -262,7 +262,7 @@ def test_decode_step_bad_kv_len(dev):
     import torch
     import trainable_block_sparse_infllm_gb300 as T
     inp = S.make_random(batch=2, n_kv_heads=1, kv_len=1000, n_q=1, topk=4, seed=3, kv_lens=[1000, 900])
-    run = GpuRun(inp, dev)
+    run = DeviceRun(inp, dev)
     run.compress()
     run.lens[1] = 1001                      # beyond max_kv_len
     run.step()
@@ -290,7 +290,7 @@ def test_workload_parity(dev, name):
     wl = S.WORKLOADS[name]
     inp = S.make_inputs(wl)
     st = _settings(wl)
-    run = GpuRun(inp, dev)
+    run = DeviceRun(inp, dev)
     run.compress()
     run.select()
     run.attend()
@@ -344,7 +344,7 @@ def test_chunked_prefill_on_a_cache(dev):
     inp = S.make_random(batch=2, n_kv_heads=2, kv_len=20000, n_q=nq, topk=32, includes_forced=False,
                         seed=77, kv_lens=[20000, 9000])
     st = _settings(inp.wl)
-    run = GpuRun(inp, dev)
+    run = DeviceRun(inp, dev)
     run.compress()
     run.select(with_scores=False)
     run.attend()
@@ -369,7 +369,7 @@ def test_chunked_prefill_on_a_cache(dev):
 def test_coarse_means_match_oracle(dev, sc):
     import torch
     inp = S.make_random(batch=2, n_kv_heads=2, kv_len=5000, n_q=1, topk=8, seed=61, kv_lens=[5000, 1111])
-    run = GpuRun(inp, dev)
+    run = DeviceRun(inp, dev)
     kcc = run.T.alloc_kcc(run.p, sc, dev)
     kcc.view(torch.int16).fill_(0x7FC0)
     run.T.coarse_means(run.p, run.k, run.lens, sc, kcc)
@@ -400,7 +400,7 @@ def test_select_coarse_lse_parity(dev, case):
     B, H, cap, lens, nq, topk, inc, sc = case
     inp = S.make_random(batch=B, n_kv_heads=H, kv_len=cap, n_q=nq, topk=topk, includes_forced=inc,
                         seed=400 + sum(lens) + nq, kv_lens=lens)
-    run = GpuRun(inp, dev)
+    run = DeviceRun(inp, dev)
     run.compress()
     kcc = run.T.alloc_kcc(run.p, sc, dev)
     run.T.coarse_means(run.p, run.k, run.lens, sc, kcc)
@@ -426,7 +426,7 @@ def test_select_exact_ties_break_to_lower_block(dev):
             n = min(half, L - start)
             k[:, :, start:start + n] = inp.k[:, :, :n]
         inp.k[...] = k
-        run = GpuRun(inp, dev)
+        run = DeviceRun(inp, dev)
         run.compress()
         run.select()
         torch.cuda.synchronize()
@@ -444,7 +444,7 @@ def test_append_kv_then_decode_step(dev, nq):
     import torch
     import trainable_block_sparse_infllm_gb300 as T
     inp = S.make_random(batch=2, n_kv_heads=2, kv_len=3000, n_q=nq, topk=16, seed=31 + nq, kv_lens=[3000, 2100])
-    run = GpuRun(inp, dev)
+    run = DeviceRun(inp, dev)
     run.compress()
     full_k, full_v = run.k.clone(), run.v.clone()
     run.blank_step_kernels()
@@ -471,7 +471,7 @@ def test_append_kv_bad_kv_len(dev):
     import torch
     import trainable_block_sparse_infllm_gb300 as T
     inp = S.make_random(batch=2, n_kv_heads=1, kv_len=500, n_q=2, topk=4, seed=6, kv_lens=[500, 1])
-    run = GpuRun(inp, dev)
+    run = DeviceRun(inp, dev)
     before_k, before_v = run.k.clone(), run.v.clone()
     k_new = torch.zeros((2, 1, 2, 128), dtype=torch.bfloat16, device=dev)
     T.append_kv(run.p, k_new, k_new, run.lens, run.k, run.v)
@@ -489,7 +489,7 @@ def test_select_long_capacity_takes_the_mma_sync_kernel(dev, sc):
     # selection runs on the mma.sync kernel; the result rule is the same.
     import torch
     inp = S.make_random(batch=1, n_kv_heads=2, kv_len=3000, n_q=40, topk=16, seed=77, max_kv_len=200_000)
-    run = GpuRun(inp, dev)
+    run = DeviceRun(inp, dev)
     run.compress()
     if sc:
         kcc = run.T.alloc_kcc(run.p, sc, dev)
