@@ -26,8 +26,9 @@
 //              writes zeros.
 //   warp 8     MMA issuer (one thread): S_i = Q K_i^T (M 128, N 128, K 128,
 //              both operands in shared memory) into one of two TMEM S
-//              buffers, then O += P_{i-1} V_{i-1} (M 128, N 128, K 128; P
-//              from TMEM, V an MN-major shared operand).
+//              buffers, and O += P_i V_i (M 128, N 128, K 128; P from TMEM,
+//              V an MN-major shared operand), each stream issued as soon as
+//              its operands are ready.
 //   warp 9     TMA producer: the Q tile, then each item's two K tiles into a
 //              3-stage ring (a stage frees once S is computed).
 //   warp 10    TMA producer: each item's two V tiles into a 2-stage ring (a
@@ -284,12 +285,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint64_t k_desc0 = tc::sdesc_sw128(kv_s, 16, 1024);
       const uint64_t v_desc0 = tc::sdesc_sw128(vv_s, 16384, 1024);
       bool ok = mbar_wait(&bars[kQFull], 0, p.status);
-      for (int it = 0; it <= nit && ok; ++it) {
-        if (it < nit) {
-          const int st = it % kTcKStages, sb = it & 1;
-          ok = mbar_wait(&bars[kKFull + st], (it / kTcKStages) & 1, p.status);
-          if (ok && it >= 2) ok = mbar_wait(&bars[kSFree + sb], ((it >> 1) - 1) & 1, p.status);
-          if (!ok) break;
+      // Two in-order streams, each issued as soon as its inputs are there:
+      // S of item n_s (its K tiles loaded, its S buffer read out two items
+      // back) and O += P V of item n_o (its P written, its V tiles loaded).
+      // Neither waits behind the other, so a late K tile does not hold back
+      // the P V product that frees a V stage.
+      int n_s = 0, n_o = 0;
+      uint32_t idle = 0;
+      while (ok && n_o < nit) {
+        bool progressed = false;
+        if (n_s < nit && mbar_try_wait(&bars[kKFull + n_s % kTcKStages], (n_s / kTcKStages) & 1) &&
+            (n_s < 2 || mbar_try_wait(&bars[kSFree + (n_s & 1)], ((n_s >> 1) - 1) & 1))) {
+          const int st = n_s % kTcKStages, sb = n_s & 1;
           tc::fence_after_sync();
           const uint64_t kd = k_desc0 + static_cast<uint64_t>(st * (kTcItemBytes >> 4));
 #pragma unroll
@@ -299,11 +306,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           tc::commit(&bars[kSFull + sb]);
           tc::commit(&bars[kKEmpty + st]);
+          ++n_s;
+          progressed = true;
         }
-        if (it >= 1) {
-          const int m = it - 1, pb = m & 1, st = m % kTcVStages;
-          if (!mbar_wait(&bars[kPFull + pb], (m >> 1) & 1, p.status)) break;
-          if (!mbar_wait(&bars[kVFull + st], (m / kTcVStages) & 1, p.status)) break;
+        if (n_o < n_s && mbar_try_wait(&bars[kPFull + (n_o & 1)], (n_o >> 1) & 1) &&
+            mbar_try_wait(&bars[kVFull + n_o % kTcVStages], (n_o / kTcVStages) & 1)) {
+          const int m = n_o, pb = m & 1, st = m % kTcVStages;
           tc::fence_after_sync();
           const uint64_t vd = v_desc0 + static_cast<uint64_t>(st * (kTcItemBytes >> 4));
 #pragma unroll
@@ -312,6 +320,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                        kIdO, (m > 0 || k > 0) ? 1u : 0u);
           tc::commit(&bars[kODone + (m & 1)]);
           tc::commit(&bars[kVEmpty + st]);
+          ++n_o;
+          progressed = true;
+        }
+        if (progressed) {
+          idle = 0;
+        } else if (++idle > 4 * kSpinLimit) {
+          atomicOr(p.status, kStatusTimeout);
+          ok = false;
         }
       }
     }
