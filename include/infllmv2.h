@@ -137,7 +137,9 @@ int infllmv2_compress_keys(const infllmv2_params* p, const void* k_cache, const 
  *              topk - |forced| of them if topk_includes_forced, else topk.
  * block_scores (nullable) receives r as fp32 [B, Hkv, n_q, n_b(max_kv_len)]
  * (-inf past floor(i/m)).  n_q >= 1; workspace from
- * infllmv2_workspace_size(p, n_q, INFLLMV2_OP_SELECT).
+ * infllmv2_workspace_size(p, n_q, INFLLMV2_OP_SELECT).  For n_q > 16 the
+ * selection keeps 8 tokens' block scores on chip, which bounds max_kv_len
+ * at 261824 (INFLLMV2_UNSUPPORTED above).
  */
 int infllmv2_select_blocks(const infllmv2_params* p, const void* q, int32_t n_q, const void* kc,
                            const int32_t* kv_lens, int32_t* block_idx, int32_t* n_selected,

@@ -156,3 +156,13 @@ def test_append_and_backward_entry_points_validate_first(L):
     assert need > 0
     assert bwd(ctypes.byref(p), FAKE, 4, *ptrs, FAKE, need - 1, None) == L.WORKSPACE_TOO_SMALL
     assert bwd(ctypes.byref(p), FAKE_ODD, 4, *ptrs, FAKE, need, None) == L.UNSUPPORTED
+
+
+def test_prefill_selection_capacity_bound(L):
+    # Prefill selection (n_q > 16) keeps 8 tokens' block scores on chip.
+    p = _params(L, batch=1, hkv=1, lmax=300_000)
+    rc = L.lib.infllmv2_select_blocks(ctypes.byref(p), FAKE, 100, FAKE, FAKE, FAKE, FAKE, None, None, 0, None)
+    assert rc == L.UNSUPPORTED
+    assert b"261824" in L.lib.infllmv2_last_error()
+    ok = _params(L, batch=1, hkv=1, lmax=250_000)
+    assert L.lib.infllmv2_workspace_size(ctypes.byref(ok), 100, L.OP_SELECT) == 0

@@ -483,12 +483,12 @@ def test_append_kv_bad_kv_len(dev):
 
 
 @pytest.mark.parametrize("sc", [0, 64])
-def test_select_long_capacity_takes_the_mma_sync_kernel(dev, sc):
-    # A cache capacity of 200K tokens (3125 blocks): 8 tokens' block scores no
-    # longer fit the tcgen05 selection kernel's shared memory, so the prefill
-    # selection runs on the mma.sync kernel; the result rule is the same.
+def test_select_long_capacity(dev, sc):
+    # A cache capacity of 250K tokens (3907 blocks): the prefill selection
+    # keeps 8 tokens' block scores on chip with a 2-stage ring and its top-k
+    # scratch laid over the ring; the result rule is the same.
     import torch
-    inp = S.make_random(batch=1, n_kv_heads=2, kv_len=3000, n_q=40, topk=16, seed=77, max_kv_len=200_000)
+    inp = S.make_random(batch=1, n_kv_heads=2, kv_len=3000, n_q=40, topk=16, seed=77, max_kv_len=250_000)
     run = DeviceRun(inp, dev)
     run.compress()
     if sc:

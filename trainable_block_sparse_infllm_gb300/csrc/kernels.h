@@ -31,6 +31,10 @@ cudaError_t launch_coarse(const Shape& s, const void* k, const int32_t* kv_lens,
 constexpr int kSelDecodeMaxNq = 16;   // n_q at or below this uses the decode path
 
 size_t select_workspace_bytes(const Shape& s);
+// The prefill selection (n_q > 16) keeps 8 tokens' block scores in shared
+// memory: at most 4091 blocks (261824 tokens) of cache capacity.
+bool select_tc_supported(const Shape& s);
+bool select_supported(const Shape& s);
 cudaError_t launch_select(const Shape& s, const CUtensorMap& kc_map, const CUtensorMap& q_map,
                           const void* q, const int32_t* kv_lens, int32_t* block_idx,
                           int32_t* n_sel, float* block_scores, void* ws, uint32_t* status,

@@ -45,17 +45,22 @@ struct StLayout {
   int ring, q, r, flag, tk, xch, bars, slot, total;
 };
 
+// The top-k flags and scratch overlay the chunk ring, which is idle once the
+// last chunk's products are done (every row warp has waited for them before
+// its top-k).
 __host__ __device__ inline StLayout st_layout(int nbmax, int stages) {
   StLayout l;
   l.ring = 0;
+  l.flag = 0;                                           // [8 tokens][nbmax] top-k flags (in the ring)
+  l.tk = (kStTokens * nbmax + 15) & ~15;                // one warp top-k scratch per token (in the ring)
   l.q = stages * kStChunkBytes;                         // two 64-column boxes x 128 rows
   l.r = l.q + 32768;                                    // [8 tokens][nbmax] block scores
-  l.flag = l.r + kStTokens * nbmax * 4;                 // [8 tokens][nbmax] top-k flags
-  l.tk = (l.flag + kStTokens * nbmax + 15) & ~15;       // one warp top-k scratch per token
-  l.xch = (l.tk + kStTokens * static_cast<int>(sizeof(WarpTopkScratch)) + 15) & ~15;   // [2][128] (max, sum)
+  l.xch = (l.r + kStTokens * nbmax * 4 + 15) & ~15;     // [2][128] (max, sum)
   l.bars = l.xch + 2 * 128 * 8;
   l.slot = l.bars + 16 * 8;
   l.total = l.slot + 16;
+  const int ring_need = l.tk + kStTokens * static_cast<int>(sizeof(WarpTopkScratch));
+  if (ring_need > l.q) l.total = 1 << 30;               // does not fit: never chosen
   return l;
 }
 
@@ -325,6 +330,10 @@ __global__ void __launch_bounds__(kStThreads, 1)
       if (j <= c_t && j < p.nbmax && 4 * j - 1 < nvis_t) r_tok[j] = carry;
     }
     quad_pair_sync(q4);
+    // The top-k flags and scratch lie over the chunk ring, which the TMA and
+    // the tensor cores are done with (every row warp has seen the last
+    // chunk's products complete); order these ordinary stores after them.
+    fence_proxy_async_smem();
     // Top-k: warp (q, hf) takes token 2 q + hf, whose scores the two warps of
     // the quadrant wrote.
     {

@@ -181,10 +181,12 @@ __device__ void select_topk(const float* r, uint8_t* flag, int nb, int n_init, i
 constexpr int kWarpTopkSurv = 64;
 
 struct WarpTopkScratch {
-  uint32_t hist[256];
+  union {
+    uint32_t hist[256];
+    TopkScratch<32> radix;   // the fallback runs after the histogram is read
+  };
   unsigned long long surv[kWarpTopkSurv];
   int n_surv;
-  TopkScratch<32> radix;
 };
 
 __device__ inline void select_topk_warp(const float* r, uint8_t* flag, int nb, int n_init, int n_local, int topk,
