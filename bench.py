@@ -569,8 +569,8 @@ def main():
     # Each step's inputs (q and the new token's key and value per sequence)
     # sit back to back in pinned host memory: one copy in, the cache append and
     # the step as one graph, one copy of the output back.
-    # Each step is one graph: the copy in, the cache append, the decode step
-    # and the copy of the output back to pinned host memory.
+    # Each step is one graph: the copy in, the cache append and the decode
+    # step, which stores its output straight into pinned host memory.
     in_h = torch.empty((REPLICAS, bench.reps[0]["packed"].numel()), dtype=torch.bfloat16).pin_memory()
     out_h = torch.empty((REPLICAS,) + tuple(bench.reps[0]["out"].shape), dtype=torch.bfloat16).pin_memory()
     for r in range(REPLICAS):
@@ -583,8 +583,8 @@ def main():
         with torch.cuda.graph(g):
             rep["packed"].copy_(in_h[r], non_blocking=True)
             T.append_kv(bench.p, rep["k_new"], rep["v_new"], bench.lens, rep["k"], rep["v"])
-            bench.step(r)
-            out_h[r].copy_(rep["out"], non_blocking=True)
+            T.decode_step(bench.p, rep["q"], rep["k"], rep["v"], bench.lens, rep["kc"], rep["idx"], rep["nsel"],
+                          out_h[r], None, rep["ws_step"])
         graphs_e2e.append(g)
     torch.cuda.synchronize()
 
@@ -645,7 +645,8 @@ def main():
                      "traffic": _traffic("decode_step_kernel", DECODE)},
         "e2e": {"value": world * tokens_per_step * args.steps / t_e2e, "unit": "tokens/s",
                 "h2d_bytes_per_step": int(in_h[0].numel() * 2),
-                "d2h_bytes_per_step": int(out_h[0].numel() * 2), "wall_s": wall},
+                "d2h_bytes_per_step": int(out_h[0].numel() * 2), "wall_s": wall,
+                "transfers": "one copy of q, k, v in; the step stores its output into pinned host memory"},
         "prefill": prefill,
     }
     if world == 1 and not args.no_cpu_baseline:

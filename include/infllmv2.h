@@ -243,7 +243,11 @@ int infllmv2_append_kv(const infllmv2_params* p, int32_t n_q, const void* k_new,
  *           newest complete kernel n_c(L) - 1) are recomputed from k_cache
  *           and written back.
  *   block_idx, n_selected, out, lse: as from infllmv2_select_blocks followed
- *           by infllmv2_sparse_attn_decode (lse nullable).
+ *           by infllmv2_sparse_attn_decode (lse nullable).  out and lse are
+ *           written with ordinary stores, so they may also be page-locked host
+ *           memory mapped for the device (e.g. from cudaHostAlloc on a system
+ *           with unified addressing): the result then reaches the host without
+ *           a separate copy.
  *   n_q in [1, 16].  With n_q = 1 and a cache of at most 128 * 16 blocks
  *   (131072 tokens; 65536 where only 8-CTA clusters fit) the step is one
  *   launch of a thread-block cluster per (b, h_kv) that keeps every

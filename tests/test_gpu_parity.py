@@ -500,3 +500,22 @@ def test_select_long_capacity(dev, sc):
     torch.cuda.synchronize()
     st = O.Settings(topk=16, coarse=sc)
     check_selections(run, O.run_selection(inp, st))
+
+
+def test_decode_step_output_to_pinned_host_memory(dev):
+    # The fused step stores its output with ordinary stores, so a pinned host
+    # buffer receives the same bytes as device memory.
+    import torch
+    inp = S.make_random(batch=2, n_kv_heads=2, kv_len=3000, n_q=1, topk=16, seed=44, kv_lens=[3000, 2500])
+    run = DeviceRun(inp, dev)
+    run.blank_step_kernels()
+    run.step()
+    ref_out, ref_lse = run.out.clone(), run.lse.clone()
+    run.blank_step_kernels()
+    out_h = torch.full(tuple(run.out.shape), float("nan"), dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.full(tuple(run.lse.shape), float("nan"), dtype=torch.float32).pin_memory()
+    ws = run.T.alloc_workspace(run.p, run.nq, run.T.OP_DECODE_STEP, dev)
+    run.T.decode_step(run.p, run.q, run.k, run.v, run.lens, run.kc, run.idx, run.nsel, out_h, lse_h, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out_h.view(torch.int16), ref_out.cpu().view(torch.int16))
+    assert torch.equal(lse_h, ref_lse.cpu())

@@ -71,10 +71,12 @@ def workspace_size(p: Params, n_q: int, op: int) -> int:
     return int(_lib.lib.infllmv2_workspace_size(ctypes.byref(p), n_q, op))
 
 
-def _ptr(t: torch.Tensor | None):
+def _ptr(t: torch.Tensor | None, host_ok: bool = False):
+    """Device pointer of ``t``.  host_ok: a pinned host tensor is accepted too
+    (for outputs the kernels write with ordinary stores)."""
     if t is None:
         return None
-    if not t.is_cuda:
+    if not t.is_cuda and not (host_ok and t.is_pinned()):
         raise InfLLMv2Error(_lib.INVALID_ARGUMENT, "tensors must live on a CUDA device")
     if not t.is_contiguous():
         raise InfLLMv2Error(_lib.INVALID_ARGUMENT, "tensors must be contiguous")
@@ -183,12 +185,15 @@ def decode_step(p: Params, q, k_cache, v_cache, kv_lens, kc, block_idx, n_select
     """Newest kernel mean(s), selection and attention for the last n_q tokens.
 
     ``kc`` must hold every kernel that ends before those tokens; the ones that
-    end inside them are recomputed and written back."""
+    end inside them are recomputed and written back.  ``out`` and ``lse`` may
+    be pinned host tensors: the step then stores its result straight to host
+    memory."""
     n_q = q.shape[1]
     ws_bytes = workspace.numel() if workspace is not None else 0
     _lib.check(_lib.lib.infllmv2_decode_step(ctypes.byref(p), _ptr(q), n_q, _ptr(k_cache), _ptr(v_cache),
                                              _ptr(kv_lens), _ptr(kc), _ptr(block_idx), _ptr(n_selected),
-                                             _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream)))
+                                             _ptr(out, host_ok=True), _ptr(lse, host_ok=True), _ptr(workspace),
+                                             ws_bytes, _stream(stream)))
     return block_idx, n_selected, out, lse
 
 
