@@ -225,12 +225,18 @@ int infllmv2_sparse_attn_prefill(const infllmv2_params* p, const void* q, int32_
  * already counts them [InfLLM v2 > Block-level key-value partitioning: the
  * cache grows by the decoded tokens].  A sequence whose kv_lens[b] lies
  * outside [n_q, max_kv_len] is left untouched and sets
- * INFLLMV2_DEVICE_BAD_KV_LEN.  The launch may start while the previous kernel
- * of the stream drains; it writes only after that kernel has finished, and
- * infllmv2_decode_step on the same stream reads the rows it wrote.
+ * INFLLMV2_DEVICE_BAD_KV_LEN.  q_src / q_dst (both NULL, or both given):
+ * also copy the step's queries, bf16 [batch, n_q, Hq, d], from q_src to q_dst.
+ * k_new, v_new and q_src are read with ordinary loads, so they may be
+ * page-locked host memory mapped for the device: a decode step whose inputs
+ * sit in host memory then needs no separate copy.  The launch may start
+ * while the previous kernel of the stream drains; it writes only after that
+ * kernel has finished, and infllmv2_decode_step on the same stream reads
+ * what it wrote.
  */
 int infllmv2_append_kv(const infllmv2_params* p, int32_t n_q, const void* k_new, const void* v_new,
-                       const int32_t* kv_lens, void* k_cache, void* v_cache, void* stream);
+                       const int32_t* kv_lens, void* k_cache, void* v_cache, const void* q_src, void* q_dst,
+                       void* stream);
 
 /*
  * One whole decode step: stages 1-3 for the newest n_q tokens of each

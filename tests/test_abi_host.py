@@ -142,9 +142,11 @@ def test_coarse_lse_entry_points_validate_first(L):
 def test_append_and_backward_entry_points_validate_first(L):
     p = _params(L)
     app = L.lib.infllmv2_append_kv
-    assert app(ctypes.byref(p), 1, None, FAKE, FAKE, FAKE, FAKE, None) == L.INVALID_ARGUMENT
-    assert app(ctypes.byref(p), 1, FAKE_ODD, FAKE, FAKE, FAKE, FAKE, None) == L.UNSUPPORTED
-    assert app(ctypes.byref(p), 0, FAKE, FAKE, FAKE, FAKE, FAKE, None) == L.INVALID_ARGUMENT
+    assert app(ctypes.byref(p), 1, None, FAKE, FAKE, FAKE, FAKE, None, None, None) == L.INVALID_ARGUMENT
+    assert app(ctypes.byref(p), 1, FAKE_ODD, FAKE, FAKE, FAKE, FAKE, None, None, None) == L.UNSUPPORTED
+    assert app(ctypes.byref(p), 0, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None) == L.INVALID_ARGUMENT
+    assert app(ctypes.byref(p), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == L.INVALID_ARGUMENT  # q_src alone
+    assert app(ctypes.byref(p), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE_ODD, FAKE, None) == L.UNSUPPORTED
     bwd = L.lib.infllmv2_sparse_attn_backward
     # q, n_q, then k_cache, v_cache, kv_lens, block_idx, n_selected, out, lse, dout, dq, dk, dv
     ptrs = [FAKE] * 11

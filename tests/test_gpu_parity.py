@@ -519,3 +519,25 @@ def test_decode_step_output_to_pinned_host_memory(dev):
     torch.cuda.synchronize()
     assert torch.equal(out_h.view(torch.int16), ref_out.cpu().view(torch.int16))
     assert torch.equal(lse_h, ref_lse.cpu())
+
+
+def test_append_kv_from_pinned_host_memory_with_queries(dev):
+    # k_new, v_new and the step's queries read straight from pinned host
+    # memory; the cache rows and the query buffer receive the same bytes.
+    import torch
+    import trainable_block_sparse_infllm_gb300 as T
+    inp = S.make_random(batch=2, n_kv_heads=2, kv_len=1500, n_q=2, topk=8, seed=45, kv_lens=[1500, 700])
+    run = DeviceRun(inp, dev)
+    full_k, full_v, q_ref = run.k.clone(), run.v.clone(), run.q.clone()
+    k_h = torch.stack([full_k[b, :, int(L) - 2:int(L)] for b, L in enumerate(inp.kv_lens)]).cpu().pin_memory()
+    v_h = torch.stack([full_v[b, :, int(L) - 2:int(L)] for b, L in enumerate(inp.kv_lens)]).cpu().pin_memory()
+    q_h = q_ref.cpu().pin_memory()
+    for b, L in enumerate(inp.kv_lens):
+        run.k[b, :, int(L) - 2:int(L)].view(torch.int16).fill_(0x7FC0)
+        run.v[b, :, int(L) - 2:int(L)].view(torch.int16).fill_(0x7FC0)
+    run.q.view(torch.int16).fill_(0x7FC0)
+    T.append_kv(run.p, k_h, v_h, run.lens, run.k, run.v, q_src=q_h, q_dst=run.q)
+    torch.cuda.synchronize()
+    assert torch.equal(run.k.view(torch.int16), full_k.view(torch.int16))
+    assert torch.equal(run.v.view(torch.int16), full_v.view(torch.int16))
+    assert torch.equal(run.q.view(torch.int16), q_ref.view(torch.int16))

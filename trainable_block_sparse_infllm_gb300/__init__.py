@@ -197,11 +197,13 @@ def decode_step(p: Params, q, k_cache, v_cache, kv_lens, kc, block_idx, n_select
     return block_idx, n_selected, out, lse
 
 
-def append_kv(p: Params, k_new, v_new, kv_lens, k_cache, v_cache, stream=None):
-    """Write k_new / v_new [B, Hkv, n_q, d] to cache rows kv_lens - n_q .. kv_lens - 1."""
+def append_kv(p: Params, k_new, v_new, kv_lens, k_cache, v_cache, q_src=None, q_dst=None, stream=None):
+    """Write k_new / v_new [B, Hkv, n_q, d] to cache rows kv_lens - n_q .. kv_lens - 1 and, if given,
+    copy q_src to q_dst.  k_new, v_new and q_src may be pinned host tensors."""
     n_q = k_new.shape[2]
-    _lib.check(_lib.lib.infllmv2_append_kv(ctypes.byref(p), n_q, _ptr(k_new), _ptr(v_new), _ptr(kv_lens),
-                                           _ptr(k_cache), _ptr(v_cache), _stream(stream)))
+    _lib.check(_lib.lib.infllmv2_append_kv(ctypes.byref(p), n_q, _ptr(k_new, host_ok=True),
+                                           _ptr(v_new, host_ok=True), _ptr(kv_lens), _ptr(k_cache),
+                                           _ptr(v_cache), _ptr(q_src, host_ok=True), _ptr(q_dst), _stream(stream)))
     return k_cache, v_cache
 
 

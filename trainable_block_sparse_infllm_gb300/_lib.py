@@ -93,7 +93,7 @@ lib.infllmv2_select_blocks_coarse_lse.restype = ctypes.c_int
 lib.infllmv2_decode_step.argtypes = [_P, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                      ctypes.c_size_t, _vp]
 lib.infllmv2_decode_step.restype = ctypes.c_int
-lib.infllmv2_append_kv.argtypes = [_P, _i32, _vp, _vp, _vp, _vp, _vp, _vp]
+lib.infllmv2_append_kv.argtypes = [_P, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
 lib.infllmv2_append_kv.restype = ctypes.c_int
 lib.infllmv2_sparse_attn_backward.argtypes = [_P, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                               _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]

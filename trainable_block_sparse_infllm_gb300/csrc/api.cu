@@ -428,7 +428,8 @@ int infllmv2_sparse_attn_prefill(const infllmv2_params* p, const void* q, int32_
 }
 
 int infllmv2_append_kv(const infllmv2_params* p, int32_t n_q, const void* k_new, const void* v_new,
-                       const int32_t* kv_lens, void* k_cache, void* v_cache, void* stream) {
+                       const int32_t* kv_lens, void* k_cache, void* v_cache, const void* q_src, void* q_dst,
+                       void* stream) {
   INFLLMV2_GUARD({
     Shape s;
     int rc = check_params(p, n_q, &s);
@@ -437,9 +438,14 @@ int infllmv2_append_kv(const infllmv2_params* p, int32_t n_q, const void* k_new,
       return fail(INFLLMV2_INVALID_ARGUMENT, "a required pointer is NULL");
     if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
       return fail(INFLLMV2_UNSUPPORTED, "k_new, v_new, k_cache and v_cache must be 16-byte aligned");
+    if ((q_src == nullptr) != (q_dst == nullptr))
+      return fail(INFLLMV2_INVALID_ARGUMENT, "q_src and q_dst are given together or not at all");
+    if ((q_src && !aligned16(q_src)) || (q_dst && !aligned16(q_dst)))
+      return fail(INFLLMV2_UNSUPPORTED, "q_src and q_dst must be 16-byte aligned");
     uint32_t* status = status_ptr();
     if (!status) return fail(INFLLMV2_CUDA_ERROR, "no device status word (no current CUDA device?)");
-    cudaError_t e = launch_append(s, k_new, v_new, kv_lens, k_cache, v_cache, status, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_append(s, k_new, v_new, kv_lens, k_cache, v_cache, q_src, q_dst, status,
+                                  static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "append_kv");
     return INFLLMV2_OK;
   });

@@ -4,6 +4,11 @@
 // blocks grows by the decoded tokens; their keys also complete the newest
 // semantic kernel, which the decode step recomputes).
 //
+// Optionally the step's queries are copied too (q_src -> q_dst), so that a
+// step whose inputs sit in host memory needs no separate copy: the kernel
+// reads k_new, v_new and q_src with ordinary loads, which may be page-locked
+// host memory mapped for the device.
+//
 // One 16-byte chunk per thread (a 128-dim bf16 row is 16 chunks).  The
 // launch carries a programmatic dependency: the kernel waits for the
 // previous kernel of the stream before writing and lets the next one (the
@@ -19,10 +24,13 @@ constexpr int kAppendThreads = 256;
 
 __global__ void __launch_bounds__(kAppendThreads)
     append_kernel(const uint4* k_new, const uint4* v_new, const int32_t* kv_lens, uint4* k_cache, uint4* v_cache,
-                  int Hkv, int Lmax, int nq, long long total, uint32_t* status) {
+                  int Hkv, int Lmax, int nq, long long total, const uint4* q_src, uint4* q_dst, long long q_chunks,
+                  uint32_t* status) {
   const long long e = static_cast<long long>(blockIdx.x) * kAppendThreads + threadIdx.x;
   pdl_wait();
-  if (e < total) {
+  if (e >= total) {
+    if (e - total < q_chunks) q_dst[e - total] = q_src[e - total];   // the step's queries
+  } else {
     const int chunk = static_cast<int>(e & 15);
     const int which = static_cast<int>((e >> 4) & 1);   // 0: key row, 1: value row
     const long long unit = e >> 5;                      // (b, h, t)
@@ -43,10 +51,11 @@ __global__ void __launch_bounds__(kAppendThreads)
 }  // namespace
 
 cudaError_t launch_append(const Shape& s, const void* k_new, const void* v_new, const int32_t* kv_lens, void* k_cache,
-                          void* v_cache, uint32_t* status, cudaStream_t st) {
+                          void* v_cache, const void* q_src, void* q_dst, uint32_t* status, cudaStream_t st) {
   const long long total = static_cast<long long>(s.B) * s.Hkv * s.nq * 32;
+  const long long q_chunks = q_src ? static_cast<long long>(s.B) * s.nq * s.Hkv * kGroup * 16 : 0;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((total + kAppendThreads - 1) / kAppendThreads), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>((total + q_chunks + kAppendThreads - 1) / kAppendThreads), 1, 1);
   cfg.blockDim = dim3(kAppendThreads, 1, 1);
   cfg.stream = st;
   cudaLaunchAttribute attr;
@@ -56,7 +65,7 @@ cudaError_t launch_append(const Shape& s, const void* k_new, const void* v_new, 
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, append_kernel, static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
                             kv_lens, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), s.Hkv, s.Lmax, s.nq,
-                            total, status);
+                            total, static_cast<const uint4*>(q_src), static_cast<uint4*>(q_dst), q_chunks, status);
 }
 
 }  // namespace infllmv2

@@ -60,7 +60,7 @@ cudaError_t launch_attn_tc(const Shape& s, const CUtensorMap& q_map, const CUten
 
 // ---- cache append of a decode step (rows kv_lens[b] - n_q .. kv_lens[b] - 1)
 cudaError_t launch_append(const Shape& s, const void* k_new, const void* v_new, const int32_t* kv_lens, void* k_cache,
-                          void* v_cache, uint32_t* status, cudaStream_t st);
+                          void* v_cache, const void* q_src, void* q_dst, uint32_t* status, cudaStream_t st);
 
 // ---- fused decode step (n_q = 1): newest kernel + selection + attention ----
 // Cluster size of the single-launch form on the current device (16 or 8),
