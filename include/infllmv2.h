@@ -18,9 +18,16 @@
  *      infllmv2_sparse_attn_prefill KV blocks [InfLLM v2 > Block-level key-value
  *                                   partitioning, eq. B_j; > Complexity analysis]
  *
+ * Around them: infllmv2_append_kv and infllmv2_decode_step (a whole decode
+ * step, one launch for n_q = 1), infllmv2_coarse_means and
+ * infllmv2_select_blocks_coarse_lse (the coarse-kernel LSE approximation),
+ * and infllmv2_sparse_attn_backward (gradients of stage 3 with the selection
+ * fixed [InfLLM v2 > Training-time considerations]).
+ *
  * Conventions shared by every entry point
  * ---------------------------------------
- * - Every tensor argument is a DEVICE pointer owned by the caller.  The
+ * - Every tensor argument is a DEVICE pointer owned by the caller (the few
+ *   arguments documented as possibly host memory excepted).  The
  *   library never allocates, frees or synchronises in these calls; all work
  *   is enqueued on `stream` (a cudaStream_t passed as void*, NULL = legacy
  *   default stream) and the calls return before it runs.
