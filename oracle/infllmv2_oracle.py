@@ -200,6 +200,18 @@ def top_k_blocks(r: np.ndarray, forced: list[int], topk: int, includes_forced: b
     return np.array(sorted(fset.union(int(x) for x in taken)), dtype=np.int64)
 
 
+def boundary_score(r: np.ndarray, blocks: np.ndarray, forced: list[int]) -> float:
+    """Score of the lowest-ranked scored block taken: the smallest r over the
+    selected blocks that are not forced, nan when no scored block is taken.
+
+    This is the k-th best score among the candidates of top_k_blocks, the one
+    the acceptance rule's 1e-4 relative tie band is measured from.
+    """
+    fset = set(forced)
+    scored = [int(j) for j in blocks if int(j) not in fset]
+    return float(min(r[j] for j in scored)) if scored else float("nan")
+
+
 @dataclasses.dataclass
 class Selection:
     blocks: np.ndarray   # selected block indices, ascending
@@ -235,9 +247,7 @@ def select_for_query(q: np.ndarray, Kc: np.ndarray, i: int, st: Settings,
     r = block_relevance(g, i, st.block, st.kernel, st.stride)
     forced = forced_blocks(i, st.block, st.n_init, st.n_local)
     blocks = top_k_blocks(r, forced, st.topk, st.includes_forced)
-    scored = [j for j in blocks if j not in set(forced)]
-    boundary = float(min(r[j] for j in scored)) if scored else float("nan")
-    return Selection(blocks=blocks, r=r, g=g, boundary=boundary)
+    return Selection(blocks=blocks, r=r, g=g, boundary=boundary_score(r, blocks, forced))
 
 
 # --------------------------------------------------------------------------

@@ -163,6 +163,11 @@ def test_hand_worked_selections():
             want = [float(Fraction(a, b)) for a, b in zip(case["r_block_num"], case["r_block_den"])]
             np.testing.assert_allclose(sel.r, want, rtol=1e-14)
             assert sel.blocks.tolist() == expect, (case["name"], topk_s)
+            bnd = case["boundary"][topk_s]
+            if bnd is None:
+                assert math.isnan(sel.boundary), (case["name"], topk_s, sel.boundary)
+            else:
+                assert abs(sel.boundary - float(Fraction(*bnd))) <= 1e-14, (case["name"], topk_s, sel.boundary)
 
 
 # --------------------------------------------------- selection invariants ----
@@ -427,12 +432,25 @@ def _planted_mistakes():
     def lse_plain_max(z):                              # max instead of log-sum-exp
         return z.max(axis=1)
 
+    def bnd_max_not_min(r, blocks, forced):            # best taken score instead of the last
+        scored = [int(j) for j in blocks if int(j) not in set(forced)]
+        return float(max(r[j] for j in scored)) if scored else float("nan")
+
+    def bnd_with_forced(r, blocks, forced):            # forced blocks counted in
+        return float(min(r[int(j)] for j in blocks)) if len(blocks) else float("nan")
+
+    def bnd_first_not_taken(r, blocks, forced):        # best score left out instead
+        rest = [j for j in range(r.shape[0]) if j not in set(int(b) for b in blocks) and np.isfinite(r[j])]
+        return float(max(r[j] for j in rest)) if rest else float("nan")
+
     return [("block_relevance", br_off_by_one), ("group_relevance", gr_max_not_mean),
             ("kernel_softmax", ks_no_norm), ("forced_blocks", forced_no_prev),
-            ("window_means", wm_half_stride), ("log_sum_exp", lse_plain_max)]
+            ("window_means", wm_half_stride), ("log_sum_exp", lse_plain_max),
+            ("boundary_score", bnd_max_not_min), ("boundary_score", bnd_with_forced),
+            ("boundary_score", bnd_first_not_taken)]
 
 
-@pytest.mark.parametrize("name,bad", _planted_mistakes())
+@pytest.mark.parametrize("name,bad", _planted_mistakes(), ids=lambda x: x if isinstance(x, str) else x.__name__)
 def test_planted_oracle_mistakes_are_caught(monkeypatch, name, bad):
     monkeypatch.setattr(O.infllmv2_oracle, name, bad)
     monkeypatch.setattr(O, name, bad)

@@ -35,6 +35,15 @@
 //              stage frees once its P V product is done).
 // TMEM: columns [0,256) two S buffers, [256,384) the O accumulator,
 // [384,512) two P buffers.
+//
+// P enters P V as bf16.  One bf16 carries 8 significant bits, and where a
+// row averages only a few values the rounding of its probabilities reaches
+// the output at 2^-9 |V|.  A tile in which some token attends fewer than
+// kSplitKeys keys therefore feeds P as hi = bf16(p) plus lo = bf16(p - hi)
+// (16 significant bits): the softmax warps write lo into the S columns they
+// have just read, the issuer adds a second product per item, and S of item
+// i + 2 waits until P V of item i (which reads that S buffer) is done.
+// Longer rows average the rounding away (error below 3e-4 at 1024 keys).
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -55,6 +64,7 @@ constexpr uint32_t kTmemCols = 512;
 // buffers (bf16 pairs, one row per lane: the A operand of O += P V).
 constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
 constexpr float kLazyRescale = 8.0f;
+constexpr int kSplitKeys = 2048;   // tiles with a row attending fewer keys feed P as hi + lo
 
 struct TcParams {
   int B, Hkv, Lmax, nq, kmax, nbmax;
@@ -68,7 +78,7 @@ struct TcParams {
 };
 
 struct TcLayout {
-  int q, kv, vv, bars, slot, bits, ulist, umask, scan, xch, total;
+  int q, kv, vv, bars, slot, bits, ulist, umask, scan, kcnt, xch, total;
 };
 
 __host__ __device__ inline TcLayout tc_layout(int nbmax) {
@@ -82,7 +92,8 @@ __host__ __device__ inline TcLayout tc_layout(int nbmax) {
   l.ulist = l.bits + ((nbmax + 15) & ~15);
   l.umask = l.ulist + nbmax * 4;
   l.scan = l.umask + ((nbmax + 15) & ~15);
-  l.xch = l.scan + 64;                       // [2 column halves][128 rows] fp32 exchange
+  l.kcnt = l.scan + 64;                      // keys attended per token of the tile
+  l.xch = l.kcnt + 64;                       // [2 column halves][128 rows] fp32 exchange
   l.total = l.xch + 2 * 128 * 4;
   return l;
 }
@@ -112,6 +123,63 @@ __device__ __forceinline__ float exp2_fma(float x) {
   y = fmaf(y, f, 1.0f);
   const int e = static_cast<int>(n);
   return e < -125 ? 0.f : __int_as_float(__float_as_int(y) + (e << 23));
+}
+
+// bf16 pair of the rounding residues p - bf16(p) of two probabilities whose
+// rounded pair is `hi` (pack_bf16x2 order: p0 in the low half).
+__device__ __forceinline__ uint32_t lo_bf16x2(float p0, float p1, uint32_t hi) {
+  const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xFFFF0000u);
+  return pack_bf16x2(p0 - h0, p1 - h1);
+}
+
+// One warp's 64 probabilities of its row for an item (bf16 pairs into w),
+// returning their sum.  whole: the row sees all 64 keys or none (sel false),
+// so no per-key mask; otherwise keys [0, nv) count.  Three in eight
+// exponentials go through the FMA pipe to share the load with the MUFU unit.
+// kSplit: the lo parts p - bf16(p) go to TMEM at lo_addr, 16 pairs at a time.
+template <bool kSplit>
+__device__ __forceinline__ float row_probs(const uint32_t (&s)[64], uint32_t (&w)[32], bool whole, bool sel,
+                                           float m_use, int nv, float scale2, uint32_t lo_addr) {
+  float lsum = 0.f;
+  if (whole) {
+    // A row that skipped the block subtracts +inf: every exp2 is 0.
+    const float m_eff = sel ? m_use : INFINITY;
+    float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+    for (int x0 = 0; x0 < 32; x0 += 16) {
+      uint32_t wl[16];
+#pragma unroll
+      for (int x = x0; x < x0 + 16; ++x) {
+        const float a0 = fmaf(__uint_as_float(s[2 * x]), scale2, -m_eff);
+        const float a1 = fmaf(__uint_as_float(s[2 * x + 1]), scale2, -m_eff);
+        const float p0 = ((x & 3) == 3) ? exp2_fma(a0) : fast_exp2(a0);
+        const float p1 = ((x & 3) != 0) ? exp2_fma(a1) : fast_exp2(a1);
+        ls0 += p0;
+        ls1 += p1;
+        w[x] = pack_bf16x2(p0, p1);
+        if (kSplit) wl[x - x0] = lo_bf16x2(p0, p1, w[x]);
+      }
+      if (kSplit) tc::st16(lo_addr + x0, wl);
+    }
+    lsum = ls0 + ls1;
+  } else {
+#pragma unroll
+    for (int x0 = 0; x0 < 32; x0 += 16) {
+      uint32_t wl[16];
+#pragma unroll
+      for (int x = x0; x < x0 + 16; ++x) {
+        const float a0 = __uint_as_float(s[2 * x]) * scale2 - m_use;
+        const float a1 = __uint_as_float(s[2 * x + 1]) * scale2 - m_use;
+        const float p0 = (2 * x < nv) ? fast_exp2(a0) : 0.f;
+        const float p1 = (2 * x + 1 < nv) ? fast_exp2(a1) : 0.f;
+        lsum += p0 + p1;
+        w[x] = pack_bf16x2(p0, p1);
+        if (kSplit) wl[x - x0] = lo_bf16x2(p0, p1, w[x]);
+      }
+      if (kSplit) tc::st16(lo_addr + x0, wl);
+    }
+  }
+  return lsum;
 }
 
 enum Bar { kQFull = 0, kKFull = 1, kKEmpty = kKFull + kTcKStages, kVFull = kKEmpty + kTcKStages,
@@ -156,19 +224,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   // ---- union of the tile's block sets: bit `tok` of bits[j] ----
   uint32_t* bits32 = reinterpret_cast<uint32_t*>(bits);
+  int* kcnt = reinterpret_cast<int*>(smem + lay.kcnt);
   for (int w = tid; w < (nb + 3) / 4; w += kTcThreads) bits32[w] = 0u;
   __syncthreads();
-  for (int e = tid; e < n_act * p.kmax; e += kTcThreads) {
-    const int tok = e / p.kmax, k = e % p.kmax;
-    const size_t u = static_cast<size_t>(bh) * p.nq + t0 + tok;
-    const int ns = min(p.n_sel[u], p.kmax);
-    if (k < ns) {
-      const int j = p.block_idx[u * p.kmax + k];
-      const int c_tok = (L - p.nq + t0 + tok) / kBlock;
-      if (j >= 0 && j <= c_tok) atomicOr(&bits32[j >> 2], (1u << tok) << ((j & 3) * 8));
+  // Warp `tok` (< 8) marks its token's blocks and counts the keys it attends.
+  if (warp < kTcTokens) {
+    const int tok = warp;
+    int keys = 0;
+    if (tok < n_act) {
+      const size_t u = static_cast<size_t>(bh) * p.nq + t0 + tok;
+      const int ns = min(p.n_sel[u], p.kmax);
+      const int i_tok = L - p.nq + t0 + tok;
+      for (int k = lane; k < ns; k += 32) {
+        const int j = p.block_idx[u * p.kmax + k];
+        if (j >= 0 && j <= i_tok / kBlock) {
+          atomicOr(&bits32[j >> 2], (1u << tok) << ((j & 3) * 8));
+          keys += min(kBlock, i_tok - j * kBlock + 1);
+        }
+      }
     }
+    keys = warp_sum_int(keys);
+    if (lane == 0) kcnt[tok] = keys;
   }
   __syncthreads();
+  // Hi + lo probabilities when some token of the tile attends few keys.
+  bool split = false;
+#pragma unroll
+  for (int tok = 0; tok < kTcTokens; ++tok) split |= (tok < n_act) && (kcnt[tok] < kSplitKeys);
   {
     const int per = (nb + kTcThreads - 1) / kTcThreads;
     const int lo = tid * per, hi = min(nb, lo + per);
@@ -294,8 +376,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t idle = 0;
       while (ok && n_o < nit) {
         bool progressed = false;
+        // With split probabilities S buffer n_s & 1 also holds the lo part of
+        // item n_s - 2, read by that item's P V product.
         if (n_s < nit && mbar_try_wait(&bars[kKFull + n_s % kTcKStages], (n_s / kTcKStages) & 1) &&
-            (n_s < 2 || mbar_try_wait(&bars[kSFree + (n_s & 1)], ((n_s >> 1) - 1) & 1))) {
+            (n_s < 2 || (mbar_try_wait(&bars[kSFree + (n_s & 1)], ((n_s >> 1) - 1) & 1) &&
+                         (!split || mbar_try_wait(&bars[kODone + (n_s & 1)], ((n_s - 2) >> 1) & 1))))) {
           const int st = n_s % kTcKStages, sb = n_s & 1;
           tc::fence_after_sync();
           const uint64_t kd = k_desc0 + static_cast<uint64_t>(st * (kTcItemBytes >> 4));
@@ -318,6 +403,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int k = 0; k < 8; ++k)
             tc::mma_ts(tmem + kColO, tmem + kColP + pb * 64 + 8 * k, vd + static_cast<uint64_t>((k * 2048) >> 4),
                        kIdO, (m > 0 || k > 0) ? 1u : 0u);
+          if (split) {
+            // lo parts: keys 64 x + [0, 64) of the item sit in S columns
+            // 128 (m & 1) + 64 x + [0, 32).
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              tc::mma_ts(tmem + kColO, tmem + kColS + pb * 128 + 64 * (k >> 2) + 8 * (k & 3),
+                         vd + static_cast<uint64_t>((k * 2048) >> 4), kIdO, 1u);
+          }
           tc::commit(&bars[kODone + (m & 1)]);
           tc::commit(&bars[kVEmpty + st]);
           ++n_o;
@@ -424,39 +517,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       uint32_t w[32];   // this warp's 64 probabilities of the row, bf16 pairs
       float lsum = 0.f;
+      // In split tiles the lo parts go, 16 pairs at a time, over the S
+      // columns this warp read for the item (its S buffer is not refilled
+      // before this item's P V product is done).
+      const uint32_t lo_addr = lane_addr + kColS + sb * 128 + half * 64;
       if (warp_sel) {
         // Probabilities before waiting on the tensor core: only the P store
-        // and an O rescale depend on earlier products.  Three in eight go
-        // through the FMA pipe to share the load with the MUFU unit.
-        if (whole) {
-          // A row that skipped the block subtracts +inf: every exp2 is 0.
-          const float m_eff = sel ? m_use : INFINITY;
-          float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-          for (int x = 0; x < 32; ++x) {
-            const float a0 = fmaf(__uint_as_float(s[2 * x]), p.scale2, -m_eff);
-            const float a1 = fmaf(__uint_as_float(s[2 * x + 1]), p.scale2, -m_eff);
-            const float p0 = ((x & 3) == 3) ? exp2_fma(a0) : fast_exp2(a0);
-            const float p1 = ((x & 3) != 0) ? exp2_fma(a1) : fast_exp2(a1);
-            ls0 += p0;
-            ls1 += p1;
-            w[x] = pack_bf16x2(p0, p1);
-          }
-          lsum = ls0 + ls1;
-        } else {
-#pragma unroll
-          for (int x = 0; x < 32; ++x) {
-            const float a0 = __uint_as_float(s[2 * x]) * p.scale2 - m_use;
-            const float a1 = __uint_as_float(s[2 * x + 1]) * p.scale2 - m_use;
-            const float p0 = (2 * x < nv) ? fast_exp2(a0) : 0.f;
-            const float p1 = (2 * x + 1 < nv) ? fast_exp2(a1) : 0.f;
-            lsum += p0 + p1;
-            w[x] = pack_bf16x2(p0, p1);
-          }
-        }
+        // and an O rescale depend on earlier products.
+        lsum = split ? row_probs<true>(s, w, whole, sel, m_use, nv, p.scale2, lo_addr)
+                     : row_probs<false>(s, w, whole, sel, m_use, nv, p.scale2, lo_addr);
       } else {
 #pragma unroll
         for (int x = 0; x < 32; ++x) w[x] = 0u;
+        if (split) {
+          uint32_t z16[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x) z16[x] = 0u;
+          tc::st16(lo_addr, z16);
+          tc::st16(lo_addr + 16, z16);
+        }
       }
       // P buffer it & 1 was last read by the product of item it - 2.
       if (it >= 2 && ok)
