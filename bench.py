@@ -130,16 +130,22 @@ def _traffic(kernel: str, workload: str):
 # ----------------------------------------------------------------- decode ---
 
 class DecodeBench:
-    def __init__(self, dev, seed_offset=0):
+    """One decode-path workload (n_q <= 16 tokens per sequence) on `replicas`
+    rotating device copies of its inputs; a step is one infllmv2_decode_step
+    call (one fused launch for n_q = 1, compress + select + attend otherwise)."""
+
+    def __init__(self, dev, seed_offset=0, name=DECODE, replicas=REPLICAS):
         import torch
         import trainable_block_sparse_infllm_gb300 as T
         self.T, self.torch, self.dev = T, torch, dev
-        wl = S.WORKLOADS[DECODE]
+        self.name, self.replicas = name, replicas
+        wl = S.WORKLOADS[name]
         if seed_offset:
             wl = wl.scaled(seed=wl.seed + 1000 * seed_offset)
         self.wl = wl
         inp = S.make_inputs(wl)
         self.inp = inp
+        self.sha256 = inp.sha256()
         self.p = T.make_params(wl.batch, wl.n_kv_heads, wl.kv_len, wl.topk, wl.topk_includes_forced)
         B, H, L, nq = wl.batch, wl.n_kv_heads, wl.kv_len, wl.n_q
 
@@ -152,7 +158,7 @@ class DecodeBench:
         self.reps = []
         d = wl.head_dim
         nq_el, kv_el = q0.numel(), B * H * nq * d
-        for r in range(REPLICAS):
+        for r in range(replicas):
             # One device buffer per replica holds a step's inputs back to back
             # (q, then the new tokens' keys and values), so that the end-to-end
             # leg moves them with one host-to-device copy.
@@ -197,56 +203,89 @@ class DecodeBench:
         self.T.decode_step(self.p, rep["q"], rep["k"], rep["v"], self.lens, rep["kc"], rep["idx"], rep["nsel"],
                            rep["out"], rep["lse"], rep["ws_step"])
 
-    def capture(self):
+    def capture(self, per_graph=REPLICAS):
+        """CUDA graphs: one step per replica, and `per_graph` steps back to
+        back over the rotating replicas."""
         torch = self.torch
-        for r in range(REPLICAS):
+        R = self.replicas
+        for r in range(R):
             self.step(r)                        # warm: module load, attributes, symbols
         torch.cuda.synchronize()
         self.graphs = []                        # one step each (end-to-end leg, remainders)
-        for r in range(REPLICAS):
+        for r in range(R):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 self.step(r)
             self.graphs.append(g)
-        self.round = torch.cuda.CUDAGraph()     # REPLICAS steps back to back
+        self.per_graph = per_graph
+        self.round = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.round):
-            for r in range(REPLICAS):
-                self.step(r)
+            for x in range(per_graph):
+                self.step(x % R)
         torch.cuda.synchronize()
 
     def run_steps(self, n):
-        """n steps: whole rounds of REPLICAS, then single steps."""
-        for _ in range(n // REPLICAS):
+        """n steps: whole graphs of per_graph steps, then single steps."""
+        for _ in range(n // self.per_graph):
             self.round.replay()
-        for r in range(n % REPLICAS):
-            self.graphs[r].replay()
+        for x in range(n % self.per_graph):
+            self.graphs[x % self.replicas].replay()
+
+    def timed_steps(self, n, warmup):
+        """Seconds per step over n steps (CUDA events on the launching stream)."""
+        torch = self.torch
+        self.run_steps(max(warmup, self.per_graph))
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        self.run_steps(n)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e-3 / n
 
     def time_fn(self, fn, n, warm=3):
         torch = self.torch
         for i in range(warm):
-            fn(i % REPLICAS)
+            fn(i % self.replicas)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for i in range(n):
-            fn(i % REPLICAS)
+            fn(i % self.replicas)
         e1.record()
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / n * 1e-3     # seconds per call
 
+    def working_set_bytes(self):
+        rep = self.reps[0]
+        return sum(rep[k].numel() * rep[k].element_size() for k in ("k", "v", "kc", "q"))
+
     def algorithmic_bytes(self):
         """Bytes a decode step must move: queries, both kernel-mean planes, the
-        selected K and V tiles, outputs, indices and the newest kernel."""
+        K and V tiles of the union of the step's selected blocks per (b, h_kv)
+        (each block once, however many of the n_q tokens chose it), outputs,
+        indices and the newest kernels."""
         wl = self.wl
         B, H, nq, d = wl.batch, wl.n_kv_heads, wl.n_q, wl.head_dim
         n_c = S_n_c(wl.kv_len)
+        idx = self.reps[0]["idx"].cpu().numpy()
         nsel = self.reps[0]["nsel"].cpu().numpy()
+        union = 0
+        for b in range(B):
+            for h in range(H):
+                blocks = set()
+                for t in range(nq):
+                    blocks.update(idx[b, h, t, :nsel[b, h, t]].tolist())
+                union += len(blocks)
+        self.union_blocks = union
+        self.selected_blocks = int(nsel.sum())
         q_b = B * nq * wl.n_heads * d * 2
         kc_b = B * H * n_c * d * 4                      # hi + lo planes
-        kv_b = int(nsel.sum()) * wl.block * d * 2 * 2   # selected K and V tiles
+        kv_b = union * wl.block * d * 2 * 2             # selected K and V tiles, each block once
         out_b = q_b
         idx_b = B * H * nq * (self.kmax + 1) * 4
-        comp_b = B * H * (wl.kernel * d * 2 + d * 4)    # newest kernel: 32 keys in, 512 B out
+        n_new = S_n_c(wl.kv_len) - S_n_c(wl.kv_len - nq)  # kernels ending inside the step's tokens
+        comp_b = B * H * n_new * (wl.kernel * d * 2 + d * 4)   # 32 keys in, 512 B out each
         return {"compress": comp_b, "select": kc_b + q_b + idx_b,
                 "attend": kv_b + q_b + out_b + idx_b + B * nq * wl.n_heads * 4,
                 "step": comp_b + kc_b + q_b * 2 + kv_b + idx_b}
@@ -264,6 +303,138 @@ def max_over_ranks(value: float, dist=None, device=None) -> float:
 
 def S_n_c(L, p=32, s=16):
     return (L - p) // s + 1 if L >= p else 0
+
+
+# ------------------------------------------------- every decode workload ---
+
+WORKLOAD_TEXT = {
+    "decode_4k": "decode_4k: batch 1, 16 q / 1 kv head, 4096-token cache, top-16 incl. forced, 1 query/seq",
+    "decode_32k": "decode_32k: batch 8, 32 q / 2 kv heads, 32768-token cache, top-64 incl. forced, 1 query/seq",
+    "decode_128k": "decode_128k: batch 4, 32 q / 2 kv heads, 131072-token cache, top-64 incl. forced, 1 query/seq",
+    "verify_128k": "verify_128k: batch 4, 32 q / 2 kv heads, 131072-token cache + 8 draft tokens attending "
+                   "causally, top-64 per token incl. forced",
+    "prefill_32k": "prefill_32k: batch 1, 32 q / 2 kv heads, causal 32768 x 32768, top-64 + init + local",
+}
+
+
+def _l2_bytes(dev):
+    import torch
+    try:
+        return int(torch.cuda.get_device_properties(dev).L2_cache_size)
+    except Exception:
+        return 129 * 2 ** 20
+
+
+def decode_workload_line(name, dev, steps, warmup, peaks, warm_l2=False, bench=None):
+    """tokens/s and the HBM roofline of one decode-path workload.  Inputs
+    rotate over enough replicas that every step reads cold HBM (three times
+    L2 at least), except where one copy of the working set is already small
+    enough that the step is latency-bound, which the line then says; with
+    warm_l2 one more figure replays a single replica (labelled)."""
+    import torch
+    if bench is None:
+        wl = S.WORKLOADS[name]
+        probe = wl.batch * wl.n_kv_heads * wl.kv_len * wl.head_dim * 2 * 2
+        l2 = _l2_bytes(dev)
+        reps = 1 if probe * 16 < l2 else min(REPLICAS, max(2, -(-3 * l2 // probe)))
+        bench = DecodeBench(dev, name=name, replicas=reps)
+        bench.capture(per_graph=max(8, reps))
+    wl = bench.wl
+    t = bench.timed_steps(steps, warmup)
+    ab = bench.algorithmic_bytes()
+    ws = bench.working_set_bytes()
+    achieved = ab["step"] / t / 1e9
+    # The single-launch form of the step is the one that needs no workspace.
+    launches = 1 if bench.T.workspace_size(bench.p, wl.n_q, bench.T.OP_DECODE_STEP) == 0 else 3
+    line = {
+        "workload": WORKLOAD_TEXT[name],
+        "tokens_per_s": wl.batch * wl.n_q / t,
+        "us_per_step": t * 1e6,
+        "launches_per_step": launches,
+        "l2": (f"{bench.replicas} rotating input replicas ({bench.replicas * ws / 1e9:.2f} GB, "
+               f"{bench.replicas * ws / _l2_bytes(dev):.1f}x L2)" if bench.replicas > 1 else
+               f"one input copy ({ws / 1e6:.1f} MB, inside L2): latency-bound, cached bytes"),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks[0], "unit": "GB/s",
+                     "frac": achieved / peaks[0], "peak_kind": peaks[3],
+                     "algorithmic_bytes_per_step": ab["step"],
+                     "kv_blocks": {"selected": bench.selected_blocks, "union_fetched": bench.union_blocks}},
+        "sha256": bench.sha256,
+    }
+    if warm_l2:
+        one = DecodeBench(dev, name=name, replicas=1)
+        one.capture(per_graph=8)
+        tw = one.timed_steps(steps, warmup)
+        line["warm_l2"] = {"tokens_per_s": wl.batch * wl.n_q / tw, "us_per_step": tw * 1e6,
+                           "note": "one input copy replayed: the step's 50 MB of kernel means and selected "
+                                   "blocks stay in L2 between steps (not a roofline figure)"}
+        del one
+    return line
+
+
+# The oracle as it stands, timed on the host: one thread, and every core
+# (independent units spread over a spawn process pool, one thread each).
+
+_POOL = {}
+
+
+def _pool_init(folder, names, wl, st):
+    for n in names:
+        _POOL[n] = np.load(os.path.join(folder, n + ".npy"), mmap_mode="r")
+    _POOL["inp"] = S.Inputs(wl=wl, q=_POOL["q"], k=_POOL["k"], v=_POOL["v"], kv_lens=np.asarray(_POOL["kv_lens"]),
+                            planted=np.zeros((wl.batch, wl.n_kv_heads, 0), dtype=np.int64))
+    _POOL["st"] = st
+
+
+def _oracle_units(inp, st, units):
+    import oracle as O
+    sels = O.run_selection(inp, st, units=units)
+    O.run_attention(inp, st, {u: x.blocks for u, x in sels.items()}, units=units)
+    return len(units)
+
+
+def _pool_task(units):
+    return _oracle_units(_POOL["inp"], _POOL["st"], units)
+
+
+def oracle_baseline(name, budget_s=4.0, inp=None):
+    """Oracle tokens/s on a bounded sample of the workload: one thread, then
+    all host cores.  A token of a sequence is its units over every KV head."""
+    import multiprocessing as mp
+    import tempfile
+    import oracle as O
+    wl = S.WORKLOADS[name]
+    inp = S.make_inputs(wl) if inp is None else inp
+    st = O.Settings(topk=wl.topk, n_init=wl.n_init, n_local=wl.n_local, includes_forced=wl.topk_includes_forced)
+    units = [(b, h, t) for b in range(wl.batch) for t in range(wl.n_q) for h in range(wl.n_kv_heads)]
+    rng = np.random.default_rng(0)
+    order = rng.permutation(len(units))
+    # one thread (this process keeps BLAS at one thread)
+    t0 = time.perf_counter()
+    done = 0
+    while done == 0 or (time.perf_counter() - t0 < budget_s and done < len(units)):
+        done += _oracle_units(inp, st, [units[order[done % len(units)]]])
+    one = done / wl.n_kv_heads / (time.perf_counter() - t0)
+    # all cores: as many units per worker as one thread managed in the budget
+    cores = os.cpu_count() or 1
+    per_worker = max(1, done)
+    sample = [units[order[x % len(units)]] for x in range(cores * per_worker)]
+    tasks = [sample[w * per_worker:(w + 1) * per_worker] for w in range(cores)]
+    with tempfile.TemporaryDirectory() as folder:
+        arrays = {"q": inp.q, "k": inp.k, "v": inp.v, "kv_lens": inp.kv_lens}
+        for n, a in arrays.items():
+            np.save(os.path.join(folder, n + ".npy"), np.ascontiguousarray(a))
+        with mp.get_context("spawn").Pool(cores, initializer=_pool_init,
+                                          initargs=(folder, list(arrays), wl, st)) as pool:
+            pool.map(_pool_task, [[u] for u in sample[:cores]], chunksize=1)   # workers up, inputs mapped
+            t1 = time.perf_counter()
+            n_all = sum(pool.map(_pool_task, tasks, chunksize=1))
+            dt = time.perf_counter() - t1
+    allc = n_all / wl.n_kv_heads / dt
+    return {"value": allc, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "one_thread": {"value": one, "cores": 1},
+            "sample": f"{name}: {done} (one thread) and {n_all} (all cores) of its {len(units)} (b, h_kv, t) units, "
+                      f"kernel means + selection + attention in numpy fp64; a token counts its {wl.n_kv_heads} "
+                      f"KV-head units"}
 
 
 # ---------------------------------------------------------------- prefill ---
@@ -329,6 +500,7 @@ def prefill_line(dev, steps, warmup, peaks):
             pairs += int(keys.clip(min=0).sum())
     flops = 4.0 * wl.head_dim * pairs * wl.group
     achieved = flops / t_stage["attend"] / 1e12
+    issued, split_tiles, n_tiles, union_sum, sel_sum = _prefill_issued_flops(wl, inp.kv_lens, idx_h, nsel_h)
 
     # The coarse-kernel LSE approximation of the selection (windows of 64
     # keys): its time against the exact selection's, and how many of the
@@ -377,34 +549,54 @@ def prefill_line(dev, steps, warmup, peaks):
         "roofline": {"kernel": "attn_tc_kernel (sparse_attn_prefill)", "bound": "tensor",
                      "achieved": achieved, "peak": peaks[1], "unit": "TFLOP/s",
                      "frac": achieved / peaks[1], "peak_kind": peaks[3] + " burst bf16",
-                     "algorithmic_flop_per_launch": flops, "traffic": _traffic("attn_tc_kernel", PREFILL)},
+                     "algorithmic_flop_per_launch": flops, "traffic": _traffic("attn_tc_kernel", PREFILL),
+                     "issued": {"flop_per_launch": issued, "tflops": issued / t_stage["attend"] / 1e12,
+                                "frac": issued / t_stage["attend"] / 1e12 / peaks[1],
+                                "issued_over_useful": issued / flops,
+                                "union_over_selected_blocks": union_sum / max(sel_sum, 1),
+                                "tiles_with_hi_lo_probabilities": f"{split_tiles} of {n_tiles}",
+                                "note": "tcgen05 products the kernel issues: S and O += P V over the union of each "
+                                        "8-token tile's blocks, two blocks per item (a lone last block is issued "
+                                        "as a pair), a second P V product in tiles fed hi + lo probabilities"}},
         "coarse_lse": coarse,
         "backward": backward,
     }
 
 
+def _prefill_issued_flops(wl, kv_lens, idx_h, nsel_h, tile=8, split_keys=2048):
+    """MMA FLOPs the prefill kernel issues for this selection: per tile of
+    `tile` tokens x 16 heads (128 rows), ceil(|union| / 2) items of 128 keys,
+    each an S product and a P V product of 2 * 128 * 128 * 128 FLOPs, plus a
+    second P V product in tiles where some token attends < split_keys keys."""
+    B, H, nq, m = wl.batch, wl.n_kv_heads, wl.n_q, wl.block
+    item = 2.0 * 128 * 128 * 128
+    issued, split_tiles, n_tiles, union_sum, sel_sum = 0.0, 0, 0, 0, 0
+    nbmax = -(-wl.kv_len // m)
+    for b in range(B):
+        L = int(kv_lens[b])
+        pos = L - nq + np.arange(nq)
+        for h in range(H):
+            rows = idx_h[b, h]
+            valid = (np.arange(rows.shape[1])[None, :] < nsel_h[b, h][:, None]) & (rows >= 0)
+            keys = np.where(valid, np.minimum(m, pos[:, None] - rows * m + 1), 0).clip(min=0).sum(axis=1)
+            nt = -(-nq // tile)
+            mask = np.zeros((nt, nbmax), dtype=bool)
+            tok = np.broadcast_to(np.arange(nq)[:, None], rows.shape)
+            mask[(tok[valid] // tile), rows[valid]] = True
+            union = mask.sum(axis=1)
+            tile_min_keys = np.full(nt, np.iinfo(np.int64).max)
+            np.minimum.at(tile_min_keys, np.arange(nq) // tile, keys)
+            split = tile_min_keys < split_keys
+            items = -(-union // 2)
+            issued += float(items.sum()) * item * 2 + float(items[split].sum()) * item
+            split_tiles += int(split.sum())
+            n_tiles += nt
+            union_sum += int(union.sum())
+            sel_sum += int(valid.sum())
+    return issued, split_tiles, n_tiles, union_sum * tile, sel_sum
+
+
 # ----------------------------------------------------------- CPU baseline ---
-
-def cpu_baseline(budget_s=15.0):
-    """The fp64 oracle, as it stands, on a bounded sample of the decode workload."""
-    import oracle as O
-    wl = S.WORKLOADS[DECODE]
-    inp = S.make_inputs(wl)
-    st = O.Settings(topk=wl.topk, includes_forced=wl.topk_includes_forced)
-    t0 = time.perf_counter()
-    seqs = 0
-    for b in range(wl.batch):
-        units = [(b, h, t) for h in range(wl.n_kv_heads) for t in range(wl.n_q)]
-        sels = O.run_selection(inp, st, units=units)
-        O.run_attention(inp, st, {u: s.blocks for u, s in sels.items()}, units=units)
-        seqs += 1
-        if time.perf_counter() - t0 > budget_s:
-            break
-    dt = time.perf_counter() - t0
-    return {"value": seqs * wl.n_q / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{seqs} of {wl.batch} sequences of {DECODE} (both KV heads: kernel means, "
-                      f"selection, attention), single-threaded numpy fp64"}
-
 
 def reference_arm(args):
     rank = int(os.environ.get("RANK", "0"))
@@ -509,6 +701,7 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true", help="headline workload and prefill only")
     ap.add_argument("--profile", choices=["decode", "prefill", "backward"],
                     help="run warmup + steps untimed passes of one path on one input copy and exit "
                          "(a small, fixed launch sequence for ncu)")
@@ -617,6 +810,16 @@ def main():
     if not args.no_prefill and rank == 0:
         prefill = prefill_line(dev, max(3, min(10, args.steps // 20)), 3, peaks)
 
+    # Every other workload on its own, and decode_128k's warm-L2 figure.
+    workloads = {}
+    if rank == 0 and not args.no_workloads:
+        n_w = max(20, min(200, args.steps))
+        workloads[DECODE] = decode_workload_line(DECODE, dev, n_w, args.warmup, peaks, warm_l2=True, bench=bench)
+        for name in ("decode_4k", "decode_32k", "verify_128k"):
+            workloads[name] = decode_workload_line(name, dev, n_w, args.warmup, peaks)
+            torch.cuda.empty_cache()
+        assert T.get_device_status(clear=True) == 0, "device status flagged during the workload lines"
+
     if rank != 0:
         if dist:
             dist.destroy_process_group()
@@ -660,8 +863,15 @@ def main():
                 "transfers": "the append kernel reads q, k, v from pinned host memory; the step stores its output there"},
         "prefill": prefill,
     }
+    line["workloads"] = workloads
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline()
+        for name in list(workloads) + ([PREFILL] if prefill else []):
+            cb = oracle_baseline(name)
+            (prefill if name == PREFILL else workloads[name])["cpu_baseline"] = cb
+            if name == DECODE:
+                line["cpu_baseline"] = cb
+        if DECODE not in workloads:
+            line["cpu_baseline"] = oracle_baseline(DECODE)
     print(json.dumps(line))
     if dist:
         dist.destroy_process_group()

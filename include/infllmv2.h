@@ -261,13 +261,15 @@ int infllmv2_append_kv(const infllmv2_params* p, int32_t n_q, const void* k_new,
  *           memory mapped for the device (e.g. from cudaHostAlloc on a system
  *           with unified addressing): the result then reaches the host without
  *           a separate copy.
- *   n_q in [1, 16].  With n_q = 1 and a cache of at most 128 * 16 blocks
- *   (131072 tokens; 65536 where only 8-CTA clusters fit) the step is one
- *   launch of a thread-block cluster per (b, h_kv) that keeps every
- *   intermediate on chip and needs no workspace; otherwise it enqueues the
- *   three stages in order.  Workspace: infllmv2_workspace_size(p, n_q,
- *   INFLLMV2_OP_DECODE_STEP) bytes (0 for the single-launch form; workspace
- *   may then be NULL).
+ *   n_q in [1, 16].  With n_q = 1 the step is one launch of a thread-block
+ *   cluster of C CTAs per (b, h_kv), one CTA per SM, that keeps every
+ *   intermediate on chip and needs no workspace.  C (at most 16) is chosen
+ *   for the device and batch so that all batch * n_kv_heads clusters are
+ *   resident at once; the form applies while the cache holds at most
+ *   256 C blocks of 64 tokens and at most 4096 blocks (262144 tokens).
+ *   Otherwise the step enqueues the three stages in order.  Workspace:
+ *   infllmv2_workspace_size(p, n_q, INFLLMV2_OP_DECODE_STEP) bytes (0 for
+ *   the single-launch form; workspace may then be NULL).
  */
 int infllmv2_decode_step(const infllmv2_params* p, const void* q, int32_t n_q, const void* k_cache,
                          const void* v_cache, const int32_t* kv_lens, void* kc, int32_t* block_idx,

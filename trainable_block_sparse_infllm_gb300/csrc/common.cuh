@@ -159,6 +159,20 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Split cluster barrier: every thread of every CTA arrives, then waits for
+// the phase to complete.  arrive.release orders this thread's earlier
+// (including remote) shared-memory writes before the waiters' acquire;
+// the relaxed form orders nothing and only marks the CTA as running.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Address of the same shared-memory variable in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank) {
   uint32_t r;
@@ -197,6 +211,16 @@ __device__ __forceinline__ float2 ld_dsmem_f32x2(uint32_t addr) {
 // makes them visible to the owning CTA.
 __device__ __forceinline__ void st_dsmem_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_dsmem_f32x2(uint32_t addr, float2 v) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y) : "memory");
+}
+
+__device__ __forceinline__ void st_dsmem_f32x4(uint32_t addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w)
+               : "memory");
 }
 
 __device__ __forceinline__ void st_dsmem_u32(uint32_t addr, uint32_t v) {

@@ -8,32 +8,44 @@
 // selected], [> Block-level key-value partitioning], [> Complexity analysis,
 // stage 2].
 //
-// CTA r of the cluster owns the 16-block groups [r per, (r + 1) per) and the
-// matching 64-kernel chunks (the kernels of blocks [16k, 16k + 16) are
-// 64k - 1 .. 64k + 63).
+// One CTA per SM (its shared memory keeps a second one off); the cluster
+// size C (1..16) is chosen at launch so that every group's cluster is
+// resident at once.  CTA r owns the 16-block groups [r per, (r + 1) per) and
+// the matching 64-kernel chunks (the kernels of blocks [16k, 16k + 16) are
+// 64k - 1 .. 64k + 63).  One 192 KB region of shared memory serves, in turn,
+// the phase-A ring and scores, the block scores and top-k scratch, and the
+// attention stages.
 //   compress  the CTA whose chunks hold the newest complete kernel recomputes
 //             it from the keys with the compression kernel's arithmetic,
 //             stores it in the kernel-mean planes and patches its own
 //             shared-memory copy of the chunk.
-//   phase A   hi/lo chunks streamed by TMA; z = score_scale q . Mean on the
-//             tensor cores; z stays in registers (4 values per thread and
-//             chunk), so nothing is written to global memory.
-//   LSE       per-warp maxima, exp2(z - max) in place, per-warp sums; CTA
-//             partials merged across the cluster through distributed shared
-//             memory -> exact lse per head.
+//   phase A   hi/lo chunks streamed by TMA through a 4-stage ring (the rest
+//             of the CTA's chunks head for L2 at once); z = score_scale
+//             q . Mean on the tensor cores (8 warps), kept in shared memory.
+//   LSE       per-warp maxima, exp2(z - max) in place, per-warp sums merged
+//             into the CTA's (max, sum) per head, which is pushed into every
+//             CTA of the cluster; after one cluster barrier each CTA merges
+//             the C partials itself -> exact lse per head.
 //   phase B   g = (1/16) sum_h exp2(z - lse_h) from the stored exponentials
 //             and one weight per (warp, head); block maxima of the CTA's
-//             blocks, pushed to the group's owner CTA.  The kernel 64k - 1
-//             shared with the previous CTA is merged in by the owner.
-//   top-k     the owner holds all block scores in registers, selects
-//             (bitmask top-k) and pushes the list to every CTA.
-//   attend    the selected blocks are dealt round-robin to three warp pairs
-//             per CTA; a pair TMA-loads one block's K and V tiles (32 KB) and
-//             each warp of the pair takes 32 of its keys: S = Q K^T on the
-//             tensor cores, online softmax in base 2, O += P V with P fed as
-//             bf16 hi + lo.
-//   merge     warps merge in shared memory, CTAs through distributed shared
-//             memory: CTA r writes heads [16 r / C, 16 (r + 1) / C).
+//             blocks, pushed into every CTA together with a summary (the
+//             g of the CTA's last kernel, which the next CTA's first block
+//             also meets; the count and best score of its candidates).  The
+//             CTA's likeliest blocks head for L2.  One cluster barrier.
+//   top-k     every CTA holds every block score and runs the same exact
+//             top-k (its first pass replaced by the summaries), so the
+//             selection needs no broadcast; CTA 0 writes it.
+//   attend    the selected blocks rank, rank + C, ... are dealt to six warp
+//             pairs; a pair TMA-loads one block's K and V tiles (32 KB) into
+//             its stage, and each warp of the pair takes 32 of its keys:
+//             S = Q K^T on the tensor cores, online softmax in base 2,
+//             O += P V with P fed as bf16 hi + lo.  Blocks of a second round
+//             head for L2 as soon as the selection is known.
+//   merge     warps merge in shared memory; each head's CTA partial is
+//             pushed to the CTA that writes the head (head h: CTA h mod C),
+//             which, after one cluster barrier, merges the C partials.
+// Every remote access is a store issued before a cluster barrier; after the
+// last barrier a CTA only reads its own shared memory, so it may exit.
 #include "compress.cuh"
 #include "select_common.cuh"
 
@@ -41,15 +53,34 @@ namespace infllmv2 {
 
 namespace {
 
-constexpr int kDsThreads = 256;
+constexpr int kDsThreads = 384;
+constexpr int kDsWarps = kDsThreads / 32;
+constexpr int kDsAWarps = 8;          // phase-A warps: one 8-kernel n-tile each per chunk
+constexpr int kDsProducer = 8;        // warp issuing the phase-A ring loads
 constexpr int kDsChunk = 64;          // kernels per phase-A stage
-constexpr int kDsStages = 2;          // phase-A stages
-constexpr int kDsMaxIt = 8;           // chunks per CTA (their z live in registers)
-constexpr int kDsPairs = 3;           // attention warp pairs, one 32 KB stage each
+constexpr int kDsRing = 4;            // phase-A stages
+constexpr int kDsPairs = kDsWarps / 2;   // attention warp pairs, one stage each
 constexpr int kDsStageBytes = 32768;  // 64 kernels hi + lo, or one block's K + V
-constexpr int kDsCtaOOff = 16384;     // CTA partial O: stage 0's V half
-constexpr int kDsZOff = 2 * 32768;    // phase-A scores: the stage slot phase A leaves free
-static_assert(kDsMaxIt * kGroup * kDsChunk * 4 <= 32768, "phase-A scores fit one stage slot");
+constexpr int kDsRegion = kDsPairs * kDsStageBytes;
+constexpr int kDsZOff = kDsRing * kDsStageBytes;   // phase-A scores after the ring
+constexpr int kDsMaxIt = (kDsRegion - kDsZOff) / (kGroup * kDsChunk * 4);   // chunks per CTA
+constexpr int kDsMaxC = 16;
+constexpr int kDsOutRows = 32;        // C * ceil(16 / C) <= 30 partial rows a CTA may receive
+constexpr int kDsMaxBlocks = 4096;    // block scores over the region's first 16 KB
+constexpr int kDsGbufOff = 65536;     // g of the CTA's kernels: in the ring, after the phase
+constexpr int kDsRmineOff = kDsGbufOff + kDsMaxIt * kDsChunk * 4;
+constexpr int kDsTkOff = kDsZOff;     // top-k scratch over the phase-A scores
+static_assert(kDsMaxIt >= 16, "16 chunks per CTA");
+static_assert(kDsRmineOff + 16 * kDsMaxIt * 4 <= kDsZOff, "phase-B buffers inside the ring");
+static_assert(kDsMaxBlocks * 4 <= kDsGbufOff, "block scores ahead of the phase-B buffers");
+
+// Pushed per CTA before the second barrier.
+struct DsSummary {
+  float tail;         // g of the CTA's last kernel (-inf if it has none)
+  uint32_t lead;      // best topk_lead over its candidate blocks (0 if none)
+  int n_cand;         // its candidate blocks (finite, not forced)
+  int pad;
+};
 
 struct DsParams {
   int B, Hkv, Lmax, ncmax, nbmax, kmax;
@@ -65,41 +96,49 @@ struct DsParams {
   uint32_t* status;
 };
 
+// Shared memory after the region (fixed sizes: the footprint, and with it
+// the cluster occupancy, does not depend on the shape).
 struct DsLayout {
-  int bits, surv, rfull, glall, q, wpart, cpart, lse, gbuf, wtab, sel, cta_ml, warp_ml, wgt, items, bar, total;
+  int q, lse_in, summ, o_in, ml_in, wpart, cpart, lse, wtab, sel, nsel, warp_ml, wgt, bar, total;
 };
 
-// The stage area (kDsPairs x 32 KB) holds, in turn: the phase-A chunks; in
-// the owner CTA the gathered block scores and the top-k scratch (other CTAs
-// write the scores there only after every CTA's phase A); the attention K/V
-// tiles; the per-warp O partials.
-__host__ __device__ inline DsLayout ds_layout(int nbmax, int kmax) {
-  DsLayout l;
-  l.bits = (static_cast<int>(sizeof(SmemTopkScratch<kDsThreads>)) + 15) & ~15;
-  l.surv = (l.bits + (nbmax + 31) / 32 * 4 + 15) & ~15;
-  l.rfull = l.surv + nbmax * 8;
-  l.glall = l.rfull + nbmax * 4;
-  l.q = kDsPairs * kDsStageBytes;
-  l.wpart = l.q + 4096;
-  l.cpart = l.wpart + 8 * kGroup * 8;
-  l.lse = l.cpart + kGroup * 8;
-  l.gbuf = l.lse + kGroup * 4;
-  l.wtab = l.gbuf + kDsMaxIt * kDsChunk * 4;
-  l.sel = l.wtab + 8 * kGroup * 4;
-  l.cta_ml = (l.sel + kmax * 4 + 15) & ~15;
-  l.warp_ml = l.cta_ml + kGroup * 8;
-  l.wgt = l.warp_ml + 2 * kDsPairs * kGroup * 8;
-  l.items = l.wgt + 2 * kDsPairs * kGroup * 4;   // item counter + two mailbox slots per pair
-  l.bar = (l.items + (1 + 2 * kDsPairs) * 4 + 15) & ~15;
-  l.total = l.bar + (2 * kDsStages + 1 + kDsPairs) * 8;
+__host__ __device__ constexpr DsLayout ds_layout() {
+  DsLayout l{};
+  l.q = kDsRegion;                                 // 16 rows x 256 B, two swizzled boxes
+  l.lse_in = l.q + 4096;                           // [16 CTAs][16 heads] (max, sum)
+  l.summ = l.lse_in + kDsMaxC * kGroup * 8;        // [16 CTAs] DsSummary
+  l.o_in = l.summ + kDsMaxC * 16;                  // [32 rows][128] partial O of the heads written here
+  l.ml_in = l.o_in + kDsOutRows * kHeadDim * 4;    // [32 rows] their (max, sum)
+  l.wpart = l.ml_in + kDsOutRows * 8;              // [8 warps][16 heads] (max, sum)
+  l.cpart = l.wpart + kDsAWarps * kGroup * 8;      // [16] CTA (max, sum)
+  l.lse = l.cpart + kGroup * 8;                    // [16] lse per head (base 2)
+  l.wtab = l.lse + kGroup * 4;                     // [8 warps][16 heads] exponential weights
+  l.sel = l.wtab + kDsAWarps * kGroup * 4;         // [kmax <= 256] ascending, -1 padded
+  l.nsel = l.sel + 256 * 4;
+  l.warp_ml = l.nsel + 16;                         // [12 warps][16 heads] attention (max, sum)
+  l.wgt = l.warp_ml + kDsWarps * kGroup * 8;       // [12 warps][16 heads] merge weights, then [16][16]
+  l.bar = l.wgt + 16 * 16 * 4;
+  l.total = l.bar + (2 * kDsRing + 1 + kDsPairs) * 8;
   return l;
 }
 
+constexpr int kDsSmem = ds_layout().total + 1024;   // + 1024-byte alignment slack
+static_assert(kDsSmem <= 227 * 1024, "one CTA per SM");
+
 __host__ __device__ inline int ds_per(int groups, int C) { return (groups + C - 1) / C; }
 
-// Barrier of the two warps of attention pair `pair` (ids 1..3; 0 is __syncthreads).
+// Likely winners a CTA prefetches into L2 before the selection is known.
+__host__ __device__ inline int ds_prefetch_count(int n_take, int C) { return (n_take + C - 1) / C + 2; }
+
+// Barrier of the two warps of attention pair `pair` (ids 1..6; 0 is __syncthreads).
 __device__ __forceinline__ void pair_sync(int pair) {
   asm volatile("bar.sync %0, 64;" ::"r"(pair + 1) : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
 }
 
 // K and V tiles of one block into L2 (no shared memory, no completion).
@@ -119,41 +158,40 @@ __device__ __forceinline__ void tma_block(uint8_t* stage, const CUtensorMap* kma
   tma_load_2d(stage + 24576, vmap, 64, row, bar);
 }
 
-template <int C>
-__global__ void __launch_bounds__(kDsThreads, 2)
+__global__ void __launch_bounds__(kDsThreads, 1)
     decode_step_kernel(const __grid_constant__ CUtensorMap kc_map, const __grid_constant__ CUtensorMap q_map,
                        const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
                        DsParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  const DsLayout lay = ds_layout(p.nbmax, p.kmax);
-  float2* wpart = reinterpret_cast<float2*>(smem + lay.wpart);   // [8 warps][16 heads]
-  float2* cpart = reinterpret_cast<float2*>(smem + lay.cpart);   // [16]
-  float* lse2 = reinterpret_cast<float*>(smem + lay.lse);        // [16]
-  float* gbuf = reinterpret_cast<float*>(smem + lay.gbuf);       // [kDsMaxIt * 64]
-  float* wtab = reinterpret_cast<float*>(smem + lay.wtab);       // [8 warps][16 heads] exponential weights
-  float* rfull = reinterpret_cast<float*>(smem + lay.rfull);     // owner: [nbmax] all block scores
-  float* glall = reinterpret_cast<float*>(smem + lay.glall);     // owner: [C] each CTA's last-kernel g
-  int* item_ctr = reinterpret_cast<int*>(smem + lay.items);      // next attention item of this CTA
-  int* pair_next = item_ctr + 1;                                 // [pairs][2] mailbox
-  int32_t* selS = reinterpret_cast<int32_t*>(smem + lay.sel);    // [kmax] ascending, -1 padded
-  float2* cta_ml = reinterpret_cast<float2*>(smem + lay.cta_ml);
+  constexpr DsLayout lay = ds_layout();
+  float* zs = reinterpret_cast<float*>(smem + kDsZOff);              // [it][16 heads][64]
+  float* rfull = reinterpret_cast<float*>(smem);                     // [nb] every block score
+  float* gbuf = reinterpret_cast<float*>(smem + kDsGbufOff);         // g of this CTA's kernels
+  float* rmine = reinterpret_cast<float*>(smem + kDsRmineOff);       // this CTA's block scores
+  float2* lse_in = reinterpret_cast<float2*>(smem + lay.lse_in);     // [C][16]
+  DsSummary* summ = reinterpret_cast<DsSummary*>(smem + lay.summ);   // [C]
+  float* o_in = reinterpret_cast<float*>(smem + lay.o_in);           // [C * hmax][128]
+  float2* ml_in = reinterpret_cast<float2*>(smem + lay.ml_in);       // [C * hmax]
+  float2* wpart = reinterpret_cast<float2*>(smem + lay.wpart);
+  float2* cpart = reinterpret_cast<float2*>(smem + lay.cpart);
+  float* lse2 = reinterpret_cast<float*>(smem + lay.lse);
+  float* wtab = reinterpret_cast<float*>(smem + lay.wtab);
+  int32_t* selS = reinterpret_cast<int32_t*>(smem + lay.sel);
+  int32_t* nselS = reinterpret_cast<int32_t*>(smem + lay.nsel);
   float2* warp_ml = reinterpret_cast<float2*>(smem + lay.warp_ml);
   float* wgt = reinterpret_cast<float*>(smem + lay.wgt);
-  float* cta_o = reinterpret_cast<float*>(smem + kDsCtaOOff);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.bar);
-  uint64_t* empty = full + kDsStages;
-  uint64_t* qbar = empty + kDsStages;
+  uint64_t* empty = full + kDsRing;
+  uint64_t* qbar = empty + kDsRing;
   uint64_t* kvfull = qbar + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, tq = lane & 3;
   const int rank = static_cast<int>(cluster_ctarank());
+  const int C = static_cast<int>(cluster_nctarank());
+  const int hmax = (kGroup + C - 1) / C;   // heads a CTA writes at most (head h: CTA h % C)
   const int bh = blockIdx.y;
-  // The CTA that gathers the block scores and selects; it differs between
-  // neighbouring groups so that two clusters sharing SMs do not stack their
-  // selections on one SM.
-  const int owner = bh % C;
   const int b = bh / p.Hkv, h = bh % p.Hkv;
   const int Hq = p.Hkv * kGroup;
   const size_t orow = static_cast<size_t>(b) * Hq + static_cast<size_t>(h) * kGroup;
@@ -163,15 +201,17 @@ __global__ void __launch_bounds__(kDsThreads, 2)
     prefetch_tensormap(&q_map);
     prefetch_tensormap(&k_map);
     prefetch_tensormap(&v_map);
-    for (int s = 0; s < kDsStages; ++s) {
+    for (int s = 0; s < kDsRing; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 8);
+      mbar_init(&empty[s], kDsAWarps);
     }
     mbar_init(qbar, 1);
     for (int s = 0; s < kDsPairs; ++s) mbar_init(&kvfull[s], 1);
     fence_barrier_init();
-    *item_ctr = kDsPairs;
   }
+  // Marks this CTA as running; the matching wait, before the first remote
+  // store, makes sure every CTA of the cluster is.
+  cluster_arrive_relaxed();
   __syncthreads();
   pdl_wait();
   pdl_trigger();
@@ -185,7 +225,7 @@ __global__ void __launch_bounds__(kDsThreads, 2)
   const int nbt = L >= 1 ? (L - 1) / kBlock + 1 : 0;
   const int groups = (nbt + 15) / 16;
   const int per = ds_per(groups, C);
-  if (L < 1 || L > p.Lmax || per > kDsMaxIt) {   // same for every CTA of the cluster
+  if (L < 1 || L > p.Lmax || per > kDsMaxIt || nbt > kDsMaxBlocks) {   // same for every CTA of the cluster
     if (rank == 0) {
       for (int e = tid; e < p.kmax; e += kDsThreads) p.block_idx[static_cast<size_t>(bh) * p.kmax + e] = -1;
       for (int e = tid; e < kGroup * kHeadDim; e += kDsThreads) p.out[orow * kHeadDim + e] = __float2bfloat16(0.f);
@@ -196,6 +236,7 @@ __global__ void __launch_bounds__(kDsThreads, 2)
       }
     }
     mbar_wait(qbar, 0, p.status);   // no copy may still be landing in this CTA's memory
+    cluster_wait();
     return;
   }
   const int i = L - 1, c = i / kBlock;
@@ -205,9 +246,13 @@ __global__ void __launch_bounds__(kDsThreads, 2)
   const int jn = nc - 1;   // newest complete kernel
   const int it_new = (jn >= 0 && jn / kDsChunk >= k0 && jn / kDsChunk < k0 + nmy) ? jn / kDsChunk - k0 : -1;
   const size_t plane_rows = static_cast<size_t>(p.ncmax) * kHeadDim;
+  const int n_first = min(p.n_init, c + 1);
+  const int local_lo = max(n_first, c - p.n_local + 1);
+  const int n_forced = n_first + max(0, c - local_lo + 1);
+  const int n_take = max(0, p.inc_forced ? p.topk - n_forced : p.topk);
 
   auto issue = [&](int it) {
-    const int st = it % kDsStages;
+    const int st = it % kDsRing;
     const int row = (k0 + it) * kDsChunk;
     uint8_t* dst = smem + st * kDsStageBytes;
     mbar_arrive_expect_tx(&full[st], kDsStageBytes);
@@ -217,37 +262,35 @@ __global__ void __launch_bounds__(kDsThreads, 2)
     tma_load_2d(dst + 24576, &kc_map, 64, (bh * 2 + 1) * p.ncmax + row, &full[st]);
   };
   const int kv_row0 = bh * p.Lmax;
-  if (rank == owner && warp == 2) {
-    // The forced blocks are known now: their K/V head for L2 at once.
-    const int n_first = min(p.n_init, c + 1);
-    const int lo = max(n_first, c - p.n_local + 1);
-    const int n_f = n_first + max(0, c - lo + 1);
-    for (int x = lane; x < n_f; x += 32)
-      prefetch_block(&k_map, &v_map, kv_row0 + (x < n_first ? x : lo + x - n_first) * kBlock);
+  if (warp == 9) {
+    // The forced blocks are known now: their K/V head for L2 at once, each
+    // from one CTA of the cluster.
+    for (int x = rank + C * lane; x < n_forced; x += 32 * C)
+      prefetch_block(&k_map, &v_map, kv_row0 + (x < n_first ? x : local_lo + x - n_first) * kBlock);
   }
-  if (it_new >= 0 && warp == 7) {
+  if (it_new >= 0 && warp == 11) {
     // The 32 keys of the newest kernel (8 KB): into L2 while Q and the first chunks load.
     const char* kr = reinterpret_cast<const char*>(p.k + (static_cast<size_t>(bh) * p.Lmax + jn * kStride) * kHeadDim);
     asm volatile("prefetch.global.L2 [%0];" ::"l"(kr + lane * 256));
     asm volatile("prefetch.global.L2 [%0];" ::"l"(kr + lane * 256 + 128));
   }
-  if (tid == 0)
-    for (int it = 0; it < min(kDsStages, nmy); ++it) issue(it);
-  if (warp == 1) {
+  if (warp == 10) {
     // The rest of this CTA's chunks go to L2 now (one box per lane), so HBM
-    // streams at full rate while the two shared-memory stages trail behind.
-    for (int x = lane; x < 4 * (nmy - kDsStages); x += 32) {
-      const int row = (k0 + kDsStages + (x >> 2)) * kDsChunk;
+    // streams at full rate while the shared-memory stages trail behind.
+    for (int x = lane; x < 4 * (nmy - kDsRing); x += 32) {
+      const int row = (k0 + kDsRing + (x >> 2)) * kDsChunk;
       tma_prefetch_2d(&kc_map, (x & 1) * 64, (bh * 2 + ((x >> 1) & 1)) * p.ncmax + row);
     }
   }
+  if (tid == kDsProducer * 32)
+    for (int it = 0; it < min(kDsRing, nmy); ++it) issue(it);
 
   // ------------------------------------------------------------ phase A --
   bool ok = __syncthreads_and(mbar_wait(qbar, 0, p.status));
-  // Newest kernel, by warp 7 while the other warps start on the chunks.
-  // Warp 7: lane = 16 * half + sub sums chunk jn + half over dims [8 sub, 8 sub + 8).
+  // Newest kernel, by warp 11 while warps 0-7 start on the chunks.
+  // Warp 11: lane = 16 * half + sub sums chunk jn + half over dims [8 sub, 8 sub + 8).
   uint4 new_hi = make_uint4(0, 0, 0, 0), new_lo = make_uint4(0, 0, 0, 0);
-  if (it_new >= 0 && warp == 7) {
+  if (it_new >= 0 && warp == 11) {
     const __nv_bfloat16* kbh = p.k + static_cast<size_t>(bh) * p.Lmax * kHeadDim;
     const int sub = lane & 15, half = lane >> 4;
     float acc[8], oth[8];
@@ -268,28 +311,20 @@ __global__ void __launch_bounds__(kDsThreads, 2)
 
   const uint32_t q_b = smem_u32(smem + lay.q);
   // z (then exp2(z - warp max)) of chunk it, head h, kernel x of the chunk:
-  // zs[(it * 16 + h) * 64 + x], in the stage slot phase A leaves free.
-  float* zs = reinterpret_cast<float*>(smem + kDsZOff);
+  // zs[(it * 16 + h) * 64 + x].
   float mx0 = -INFINITY, mx1 = -INFINITY;   // this warp's max of heads g and g + 8
-  {
+  if (warp < kDsAWarps) {
     uint32_t a[8][4];
     load_q_frags(a, q_b, lane);
 #pragma unroll 1
     for (int it = 0; it < nmy; ++it) {
-      const int st = it % kDsStages;
-      const uint32_t ph = static_cast<uint32_t>(it / kDsStages) & 1u;
+      const int st = it % kDsRing;
+      const uint32_t ph = static_cast<uint32_t>(it / kDsRing) & 1u;
       bool got = ok && mbar_wait(&full[st], ph, p.status);
       ok = __all_sync(0xffffffffu, got);
-      if (it == it_new) {   // the same iteration in every warp of the CTA
-        ok = __syncthreads_and(ok);
-        if (ok && warp == 7 && lane < 16) {
-          uint8_t* stg = smem + st * kDsStageBytes;
-          const uint32_t off = swz128_offset(jn - (k0 + it) * kDsChunk, lane, kDsChunk);
-          *reinterpret_cast<uint4*>(stg + off) = new_hi;
-          *reinterpret_cast<uint4*>(stg + 16384 + off) = new_lo;
-        }
-        __syncthreads();
-      }
+      // The chunk holding the newest kernel is read only after warp 11 has
+      // patched it (named barrier 7: warps 0-7 and 11).
+      if (it == it_new) asm volatile("bar.sync 7, %0;" ::"n"(kDsAWarps * 32 + 32) : "memory");
       float z0 = -INFINITY, z1 = -INFINITY, z2 = -INFINITY, z3 = -INFINITY;
       if (ok) {
         const uint32_t hi_b = smem_u32(smem + st * kDsStageBytes);
@@ -309,47 +344,72 @@ __global__ void __launch_bounds__(kDsThreads, 2)
       *reinterpret_cast<float2*>(zrow + 8 * kDsChunk) = make_float2(z2, z3);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
-      if (tid == 0 && ok && it + kDsStages < nmy) {
-        if (mbar_wait(&empty[st], ph, p.status)) issue(it + kDsStages);
-      }
-      __syncwarp();
     }
+  } else if (warp == kDsProducer) {
+    // Ring refills: chunk it + 4 into the stage chunk it leaves.
+    if (lane == 0) {
+#pragma unroll 1
+      for (int it = 0; it + kDsRing < nmy && ok; ++it) {
+        const int st = it % kDsRing;
+        if (!mbar_wait(&empty[st], static_cast<uint32_t>(it / kDsRing) & 1u, p.status)) {
+          ok = false;
+          break;
+        }
+        issue(it + kDsRing);
+      }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+  } else if (warp == 11 && it_new >= 0) {
+    // Patch the newest kernel into its chunk once the chunk has landed,
+    // before the phase-A warps read it (named barrier 7: warps 0-7 and 11).
+    const int st = it_new % kDsRing;
+    bool got = ok && mbar_wait(&full[st], static_cast<uint32_t>(it_new / kDsRing) & 1u, p.status);
+    got = __all_sync(0xffffffffu, got);
+    if (got && lane < 16) {
+      uint8_t* stg = smem + st * kDsStageBytes;
+      const uint32_t off = swz128_offset(jn - (k0 + it_new) * kDsChunk, lane, kDsChunk);
+      *reinterpret_cast<uint4*>(stg + off) = new_hi;
+      *reinterpret_cast<uint4*>(stg + 16384 + off) = new_lo;
+    }
+    asm volatile("bar.sync 7, %0;" ::"n"(kDsAWarps * 32 + 32) : "memory");
   }
 
   // --------------------------------------------------- LSE over the cluster --
   // Row g holds head g, row g + 8 head g + 8; the four tq lanes share a row.
   // Each thread turns its own z into exp2(z - warp max) in place.
+  if (warp < kDsAWarps) {
 #pragma unroll
-  for (int o = 1; o <= 2; o <<= 1) {
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-  }
-  float l0 = 0.f, l1 = 0.f;
+    for (int o = 1; o <= 2; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    float l0 = 0.f, l1 = 0.f;
 #pragma unroll 4
-  for (int it = 0; it < nmy; ++it) {
-    float2* z01 = reinterpret_cast<float2*>(zs + (it * kGroup + g) * kDsChunk + warp * 8 + 2 * tq);
-    float2* z23 = reinterpret_cast<float2*>(reinterpret_cast<float*>(z01) + 8 * kDsChunk);
-    float2 u = *z01, w = *z23;
-    u.x = (mx0 == -INFINITY) ? 0.f : fast_exp2(u.x - mx0);
-    u.y = (mx0 == -INFINITY) ? 0.f : fast_exp2(u.y - mx0);
-    w.x = (mx1 == -INFINITY) ? 0.f : fast_exp2(w.x - mx1);
-    w.y = (mx1 == -INFINITY) ? 0.f : fast_exp2(w.y - mx1);
-    *z01 = u;
-    *z23 = w;
-    l0 += u.x + u.y;
-    l1 += w.x + w.y;
-  }
+    for (int it = 0; it < nmy; ++it) {
+      float2* z01 = reinterpret_cast<float2*>(zs + (it * kGroup + g) * kDsChunk + warp * 8 + 2 * tq);
+      float2* z23 = reinterpret_cast<float2*>(reinterpret_cast<float*>(z01) + 8 * kDsChunk);
+      float2 u = *z01, w = *z23;
+      u.x = (mx0 == -INFINITY) ? 0.f : fast_exp2(u.x - mx0);
+      u.y = (mx0 == -INFINITY) ? 0.f : fast_exp2(u.y - mx0);
+      w.x = (mx1 == -INFINITY) ? 0.f : fast_exp2(w.x - mx1);
+      w.y = (mx1 == -INFINITY) ? 0.f : fast_exp2(w.y - mx1);
+      *z01 = u;
+      *z23 = w;
+      l0 += u.x + u.y;
+      l1 += w.x + w.y;
+    }
 #pragma unroll
-  for (int o = 1; o <= 2; o <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    for (int o = 1; o <= 2; o <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    }
+    if (tq == 0) {
+      wpart[warp * kGroup + g] = make_float2(mx0, l0);
+      wpart[warp * kGroup + g + 8] = make_float2(mx1, l1);
+    }
   }
-  if (tq == 0) {
-    wpart[warp * kGroup + g] = make_float2(mx0, l0);
-    wpart[warp * kGroup + g + 8] = make_float2(mx1, l1);
-  }
-  __syncthreads();
-  if (tid < 8 * kGroup) {   // head tid / 8, warp tid % 8: a shuffle tree over the 8 warps
+  ok = __syncthreads_and(ok);
+  if (tid < kDsAWarps * kGroup) {   // head tid / 8, warp tid % 8: a shuffle tree over the 8 warps
     const float2 v = wpart[(tid & 7) * kGroup + (tid >> 3)];
     float m = v.x, l = v.y;
 #pragma unroll
@@ -357,20 +417,26 @@ __global__ void __launch_bounds__(kDsThreads, 2)
       lse_merge(m, l, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, l, o));
     if ((tid & 7) == 0) cpart[tid >> 3] = make_float2(m, l);
   }
-  cluster_sync();
-  if (tid < C * kGroup) {   // head tid / C, CTA tid % C: one remote load each, then a shuffle tree
-    const float2 v = ld_dsmem_f32x2(dsmem_addr(&cpart[tid / C], tid % C));
+  __syncthreads();
+  cluster_wait();   // every CTA of the cluster is running
+  if (tid < C * kGroup)   // the CTA's partial of head tid % 16 into CTA tid / 16
+    st_dsmem_f32x2(dsmem_addr(&lse_in[rank * kGroup + (tid % kGroup)], tid / kGroup), cpart[tid % kGroup]);
+  cluster_arrive();
+  cluster_wait();
+  if (tid < kGroup * kDsMaxC) {   // head tid / 16, CTA tid % 16: a shuffle tree over the C partials
+    const int q = tid % kDsMaxC, hd = tid / kDsMaxC;
+    const float2 v = q < C ? lse_in[q * kGroup + hd] : make_float2(-INFINITY, 0.f);
     float m = v.x, l = v.y;
 #pragma unroll
-    for (int o = 1; o < C; o <<= 1)
+    for (int o = 1; o < kDsMaxC; o <<= 1)
       lse_merge(m, l, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, l, o));
-    if (tid % C == 0) lse2[tid / C] = (m == -INFINITY) ? -INFINITY : m + fast_log2(l);
+    if (q == 0) lse2[hd] = (m == -INFINITY) ? -INFINITY : m + fast_log2(l);
   }
   __syncthreads();
 
   // ------------------------------------------------------------ phase B --
   // Weight of warp w's exponentials of head h: exp2(max_wh - lse_h) / 16.
-  if (tq == 0) {
+  if (warp < kDsAWarps && tq == 0) {
     wtab[warp * kGroup + g] = (mx0 == -INFINITY) ? 0.f : fast_exp2(mx0 - lse2[g]) * (1.0f / kGroup);
     wtab[warp * kGroup + g + 8] = (mx1 == -INFINITY) ? 0.f : fast_exp2(mx1 - lse2[g + 8]) * (1.0f / kGroup);
   }
@@ -383,72 +449,152 @@ __global__ void __launch_bounds__(kDsThreads, 2)
     const float* wt = wtab + (x >> 3) * kGroup;
     float acc = 0.f;
 #pragma unroll
-    for (int h = 0; h < kGroup; ++h) acc += zc[h * kDsChunk] * wt[h];
+    for (int hh = 0; hh < kGroup; ++hh) acc += zc[hh * kDsChunk] * wt[hh];
     gbuf[k] = acc;
   }
   __syncthreads();
+  // The top-k scratch lies over the scores, which are dead now.
+  // (the general routine's scratch, for the rare fallback, overlays it too)
+  FastTopkScratch<kDsThreads>& tk = *reinterpret_cast<FastTopkScratch<kDsThreads>*>(smem + kDsTkOff);
+  SmemTopkScratch<kDsThreads>& tk_slow = *reinterpret_cast<SmemTopkScratch<kDsThreads>*>(smem + kDsTkOff);
+  constexpr int kTkBytes = sizeof(SmemTopkScratch<kDsThreads>) > sizeof(FastTopkScratch<kDsThreads>)
+                               ? sizeof(SmemTopkScratch<kDsThreads>) : sizeof(FastTopkScratch<kDsThreads>);
+  uint32_t* tk_bits = reinterpret_cast<uint32_t*>(smem + kDsTkOff + ((kTkBytes + 15) & ~15));
+  unsigned long long* tk_surv = reinterpret_cast<unsigned long long*>(smem + kDsTkOff + ((kTkBytes + 15) & ~15) + 512);
+  topk_fast_clear<kDsThreads>(tk, tk_bits, nbt, tid);
+  const int jb0 = 16 * k0, jb1 = min(16 * k1, nbt);
+  const int nv4 = (jb1 - jb0 + 3) / 4;   // the CTA's block scores as float4s (padded with -inf)
   {
-    const int jb0 = 16 * k0, jb1 = min(16 * k1, nbt);
     const int kb0 = kDsChunk * k0;
+    int my_cand = 0;
+    uint32_t my_lead = 0;
 #pragma unroll 1
-    for (int j = jb0 + tid; j < jb1; j += kDsThreads) {
-      const int a0 = max(4 * j - 1, kb0), e0 = min(nc - 1, 4 * j + 3);
+    for (int j = jb0 + tid; j < jb0 + 4 * nv4; j += kDsThreads) {
       float r = -INFINITY;
-      for (int k = a0; k <= e0; ++k) r = fmaxf(r, gbuf[k - kb0]);
-      st_dsmem_f32(dsmem_addr(rfull + j, owner), r);   // the owner gathers every block score
+      if (j < jb1) {
+        const int a0 = max(4 * j - 1, kb0), e0 = min(nc - 1, 4 * j + 3);
+        for (int k = a0; k <= e0; ++k) r = fmaxf(r, gbuf[k - kb0]);
+      }
+      rmine[j - jb0] = r;
+      if (j >= n_first && j < local_lo && r > -INFINITY) {
+        ++my_cand;
+        my_lead = max(my_lead, topk_lead(r));
+      }
     }
-    if (tid == 0) {
-      const float gl = (k1 > k0 && kDsChunk * k1 - 1 < nc) ? gbuf[kDsChunk * (k1 - k0) - 1] : -INFINITY;
-      st_dsmem_f32(dsmem_addr(glall + rank, owner), gl);
+    my_cand = __reduce_add_sync(0xffffffffu, my_cand);
+    my_lead = __reduce_max_sync(0xffffffffu, my_lead);
+    if (lane == 0) {
+      warp_ml[warp] = make_float2(__int_as_float(my_cand), __uint_as_float(my_lead));
     }
   }
-  cluster_sync();
+  __syncthreads();
+  // Push the block scores and the summary into every CTA.
+#pragma unroll 1
+  for (int e = tid; e < C * nv4; e += kDsThreads) {
+    const int dst = e / nv4, x = e % nv4;
+    st_dsmem_f32x4(dsmem_addr(rfull + jb0 + 4 * x, dst), reinterpret_cast<const float4*>(rmine)[x]);
+  }
+  if (tid < C) {
+    int cnt = 0;
+    uint32_t lead = 0;
+    for (int w = 0; w < kDsWarps; ++w) {
+      cnt += __float_as_int(warp_ml[w].x);
+      lead = max(lead, __float_as_uint(warp_ml[w].y));
+    }
+    const float gl = (k1 > k0 && kDsChunk * k1 - 1 < nc) ? gbuf[kDsChunk * (k1 - k0) - 1] : -INFINITY;
+    st_dsmem_f32x4(dsmem_addr(&summ[rank], tid),
+                   make_float4(gl, __uint_as_float(lead), __int_as_float(cnt), 0.f));
+  }
+  if (warp == 9) {
+    // The CTA's likeliest winners head for L2 while the selection is made:
+    // its best few candidate blocks by score.
+    const int n_pf = min(ds_prefetch_count(n_take, C), jb1 - jb0);
+    uint32_t key[4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const int j = jb0 + lane + 32 * x;
+      const bool cand = j < jb1 && j >= n_first && j < local_lo && rmine[lane + 32 * x] > -INFINITY;
+      key[x] = cand ? ((topk_lead(rmine[lane + 32 * x]) << 12) | static_cast<uint32_t>(4095 - (lane + 32 * x))) : 0u;
+    }
+    // (a CTA owns at most 16 kDsMaxIt blocks; those past 128 are not prefetched)
+#pragma unroll 1
+    for (int n = 0; n < n_pf; ++n) {
+      uint32_t best = max(max(key[0], key[1]), max(key[2], key[3]));
+      best = __reduce_max_sync(0xffffffffu, best);
+      if (best == 0u) break;
+      const int x = 4095 - static_cast<int>(best & 4095u);
+      if (lane == 0) prefetch_block(&k_map, &v_map, kv_row0 + (jb0 + x) * kBlock);
+#pragma unroll
+      for (int y = 0; y < 4; ++y)
+        if (key[y] == best) key[y] = 0u;
+    }
+  }
+  cluster_arrive();
+  cluster_wait();
 
   // ------------------------------------------------------------- top-k --
-  if (rank == owner) {
-    // Block 16 per q starts CTA q's range; its kernel 64 per q - 1 was scored by CTA q - 1.
-    if (tid > 0 && tid < C && 16 * per * tid < nbt)
-      rfull[16 * per * tid] = fmaxf(rfull[16 * per * tid], glall[tid - 1]);
-    __syncthreads();
-    SmemTopkScratch<kDsThreads>& tk = *reinterpret_cast<SmemTopkScratch<kDsThreads>*>(smem);
-    select_topk_smem<kDsThreads>(rfull, nbt, p.n_init, p.n_local, p.topk, p.inc_forced != 0, p.kmax,
-                                 p.block_idx + static_cast<size_t>(bh) * p.kmax, p.n_sel + bh, tk,
-                                 reinterpret_cast<uint32_t*>(smem + lay.bits),
-                                 reinterpret_cast<unsigned long long*>(smem + lay.surv), tid, selS);
-    __syncthreads();
-    // Every CTA gets the list in its own shared memory.
-#pragma unroll 1
-    for (int e = tid; e < C * p.kmax; e += kDsThreads) {
-      const int q = e / p.kmax, x = e % p.kmax;
-      if (q != owner) st_dsmem_u32(dsmem_addr(selS + x, q), static_cast<uint32_t>(selS[x]));
+  // Block 16 per q starts CTA q's range; its kernel 64 per q - 1 was scored
+  // by CTA q - 1.  The candidate count and the best leading bits follow.
+  if (warp == 0) {   // lane q < C: CTA q's summary and the block its tail meets
+    int n_cand = 0;
+    uint32_t lead = 0;
+    if (lane < C) {
+      const DsSummary sq = summ[lane];
+      n_cand = sq.n_cand;
+      lead = sq.lead;
+      const int j = 16 * per * (lane + 1);
+      if (lane + 1 < C && j < nbt && sq.tail > -INFINITY) {
+        const float before = rfull[j];
+        const float after = fmaxf(before, sq.tail);
+        rfull[j] = after;
+        if (j >= n_first && j < local_lo) {
+          n_cand += (before == -INFINITY) ? 1 : 0;
+          lead = max(lead, topk_lead(after));
+        }
+      }
+    }
+    n_cand = __reduce_add_sync(0xffffffffu, n_cand);
+    lead = __reduce_max_sync(0xffffffffu, lead);
+    if (lane == 0) {
+      nselS[1] = n_cand;
+      nselS[2] = static_cast<int>(lead);
     }
   }
-  cluster_sync();
+  __syncthreads();
+  select_topk_fast<kDsThreads>(rfull, nbt, p.n_init, p.n_local, p.topk, p.inc_forced != 0, p.kmax, selS, nselS, tk,
+                               tk_bits, tk_surv, tid, nselS[1], static_cast<uint32_t>(nselS[2]), tk_slow);
+  __syncthreads();
+  const int nsel = nselS[0];
+  if (rank == 0) {
+    for (int e = tid; e < p.kmax; e += kDsThreads) p.block_idx[static_cast<size_t>(bh) * p.kmax + e] = selS[e];
+    if (tid == 0) p.n_sel[bh] = nsel;
+  }
+  if (tid == 32)   // blocks of the second and later rounds: into L2 now
+    for (int n = rank + C * kDsPairs; n < nsel; n += C) prefetch_block(&k_map, &v_map, kv_row0 + selS[n] * kBlock);
 
   // ------------------------------------------------------------ attend --
   const int pair = warp >> 1, half = warp & 1;
-  if (pair < kDsPairs) {
+  float l0 = 0.f, l1 = 0.f;
+  {
     uint8_t* stage = smem + pair * kDsStageBytes;
     const uint32_t k_b = smem_u32(stage), v_b = k_b + 16384;
     const int rbase = 32 * half;
-    // Item x of this CTA is list entry rank + C x: items 0..2 go to pairs
-    // 0..2, each later one to whichever pair frees its stage first.
+    // Item x of this CTA is list entry rank + C x; pair `pair` takes items
+    // pair, pair + 6, ...
     auto block_of = [&](int item) {
       const int n = rank + C * item;
-      const int j = n < p.kmax ? selS[n] : -1;
+      const int j = n < nsel ? selS[n] : -1;
       return j > c ? -1 : j;
     };
-    int j = block_of(pair);
-    if (half == 0 && lane == 0 && j >= 0) tma_block(stage, &k_map, &v_map, kv_row0 + j * kBlock, &kvfull[pair]);
+    int item = pair;
+    int j = block_of(item);
+    if (half == 0 && lane == 0 && j >= 0 && ok) tma_block(stage, &k_map, &v_map, kv_row0 + j * kBlock, &kvfull[pair]);
 
     float o[16][4];
 #pragma unroll
     for (int x = 0; x < 16; ++x) o[x][0] = o[x][1] = o[x][2] = o[x][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY;
-    l0 = 0.f;
-    l1 = 0.f;
     uint32_t phase = 0;
-    int iter = 0;
 #pragma unroll 1
     while (j >= 0) {
       bool got = ok && mbar_wait(&kvfull[pair], phase, p.status);
@@ -547,15 +693,12 @@ __global__ void __launch_bounds__(kDsThreads, 2)
           }
         }
       }
-      // Next item of this pair: drawn by the even warp, shared through a
-      // two-slot mailbox (a slot is rewritten only two pair barriers later).
-      if (half == 0 && lane == 0) pair_next[pair * 2 + (iter & 1)] = atomicAdd(item_ctr, 1);
       // Both warps are done with the stage; order the zeroed V rows
       // (generic writes) before the TMA refill (async proxy).
       fence_proxy_async_smem();
       pair_sync(pair);
-      j = block_of(pair_next[pair * 2 + (iter & 1)]);
-      ++iter;
+      item += kDsPairs;
+      j = block_of(item);
       if (j >= 0 && half == 0 && lane == 0 && ok)
         tma_block(stage, &k_map, &v_map, kv_row0 + j * kBlock, &kvfull[pair]);
     }
@@ -577,77 +720,85 @@ __global__ void __launch_bounds__(kDsThreads, 2)
     }
   }
   __syncthreads();
-  constexpr int kAw = 2 * kDsPairs;   // warps holding attention partials
-  if (tid < kGroup) {
-    float M = -INFINITY;
+  if (tid < kGroup * 16) {   // head tid / 16, warp tid % 16 (< 12): shuffle trees over the warps
+    const int w = tid % 16, hd = tid / 16;
+    const float2 v = w < kDsWarps ? warp_ml[w * kGroup + hd] : make_float2(-INFINITY, 0.f);
+    float M = v.x;
 #pragma unroll
-    for (int w = 0; w < kAw; ++w) M = fmaxf(M, warp_ml[w * kGroup + tid].x);
-    float lsum = 0.f;
+    for (int o = 1; o < 16; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float wt = (M == -INFINITY) ? 0.f : fast_exp2(v.x - M);
+    if (w < kDsWarps) wgt[w * kGroup + hd] = wt;
+    float lsum = wt * v.y;
 #pragma unroll
-    for (int w = 0; w < kAw; ++w) {
-      const float2 v = warp_ml[w * kGroup + tid];
-      const float wt = (M == -INFINITY) ? 0.f : fast_exp2(v.x - M);
-      wgt[w * kGroup + tid] = wt;
-      lsum += wt * v.y;
-    }
-    cta_ml[tid] = make_float2(M, lsum);
+    for (int o = 1; o < 16; o <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+    // This CTA's (max, sum) of head hd into the CTA that writes the head.
+    if (w == 0) st_dsmem_f32x2(dsmem_addr(&ml_in[rank * hmax + hd / C], hd % C), make_float2(M, lsum));
   }
   __syncthreads();
-  for (int e = tid; e < kGroup * kHeadDim; e += kDsThreads) {
-    const int hd = e >> 7;
-    float acc = 0.f;
-#pragma unroll
-    for (int w = 0; w < kAw; ++w)
-      acc += wgt[w * kGroup + hd] *
-             reinterpret_cast<const float*>(smem + (w >> 1) * kDsStageBytes + (w & 1) * 8192)[e];
-    cta_o[e] = acc;
-  }
-  cluster_sync();
-
-  // Heads [hpc * rank, hpc * (rank + 1)) of the output from all partials.
-  constexpr int hpc = kGroup / C;
+  // This CTA's partial O of each head into the CTA that writes the head:
+  // 4 dims per item, merged over the warps on the way.
 #pragma unroll 1
-  for (int e = tid; e < hpc * kHeadDim; e += kDsThreads) {
-    const int hd = rank * hpc + e / kHeadDim;
-    const int d = e % kHeadDim;
-    float2 ml[C];
-    float ov[C];
+  for (int e = tid; e < kGroup * (kHeadDim / 4); e += kDsThreads) {
+    const int hd = e / (kHeadDim / 4), d4 = 4 * (e % (kHeadDim / 4));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int q = 0; q < C; ++q) {
-      ml[q] = ld_dsmem_f32x2(dsmem_addr(&cta_ml[hd], q));
-      ov[q] = ld_dsmem_f32(dsmem_addr(&cta_o[hd * kHeadDim + d], q));
+    for (int w = 0; w < kDsWarps; ++w) {
+      const float wt = wgt[w * kGroup + hd];
+      const float4 v = *reinterpret_cast<const float4*>(smem + (w >> 1) * kDsStageBytes + (w & 1) * 8192 +
+                                                          (hd * kHeadDim + d4) * 4);
+      acc.x += wt * v.x;
+      acc.y += wt * v.y;
+      acc.z += wt * v.z;
+      acc.w += wt * v.w;
     }
-    float M = -INFINITY;
+    st_dsmem_f32x4(dsmem_addr(o_in + (rank * hmax + hd / C) * kHeadDim + d4, hd % C), acc);
+  }
+  cluster_arrive();
+  cluster_wait();
+
+  // Heads rank, rank + C, ... of the output from the C partials: first the
+  // weight of each (head, source) and each head's sum (16 lanes per head),
+  // then the dims.
+  float* mw = wgt;   // [hmax][16] source weights / sum, reusing the warp-merge weights
+  if (warp < (hmax * 16 + 31) / 32) {   // whole warps: lanes past hmax * 16 carry neutral values
+    const int q = tid % 16, hl = tid / 16;
+    const float2 ml = (q < C && hl < hmax) ? ml_in[q * hmax + hl] : make_float2(-INFINITY, 0.f);
+    float M = ml.x;
 #pragma unroll
-    for (int q = 0; q < C; ++q) M = fmaxf(M, ml[q].x);
-    float lsum = 0.f, acc = 0.f;
+    for (int o = 1; o < 16; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float wt = (M == -INFINITY) ? 0.f : fast_exp2(ml.x - M);
+    float lsum = wt * ml.y;
 #pragma unroll
-    for (int q = 0; q < C; ++q) {
-      const float wt = (M == -INFINITY) ? 0.f : fast_exp2(ml[q].x - M);
-      lsum += wt * ml[q].y;
-      acc += wt * ov[q];
-    }
-    p.out[(orow + hd) * kHeadDim + d] = __float2bfloat16(lsum > 0.f ? acc / lsum : 0.f);
-    if (d == 0 && p.lse)
+    for (int o = 1; o < 16; o <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+    const int hd = rank + C * hl;
+    if (hl < hmax) mw[hl * 16 + q] = lsum > 0.f ? wt / lsum : 0.f;
+    if (q == 0 && hl < hmax && hd < kGroup && p.lse)
       p.lse[orow + hd] = lsum > 0.f ? (M + fast_log2(lsum)) * 0.69314718055994531f : -INFINITY;
   }
-  cluster_sync();   // keeps this CTA's shared memory alive for remote readers
+  __syncthreads();
+#pragma unroll 1
+  for (int e = tid; e < hmax * kHeadDim; e += kDsThreads) {
+    const int hl = e / kHeadDim, d = e % kHeadDim;
+    const int hd = rank + C * hl;
+    if (hd >= kGroup) continue;
+    float acc = 0.f;
+#pragma unroll 4
+    for (int q = 0; q < C; ++q) acc += mw[hl * 16 + q] * o_in[(q * hmax + hl) * kHeadDim + d];
+    p.out[(orow + hd) * kHeadDim + d] = __float2bfloat16(acc);
+  }
 }
 
-template <int C>
-bool ds_fits(const Shape& s) {
+bool ds_fits(const Shape& s, int C) {
   const int groups = (s.nbmax + 15) / 16;
-  const DsLayout l = ds_layout(s.nbmax, s.kmax);
-  return s.nq == 1 && ds_per(groups, C) <= kDsMaxIt &&
-         l.glall + 16 * 4 <= kDsZOff && l.total + 1024 <= 113 * 1024;
+  return s.nq == 1 && C >= 1 && C <= kDsMaxC && ds_per(groups, C) <= kDsMaxIt && s.nbmax <= kDsMaxBlocks &&
+         s.kmax <= 256;
 }
 
-template <int C>
-void ds_config(const Shape& s, cudaLaunchConfig_t* cfg, cudaLaunchAttribute (&attrs)[2], cudaStream_t st) {
+void ds_config(const Shape& s, int C, cudaLaunchConfig_t* cfg, cudaLaunchAttribute (&attrs)[2], cudaStream_t st) {
   *cfg = cudaLaunchConfig_t{};
   cfg->gridDim = dim3(C, s.B * s.Hkv, 1);
   cfg->blockDim = dim3(kDsThreads, 1, 1);
-  cfg->dynamicSmemBytes = ds_layout(s.nbmax, s.kmax).total + 1024;
+  cfg->dynamicSmemBytes = kDsSmem;
   cfg->stream = st;
   attrs[0].id = cudaLaunchAttributeClusterDimension;
   attrs[0].val.clusterDim.x = C;
@@ -659,39 +810,73 @@ void ds_config(const Shape& s, cudaLaunchConfig_t* cfg, cudaLaunchAttribute (&at
   cfg->numAttrs = 2;
 }
 
-// True when the C-CTA form fits this shape and, for C = 16, every group's
-// cluster can be resident at once (the only case in which it pays off).
-template <int C>
-bool ds_ready(const Shape& s) {
-  if (!ds_fits<C>(s)) return false;
-  cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attrs[2];
-  ds_config<C>(s, &cfg, attrs, nullptr);
-  if (cudaFuncSetAttribute(decode_step_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(cfg.dynamicSmemBytes)) != cudaSuccess)
-    return cudaGetLastError(), false;
-  if (C > 8 && cudaFuncSetAttribute(decode_step_kernel<C>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-                   cudaSuccess)
-    return cudaGetLastError(), false;
-  cfg.numAttrs = 1;
-  int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, decode_step_kernel<C>, &cfg) != cudaSuccess)
-    return cudaGetLastError(), false;
-  return clusters >= ((C > 8) ? s.B * s.Hkv : 1);
+// Clusters of C CTAs that can be resident at once on the current device
+// (0 if the configuration cannot launch), cached per device.
+int ds_active_clusters(int C) {
+  static int cache[64][kDsMaxC + 1];
+  static bool done[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!done[dev]) {
+    bool ok = cudaFuncSetAttribute(decode_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDsSmem) ==
+                  cudaSuccess &&
+              cudaFuncSetAttribute(decode_step_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                  cudaSuccess;
+    for (int c = 1; c <= kDsMaxC; ++c) {
+      int n = 0;
+      if (ok) {
+        Shape s{};
+        s.B = 1;
+        s.Hkv = 1;
+        cudaLaunchConfig_t cfg;
+        cudaLaunchAttribute attrs[2];
+        ds_config(s, c, &cfg, attrs, nullptr);
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, decode_step_kernel, &cfg) != cudaSuccess) n = 0;
+      }
+      cache[dev][c] = n;
+    }
+    cudaGetLastError();
+    done[dev] = true;
+  }
+  return cache[dev][C];
 }
 
 }  // namespace
 
+// The cluster size for this shape: every group's cluster resident at once
+// (a second wave would double the step), then the fewest load rounds and
+// the most CTAs per group (more SMs streaming the kernel means).  0 when no
+// size fits.
 int decode_step_cluster_size(const Shape& s) {
-  if (s.B * s.Hkv * 16 <= 2 * device_sm_count() && ds_ready<16>(s)) return 16;
-  if (ds_ready<8>(s)) return 8;
-  return 0;
+  const int G = s.B * s.Hkv;
+  int best = 0;
+  double best_cost = 0.0;
+  for (int C = kDsMaxC; C >= 1; --C) {
+    if (!ds_fits(s, C)) continue;
+    const int active = ds_active_clusters(C);
+    if (active < 1) continue;
+    const int waves = (G + active - 1) / active;
+    const int rounds = (s.kmax + C * kDsPairs - 1) / (C * kDsPairs);
+    // Per CTA: its share of the kernel means (4 B per element) and of the
+    // selected blocks (32 KB each), streamed at ~50 GB/s per SM, plus ~2 us
+    // per attention round and ~8 us of fixed latency.
+    const double bytes = (static_cast<double>(s.ncmax) * kHeadDim * 4 + static_cast<double>(s.kmax) * 32768) / C;
+    const double cost = waves * (8.0 + 2.0 * rounds + bytes / 50e3);
+    if (!best || cost < best_cost - 1e-9) {
+      best = C;
+      best_cost = cost;
+    }
+  }
+  return best;
 }
 
 cudaError_t launch_decode_step(const Shape& s, int cluster, const CUtensorMap& kc_map, const CUtensorMap& q_map,
                                const CUtensorMap& k_map, const CUtensorMap& v_map, const void* k,
                                const int32_t* kv_lens, void* kc, int32_t* block_idx, int32_t* n_sel, void* out,
                                float* lse, uint32_t* status, cudaStream_t st) {
+  if (cluster < 1 || cluster > kDsMaxC || !ds_fits(s, cluster) || ds_active_clusters(cluster) < 1)
+    return cudaErrorInvalidConfiguration;
   DsParams p{};
   p.B = s.B;
   p.Hkv = s.Hkv;
@@ -715,15 +900,8 @@ cudaError_t launch_decode_step(const Shape& s, int cluster, const CUtensorMap& k
   p.status = status;
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attrs[2];
-  if (cluster == 16) {
-    ds_config<16>(s, &cfg, attrs, st);
-    return cudaLaunchKernelEx(&cfg, decode_step_kernel<16>, kc_map, q_map, k_map, v_map, p);
-  }
-  if (cluster == 8) {
-    ds_config<8>(s, &cfg, attrs, st);
-    return cudaLaunchKernelEx(&cfg, decode_step_kernel<8>, kc_map, q_map, k_map, v_map, p);
-  }
-  return cudaErrorInvalidConfiguration;
+  ds_config(s, cluster, &cfg, attrs, st);
+  return cudaLaunchKernelEx(&cfg, decode_step_kernel, kc_map, q_map, k_map, v_map, p);
 }
 
 }  // namespace infllmv2
