@@ -80,6 +80,7 @@ extern "C" {
 /* Device status bits (infllmv2_get_device_status). */
 #define INFLLMV2_DEVICE_BAD_KV_LEN   0x1u  /* kv_lens[b] < n_q or > max_kv_len */
 #define INFLLMV2_DEVICE_TIMEOUT      0x2u  /* a bounded mbarrier wait expired */
+#define INFLLMV2_DEVICE_BOUNDS       0x4u  /* checked build only: a caller-given index out of range */
 
 /* Workspace kinds for infllmv2_workspace_size. */
 #define INFLLMV2_OP_SELECT  1
@@ -301,6 +302,29 @@ int infllmv2_sparse_attn_backward(const infllmv2_params* p, const void* q, int32
                                   const int32_t* n_selected, const void* out, const float* lse, const void* dout,
                                   float* dq, float* dk, float* dv, void* workspace, size_t workspace_bytes,
                                   void* stream);
+
+/*
+ * The checked build.  The library can also be built with INFLLMV2_CHECKED
+ * (libinfllmv2_checked.so), in place of a memory checker.  It verifies
+ * every index that comes from the caller before use (each counted
+ * block_idx entry within [0, floor(i/m)], each n_selected within
+ * [0, k_max]) and the start of every K/V tile formed from one; a violation
+ * sets INFLLMV2_DEVICE_BOUNDS and the access is skipped (the product build
+ * skips the same accesses without reporting them).  Its bounded waits give
+ * up after 2^16 polls instead of 2^22.
+ *
+ * infllmv2_is_checked_build: 1 in the checked build, 0 otherwise.
+ *
+ * infllmv2_test_hooks: fault injection for the library's own tests, checked
+ * build only (the product build returns INFLLMV2_UNSUPPORTED and changes
+ * nothing).  flags = 1: in every later infllmv2_decode_step of the
+ * single-launch form, one warp per CTA withholds the release of its first
+ * ring stage, so a bounded wait expires: the call still returns, sets
+ * INFLLMV2_DEVICE_TIMEOUT and leaves no copy in flight.  flags = 0 turns it
+ * off.  Process-wide; not for concurrent use with other calls.
+ */
+int infllmv2_is_checked_build(void);
+int infllmv2_test_hooks(uint32_t flags);
 
 /* Human-readable name of an INFLLMV2_* return code. */
 const char* infllmv2_status_string(int status);

@@ -28,14 +28,14 @@ import torch
 
 from . import _lib
 from ._lib import (InfLLMv2Error, OP_BACKWARD, OP_DECODE, OP_DECODE_STEP, OP_PREFILL, OP_SELECT,  # noqa: F401
-                   Params, DEVICE_BAD_KV_LEN, DEVICE_TIMEOUT)
+                   Params, DEVICE_BAD_KV_LEN, DEVICE_BOUNDS, DEVICE_TIMEOUT)
 
 __all__ = [
     "Params", "InfLLMv2Error", "make_params", "num_kernels", "max_selected", "workspace_size",
     "alloc_kc", "alloc_workspace", "compress_keys", "select_blocks", "sparse_attn_decode",
     "sparse_attn_prefill", "decode_step", "coarse_means", "alloc_kcc", "select_blocks_coarse_lse",
     "sparse_attn_backward", "append_kv", "get_device_status", "OP_SELECT", "OP_DECODE", "OP_PREFILL",
-    "OP_DECODE_STEP", "OP_BACKWARD", "DECODE_MAX_NQ",
+    "OP_DECODE_STEP", "OP_BACKWARD", "DECODE_MAX_NQ", "is_checked_build", "test_hooks",
 ]
 
 DECODE_MAX_NQ = 16
@@ -218,6 +218,16 @@ def sparse_attn_backward(p: Params, q, k_cache, v_cache, kv_lens, block_idx, n_s
         _ptr(n_selected), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
         ws_bytes, _stream(stream)))
     return dq, dk, dv
+
+
+def is_checked_build() -> bool:
+    """True when the loaded library is the checked build (INFLLMV2_CHECKED)."""
+    return bool(_lib.lib.infllmv2_is_checked_build())
+
+
+def test_hooks(flags: int) -> None:
+    """Fault injection of the checked build's tests (infllmv2_test_hooks)."""
+    _lib.check(_lib.lib.infllmv2_test_hooks(flags))
 
 
 def get_device_status(clear: bool = True) -> int:

@@ -12,7 +12,10 @@ import ctypes
 import os
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libinfllmv2.so")
+# INFLLMV2_LIBRARY=checked loads the checked build (libinfllmv2_checked.so,
+# build_lib.build(checked=True)) instead of the product library.
+LIB_PATH = os.path.join(_PKG, "libinfllmv2_checked.so" if os.environ.get("INFLLMV2_LIBRARY") == "checked"
+                        else "libinfllmv2.so")
 
 OK = 0
 INVALID_ARGUMENT = 1
@@ -21,6 +24,7 @@ WORKSPACE_TOO_SMALL = 3
 CUDA_ERROR = 4
 DEVICE_BAD_KV_LEN = 0x1
 DEVICE_TIMEOUT = 0x2
+DEVICE_BOUNDS = 0x4
 OP_SELECT = 1
 OP_DECODE = 2
 OP_PREFILL = 3
@@ -86,6 +90,10 @@ for _name in ("infllmv2_sparse_attn_decode", "infllmv2_sparse_attn_prefill"):
     getattr(lib, _name).argtypes = [_P, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                     ctypes.c_size_t, _vp]
     getattr(lib, _name).restype = ctypes.c_int
+lib.infllmv2_is_checked_build.argtypes = []
+lib.infllmv2_is_checked_build.restype = ctypes.c_int
+lib.infllmv2_test_hooks.argtypes = [ctypes.c_uint32]
+lib.infllmv2_test_hooks.restype = ctypes.c_int
 lib.infllmv2_coarse_means.argtypes = [_P, _vp, _vp, _i32, _vp, _vp]
 lib.infllmv2_coarse_means.restype = ctypes.c_int
 lib.infllmv2_select_blocks_coarse_lse.argtypes = [_P, _vp, _i32, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp]

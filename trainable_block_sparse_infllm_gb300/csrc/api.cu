@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <atomic>
 #include <mutex>
 #include <string>
 
@@ -58,6 +59,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 constexpr int kMaxDevices = 64;
+
+// Fault-injection flags of the checked build's tests (infllmv2_test_hooks).
+std::atomic<uint32_t> g_test_flags{0};
 
 uint32_t* status_ptr() {
   static uint32_t* ptrs[kMaxDevices] = {};
@@ -486,7 +490,7 @@ int infllmv2_decode_step(const infllmv2_params* p, const void* q, int32_t n_q, c
     cudaError_t e;
     if (cluster) {
       e = launch_decode_step(s, cluster, kcm, qm, km, vm, k_cache, kv_lens, kc, block_idx, n_selected, out, lse,
-                             status, st);
+                             status, g_test_flags.load(), st);
       if (e != cudaSuccess) return cuda_fail(e, "decode_step");
       return INFLLMV2_OK;
     }
@@ -559,6 +563,26 @@ const char* infllmv2_status_string(int status) {
 }
 
 const char* infllmv2_last_error(void) { return g_last_error.c_str(); }
+
+int infllmv2_test_hooks(uint32_t flags) {
+  INFLLMV2_GUARD({
+#ifdef INFLLMV2_CHECKED
+    g_test_flags.store(flags);
+    return INFLLMV2_OK;
+#else
+    (void)flags;
+    return fail(INFLLMV2_UNSUPPORTED, "test hooks exist only in the checked build (INFLLMV2_CHECKED)");
+#endif
+  });
+}
+
+int infllmv2_is_checked_build(void) {
+#ifdef INFLLMV2_CHECKED
+  return 1;
+#else
+  return 0;
+#endif
+}
 
 int infllmv2_get_device_status(uint32_t* status_out, int clear) {
   INFLLMV2_GUARD({

@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2)
   const int32_t* sel = p.block_idx + u * p.kmax;
   const size_t kv_row0 = static_cast<size_t>(bh) * p.Lmax;
   constexpr int kStride = C * kAttnWarps;   // warps in the cluster
+  if (split == 0 && warp == 0) check_selection_row(sel, p.n_sel[u], p.kmax, c, p.status, lane);
   const int first = split * kAttnWarps + warp;
 
   if (tid == 0) {
@@ -118,7 +119,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2)
   // Start this warp's first block load before waiting for Q.
   int n = first;
   while (n < ns && (sel[n] < 0 || sel[n] > c)) n += kStride;
-  if (lane == 0 && n < ns) tma_kv(stage, &k_map, &v_map, static_cast<int>(kv_row0 + static_cast<size_t>(sel[n]) * kBlock), kvbar);
+  if (lane == 0 && n < ns && kv_row_ok(kv_row0 + static_cast<size_t>(sel[n]) * kBlock, kv_row0, p.Lmax, p.status))
+    tma_kv(stage, &k_map, &v_map, static_cast<int>(kv_row0 + static_cast<size_t>(sel[n]) * kBlock), kvbar);
 
   bool ok = __all_sync(0xffffffffu, mbar_wait(qbar, 0, p.status));
   uint32_t qa[8][4];
@@ -234,7 +236,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2)
       // async-proxy (TMA) writes that refill it.
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) tma_kv(stage, &k_map, &v_map, static_cast<int>(kv_row0 + static_cast<size_t>(sel[n]) * kBlock), kvbar);
+      if (lane == 0 && kv_row_ok(kv_row0 + static_cast<size_t>(sel[n]) * kBlock, kv_row0, p.Lmax, p.status))
+        tma_kv(stage, &k_map, &v_map, static_cast<int>(kv_row0 + static_cast<size_t>(sel[n]) * kBlock), kvbar);
     }
   }
   __syncwarp();

@@ -232,12 +232,14 @@ __global__ void __launch_bounds__(kBqWarps * 32, 1)
   const int c = i / kBlock;
   const int ns = min(p.n_sel[u], p.kmax);
   const int32_t* sel = p.block_idx + u * p.kmax;
+  check_selection_row(sel, p.n_sel[u], p.kmax, c, p.status, lane);
   uint8_t* ring = smem + warp * kBqStages * kBqStageBytes;
   uint64_t* full = bars + warp * kBqStages;
   const size_t kv_row0 = static_cast<size_t>(bh) * p.Lmax;
 
   auto issue = [&](int pos, int st) {
     const int row = static_cast<int>(kv_row0 + static_cast<size_t>(sel[pos >> 2]) * kBlock + (pos & 3) * kBqRows);
+    if (!kv_row_ok(kv_row0 + static_cast<size_t>(sel[pos >> 2]) * kBlock, kv_row0, p.Lmax, p.status)) return;
     uint8_t* dst = ring + st * kBqStageBytes;
     mbar_arrive_expect_tx(&full[st], kBqStageBytes);
     tma_load_2d(dst, &k_map16, 0, row, &full[st]);
@@ -479,7 +481,8 @@ __global__ void __launch_bounds__(kBkThreads, 1)
 
   if (warp == kBkTmaWarp) {
     // ----------------------------------------------------------- producer
-    if (lane == 0) {
+    if (lane == 0 && kv_row_ok(static_cast<size_t>(bh) * p.Lmax + static_cast<size_t>(j) * kBlock,
+                               static_cast<size_t>(bh) * p.Lmax, p.Lmax, p.status)) {
       const int row = bh * p.Lmax + j * kBlock;
       mbar_arrive_expect_tx(&bars[kBKv], 32768);
       tma_load_2d(smem + kOffKV, &k_map, 0, row, &bars[kBKv]);

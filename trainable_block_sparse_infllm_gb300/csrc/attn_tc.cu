@@ -235,6 +235,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const size_t u = static_cast<size_t>(bh) * p.nq + t0 + tok;
       const int ns = min(p.n_sel[u], p.kmax);
       const int i_tok = L - p.nq + t0 + tok;
+      check_selection_row(p.block_idx + u * p.kmax, p.n_sel[u], p.kmax, i_tok / kBlock, p.status, lane);
       for (int k = lane; k < ns; k += 32) {
         const int j = p.block_idx[u * p.kmax + k];
         if (j >= 0 && j <= i_tok / kBlock) {
@@ -335,6 +336,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_arrive_expect_tx(&bars[kKFull + st], kTcItemBytes);
         for (int hf = 0; hf < 2; ++hf) {
           const int row = bh * p.Lmax + item_block(it, hf) * kBlock;
+          if (!kv_row_ok(row, static_cast<size_t>(bh) * p.Lmax, p.Lmax, p.status)) continue;
           tma_load_2d(dst + hf * 8192, &k_map, 0, row, &bars[kKFull + st]);
           tma_load_2d(dst + 16384 + hf * 8192, &k_map, 64, row, &bars[kKFull + st]);
         }
@@ -351,6 +353,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_arrive_expect_tx(&bars[kVFull + st], kTcItemBytes);
         for (int hf = 0; hf < 2; ++hf) {
           const int row = bh * p.Lmax + item_block(it, hf) * kBlock;
+          if (!kv_row_ok(row, static_cast<size_t>(bh) * p.Lmax, p.Lmax, p.status)) continue;
           tma_load_2d(dst + hf * 8192, &v_map, 0, row, &bars[kVFull + st]);
           tma_load_2d(dst + 16384 + hf * 8192, &v_map, 64, row, &bars[kVFull + st]);
         }

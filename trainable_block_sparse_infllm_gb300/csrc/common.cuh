@@ -19,10 +19,54 @@ constexpr int kStride = 16;    // s, semantic kernel stride
 
 constexpr uint32_t kStatusBadKvLen = 0x1u;
 constexpr uint32_t kStatusTimeout = 0x2u;
+constexpr uint32_t kStatusBounds = 0x4u;
 
 // Bounded spin on an mbarrier: ~2^22 polls, each of which may suspend the
 // thread for a hardware-chosen time, is far above any legitimate wait here.
+// The checked build (INFLLMV2_CHECKED), which its tests drive into expired
+// waits on purpose, gives up after 2^16 polls, still far above any
+// legitimate wait of its small test cases.
+#ifdef INFLLMV2_CHECKED
+constexpr uint32_t kSpinLimit = 1u << 16;
+#else
 constexpr uint32_t kSpinLimit = 1u << 22;
+#endif
+
+// `ok`, and in the checked build a false `ok` also records
+// INFLLMV2_DEVICE_BOUNDS: every index that comes from the caller (a
+// block_idx entry, a selection count) and every K/V tile row built from one
+// passes through here before use.  The product build skips the same
+// accesses silently.
+__device__ __forceinline__ bool bounds_ok(bool ok, uint32_t* status) {
+#ifdef INFLLMV2_CHECKED
+  if (!ok) atomicOr(status, kStatusBounds);
+#else
+  (void)status;
+#endif
+  return ok;
+}
+
+// One warp: the checked build verifies a caller-given selection row (its
+// count within [0, kmax], every counted entry within [0, c]); the product
+// build compiles this to nothing and skips bad entries where they are read.
+__device__ __forceinline__ void check_selection_row(const int32_t* row, int n_sel, int kmax, int c,
+                                                    uint32_t* status, int lane) {
+#ifdef INFLLMV2_CHECKED
+  bool ok = n_sel >= 0 && n_sel <= kmax;
+  const int n = min(max(n_sel, 0), kmax);
+  for (int k = lane; k < n; k += 32) ok = ok && row[k] >= 0 && row[k] <= c;
+  if (!__all_sync(0xffffffffu, ok) && lane == 0) atomicOr(status, kStatusBounds);
+#else
+  (void)row; (void)n_sel; (void)kmax; (void)c; (void)status; (void)lane;
+#endif
+}
+
+// A K/V tile starting at `row` starts inside its (b, h) plane [plane0,
+// plane0 + Lmax).  (The tile of a cache's last, partial block runs past the
+// plane; its rows beyond kv_len are masked.)
+__device__ __forceinline__ bool kv_row_ok(size_t row, size_t plane0, int Lmax, uint32_t* status) {
+  return bounds_ok(row >= plane0 && row < plane0 + static_cast<size_t>(Lmax), status);
+}
 
 __host__ __device__ __forceinline__ int n_complete_kernels(int L) {
   return L >= kKernel ? (L - kKernel) / kStride + 1 : 0;

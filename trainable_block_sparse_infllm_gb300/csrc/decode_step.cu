@@ -94,7 +94,15 @@ struct DsParams {
   __nv_bfloat16* out;
   float* lse;
   uint32_t* status;
+  uint32_t test_flags;   // checked build: kTestWithholdArrive makes a bounded wait expire
 };
+
+// Fault injection of the checked build's own tests: warp 0 of every CTA
+// does not release the ring stage of its first chunk, so the producer's
+// bounded wait for that stage expires (TIMEOUT), no later chunk is issued,
+// and the phase-A warps' waits for those chunks expire too; every copy that
+// was issued has landed before the CTA moves on.
+constexpr uint32_t kTestWithholdArrive = 0x1u;
 
 // Shared memory after the region (fixed sizes: the footprint, and with it
 // the cluster occupancy, does not depend on the shape).
@@ -343,6 +351,9 @@ __global__ void __launch_bounds__(kDsThreads, 1)
       *reinterpret_cast<float2*>(zrow) = make_float2(z0, z1);
       *reinterpret_cast<float2*>(zrow + 8 * kDsChunk) = make_float2(z2, z3);
       __syncwarp();
+#ifdef INFLLMV2_CHECKED
+      if ((p.test_flags & kTestWithholdArrive) && warp == 0 && it == 0) continue;
+#endif
       if (lane == 0) mbar_arrive(&empty[st]);
     }
   } else if (warp == kDsProducer) {
@@ -588,7 +599,9 @@ __global__ void __launch_bounds__(kDsThreads, 1)
     };
     int item = pair;
     int j = block_of(item);
-    if (half == 0 && lane == 0 && j >= 0 && ok) tma_block(stage, &k_map, &v_map, kv_row0 + j * kBlock, &kvfull[pair]);
+    if (half == 0 && lane == 0 && j >= 0 && ok &&
+        kv_row_ok(static_cast<size_t>(kv_row0) + static_cast<size_t>(j) * kBlock, kv_row0, p.Lmax, p.status))
+      tma_block(stage, &k_map, &v_map, kv_row0 + j * kBlock, &kvfull[pair]);
 
     float o[16][4];
 #pragma unroll
@@ -699,7 +712,8 @@ __global__ void __launch_bounds__(kDsThreads, 1)
       pair_sync(pair);
       item += kDsPairs;
       j = block_of(item);
-      if (j >= 0 && half == 0 && lane == 0 && ok)
+      if (j >= 0 && half == 0 && lane == 0 && ok &&
+          kv_row_ok(static_cast<size_t>(kv_row0) + static_cast<size_t>(j) * kBlock, kv_row0, p.Lmax, p.status))
         tma_block(stage, &k_map, &v_map, kv_row0 + j * kBlock, &kvfull[pair]);
     }
 #pragma unroll
@@ -874,7 +888,7 @@ int decode_step_cluster_size(const Shape& s) {
 cudaError_t launch_decode_step(const Shape& s, int cluster, const CUtensorMap& kc_map, const CUtensorMap& q_map,
                                const CUtensorMap& k_map, const CUtensorMap& v_map, const void* k,
                                const int32_t* kv_lens, void* kc, int32_t* block_idx, int32_t* n_sel, void* out,
-                               float* lse, uint32_t* status, cudaStream_t st) {
+                               float* lse, uint32_t* status, uint32_t test_flags, cudaStream_t st) {
   if (cluster < 1 || cluster > kDsMaxC || !ds_fits(s, cluster) || ds_active_clusters(cluster) < 1)
     return cudaErrorInvalidConfiguration;
   DsParams p{};
@@ -898,6 +912,7 @@ cudaError_t launch_decode_step(const Shape& s, int cluster, const CUtensorMap& k
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
   p.status = status;
+  p.test_flags = test_flags;
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attrs[2];
   ds_config(s, cluster, &cfg, attrs, st);

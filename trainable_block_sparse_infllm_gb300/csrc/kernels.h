@@ -69,7 +69,7 @@ int decode_step_cluster_size(const Shape& s);
 cudaError_t launch_decode_step(const Shape& s, int cluster, const CUtensorMap& kc_map, const CUtensorMap& q_map,
                                const CUtensorMap& k_map, const CUtensorMap& v_map, const void* k,
                                const int32_t* kv_lens, void* kc, int32_t* block_idx, int32_t* n_sel, void* out,
-                               float* lse, uint32_t* status, cudaStream_t st);
+                               float* lse, uint32_t* status, uint32_t test_flags, cudaStream_t st);
 
 // ---- backward of stage 3 (fixed selection) --------------------------------
 size_t attn_bwd_workspace_bytes(const Shape& s);
