@@ -638,7 +638,8 @@ def profile_passes(path, n):
     """n passes of one path on a single input copy, nothing timed: the decode
     path is one decode_step launch per pass (decode_128k, 0.57 GB of inputs);
     the prefill path is compress + select + attention (prefill_32k); the
-    backward path is one forward, then n backward calls (prefill_32k)."""
+    backward path is one forward, then n backward calls (prefill_32k).  The
+    *8k variants run the prefill workload cut to 8192 tokens."""
     import torch
     import __graft_entry__
     __graft_entry__.build()
@@ -646,6 +647,11 @@ def profile_passes(path, n):
     dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
     wl = S.WORKLOADS[DECODE if path == "decode" else PREFILL]
+    if path.endswith("8k"):
+        # The prefill workload cut to an 8192-token causal prefill (inputs of
+        # ~150 MB, above L2): a case small enough for full ncu captures.
+        wl = wl.scaled(kv_len=8192, n_q=8192)
+        path = path[:-2]
     inp = S.make_inputs(wl)
     p = T.make_params(wl.batch, wl.n_kv_heads, wl.kv_len, wl.topk, wl.topk_includes_forced)
 
@@ -702,7 +708,7 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-workloads", action="store_true", help="headline workload and prefill only")
-    ap.add_argument("--profile", choices=["decode", "prefill", "backward"],
+    ap.add_argument("--profile", choices=["decode", "prefill", "backward", "prefill8k", "backward8k"],
                     help="run warmup + steps untimed passes of one path on one input copy and exit "
                          "(a small, fixed launch sequence for ncu)")
     args = ap.parse_args()
