@@ -568,3 +568,32 @@ def test_append_kv_from_pinned_host_memory_with_queries(dev):
     assert torch.equal(run.k.view(torch.int16), full_k.view(torch.int16))
     assert torch.equal(run.v.view(torch.int16), full_v.view(torch.int16))
     assert torch.equal(run.q.view(torch.int16), q_ref.view(torch.int16))
+
+
+def test_decode_step_256k_capacity(dev):
+    # A 262,144-token cache (4096 blocks) with two KV heads, one of them
+    # filled to 261,500 tokens: the fused step stays one launch (16-CTA
+    # clusters, 16 kernel-mean chunks per CTA) and matches the oracle, and
+    # the three separate stages agree with it.
+    import torch
+    cap = 262_144
+    inp = S.make_random(batch=2, n_kv_heads=1, kv_len=cap, n_q=1, topk=64, seed=91, kv_lens=[cap, 261_500])
+    st = _settings(inp.wl)
+    run = DeviceRun(inp, dev)
+    assert run.T.workspace_size(run.p, 1, run.T.OP_DECODE_STEP) == 0   # the single-launch form
+    full = run.blank_step_kernels()
+    run.step()
+    torch.cuda.synchronize()
+    assert torch.equal(run.kc.view(torch.int16), full.view(torch.int16))
+    sels = O.run_selection(inp, st)
+    check_selections(run, sels, check_scores=False)
+    got = run.gpu_blocks(sels.keys())
+    refs = O.run_attention(inp, st, got)
+    mx, mean = check_attention(run, refs, strict=True, strict_units=strict_units(inp, got))
+    out_step = run.out.float().clone()
+    run.select(with_scores=False)
+    run.attend()
+    torch.cuda.synchronize()
+    check_selections(run, sels, check_scores=False)
+    assert (run.out.float() - out_step).abs().max().item() <= 2e-3
+    print(f"256K capacity: fused step max|dO|={mx:.2e} mean={mean:.2e}")

@@ -11,9 +11,12 @@
 // with P recomputed from the forward's log-sum-exp (P = exp(s - lse)).
 //
 // Three pieces:
-//   * An inverse index: for each (b, h_kv, block j) the query tokens whose
-//     selection holds j (count, scan, fill), cut into work items of at most
-//     kBkChunk tokens.
+//   * An inverse index: for each (b, h_kv, range of kBkRange query tokens,
+//     block j) the tokens of the range whose selection holds j (count, scan,
+//     fill), cut into work items of at most kBkChunk tokens.  Items come out
+//     ordered by token range, so the CTAs resident at one time share one
+//     range's q and dO rows in L2 rather than gathering rows from the whole
+//     sequence.
 //   * bwd_dq_kernel, query-centric on the warp-level tensor cores: one warp
 //     per (b, h_kv, t) unit (its 16 heads are the 16 MMA rows, [InfLLM v2 >
 //     Query group sharing]) walks the unit's selected blocks in 16-key quarters
@@ -38,10 +41,11 @@ namespace infllmv2 {
 namespace {
 
 constexpr int kBkChunk = 256;    // tokens per dK/dV work item
+constexpr int kBkRange = 2048;   // query tokens per range of the inverse index (a multiple of kIdxTokens)
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct BwdParams {
-  int B, Hkv, Lmax, nq, kmax, nbmax, nl;
+  int B, Hkv, Lmax, nq, kmax, nbmax, nr, nl;   // nr: token ranges per (b, h_kv); nl = B Hkv nr nbmax
   float scale;    // attn_scale
   float scale2;   // attn_scale * log2(e)
   const int32_t* kv_lens;
@@ -55,7 +59,7 @@ struct BwdParams {
   float* dk;
   float* dv;
   float* dsum;      // D, [B, nq, Hq]
-  int32_t* cnt;     // [nl] tokens per (b, h, j) list
+  int32_t* cnt;     // [nl] tokens per (b, h, range, j) list
   int32_t* off;     // [nl + 1] first entry of each list
   int32_t* choff;   // [nl + 1] first work item of each list
   int32_t* cursor;  // [nl] fill position
@@ -70,6 +74,7 @@ struct BwdParams {
 // of one (b, h_kv), flushed with one global atomic per block; `fill` = true
 // reserves a range per block and writes the token indices.
 constexpr int kIdxTokens = 64;
+static_assert(kBkRange % kIdxTokens == 0, "an index CTA's tokens share one range");
 constexpr int kIdxThreads = 256;
 
 template <bool kFill>
@@ -80,7 +85,7 @@ __global__ void __launch_bounds__(kIdxThreads) bwd_index_kernel(BwdParams p, boo
   const int n_tok = min(kIdxTokens, p.nq - t0);
   const int L = p.kv_lens[b];
   if (L < p.nq || L > p.Lmax) return;   // such units attend nothing
-  const int32_t l0 = bh * p.nbmax;
+  const int32_t l0 = (bh * p.nr + t0 / kBkRange) * p.nbmax;
   const int c_last = (L - p.nq + t0 + n_tok - 1) / kBlock;
   if (smem_hist) {
     for (int j = threadIdx.x; j <= c_last; j += kIdxThreads) hist[j] = 0;
@@ -443,7 +448,7 @@ __global__ void __launch_bounds__(kBkThreads, 1)
   const int l = p.items[item];
   const int e0 = p.off[l] + (item - p.choff[l]) * kBkChunk;
   const int ntok = min(kBkChunk, p.off[l + 1] - e0);
-  const int bh = l / p.nbmax, j = l % p.nbmax;
+  const int bh = l / (p.nr * p.nbmax), j = l % p.nbmax;
   const int b = bh / p.Hkv, h = bh % p.Hkv;
   const int Hq = p.Hkv * kGroup;
   const int L = p.kv_lens[b];
@@ -716,7 +721,7 @@ struct BwdWs {
 
 BwdWs bwd_ws_layout(const Shape& s) {
   BwdWs w{};
-  const long long nl = static_cast<long long>(s.B) * s.Hkv * s.nbmax;
+  const long long nl = static_cast<long long>(s.B) * s.Hkv * ((s.nq + kBkRange - 1) / kBkRange) * s.nbmax;
   const long long entries = static_cast<long long>(s.B) * s.Hkv * s.nq * s.kmax;
   w.max_items = entries / kBkChunk + nl + 1;
   size_t o = 0;
@@ -743,7 +748,7 @@ BwdWs bwd_ws_layout(const Shape& s) {
 size_t attn_bwd_workspace_bytes(const Shape& s) { return bwd_ws_layout(s).total; }
 
 bool attn_bwd_supported(const Shape& s) {
-  const long long nl = static_cast<long long>(s.B) * s.Hkv * s.nbmax;
+  const long long nl = static_cast<long long>(s.B) * s.Hkv * ((s.nq + kBkRange - 1) / kBkRange) * s.nbmax;
   const long long entries = static_cast<long long>(s.B) * s.Hkv * s.nq * s.kmax;
   return nl < (1LL << 30) && entries < (1LL << 31) - 1 && bwd_ws_layout(s).max_items < (1LL << 31) - 1;
 }
@@ -763,7 +768,8 @@ cudaError_t launch_attn_bwd(const Shape& s, const CUtensorMap& q_map, const CUte
   p.nq = s.nq;
   p.kmax = s.kmax;
   p.nbmax = s.nbmax;
-  p.nl = s.B * s.Hkv * s.nbmax;
+  p.nr = (s.nq + kBkRange - 1) / kBkRange;
+  p.nl = s.B * s.Hkv * p.nr * s.nbmax;
   p.scale = s.attn_scale;
   p.scale2 = s.attn_scale2;
   p.kv_lens = kv_lens;
