@@ -345,7 +345,7 @@ def decode_workload_line(name, dev, steps, warmup, peaks, warm_l2=False, bench=N
     ws = bench.working_set_bytes()
     achieved = ab["step"] / t / 1e9
     # The single-launch form of the step is the one that needs no workspace.
-    launches = 1 if bench.T.workspace_size(bench.p, wl.n_q, bench.T.OP_DECODE_STEP) == 0 else 3
+    launches = 1 if wl.n_q == 1 and bench.T.workspace_size(bench.p, wl.n_q, bench.T.OP_DECODE_STEP) == 0 else 3
     line = {
         "workload": WORKLOAD_TEXT[name],
         "tokens_per_s": wl.batch * wl.n_q / t,

@@ -333,7 +333,12 @@ const char* infllmv2_status_string(int status);
 const char* infllmv2_last_error(void);
 
 /* Read (and if `clear` is nonzero, reset) the device status word of the
- * current device.  Synchronises the device; not for the hot path. */
+ * current device.  Synchronises the device; not for the hot path.
+ * The library looks up the device addresses of its status word and of the
+ * built-in selection scratch once per device and keeps them: it assumes the
+ * device's primary context (the one the CUDA runtime uses) for the life of
+ * the process, and does not support a cudaDeviceReset or a separately
+ * created driver context on that device after its first call there. */
 int infllmv2_get_device_status(uint32_t* status_out, int clear);
 
 #ifdef __cplusplus

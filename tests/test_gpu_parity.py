@@ -529,11 +529,13 @@ def test_select_long_capacity(dev, sc):
     check_selections(run, O.run_selection(inp, st))
 
 
-def test_decode_step_output_to_pinned_host_memory(dev):
-    # The fused step stores its output with ordinary stores, so a pinned host
-    # buffer receives the same bytes as device memory.
+@pytest.mark.parametrize("nq", [1, 3])
+def test_decode_step_output_to_pinned_host_memory(dev, nq):
+    # The step stores its output with ordinary stores, so a pinned host buffer
+    # receives the same bytes as device memory: the single launch (n_q = 1)
+    # and the three stages in order (n_q = 3).
     import torch
-    inp = S.make_random(batch=2, n_kv_heads=2, kv_len=3000, n_q=1, topk=16, seed=44, kv_lens=[3000, 2500])
+    inp = S.make_random(batch=2, n_kv_heads=2, kv_len=3000, n_q=nq, topk=16, seed=44, kv_lens=[3000, 2500])
     run = DeviceRun(inp, dev)
     run.blank_step_kernels()
     run.step()

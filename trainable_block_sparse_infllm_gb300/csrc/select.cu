@@ -39,17 +39,27 @@ bool select_decode_supported(const Shape& s);
 cudaError_t launch_select_decode(const Shape& s, const CUtensorMap& kc_map, const CUtensorMap& q_map,
                                  const SelParams& p, cudaStream_t st);
 
+int select_verify_cluster_size(const Shape& s);
+cudaError_t launch_select_verify(const Shape& s, int cluster, const CUtensorMap& kc_map, const CUtensorMap& q_map,
+                                 const int32_t* kv_lens, int32_t* block_idx, int32_t* n_sel, float* r_buf,
+                                 uint32_t* status, cudaStream_t st);
+
 namespace {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 bool use_decode_path(const Shape& s) { return s.nq <= kSelDecodeMaxNq && select_decode_supported(s); }
 
+// 2 to 8 tokens per sequence (speculative verification): the two-pass
+// cluster kernel, when its clusters fit the device; no workspace.
+bool use_verify_path(const Shape& s) { return s.nq >= 2 && s.nq <= 8 && select_verify_cluster_size(s) > 0; }
+
 }  // namespace
 
 bool select_supported(const Shape& s) { return use_decode_path(s) || select_tc_supported(s); }
 
 size_t select_workspace_bytes(const Shape& s) {
+  if (use_verify_path(s)) return 0;
   if (use_decode_path(s)) {
     const size_t units = static_cast<size_t>(s.B) * s.Hkv * s.nq;
     return align256(units * kGroup * select_decode_ncpad(s) * sizeof(float));
@@ -82,6 +92,9 @@ cudaError_t launch_select(const Shape& s, const CUtensorMap& kc_map, const CUten
   p.write_r = block_scores != nullptr;
   p.r_buf = block_scores;
 
+  if (use_verify_path(s))
+    return launch_select_verify(s, select_verify_cluster_size(s), kc_map, q_map, kv_lens, block_idx, n_sel,
+                                block_scores, status, st);
   if (use_decode_path(s)) {
     p.ncpad = static_cast<int>(select_decode_ncpad(s));
     p.z = static_cast<float*>(ws);
