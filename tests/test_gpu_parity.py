@@ -94,6 +94,11 @@ SELECT_CASES = [
     (1, 1, 700, [700], 700, 4, True, None),             # whole sequence from position 0
     (3, 1, 300, [300, 40, 20], 20, 4, True, 1.0),       # tiny contexts, no visible kernel
     (2, 1, 200, [64, 33], 1, 3, True, None),
+    # Few tiles on long caches: each tile's chunks split over a cluster of up
+    # to 16 CTAs; the short sequence leaves most of its cluster without chunks.
+    (2, 2, 40000, [40000, 9000], 5, 32, True, None),
+    (1, 2, 30000, [30000], 12, 64, False, None),        # a partial second tile
+    (1, 1, 20000, [20000], 40, 16, False, None),        # prefill-path n_q
 ]
 
 
@@ -137,6 +142,10 @@ ATTN_CASES = [
     (2, 1, 2000, [2000, 1234], 130, 8, False, True),
     (1, 1, 700, [700], 700, 4, True, True),
     (3, 1, 300, [300, 40, 20], 20, 4, True, True),
+    # Few tiles on long caches: each tile's union split over a cluster of up
+    # to 16 CTAs (a partial last tile, ragged lengths).
+    (1, 2, 9000, [9000], 8, 64, True, True),
+    (2, 2, 20000, [20000, 7000], 13, 48, False, True),
 ]
 
 

@@ -313,17 +313,6 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 2)
   cluster_sync();
 }
 
-int device_sm_count() {
-  static int cache[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (!cache[dev]) {
-    int n = 0;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cache[dev] = n > 0 ? n : 148;
-  }
-  return cache[dev];
-}
 
 template <int C>
 cudaError_t launch_cluster(const Shape& s, const CUtensorMap& q_map, const CUtensorMap& k_map,

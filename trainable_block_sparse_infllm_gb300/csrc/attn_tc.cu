@@ -36,6 +36,16 @@
 // TMEM: columns [0,256) two S buffers, [256,384) the O accumulator,
 // [384,512) two P buffers.
 //
+// Few tiles (speculative verification: n_q <= 16 drafts per sequence, or a
+// short chunk) would leave most SMs idle, so each tile's union is then split
+// over a cluster of C CTAs: CTA r walks items [r n / C, (r + 1) n / C) and
+// ends with a partial row state (running max m, sum l, unnormalised O in
+// TMEM).  After a cluster barrier (every CTA past its last item, its K ring
+// free) each CTA pushes row r's partial into CTA r mod C's K ring through
+// distributed shared memory; after a second barrier the owner merges
+// (M = max m, weights 2^(m - M)) and writes the row.  A block several drafts
+// select is thus read once per tile instead of once per draft.
+//
 // P enters P V as bf16.  One bf16 carries 8 significant bits, and where a
 // row averages only a few values the rounding of its probabilities reaches
 // the output at 2^-9 |V|.  A tile in which some token attends fewer than
@@ -65,9 +75,18 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
 constexpr float kLazyRescale = 8.0f;
 constexpr int kSplitKeys = 2048;   // tiles with a row attending fewer keys feed P as hi + lo
+constexpr int kTcMaxSmem = 227 * 1024;
+// Cluster merge: C partial rows of ceil(128 / C) rows (O and (m, l)) land in
+// the K ring.
+__host__ __device__ constexpr int tc_merge_bytes(int C) { return C * ((128 + C - 1) / C) * (512 + 8); }
+__host__ __device__ constexpr bool tc_merge_fits(int C) {
+  return C > 16 || (tc_merge_bytes(C) <= kTcKStages * kTcItemBytes && tc_merge_fits(C + 1));
+}
+static_assert(tc_merge_fits(2), "cluster partials fit in the K ring");
 
 struct TcParams {
   int B, Hkv, Lmax, nq, kmax, nbmax;
+  int csize;   // CTAs per tile: 1, or a cluster that splits the union's items
   float scale2;
   const int32_t* kv_lens;
   const int32_t* block_idx;
@@ -204,11 +223,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int h = blockIdx.y, b = blockIdx.z;
   const int bh = b * p.Hkv + h;
   const int Hq = p.Hkv * kGroup;
-  const int t0 = blockIdx.x * kTcTokens;
+  const int csize = p.csize;
+  const int rank = static_cast<int>(blockIdx.x) % csize;   // == the rank in the cluster
+  const int t0 = (static_cast<int>(blockIdx.x) / csize) * kTcTokens;
   const int n_act = min(kTcTokens, p.nq - t0);
   const int L = p.kv_lens[b];
 
-  if (L < p.nq || L > p.Lmax) {
+  if (L < p.nq || L > p.Lmax) {   // the same in every CTA of a cluster: none touches another's memory
+    if (rank != 0) return;
     for (int e = tid; e < n_act * kGroup * kHeadDim; e += kTcThreads) {
       const int tok = e / (kGroup * kHeadDim), rem = e % (kGroup * kHeadDim);
       p.out[((static_cast<size_t>(b) * p.nq + t0 + tok) * Hq + h * kGroup) * kHeadDim + rem] = __float2bfloat16(0.f);
@@ -248,8 +270,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) kcnt[tok] = keys;
   }
   __syncthreads();
-  // Hi + lo probabilities when some token of the tile attends few keys.
-  bool split = false;
+  // Hi + lo probabilities when some token of the tile attends few keys, and
+  // always in a cluster (each CTA then sums only a share of a row's keys).
+  bool split = csize > 1;
 #pragma unroll
   for (int tok = 0; tok < kTcTokens; ++tok) split |= (tok < n_act) && (kcnt[tok] < kSplitKeys);
   {
@@ -308,14 +331,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  const int nu = scan[15];
-  const int nit = (nu + 1) / 2;   // items of two union blocks (the last may hold one)
+  // Items of two union blocks (the last may hold one); in a cluster CTA
+  // `rank` takes items [it0, it1) of the tile's nit_all.
+  const int nu_all = scan[15];
+  const int nit_all = (nu_all + 1) / 2;
+  const int it0 = rank * nit_all / csize, it1 = (rank + 1) * nit_all / csize;
+  const int ubase = 2 * it0;
+  const int nu = max(0, min(nu_all, 2 * it1) - ubase);   // this CTA's union slots ubase .. ubase + nu - 1
+  const int nit = it1 - it0;
   const uint32_t q_s = smem_u32(smem + lay.q);
   const uint32_t kv_s = smem_u32(smem + lay.kv);
   const uint32_t vv_s = smem_u32(smem + lay.vv);
   // Block of slot `half` of item `it` (a missing second block repeats the
   // first one's tiles and is masked out).
-  auto item_block = [&](int it, int half) { return ulist[min(2 * it + half, nu - 1)]; };
+  auto item_block = [&](int it, int half) { return ulist[ubase + min(2 * it + half, nu - 1)]; };
+  float m_fin = -INFINITY, l_fin = 0.f;   // a softmax thread's row state after the last item
 
   if (warp == kTcTmaWarp) {
     // ------------------------------------------------------- TMA producer
@@ -448,7 +478,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int sb = it & 1;
       const int u = 2 * it + half;            // this warp's union slot
       const bool present = u < nu;
-      const bool sel = present && active && ((umask[u] >> tok) & 1);
+      const bool sel = present && active && ((umask[ubase + u] >> tok) & 1);
       const bool warp_sel = __any_sync(0xffffffffu, sel);
       // No early exit from this loop: both warps of a quadrant must meet the
       // same pair barriers, so after a failed (timed-out) wait the warp keeps
@@ -576,32 +606,109 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     xch[half * 128 + r] = l_run;
     pair_sync(quad);
     const float l_row = l_run + xch[(half ^ 1) * 128 + r];
-    const float inv = (l_row > 0.f) ? 1.f / l_row : 0.f;
-    __nv_bfloat16* orow = p.out + ((static_cast<size_t>(b) * p.nq + t0 + tok) * Hq + h * kGroup + (r & 15)) * kHeadDim;
+    m_fin = m_run;
+    l_fin = l_row;
+    if (csize == 1) {   // (in a cluster the partial rows are merged below)
+      const float inv = (l_row > 0.f) ? 1.f / l_row : 0.f;
+      __nv_bfloat16* orow = p.out + ((static_cast<size_t>(b) * p.nq + t0 + tok) * Hq + h * kGroup + (r & 15)) * kHeadDim;
 #pragma unroll 1
-    for (int c = 0; c < 2; ++c) {
-      const int col = half * 64 + c * 32;
-      uint32_t o[32];
-      if (nit > 0) {
-        tc::ld32(lane_addr + kColO + col, o);
-        tc::wait_ld();
-      } else {
+      for (int c = 0; c < 2; ++c) {
+        const int col = half * 64 + c * 32;
+        uint32_t o[32];
+        if (nit > 0) {
+          tc::ld32(lane_addr + kColO + col, o);
+          tc::wait_ld();
+        } else {
 #pragma unroll
-        for (int x = 0; x < 32; ++x) o[x] = 0u;
+          for (int x = 0; x < 32; ++x) o[x] = 0u;
+        }
+        if (active) {
+          uint32_t wo[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x)
+            wo[x] = pack_bf16x2(__uint_as_float(o[2 * x]) * inv, __uint_as_float(o[2 * x + 1]) * inv);
+          uint4* dst = reinterpret_cast<uint4*>(orow + col);
+#pragma unroll
+          for (int x = 0; x < 4; ++x) dst[x] = make_uint4(wo[4 * x], wo[4 * x + 1], wo[4 * x + 2], wo[4 * x + 3]);
+        }
       }
-      if (active) {
-        uint32_t wo[16];
-#pragma unroll
-        for (int x = 0; x < 16; ++x)
-          wo[x] = pack_bf16x2(__uint_as_float(o[2 * x]) * inv, __uint_as_float(o[2 * x + 1]) * inv);
-        uint4* dst = reinterpret_cast<uint4*>(orow + col);
-#pragma unroll
-        for (int x = 0; x < 4; ++x) dst[x] = make_uint4(wo[4 * x], wo[4 * x + 1], wo[4 * x + 2], wo[4 * x + 3]);
+      if (active && half == 0 && p.lse) {
+        p.lse[(static_cast<size_t>(b) * p.nq + t0 + tok) * Hq + h * kGroup + (r & 15)] =
+            (l_row > 0.f) ? (m_run + fast_log2(l_row)) * 0.69314718055994531f : -INFINITY;
       }
     }
-    if (active && half == 0 && p.lse) {
-      p.lse[(static_cast<size_t>(b) * p.nq + t0 + tok) * Hq + h * kGroup + (r & 15)] =
-          (l_row > 0.f) ? (m_run + fast_log2(l_row)) * 0.69314718055994531f : -INFINITY;
+  }
+
+  if (csize > 1) {
+    // ---- cluster merge: row r of the tile is finished by CTA r % C ----
+    // Each CTA's partial row (O relative to its running max m, and the row
+    // sum l) goes into the owner's K ring, free once every CTA is past its
+    // last item: [source rank][local row r / C][128] O and [source][row] (m, l).
+    const int rp = (128 + csize - 1) / csize;
+    float* part = reinterpret_cast<float*>(smem + lay.kv);
+    float2* pml = reinterpret_cast<float2*>(smem + lay.kv + csize * rp * 512);
+    __syncwarp();
+    cluster_arrive();
+    cluster_wait();
+    if (warp < kTcSoftmaxWarps) {
+      const int quad = warp & 3, half = warp >> 2;
+      const int r = quad * 32 + lane;
+      const int dst = r % csize, lr = r / csize;
+      const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+      const uint32_t a = dsmem_addr(part + (rank * rp + lr) * 128 + half * 64, static_cast<uint32_t>(dst));
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        uint32_t o[32];
+        if (nit > 0) {
+          tc::ld32(lane_addr + kColO + half * 64 + c * 32, o);
+          tc::wait_ld();
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) o[x] = 0u;
+        }
+#pragma unroll
+        for (int x = 0; x < 8; ++x)
+          st_dsmem_f32x4(a + c * 128 + 16 * x,
+                         make_float4(__uint_as_float(o[4 * x]), __uint_as_float(o[4 * x + 1]),
+                                     __uint_as_float(o[4 * x + 2]), __uint_as_float(o[4 * x + 3])));
+      }
+      if (half == 0)
+        st_dsmem_f32x2(dsmem_addr(pml + rank * rp + lr, static_cast<uint32_t>(dst)), make_float2(m_fin, l_fin));
+    }
+    __syncwarp();
+    cluster_arrive();
+    cluster_wait();
+    // Owner: M = max_c m_c, O = sum_c 2^(m_c - M) O_c, l likewise; four
+    // columns of one row per thread.
+#pragma unroll 1
+    for (int e = tid; e < rp * 32; e += kTcThreads) {
+      const int lr = e >> 5, c4 = e & 31;
+      const int r = lr * csize + rank;
+      if (r >= 128 || (r >> 4) >= n_act) continue;
+      float mx = -INFINITY;
+      for (int c = 0; c < csize; ++c) mx = fmaxf(mx, pml[c * rp + lr].x);
+      float l = 0.f;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (mx > -INFINITY) {
+        for (int c = 0; c < csize; ++c) {
+          const float2 ml = pml[c * rp + lr];
+          const float w = fast_exp2(ml.x - mx);
+          const float4 v = *reinterpret_cast<const float4*>(part + (c * rp + lr) * 128 + 4 * c4);
+          l = fmaf(w, ml.y, l);
+          o.x = fmaf(w, v.x, o.x);
+          o.y = fmaf(w, v.y, o.y);
+          o.z = fmaf(w, v.z, o.z);
+          o.w = fmaf(w, v.w, o.w);
+        }
+      }
+      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+      const int tok = r >> 4;
+      __nv_bfloat16* orow =
+          p.out + ((static_cast<size_t>(b) * p.nq + t0 + tok) * Hq + h * kGroup + (r & 15)) * kHeadDim + 4 * c4;
+      *reinterpret_cast<uint2*>(orow) = make_uint2(pack_bf16x2(o.x * inv, o.y * inv), pack_bf16x2(o.z * inv, o.w * inv));
+      if (c4 == 0 && p.lse)
+        p.lse[(static_cast<size_t>(b) * p.nq + t0 + tok) * Hq + h * kGroup + (r & 15)] =
+            (l > 0.f) ? (mx + fast_log2(l)) * 0.69314718055994531f : -INFINITY;
     }
   }
 
@@ -613,7 +720,55 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
+// Clusters of C CTAs resident at once on the current device (cached; every
+// launch of the kernel runs one CTA per SM).
+int tc_active_clusters(int C) {
+  static int cache[64][17];
+  static bool done[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!done[dev]) {
+    const bool ok =
+        cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcMaxSmem) == cudaSuccess &&
+        cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+    for (int c = 1; c <= 16; ++c) {
+      int n = 0;
+      if (ok) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(c, 1, 1);
+        cfg.blockDim = dim3(kTcThreads, 1, 1);
+        cfg.dynamicSmemBytes = kTcMaxSmem;
+        cudaLaunchAttribute a[1];
+        a[0].id = cudaLaunchAttributeClusterDimension;
+        a[0].val.clusterDim.x = c;
+        a[0].val.clusterDim.y = 1;
+        a[0].val.clusterDim.z = 1;
+        cfg.attrs = a;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel, &cfg) != cudaSuccess) n = 0;
+      }
+      cache[dev][c] = n;
+    }
+    cudaGetLastError();
+    done[dev] = true;
+  }
+  return cache[dev][C];
+}
+
 }  // namespace
+
+bool attn_tc_fits(const Shape& s) { return tc_layout(s.nbmax).total + 1024 <= kTcMaxSmem; }
+
+// CTAs per tile: 1 while the tiles alone fill half the SMs; otherwise the
+// largest cluster (at most 16, and at most one CTA per two union blocks of a
+// full selection) with which every tile's cluster is resident at once.
+int attn_tc_cluster_size(const Shape& s) {
+  const long long units = static_cast<long long>((s.nq + kTcTokens - 1) / kTcTokens) * s.B * s.Hkv;
+  if (units * 2 > device_sm_count()) return 1;
+  for (int C = std::min(16, s.kmax / 2); C >= 2; --C)
+    if (tc_active_clusters(C) >= units) return C;
+  return 1;
+}
 
 cudaError_t launch_attn_tc(const Shape& s, const CUtensorMap& q_map, const CUtensorMap& k_map,
                            const CUtensorMap& v_map, const int32_t* kv_lens, const int32_t* block_idx,
@@ -632,13 +787,21 @@ cudaError_t launch_attn_tc(const Shape& s, const CUtensorMap& q_map, const CUten
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
   p.status = status;
-  const int smem = tc_layout(s.nbmax).total + 1024;
-  if (smem > 227 * 1024) return cudaErrorInvalidConfiguration;
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  dim3 grid((s.nq + kTcTokens - 1) / kTcTokens, s.Hkv, s.B);
-  attn_tc_kernel<<<grid, kTcThreads, smem, st>>>(q_map, k_map, v_map, p);
-  return cudaGetLastError();
+  if (!attn_tc_fits(s) || tc_active_clusters(1) < 1) return cudaErrorInvalidConfiguration;
+  p.csize = attn_tc_cluster_size(s);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(((s.nq + kTcTokens - 1) / kTcTokens) * p.csize, s.Hkv, s.B);
+  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = tc_layout(s.nbmax).total + 1024;
+  cfg.stream = st;
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = p.csize;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = p.csize > 1 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, attn_tc_kernel, q_map, k_map, v_map, p);
 }
 
 }  // namespace infllmv2

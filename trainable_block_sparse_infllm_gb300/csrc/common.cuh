@@ -120,6 +120,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with acquire at cluster scope: for a phase completed by other
+// CTAs' remote stores (st.async), whose complete_tx releases at that scope.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t* status) {
+  for (uint32_t it = 0; it < kSpinLimit; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+  }
+  atomicOr(status, kStatusTimeout);
+  return false;
+}
+
 // Returns false (and flags the status word) if the phase never completed.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
   for (uint32_t it = 0; it < kSpinLimit; ++it) {
@@ -269,6 +291,15 @@ __device__ __forceinline__ void st_dsmem_f32x4(uint32_t addr, float4 v) {
 
 __device__ __forceinline__ void st_dsmem_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Remote store whose arrival is counted on the destination CTA's mbarrier
+// (8 bytes of complete_tx): a receiver that waits on that mbarrier sees the
+// value, with no cluster barrier (threads busy in other roles need not join).
+__device__ __forceinline__ void st_async_f32x2(uint32_t addr, float2 v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(addr),
+               "f"(v.x), "f"(v.y), "r"(remote_bar)
+               : "memory");
 }
 
 // ------------------------------------------- programmatic dependent launch --

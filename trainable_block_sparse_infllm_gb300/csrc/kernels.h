@@ -19,6 +19,9 @@ struct Shape {
   float attn_scale;
 };
 
+// SMs of the current device (cached per device).
+int device_sm_count();
+
 // ---- stage 1 ---------------------------------------------------------------
 cudaError_t launch_compress(const Shape& s, const void* k, const int32_t* kv_lens, int kbegin,
                             int kend, void* kc, uint32_t* status, cudaStream_t st);
@@ -52,7 +55,11 @@ cudaError_t launch_attn(const Shape& s, bool prefill, const CUtensorMap& q_map,
                         const int32_t* kv_lens, const int32_t* block_idx, const int32_t* n_sel,
                         void* out, float* lse, void* ws, uint32_t* status, cudaStream_t st);
 
-// Prefill on tcgen05/TMEM: 8 query tokens x 16 heads per 128-row MMA tile.
+// Prefill on tcgen05/TMEM: 8 query tokens x 16 heads per 128-row MMA tile;
+// with few tiles (speculative verification, short chunks) each tile's union
+// of blocks is split over a cluster.
+bool attn_tc_fits(const Shape& s);
+int attn_tc_cluster_size(const Shape& s);
 cudaError_t launch_attn_tc(const Shape& s, const CUtensorMap& q_map, const CUtensorMap& k_map,
                            const CUtensorMap& v_map, const int32_t* kv_lens, const int32_t* block_idx,
                            const int32_t* n_sel, void* out, float* lse, uint32_t* status,

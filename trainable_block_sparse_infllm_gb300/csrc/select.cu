@@ -10,11 +10,13 @@
 //   r[blk]  = max_j g[j] over kernels meeting the block (j in 4 blk - 1 .. 4 blk + 3)
 //   top-k over r with forced initial/local blocks.
 //
-// Two paths, same result:
-//  * decode / verify (n_q <= 16): select_decode.cu, one thread-block cluster
-//    per (b, h_kv) group.
-//  * prefill (n_q > 16): select_tc.cu on tcgen05, 8 tokens x 16 heads per
-//    128-row tile.
+// Paths, same result:
+//  * decode (n_q = 1), and up to 16 tokens where nothing below fits:
+//    select_decode.cu, one thread-block cluster per (b, h_kv) group.
+//  * 2 tokens: select_verify.cu, the two-pass cluster kernel.
+//  * 3-16 tokens and prefill: select_tc.cu on tcgen05, 8 tokens x 16 heads
+//    per 128-row tile; with few tiles each tile's chunks are split over a
+//    cluster.
 #include "select_common.cuh"
 
 namespace infllmv2 {
@@ -32,6 +34,7 @@ int device_sm_count() {
 }
 
 bool select_tc_supported(const Shape& s);
+int select_tc_cluster_size(const Shape& s, int sc);
 cudaError_t launch_select_tc(const Shape& s, const CUtensorMap& kc_map, const CUtensorMap& kcc_map,
                              const CUtensorMap& q_map, const SelParams& p, cudaStream_t st);
 size_t select_decode_ncpad(const Shape& s);
@@ -50,16 +53,25 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 bool use_decode_path(const Shape& s) { return s.nq <= kSelDecodeMaxNq && select_decode_supported(s); }
 
-// 2 to 8 tokens per sequence (speculative verification): the two-pass
-// cluster kernel, when its clusters fit the device; no workspace.
+// Two tokens per sequence: the two-pass mma.sync cluster kernel (on a 128K
+// cache 27 us against 32 us for the tensor-core tile, whose cost does not
+// shrink with fewer rows); no workspace.
 bool use_verify_path(const Shape& s) { return s.nq >= 2 && s.nq <= 8 && select_verify_cluster_size(s) > 0; }
+
+// 3 to 16 tokens per sequence (speculative verification, short chunks): the
+// tensor-core tile with its chunks split over a cluster, when such clusters
+// fit the device (65 -> 32 us for 8 tokens on a 128K cache); no workspace.
+bool use_tc_cluster(const Shape& s) {
+  if (s.nq == 2 && use_verify_path(s)) return false;
+  return s.nq >= 2 && s.nq <= kSelDecodeMaxNq && select_tc_supported(s) && select_tc_cluster_size(s, 0) > 1;
+}
 
 }  // namespace
 
 bool select_supported(const Shape& s) { return use_decode_path(s) || select_tc_supported(s); }
 
 size_t select_workspace_bytes(const Shape& s) {
-  if (use_verify_path(s)) return 0;
+  if (use_tc_cluster(s) || use_verify_path(s)) return 0;
   if (use_decode_path(s)) {
     const size_t units = static_cast<size_t>(s.B) * s.Hkv * s.nq;
     return align256(units * kGroup * select_decode_ncpad(s) * sizeof(float));
@@ -92,6 +104,7 @@ cudaError_t launch_select(const Shape& s, const CUtensorMap& kc_map, const CUten
   p.write_r = block_scores != nullptr;
   p.r_buf = block_scores;
 
+  if (use_tc_cluster(s)) return launch_select_tc(s, kc_map, kc_map, q_map, p, st);
   if (use_verify_path(s))
     return launch_select_verify(s, select_verify_cluster_size(s), kc_map, q_map, kv_lens, block_idx, n_sel,
                                 block_scores, status, st);

@@ -26,6 +26,7 @@ struct SelParams {
   int write_r;
   int stages;          // prefill path: pipeline depth
   int sc, nccmax;      // prefill path: coarse-LSE window (0 = exact LSE) and windows per cache
+  int csize;           // prefill path: CTAs per 8-token tile (1, or a cluster splitting the chunks)
   uint32_t* status;
 };
 
@@ -78,8 +79,5 @@ __device__ __forceinline__ void score_ntile(float (&acc)[4], const uint32_t (&a)
 #pragma unroll
   for (int e = 0; e < 4; ++e) acc[e] = (c[0][e] + c[2][e]) + (c[1][e] + c[3][e]);
 }
-
-// Number of SMs of the current device (cached per device).
-int device_sm_count();
 
 }  // namespace infllmv2

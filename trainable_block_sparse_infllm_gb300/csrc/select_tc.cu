@@ -25,6 +25,17 @@
 // 32 of a chunk's 64 kernels; row r = 32 (w % 4) + lane: token r / 16, head
 // r % 16), warp 8 MMA issuer (one thread), warp 9 TMA producer.  The row
 // warps end with one token's warp top-k each.
+//
+// Few tiles (2-16 tokens per sequence: speculative verification, short
+// chunks) would leave most SMs idle, so a tile's chunks are then split over
+// a cluster of C CTAs (CTA r: chunks [r n / C, (r + 1) n / C)).  At the end
+// of pass 1 each CTA sends its rows' (max, sum) to every CTA with st.async,
+// counted on the receiver's mbarrier (the producer and the MMA issuer go on
+// streaming pass 2 meanwhile); each CTA merges the C partials into the LSE.
+// Pass 2 writes each block score straight into the shared memory of the
+// token's owner (token t: CTA t mod C), plus the g of the CTA's last kernel,
+// which the block after its range needs.  After one cluster barrier the
+// owner completes those boundary blocks and runs the CTA-wide top-k.
 #include "select_common.cuh"
 #include "tc.cuh"
 
@@ -42,30 +53,37 @@ constexpr int kStMmaWarp = kStRowWarps, kStTmaWarp = kStRowWarps + 1;
 constexpr uint32_t kStTmemCols = 128;      // two z buffers of 64 columns
 
 struct StLayout {
-  int ring, q, r, flag, tk, xch, bars, slot, total;
+  int ring, q, r, flag, tk, ctk, cbits, csurv, xch, lse_in, tails, bars, slot, total;
 };
+constexpr int kStMaxC = 16;
+constexpr int kStClusterMinSmem = 116 * 1024;   // a cluster launch requests at least this: one CTA per SM
 
 // The top-k flags and scratch overlay the chunk ring, which is idle once the
 // last chunk's products are done (every row warp has waited for them before
 // its top-k).
-__host__ __device__ inline StLayout st_layout(int nbmax, int stages) {
+__host__ __device__ inline StLayout st_layout(int nbmax, int stages, bool clustered) {
   StLayout l;
   l.ring = 0;
   l.flag = 0;                                           // [8 tokens][nbmax] top-k flags (in the ring)
   l.tk = (kStTokens * nbmax + 15) & ~15;                // one warp top-k scratch per token (in the ring)
+  l.ctk = 0;                                            // cluster form: the CTA-wide top-k scratch (in the ring)
+  l.cbits = (static_cast<int>(sizeof(SmemTopkScratch<kStThreads>)) + 15) & ~15;
+  l.csurv = l.cbits + (((nbmax + 31) / 32 * 4 + 15) & ~15);
   l.q = stages * kStChunkBytes;                         // two 64-column boxes x 128 rows
   l.r = l.q + 32768;                                    // [8 tokens][nbmax] block scores
   l.xch = (l.r + kStTokens * nbmax * 4 + 15) & ~15;     // [2][128] (max, sum)
-  l.bars = l.xch + 2 * 128 * 8;
+  l.lse_in = l.xch + 2 * 128 * 8;                       // cluster form: [C][128 rows] (max, sum)
+  l.tails = l.lse_in + (clustered ? kStMaxC * 128 * 8 : 0);   // cluster form: [C][8 tokens] last-kernel g
+  l.bars = l.tails + (clustered ? kStMaxC * kStTokens * 4 : 0);
   l.slot = l.bars + 16 * 8;
   l.total = l.slot + 16;
-  const int ring_need = l.tk + kStTokens * static_cast<int>(sizeof(WarpTopkScratch));
+  const int ring_need = clustered ? l.csurv + nbmax * 8 : l.tk + kStTokens * static_cast<int>(sizeof(WarpTopkScratch));
   if (ring_need > l.q) l.total = 1 << 30;               // does not fit: never chosen
   return l;
 }
 
 enum StBar { kFull = 0, kEmpty = kFull + kStMaxStages, kQ = kEmpty + kStMaxStages, kZFull = kQ + 1,
-             kZFree = kZFull + 2, kStNumBars = kZFree + 2 };
+             kZFree = kZFull + 2, kLse = kZFree + 2, kStNumBars = kLse + 1 };
 
 // Barrier of the two row warps of TMEM lane quadrant q (ids 1..4).
 __device__ __forceinline__ void quad_pair_sync(int q) {
@@ -79,7 +97,8 @@ __global__ void __launch_bounds__(kStThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int S = p.stages;
-  const StLayout lay = st_layout(p.nbmax, S);
+  const int csize = p.csize;
+  const StLayout lay = st_layout(p.nbmax, S, csize > 1);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + lay.bars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + lay.slot);
   float* r_all = reinterpret_cast<float*>(smem + lay.r);
@@ -87,11 +106,13 @@ __global__ void __launch_bounds__(kStThreads, 1)
   const int h = blockIdx.y, b = blockIdx.z;
   const int bh = b * p.Hkv + h;
   const int nq = p.nq;
-  const int t0 = blockIdx.x * kStTokens;
+  const int rank = static_cast<int>(blockIdx.x) % csize;   // == the rank in the cluster
+  const int t0 = (static_cast<int>(blockIdx.x) / csize) * kStTokens;
   const int n_act = min(kStTokens, nq - t0);
   const int L = p.kv_lens[b];
 
-  if (L < nq || L > p.Lmax) {
+  if (L < nq || L > p.Lmax) {   // the same in every CTA of a cluster: none touches another's memory
+    if (rank != 0) return;
     for (int e = tid; e < n_act * p.kmax; e += kStThreads) {
       const size_t u = static_cast<size_t>(bh) * nq + t0 + e / p.kmax;
       p.block_idx[u * p.kmax + e % p.kmax] = -1;
@@ -105,6 +126,8 @@ __global__ void __launch_bounds__(kStThreads, 1)
   }
   const int nvis_max = n_complete_kernels(L - nq + t0 + n_act);
   const int nch = (nvis_max + kStChunk - 1) / kStChunk;
+  const int ch0 = rank * nch / csize, ch1 = (rank + 1) * nch / csize;   // this CTA's fine chunks
+  const int nch_my = ch1 - ch0;
   // Stream of chunks: A (coarse windows, the LSE approximation [InfLLM v2 >
   // Efficient LSE approximation]; only with p.sc > 0), B (fine LSE, for the
   // tokens without a complete window; skipped when every token has one), C
@@ -112,8 +135,8 @@ __global__ void __launch_bounds__(kStThreads, 1)
   const int nvis_c_max = p.sc ? (L - nq + t0 + n_act) / p.sc : 0;
   const int nch_a = (nvis_c_max + kStChunk - 1) / kStChunk;
   const bool need_b = p.sc == 0 || (L - nq + t0 + 1) / p.sc == 0;
-  const int seg_c = nch_a + (need_b ? nch : 0);
-  const int total = nch > 0 ? seg_c + nch : 0;
+  const int seg_c = nch_a + (need_b ? nch_my : 0);
+  const int total = nch_my > 0 ? seg_c + nch_my : 0;
 
   for (int e = tid; e < kStTokens * p.nbmax; e += kStThreads) r_all[e] = -INFINITY;
   if (tid == 0) {
@@ -129,6 +152,9 @@ __global__ void __launch_bounds__(kStThreads, 1)
       mbar_init(&bars[kZFull + s], 1);
       mbar_init(&bars[kZFree + s], kStRowWarps);
     }
+    mbar_init(&bars[kLse], 1);
+    // Cluster form: the C partials of 128 rows arrive by st.async.
+    if (csize > 1) mbar_arrive_expect_tx(&bars[kLse], csize * 128 * 8);
     fence_barrier_init();
   }
   if (warp == kStMmaWarp) {
@@ -138,6 +164,10 @@ __global__ void __launch_bounds__(kStThreads, 1)
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  if (csize > 1) {   // every CTA's barriers and block scores initialised before any remote store
+    cluster_arrive();
+    cluster_wait();
+  }
   const uint32_t tmem = *tmem_slot;
   const uint32_t base_s = smem_u32(smem);
 
@@ -155,7 +185,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
         const int st = it % S;
         if (it >= S && !mbar_wait(&bars[kEmpty + st], ((it / S) - 1) & 1, p.status)) break;
         const bool coarse_seg = it < nch_a;
-        const int ch = coarse_seg ? it : (it < seg_c ? it - nch_a : it - seg_c);
+        const int ch = coarse_seg ? it : ch0 + (it < seg_c ? it - nch_a : it - seg_c);
         const CUtensorMap* map = coarse_seg ? &kcc_map : &kc_map;
         const int rows = coarse_seg ? p.nccmax : p.ncmax;
         uint8_t* dst = smem + lay.ring + st * kStChunkBytes;
@@ -221,18 +251,42 @@ __global__ void __launch_bounds__(kStThreads, 1)
     float m = -INFINITY, l = 0.f, lse2 = -INFINITY;
     float carry = -INFINITY;
     bool ok = true;
+    // End of pass 1: merge the two halves' (max, sum) of each row; in a
+    // cluster also the C CTAs' partials of the row.
+    auto end_pass1 = [&]() {
+      xch[hf * 128 + r] = make_float2(m, l);
+      quad_pair_sync(q4);
+      const float2 o = xch[(hf ^ 1) * 128 + r];
+      lse_merge(m, l, o.x, o.y);
+      if (csize > 1) {
+        float2* lse_in = reinterpret_cast<float2*>(smem + lay.lse_in);
+        if (hf == 0)
+          for (int d = 0; d < csize; ++d)
+            st_async_f32x2(dsmem_addr(lse_in + rank * 128 + r, static_cast<uint32_t>(d)), make_float2(m, l),
+                           dsmem_addr(&bars[kLse], static_cast<uint32_t>(d)));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_cluster(&bars[kLse], 0, p.status));
+        m = -INFINITY;
+        l = 0.f;
+        for (int c = 0; c < csize; ++c) {
+          const float2 v = lse_in[c * 128 + r];
+          lse_merge(m, l, v.x, v.y);
+        }
+      }
+      lse2 = (m == -INFINITY) ? -INFINITY : m + fast_log2(l);
+    };
+    // Block score j of this row's token: into its own row here, or into the
+    // owner's in a cluster.
+    auto put_r = [&](int j, float v) {
+      if (csize == 1)
+        r_tok[j] = v;
+      else
+        st_dsmem_f32(dsmem_addr(r_tok + j, static_cast<uint32_t>(tok % csize)), v);
+    };
     for (int it = 0; it < total; ++it) {
       const int zb = it & 1;
       const bool pass2 = it >= seg_c;
-      const int kbase = (it < nch_a ? it : (pass2 ? it - seg_c : it - nch_a)) * kStChunk;
-      if (it == seg_c) {
-        // Merge the two halves' (max, sum) of each row.
-        xch[hf * 128 + r] = make_float2(m, l);
-        quad_pair_sync(q4);
-        const float2 o = xch[(hf ^ 1) * 128 + r];
-        lse_merge(m, l, o.x, o.y);
-        lse2 = (m == -INFINITY) ? -INFINITY : m + fast_log2(l);
-      }
+      const int kbase = (it < nch_a ? it : ch0 + (pass2 ? it - seg_c : it - nch_a)) * kStChunk;
+      if (it == seg_c) end_pass1();
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars[kZFull + zb], (it >> 1) & 1, p.status));
       tc::fence_after_sync();
       uint32_t v[32];
@@ -318,14 +372,23 @@ __global__ void __launch_bounds__(kStThreads, 1)
           const float prev = x == 1 ? left : pl;
           if (active && j <= c_t && j < p.nbmax) {
             const bool has = max(0, 4 * j - 1) < nvis_t;
-            r_tok[j] = has ? fmaxf(fmaxf(prev, fmaxf(p0, p1)), fmaxf(g0, g1)) : -INFINITY;
+            put_r(j, has ? fmaxf(fmaxf(prev, fmaxf(p0, p1)), fmaxf(g0, g1)) : -INFINITY);
           }
         }
       }
     }
-    // The block after the last chunk meets one kernel of it (4 j - 1): the
-    // lower-half warp carries it.
-    if (nch > 0 && hf == 0 && x == 0 && active) {
+    if (csize > 1) {
+      // A CTA without chunks still sends its (empty) partials.
+      if (total == 0) end_pass1();
+      // The block after this CTA's range meets its last kernel (4 j - 1):
+      // the owner completes that block with it.
+      if (hf == 0 && x == 0 && active) {
+        float* tails = reinterpret_cast<float*>(smem + lay.tails);
+        st_dsmem_f32(dsmem_addr(tails + rank * kStTokens + tok, static_cast<uint32_t>(tok % csize)), carry);
+      }
+    } else if (nch > 0 && hf == 0 && x == 0 && active) {
+      // The block after the last chunk meets one kernel of it (4 j - 1): the
+      // lower-half warp carries it.
       const int j = nch * (kStChunk / 4);
       if (j <= c_t && j < p.nbmax && 4 * j - 1 < nvis_t) r_tok[j] = carry;
     }
@@ -336,7 +399,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
     fence_proxy_async_smem();
     // Top-k: warp (q, hf) takes token 2 q + hf, whose scores the two warps of
     // the quadrant wrote.
-    {
+    if (csize == 1) {
       const int tt = 2 * q4 + hf;
       if (tt < n_act) {
         WarpTopkScratch& tk = reinterpret_cast<WarpTopkScratch*>(smem + lay.tk)[tt];
@@ -351,6 +414,37 @@ __global__ void __launch_bounds__(kStThreads, 1)
     }
   }
 
+  if (csize > 1) {
+    // ---- cluster: the owner CTA's tokens (t mod C == rank) ----
+    __syncwarp();
+    cluster_arrive();
+    cluster_wait();
+    fence_proxy_async_smem();   // the top-k scratch lies over the TMA-written ring
+    SmemTopkScratch<kStThreads>& tk = *reinterpret_cast<SmemTopkScratch<kStThreads>*>(smem + lay.ctk);
+    uint32_t* tbits = reinterpret_cast<uint32_t*>(smem + lay.cbits);
+    unsigned long long* tsurv = reinterpret_cast<unsigned long long*>(smem + lay.csurv);
+    const float* tails = reinterpret_cast<const float*>(smem + lay.tails);
+#pragma unroll 1
+    for (int tt = rank; tt < n_act; tt += csize) {
+      float* rw = r_all + tt * p.nbmax;
+      const int i_t = L - nq + t0 + tt, c = i_t / kBlock;
+      if (tid == 0) {   // the block after CTA q's range, with q's last kernel (CTAs without chunks share an end)
+        const int nvis = n_complete_kernels(i_t + 1);
+        for (int q = 0; q < csize; ++q) {
+          const int j = 16 * ((q + 1) * nch / csize);
+          if (j <= c && j < p.nbmax && 4 * j - 1 < nvis) rw[j] = fmaxf(rw[j], tails[q * kStTokens + tt]);
+        }
+      }
+      __syncthreads();
+      const size_t u = static_cast<size_t>(bh) * nq + t0 + tt;
+      if (p.write_r)
+        for (int jj = tid; jj < p.nbmax; jj += kStThreads) p.r_buf[u * p.nbmax + jj] = rw[jj];
+      select_topk_smem<kStThreads>(rw, c + 1, p.n_init, p.n_local, p.topk, p.inc_forced != 0, p.kmax,
+                                   p.block_idx + u * p.kmax, p.n_sel + u, tk, tbits, tsurv, tid);
+      __syncthreads();
+    }
+  }
+
   tc::fence_before_sync();
   __syncthreads();
   if (warp == kStMmaWarp) {
@@ -359,28 +453,89 @@ __global__ void __launch_bounds__(kStThreads, 1)
   }
 }
 
-}  // namespace
+// Clusters of C CTAs resident at once on the current device (cached; a
+// cluster launch runs one CTA per SM).
+int st_active_clusters(int C) {
+  static int cache[64][kStMaxC + 1];
+  static bool done[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!done[dev]) {
+    const bool ok =
+        cudaFuncSetAttribute(sel_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) == cudaSuccess &&
+        cudaFuncSetAttribute(sel_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+    for (int c = 1; c <= kStMaxC; ++c) {
+      int n = 0;
+      if (ok) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(c, 1, 1);
+        cfg.blockDim = dim3(kStThreads, 1, 1);
+        cfg.dynamicSmemBytes = kStClusterMinSmem;
+        cudaLaunchAttribute a[1];
+        a[0].id = cudaLaunchAttributeClusterDimension;
+        a[0].val.clusterDim.x = c;
+        a[0].val.clusterDim.y = 1;
+        a[0].val.clusterDim.z = 1;
+        cfg.attrs = a;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, sel_tc_kernel, &cfg) != cudaSuccess) n = 0;
+      }
+      cache[dev][c] = n;
+    }
+    cudaGetLastError();
+    done[dev] = true;
+  }
+  return cache[dev][C];
+}
 
-int select_tc_stages(const Shape& s) {
+int stages_for(const Shape& s, bool clustered) {
   for (int st = kStMaxStages; st >= 2; --st)
-    if (st_layout(s.nbmax, st).total + 1024 <= 227 * 1024) return st;
+    if (st_layout(s.nbmax, st, clustered).total + 1024 <= 227 * 1024) return st;
   return 0;
 }
 
+}  // namespace
+
+int select_tc_stages(const Shape& s) { return stages_for(s, false); }
+
 bool select_tc_supported(const Shape& s) { return select_tc_stages(s) > 0; }
+
+// CTAs per 8-token tile: 1 while the tiles alone fill half the SMs (or with
+// the coarse LSE); otherwise the largest cluster (at most 16, at least two
+// chunks per CTA) with which every tile's cluster is resident at once.
+int select_tc_cluster_size(const Shape& s, int sc) {
+  if (sc != 0 || stages_for(s, true) == 0) return 1;
+  const long long units = static_cast<long long>((s.nq + kStTokens - 1) / kStTokens) * s.B * s.Hkv;
+  if (units * 2 > device_sm_count()) return 1;
+  const int nch = (s.ncmax + kStChunk - 1) / kStChunk;
+  for (int C = std::min(kStMaxC, nch / 2); C >= 2; --C)
+    if (st_active_clusters(C) >= units) return C;
+  return 1;
+}
 
 // p.sc > 0: coarse-window LSE from kcc_map (else kcc_map is not read).
 cudaError_t launch_select_tc(const Shape& s, const CUtensorMap& kc_map, const CUtensorMap& kcc_map,
                              const CUtensorMap& q_map, const SelParams& p, cudaStream_t st) {
   SelParams pp = p;
-  pp.stages = select_tc_stages(s);
+  if (st_active_clusters(1) < 1) return cudaErrorInvalidConfiguration;
+  pp.csize = select_tc_cluster_size(s, p.sc);
+  pp.stages = stages_for(s, pp.csize > 1);
   if (pp.stages == 0) return cudaErrorInvalidConfiguration;
-  const int smem = st_layout(s.nbmax, pp.stages).total + 1024;
-  cudaError_t e = cudaFuncSetAttribute(sel_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  dim3 grid((s.nq + kStTokens - 1) / kStTokens, s.Hkv, s.B);
-  sel_tc_kernel<<<grid, kStThreads, smem, st>>>(kc_map, kcc_map, q_map, pp);
-  return cudaGetLastError();
+  int smem = st_layout(s.nbmax, pp.stages, pp.csize > 1).total + 1024;
+  if (pp.csize > 1) smem = std::max(smem, kStClusterMinSmem);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(((s.nq + kStTokens - 1) / kStTokens) * pp.csize, s.Hkv, s.B);
+  cfg.blockDim = dim3(kStThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = pp.csize;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = pp.csize > 1 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, sel_tc_kernel, kc_map, kcc_map, q_map, pp);
 }
 
 }  // namespace infllmv2

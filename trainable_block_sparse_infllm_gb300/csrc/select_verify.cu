@@ -10,7 +10,7 @@
 // One cluster of C CTAs per (b, h_kv) group, one CTA per SM, C chosen at
 // launch so that every group's cluster is resident at once.  CTA r owns the
 // 16-block groups [r per, (r + 1) per) and the matching 64-kernel chunks.
-//   pass 1   the CTA's hi/lo chunks stream through a 4-stage TMA ring (the
+//   pass 1   the CTA's hi/lo chunks stream through a 3-stage TMA ring (the
 //            rest of them head for L2 at once); z = score_scale q_t . Mean
 //            for every token t on the tensor cores; each token's running
 //            (max, sum of 2^z) per head stays in registers.
@@ -18,11 +18,11 @@
 //            one cluster barrier; each CTA merges the C partials.
 //   pass 2   the same chunks again, now from L2: z once more, then
 //            g = (1/16) sum_h 2^(z_h - lse_h) per token and kernel (the 16
-//            heads summed across the lanes of the MMA fragment), and the
-//            block maxima of the CTA's blocks per token.
-//   push     each token's block scores (and the g of the CTA's last kernel)
-//            go to the token's owner CTA (token t: CTA t mod C); one cluster
-//            barrier.
+//            heads summed across the lanes of the MMA fragment), kept in
+//            shared memory for all of the CTA's kernels and tokens.
+//   push     each token's block maxima over the CTA's blocks (and the g of
+//            the CTA's last kernel) go to the token's owner CTA (token t:
+//            CTA t mod C); one cluster barrier.
 //   top-k    the owner selects (exact, the shared top-k routine) and writes
 //            the token's list.
 // The scores never leave the chip: a second pass over the chunks from L2
@@ -37,7 +37,7 @@ constexpr int kSvThreads = 512;     // 16 warps: warp w takes n-tile w % 8 of ev
 constexpr int kSvWarps = kSvThreads / 32;
 constexpr int kSvMaxQ = 8;
 constexpr int kSvChunk = 64;
-constexpr int kSvRing = 4;
+constexpr int kSvRing = 3;
 constexpr int kSvStageBytes = 32768;
 constexpr int kSvMaxC = 16;
 constexpr int kSvMaxIt = 16;        // chunks per CTA
@@ -59,7 +59,7 @@ struct SvParams {
 // other CTAs write into (lse_in, rown, tails) are never overlaid.
 constexpr int kSvOwnedRows = 2;     // tokens an owner CTA selects (C >= 4)
 struct SvLayout {
-  int ring, q, gst, rown, tails, lse_in, wpart, cpart, lse, tk, bits, surv, bar, total;
+  int ring, q, gbuf, rown, tails, lse_in, wpart, cpart, lse, tk, bits, surv, bar, total;
 };
 
 __host__ __device__ constexpr SvLayout sv_layout() {
@@ -69,9 +69,8 @@ __host__ __device__ constexpr SvLayout sv_layout() {
   l.bits = 20480;
   l.surv = l.bits + kSvMaxBlocks / 8;
   l.q = kSvRing * kSvStageBytes;                        // [8 tokens][16 rows x 256 B]
-  l.gst = l.q + kSvMaxQ * 4096;                         // [8 tokens][65] g of a chunk + the kernel before it
-  l.rown = l.gst + kSvMaxQ * 65 * 4 + 48;               // [2 owned tokens][4096] block scores
-  l.rown = (l.rown + 15) & ~15;
+  l.gbuf = l.q + kSvMaxQ * 4096;                        // [8 tokens][16 chunks x 64] g of this CTA's kernels
+  l.rown = l.gbuf + kSvMaxQ * kSvMaxIt * kSvChunk * 4;  // [2 owned tokens][4096] block scores
   l.tails = l.rown + kSvOwnedRows * kSvMaxBlocks * 4;   // [16 CTAs][8 tokens] last-kernel g
   l.lse_in = l.tails + kSvMaxC * kSvMaxQ * 4;           // [16 CTAs][8 tokens][16 heads] (max, sum)
   l.wpart = l.lse_in + kSvMaxC * kSvMaxQ * kGroup * 8;  // [8 warps][8 tokens][16 heads] (max, sum)
@@ -98,7 +97,7 @@ __global__ void __launch_bounds__(kSvThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   constexpr SvLayout lay = sv_layout();
-  float* gst = reinterpret_cast<float*>(smem + lay.gst);            // [t][65]: kernel 64 chunk - 1 + x
+  float* gbuf = reinterpret_cast<float*>(smem + lay.gbuf);          // [t][it * 64 + x]
   float* rown = reinterpret_cast<float*>(smem + lay.rown);          // [owned row][block]
   float* tails = reinterpret_cast<float*>(smem + lay.tails);        // [src][t]
   float2* lse_in = reinterpret_cast<float2*>(smem + lay.lse_in);    // [src][t][h]
@@ -284,14 +283,8 @@ __global__ void __launch_bounds__(kSvThreads, 1)
   __syncthreads();
 
   // ------------------------------------------------------------- pass 2 --
-  // Per chunk: g of its 64 kernels per token into gst[t][1..64] (gst[t][0]
-  // holds the kernel before the chunk, -inf before the CTA's first chunk:
-  // that kernel is the previous CTA's, merged in by the owner), then the
-  // chunk's 16 block maxima per token, pushed to the token's owner.  Only
-  // kernels visible to the token count; blocks past its own block are not
-  // its candidates and are not sent.
-  const int jb1 = min(16 * k1, nbt);
-  for (int e = tid; e < nq; e += kSvThreads) gst[e * 65] = -INFINITY;
+  // g of every kernel of the CTA's chunks per token (16 heads summed across
+  // the lanes of the MMA fragment), into gbuf; no barrier inside the loop.
 #pragma unroll 1
   for (int it = 0; it < nmy; ++it) {
     const int st = consume(nmy + it);
@@ -317,46 +310,38 @@ __global__ void __launch_bounds__(kSvThreads, 1)
           s1 += __shfl_xor_sync(0xffffffffu, s1, o);
         }
         if (g == 0) {
-          float* gr = gst + t * 65 + 1 + (warp & 7) * 8 + 2 * tq;
+          float* gr = gbuf + t * (kSvMaxIt * kSvChunk) + it * kSvChunk + (warp & 7) * 8 + 2 * tq;
           gr[0] = s0 * (1.0f / kGroup);
           gr[1] = s1 * (1.0f / kGroup);
         }
       }
     }
     release(nmy + it);
-    __syncthreads();
-    const int kc0 = (k0 + it) * kSvChunk - 1;   // kernel held in gst[t][0]
-    if (tid < nq * 16) {
-      const int t = tid >> 4, jj = tid & 15;
-      const int j = 16 * (k0 + it) + jj;
-      const int c_t = (L - nq + t) / kBlock, nv = nvis_of(t);
-      if (j <= c_t && j < jb1) {
-        float r = -INFINITY;
-#pragma unroll
-        for (int k = 4 * j - 1; k <= 4 * j + 3; ++k)
-          if (k < nv) r = fmaxf(r, gst[t * 65 + (k - kc0)]);
-        st_dsmem_f32(dsmem_addr(rown + (t / C) * kSvMaxBlocks + j, t % C), r);
-      }
-    }
-    __syncthreads();
-    if (tid < nq) gst[tid * 65] = gst[tid * 65 + 64];   // the chunk's last kernel, for the next chunk
-    __syncthreads();
   }
-  // Blocks of this CTA's range past its last chunk: only the kernel before
-  // the first of them (the last chunk's last) can meet one.
+  __syncthreads();
+
+  // ------------------------------------------------- block scores to owners --
+  // Token t's scores go to CTA t % C, into owned row t / C.  Only kernels
+  // visible to the token count; the kernel before the CTA's first is the
+  // previous CTA's (merged in by the owner); blocks past the token's own
+  // block are not its candidates and are not sent.
   {
-    const int jt0 = 16 * (k0 + nmy);
-    const int kc0 = (k0 + nmy) * kSvChunk - 1;
-    for (int e = tid; e < nq * max(0, jb1 - jt0); e += kSvThreads) {
-      const int t = e / (jb1 - jt0), j = jt0 + e % (jb1 - jt0);
-      const int c_t = (L - nq + t) / kBlock, nv = nvis_of(t);
-      if (j > c_t) continue;
-      const float r = (j == jt0 && nmy > 0 && kc0 < nv) ? gst[t * 65] : -INFINITY;
+    const int jb0 = 16 * k0, jb1 = min(16 * k1, nbt);
+    const int kb0 = kSvChunk * k0, kend = kSvChunk * (k0 + nmy);   // kernels held in gbuf: [kb0, kend)
+#pragma unroll 1
+    for (int e = tid; e < nq * (jb1 - jb0); e += kSvThreads) {
+      const int t = e / (jb1 - jb0), j = jb0 + e % (jb1 - jb0);
+      if (j > (L - nq + t) / kBlock) continue;
+      const int nv = min(nvis_of(t), kend);
+      float r = -INFINITY;
+      for (int k = max(4 * j - 1, kb0); k <= min(nv - 1, 4 * j + 3); ++k)
+        r = fmaxf(r, gbuf[t * (kSvMaxIt * kSvChunk) + (k - kb0)]);
       st_dsmem_f32(dsmem_addr(rown + (t / C) * kSvMaxBlocks + j, t % C), r);
     }
     // The g of this CTA's last kernel (64 k1 - 1), for the next CTA's first block.
     for (int t = tid; t < nq; t += kSvThreads) {
-      const float gl = (nmy == k1 - k0 && nmy > 0 && kSvChunk * k1 - 1 < nvis_of(t)) ? gst[t * 65] : -INFINITY;
+      const int kl = kSvChunk * k1 - 1;
+      const float gl = (kl >= kb0 && kl < kend && kl < nvis_of(t)) ? gbuf[t * (kSvMaxIt * kSvChunk) + (kl - kb0)] : -INFINITY;
       st_dsmem_f32(dsmem_addr(tails + rank * kSvMaxQ + t, t % C), gl);
     }
   }
