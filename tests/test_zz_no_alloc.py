@@ -79,13 +79,16 @@ def test_static_scratch_rejects_oversize(dev):
     __graft_entry__.build()
     import trainable_block_sparse_infllm_gb300 as T
     import torch
-    # 8 groups x 16 tokens x 16 heads x 8192 kernels x 4 bytes = 64 MiB > 8 MiB.
-    p = T.make_params(8, 1, 131072, 16, True)
-    q = torch.zeros((8, 16, 16, 128), dtype=torch.bfloat16, device=dev)
+    # 16 tokens for 80 groups: enough tiles that no cluster splits them, so the
+    # selection keeps one score per (token, head, kernel) in scratch:
+    # 1280 units x 16 heads x 1024 kernels x 4 bytes = 80 MiB > 8 MiB.
+    p = T.make_params(40, 2, 16384, 16, True)
+    assert T.workspace_size(p, 16, T.OP_SELECT) > 8 << 20
+    q = torch.zeros((40, 16, 32, 128), dtype=torch.bfloat16, device=dev)
     kc = T.alloc_kc(p, dev)
-    lens = torch.full((8,), 131072, dtype=torch.int32, device=dev)
-    idx = torch.empty((8, 1, 16, 16), dtype=torch.int32, device=dev)
-    n = torch.empty((8, 1, 16), dtype=torch.int32, device=dev)
+    lens = torch.full((40,), 16384, dtype=torch.int32, device=dev)
+    idx = torch.empty((40, 2, 16, 16), dtype=torch.int32, device=dev)
+    n = torch.empty((40, 2, 16), dtype=torch.int32, device=dev)
     with pytest.raises(T.InfLLMv2Error) as ei:
         T.select_blocks_static(p, q, kc, lens, idx, n)
     assert ei.value.code == 3 and "built-in scratch" in str(ei.value)

@@ -206,6 +206,9 @@ enum Bar { kQFull = 0, kKFull = 1, kKEmpty = kKFull + kTcKStages, kVFull = kKEmp
            kPFull = kSFree + 2, kODone = kPFull + 2, kNumBars = kODone + 2 };
 static_assert(kNumBars <= 32, "barrier area holds 32");
 
+// kCluster: the tile's union is split over a cluster of p.csize CTAs (a
+// separate instantiation, so the one-CTA form carries none of its code).
+template <bool kCluster>
 __global__ void __launch_bounds__(kTcThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
                    const __grid_constant__ CUtensorMap v_map, TcParams p) {
@@ -223,14 +226,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int h = blockIdx.y, b = blockIdx.z;
   const int bh = b * p.Hkv + h;
   const int Hq = p.Hkv * kGroup;
-  const int csize = p.csize;
-  const int rank = static_cast<int>(blockIdx.x) % csize;   // == the rank in the cluster
-  const int t0 = (static_cast<int>(blockIdx.x) / csize) * kTcTokens;
+  const int csize = kCluster ? p.csize : 1;
+  const int rank = kCluster ? static_cast<int>(blockIdx.x) % csize : 0;   // == the rank in the cluster
+  const int t0 = kCluster ? (static_cast<int>(blockIdx.x) / csize) * kTcTokens : blockIdx.x * kTcTokens;
   const int n_act = min(kTcTokens, p.nq - t0);
   const int L = p.kv_lens[b];
 
   if (L < p.nq || L > p.Lmax) {   // the same in every CTA of a cluster: none touches another's memory
-    if (rank != 0) return;
+    if (kCluster && rank != 0) return;
     for (int e = tid; e < n_act * kGroup * kHeadDim; e += kTcThreads) {
       const int tok = e / (kGroup * kHeadDim), rem = e % (kGroup * kHeadDim);
       p.out[((static_cast<size_t>(b) * p.nq + t0 + tok) * Hq + h * kGroup) * kHeadDim + rem] = __float2bfloat16(0.f);
@@ -272,7 +275,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   // Hi + lo probabilities when some token of the tile attends few keys, and
   // always in a cluster (each CTA then sums only a share of a row's keys).
-  bool split = csize > 1;
+  bool split = false;
+  if (kCluster) split = true;
 #pragma unroll
   for (int tok = 0; tok < kTcTokens; ++tok) split |= (tok < n_act) && (kcnt[tok] < kSplitKeys);
   {
@@ -335,10 +339,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // `rank` takes items [it0, it1) of the tile's nit_all.
   const int nu_all = scan[15];
   const int nit_all = (nu_all + 1) / 2;
-  const int it0 = rank * nit_all / csize, it1 = (rank + 1) * nit_all / csize;
-  const int ubase = 2 * it0;
-  const int nu = max(0, min(nu_all, 2 * it1) - ubase);   // this CTA's union slots ubase .. ubase + nu - 1
-  const int nit = it1 - it0;
+  const int it0 = kCluster ? rank * nit_all / csize : 0;
+  const int it1 = kCluster ? (rank + 1) * nit_all / csize : nit_all;
+  const int ubase = kCluster ? 2 * it0 : 0;
+  const int nu = kCluster ? max(0, min(nu_all, 2 * it1) - ubase) : nu_all;   // slots ubase .. ubase + nu - 1
+  const int nit = kCluster ? it1 - it0 : nit_all;
   const uint32_t q_s = smem_u32(smem + lay.q);
   const uint32_t kv_s = smem_u32(smem + lay.kv);
   const uint32_t vv_s = smem_u32(smem + lay.vv);
@@ -606,9 +611,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     xch[half * 128 + r] = l_run;
     pair_sync(quad);
     const float l_row = l_run + xch[(half ^ 1) * 128 + r];
-    m_fin = m_run;
-    l_fin = l_row;
-    if (csize == 1) {   // (in a cluster the partial rows are merged below)
+    if (kCluster) {
+      m_fin = m_run;
+      l_fin = l_row;
+    } else {   // (in a cluster the partial rows are merged below)
       const float inv = (l_row > 0.f) ? 1.f / l_row : 0.f;
       __nv_bfloat16* orow = p.out + ((static_cast<size_t>(b) * p.nq + t0 + tok) * Hq + h * kGroup + (r & 15)) * kHeadDim;
 #pragma unroll 1
@@ -639,7 +645,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   }
 
-  if (csize > 1) {
+  if (kCluster) {
     // ---- cluster merge: row r of the tile is finished by CTA r % C ----
     // Each CTA's partial row (O relative to its running max m, and the row
     // sum l) goes into the owner's K ring, free once every CTA is past its
@@ -729,8 +735,11 @@ int tc_active_clusters(int C) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (!done[dev]) {
     const bool ok =
-        cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcMaxSmem) == cudaSuccess &&
-        cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+        cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcMaxSmem) ==
+            cudaSuccess &&
+        cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcMaxSmem) ==
+            cudaSuccess &&
+        cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
     for (int c = 1; c <= 16; ++c) {
       int n = 0;
       if (ok) {
@@ -745,7 +754,7 @@ int tc_active_clusters(int C) {
         a[0].val.clusterDim.z = 1;
         cfg.attrs = a;
         cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel, &cfg) != cudaSuccess) n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<true>, &cfg) != cudaSuccess) n = 0;
       }
       cache[dev][c] = n;
     }
@@ -801,7 +810,8 @@ cudaError_t launch_attn_tc(const Shape& s, const CUtensorMap& q_map, const CUten
   attrs[0].val.clusterDim.z = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = p.csize > 1 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, attn_tc_kernel, q_map, k_map, v_map, p);
+  return p.csize > 1 ? cudaLaunchKernelEx(&cfg, attn_tc_kernel<true>, q_map, k_map, v_map, p)
+                     : cudaLaunchKernelEx(&cfg, attn_tc_kernel<false>, q_map, k_map, v_map, p);
 }
 
 }  // namespace infllmv2

@@ -22,12 +22,13 @@
 //   phase A   hi/lo chunks streamed by TMA through a 4-stage ring (the rest
 //             of the CTA's chunks head for L2 at once); z = score_scale
 //             q . Mean on the tensor cores (8 warps), kept in shared memory.
-//   LSE       per-warp maxima, exp2(z - max) in place, per-warp sums merged
-//             into the CTA's (max, sum) per head, which is pushed into every
-//             CTA of the cluster; after one cluster barrier each CTA merges
-//             the C partials itself -> exact lse per head.
+//   LSE       phase A already stores exp2(z - m) with m the running max of
+//             the warp's row and keeps the row sums, so the warps' (max, sum)
+//             merge at once into the CTA's per head, which is pushed into
+//             every CTA of the cluster; after one cluster barrier each CTA
+//             merges the C partials itself -> exact lse per head.
 //   phase B   g = (1/16) sum_h exp2(z - lse_h) from the stored exponentials
-//             and one weight per (warp, head); block maxima of the CTA's
+//             and one weight per (chunk, warp, head); block maxima of the CTA's
 //             blocks, pushed into every CTA together with a summary (the
 //             g of the CTA's last kernel, which the next CTA's first block
 //             also meets; the count and best score of its candidates).  The
@@ -107,7 +108,7 @@ constexpr uint32_t kTestWithholdArrive = 0x1u;
 // Shared memory after the region (fixed sizes: the footprint, and with it
 // the cluster occupancy, does not depend on the shape).
 struct DsLayout {
-  int q, lse_in, summ, o_in, ml_in, wpart, cpart, lse, wtab, sel, nsel, warp_ml, wgt, bar, total;
+  int q, lse_in, summ, o_in, ml_in, wpart, cpart, lse, sel, nsel, warp_ml, wgt, bar, total;
 };
 
 __host__ __device__ constexpr DsLayout ds_layout() {
@@ -120,8 +121,7 @@ __host__ __device__ constexpr DsLayout ds_layout() {
   l.wpart = l.ml_in + kDsOutRows * 8;              // [8 warps][16 heads] (max, sum)
   l.cpart = l.wpart + kDsAWarps * kGroup * 8;      // [16] CTA (max, sum)
   l.lse = l.cpart + kGroup * 8;                    // [16] lse per head (base 2)
-  l.wtab = l.lse + kGroup * 4;                     // [8 warps][16 heads] exponential weights
-  l.sel = l.wtab + kDsAWarps * kGroup * 4;         // [kmax <= 256] ascending, -1 padded
+  l.sel = l.lse + kGroup * 4;                      // [kmax <= 256] ascending, -1 padded
   l.nsel = l.sel + 256 * 4;
   l.warp_ml = l.nsel + 16;                         // [12 warps][16 heads] attention (max, sum)
   l.wgt = l.warp_ml + kDsWarps * kGroup * 8;       // [12 warps][16 heads] merge weights, then [16][16]
@@ -131,6 +131,10 @@ __host__ __device__ constexpr DsLayout ds_layout() {
 }
 
 constexpr int kDsSmem = ds_layout().total + 1024;   // + 1024-byte alignment slack
+// Phase A's running maxima per (chunk, warp, head), turned into phase B's
+// weights, lie over the merge's partial-O rows (written only after the
+// cluster barrier that follows phase B).
+static_assert(kDsMaxIt * kDsAWarps * kGroup <= kDsOutRows * kHeadDim, "weight table inside o_in");
 static_assert(kDsSmem <= 227 * 1024, "one CTA per SM");
 
 __host__ __device__ inline int ds_per(int groups, int C) { return (groups + C - 1) / C; }
@@ -184,7 +188,7 @@ __global__ void __launch_bounds__(kDsThreads, 1)
   float2* wpart = reinterpret_cast<float2*>(smem + lay.wpart);
   float2* cpart = reinterpret_cast<float2*>(smem + lay.cpart);
   float* lse2 = reinterpret_cast<float*>(smem + lay.lse);
-  float* wtab = reinterpret_cast<float*>(smem + lay.wtab);
+  float* mch = reinterpret_cast<float*>(smem + lay.o_in);            // [chunk][warp][head] (over o_in)
   int32_t* selS = reinterpret_cast<int32_t*>(smem + lay.sel);
   int32_t* nselS = reinterpret_cast<int32_t*>(smem + lay.nsel);
   float2* warp_ml = reinterpret_cast<float2*>(smem + lay.warp_ml);
@@ -318,9 +322,12 @@ __global__ void __launch_bounds__(kDsThreads, 1)
   }
 
   const uint32_t q_b = smem_u32(smem + lay.q);
-  // z (then exp2(z - warp max)) of chunk it, head h, kernel x of the chunk:
-  // zs[(it * 16 + h) * 64 + x].
-  float mx0 = -INFINITY, mx1 = -INFINITY;   // this warp's max of heads g and g + 8
+  // exp2(z - m) of chunk it, head h, kernel x of the chunk:
+  // zs[(it * 16 + h) * 64 + x], with m the running max of the warp's row of
+  // head h up to that chunk, kept in mch[(it * 8 + warp) * 16 + h].  The
+  // rows' (max, sum) are thus ready when the last chunk is scored.
+  float m0r = -INFINITY, m1r = -INFINITY;   // running max of this warp's rows of heads g and g + 8
+  float ls0 = 0.f, ls1 = 0.f;                 // this thread's sums of exp2(z - running max)
   if (warp < kDsAWarps) {
     uint32_t a[8][4];
     load_q_frags(a, q_b, lane);
@@ -344,12 +351,39 @@ __global__ void __launch_bounds__(kDsThreads, 1)
         z1 = v1 ? acc[1] * p.score_scale2 : -INFINITY;
         z2 = v0 ? acc[2] * p.score_scale2 : -INFINITY;
         z3 = v1 ? acc[3] * p.score_scale2 : -INFINITY;
-        mx0 = fmaxf(mx0, fmaxf(z0, z1));
-        mx1 = fmaxf(mx1, fmaxf(z2, z3));
       }
+      float c0 = fmaxf(z0, z1), c1 = fmaxf(z2, z3);
+#pragma unroll
+      for (int o = 1; o <= 2; o <<= 1) {   // the row's 8 kernels of this chunk (4 tq lanes)
+        c0 = fmaxf(c0, __shfl_xor_sync(0xffffffffu, c0, o));
+        c1 = fmaxf(c1, __shfl_xor_sync(0xffffffffu, c1, o));
+      }
+      const float n0 = fmaxf(m0r, c0), n1 = fmaxf(m1r, c1);
+      if (n0 > -INFINITY) {
+        ls0 *= fast_exp2(m0r - n0);
+        z0 = fast_exp2(z0 - n0);
+        z1 = fast_exp2(z1 - n0);
+        ls0 += z0 + z1;
+      } else {
+        z0 = z1 = 0.f;
+      }
+      if (n1 > -INFINITY) {
+        ls1 *= fast_exp2(m1r - n1);
+        z2 = fast_exp2(z2 - n1);
+        z3 = fast_exp2(z3 - n1);
+        ls1 += z2 + z3;
+      } else {
+        z2 = z3 = 0.f;
+      }
+      m0r = n0;
+      m1r = n1;
       float* zrow = zs + (it * kGroup + g) * kDsChunk + warp * 8 + 2 * tq;
       *reinterpret_cast<float2*>(zrow) = make_float2(z0, z1);
       *reinterpret_cast<float2*>(zrow + 8 * kDsChunk) = make_float2(z2, z3);
+      if (tq == 0) {
+        mch[(it * kDsAWarps + warp) * kGroup + g] = n0;
+        mch[(it * kDsAWarps + warp) * kGroup + g + 8] = n1;
+      }
       __syncwarp();
 #ifdef INFLLMV2_CHECKED
       if ((p.test_flags & kTestWithholdArrive) && warp == 0 && it == 0) continue;
@@ -386,37 +420,17 @@ __global__ void __launch_bounds__(kDsThreads, 1)
   }
 
   // --------------------------------------------------- LSE over the cluster --
-  // Row g holds head g, row g + 8 head g + 8; the four tq lanes share a row.
-  // Each thread turns its own z into exp2(z - warp max) in place.
+  // Row g holds head g, row g + 8 head g + 8; the four tq lanes share a row
+  // (and its running max) and sum their partial sums.
   if (warp < kDsAWarps) {
 #pragma unroll
     for (int o = 1; o <= 2; o <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-    }
-    float l0 = 0.f, l1 = 0.f;
-#pragma unroll 4
-    for (int it = 0; it < nmy; ++it) {
-      float2* z01 = reinterpret_cast<float2*>(zs + (it * kGroup + g) * kDsChunk + warp * 8 + 2 * tq);
-      float2* z23 = reinterpret_cast<float2*>(reinterpret_cast<float*>(z01) + 8 * kDsChunk);
-      float2 u = *z01, w = *z23;
-      u.x = (mx0 == -INFINITY) ? 0.f : fast_exp2(u.x - mx0);
-      u.y = (mx0 == -INFINITY) ? 0.f : fast_exp2(u.y - mx0);
-      w.x = (mx1 == -INFINITY) ? 0.f : fast_exp2(w.x - mx1);
-      w.y = (mx1 == -INFINITY) ? 0.f : fast_exp2(w.y - mx1);
-      *z01 = u;
-      *z23 = w;
-      l0 += u.x + u.y;
-      l1 += w.x + w.y;
-    }
-#pragma unroll
-    for (int o = 1; o <= 2; o <<= 1) {
-      l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+      ls0 += __shfl_xor_sync(0xffffffffu, ls0, o);
+      ls1 += __shfl_xor_sync(0xffffffffu, ls1, o);
     }
     if (tq == 0) {
-      wpart[warp * kGroup + g] = make_float2(mx0, l0);
-      wpart[warp * kGroup + g + 8] = make_float2(mx1, l1);
+      wpart[warp * kGroup + g] = make_float2(m0r, ls0);
+      wpart[warp * kGroup + g + 8] = make_float2(m1r, ls1);
     }
   }
   ok = __syncthreads_and(ok);
@@ -446,10 +460,11 @@ __global__ void __launch_bounds__(kDsThreads, 1)
   __syncthreads();
 
   // ------------------------------------------------------------ phase B --
-  // Weight of warp w's exponentials of head h: exp2(max_wh - lse_h) / 16.
-  if (warp < kDsAWarps && tq == 0) {
-    wtab[warp * kGroup + g] = (mx0 == -INFINITY) ? 0.f : fast_exp2(mx0 - lse2[g]) * (1.0f / kGroup);
-    wtab[warp * kGroup + g + 8] = (mx1 == -INFINITY) ? 0.f : fast_exp2(mx1 - lse2[g + 8]) * (1.0f / kGroup);
+  // Weight of the exponentials of (chunk, warp, head h): exp2(m - lse_h) / 16
+  // with m the running max they were taken against.
+  for (int e = tid; e < nmy * kDsAWarps * kGroup; e += kDsThreads) {
+    const float m = mch[e];
+    mch[e] = (m == -INFINITY) ? 0.f : fast_exp2(m - lse2[e % kGroup]) * (1.0f / kGroup);
   }
   __syncthreads();
   // g of every kernel of this CTA's chunks (kernel x of a chunk came from warp x / 8).
@@ -457,7 +472,7 @@ __global__ void __launch_bounds__(kDsThreads, 1)
   for (int k = tid; k < nmy * kDsChunk; k += kDsThreads) {
     const int it = k / kDsChunk, x = k % kDsChunk;
     const float* zc = zs + it * kGroup * kDsChunk + x;
-    const float* wt = wtab + (x >> 3) * kGroup;
+    const float* wt = mch + (it * kDsAWarps + (x >> 3)) * kGroup;
     float acc = 0.f;
 #pragma unroll
     for (int hh = 0; hh < kGroup; ++hh) acc += zc[hh * kDsChunk] * wt[hh];
