@@ -28,14 +28,15 @@
 //             every CTA of the cluster; after one cluster barrier each CTA
 //             merges the C partials itself -> exact lse per head.
 //   phase B   g = (1/16) sum_h exp2(z - lse_h) from the stored exponentials
-//             and one weight per (chunk, warp, head); block maxima of the CTA's
-//             blocks, pushed into every CTA together with a summary (the
-//             g of the CTA's last kernel, which the next CTA's first block
-//             also meets; the count and best score of its candidates).  The
-//             CTA's likeliest blocks head for L2.  One cluster barrier.
-//   top-k     every CTA holds every block score and runs the same exact
-//             top-k (its first pass replaced by the summaries), so the
-//             selection needs no broadcast; CTA 0 writes it.
+//             and one weight per (chunk, warp, head); block maxima of the
+//             CTA's blocks; its candidates ranked among themselves.
+//   top-k     each CTA sends every CTA one message (bulk copy, counted on
+//             the receiver's mbarrier): its best n_take keys (score, then
+//             index) sorted, its first block's partial score and its last
+//             kernel's g; each CTA ranks its own entries against all the
+//             lists (binary searches) and sends its winners as a bit mask
+//             (st.async, a second mbarrier); every CTA assembles the same
+//             ascending selection, which CTA 0 writes.
 //   attend    the selected blocks rank, rank + C, ... are dealt to six warp
 //             pairs; a pair TMA-loads one block's K and V tiles (32 KB) into
 //             its stage, and each warp of the pair takes 32 of its keys:
@@ -45,8 +46,11 @@
 //   merge     warps merge in shared memory; each head's CTA partial is
 //             pushed to the CTA that writes the head (head h: CTA h mod C),
 //             which, after one cluster barrier, merges the C partials.
-// Every remote access is a store issued before a cluster barrier; after the
-// last barrier a CTA only reads its own shared memory, so it may exit.
+// Every remote access (a store, a bulk copy or an st.async) is complete
+// before the last cluster barrier: the stores are released by a barrier
+// arrive, the copies and st.async land before their receivers' mbarrier
+// waits end.  After the last barrier a CTA only reads its own shared
+// memory, so it may exit.
 #include "compress.cuh"
 #include "select_common.cuh"
 
@@ -70,16 +74,31 @@ constexpr int kDsOutRows = 32;        // C * ceil(16 / C) <= 30 partial rows a C
 constexpr int kDsMaxBlocks = 4096;    // block scores over the region's first 16 KB
 constexpr int kDsGbufOff = 65536;     // g of the CTA's kernels: in the ring, after the phase
 constexpr int kDsRmineOff = kDsGbufOff + kDsMaxIt * kDsChunk * 4;
-constexpr int kDsTkOff = kDsZOff;     // top-k scratch over the phase-A scores
+constexpr int kDsListMax = 256;       // best candidates a CTA sends (n_take <= k_max <= 256)
+constexpr int kDsMsgBytes = 16 + kDsListMax * 8;   // a CTA's message: DsSummary, then its sorted keys
+constexpr int kDsRecvOff = 0;         // [C][kDsMsgBytes] the messages of every CTA (the ring is idle by then)
+constexpr int kDsLkeyOff = kDsRmineOff + 16 * kDsMaxIt * 4;   // this CTA's candidate keys
+constexpr int kDsSendOff = kDsLkeyOff + 16 * kDsMaxIt * 8;    // this CTA's message
+constexpr int kDsMaskWords = 12;      // a CTA's blocks in selection words (16 kDsMaxIt blocks from a 16-aligned start)
+// Selection bits [128 words], first-block keys [16], counters [16], this
+// CTA's winners [12 words], the winners of every CTA [16][12 words].
+constexpr int kDsSelOff = kDsSendOff + kDsMsgBytes;
+constexpr int kDsBkeyOff = kDsSelOff + kDsMaxBlocks / 8;
+constexpr int kDsCtrOff = kDsBkeyOff + kDsMaxC * 8;
+constexpr int kDsRmaskOff = kDsCtrOff + 16 * 4;
+constexpr int kDsMinOff = kDsRmaskOff + 64;
+constexpr int kDsCntOff = kDsMinOff + kDsMaxC * kDsMaskWords * 4;   // larger keys per own entry [257]
 static_assert(kDsMaxIt >= 16, "16 chunks per CTA");
-static_assert(kDsRmineOff + 16 * kDsMaxIt * 4 <= kDsZOff, "phase-B buffers inside the ring");
-static_assert(kDsMaxBlocks * 4 <= kDsGbufOff, "block scores ahead of the phase-B buffers");
+static_assert(kDsMsgBytes % 16 == 0 && kDsSendOff % 16 == 0 && kDsMinOff % 16 == 0, "bulk copies and st.async");
+static_assert((16 * kDsMaxIt + 31) / 32 + 1 <= kDsMaskWords, "a CTA's blocks fit its mask");
+static_assert(kDsRecvOff + kDsMaxC * kDsMsgBytes <= kDsGbufOff, "messages ahead of the phase-B buffers");
+static_assert(kDsCntOff + (kDsListMax + 1) * 4 <= kDsZOff, "phase-B buffers inside the ring");
 
 // Pushed per CTA before the second barrier.
 struct DsSummary {
   float tail;         // g of the CTA's last kernel (-inf if it has none)
-  uint32_t lead;      // best topk_lead over its candidate blocks (0 if none)
-  int n_cand;         // its candidate blocks (finite, not forced)
+  float first;        // score of its first block without the kernel before it (-inf if none)
+  int n_list;         // candidates in its sorted list (its first block excluded)
   int pad;
 };
 
@@ -103,20 +122,21 @@ struct DsParams {
 // bounded wait for that stage expires (TIMEOUT), no later chunk is issued,
 // and the phase-A warps' waits for those chunks expire too; every copy that
 // was issued has landed before the CTA moves on.
+#ifdef INFLLMV2_CHECKED
 constexpr uint32_t kTestWithholdArrive = 0x1u;
+#endif
 
 // Shared memory after the region (fixed sizes: the footprint, and with it
 // the cluster occupancy, does not depend on the shape).
 struct DsLayout {
-  int q, lse_in, summ, o_in, ml_in, wpart, cpart, lse, sel, nsel, warp_ml, wgt, bar, total;
+  int q, lse_in, o_in, ml_in, wpart, cpart, lse, sel, nsel, warp_ml, wgt, bar, total;
 };
 
 __host__ __device__ constexpr DsLayout ds_layout() {
   DsLayout l{};
   l.q = kDsRegion;                                 // 16 rows x 256 B, two swizzled boxes
   l.lse_in = l.q + 4096;                           // [16 CTAs][16 heads] (max, sum)
-  l.summ = l.lse_in + kDsMaxC * kGroup * 8;        // [16 CTAs] DsSummary
-  l.o_in = l.summ + kDsMaxC * 16;                  // [32 rows][128] partial O of the heads written here
+  l.o_in = l.lse_in + kDsMaxC * kGroup * 8;        // [32 rows][128] partial O of the heads written here
   l.ml_in = l.o_in + kDsOutRows * kHeadDim * 4;    // [32 rows] their (max, sum)
   l.wpart = l.ml_in + kDsOutRows * 8;              // [8 warps][16 heads] (max, sum)
   l.cpart = l.wpart + kDsAWarps * kGroup * 8;      // [16] CTA (max, sum)
@@ -126,7 +146,7 @@ __host__ __device__ constexpr DsLayout ds_layout() {
   l.warp_ml = l.nsel + 16;                         // [12 warps][16 heads] attention (max, sum)
   l.wgt = l.warp_ml + kDsWarps * kGroup * 8;       // [12 warps][16 heads] merge weights, then [16][16]
   l.bar = l.wgt + 16 * 16 * 4;
-  l.total = l.bar + (2 * kDsRing + 1 + kDsPairs) * 8;
+  l.total = l.bar + (2 * kDsRing + 1 + kDsPairs + 2) * 8;
   return l;
 }
 
@@ -178,11 +198,18 @@ __global__ void __launch_bounds__(kDsThreads, 1)
   uint8_t* smem = align1024(smem_raw);
   constexpr DsLayout lay = ds_layout();
   float* zs = reinterpret_cast<float*>(smem + kDsZOff);              // [it][16 heads][64]
-  float* rfull = reinterpret_cast<float*>(smem);                     // [nb] every block score
   float* gbuf = reinterpret_cast<float*>(smem + kDsGbufOff);         // g of this CTA's kernels
-  float* rmine = reinterpret_cast<float*>(smem + kDsRmineOff);       // this CTA's block scores
+  float* rmine = reinterpret_cast<float*>(smem + kDsRmineOff);       // this CTA's first block score
+  uint8_t* recv = smem + kDsRecvOff;                                 // [C][kDsMsgBytes] messages
+  uint8_t* send = smem + kDsSendOff;                                 // this CTA's message
+  unsigned long long* lkeys = reinterpret_cast<unsigned long long*>(smem + kDsLkeyOff);   // this CTA's candidates
+  uint32_t* sbits = reinterpret_cast<uint32_t*>(smem + kDsSelOff);                        // [128] selected blocks
+  unsigned long long* bkeys = reinterpret_cast<unsigned long long*>(smem + kDsBkeyOff);   // [C] first blocks
+  int* sctr = reinterpret_cast<int*>(smem + kDsCtrOff);              // [0] n_loc, [4..16) warp sums
+  uint32_t* rmask = reinterpret_cast<uint32_t*>(smem + kDsRmaskOff);                      // this CTA's winners
+  uint32_t* minbox = reinterpret_cast<uint32_t*>(smem + kDsMinOff);                      // [C][12] every CTA's
+  int* ecnt = reinterpret_cast<int*>(smem + kDsCntOff);              // [n_list + 1] larger keys per own entry
   float2* lse_in = reinterpret_cast<float2*>(smem + lay.lse_in);     // [C][16]
-  DsSummary* summ = reinterpret_cast<DsSummary*>(smem + lay.summ);   // [C]
   float* o_in = reinterpret_cast<float*>(smem + lay.o_in);           // [C * hmax][128]
   float2* ml_in = reinterpret_cast<float2*>(smem + lay.ml_in);       // [C * hmax]
   float2* wpart = reinterpret_cast<float2*>(smem + lay.wpart);
@@ -197,6 +224,8 @@ __global__ void __launch_bounds__(kDsThreads, 1)
   uint64_t* empty = full + kDsRing;
   uint64_t* qbar = empty + kDsRing;
   uint64_t* kvfull = qbar + 1;
+  uint64_t* lbar = kvfull + kDsPairs;   // every CTA's message has landed
+  uint64_t* sbar = lbar + 1;            // every CTA's winners have landed
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, tq = lane & 3;
@@ -219,6 +248,8 @@ __global__ void __launch_bounds__(kDsThreads, 1)
     }
     mbar_init(qbar, 1);
     for (int s = 0; s < kDsPairs; ++s) mbar_init(&kvfull[s], 1);
+    mbar_init(lbar, 1);
+    mbar_init(sbar, 1);
     fence_barrier_init();
   }
   // Marks this CTA as running; the matching wait, before the first remote
@@ -262,6 +293,13 @@ __global__ void __launch_bounds__(kDsThreads, 1)
   const int local_lo = max(n_first, c - p.n_local + 1);
   const int n_forced = n_first + max(0, c - local_lo + 1);
   const int n_take = max(0, p.inc_forced ? p.topk - n_forced : p.topk);
+  // Power of two >= n_take (and >= 2, so that a message is a multiple of 16 bytes), <= 256.
+  const int list_pow = n_take <= 2 ? 2 : 1 << (32 - __clz(n_take - 1));
+  const uint32_t msg_bytes = 16 + list_pow * 8;   // a CTA's message to each CTA of the cluster
+  if (tid == 0) {   // (no CTA sends before the first cluster barrier, which comes later)
+    mbar_arrive_expect_tx(lbar, static_cast<uint32_t>(C) * msg_bytes);
+    mbar_arrive_expect_tx(sbar, static_cast<uint32_t>(C) * kDsMaskWords * 4);
+  }
 
   auto issue = [&](int it) {
     const int st = it % kDsRing;
@@ -466,6 +504,9 @@ __global__ void __launch_bounds__(kDsThreads, 1)
     const float m = mch[e];
     mch[e] = (m == -INFINITY) ? 0.f : fast_exp2(m - lse2[e % kGroup]) * (1.0f / kGroup);
   }
+  // (the ring is idle since phase A: the selection's buffers lie in it)
+  for (int w = tid; w < kDsMaxBlocks / 32; w += kDsThreads) sbits[w] = 0u;
+  if (tid == 0) sctr[0] = 0;
   __syncthreads();
   // g of every kernel of this CTA's chunks (kernel x of a chunk came from warp x / 8).
 #pragma unroll 1
@@ -479,120 +520,167 @@ __global__ void __launch_bounds__(kDsThreads, 1)
     gbuf[k] = acc;
   }
   __syncthreads();
-  // The top-k scratch lies over the scores, which are dead now.
-  // (the general routine's scratch, for the rare fallback, overlays it too)
-  FastTopkScratch<kDsThreads>& tk = *reinterpret_cast<FastTopkScratch<kDsThreads>*>(smem + kDsTkOff);
-  SmemTopkScratch<kDsThreads>& tk_slow = *reinterpret_cast<SmemTopkScratch<kDsThreads>*>(smem + kDsTkOff);
-  constexpr int kTkBytes = sizeof(SmemTopkScratch<kDsThreads>) > sizeof(FastTopkScratch<kDsThreads>)
-                               ? sizeof(SmemTopkScratch<kDsThreads>) : sizeof(FastTopkScratch<kDsThreads>);
-  uint32_t* tk_bits = reinterpret_cast<uint32_t*>(smem + kDsTkOff + ((kTkBytes + 15) & ~15));
-  unsigned long long* tk_surv = reinterpret_cast<unsigned long long*>(smem + kDsTkOff + ((kTkBytes + 15) & ~15) + 512);
-  topk_fast_clear<kDsThreads>(tk, tk_bits, nbt, tid);
+  // ------------------------------------------------------------- top-k --
+  // Candidates are the blocks n_first .. local_lo - 1 with a finite score,
+  // ordered by one 64-bit key: the score, then the lower index.  Each CTA
+  // sorts its own candidates (all but its first block, whose kernel before
+  // it was scored by the previous CTA) and sends every CTA one message: the
+  // g of its last kernel, its first block's partial score, and its best
+  // n_take keys, sorted and zero-padded (one bulk copy per CTA, counted on
+  // the receiver's mbarrier).  Once all C messages are in, each CTA
+  // completes the C first blocks and ranks its own entries by counting the
+  // larger keys of every list (binary searches); rank < n_take wins.  Its
+  // winners go to every CTA as a bit mask (st.async, a second mbarrier), and
+  // every CTA assembles the same selection.
   const int jb0 = 16 * k0, jb1 = min(16 * k1, nbt);
-  const int nv4 = (jb1 - jb0 + 3) / 4;   // the CTA's block scores as float4s (padded with -inf)
+  const int w0 = jb0 >> 5;   // first selection word of this CTA's blocks
+  unsigned long long* skeys = reinterpret_cast<unsigned long long*>(send + 16);
+  auto block_key = [](float r, int j) {
+    return (static_cast<unsigned long long>(float_to_ordered(r)) << 32) | static_cast<uint32_t>(~j);
+  };
+  auto msg_keys = [&](int q) { return reinterpret_cast<const unsigned long long*>(recv + q * kDsMsgBytes + 16); };
+  auto msg_summary = [&](int q) { return *reinterpret_cast<const DsSummary*>(recv + q * kDsMsgBytes); };
   {
     const int kb0 = kDsChunk * k0;
-    int my_cand = 0;
-    uint32_t my_lead = 0;
+    const int nrange = max(0, jb1 - jb0);
+    for (int x = tid; x < list_pow; x += kDsThreads) skeys[x] = 0ull;   // 0: below every key
+    for (int x = tid; x <= list_pow; x += kDsThreads) ecnt[x] = 0;
+    if (tid < kDsMaskWords) rmask[tid] = 0u;
+    // (the trip count is the same in every lane: the warp votes below)
 #pragma unroll 1
-    for (int j = jb0 + tid; j < jb0 + 4 * nv4; j += kDsThreads) {
+    for (int x0 = 0; x0 < nrange; x0 += kDsThreads) {
+      const int j = jb0 + x0 + tid;
       float r = -INFINITY;
       if (j < jb1) {
         const int a0 = max(4 * j - 1, kb0), e0 = min(nc - 1, 4 * j + 3);
         for (int k = a0; k <= e0; ++k) r = fmaxf(r, gbuf[k - kb0]);
+        if (j == jb0) rmine[0] = r;
       }
-      rmine[j - jb0] = r;
-      if (j >= n_first && j < local_lo && r > -INFINITY) {
-        ++my_cand;
-        my_lead = max(my_lead, topk_lead(r));
-      }
-    }
-    my_cand = __reduce_add_sync(0xffffffffu, my_cand);
-    my_lead = __reduce_max_sync(0xffffffffu, my_lead);
-    if (lane == 0) {
-      warp_ml[warp] = make_float2(__int_as_float(my_cand), __uint_as_float(my_lead));
+      const bool cand = j < jb1 && j > jb0 && j >= n_first && j < local_lo && r > -INFINITY;
+      const uint32_t bal = __ballot_sync(0xffffffffu, cand);
+      int base = 0;
+      if (lane == 0 && bal) base = atomicAdd(&sctr[0], __popc(bal));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      if (cand) lkeys[base + __popc(bal & ((1u << lane) - 1u))] = block_key(r, j);
     }
   }
   __syncthreads();
-  // Push the block scores and the summary into every CTA.
+  const int n_list = min(sctr[0], n_take);
+  {
+    const int n_loc = sctr[0];
+    const int n_pf = ds_prefetch_count(n_take, C);
+    // Two threads per key, each comparing it with half of the keys.
+    const int part = tid & 1;
 #pragma unroll 1
-  for (int e = tid; e < C * nv4; e += kDsThreads) {
-    const int dst = e / nv4, x = e % nv4;
-    st_dsmem_f32x4(dsmem_addr(rfull + jb0 + 4 * x, dst), reinterpret_cast<const float4*>(rmine)[x]);
+    for (int x0 = 0; x0 < n_loc; x0 += kDsThreads / 2) {   // (same trip count in every lane)
+      const int x = x0 + (tid >> 1);
+      const unsigned long long me = x < n_loc ? lkeys[x] : 0ull;
+      int rk = 0;
+#pragma unroll 4
+      for (int y = part; y < n_loc; y += 2) rk += lkeys[y] > me ? 1 : 0;
+      rk += __shfl_xor_sync(0xffffffffu, rk, 1);
+      if (part == 0 && x < n_loc && rk < n_list) {
+        skeys[rk] = me;
+        // The CTA's likeliest winners head for L2 while the selection is made.
+        if (rk < n_pf) prefetch_block(&k_map, &v_map, kv_row0 + static_cast<int>(~static_cast<uint32_t>(me)) * kBlock);
+      }
+    }
+    if (tid == 0) {
+      const float gl = (k1 > k0 && kDsChunk * k1 - 1 < nc) ? gbuf[kDsChunk * (k1 - k0) - 1] : -INFINITY;
+      const float first = jb0 < jb1 ? rmine[0] : -INFINITY;
+      *reinterpret_cast<float4*>(send) = make_float4(gl, first, __int_as_float(n_list), 0.f);
+    }
   }
+  fence_proxy_async_smem();   // the message is read by the bulk copies
+  __syncthreads();
+  if (tid < C)
+    bulk_copy_to_cta(dsmem_addr(recv + rank * kDsMsgBytes, static_cast<uint32_t>(tid)), send, msg_bytes,
+                     dsmem_addr(lbar, static_cast<uint32_t>(tid)));
+  // (waited for even after an earlier timeout: no copy may still be landing later)
+  ok = __syncthreads_and(mbar_wait_cluster(lbar, 0, p.status)) && ok;
+  // First block of CTA q (16 per q), completed with CTA q - 1's last kernel.
   if (tid < C) {
-    int cnt = 0;
-    uint32_t lead = 0;
-    for (int w = 0; w < kDsWarps; ++w) {
-      cnt += __float_as_int(warp_ml[w].x);
-      lead = max(lead, __float_as_uint(warp_ml[w].y));
+    const int q = tid, j = 16 * per * q;
+    unsigned long long key = 0ull;   // 0: not a candidate (every candidate's key is larger)
+    if (j < nbt) {
+      float r = msg_summary(q).first;
+      if (q > 0) r = fmaxf(r, msg_summary(q - 1).tail);
+      if (j >= n_first && j < local_lo && r > -INFINITY) key = block_key(r, j);
     }
-    const float gl = (k1 > k0 && kDsChunk * k1 - 1 < nc) ? gbuf[kDsChunk * (k1 - k0) - 1] : -INFINITY;
-    st_dsmem_f32x4(dsmem_addr(&summ[rank], tid),
-                   make_float4(gl, __uint_as_float(lead), __int_as_float(cnt), 0.f));
+    bkeys[q] = key;
   }
-  if (warp == 9) {
-    // The CTA's likeliest winners head for L2 while the selection is made:
-    // its best few candidate blocks by score.
-    const int n_pf = min(ds_prefetch_count(n_take, C), jb1 - jb0);
-    uint32_t key[4];
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      const int j = jb0 + lane + 32 * x;
-      const bool cand = j < jb1 && j >= n_first && j < local_lo && rmine[lane + 32 * x] > -INFINITY;
-      key[x] = cand ? ((topk_lead(rmine[lane + 32 * x]) << 12) | static_cast<uint32_t>(4095 - (lane + 32 * x))) : 0u;
-    }
-    // (a CTA owns at most 16 kDsMaxIt blocks; those past 128 are not prefetched)
+  for (int j = tid; j < n_first; j += kDsThreads) atomicOr(&sbits[j >> 5], 1u << (j & 31));
+  for (int j = local_lo + tid; j <= c; j += kDsThreads) atomicOr(&sbits[j >> 5], 1u << (j & 31));
+  __syncthreads();
+  // This CTA's entries (its list, then its first block) against every list:
+  // thread e takes entry e / C and list e % C, a binary search over that
+  // sorted, zero-padded list (list 0's thread also counts the first blocks);
+  // the counts add up per entry.
+  if (n_take > 0) {
 #pragma unroll 1
-    for (int n = 0; n < n_pf; ++n) {
-      uint32_t best = max(max(key[0], key[1]), max(key[2], key[3]));
-      best = __reduce_max_sync(0xffffffffu, best);
-      if (best == 0u) break;
-      const int x = 4095 - static_cast<int>(best & 4095u);
-      if (lane == 0) prefetch_block(&k_map, &v_map, kv_row0 + (jb0 + x) * kBlock);
-#pragma unroll
-      for (int y = 0; y < 4; ++y)
-        if (key[y] == best) key[y] = 0u;
-    }
-  }
-  cluster_arrive();
-  cluster_wait();
-
-  // ------------------------------------------------------------- top-k --
-  // Block 16 per q starts CTA q's range; its kernel 64 per q - 1 was scored
-  // by CTA q - 1.  The candidate count and the best leading bits follow.
-  if (warp == 0) {   // lane q < C: CTA q's summary and the block its tail meets
-    int n_cand = 0;
-    uint32_t lead = 0;
-    if (lane < C) {
-      const DsSummary sq = summ[lane];
-      n_cand = sq.n_cand;
-      lead = sq.lead;
-      const int j = 16 * per * (lane + 1);
-      if (lane + 1 < C && j < nbt && sq.tail > -INFINITY) {
-        const float before = rfull[j];
-        const float after = fmaxf(before, sq.tail);
-        rfull[j] = after;
-        if (j >= n_first && j < local_lo) {
-          n_cand += (before == -INFINITY) ? 1 : 0;
-          lead = max(lead, topk_lead(after));
-        }
-      }
-    }
-    n_cand = __reduce_add_sync(0xffffffffu, n_cand);
-    lead = __reduce_max_sync(0xffffffffu, lead);
-    if (lane == 0) {
-      nselS[1] = n_cand;
-      nselS[2] = static_cast<int>(lead);
+    for (int e = tid; e < (n_list + 1) * C; e += kDsThreads) {
+      const int x = e / C, q2 = e % C;
+      const unsigned long long k = x < n_list ? msg_keys(rank)[x] : bkeys[rank];
+      if (k == 0ull) continue;
+      const unsigned long long* l2 = msg_keys(q2);
+      int pos = 0;
+#pragma unroll 1
+      for (int step = list_pow >> 1; step >= 1; step >>= 1)
+        if (l2[pos + step - 1] > k) pos += step;
+      pos += l2[pos] > k ? 1 : 0;
+      if (q2 == 0)
+        for (int q = 0; q < C; ++q) pos += bkeys[q] > k ? 1 : 0;
+      atomicAdd(&ecnt[x], pos);
     }
   }
   __syncthreads();
-  select_topk_fast<kDsThreads>(rfull, nbt, p.n_init, p.n_local, p.topk, p.inc_forced != 0, p.kmax, selS, nselS, tk,
-                               tk_bits, tk_surv, tid, nselS[1], static_cast<uint32_t>(nselS[2]), tk_slow);
+  if (n_take > 0 && tid <= n_list) {
+    const unsigned long long k = tid < n_list ? msg_keys(rank)[tid] : bkeys[rank];
+    if (k != 0ull && ecnt[tid] < n_take) {
+      const int j = static_cast<int>(~static_cast<uint32_t>(k));
+      atomicOr(&rmask[(j >> 5) - w0], 1u << (j & 31));
+    }
+  }
+  __syncthreads();
+  if (tid < C) {   // this CTA's winners (words w0 ..) into CTA tid
+    const uint32_t dst = dsmem_addr(minbox + rank * kDsMaskWords, static_cast<uint32_t>(tid));
+    const uint32_t bar = dsmem_addr(sbar, static_cast<uint32_t>(tid));
+#pragma unroll
+    for (int x = 0; x < kDsMaskWords / 4; ++x)
+      st_async_u32x4(dst + 16 * x, make_uint4(rmask[4 * x], rmask[4 * x + 1], rmask[4 * x + 2], rmask[4 * x + 3]), bar);
+  }
+  ok = __syncthreads_and(mbar_wait_cluster(sbar, 0, p.status)) && ok;
+  for (int e = tid; e < C * kDsMaskWords; e += kDsThreads) {
+    const int q = e / kDsMaskWords, w = ((16 * per * q) >> 5) + e % kDsMaskWords;
+    const uint32_t v = minbox[e];
+    if (v != 0u && w < kDsMaxBlocks / 32) atomicOr(&sbits[w], v);
+  }
+  __syncthreads();
+  {
+    // Ascending list: word w's set bits go to positions [prefix(w), ...).
+    const int n_words = (nbt + 31) / 32;   // <= kDsMaxBlocks / 32 <= kDsThreads
+    const uint32_t bw = tid < n_words ? sbits[tid] : 0u;
+    const int cnt = __popc(bw);
+    const int incl = warp_inclusive_scan(cnt);
+    if (lane == 31) sctr[4 + warp] = incl;
+    __syncthreads();
+    int pos = incl - cnt;
+#pragma unroll
+    for (int w = 0; w < kDsWarps; ++w) pos += (w < warp) ? sctr[4 + w] : 0;
+    if (tid == kDsThreads - 1) nselS[0] = min(pos + cnt, p.kmax);
+    uint32_t rest = bw;
+    while (rest) {
+      const int j = tid * 32 + __ffs(rest) - 1;
+      rest &= rest - 1u;
+      if (pos < p.kmax) selS[pos] = j;
+      ++pos;
+    }
+  }
   __syncthreads();
   const int nsel = nselS[0];
   if (rank == 0) {
-    for (int e = tid; e < p.kmax; e += kDsThreads) p.block_idx[static_cast<size_t>(bh) * p.kmax + e] = selS[e];
+    for (int e = tid; e < p.kmax; e += kDsThreads)
+      p.block_idx[static_cast<size_t>(bh) * p.kmax + e] = e < nsel ? selS[e] : -1;
     if (tid == 0) p.n_sel[bh] = nsel;
   }
   if (tid == 32)   // blocks of the second and later rounds: into L2 now

@@ -521,28 +521,10 @@ __device__ __forceinline__ int smem_topk_boundary(SmemTopkScratch<NT>& sm, int n
   return sm.ctrl[0];
 }
 
-// Clear the scratch select_topk_smem needs when it is given the candidate
-// count and best leading bits (known_cand >= 0); the caller synchronises
-// before the selection starts.
-template <int NT>
-__device__ __forceinline__ void topk_smem_clear(SmemTopkScratch<NT>& sm, uint32_t* bits, int nb, int tid) {
-  for (int b = tid; b < (NT / 32) * 256; b += NT) (&sm.hist[0][0])[b] = 0u;
-  for (int w = tid; w < (nb + 31) / 32; w += NT) bits[w] = 0u;
-  if (tid == 0) sm.ctrl[2] = 0;
-}
-
-// Leading bits of a score as select_topk_smem bins them (a key with larger
-// leading bits scores higher).
-__device__ __forceinline__ uint32_t topk_lead(float x) { return float_to_ordered(x) >> 17; }
-
-// known_cand >= 0: the caller supplies the number of candidates (non-forced
-// blocks with a finite score) and an upper bound known_top >= topk_lead of
-// every candidate, and has run topk_smem_clear; the first pass is skipped.
 template <int NT>
 __device__ void select_topk_smem(const float* r, int nb, int n_init, int n_local, int topk, bool includes_forced,
                                  int k_max, int32_t* out_idx, int32_t* out_n, SmemTopkScratch<NT>& sm,
-                                 uint32_t* bits, unsigned long long* surv, int tid, int32_t* sorted_copy = nullptr,
-                                 int known_cand = -1, uint32_t known_top = 0) {
+                                 uint32_t* bits, unsigned long long* surv, int tid, int32_t* sorted_copy = nullptr) {
   static_assert(NT >= 256, "one thread per histogram bin");
   constexpr int NWARP = NT / 32;
   constexpr int kShift = 17;
@@ -552,9 +534,9 @@ __device__ void select_topk_smem(const float* r, int nb, int n_init, int n_local
   const int local_lo = max(n_first, c - n_local + 1);
   const int n_words = (nb + 31) / 32;
   auto is_cand = [&](int j, float x) { return j >= n_first && j < local_lo && x > -INFINITY; };
-  int n_cand = known_cand;
-  uint32_t top = known_top;
-  if (known_cand < 0) {
+  int n_cand = 0;
+  uint32_t top = 0;
+  {
     // 1. candidates, their count and the best leading bits; clear the scratch.
     int my_cand = 0;
     uint32_t my_top = 0;
@@ -678,172 +660,5 @@ __device__ void select_topk_smem(const float* r, int nb, int n_init, int n_local
   }
 }
 
-
-// The same selection as select_topk_smem for NT threads (NT >= 256, a
-// multiple of 32) with every step spread over the whole CTA, for the fused
-// decode step where it sits on the critical path: two histogram levels
-// narrow the boundary to the few scores sharing the n_take-th best score's
-// leading 23 bits, which are ranked exactly by (score desc, index asc);
-// survivors are gathered with one atomic per warp; the ascending list comes
-// from a CTA-wide scan of the bitmask.  Needs nb <= 32 * NT.  The caller
-// gives the candidate count and an upper bound `top` on the candidates'
-// topk_lead (as select_topk_smem with known_cand), and must have run
-// topk_fast_clear before.  A boundary in the last (catch-all) first-level
-// bin falls back to select_topk_smem's second level.
-template <int NT>
-struct FastTopkScratch {
-  uint32_t hist[NT / 32][256];
-  int wtot[NT / 32];
-  int ctrl[8];   // 0: level-1 bin, 1: above it, 2: level-2 bin, 3: above it, 4: survivors, 5: total
-};
-
-template <int NT>
-__device__ __forceinline__ void topk_fast_clear(FastTopkScratch<NT>& sm, uint32_t* bits, int nb, int tid) {
-  for (int b = tid; b < (NT / 32) * 256; b += NT) (&sm.hist[0][0])[b] = 0u;
-  for (int w = tid; w < (nb + 31) / 32; w += NT) bits[w] = 0u;
-  if (tid < 8) sm.ctrl[tid] = 0;
-}
-
-// Bin (0 = best) holding the need-th best entry of the per-warp histograms,
-// and the count in better bins (ctrl[slot], ctrl[slot + 1]).  Re-zeroes the
-// histograms.  Two barriers.
-template <int NT>
-__device__ __forceinline__ void topk_fast_bin(FastTopkScratch<NT>& sm, int need, int tid, int slot) {
-  constexpr int NWARP = NT / 32;
-  const int lane = tid & 31, warp = tid >> 5;
-  int cnt = 0;
-  if (tid < 256) {
-#pragma unroll
-    for (int w = 0; w < NWARP; ++w) cnt += static_cast<int>(sm.hist[w][tid]);
-  }
-  const int incl = warp_inclusive_scan(cnt);
-  if (lane == 31) sm.wtot[warp] = incl;
-  __syncthreads();
-  int before = 0;
-#pragma unroll
-  for (int w = 0; w < NWARP; ++w) before += (w < warp) ? sm.wtot[w] : 0;
-  const int run = before + incl - cnt;
-  if (tid < 256 && run < need && run + cnt >= need) {
-    sm.ctrl[slot] = tid;
-    sm.ctrl[slot + 1] = run;
-  }
-  for (int b = lane; b < 256; b += 32) sm.hist[warp][b] = 0u;
-  __syncthreads();
-}
-
-template <int NT>
-__device__ void select_topk_fast(const float* r, int nb, int n_init, int n_local, int topk, bool includes_forced,
-                                 int k_max, int32_t* out_idx, int32_t* out_n, FastTopkScratch<NT>& sm,
-                                 uint32_t* bits, unsigned long long* surv, int tid, int n_cand, uint32_t top,
-                                 SmemTopkScratch<NT>& slow) {
-  const int lane = tid & 31, warp = tid >> 5;
-  const int c = nb - 1;
-  const int n_first = min(n_init, nb);
-  const int local_lo = max(n_first, c - n_local + 1);
-  const int n_forced = n_first + max(0, c - local_lo + 1);
-  const int n_take = max(0, includes_forced ? topk - n_forced : topk);
-  // Thread tid looks at j = tid + NT x; the trip count is the same in every
-  // lane (the loops below hold warp votes).
-  const int nv = (nb + NT - 1) / NT;
-  auto cand_key = [&](int x, uint32_t& key) {
-    const int j = tid + NT * x;
-    const float v = j < nb ? r[j] : -INFINITY;
-    key = float_to_ordered(v);
-    return j >= n_first && j < local_lo && v > -INFINITY;
-  };
-  if (n_take > 0 && n_take < n_cand) {
-    // Level 1: d1 = distance of the leading bits (sign, exponent, 6 mantissa
-    // bits) from `top`, the last bin catching everything further.
-#pragma unroll 1
-    for (int x = 0; x < nv; ++x) {
-      uint32_t key;
-      if (cand_key(x, key)) atomicAdd(&sm.hist[warp][min(255u, top - (key >> 17))], 1u);
-    }
-    __syncthreads();
-    topk_fast_bin<NT>(sm, n_take, tid, 0);
-    const int b1 = sm.ctrl[0], above1 = sm.ctrl[1];
-    if (b1 == 255) {
-      // Rare (the boundary lies more than four octaves below the best):
-      // the general routine, from its first pass.
-      select_topk_smem<NT>(r, nb, n_init, n_local, topk, includes_forced, k_max, out_idx, out_n, slow, bits, surv,
-                           tid);
-      return;
-    }
-    // Level 2: within bin b1 (one leading-bit value), the next 8 bits, best first.
-    const uint32_t lead1 = top - static_cast<uint32_t>(b1);
-#pragma unroll 1
-    for (int x = 0; x < nv; ++x) {
-      uint32_t key;
-      if (cand_key(x, key) && (key >> 17) == lead1) atomicAdd(&sm.hist[warp][255u - ((key >> 9) & 255u)], 1u);
-    }
-    __syncthreads();
-    topk_fast_bin<NT>(sm, n_take - above1, tid, 2);
-    const int b2 = sm.ctrl[2], above2 = sm.ctrl[3];
-    const uint32_t lead2 = (lead1 << 8) | (255u - static_cast<uint32_t>(b2));   // key >> 9 of the boundary
-    // Mark everything better than the boundary; gather the boundary scores.
-#pragma unroll 1
-    for (int x = 0; x < nv; ++x) {
-      uint32_t key;
-      const bool cand = cand_key(x, key);
-      const int j = tid + NT * x;
-      const bool better = cand && (key >> 9) > lead2;
-      const bool tie = cand && (key >> 9) == lead2;
-      if (better) atomicOr(&bits[j >> 5], 1u << (j & 31));
-      const uint32_t tw = __ballot_sync(0xffffffffu, tie);
-      int base = 0;
-      if (lane == 0 && tw) base = atomicAdd(&sm.ctrl[4], __popc(tw));
-      base = __shfl_sync(0xffffffffu, base, 0);
-      if (tie) surv[base + __popc(tw & ((1u << lane) - 1u))] =
-          (static_cast<unsigned long long>(key) << 32) | static_cast<uint32_t>(~j);
-    }
-    __syncthreads();
-    // The boundary scores that still fit, by exact rank among themselves.
-    const int m = sm.ctrl[4], need = n_take - above1 - above2;
-#pragma unroll 1
-    for (int x = tid; x < m; x += NT) {
-      const unsigned long long me = surv[x];
-      int rk = 0;
-#pragma unroll 4
-      for (int y = 0; y < m; ++y) rk += (surv[y] > me) ? 1 : 0;
-      if (rk < need) {
-        const int j = static_cast<int>(~static_cast<uint32_t>(me & 0xffffffffu));
-        atomicOr(&bits[j >> 5], 1u << (j & 31));
-      }
-    }
-  } else if (n_take > 0) {
-    // Every candidate fits.
-#pragma unroll 1
-    for (int x = 0; x < nv; ++x) {
-      uint32_t key;
-      const int j = tid + NT * x;
-      if (cand_key(x, key)) atomicOr(&bits[j >> 5], 1u << (j & 31));
-    }
-  }
-  for (int j = tid; j < n_first; j += NT) atomicOr(&bits[j >> 5], 1u << (j & 31));
-  for (int j = local_lo + tid; j <= c; j += NT) atomicOr(&bits[j >> 5], 1u << (j & 31));
-  __syncthreads();
-  // Ascending list: word w's set bits go to positions [prefix(w), ...).
-  const int n_words = (nb + 31) / 32;   // <= NT
-  const uint32_t bw = tid < n_words ? bits[tid] : 0u;
-  const int cnt = __popc(bw);
-  const int incl = warp_inclusive_scan(cnt);
-  if (lane == 31) sm.wtot[warp] = incl;
-  __syncthreads();
-  int pos = incl - cnt;
-#pragma unroll
-  for (int w = 0; w < NT / 32; ++w) pos += (w < warp) ? sm.wtot[w] : 0;
-  if (tid == NT - 1) sm.ctrl[5] = pos + cnt;
-  uint32_t rest = bw;
-  while (rest) {
-    const int j = tid * 32 + __ffs(rest) - 1;
-    rest &= rest - 1u;
-    if (pos < k_max) out_idx[pos] = j;
-    ++pos;
-  }
-  __syncthreads();
-  const int total = min(sm.ctrl[5], k_max);
-  for (int x = total + tid; x < k_max; x += NT) out_idx[x] = -1;
-  if (tid == 0) *out_n = total;
-}
 
 }  // namespace infllmv2
