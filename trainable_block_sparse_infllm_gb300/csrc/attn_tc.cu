@@ -230,6 +230,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int rank = kCluster ? static_cast<int>(blockIdx.x) % csize : 0;   // == the rank in the cluster
   const int t0 = kCluster ? (static_cast<int>(blockIdx.x) / csize) * kTcTokens : blockIdx.x * kTcTokens;
   const int n_act = min(kTcTokens, p.nq - t0);
+  pdl_wait();   // the previous kernel of the stream may still be writing the inputs
+  pdl_trigger();
   const int L = p.kv_lens[b];
 
   if (L < p.nq || L > p.Lmax) {   // the same in every CTA of a cluster: none touches another's memory
@@ -803,13 +805,17 @@ cudaError_t launch_attn_tc(const Shape& s, const CUtensorMap& q_map, const CUten
   cfg.blockDim = dim3(kTcThreads, 1, 1);
   cfg.dynamicSmemBytes = tc_layout(s.nbmax).total + 1024;
   cfg.stream = st;
-  cudaLaunchAttribute attrs[1];
-  attrs[0].id = cudaLaunchAttributeClusterDimension;
-  attrs[0].val.clusterDim.x = p.csize;
-  attrs[0].val.clusterDim.y = 1;
-  attrs[0].val.clusterDim.z = 1;
+  // Programmatic dependent launch: the CTAs start while the previous kernel
+  // drains and wait for it before their first global read.
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  attrs[1].id = cudaLaunchAttributeClusterDimension;
+  attrs[1].val.clusterDim.x = p.csize;
+  attrs[1].val.clusterDim.y = 1;
+  attrs[1].val.clusterDim.z = 1;
   cfg.attrs = attrs;
-  cfg.numAttrs = p.csize > 1 ? 1 : 0;
+  cfg.numAttrs = p.csize > 1 ? 2 : 1;
   return p.csize > 1 ? cudaLaunchKernelEx(&cfg, attn_tc_kernel<true>, q_map, k_map, v_map, p)
                      : cudaLaunchKernelEx(&cfg, attn_tc_kernel<false>, q_map, k_map, v_map, p);
 }

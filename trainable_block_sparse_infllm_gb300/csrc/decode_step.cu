@@ -270,7 +270,9 @@ __global__ void __launch_bounds__(kDsThreads, 1)
   const int per = ds_per(groups, C);
   if (L < 1 || L > p.Lmax || per > kDsMaxIt || nbt > kDsMaxBlocks) {   // same for every CTA of the cluster
     if (rank == 0) {
+#pragma unroll 1
       for (int e = tid; e < p.kmax; e += kDsThreads) p.block_idx[static_cast<size_t>(bh) * p.kmax + e] = -1;
+#pragma unroll 1
       for (int e = tid; e < kGroup * kHeadDim; e += kDsThreads) p.out[orow * kHeadDim + e] = __float2bfloat16(0.f);
       if (tid < kGroup && p.lse) p.lse[orow + tid] = -INFINITY;
       if (tid == 0) {
@@ -315,6 +317,7 @@ __global__ void __launch_bounds__(kDsThreads, 1)
   if (warp == 9) {
     // The forced blocks are known now: their K/V head for L2 at once, each
     // from one CTA of the cluster.
+#pragma unroll 1
     for (int x = rank + C * lane; x < n_forced; x += 32 * C)
       prefetch_block(&k_map, &v_map, kv_row0 + (x < n_first ? x : local_lo + x - n_first) * kBlock);
   }
@@ -327,12 +330,14 @@ __global__ void __launch_bounds__(kDsThreads, 1)
   if (warp == 10) {
     // The rest of this CTA's chunks go to L2 now (one box per lane), so HBM
     // streams at full rate while the shared-memory stages trail behind.
+#pragma unroll 1
     for (int x = lane; x < 4 * (nmy - kDsRing); x += 32) {
       const int row = (k0 + kDsRing + (x >> 2)) * kDsChunk;
       tma_prefetch_2d(&kc_map, (x & 1) * 64, (bh * 2 + ((x >> 1) & 1)) * p.ncmax + row);
     }
   }
   if (tid == kDsProducer * 32)
+#pragma unroll 1
     for (int it = 0; it < min(kDsRing, nmy); ++it) issue(it);
 
   // ------------------------------------------------------------ phase A --
@@ -500,11 +505,13 @@ __global__ void __launch_bounds__(kDsThreads, 1)
   // ------------------------------------------------------------ phase B --
   // Weight of the exponentials of (chunk, warp, head h): exp2(m - lse_h) / 16
   // with m the running max they were taken against.
+#pragma unroll 1
   for (int e = tid; e < nmy * kDsAWarps * kGroup; e += kDsThreads) {
     const float m = mch[e];
     mch[e] = (m == -INFINITY) ? 0.f : fast_exp2(m - lse2[e % kGroup]) * (1.0f / kGroup);
   }
   // (the ring is idle since phase A: the selection's buffers lie in it)
+#pragma unroll 1
   for (int w = tid; w < kDsMaxBlocks / 32; w += kDsThreads) sbits[w] = 0u;
   if (tid == 0) sctr[0] = 0;
   __syncthreads();
@@ -543,7 +550,9 @@ __global__ void __launch_bounds__(kDsThreads, 1)
   {
     const int kb0 = kDsChunk * k0;
     const int nrange = max(0, jb1 - jb0);
+#pragma unroll 1
     for (int x = tid; x < list_pow; x += kDsThreads) skeys[x] = 0ull;   // 0: below every key
+#pragma unroll 1
     for (int x = tid; x <= list_pow; x += kDsThreads) ecnt[x] = 0;
     if (tid < kDsMaskWords) rmask[tid] = 0u;
     // (the trip count is the same in every lane: the warp votes below)
@@ -553,6 +562,7 @@ __global__ void __launch_bounds__(kDsThreads, 1)
       float r = -INFINITY;
       if (j < jb1) {
         const int a0 = max(4 * j - 1, kb0), e0 = min(nc - 1, 4 * j + 3);
+#pragma unroll 1
         for (int k = a0; k <= e0; ++k) r = fmaxf(r, gbuf[k - kb0]);
         if (j == jb0) rmine[0] = r;
       }
@@ -568,7 +578,6 @@ __global__ void __launch_bounds__(kDsThreads, 1)
   const int n_list = min(sctr[0], n_take);
   {
     const int n_loc = sctr[0];
-    const int n_pf = ds_prefetch_count(n_take, C);
     // Two threads per key, each comparing it with half of the keys.
     const int part = tid & 1;
 #pragma unroll 1
@@ -579,11 +588,7 @@ __global__ void __launch_bounds__(kDsThreads, 1)
 #pragma unroll 4
       for (int y = part; y < n_loc; y += 2) rk += lkeys[y] > me ? 1 : 0;
       rk += __shfl_xor_sync(0xffffffffu, rk, 1);
-      if (part == 0 && x < n_loc && rk < n_list) {
-        skeys[rk] = me;
-        // The CTA's likeliest winners head for L2 while the selection is made.
-        if (rk < n_pf) prefetch_block(&k_map, &v_map, kv_row0 + static_cast<int>(~static_cast<uint32_t>(me)) * kBlock);
-      }
+      if (part == 0 && x < n_loc && rk < n_list) skeys[rk] = me;
     }
     if (tid == 0) {
       const float gl = (k1 > k0 && kDsChunk * k1 - 1 < nc) ? gbuf[kDsChunk * (k1 - k0) - 1] : -INFINITY;
@@ -596,6 +601,10 @@ __global__ void __launch_bounds__(kDsThreads, 1)
   if (tid < C)
     bulk_copy_to_cta(dsmem_addr(recv + rank * kDsMsgBytes, static_cast<uint32_t>(tid)), send, msg_bytes,
                      dsmem_addr(lbar, static_cast<uint32_t>(tid)));
+  // The CTA's likeliest winners head for L2 while the selection is made
+  // (after the copies, which they would otherwise queue ahead of).
+  if (warp == 1 && lane < min(ds_prefetch_count(n_take, C), n_list))
+    prefetch_block(&k_map, &v_map, kv_row0 + static_cast<int>(~static_cast<uint32_t>(skeys[lane])) * kBlock);
   // (waited for even after an earlier timeout: no copy may still be landing later)
   ok = __syncthreads_and(mbar_wait_cluster(lbar, 0, p.status)) && ok;
   // First block of CTA q (16 per q), completed with CTA q - 1's last kernel.
@@ -609,7 +618,9 @@ __global__ void __launch_bounds__(kDsThreads, 1)
     }
     bkeys[q] = key;
   }
+#pragma unroll 1
   for (int j = tid; j < n_first; j += kDsThreads) atomicOr(&sbits[j >> 5], 1u << (j & 31));
+#pragma unroll 1
   for (int j = local_lo + tid; j <= c; j += kDsThreads) atomicOr(&sbits[j >> 5], 1u << (j & 31));
   __syncthreads();
   // This CTA's entries (its list, then its first block) against every list:
@@ -629,6 +640,7 @@ __global__ void __launch_bounds__(kDsThreads, 1)
         if (l2[pos + step - 1] > k) pos += step;
       pos += l2[pos] > k ? 1 : 0;
       if (q2 == 0)
+#pragma unroll 1
         for (int q = 0; q < C; ++q) pos += bkeys[q] > k ? 1 : 0;
       atomicAdd(&ecnt[x], pos);
     }
@@ -650,6 +662,7 @@ __global__ void __launch_bounds__(kDsThreads, 1)
       st_async_u32x4(dst + 16 * x, make_uint4(rmask[4 * x], rmask[4 * x + 1], rmask[4 * x + 2], rmask[4 * x + 3]), bar);
   }
   ok = __syncthreads_and(mbar_wait_cluster(sbar, 0, p.status)) && ok;
+#pragma unroll 1
   for (int e = tid; e < C * kDsMaskWords; e += kDsThreads) {
     const int q = e / kDsMaskWords, w = ((16 * per * q) >> 5) + e % kDsMaskWords;
     const uint32_t v = minbox[e];
@@ -679,11 +692,13 @@ __global__ void __launch_bounds__(kDsThreads, 1)
   __syncthreads();
   const int nsel = nselS[0];
   if (rank == 0) {
+#pragma unroll 1
     for (int e = tid; e < p.kmax; e += kDsThreads)
       p.block_idx[static_cast<size_t>(bh) * p.kmax + e] = e < nsel ? selS[e] : -1;
     if (tid == 0) p.n_sel[bh] = nsel;
   }
   if (tid == 32)   // blocks of the second and later rounds: into L2 now
+#pragma unroll 1
     for (int n = rank + C * kDsPairs; n < nsel; n += C) prefetch_block(&k_map, &v_map, kv_row0 + selS[n] * kBlock);
 
   // ------------------------------------------------------------ attend --
@@ -723,6 +738,7 @@ __global__ void __launch_bounds__(kDsThreads, 1)
           // Keys past i: zero their V rows so masked probabilities never
           // meet non-finite values that may sit in the cache beyond kv_len.
           const int r0 = i - key0 + 1;
+#pragma unroll 1
           for (int e = lane; e < (32 - r0) * 16; e += 32) {
             const int row = rbase + r0 + (e >> 4), q16 = e & 15;
             *reinterpret_cast<uint4*>(stage + 16384 + (q16 >> 3) * 8192 + row * 128 + (q16 & 7) * 16) =

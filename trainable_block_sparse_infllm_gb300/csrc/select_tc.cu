@@ -109,6 +109,8 @@ __global__ void __launch_bounds__(kStThreads, 1)
   const int rank = static_cast<int>(blockIdx.x) % csize;   // == the rank in the cluster
   const int t0 = (static_cast<int>(blockIdx.x) / csize) * kStTokens;
   const int n_act = min(kStTokens, nq - t0);
+  pdl_wait();   // the previous kernel of the stream may still be writing the inputs
+  pdl_trigger();
   const int L = p.kv_lens[b];
 
   if (L < nq || L > p.Lmax) {   // the same in every CTA of a cluster: none touches another's memory
@@ -528,13 +530,17 @@ cudaError_t launch_select_tc(const Shape& s, const CUtensorMap& kc_map, const CU
   cfg.blockDim = dim3(kStThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attrs[1];
-  attrs[0].id = cudaLaunchAttributeClusterDimension;
-  attrs[0].val.clusterDim.x = pp.csize;
-  attrs[0].val.clusterDim.y = 1;
-  attrs[0].val.clusterDim.z = 1;
+  // Programmatic dependent launch: the CTAs start while the previous kernel
+  // drains and wait for it before their first global read.
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  attrs[1].id = cudaLaunchAttributeClusterDimension;
+  attrs[1].val.clusterDim.x = pp.csize;
+  attrs[1].val.clusterDim.y = 1;
+  attrs[1].val.clusterDim.z = 1;
   cfg.attrs = attrs;
-  cfg.numAttrs = pp.csize > 1 ? 1 : 0;
+  cfg.numAttrs = pp.csize > 1 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, sel_tc_kernel, kc_map, kcc_map, q_map, pp);
 }
 
