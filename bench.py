@@ -636,7 +636,8 @@ def reference_arm(args):
 
 def profile_passes(path, n):
     """n passes of one path on a single input copy, nothing timed: the decode
-    path is one decode_step launch per pass (decode_128k, 0.57 GB of inputs);
+    path is one decode_step launch per pass (decode_128k, 0.57 GB of inputs),
+    the verify path one three-stage decode step of verify_128k (0.57 GB);
     the prefill path is compress + select + attention (prefill_32k); the
     backward path is one forward, then n backward calls (prefill_32k).  The
     *8k variants run the prefill workload cut to 8192 tokens."""
@@ -646,7 +647,7 @@ def profile_passes(path, n):
     import trainable_block_sparse_infllm_gb300 as T
     dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
-    wl = S.WORKLOADS[DECODE if path == "decode" else PREFILL]
+    wl = S.WORKLOADS[{"decode": DECODE, "verify": "verify_128k"}.get(path, PREFILL)]
     if path.endswith("8k"):
         # The prefill workload cut to an 8192-token causal prefill (inputs of
         # ~150 MB, above L2): a case small enough for full ncu captures.
@@ -668,7 +669,7 @@ def profile_passes(path, n):
     out = torch.empty_like(q)
     lse = torch.empty((B, nq, wl.n_heads), dtype=torch.float32, device=dev)
     T.compress_keys(p, k, lens, kc)
-    if path == "decode":
+    if path in ("decode", "verify"):
         ws = T.alloc_workspace(p, nq, T.OP_DECODE_STEP, dev)
         for _ in range(n):
             T.decode_step(p, q, k, v, lens, kc, idx, nsel, out, lse, ws)
@@ -708,7 +709,7 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-workloads", action="store_true", help="headline workload and prefill only")
-    ap.add_argument("--profile", choices=["decode", "prefill", "backward", "prefill8k", "backward8k"],
+    ap.add_argument("--profile", choices=["decode", "verify", "prefill", "backward", "prefill8k", "backward8k"],
                     help="run warmup + steps untimed passes of one path on one input copy and exit "
                          "(a small, fixed launch sequence for ncu)")
     args = ap.parse_args()
