@@ -87,12 +87,11 @@ constexpr int kDsBkeyOff = kDsSelOff + kDsMaxBlocks / 8;
 constexpr int kDsCtrOff = kDsBkeyOff + kDsMaxC * 8;
 constexpr int kDsRmaskOff = kDsCtrOff + 16 * 4;
 constexpr int kDsMinOff = kDsRmaskOff + 64;
-constexpr int kDsCntOff = kDsMinOff + kDsMaxC * kDsMaskWords * 4;   // larger keys per own entry [257]
 static_assert(kDsMaxIt >= 16, "16 chunks per CTA");
 static_assert(kDsMsgBytes % 16 == 0 && kDsSendOff % 16 == 0 && kDsMinOff % 16 == 0, "bulk copies and st.async");
 static_assert((16 * kDsMaxIt + 31) / 32 + 1 <= kDsMaskWords, "a CTA's blocks fit its mask");
 static_assert(kDsRecvOff + kDsMaxC * kDsMsgBytes <= kDsGbufOff, "messages ahead of the phase-B buffers");
-static_assert(kDsCntOff + (kDsListMax + 1) * 4 <= kDsZOff, "phase-B buffers inside the ring");
+static_assert(kDsMinOff + kDsMaxC * kDsMaskWords * 4 <= kDsZOff, "phase-B buffers inside the ring");
 
 // Pushed per CTA before the second barrier.
 struct DsSummary {
@@ -208,7 +207,6 @@ __global__ void __launch_bounds__(kDsThreads, 1)
   int* sctr = reinterpret_cast<int*>(smem + kDsCtrOff);              // [0] n_loc, [4..16) warp sums
   uint32_t* rmask = reinterpret_cast<uint32_t*>(smem + kDsRmaskOff);                      // this CTA's winners
   uint32_t* minbox = reinterpret_cast<uint32_t*>(smem + kDsMinOff);                      // [C][12] every CTA's
-  int* ecnt = reinterpret_cast<int*>(smem + kDsCntOff);              // [n_list + 1] larger keys per own entry
   float2* lse_in = reinterpret_cast<float2*>(smem + lay.lse_in);     // [C][16]
   float* o_in = reinterpret_cast<float*>(smem + lay.o_in);           // [C * hmax][128]
   float2* ml_in = reinterpret_cast<float2*>(smem + lay.ml_in);       // [C * hmax]
@@ -552,8 +550,6 @@ __global__ void __launch_bounds__(kDsThreads, 1)
     const int nrange = max(0, jb1 - jb0);
 #pragma unroll 1
     for (int x = tid; x < list_pow; x += kDsThreads) skeys[x] = 0ull;   // 0: below every key
-#pragma unroll 1
-    for (int x = tid; x <= list_pow; x += kDsThreads) ecnt[x] = 0;
     if (tid < kDsMaskWords) rmask[tid] = 0u;
     // (the trip count is the same in every lane: the warp votes below)
 #pragma unroll 1
@@ -578,15 +574,32 @@ __global__ void __launch_bounds__(kDsThreads, 1)
   const int n_list = min(sctr[0], n_take);
   {
     const int n_loc = sctr[0];
-    // Two threads per key, each comparing it with half of the keys.
+    // Two threads per key, each comparing it with one half of the keys
+    // (keys [0, h) and [h, n_loc), h even), eight keys per iteration from
+    // four independent 16-byte loads: the loop is bound by load latency.
     const int part = tid & 1;
+    const int h = (n_loc / 2 + 1) & ~1;
+    const int y0 = part ? h : 0, y1 = part ? n_loc : min(h, n_loc);
 #pragma unroll 1
     for (int x0 = 0; x0 < n_loc; x0 += kDsThreads / 2) {   // (same trip count in every lane)
       const int x = x0 + (tid >> 1);
       const unsigned long long me = x < n_loc ? lkeys[x] : 0ull;
-      int rk = 0;
-#pragma unroll 4
-      for (int y = part; y < n_loc; y += 2) rk += lkeys[y] > me ? 1 : 0;
+      int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+      int y = y0;
+#pragma unroll 1
+      for (; y + 8 <= y1; y += 8) {
+        const ulonglong2 a0 = *reinterpret_cast<const ulonglong2*>(lkeys + y);
+        const ulonglong2 a1 = *reinterpret_cast<const ulonglong2*>(lkeys + y + 2);
+        const ulonglong2 a2 = *reinterpret_cast<const ulonglong2*>(lkeys + y + 4);
+        const ulonglong2 a3 = *reinterpret_cast<const ulonglong2*>(lkeys + y + 6);
+        r0 += (a0.x > me ? 1 : 0) + (a0.y > me ? 1 : 0);
+        r1 += (a1.x > me ? 1 : 0) + (a1.y > me ? 1 : 0);
+        r2 += (a2.x > me ? 1 : 0) + (a2.y > me ? 1 : 0);
+        r3 += (a3.x > me ? 1 : 0) + (a3.y > me ? 1 : 0);
+      }
+#pragma unroll 1
+      for (; y < y1; ++y) r0 += lkeys[y] > me ? 1 : 0;
+      int rk = (r0 + r1) + (r2 + r3);
       rk += __shfl_xor_sync(0xffffffffu, rk, 1);
       if (part == 0 && x < n_loc && rk < n_list) skeys[rk] = me;
     }
@@ -624,33 +637,30 @@ __global__ void __launch_bounds__(kDsThreads, 1)
   for (int j = local_lo + tid; j <= c; j += kDsThreads) atomicOr(&sbits[j >> 5], 1u << (j & 31));
   __syncthreads();
   // This CTA's entries (its list, then its first block) against every list:
-  // thread e takes entry e / C and list e % C, a binary search over that
-  // sorted, zero-padded list (list 0's thread also counts the first blocks);
-  // the counts add up per entry.
+  // half-warp entry x, lane q searches list q (sorted, zero-padded) and
+  // compares first block q; the 16 lanes' counts add up to the entry's rank.
   if (n_take > 0) {
+    const int q2 = lane & 15;
 #pragma unroll 1
-    for (int e = tid; e < (n_list + 1) * C; e += kDsThreads) {
-      const int x = e / C, q2 = e % C;
-      const unsigned long long k = x < n_list ? msg_keys(rank)[x] : bkeys[rank];
-      if (k == 0ull) continue;
-      const unsigned long long* l2 = msg_keys(q2);
+    for (int x0 = 0; x0 <= n_list; x0 += 2 * kDsWarps) {   // (same trip count in every lane)
+      const int x = x0 + 2 * warp + (lane >> 4);
+      unsigned long long k = 0ull;   // 0: no entry
+      if (x <= n_list) k = x < n_list ? msg_keys(rank)[x] : bkeys[rank];
       int pos = 0;
+      if (k != 0ull && q2 < C) {
+        const unsigned long long* l2 = msg_keys(q2);
+        // Branchless binary search: the entries above k form a prefix.
 #pragma unroll 1
-      for (int step = list_pow >> 1; step >= 1; step >>= 1)
-        if (l2[pos + step - 1] > k) pos += step;
-      pos += l2[pos] > k ? 1 : 0;
-      if (q2 == 0)
-#pragma unroll 1
-        for (int q = 0; q < C; ++q) pos += bkeys[q] > k ? 1 : 0;
-      atomicAdd(&ecnt[x], pos);
-    }
-  }
-  __syncthreads();
-  if (n_take > 0 && tid <= n_list) {
-    const unsigned long long k = tid < n_list ? msg_keys(rank)[tid] : bkeys[rank];
-    if (k != 0ull && ecnt[tid] < n_take) {
-      const int j = static_cast<int>(~static_cast<uint32_t>(k));
-      atomicOr(&rmask[(j >> 5) - w0], 1u << (j & 31));
+        for (int step = list_pow >> 1; step >= 1; step >>= 1)
+          if (l2[pos + step - 1] > k) pos += step;
+        pos += (l2[pos] > k ? 1 : 0) + (bkeys[q2] > k ? 1 : 0);
+      }
+#pragma unroll
+      for (int o = 8; o >= 1; o >>= 1) pos += __shfl_xor_sync(0xffffffffu, pos, o);
+      if (q2 == 0 && k != 0ull && pos < n_take) {
+        const int j = static_cast<int>(~static_cast<uint32_t>(k));
+        atomicOr(&rmask[(j >> 5) - w0], 1u << (j & 31));
+      }
     }
   }
   __syncthreads();
