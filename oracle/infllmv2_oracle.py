@@ -323,6 +323,38 @@ def sparse_attention_grad(q: np.ndarray, K: np.ndarray, V: np.ndarray, blocks: n
     return dq, dK, dV
 
 
+def block_grad_kv(Q: np.ndarray, dO: np.ndarray, lse: np.ndarray, D: np.ndarray, pos: np.ndarray,
+                  Kj: np.ndarray, Vj: np.ndarray, key0: int, scale: float, extra: np.ndarray | None = None):
+    """Gradients of one key block with respect to its keys and values, from
+    every query that selected the block (the selection held fixed,
+    [InfLLM v2 › Training-time considerations]): the sum over those queries of
+    sparse_attention_grad_selected's dK_sel and dV_sel rows for this block's
+    keys, with each query's softmax normalised by its own log-sum-exp over all
+    the keys it attends.
+
+    Q, dO [T, G, d]: the T queries' rows and upstream gradients; lse, D [T, G]:
+    each query's natural log-sum-exp of its scaled scores and rowsum(dO * O);
+    pos [T]: the query positions (keys after a query's position are not
+    attended); Kj, Vj [m, d]: the block's keys key0 .. key0 + m - 1.
+        P = exp(scale q K_j^T - lse) on attended keys,  dP = dO V_j^T,
+        dS = P * (dP - D),  dK_j = scale sum dS^T q,  dV_j = sum P^T dO.
+    extra [T, G, d] (optional): also returns sum P^T extra.
+    Returns (dK_j [m, d], dV_j [m, d], sum P^T extra or None).
+    """
+    T, G, d = Q.shape
+    m = Kj.shape[0]
+    keys = key0 + np.arange(m)
+    S = scale * (Q.reshape(T * G, d) @ Kj.T).reshape(T, G, m)
+    valid = (keys[None, :] <= pos[:, None])[:, None, :]
+    P = np.where(valid, np.exp(np.where(valid, S, 0.0) - lse[:, :, None]), 0.0)
+    dP = (dO.reshape(T * G, d) @ Vj.T).reshape(T, G, m)
+    dS = P * (dP - D[:, :, None])
+    dK = scale * (dS.reshape(T * G, m).T @ Q.reshape(T * G, d))
+    dV = P.reshape(T * G, m).T @ dO.reshape(T * G, d)
+    ex = None if extra is None else P.reshape(T * G, m).T @ extra.reshape(T * G, d)
+    return dK, dV, ex
+
+
 # --------------------------------------------------------------------------
 # Drivers over the [B, Hkv, n_q] units of one input set
 # --------------------------------------------------------------------------

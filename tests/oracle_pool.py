@@ -97,6 +97,138 @@ def _init_attend(folder, names, wl, st, strict_keys):
     _W["strict_keys"] = strict_keys
 
 
+def _kv_f64(b, h):
+    """This worker's fp64 copy of one (b, h) cache, kept across its tasks."""
+    import synthetic_inputs as S
+    key = ("kv", b, h)
+    if key not in _W:
+        L = int(_W["inp"].kv_lens[b])
+        for k in [k for k in _W if isinstance(k, tuple) and k[0] == "kv"]:
+            del _W[k]
+        _W[key] = (S.bf16_bits_to_f64(_W["inp"].k[b, h, :L]), S.bf16_bits_to_f64(_W["inp"].v[b, h, :L]))
+    return _W[key]
+
+
+def _grad_q_task(task):
+    """Per unit of (b, h, t0..t1-1), on the given selection: the oracle's
+    forward (lse, and D = rowsum(dO * O) from its own O), its dq against the
+    device's, and the allowance for the bf16 forward output the device's D
+    is built from (dD = |rowsum(dO * (out - O))|).  Returns the error
+    statistics and each unit's lse, D and dD."""
+    import oracle as O
+    import synthetic_inputs as S
+    b, h, t0, t1 = task
+    inp, st = _W["inp"], _W["st"]
+    wl = inp.wl
+    G, d, m = wl.group, wl.head_dim, wl.block
+    scale = st.ascale(d)
+    K, V = _kv_f64(b, h)
+    L = int(inp.kv_lens[b])
+    idx, nsel, dO_all, out, dq = _W["idx"], _W["nsel"], _W["dout"], _W["out"], _W["dq"]
+    res = {"ref": 0.0, "over": 0.0, "err": 0.0, "allow": 0.0, "count": 0}
+    stats = np.zeros((t1 - t0, 3, G))
+    for t in range(t0, t1):
+        i = O.query_position(L, wl.n_q, t)
+        blocks = np.asarray(idx[b, h, t][:nsel[b, h, t]])
+        q = S.bf16_bits_to_f64(inp.q[b, t, h * G:(h + 1) * G])
+        dOu = S.bf16_bits_to_f64(dO_all[b, t, h * G:(h + 1) * G])
+        o_ref, lse = O.sparse_attention(q, K, V, blocks, i, m, scale)
+        gq = O.sparse_attention_grad_selected(q, K, V, blocks, i, m, scale, dOu)[0]
+        o_dev = S.bf16_bits_to_f64(out[b, t, h * G:(h + 1) * G])
+        dD = np.abs((dOu * (o_dev - o_ref)).sum(axis=1))
+        pk = O.sparse_attention(q, K, np.abs(K), blocks, i, m, scale)[0]
+        allow = scale * dD[:, None] * pk
+        err = np.abs(np.asarray(dq[b, t, h * G:(h + 1) * G], dtype=np.float64) - gq)
+        res["ref"] = max(res["ref"], float(np.abs(gq).max()))
+        res["over"] = max(res["over"], float((err - 1.001 * allow).max()))
+        res["err"] += float(err.sum())
+        res["allow"] += float(allow.sum())
+        res["count"] += err.size
+        stats[t - t0] = (lse, (dOu * o_ref).sum(axis=1), dD)
+    return b, h, t0, t1, res, stats
+
+
+def _grad_kv_task(task):
+    """dK, dV of the key blocks j0..j1-1 of (b, h) from every query that
+    selected them (oracle.block_grad_kv with the queries' own lse and D),
+    the allowance for the bf16 forward output, and the keys some query
+    attends."""
+    import oracle as O
+    import synthetic_inputs as S
+    b, h, j0, j1 = task
+    inp, st = _W["inp"], _W["st"]
+    wl = inp.wl
+    G, d, m = wl.group, wl.head_dim, wl.block
+    scale = st.ascale(d)
+    K, V = _kv_f64(b, h)
+    L = int(inp.kv_lens[b])
+    idx, nsel, dO_all, stats = _W["idx"], _W["nsel"], _W["dout"], _W["stats"]
+    sel = np.asarray(idx[b, h])                       # [n_q, k_max]
+    n = np.asarray(nsel[b, h])
+    live = np.arange(sel.shape[1])[None, :] < n[:, None]
+    lo, hi = j0 * m, min(j1 * m, L)
+    rk, rv, ra = (np.zeros((max(0, hi - lo), d)) for _ in range(3))
+    used = np.zeros(max(0, hi - lo), dtype=bool)
+    for j in range(j0, j1):
+        if j * m >= L:
+            break
+        toks = np.nonzero(((sel == j) & live).any(axis=1))[0]
+        if toks.size == 0:
+            continue
+        pos = np.array([O.query_position(L, wl.n_q, int(t)) for t in toks])
+        Q = S.bf16_bits_to_f64(inp.q[b, toks][:, h * G:(h + 1) * G])
+        dOt = S.bf16_bits_to_f64(dO_all[b, toks][:, h * G:(h + 1) * G])
+        st3 = np.asarray(stats[b, h, toks])           # [T, 3, G]: lse, D, dD
+        rows = slice(j * m, min((j + 1) * m, L))
+        dk, dv, ex = O.block_grad_kv(Q, dOt, st3[:, 0], st3[:, 1], pos, K[rows], V[rows], j * m, scale,
+                                     st3[:, 2][:, :, None] * np.abs(Q))
+        r = slice(j * m - lo, min((j + 1) * m, L) - lo)
+        rk[r], rv[r], ra[r] = dk, dv, scale * ex
+        used[r] = np.arange(j * m, min((j + 1) * m, L)) <= pos.max()
+    return b, h, j0, j1, rk, rv, ra, used
+
+
+def all_backward(inp, st, idx, nsel, dout, out, dq, chunk=256, blocks_per_task=16):
+    """Oracle gradients of every unit of a workload with the selection
+    (idx, nsel) held fixed.  dout, out: bf16 bits [B, n_q, Hq, d] (the
+    upstream gradient and the device's forward output); dq: the device's
+    dq.  Returns (dq statistics, dK ref, dV ref, dK allowance, keys used),
+    the key arrays shaped like the caches."""
+    wl = inp.wl
+    with tempfile.TemporaryDirectory() as folder:
+        arrays = {"q": inp.q, "k": inp.k, "v": inp.v, "kv_lens": inp.kv_lens, "idx": idx, "nsel": nsel,
+                  "dout": dout, "out": out, "dq": dq}
+        _save(folder, arrays)
+        ctx = mp.get_context("spawn")
+        G = wl.group
+        stats = np.zeros((wl.batch, wl.n_kv_heads, wl.n_q, 3, G))
+        tot = {"ref": 0.0, "over": 0.0, "err": 0.0, "allow": 0.0, "count": 0}
+        with _OneBlasThread(), ctx.Pool(_workers(), initializer=_init,
+                                        initargs=(folder, list(arrays), wl, st)) as pool:
+            for b, h, t0, t1, r, sts in pool.imap_unordered(_grad_q_task, _tasks(inp, chunk)):
+                tot["ref"] = max(tot["ref"], r["ref"])
+                tot["over"] = max(tot["over"], r["over"])
+                for k in ("err", "allow", "count"):
+                    tot[k] += r[k]
+                stats[b, h, t0:t1] = sts
+        _save(folder, {"stats": stats})
+        shape = (wl.batch, wl.n_kv_heads, wl.kv_len, wl.head_dim)
+        rk, rv, ra = np.zeros(shape), np.zeros(shape), np.zeros(shape)
+        used = np.zeros(shape[:3], dtype=bool)
+        nb = (wl.kv_len + wl.block - 1) // wl.block
+        tasks = [(b, h, j0, min(nb, j0 + blocks_per_task)) for b in range(wl.batch) for h in range(wl.n_kv_heads)
+                 for j0 in range(0, nb, blocks_per_task)]
+        with _OneBlasThread(), ctx.Pool(_workers(), initializer=_init,
+                                        initargs=(folder, list(arrays) + ["stats"], wl, st)) as pool:
+            for b, h, j0, j1, k_, v_, a_, u_ in pool.imap_unordered(_grad_kv_task, tasks):
+                lo = j0 * wl.block
+                rk[b, h, lo:lo + k_.shape[0]] = k_
+                rv[b, h, lo:lo + v_.shape[0]] = v_
+                ra[b, h, lo:lo + a_.shape[0]] = a_
+                used[b, h, lo:lo + u_.shape[0]] = u_
+    return tot, rk, rv, ra, used
+
+
 def _tasks(inp, chunk):
     wl = inp.wl
     return [(b, h, t0, min(wl.n_q, t0 + chunk)) for b in range(wl.batch) for h in range(wl.n_kv_heads)

@@ -405,6 +405,73 @@ def test_attention_grad_finite_differences():
     assert np.all(dK[64:128] == 0) and np.all(dV[136:] == 0)
 
 
+def _block_grad_case(seed=22, G=4, d=6, L=300, m=64, T=9):
+    """Queries at scattered positions, each with its own block set (its own
+    block always in it): the key-centric gradients of every block against
+    the per-query gradients summed."""
+    rng = np.random.default_rng(seed)
+    K, V = rng.standard_normal((L, d)), rng.standard_normal((L, d))
+    Q, dO, X = (rng.standard_normal((T, G, d)) for _ in range(3))
+    pos = np.sort(rng.choice(np.arange(40, L), size=T, replace=False))
+    nb = (L + m - 1) // m
+    sets = []
+    for t in range(T):
+        own = pos[t] // m
+        others = [j for j in range(own) if rng.random() < 0.5]
+        sets.append(np.array(sorted(set(others + [own]))))
+    return K, V, Q, dO, X, pos, sets, nb
+
+
+def test_block_grad_kv_matches_per_query_sums(fn=None):
+    fn = fn or O.block_grad_kv
+    K, V, Q, dO, X, pos, sets, nb = _block_grad_case()
+    m, scale = 64, 0.41
+    T = Q.shape[0]
+    lse, D = np.zeros(Q.shape[:2]), np.zeros(Q.shape[:2])
+    ref_k, ref_v, ref_x = np.zeros(K.shape), np.zeros(K.shape), np.zeros(K.shape)
+    for t in range(T):
+        o, lse[t] = O.sparse_attention(Q[t], K, V, sets[t], pos[t], m, scale)
+        D[t] = (dO[t] * o).sum(axis=1)
+        _, keys, gk, gv = O.sparse_attention_grad_selected(Q[t], K, V, sets[t], pos[t], m, scale, dO[t])
+        ref_k[keys] += gk
+        ref_v[keys] += gv
+        ref_x[keys] += O.sparse_attention_grad_selected(Q[t], K, V, sets[t], pos[t], m, scale, X[t])[3]
+    for j in range(nb):
+        sel = np.array([t for t in range(T) if j in set(sets[t].tolist())], dtype=int)
+        rows = slice(j * m, min((j + 1) * m, K.shape[0]))
+        if sel.size == 0:
+            continue
+        dk, dv, dx = fn(Q[sel], dO[sel], lse[sel], D[sel], pos[sel], K[rows], V[rows], j * m, scale, X[sel])
+        np.testing.assert_allclose(dk, ref_k[rows], rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(dv, ref_v[rows], rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(dx, ref_x[rows], rtol=1e-10, atol=1e-12)
+
+
+def _planted_block_grad_mistakes():
+    good = O.block_grad_kv
+
+    def no_causal_mask(Q, dO, lse, D, pos, Kj, Vj, key0, scale, extra=None):   # keys after the query counted
+        return good(Q, dO, lse, D, pos + 10 ** 6, Kj, Vj, key0, scale, extra)
+
+    def no_d_term(Q, dO, lse, D, pos, Kj, Vj, key0, scale, extra=None):        # dS = P dP
+        return good(Q, dO, lse, np.zeros_like(D), pos, Kj, Vj, key0, scale, extra)
+
+    def no_scale(Q, dO, lse, D, pos, Kj, Vj, key0, scale, extra=None):         # dK without the softmax scale
+        dk, dv, dx = good(Q, dO, lse, D, pos, Kj, Vj, key0, scale, extra)
+        return dk / scale, dv, dx
+
+    def shifted_keys(Q, dO, lse, D, pos, Kj, Vj, key0, scale, extra=None):     # block credited one key off
+        return good(Q, dO, lse, D, pos, Kj, Vj, key0 + 1, scale, extra)
+
+    return [no_causal_mask, no_d_term, no_scale, shifted_keys]
+
+
+@pytest.mark.parametrize("bad", _planted_block_grad_mistakes())
+def test_planted_block_grad_mistakes_are_caught(bad):
+    with pytest.raises(AssertionError):
+        test_block_grad_kv_matches_per_query_sums(bad)
+
+
 # ------------------------------------------------ the pins catch mistakes ----
 
 def _planted_mistakes():
