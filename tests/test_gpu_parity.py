@@ -116,6 +116,30 @@ def test_select_blocks_parity(dev, case):
     check_selections(run, sels)
 
 
+def test_prefill_selection_past_on_chip_capacity(dev):
+    # 270,000 tokens of capacity (4219 blocks): past the 4091 blocks whose 8
+    # tokens' block scores fit in shared memory, the prefill-path selection
+    # keeps them in one workspace slot per SM.  Ragged lengths; the selection
+    # (with its scores) and the attention on it against the oracle.
+    import torch
+    inp = S.make_random(batch=2, n_kv_heads=2, kv_len=270000, n_q=24, topk=48, includes_forced=False, seed=91,
+                        kv_lens=[270000, 151000])
+    run = DeviceRun(inp, dev)
+    assert run.T.workspace_size(run.p, 24, run.T.OP_SELECT) > 0
+    run.compress()
+    run.select()
+    torch.cuda.synchronize()
+    st = _settings(inp.wl)
+    sels = O.run_selection(inp, st)
+    check_selections(run, sels)
+    idx, nsel = run.upload_selection(sels)
+    run.attend(idx, nsel)
+    torch.cuda.synchronize()
+    blocks_of = {u: s.blocks for u, s in sels.items()}
+    refs = O.run_attention(inp, st, blocks_of)
+    check_attention(run, refs, strict=True, strict_units=strict_units(inp, blocks_of))
+
+
 def test_select_blocks_dense_when_context_short(dev):
     import torch
     inp = S.make_random(batch=1, n_kv_heads=2, kv_len=1024, n_q=4, topk=16, seed=5)

@@ -296,7 +296,7 @@ int infllmv2_select_blocks(const infllmv2_params* p, const void* q, int32_t n_q,
     if (!aligned16(q) || !aligned16(kc)) return fail(INFLLMV2_UNSUPPORTED, "q and kc must be 16-byte aligned");
     if (!select_supported(s))
       return fail(INFLLMV2_UNSUPPORTED,
-                  "selection for n_q > 16 keeps 8 tokens' block scores on chip: max_kv_len up to 261824");
+                  "selection for n_q > 16: max_kv_len beyond the supported capacity (about 680K tokens)");
     const size_t need = select_workspace_bytes(s);
     if (need > 0 && (!workspace || workspace_bytes < need))
       return fail(INFLLMV2_WORKSPACE_TOO_SMALL, "workspace needs %zu bytes (got %zu)", need, workspace_bytes);
@@ -329,7 +329,7 @@ int infllmv2_select_blocks_static(const infllmv2_params* p, const void* q, int32
     if (!aligned16(q) || !aligned16(kc)) return fail(INFLLMV2_UNSUPPORTED, "q and kc must be 16-byte aligned");
     if (!select_supported(s))
       return fail(INFLLMV2_UNSUPPORTED,
-                  "selection for n_q > 16 keeps 8 tokens' block scores on chip: max_kv_len up to 261824");
+                  "selection for n_q > 16: max_kv_len beyond the supported capacity (about 680K tokens)");
     const size_t need = select_workspace_bytes(s);
     if (need > kStaticSelectScratchBytes)
       return fail(INFLLMV2_WORKSPACE_TOO_SMALL,
@@ -398,9 +398,9 @@ int infllmv2_select_blocks_coarse_lse(const infllmv2_params* p, const void* q, i
       return fail(INFLLMV2_UNSUPPORTED, "q, kc and kcc must be 16-byte aligned");
     if (s.ncmax < 1 || s.Lmax / coarse < 1)
       return fail(INFLLMV2_UNSUPPORTED, "max_kv_len must hold a kernel and a coarse window");
-    if (!select_tc_supported(s))
+    if (!select_tc_onchip(s))
       return fail(INFLLMV2_UNSUPPORTED,
-                  "selection for n_q > 16 keeps 8 tokens' block scores on chip: max_kv_len up to 261824");
+                  "the coarse-LSE selection keeps 8 tokens' block scores on chip: max_kv_len up to 261824");
     uint32_t* status = status_ptr();
     if (!status) return fail(INFLLMV2_CUDA_ERROR, "no device status word (no current CUDA device?)");
     CUtensorMap kcm, kccm, qm;
@@ -473,7 +473,7 @@ int infllmv2_decode_step(const infllmv2_params* p, const void* q, int32_t n_q, c
     const int cluster = decode_step_cluster_size(s);
     if (!cluster && !select_supported(s))
       return fail(INFLLMV2_UNSUPPORTED,
-                  "selection for n_q > 16 keeps 8 tokens' block scores on chip: max_kv_len up to 261824");
+                  "selection for n_q > 16: max_kv_len beyond the supported capacity (about 680K tokens)");
     const size_t need = cluster ? 0 : select_workspace_bytes(s) + attn_workspace_bytes(s, false);
     if (need > 0 && (!workspace || workspace_bytes < need))
       return fail(INFLLMV2_WORKSPACE_TOO_SMALL, "workspace needs %zu bytes (got %zu)", need, workspace_bytes);

@@ -216,6 +216,20 @@ __device__ __forceinline__ uint32_t swz128_offset(int row, int chunk, int rows) 
 
 // --------------------------------------------- clusters / distributed smem --
 
+// The SM this thread runs on (a slot index for scratch that only one CTA per
+// SM uses at a time), and the bound on SM identifiers (which need not be
+// contiguous, so it may exceed the number of SMs).
+__device__ __forceinline__ uint32_t sm_id() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t sm_id_bound() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nsmid;" : "=r"(r));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));

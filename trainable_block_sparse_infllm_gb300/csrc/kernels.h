@@ -37,6 +37,7 @@ size_t select_workspace_bytes(const Shape& s);
 // The prefill selection (n_q > 16) keeps 8 tokens' block scores in shared
 // memory: at most 4091 blocks (261824 tokens) of cache capacity.
 bool select_tc_supported(const Shape& s);
+bool select_tc_onchip(const Shape& s);   // the prefill path's block scores fit in shared memory
 bool select_supported(const Shape& s);
 cudaError_t launch_select(const Shape& s, const CUtensorMap& kc_map, const CUtensorMap& q_map,
                           const void* q, const int32_t* kv_lens, int32_t* block_idx,

@@ -33,8 +33,8 @@ int device_sm_count() {
   return cache[dev];
 }
 
-bool select_tc_supported(const Shape& s);
 int select_tc_cluster_size(const Shape& s, int sc);
+size_t select_tc_scratch_bytes(const Shape& s);
 cudaError_t launch_select_tc(const Shape& s, const CUtensorMap& kc_map, const CUtensorMap& kcc_map,
                              const CUtensorMap& q_map, const SelParams& p, cudaStream_t st);
 size_t select_decode_ncpad(const Shape& s);
@@ -76,7 +76,9 @@ size_t select_workspace_bytes(const Shape& s) {
     const size_t units = static_cast<size_t>(s.B) * s.Hkv * s.nq;
     return align256(units * kGroup * select_decode_ncpad(s) * sizeof(float));
   }
-  return 0;  // the prefill path keeps everything on chip
+  // The prefill path keeps everything on chip up to 4091 blocks of capacity;
+  // past that its block scores take one slot per SM of a global scratch.
+  return align256(select_tc_scratch_bytes(s));
 }
 
 cudaError_t launch_select(const Shape& s, const CUtensorMap& kc_map, const CUtensorMap& q_map,
@@ -114,6 +116,7 @@ cudaError_t launch_select(const Shape& s, const CUtensorMap& kc_map, const CUten
     return launch_select_decode(s, kc_map, q_map, p, st);
   }
   if (!select_tc_supported(s)) return cudaErrorInvalidConfiguration;   // rejected by the entry points
+  p.r_scratch = static_cast<float*>(ws);
   return launch_select_tc(s, kc_map, kc_map, q_map, p, st);
 }
 
@@ -141,7 +144,7 @@ cudaError_t launch_select_coarse(const Shape& s, const CUtensorMap& kc_map, cons
   p.r_buf = block_scores;
   p.sc = sc;
   p.nccmax = s.Lmax / sc;
-  if (!select_tc_supported(s)) return cudaErrorInvalidConfiguration;   // rejected by the entry points
+  if (!select_tc_onchip(s)) return cudaErrorInvalidConfiguration;   // rejected by the entry point
   return launch_select_tc(s, kc_map, kcc_map, q_map, p, st);
 }
 

@@ -27,6 +27,8 @@ struct SelParams {
   int stages;          // prefill path: pipeline depth
   int sc, nccmax;      // prefill path: coarse-LSE window (0 = exact LSE) and windows per cache
   int csize;           // prefill path: CTAs per 8-token tile (1, or a cluster splitting the chunks)
+  float* r_scratch;    // prefill path: block scores off chip, [r_slots][8][nbmax] (null: in shared memory)
+  int r_slots;         // slots of r_scratch (one per SM identifier)
   uint32_t* status;
 };
 

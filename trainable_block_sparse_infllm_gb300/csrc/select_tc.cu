@@ -61,7 +61,8 @@ constexpr int kStClusterMinSmem = 116 * 1024;   // a cluster launch requests at 
 // The top-k flags and scratch overlay the chunk ring, which is idle once the
 // last chunk's products are done (every row warp has waited for them before
 // its top-k).
-__host__ __device__ inline StLayout st_layout(int nbmax, int stages, bool clustered) {
+// offchip: the block scores live in global scratch (r_scratch), not here.
+__host__ __device__ inline StLayout st_layout(int nbmax, int stages, bool clustered, bool offchip = false) {
   StLayout l;
   l.ring = 0;
   l.flag = 0;                                           // [8 tokens][nbmax] top-k flags (in the ring)
@@ -71,7 +72,7 @@ __host__ __device__ inline StLayout st_layout(int nbmax, int stages, bool cluste
   l.csurv = l.cbits + (((nbmax + 31) / 32 * 4 + 15) & ~15);
   l.q = stages * kStChunkBytes;                         // two 64-column boxes x 128 rows
   l.r = l.q + 32768;                                    // [8 tokens][nbmax] block scores
-  l.xch = (l.r + kStTokens * nbmax * 4 + 15) & ~15;     // [2][128] (max, sum)
+  l.xch = (l.r + (offchip ? 0 : kStTokens * nbmax * 4) + 15) & ~15;   // [2][128] (max, sum)
   l.lse_in = l.xch + 2 * 128 * 8;                       // cluster form: [C][128 rows] (max, sum)
   l.tails = l.lse_in + (clustered ? kStMaxC * 128 * 8 : 0);   // cluster form: [C][8 tokens] last-kernel g
   l.bars = l.tails + (clustered ? kStMaxC * kStTokens * 4 : 0);
@@ -98,10 +99,9 @@ __global__ void __launch_bounds__(kStThreads, 1)
   uint8_t* smem = align1024(smem_raw);
   const int S = p.stages;
   const int csize = p.csize;
-  const StLayout lay = st_layout(p.nbmax, S, csize > 1);
+  const StLayout lay = st_layout(p.nbmax, S, csize > 1, p.r_scratch != nullptr);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + lay.bars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + lay.slot);
-  float* r_all = reinterpret_cast<float*>(smem + lay.r);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.y, b = blockIdx.z;
   const int bh = b * p.Hkv + h;
@@ -111,6 +111,19 @@ __global__ void __launch_bounds__(kStThreads, 1)
   const int n_act = min(kStTokens, nq - t0);
   pdl_wait();   // the previous kernel of the stream may still be writing the inputs
   pdl_trigger();
+  // Block scores of the tile's 8 tokens: in shared memory, or past that
+  // capacity in this SM's slot of the global scratch (the kernel needs more
+  // than half an SM's shared memory, so no two of its CTAs share an SM).
+  const uint32_t slot = sm_id();
+  if (p.r_scratch && slot >= static_cast<uint32_t>(p.r_slots)) {   // cannot happen with slots from %nsmid
+    for (int e = tid; e < n_act * p.kmax; e += kStThreads)
+      p.block_idx[(static_cast<size_t>(bh) * nq + t0 + e / p.kmax) * p.kmax + e % p.kmax] = -1;
+    if (tid < n_act) p.n_sel[static_cast<size_t>(bh) * nq + t0 + tid] = 0;
+    if (tid == 0) atomicOr(p.status, kStatusBounds);
+    return;
+  }
+  float* r_all = p.r_scratch ? p.r_scratch + static_cast<size_t>(slot) * kStTokens * p.nbmax
+                             : reinterpret_cast<float*>(smem + lay.r);
   const int L = p.kv_lens[b];
 
   if (L < nq || L > p.Lmax) {   // the same in every CTA of a cluster: none touches another's memory
@@ -490,9 +503,9 @@ int st_active_clusters(int C) {
   return cache[dev][C];
 }
 
-int stages_for(const Shape& s, bool clustered) {
+int stages_for(const Shape& s, bool clustered, bool offchip = false) {
   for (int st = kStMaxStages; st >= 2; --st)
-    if (st_layout(s.nbmax, st, clustered).total + 1024 <= 227 * 1024) return st;
+    if (st_layout(s.nbmax, st, clustered, offchip).total + 1024 <= 227 * 1024) return st;
   return 0;
 }
 
@@ -500,7 +513,52 @@ int stages_for(const Shape& s, bool clustered) {
 
 int select_tc_stages(const Shape& s) { return stages_for(s, false); }
 
-bool select_tc_supported(const Shape& s) { return select_tc_stages(s) > 0; }
+// The 8 tokens' block scores fit in shared memory (the coarse-LSE selection
+// needs this: it takes no workspace).
+bool select_tc_onchip(const Shape& s) { return select_tc_stages(s) > 0; }
+
+bool select_tc_supported(const Shape& s) { return select_tc_onchip(s) || stages_for(s, false, true) > 0; }
+
+namespace {
+
+__device__ int g_sm_id_bound;
+
+__global__ void sm_id_bound_kernel() { g_sm_id_bound = static_cast<int>(sm_id_bound()); }
+
+// The bound on SM identifiers of the current device (%nsmid), read once per
+// device by a one-thread kernel on a private stream (no allocation); without
+// a device, twice the SM count.
+int device_sm_id_bound() {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 2 * device_sm_count();
+  if (!cache[dev]) {
+    int n = 0;
+    cudaStream_t st = nullptr;
+    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) == cudaSuccess) {
+      sm_id_bound_kernel<<<1, 1, 0, st>>>();
+      if (cudaMemcpyFromSymbolAsync(&n, g_sm_id_bound, sizeof(int), 0, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+          cudaStreamSynchronize(st) != cudaSuccess)
+        n = 0;
+      cudaStreamDestroy(st);
+    }
+    cudaGetLastError();
+    cache[dev] = n > 0 ? n : 2 * device_sm_count();
+  }
+  return cache[dev];
+}
+
+}  // namespace
+
+// Global scratch for the block scores where they do not fit on chip: one
+// [8][nbmax] slot per SM identifier.
+int select_tc_scratch_slots(const Shape& s) {
+  return (select_tc_onchip(s) || !select_tc_supported(s)) ? 0 : device_sm_id_bound();
+}
+
+size_t select_tc_scratch_bytes(const Shape& s) {
+  return static_cast<size_t>(select_tc_scratch_slots(s)) * kStTokens * s.nbmax * sizeof(float);
+}
 
 // CTAs per 8-token tile: 1 while the tiles alone fill half the SMs (or with
 // the coarse LSE); otherwise the largest cluster (at most 16, at least two
@@ -520,11 +578,15 @@ cudaError_t launch_select_tc(const Shape& s, const CUtensorMap& kc_map, const CU
                              const CUtensorMap& q_map, const SelParams& p, cudaStream_t st) {
   SelParams pp = p;
   if (st_active_clusters(1) < 1) return cudaErrorInvalidConfiguration;
-  pp.csize = select_tc_cluster_size(s, p.sc);
-  pp.stages = stages_for(s, pp.csize > 1);
+  const bool offchip = !select_tc_onchip(s);
+  if (offchip && (p.r_scratch == nullptr || p.sc != 0)) return cudaErrorInvalidConfiguration;
+  if (!offchip) pp.r_scratch = nullptr;
+  pp.r_slots = offchip ? select_tc_scratch_slots(s) : 0;
+  pp.csize = offchip ? 1 : select_tc_cluster_size(s, p.sc);
+  pp.stages = stages_for(s, pp.csize > 1, offchip);
   if (pp.stages == 0) return cudaErrorInvalidConfiguration;
-  int smem = st_layout(s.nbmax, pp.stages, pp.csize > 1).total + 1024;
-  if (pp.csize > 1) smem = std::max(smem, kStClusterMinSmem);
+  int smem = st_layout(s.nbmax, pp.stages, pp.csize > 1, offchip).total + 1024;
+  if (pp.csize > 1 || offchip) smem = std::max(smem, kStClusterMinSmem);   // one CTA per SM
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(((s.nq + kStTokens - 1) / kStTokens) * pp.csize, s.Hkv, s.B);
   cfg.blockDim = dim3(kStThreads, 1, 1);
