@@ -31,7 +31,7 @@
  *   library never allocates, frees or synchronises in these calls; all work
  *   is enqueued on `stream` (a cudaStream_t passed as void*, NULL = legacy
  *   default stream) and the calls return before it runs.  (One exception:
- *   the prefill selection past 261824 tokens of capacity reads the device's
+ *   the prefill selection past 327360 tokens of capacity reads the device's
  *   SM-identifier bound once per device with a small synchronous query on a
  *   private stream; see infllmv2_select_blocks.)
  * - Shapes (row-major, innermost last; d = head_dim, G = group_size,
@@ -149,7 +149,7 @@ int infllmv2_compress_keys(const infllmv2_params* p, const void* k_cache, const 
  * block_scores (nullable) receives r as fp32 [B, Hkv, n_q, n_b(max_kv_len)]
  * (-inf past floor(i/m)).  n_q >= 1; workspace from
  * infllmv2_workspace_size(p, n_q, INFLLMV2_OP_SELECT).  For n_q > 16 the
- * selection keeps 8 tokens' block scores on chip up to max_kv_len 261824
+ * selection keeps 8 tokens' block scores on chip up to max_kv_len 327360
  * (no workspace); above that they take one slot per SM of the workspace
  * (SM identifiers x 8 x n_b(max_kv_len) x 4 bytes), up to about 680K tokens
  * (INFLLMV2_UNSUPPORTED above).  The number of SM identifiers is read from
@@ -201,7 +201,7 @@ int infllmv2_select_blocks_static(const infllmv2_params* p, const void* q, int32
  * the kernel means by coarse / kernel_stride.  The decode path (n_q <= 16)
  * already computes the exact LSE without a second pass over memory, so it
  * has no coarse form (n_q <= 16 returns INFLLMV2_UNSUPPORTED).  Needs no
- * workspace; max_kv_len up to 261824 (the block scores stay on chip).
+ * workspace; max_kv_len up to 327360 (the block scores stay on chip).
  */
 int infllmv2_coarse_means(const infllmv2_params* p, const void* k_cache, const int32_t* kv_lens, int32_t coarse,
                           void* kcc, void* stream);

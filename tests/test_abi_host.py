@@ -162,20 +162,21 @@ def test_append_and_backward_entry_points_validate_first(L):
 
 def test_prefill_selection_capacity_bound(L):
     # Prefill selection (n_q > 16): 8 tokens' block scores on chip up to
-    # 261,824 tokens of capacity (no workspace); past it they take one
+    # 327,360 tokens of capacity (no workspace); past it they take one
     # workspace slot per SM, up to about 680K tokens; the coarse-LSE form
     # takes no workspace and keeps the on-chip bound.
-    ok = _params(L, batch=1, hkv=1, lmax=250_000)
-    assert L.lib.infllmv2_workspace_size(ctypes.byref(ok), 100, L.OP_SELECT) == 0
-    p = _params(L, batch=1, hkv=1, lmax=300_000)
+    for lmax in (250_000, 327_360):
+        ok = _params(L, batch=1, hkv=1, lmax=lmax)
+        assert L.lib.infllmv2_workspace_size(ctypes.byref(ok), 100, L.OP_SELECT) == 0
+    p = _params(L, batch=1, hkv=1, lmax=327_361)
     need = L.lib.infllmv2_workspace_size(ctypes.byref(p), 100, L.OP_SELECT)
-    assert need >= 8 * ((300_000 + 63) // 64) * 4
+    assert need >= 8 * ((327_361 + 63) // 64) * 4
     rc = L.lib.infllmv2_select_blocks(ctypes.byref(p), FAKE, 100, FAKE, FAKE, FAKE, FAKE, None, None, 0, None)
     assert rc == L.WORKSPACE_TOO_SMALL
     rc = L.lib.infllmv2_select_blocks_coarse_lse(ctypes.byref(p), FAKE, 100, FAKE, 64, FAKE, FAKE, FAKE, FAKE, None,
                                                  None)
     assert rc == L.UNSUPPORTED
-    assert b"261824" in L.lib.infllmv2_last_error()
+    assert b"327360" in L.lib.infllmv2_last_error()
     big = _params(L, batch=1, hkv=1, lmax=1_000_000)
     rc = L.lib.infllmv2_select_blocks(ctypes.byref(big), FAKE, 100, FAKE, FAKE, FAKE, FAKE, None, None, 0, None)
     assert rc == L.UNSUPPORTED

@@ -99,6 +99,9 @@ SELECT_CASES = [
     (2, 2, 40000, [40000, 9000], 5, 32, True, None),
     (1, 2, 30000, [30000], 12, 64, False, None),        # a partial second tile
     (1, 1, 20000, [20000], 40, 16, False, None),        # prefill-path n_q
+    # 80 tiles (no cluster) with 1563 blocks of scores per token: too many for
+    # two CTAs per SM, so one CTA per SM with a three-chunk ring.
+    (1, 2, 100000, [100000], 320, 32, False, None),
 ]
 
 
@@ -117,13 +120,13 @@ def test_select_blocks_parity(dev, case):
 
 
 def test_prefill_selection_past_on_chip_capacity(dev):
-    # 270,000 tokens of capacity (4219 blocks): past the 4091 blocks whose 8
+    # 340,000 tokens of capacity (5313 blocks): past the 5115 blocks whose 8
     # tokens' block scores fit in shared memory, the prefill-path selection
     # keeps them in one workspace slot per SM.  Ragged lengths; the selection
     # (with its scores) and the attention on it against the oracle.
     import torch
-    inp = S.make_random(batch=2, n_kv_heads=2, kv_len=270000, n_q=24, topk=48, includes_forced=False, seed=91,
-                        kv_lens=[270000, 151000])
+    inp = S.make_random(batch=2, n_kv_heads=2, kv_len=340000, n_q=24, topk=48, includes_forced=False, seed=91,
+                        kv_lens=[340000, 151000])
     run = DeviceRun(inp, dev)
     assert run.T.workspace_size(run.p, 24, run.T.OP_SELECT) > 0
     run.compress()

@@ -400,15 +400,14 @@ int infllmv2_select_blocks_coarse_lse(const infllmv2_params* p, const void* q, i
       return fail(INFLLMV2_UNSUPPORTED, "max_kv_len must hold a kernel and a coarse window");
     if (!select_tc_onchip(s))
       return fail(INFLLMV2_UNSUPPORTED,
-                  "the coarse-LSE selection keeps 8 tokens' block scores on chip: max_kv_len up to 261824");
+                  "the coarse-LSE selection keeps 8 tokens' block scores on chip: max_kv_len up to 327360");
     uint32_t* status = status_ptr();
     if (!status) return fail(INFLLMV2_CUDA_ERROR, "no device status word (no current CUDA device?)");
-    CUtensorMap kcm, kccm, qm;
-    if ((rc = make_map(&qm, q, static_cast<uint64_t>(s.B) * s.nq * s.Hkv * kGroup, 16, "q"))) return rc;
+    CUtensorMap kcm, kccm;
     if ((rc = make_map(&kcm, kc, static_cast<uint64_t>(s.B) * s.Hkv * 2 * s.ncmax, 64, "kc"))) return rc;
     if ((rc = make_map(&kccm, kcc, static_cast<uint64_t>(s.B) * s.Hkv * 2 * (s.Lmax / coarse), 64, "kcc")))
       return rc;
-    cudaError_t e = launch_select_coarse(s, kcm, kccm, coarse, qm, kv_lens, block_idx, n_selected, block_scores,
+    cudaError_t e = launch_select_coarse(s, kcm, kccm, coarse, q, kv_lens, block_idx, n_selected, block_scores,
                                          status, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "select_blocks_coarse_lse");
     return INFLLMV2_OK;

@@ -35,7 +35,7 @@ constexpr int kSelDecodeMaxNq = 16;   // n_q at or below this uses the decode pa
 
 size_t select_workspace_bytes(const Shape& s);
 // The prefill selection (n_q > 16) keeps 8 tokens' block scores in shared
-// memory: at most 4091 blocks (261824 tokens) of cache capacity.
+// memory: at most 5115 blocks (327360 tokens) of cache capacity.
 bool select_tc_supported(const Shape& s);
 bool select_tc_onchip(const Shape& s);   // the prefill path's block scores fit in shared memory
 bool select_supported(const Shape& s);
@@ -46,7 +46,7 @@ cudaError_t launch_select(const Shape& s, const CUtensorMap& kc_map, const CUten
 // Prefill path (n_q > 16) with the per-head LSE taken over coarse kernels of
 // sc keys (kcc_map over [B, Hkv, 2, Lmax / sc, 128]).
 cudaError_t launch_select_coarse(const Shape& s, const CUtensorMap& kc_map, const CUtensorMap& kcc_map, int sc,
-                                 const CUtensorMap& q_map, const int32_t* kv_lens, int32_t* block_idx,
+                                 const void* q, const int32_t* kv_lens, int32_t* block_idx,
                                  int32_t* n_sel, float* block_scores, uint32_t* status, cudaStream_t st);
 
 // ---- stage 3 ---------------------------------------------------------------

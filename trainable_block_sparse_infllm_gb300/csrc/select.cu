@@ -36,7 +36,7 @@ int device_sm_count() {
 int select_tc_cluster_size(const Shape& s, int sc);
 size_t select_tc_scratch_bytes(const Shape& s);
 cudaError_t launch_select_tc(const Shape& s, const CUtensorMap& kc_map, const CUtensorMap& kcc_map,
-                             const CUtensorMap& q_map, const SelParams& p, cudaStream_t st);
+                             const SelParams& p, cudaStream_t st);
 size_t select_decode_ncpad(const Shape& s);
 bool select_decode_supported(const Shape& s);
 cudaError_t launch_select_decode(const Shape& s, const CUtensorMap& kc_map, const CUtensorMap& q_map,
@@ -85,7 +85,6 @@ cudaError_t launch_select(const Shape& s, const CUtensorMap& kc_map, const CUten
                           const void* q, const int32_t* kv_lens, int32_t* block_idx,
                           int32_t* n_sel, float* block_scores, void* ws, uint32_t* status,
                           cudaStream_t st) {
-  (void)q;
   SelParams p{};
   p.B = s.B;
   p.Hkv = s.Hkv;
@@ -105,8 +104,9 @@ cudaError_t launch_select(const Shape& s, const CUtensorMap& kc_map, const CUten
   p.status = status;
   p.write_r = block_scores != nullptr;
   p.r_buf = block_scores;
+  p.q = static_cast<const uint16_t*>(q);
 
-  if (use_tc_cluster(s)) return launch_select_tc(s, kc_map, kc_map, q_map, p, st);
+  if (use_tc_cluster(s)) return launch_select_tc(s, kc_map, kc_map, p, st);
   if (use_verify_path(s))
     return launch_select_verify(s, select_verify_cluster_size(s), kc_map, q_map, kv_lens, block_idx, n_sel,
                                 block_scores, status, st);
@@ -117,11 +117,11 @@ cudaError_t launch_select(const Shape& s, const CUtensorMap& kc_map, const CUten
   }
   if (!select_tc_supported(s)) return cudaErrorInvalidConfiguration;   // rejected by the entry points
   p.r_scratch = static_cast<float*>(ws);
-  return launch_select_tc(s, kc_map, kc_map, q_map, p, st);
+  return launch_select_tc(s, kc_map, kc_map, p, st);
 }
 
 cudaError_t launch_select_coarse(const Shape& s, const CUtensorMap& kc_map, const CUtensorMap& kcc_map, int sc,
-                                 const CUtensorMap& q_map, const int32_t* kv_lens, int32_t* block_idx,
+                                 const void* q, const int32_t* kv_lens, int32_t* block_idx,
                                  int32_t* n_sel, float* block_scores, uint32_t* status, cudaStream_t st) {
   SelParams p{};
   p.B = s.B;
@@ -142,10 +142,11 @@ cudaError_t launch_select_coarse(const Shape& s, const CUtensorMap& kc_map, cons
   p.status = status;
   p.write_r = block_scores != nullptr;
   p.r_buf = block_scores;
+  p.q = static_cast<const uint16_t*>(q);
   p.sc = sc;
   p.nccmax = s.Lmax / sc;
   if (!select_tc_onchip(s)) return cudaErrorInvalidConfiguration;   // rejected by the entry point
-  return launch_select_tc(s, kc_map, kcc_map, q_map, p, st);
+  return launch_select_tc(s, kc_map, kcc_map, p, st);
 }
 
 }  // namespace infllmv2

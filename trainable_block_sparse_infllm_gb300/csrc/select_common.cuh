@@ -29,6 +29,8 @@ struct SelParams {
   int csize;           // prefill path: CTAs per 8-token tile (1, or a cluster splitting the chunks)
   float* r_scratch;    // prefill path: block scores off chip, [r_slots][8][nbmax] (null: in shared memory)
   int r_slots;         // slots of r_scratch (one per SM identifier)
+  int r_rows;          // prefill path: tokens whose block scores a CTA keeps in shared memory
+  const uint16_t* q;   // prefill path: q as bf16 bits, [B*nq*Hkv*16][128]
   uint32_t* status;
 };
 

@@ -13,7 +13,10 @@
 // the 128 rows of the tcgen05 tile and share every 64-kernel chunk of kernel
 // means (causality gives the 8 tokens the same kernels but for the last one
 // or two).  z = q . hi + q . lo accumulates in TMEM (M 128, N 64, K 128, hi and
-// lo as two products into one accumulator).  The chunks are streamed twice:
+// lo as two products into one accumulator); q, the A operand, sits in TMEM
+// too (the row warps write it there), so shared memory holds only the chunk
+// ring and the block scores and two CTAs fit on an SM while the scores are
+// small.  The chunks are streamed twice:
 //   pass 1: each row thread keeps its head's running (max, sum of 2^z)
 //           (over coarse windows instead, for the LSE approximation);
 //   pass 2: each row thread forms 2^(z - lse) for its head, and the 16 lanes
@@ -50,19 +53,22 @@ constexpr int kStChunkBytes = 32768;       // hi then lo: 64 rows x 256 B each
 constexpr int kStRowWarps = 8;             // two per TMEM lane quadrant, 32 of a chunk's 64 kernels each
 constexpr int kStThreads = (kStRowWarps + 2) * 32;
 constexpr int kStMmaWarp = kStRowWarps, kStTmaWarp = kStRowWarps + 1;
-constexpr uint32_t kStTmemCols = 128;      // two z buffers of 64 columns
+constexpr uint32_t kStTmemCols = 256;      // two z buffers of 64 columns, then q
+constexpr uint32_t kStColQ = 128;          // q: 128 rows x 128 dims as bf16 pairs (the A operand)
+constexpr int kStTwoPerSmSmem = 112 * 1024;   // a request this small leaves room for a second CTA on the SM
 
 struct StLayout {
-  int ring, q, r, flag, tk, ctk, cbits, csurv, xch, lse_in, tails, bars, slot, total;
+  int ring, r, flag, tk, ctk, cbits, csurv, xch, lse_in, tails, bars, slot, total;
 };
 constexpr int kStMaxC = 16;
-constexpr int kStClusterMinSmem = 116 * 1024;   // a cluster launch requests at least this: one CTA per SM
+constexpr int kStOnePerSmSmem = 116 * 1024;     // a request this large leaves no room for a second CTA
 
 // The top-k flags and scratch overlay the chunk ring, which is idle once the
 // last chunk's products are done (every row warp has waited for them before
 // its top-k).
-// offchip: the block scores live in global scratch (r_scratch), not here.
-__host__ __device__ inline StLayout st_layout(int nbmax, int stages, bool clustered, bool offchip = false) {
+// r_rows: tokens whose block scores this CTA holds (8; in a cluster of C
+// the ceil(8 / C) it owns; 0 when they live in global scratch).
+__host__ __device__ inline StLayout st_layout(int nbmax, int stages, bool clustered, int r_rows) {
   StLayout l;
   l.ring = 0;
   l.flag = 0;                                           // [8 tokens][nbmax] top-k flags (in the ring)
@@ -70,16 +76,15 @@ __host__ __device__ inline StLayout st_layout(int nbmax, int stages, bool cluste
   l.ctk = 0;                                            // cluster form: the CTA-wide top-k scratch (in the ring)
   l.cbits = (static_cast<int>(sizeof(SmemTopkScratch<kStThreads>)) + 15) & ~15;
   l.csurv = l.cbits + (((nbmax + 31) / 32 * 4 + 15) & ~15);
-  l.q = stages * kStChunkBytes;                         // two 64-column boxes x 128 rows
-  l.r = l.q + 32768;                                    // [8 tokens][nbmax] block scores
-  l.xch = (l.r + (offchip ? 0 : kStTokens * nbmax * 4) + 15) & ~15;   // [2][128] (max, sum)
+  l.r = stages * kStChunkBytes;                         // [r_rows][nbmax] block scores
+  l.xch = (l.r + r_rows * nbmax * 4 + 15) & ~15;        // [2][128] (max, sum)
   l.lse_in = l.xch + 2 * 128 * 8;                       // cluster form: [C][128 rows] (max, sum)
   l.tails = l.lse_in + (clustered ? kStMaxC * 128 * 8 : 0);   // cluster form: [C][8 tokens] last-kernel g
   l.bars = l.tails + (clustered ? kStMaxC * kStTokens * 4 : 0);
   l.slot = l.bars + 16 * 8;
   l.total = l.slot + 16;
   const int ring_need = clustered ? l.csurv + nbmax * 8 : l.tk + kStTokens * static_cast<int>(sizeof(WarpTopkScratch));
-  if (ring_need > l.q) l.total = 1 << 30;               // does not fit: never chosen
+  if (ring_need > stages * kStChunkBytes) l.total = 1 << 30;   // does not fit: never chosen
   return l;
 }
 
@@ -92,14 +97,14 @@ __device__ __forceinline__ void quad_pair_sync(int q) {
 }
 static_assert(kStNumBars <= 16, "barrier area holds 16");
 
-__global__ void __launch_bounds__(kStThreads, 1)
+__global__ void __launch_bounds__(kStThreads, 2)
     sel_tc_kernel(const __grid_constant__ CUtensorMap kc_map, const __grid_constant__ CUtensorMap kcc_map,
-                  const __grid_constant__ CUtensorMap q_map, SelParams p) {
+                  SelParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int S = p.stages;
   const int csize = p.csize;
-  const StLayout lay = st_layout(p.nbmax, S, csize > 1, p.r_scratch != nullptr);
+  const StLayout lay = st_layout(p.nbmax, S, csize > 1, p.r_rows);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + lay.bars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + lay.slot);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -124,6 +129,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
   }
   float* r_all = p.r_scratch ? p.r_scratch + static_cast<size_t>(slot) * kStTokens * p.nbmax
                              : reinterpret_cast<float*>(smem + lay.r);
+  const int r_rows = p.r_scratch ? kStTokens : p.r_rows;
   const int L = p.kv_lens[b];
 
   if (L < nq || L > p.Lmax) {   // the same in every CTA of a cluster: none touches another's memory
@@ -153,16 +159,15 @@ __global__ void __launch_bounds__(kStThreads, 1)
   const int seg_c = nch_a + (need_b ? nch_my : 0);
   const int total = nch_my > 0 ? seg_c + nch_my : 0;
 
-  for (int e = tid; e < kStTokens * p.nbmax; e += kStThreads) r_all[e] = -INFINITY;
+  for (int e = tid; e < r_rows * p.nbmax; e += kStThreads) r_all[e] = -INFINITY;
   if (tid == 0) {
     prefetch_tensormap(&kc_map);
     if (p.sc) prefetch_tensormap(&kcc_map);
-    prefetch_tensormap(&q_map);
     for (int s = 0; s < S; ++s) {
       mbar_init(&bars[kFull + s], 1);
       mbar_init(&bars[kEmpty + s], 1);
     }
-    mbar_init(&bars[kQ], 1);
+    mbar_init(&bars[kQ], kStRowWarps);   // q written to TMEM by the row warps
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars[kZFull + s], 1);
       mbar_init(&bars[kZFree + s], kStRowWarps);
@@ -189,13 +194,6 @@ __global__ void __launch_bounds__(kStThreads, 1)
   if (warp == kStTmaWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && total > 0) {
-      const int Hq = p.Hkv * kGroup;
-      mbar_arrive_expect_tx(&bars[kQ], n_act * 4096);
-      for (int tt = 0; tt < n_act; ++tt) {
-        const int row = (b * nq + t0 + tt) * Hq + h * kGroup;
-        tma_load_2d(smem + lay.q + tt * 2048, &q_map, 0, row, &bars[kQ]);
-        tma_load_2d(smem + lay.q + 16384 + tt * 2048, &q_map, 64, row, &bars[kQ]);
-      }
       for (int it = 0; it < total; ++it) {
         const int st = it % S;
         if (it >= S && !mbar_wait(&bars[kEmpty + st], ((it / S) - 1) & 1, p.status)) break;
@@ -218,7 +216,6 @@ __global__ void __launch_bounds__(kStThreads, 1)
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0 && total > 0) {
       constexpr uint32_t kId = tc::idesc_bf16(128, 64, 0, 0);
-      const uint64_t q_desc = tc::sdesc_sw128(base_s + lay.q, 16, 1024);
       bool ok = mbar_wait(&bars[kQ], 0, p.status);
       for (int it = 0; it < total && ok; ++it) {
         const int st = it % S, zb = it & 1;
@@ -231,10 +228,11 @@ __global__ void __launch_bounds__(kStThreads, 1)
         const uint64_t lo_desc = tc::sdesc_sw128(stage + 16384, 16, 1024);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint64_t ta = static_cast<uint64_t>(((k >> 2) * 16384 + (k & 3) * 32) >> 4);
+          // A: q from TMEM (16 dims = 8 columns per step); B: the chunk's
+          // hi and lo rows, dims 16 k .. 16 k + 15 of the 64-dim boxes.
           const uint64_t tb = static_cast<uint64_t>(((k >> 2) * 8192 + (k & 3) * 32) >> 4);
-          tc::mma_ss(tmem + zb * 64, q_desc + ta, hi_desc + tb, kId, k > 0 ? 1u : 0u);
-          tc::mma_ss(tmem + zb * 64, q_desc + ta, lo_desc + tb, kId, 1u);
+          tc::mma_ts(tmem + zb * 64, tmem + kStColQ + 8 * k, hi_desc + tb, kId, k > 0 ? 1u : 0u);
+          tc::mma_ts(tmem + zb * 64, tmem + kStColQ + 8 * k, lo_desc + tb, kId, 1u);
         }
         tc::commit(&bars[kZFull + zb]);
         tc::commit(&bars[kEmpty + st]);
@@ -257,7 +255,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
     const bool coarse_t = nvis_c_t > 0;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
     float2* xch = reinterpret_cast<float2*>(smem + lay.xch);
-    float* r_tok = r_all + tok * p.nbmax;
+    float* r_tok = r_all + (tok / csize) * p.nbmax;   // in the owner's rows (token t: CTA t mod C, row t / C)
     const int col0 = 32 * hf;
     // The kernel left of this half's first block: column 31 of the same
     // chunk for the upper half; for the lower half, column 63 of the
@@ -266,6 +264,31 @@ __global__ void __launch_bounds__(kStThreads, 1)
     float m = -INFINITY, l = 0.f, lse2 = -INFINITY;
     float carry = -INFINITY;
     bool ok = true;
+    // q of this row, dims 64 hf .. 64 hf + 63, into TMEM columns
+    // kStColQ + 32 hf .. + 31 as bf16 pairs: the A operand of the products.
+    if (total > 0) {
+      uint32_t w[32];
+      if (active) {
+        const size_t row = (static_cast<size_t>(b) * nq + t0 + tok) * (p.Hkv * kGroup) + h * kGroup + x;
+        const uint4* src = reinterpret_cast<const uint4*>(p.q + row * 128 + 64 * hf);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 u = __ldg(src + i);
+          w[4 * i] = u.x;
+          w[4 * i + 1] = u.y;
+          w[4 * i + 2] = u.z;
+          w[4 * i + 3] = u.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) w[i] = 0u;
+      }
+      tc::st32(lane_addr + kStColQ + 32 * hf, w);
+      tc::wait_st();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kQ]);
+    }
     // End of pass 1: merge the two halves' (max, sum) of each row; in a
     // cluster also the C CTAs' partials of the row.
     auto end_pass1 = [&]() {
@@ -441,7 +464,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
     const float* tails = reinterpret_cast<const float*>(smem + lay.tails);
 #pragma unroll 1
     for (int tt = rank; tt < n_act; tt += csize) {
-      float* rw = r_all + tt * p.nbmax;
+      float* rw = r_all + (tt / csize) * p.nbmax;
       const int i_t = L - nq + t0 + tt, c = i_t / kBlock;
       if (tid == 0) {   // the block after CTA q's range, with q's last kernel (CTAs without chunks share an end)
         const int nvis = n_complete_kernels(i_t + 1);
@@ -468,10 +491,11 @@ __global__ void __launch_bounds__(kStThreads, 1)
   }
 }
 
-// Clusters of C CTAs resident at once on the current device (cached; a
-// cluster launch runs one CTA per SM).
-int st_active_clusters(int C) {
-  static int cache[64][kStMaxC + 1];
+// Clusters of C CTAs of `smem` bytes each resident at once on the current
+// device (cached per device, C and smem class: up to kStTwoPerSmSmem, two
+// CTAs fit on an SM; past it one).
+int st_active_clusters(int C, int smem) {
+  static int cache[64][2][kStMaxC + 1];
   static bool done[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
@@ -479,45 +503,62 @@ int st_active_clusters(int C) {
     const bool ok =
         cudaFuncSetAttribute(sel_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) == cudaSuccess &&
         cudaFuncSetAttribute(sel_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
-    for (int c = 1; c <= kStMaxC; ++c) {
-      int n = 0;
-      if (ok) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(c, 1, 1);
-        cfg.blockDim = dim3(kStThreads, 1, 1);
-        cfg.dynamicSmemBytes = kStClusterMinSmem;
-        cudaLaunchAttribute a[1];
-        a[0].id = cudaLaunchAttributeClusterDimension;
-        a[0].val.clusterDim.x = c;
-        a[0].val.clusterDim.y = 1;
-        a[0].val.clusterDim.z = 1;
-        cfg.attrs = a;
-        cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&n, sel_tc_kernel, &cfg) != cudaSuccess) n = 0;
+    for (int k = 0; k < 2; ++k)
+      for (int c = 1; c <= kStMaxC; ++c) {
+        int n = 0;
+        if (ok) {
+          cudaLaunchConfig_t cfg = {};
+          cfg.gridDim = dim3(c, 1, 1);
+          cfg.blockDim = dim3(kStThreads, 1, 1);
+          cfg.dynamicSmemBytes = k == 0 ? kStTwoPerSmSmem : kStOnePerSmSmem;
+          cudaLaunchAttribute a[1];
+          a[0].id = cudaLaunchAttributeClusterDimension;
+          a[0].val.clusterDim.x = c;
+          a[0].val.clusterDim.y = 1;
+          a[0].val.clusterDim.z = 1;
+          cfg.attrs = a;
+          cfg.numAttrs = 1;
+          if (cudaOccupancyMaxActiveClusters(&n, sel_tc_kernel, &cfg) != cudaSuccess) n = 0;
+        }
+        cache[dev][k][c] = n;
       }
-      cache[dev][c] = n;
-    }
     cudaGetLastError();
     done[dev] = true;
   }
-  return cache[dev][C];
+  return cache[dev][smem <= kStTwoPerSmSmem ? 0 : 1][C];
 }
 
-int stages_for(const Shape& s, bool clustered, bool offchip = false) {
-  for (int st = kStMaxStages; st >= 2; --st)
-    if (st_layout(s.nbmax, st, clustered, offchip).total + 1024 <= 227 * 1024) return st;
-  return 0;
+// Pipeline depth and dynamic shared memory of a launch with C CTAs per tile.
+// Two stages when that leaves room for a second CTA on the SM (each SM then
+// streams four chunks at once and overlaps one CTA's row work with the
+// other's products); else the deepest ring that fits.  Off chip the block
+// scores take one global slot per SM, so one CTA per SM (padded to
+// kStOnePerSmSmem).
+struct StConfig {
+  int stages, smem, r_rows;
+};
+
+StConfig st_config(const Shape& s, int csize, bool offchip) {
+  StConfig c{0, 0, offchip ? 0 : (kStTokens + csize - 1) / csize};
+  const bool clustered = csize > 1;
+  const int two = st_layout(s.nbmax, 2, clustered, c.r_rows).total + 1024;
+  if (!offchip && two <= kStTwoPerSmSmem) return StConfig{2, two, c.r_rows};
+  for (int st = kStMaxStages; st >= 2; --st) {
+    const int t = st_layout(s.nbmax, st, clustered, c.r_rows).total + 1024;
+    if (t <= 227 * 1024) return StConfig{st, offchip ? std::max(t, kStOnePerSmSmem) : t, c.r_rows};
+  }
+  return c;
 }
 
 }  // namespace
 
-int select_tc_stages(const Shape& s) { return stages_for(s, false); }
+int select_tc_stages(const Shape& s) { return st_config(s, 1, false).stages; }
 
 // The 8 tokens' block scores fit in shared memory (the coarse-LSE selection
 // needs this: it takes no workspace).
 bool select_tc_onchip(const Shape& s) { return select_tc_stages(s) > 0; }
 
-bool select_tc_supported(const Shape& s) { return select_tc_onchip(s) || stages_for(s, false, true) > 0; }
+bool select_tc_supported(const Shape& s) { return select_tc_onchip(s) || st_config(s, 1, true).stages > 0; }
 
 namespace {
 
@@ -564,29 +605,32 @@ size_t select_tc_scratch_bytes(const Shape& s) {
 // the coarse LSE); otherwise the largest cluster (at most 16, at least two
 // chunks per CTA) with which every tile's cluster is resident at once.
 int select_tc_cluster_size(const Shape& s, int sc) {
-  if (sc != 0 || stages_for(s, true) == 0) return 1;
+  if (sc != 0) return 1;
   const long long units = static_cast<long long>((s.nq + kStTokens - 1) / kStTokens) * s.B * s.Hkv;
   if (units * 2 > device_sm_count()) return 1;
   const int nch = (s.ncmax + kStChunk - 1) / kStChunk;
-  for (int C = std::min(kStMaxC, nch / 2); C >= 2; --C)
-    if (st_active_clusters(C) >= units) return C;
+  for (int C = std::min(kStMaxC, nch / 2); C >= 2; --C) {
+    const StConfig c = st_config(s, C, false);
+    if (c.stages > 0 && st_active_clusters(C, c.smem) >= units) return C;
+  }
   return 1;
 }
 
 // p.sc > 0: coarse-window LSE from kcc_map (else kcc_map is not read).
 cudaError_t launch_select_tc(const Shape& s, const CUtensorMap& kc_map, const CUtensorMap& kcc_map,
-                             const CUtensorMap& q_map, const SelParams& p, cudaStream_t st) {
+                             const SelParams& p, cudaStream_t st) {
   SelParams pp = p;
-  if (st_active_clusters(1) < 1) return cudaErrorInvalidConfiguration;
+  if (st_active_clusters(1, kStOnePerSmSmem) < 1 || p.q == nullptr) return cudaErrorInvalidConfiguration;
   const bool offchip = !select_tc_onchip(s);
   if (offchip && (p.r_scratch == nullptr || p.sc != 0)) return cudaErrorInvalidConfiguration;
   if (!offchip) pp.r_scratch = nullptr;
   pp.r_slots = offchip ? select_tc_scratch_slots(s) : 0;
   pp.csize = offchip ? 1 : select_tc_cluster_size(s, p.sc);
-  pp.stages = stages_for(s, pp.csize > 1, offchip);
-  if (pp.stages == 0) return cudaErrorInvalidConfiguration;
-  int smem = st_layout(s.nbmax, pp.stages, pp.csize > 1, offchip).total + 1024;
-  if (pp.csize > 1 || offchip) smem = std::max(smem, kStClusterMinSmem);   // one CTA per SM
+  const StConfig c = st_config(s, pp.csize, offchip);
+  if (c.stages == 0) return cudaErrorInvalidConfiguration;
+  pp.stages = c.stages;
+  pp.r_rows = c.r_rows;
+  const int smem = c.smem;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(((s.nq + kStTokens - 1) / kStTokens) * pp.csize, s.Hkv, s.B);
   cfg.blockDim = dim3(kStThreads, 1, 1);
@@ -603,7 +647,7 @@ cudaError_t launch_select_tc(const Shape& s, const CUtensorMap& kc_map, const CU
   attrs[1].val.clusterDim.z = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = pp.csize > 1 ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, sel_tc_kernel, kc_map, kcc_map, q_map, pp);
+  return cudaLaunchKernelEx(&cfg, sel_tc_kernel, kc_map, kcc_map, pp);
 }
 
 }  // namespace infllmv2
