@@ -125,25 +125,6 @@ __device__ __forceinline__ void pair_sync(int q) {
   asm volatile("bar.sync %0, 64;" ::"r"(q + 1) : "memory");
 }
 
-// 2^x on the FMA pipe, for x <= 9 (probabilities after the lazy rescale):
-// x = n + f with n = rint(x), |f| <= 1/2, and 2^f = e^(f ln 2) by its Taylor
-// series to degree 5 (relative error below 4e-6 for |f| <= 1/2), scaled by 2^n
-// through the exponent field; x < -125 (and x = -inf) gives 0.
-__device__ __forceinline__ float exp2_fma(float x) {
-  x = fmaxf(x, -127.f);
-  const float n = rintf(x);
-  const float f = x - n;
-  constexpr float c1 = 0.6931471805599453f, c2 = 0.2402265069591007f, c3 = 0.05550410866482158f;
-  constexpr float c4 = 0.009618129107628477f, c5 = 0.0013333558146428443f;
-  float y = fmaf(c5, f, c4);
-  y = fmaf(y, f, c3);
-  y = fmaf(y, f, c2);
-  y = fmaf(y, f, c1);
-  y = fmaf(y, f, 1.0f);
-  const int e = static_cast<int>(n);
-  return e < -125 ? 0.f : __int_as_float(__float_as_int(y) + (e << 23));
-}
-
 // bf16 pair of the rounding residues p - bf16(p) of two probabilities whose
 // rounded pair is `hi` (pack_bf16x2 order: p0 in the low half).
 __device__ __forceinline__ uint32_t lo_bf16x2(float p0, float p1, uint32_t hi) {
@@ -153,8 +134,11 @@ __device__ __forceinline__ uint32_t lo_bf16x2(float p0, float p1, uint32_t hi) {
 
 // One warp's 64 probabilities of its row for an item (bf16 pairs into w),
 // returning their sum.  whole: the row sees all 64 keys or none (sel false),
-// so no per-key mask; otherwise keys [0, nv) count.  Three in eight
-// exponentials go through the FMA pipe to share the load with the MUFU unit.
+// so no per-key mask; otherwise keys [0, nv) count.  Every exponential
+// goes to the MUFU unit: in a sparse union about half the warps skip each
+// block, which leaves the unit room, and a polynomial on the FMA pipe costs
+// a dozen instructions per value (with half of the values on it the 32K
+// prefill launch took 6.66 ms, against 5.46 ms).
 // kSplit: the lo parts p - bf16(p) go to TMEM at lo_addr, 16 pairs at a time.
 template <bool kSplit>
 __device__ __forceinline__ float row_probs(const uint32_t (&s)[64], uint32_t (&w)[32], bool whole, bool sel,
@@ -171,8 +155,8 @@ __device__ __forceinline__ float row_probs(const uint32_t (&s)[64], uint32_t (&w
       for (int x = x0; x < x0 + 16; ++x) {
         const float a0 = fmaf(__uint_as_float(s[2 * x]), scale2, -m_eff);
         const float a1 = fmaf(__uint_as_float(s[2 * x + 1]), scale2, -m_eff);
-        const float p0 = ((x & 3) == 3) ? exp2_fma(a0) : fast_exp2(a0);
-        const float p1 = ((x & 3) != 0) ? exp2_fma(a1) : fast_exp2(a1);
+        const float p0 = fast_exp2(a0);
+        const float p1 = fast_exp2(a1);
         ls0 += p0;
         ls1 += p1;
         w[x] = pack_bf16x2(p0, p1);
