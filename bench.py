@@ -770,45 +770,54 @@ def main():
 
     # End to end through the public API with host buffers: per step the new
     # token's q, k, v come from pinned host memory (k, v appended to the
-    # cache) and the attention output goes back to pinned host memory.
+    # cache) and the attention output goes back to pinned host memory.  Each
+    # step is two launches: the cache append, which reads the step's q, k and
+    # v from pinned host memory (q into the device buffer the step reads), and
+    # the decode step, which stores its output into pinned host memory.  Steps
+    # are batched into CUDA graphs exactly as in the device-timed leg: one
+    # graph of REPLICAS steps over the rotating replicas (single-step graphs
+    # for a remainder).  A graph per step would add its own launch (about
+    # 4.6 us on this path) to every step.
     B, H, nq, d = wl.batch, wl.n_kv_heads, wl.n_q, wl.head_dim
-    # Each step's inputs (q and the new token's key and value per sequence)
-    # sit back to back in pinned host memory: one copy in, the cache append and
-    # the step as one graph, one copy of the output back.
-    # Each step is one graph of two launches: the cache append, which reads
-    # the step's q, k and v from pinned host memory (q into the device buffer
-    # the step reads), and the decode step, which stores its output into
-    # pinned host memory.
     in_h = torch.empty((REPLICAS, bench.reps[0]["packed"].numel()), dtype=torch.bfloat16).pin_memory()
     out_h = torch.empty((REPLICAS,) + tuple(bench.reps[0]["out"].shape), dtype=torch.bfloat16).pin_memory()
     for r in range(REPLICAS):
         in_h[r].copy_(bench.reps[r]["packed"])
     torch.cuda.synchronize()
-    graphs_e2e = []
     nq_el, kv_el = bench.reps[0]["q"].numel(), bench.reps[0]["k_new"].numel()
-    for r in range(REPLICAS):
+
+    def e2e_one(r):
         rep = bench.reps[r]
         q_h = in_h[r][:nq_el].view(rep["q"].shape)
         k_h = in_h[r][nq_el:nq_el + kv_el].view(rep["k_new"].shape)
         v_h = in_h[r][nq_el + kv_el:].view(rep["v_new"].shape)
+        T.append_kv(bench.p, k_h, v_h, bench.lens, rep["k"], rep["v"], q_src=q_h, q_dst=rep["q"])
+        T.decode_step(bench.p, rep["q"], rep["k"], rep["v"], bench.lens, rep["kc"], rep["idx"], rep["nsel"],
+                      out_h[r], None, rep["ws_step"])
+
+    graphs_e2e = []
+    for r in range(REPLICAS):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            T.append_kv(bench.p, k_h, v_h, bench.lens, rep["k"], rep["v"], q_src=q_h, q_dst=rep["q"])
-            T.decode_step(bench.p, rep["q"], rep["k"], rep["v"], bench.lens, rep["kc"], rep["idx"], rep["nsel"],
-                          out_h[r], None, rep["ws_step"])
+            e2e_one(r)
         graphs_e2e.append(g)
+    round_e2e = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(round_e2e):
+        for r in range(REPLICAS):
+            e2e_one(r)
     torch.cuda.synchronize()
 
-    def e2e_step(i):
-        graphs_e2e[i % REPLICAS].replay()
+    def e2e_steps(n):
+        for _ in range(n // REPLICAS):
+            round_e2e.replay()
+        for x in range(n % REPLICAS):
+            graphs_e2e[x].replay()
 
-    for i in range(args.warmup):
-        e2e_step(i)
+    e2e_steps(max(args.warmup, REPLICAS))
     torch.cuda.synchronize()
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     f0.record()
-    for i in range(args.steps):
-        e2e_step(i)
+    e2e_steps(args.steps)
     f1.record()
     torch.cuda.synchronize()
     t_e2e = max_over_ranks(f0.elapsed_time(f1) * 1e-3, dist, dev)
@@ -867,7 +876,8 @@ def main():
         "e2e": {"value": world * tokens_per_step * args.steps / t_e2e, "unit": "tokens/s",
                 "h2d_bytes_per_step": int(in_h[0].numel() * 2),
                 "d2h_bytes_per_step": int(out_h[0].numel() * 2), "wall_s": wall,
-                "transfers": "the append kernel reads q, k, v from pinned host memory; the step stores its output there"},
+                "transfers": "the append kernel reads q, k, v from pinned host memory; the step stores its output there",
+                "graph": f"append + decode_step per step, {REPLICAS} steps per CUDA graph as in the device-timed leg"},
         "prefill": prefill,
     }
     line["workloads"] = workloads
