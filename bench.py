@@ -771,13 +771,12 @@ def main():
     # End to end through the public API with host buffers: per step the new
     # token's q, k, v come from pinned host memory (k, v appended to the
     # cache) and the attention output goes back to pinned host memory.  Each
-    # step is two launches: the cache append, which reads the step's q, k and
-    # v from pinned host memory (q into the device buffer the step reads), and
-    # the decode step, which stores its output into pinned host memory.  Steps
-    # are batched into CUDA graphs exactly as in the device-timed leg: one
-    # graph of REPLICAS steps over the rotating replicas (single-step graphs
-    # for a remainder).  A graph per step would add its own launch (about
-    # 4.6 us on this path) to every step.
+    # step is one launch of infllmv2_append_decode_step, which reads q, k and v
+    # from pinned host memory, writes k and v into the caches and stores its
+    # output into pinned host memory.  Steps are batched into CUDA graphs
+    # exactly as in the device-timed leg: one graph of REPLICAS steps over the
+    # rotating replicas (single-step graphs for a remainder).  A graph per step
+    # would add its own launch (about 4.6 us on this path) to every step.
     B, H, nq, d = wl.batch, wl.n_kv_heads, wl.n_q, wl.head_dim
     in_h = torch.empty((REPLICAS, bench.reps[0]["packed"].numel()), dtype=torch.bfloat16).pin_memory()
     out_h = torch.empty((REPLICAS,) + tuple(bench.reps[0]["out"].shape), dtype=torch.bfloat16).pin_memory()
@@ -791,9 +790,8 @@ def main():
         q_h = in_h[r][:nq_el].view(rep["q"].shape)
         k_h = in_h[r][nq_el:nq_el + kv_el].view(rep["k_new"].shape)
         v_h = in_h[r][nq_el + kv_el:].view(rep["v_new"].shape)
-        T.append_kv(bench.p, k_h, v_h, bench.lens, rep["k"], rep["v"], q_src=q_h, q_dst=rep["q"])
-        T.decode_step(bench.p, rep["q"], rep["k"], rep["v"], bench.lens, rep["kc"], rep["idx"], rep["nsel"],
-                      out_h[r], None, rep["ws_step"])
+        T.append_decode_step(bench.p, q_h, k_h, v_h, rep["k"], rep["v"], bench.lens, rep["kc"], rep["idx"],
+                             rep["nsel"], out_h[r], None)
 
     graphs_e2e = []
     for r in range(REPLICAS):
@@ -876,8 +874,9 @@ def main():
         "e2e": {"value": world * tokens_per_step * args.steps / t_e2e, "unit": "tokens/s",
                 "h2d_bytes_per_step": int(in_h[0].numel() * 2),
                 "d2h_bytes_per_step": int(out_h[0].numel() * 2), "wall_s": wall,
-                "transfers": "the append kernel reads q, k, v from pinned host memory; the step stores its output there",
-                "graph": f"append + decode_step per step, {REPLICAS} steps per CUDA graph as in the device-timed leg"},
+                "transfers": "one launch per step (infllmv2_append_decode_step): it reads q, k, v from pinned host "
+                             "memory, appends k, v to the caches and stores its output there",
+                "graph": f"{REPLICAS} steps per CUDA graph as in the device-timed leg"},
         "prefill": prefill,
     }
     line["workloads"] = workloads

@@ -19,7 +19,8 @@
  *                                   partitioning, eq. B_j; > Complexity analysis]
  *
  * Around them: infllmv2_append_kv and infllmv2_decode_step (a whole decode
- * step, one launch for n_q = 1), infllmv2_coarse_means and
+ * step, one launch for n_q = 1), infllmv2_append_decode_step (both as one
+ * launch), infllmv2_coarse_means and
  * infllmv2_select_blocks_coarse_lse (the coarse-kernel LSE approximation),
  * and infllmv2_sparse_attn_backward (gradients of stage 3 with the selection
  * fixed [InfLLM v2 > Training-time considerations]).
@@ -284,6 +285,31 @@ int infllmv2_decode_step(const infllmv2_params* p, const void* q, int32_t n_q, c
                          const void* v_cache, const int32_t* kv_lens, void* kc, int32_t* block_idx,
                          int32_t* n_selected, void* out, float* lse, void* workspace,
                          size_t workspace_bytes, void* stream);
+
+/*
+ * infllmv2_append_kv followed by infllmv2_decode_step for one new token per
+ * sequence (n_q = 1), as a single launch of the decode step's cluster form
+ * [InfLLM v2 > Block-level key-value partitioning: the cache grows by the
+ * decoded token; the step's stages as for infllmv2_decode_step].
+ *   q       bf16 [batch, 1, Hq, d]: the token's queries.
+ *   k_new, v_new  bf16 [batch, n_kv_heads, 1, d]: its key and value, written
+ *           to cache row kv_lens[b] - 1 of k_cache / v_cache (kv_lens
+ *           already counts the token); the step reads the key from k_new
+ *           where it needs it before the store is visible.
+ *   q, k_new and v_new are read with ordinary loads and out / lse written
+ *   with ordinary stores, so any of them may be page-locked host memory mapped
+ *   for the device: a step whose inputs and result live in host memory is one
+ *   launch and no copy.  kc, block_idx, n_selected, out, lse: as for
+ *   infllmv2_decode_step.  No workspace.
+ * INFLLMV2_UNSUPPORTED for n_q != 1 or a shape outside the single-launch
+ * form (see infllmv2_decode_step): call infllmv2_append_kv and
+ * infllmv2_decode_step there.  A sequence whose kv_lens[b] lies outside
+ * [1, max_kv_len] is left untouched (no row written, out zero, block_idx
+ * -1) and sets INFLLMV2_DEVICE_BAD_KV_LEN.
+ */
+int infllmv2_append_decode_step(const infllmv2_params* p, const void* q, int32_t n_q, const void* k_new,
+                                const void* v_new, void* k_cache, void* v_cache, const int32_t* kv_lens, void* kc,
+                                int32_t* block_idx, int32_t* n_selected, void* out, float* lse, void* stream);
 
 /*
  * Backward of stage 3 with the selection held fixed [InfLLM v2 >

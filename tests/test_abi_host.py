@@ -147,6 +147,14 @@ def test_append_and_backward_entry_points_validate_first(L):
     assert app(ctypes.byref(p), 0, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None) == L.INVALID_ARGUMENT
     assert app(ctypes.byref(p), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == L.INVALID_ARGUMENT  # q_src alone
     assert app(ctypes.byref(p), 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE_ODD, FAKE, None) == L.UNSUPPORTED
+    # The one-launch append + step: one token per sequence, every pointer but lse.
+    ads = L.lib.infllmv2_append_decode_step
+    args = [FAKE] * 9   # k_new, v_new, k_cache, v_cache, kv_lens, kc, block_idx, n_selected, out
+    assert len(ads.argtypes) == 3 + len(args) + 2
+    assert ads(ctypes.byref(p), FAKE, 1, None, *args[1:], None, None) == L.INVALID_ARGUMENT
+    assert ads(ctypes.byref(p), FAKE, 2, *args, None, None) == L.UNSUPPORTED
+    assert b"n_q = 1" in L.lib.infllmv2_last_error()
+    assert ads(ctypes.byref(p), FAKE_ODD, 1, *args, None, None) == L.UNSUPPORTED
     bwd = L.lib.infllmv2_sparse_attn_backward
     # q, n_q, then k_cache, v_cache, kv_lens, block_idx, n_selected, out, lse, dout, dq, dk, dv
     ptrs = [FAKE] * 11

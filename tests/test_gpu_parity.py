@@ -530,6 +530,50 @@ def test_append_kv_then_decode_step(dev, nq):
     assert torch.equal(run.out.view(torch.int16), out_ref.view(torch.int16))
 
 
+@pytest.mark.parametrize("where", ["device", "host"])
+def test_append_decode_step_one_launch(dev, where):
+    # The cache append fused into the decode step gives the caches, kernel
+    # means, selection, output and lse of the step on a cache that already
+    # held the token.  The appended rows start out as NaN in the caches; with
+    # lengths 4096 and 2080 the newest kernel ends on the appended key, with
+    # 3000 it does not.  "host": q, k_new, v_new, out and lse in pinned host
+    # memory.
+    import torch
+    import trainable_block_sparse_infllm_gb300 as T
+    inp = S.make_random(batch=3, n_kv_heads=2, kv_len=4096, n_q=1, topk=16, seed=57, kv_lens=[4096, 3000, 2080])
+    run = DeviceRun(inp, dev)
+    full_k, full_v = run.k.clone(), run.v.clone()
+    kc_full = run.blank_step_kernels()
+    run.step()
+    torch.cuda.synchronize()
+    assert torch.equal(run.kc.view(torch.int16), kc_full.view(torch.int16))
+    out_ref, lse_ref = run.out.clone(), run.lse.clone()
+    idx_ref, nsel_ref = run.idx.clone(), run.nsel.clone()
+    k_new = torch.stack([full_k[b, :, int(L) - 1:int(L)] for b, L in enumerate(inp.kv_lens)]).contiguous()
+    v_new = torch.stack([full_v[b, :, int(L) - 1:int(L)] for b, L in enumerate(inp.kv_lens)]).contiguous()
+    q = run.q.clone()
+    out = torch.full_like(run.out, float("nan"))
+    lse = torch.full_like(run.lse, float("nan"))
+    if where == "host":
+        k_new, v_new, q = k_new.cpu().pin_memory(), v_new.cpu().pin_memory(), q.cpu().pin_memory()
+        out, lse = out.cpu().pin_memory(), lse.cpu().pin_memory()
+    run.blank_step_kernels()
+    for b, L in enumerate(inp.kv_lens):
+        run.k[b, :, int(L) - 1].view(torch.int16).fill_(0x7FC0)
+        run.v[b, :, int(L) - 1].view(torch.int16).fill_(0x7FC0)
+    run.idx.fill_(-7)
+    run.nsel.fill_(-7)
+    T.append_decode_step(run.p, q, k_new, v_new, run.k, run.v, run.lens, run.kc, run.idx, run.nsel, out, lse)
+    torch.cuda.synchronize()
+    assert T.get_device_status(clear=True) == 0
+    assert torch.equal(run.k.view(torch.int16), full_k.view(torch.int16))
+    assert torch.equal(run.v.view(torch.int16), full_v.view(torch.int16))
+    assert torch.equal(run.kc.view(torch.int16), kc_full.view(torch.int16))
+    assert torch.equal(run.idx, idx_ref) and torch.equal(run.nsel, nsel_ref)
+    assert torch.equal(out.to(dev).view(torch.int16), out_ref.view(torch.int16))
+    assert torch.equal(lse.to(dev), lse_ref)
+
+
 def test_append_kv_bad_kv_len(dev):
     import torch
     import trainable_block_sparse_infllm_gb300 as T

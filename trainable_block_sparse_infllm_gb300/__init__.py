@@ -11,6 +11,7 @@ memory and streams.  Entry points mirror the C names:
     sparse_attn_prefill  stage 3 for prefill
     append_kv            write the newest tokens' keys and values to the caches
     decode_step          stages 1-3 for the newest token(s), one launch when n_q = 1
+    append_decode_step   the cache append and stages 1-3 for one new token, one launch
     coarse_means, select_blocks_coarse_lse
                          the coarse-kernel LSE approximation (prefill path)
     sparse_attn_backward dq, dk, dv of stage 3 with the selection held fixed
@@ -34,7 +35,7 @@ __all__ = [
     "Params", "InfLLMv2Error", "make_params", "num_kernels", "max_selected", "workspace_size",
     "alloc_kc", "alloc_workspace", "compress_keys", "select_blocks", "sparse_attn_decode",
     "sparse_attn_prefill", "decode_step", "coarse_means", "alloc_kcc", "select_blocks_coarse_lse",
-    "sparse_attn_backward", "append_kv", "get_device_status", "OP_SELECT", "OP_DECODE", "OP_PREFILL",
+    "sparse_attn_backward", "append_kv", "append_decode_step", "get_device_status", "OP_SELECT", "OP_DECODE", "OP_PREFILL",
     "OP_DECODE_STEP", "OP_BACKWARD", "DECODE_MAX_NQ", "is_checked_build", "test_hooks",
 ]
 
@@ -205,6 +206,20 @@ def append_kv(p: Params, k_new, v_new, kv_lens, k_cache, v_cache, q_src=None, q_
                                            _ptr(v_new, host_ok=True), _ptr(kv_lens), _ptr(k_cache),
                                            _ptr(v_cache), _ptr(q_src, host_ok=True), _ptr(q_dst), _stream(stream)))
     return k_cache, v_cache
+
+
+def append_decode_step(p: Params, q, k_new, v_new, k_cache, v_cache, kv_lens, kc, block_idx, n_selected, out,
+                       lse=None, stream=None):
+    """append_kv then decode_step for one new token per sequence, as one launch.
+
+    ``q`` [B, 1, Hq, d], ``k_new`` / ``v_new`` [B, Hkv, 1, d] may be pinned host
+    tensors, like ``out`` and ``lse``; the token's key and value go to cache
+    rows kv_lens - 1."""
+    _lib.check(_lib.lib.infllmv2_append_decode_step(
+        ctypes.byref(p), _ptr(q, host_ok=True), q.shape[1], _ptr(k_new, host_ok=True), _ptr(v_new, host_ok=True),
+        _ptr(k_cache), _ptr(v_cache), _ptr(kv_lens), _ptr(kc), _ptr(block_idx), _ptr(n_selected),
+        _ptr(out, host_ok=True), _ptr(lse, host_ok=True), _stream(stream)))
+    return block_idx, n_selected, out, lse
 
 
 def sparse_attn_backward(p: Params, q, k_cache, v_cache, kv_lens, block_idx, n_selected, out, lse, dout,

@@ -103,6 +103,8 @@ lib.infllmv2_decode_step.argtypes = [_P, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp
 lib.infllmv2_decode_step.restype = ctypes.c_int
 lib.infllmv2_append_kv.argtypes = [_P, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
 lib.infllmv2_append_kv.restype = ctypes.c_int
+lib.infllmv2_append_decode_step.argtypes = [_P, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+lib.infllmv2_append_decode_step.restype = ctypes.c_int
 lib.infllmv2_sparse_attn_backward.argtypes = [_P, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                               _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
 lib.infllmv2_sparse_attn_backward.restype = ctypes.c_int
@@ -119,7 +121,7 @@ EXPORTED = (
     "infllmv2_select_blocks_static",
     "infllmv2_sparse_attn_decode", "infllmv2_sparse_attn_prefill", "infllmv2_decode_step",
     "infllmv2_coarse_means", "infllmv2_select_blocks_coarse_lse", "infllmv2_sparse_attn_backward",
-    "infllmv2_append_kv",
+    "infllmv2_append_kv", "infllmv2_append_decode_step",
     "infllmv2_status_string",
     "infllmv2_last_error", "infllmv2_get_device_status",
 )

@@ -489,7 +489,7 @@ int infllmv2_decode_step(const infllmv2_params* p, const void* q, int32_t n_q, c
     cudaError_t e;
     if (cluster) {
       e = launch_decode_step(s, cluster, kcm, qm, km, vm, k_cache, kv_lens, kc, block_idx, n_selected, out, lse,
-                             status, g_test_flags.load(), st);
+                             nullptr, status, g_test_flags.load(), st);
       if (e != cudaSuccess) return cuda_fail(e, "decode_step");
       return INFLLMV2_OK;
     }
@@ -502,6 +502,43 @@ int infllmv2_decode_step(const infllmv2_params* p, const void* q, int32_t n_q, c
     e = launch_attn(s, false, qm, km, vm, kv_lens, block_idx, n_selected, out, lse,
                     static_cast<unsigned char*>(workspace) + sel_ws, status, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode_step (attend)");
+    return INFLLMV2_OK;
+  });
+}
+
+int infllmv2_append_decode_step(const infllmv2_params* p, const void* q, int32_t n_q, const void* k_new,
+                                const void* v_new, void* k_cache, void* v_cache, const int32_t* kv_lens, void* kc,
+                                int32_t* block_idx, int32_t* n_selected, void* out, float* lse, void* stream) {
+  INFLLMV2_GUARD({
+    Shape s;
+    int rc = check_params(p, n_q, &s);
+    if (rc) return rc;
+    if (!q || !k_new || !v_new || !k_cache || !v_cache || !kv_lens || !kc || !block_idx || !n_selected || !out)
+      return fail(INFLLMV2_INVALID_ARGUMENT, "a required pointer is NULL");
+    if (n_q != 1)
+      return fail(INFLLMV2_UNSUPPORTED,
+                  "append_decode_step takes n_q = 1 (got %d): use infllmv2_append_kv and infllmv2_decode_step", n_q);
+    if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        !aligned16(kc) || !aligned16(out))
+      return fail(INFLLMV2_UNSUPPORTED, "q, k_new, v_new, k_cache, v_cache, kc and out must be 16-byte aligned");
+    if (s.ncmax < 1) return fail(INFLLMV2_UNSUPPORTED, "max_kv_len must hold at least one semantic kernel");
+    const int cluster = decode_step_cluster_size(s);
+    if (!cluster)
+      return fail(INFLLMV2_UNSUPPORTED,
+                  "the one-launch step does not fit this shape: use infllmv2_append_kv and infllmv2_decode_step");
+    uint32_t* status = status_ptr();
+    if (!status) return fail(INFLLMV2_CUDA_ERROR, "no device status word (no current CUDA device?)");
+    CUtensorMap kcm, km, vm;
+    const uint64_t kv_rows = static_cast<uint64_t>(s.B) * s.Hkv * s.Lmax;
+    if ((rc = make_map(&kcm, kc, static_cast<uint64_t>(s.B) * s.Hkv * 2 * s.ncmax, 64, "kc"))) return rc;
+    if ((rc = make_map(&km, k_cache, kv_rows, 64, "k_cache"))) return rc;
+    if ((rc = make_map(&vm, v_cache, kv_rows, 64, "v_cache"))) return rc;
+    const DsAppend app{q, k_new, v_new, k_cache, v_cache};
+    // q is read with ordinary loads (it may sit in host memory): the q map
+    // slot of the kernel takes the key map, which it then leaves unused.
+    cudaError_t e = launch_decode_step(s, cluster, kcm, km, km, vm, k_cache, kv_lens, kc, block_idx, n_selected,
+                                       out, lse, &app, status, g_test_flags.load(), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "append_decode_step");
     return INFLLMV2_OK;
   });
 }

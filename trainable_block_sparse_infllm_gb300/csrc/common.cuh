@@ -87,6 +87,13 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Orders this thread's ordinary global accesses with its TMA (async proxy)
+// accesses: after ordinary stores that another thread's TMA will read (with
+// a release / acquire between them), and before a TMA load of such data.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier --
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

@@ -22,16 +22,21 @@ __device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4& w) {
 
 // fp32 sum over keys tok0 .. tok0 + 15 of dims [8 sub, 8 sub + 8) of one
 // (b, h_kv) key plane `kbh` ([L_max][128] bf16).  Two batches of eight loads.
+// Key `row_new` (if in range) is read from `k_row_new` (a 128-dim bf16 row)
+// instead of the plane: a key this launch appends and has not yet stored.
 __device__ __forceinline__ void chunk_sum16(float (&acc)[8], const __nv_bfloat16* __restrict__ kbh, int tok0,
-                                            int sub) {
+                                            int sub, int row_new = -1, const uint4* k_row_new = nullptr) {
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] = 0.f;
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     uint4 w[kStride / 2];
 #pragma unroll
-    for (int t = 0; t < kStride / 2; ++t)
-      w[t] = __ldg(reinterpret_cast<const uint4*>(kbh + static_cast<size_t>(tok0 + half * 8 + t) * kHeadDim) + sub);
+    for (int t = 0; t < kStride / 2; ++t) {
+      const int tok = tok0 + half * 8 + t;
+      w[t] = tok == row_new ? k_row_new[sub]
+                            : __ldg(reinterpret_cast<const uint4*>(kbh + static_cast<size_t>(tok) * kHeadDim) + sub);
+    }
 #pragma unroll
     for (int t = 0; t < kStride / 2; ++t) add_bf16x8(acc, w[t]);
   }

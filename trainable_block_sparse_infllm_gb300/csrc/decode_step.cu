@@ -15,8 +15,14 @@
 // 64k - 1 .. 64k + 63).  One 192 KB region of shared memory serves, in turn,
 // the phase-A ring and scores, the block scores and top-k scratch, and the
 // attention stages.
+//   append    (infllmv2_append_decode_step only) the phase-A warps load q
+//             with ordinary loads instead of the TMA, since it may sit in
+//             host memory; CTA 0 stores the token's key and value rows into
+//             the caches, which the other CTAs' TMA loads read only after
+//             the cluster barrier that follows phase A.
 //   compress  the CTA whose chunks hold the newest complete kernel recomputes
-//             it from the keys with the compression kernel's arithmetic,
+//             it from the keys with the compression kernel's arithmetic
+//             (an appended key taken from its source row),
 //             stores it in the kernel-mean planes and patches its own
 //             shared-memory copy of the chunk.
 //   phase A   hi/lo chunks streamed by TMA through a 4-stage ring (the rest
@@ -114,6 +120,14 @@ struct DsParams {
   float* lse;
   uint32_t* status;
   uint32_t test_flags;   // checked build: kTestWithholdArrive makes a bounded wait expire
+  // Fused cache append (all null when the caller has appended the token):
+  // the newest token's q, k and v rows, read with ordinary loads (they may be
+  // page-locked host memory), and the caches that take its k and v.
+  const uint4* q_src;    // [B][Hq][16 chunks]
+  const uint4* k_new;    // [B * Hkv][16 chunks]
+  const uint4* v_new;
+  uint4* k_w;            // the k and v caches, [B * Hkv * Lmax][16 chunks]
+  uint4* v_w;
 };
 
 // Fault injection of the checked build's own tests: warp 0 of every CTA
@@ -244,7 +258,7 @@ __global__ void __launch_bounds__(kDsThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kDsAWarps);
     }
-    mbar_init(qbar, 1);
+    mbar_init(qbar, p.q_src ? kDsAWarps : 1);   // the q tile: one TMA load, or the phase-A warps' stores
     for (int s = 0; s < kDsPairs; ++s) mbar_init(&kvfull[s], 1);
     mbar_init(lbar, 1);
     mbar_init(sbar, 1);
@@ -256,7 +270,16 @@ __global__ void __launch_bounds__(kDsThreads, 1)
   __syncthreads();
   pdl_wait();
   pdl_trigger();
-  if (tid == 0) {   // Q does not depend on the length: start it first
+  if (p.q_src) {
+    // Fused append: the group's 16 q rows (4 KB) by the phase-A warps, one
+    // 16-byte chunk per thread, into the layout the TMA load would give.
+    if (warp < kDsAWarps) {
+      const int r = tid >> 4, ch = tid & 15;
+      *reinterpret_cast<uint4*>(smem + lay.q + swz128_offset(r, ch, kGroup)) = p.q_src[(orow + r) * 16 + ch];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qbar);
+    }
+  } else if (tid == 0) {   // Q does not depend on the length: start it first
     mbar_arrive_expect_tx(qbar, 4096);
     tma_load_2d(smem + lay.q, &q_map, 0, static_cast<int>(orow), qbar);
     tma_load_2d(smem + lay.q + 2048, &q_map, 64, static_cast<int>(orow), qbar);
@@ -312,6 +335,19 @@ __global__ void __launch_bounds__(kDsThreads, 1)
     tma_load_2d(dst + 24576, &kc_map, 64, (bh * 2 + 1) * p.ncmax + row, &full[st]);
   };
   const int kv_row0 = bh * p.Lmax;
+  if (p.k_new && rank == 0 && warp == 10) {
+    // Fused append: the token's key and value rows into the caches (row
+    // L - 1).  Other CTAs' TMA loads read them only after the cluster barrier
+    // that follows phase A (release here, acquire there); the newest kernel
+    // below takes the key from k_new itself.
+    const size_t row = static_cast<size_t>(kv_row0) + (L - 1);
+    const int ch = lane & 15;
+    if (lane < 16)
+      p.k_w[row * 16 + ch] = p.k_new[static_cast<size_t>(bh) * 16 + ch];
+    else
+      p.v_w[row * 16 + ch] = p.v_new[static_cast<size_t>(bh) * 16 + ch];
+    fence_proxy_async_global();
+  }
   if (warp == 9) {
     // The forced blocks are known now: their K/V head for L2 at once, each
     // from one CTA of the cluster.
@@ -347,7 +383,8 @@ __global__ void __launch_bounds__(kDsThreads, 1)
     const __nv_bfloat16* kbh = p.k + static_cast<size_t>(bh) * p.Lmax * kHeadDim;
     const int sub = lane & 15, half = lane >> 4;
     float acc[8], oth[8];
-    chunk_sum16(acc, kbh, (jn + half) * kStride, sub);
+    chunk_sum16(acc, kbh, (jn + half) * kStride, sub, p.k_new ? L - 1 : -1,
+                p.k_new ? p.k_new + static_cast<size_t>(bh) * 16 : nullptr);
 #pragma unroll
     for (int e = 0; e < 8; ++e) oth[e] = __shfl_down_sync(0xffffffffu, acc[e], 16);
     if (half == 0) {
@@ -489,6 +526,7 @@ __global__ void __launch_bounds__(kDsThreads, 1)
     st_dsmem_f32x2(dsmem_addr(&lse_in[rank * kGroup + (tid % kGroup)], tid / kGroup), cpart[tid % kGroup]);
   cluster_arrive();
   cluster_wait();
+  if (p.k_new) fence_proxy_async_global();   // the appended rows, before this CTA's TMA loads of them
   if (tid < kGroup * kDsMaxC) {   // head tid / 16, CTA tid % 16: a shuffle tree over the C partials
     const int q = tid % kDsMaxC, hd = tid / kDsMaxC;
     const float2 v = q < C ? lse_in[q * kGroup + hd] : make_float2(-INFINITY, 0.f);
@@ -1017,7 +1055,8 @@ int decode_step_cluster_size(const Shape& s) {
 cudaError_t launch_decode_step(const Shape& s, int cluster, const CUtensorMap& kc_map, const CUtensorMap& q_map,
                                const CUtensorMap& k_map, const CUtensorMap& v_map, const void* k,
                                const int32_t* kv_lens, void* kc, int32_t* block_idx, int32_t* n_sel, void* out,
-                               float* lse, uint32_t* status, uint32_t test_flags, cudaStream_t st) {
+                               float* lse, const DsAppend* append, uint32_t* status, uint32_t test_flags,
+                               cudaStream_t st) {
   if (cluster < 1 || cluster > kDsMaxC || !ds_fits(s, cluster) || ds_active_clusters(cluster) < 1)
     return cudaErrorInvalidConfiguration;
   DsParams p{};
@@ -1042,6 +1081,13 @@ cudaError_t launch_decode_step(const Shape& s, int cluster, const CUtensorMap& k
   p.lse = lse;
   p.status = status;
   p.test_flags = test_flags;
+  if (append) {
+    p.q_src = static_cast<const uint4*>(append->q);
+    p.k_new = static_cast<const uint4*>(append->k_new);
+    p.v_new = static_cast<const uint4*>(append->v_new);
+    p.k_w = static_cast<uint4*>(append->k_cache);
+    p.v_w = static_cast<uint4*>(append->v_cache);
+  }
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attrs[2];
   ds_config(s, cluster, &cfg, attrs, st);

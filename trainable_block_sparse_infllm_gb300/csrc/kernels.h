@@ -74,10 +74,21 @@ cudaError_t launch_append(const Shape& s, const void* k_new, const void* v_new, 
 // Cluster size of the single-launch form on the current device (16 or 8),
 // or 0 when it does not apply to this shape.
 int decode_step_cluster_size(const Shape& s);
+// The cache append fused into the decode step: the newest token's q, k and
+// v (device or page-locked host memory) and the caches k and v go into.
+struct DsAppend {
+  const void* q;
+  const void* k_new;
+  const void* v_new;
+  void* k_cache;
+  void* v_cache;
+};
+// append: null when the caller has appended the token (q_map then covers q).
 cudaError_t launch_decode_step(const Shape& s, int cluster, const CUtensorMap& kc_map, const CUtensorMap& q_map,
                                const CUtensorMap& k_map, const CUtensorMap& v_map, const void* k,
                                const int32_t* kv_lens, void* kc, int32_t* block_idx, int32_t* n_sel, void* out,
-                               float* lse, uint32_t* status, uint32_t test_flags, cudaStream_t st);
+                               float* lse, const DsAppend* append, uint32_t* status, uint32_t test_flags,
+                               cudaStream_t st);
 
 // ---- backward of stage 3 (fixed selection) --------------------------------
 size_t attn_bwd_workspace_bytes(const Shape& s);
