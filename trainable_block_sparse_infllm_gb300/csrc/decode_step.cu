@@ -203,6 +203,10 @@ __device__ __forceinline__ void tma_block(uint8_t* stage, const CUtensorMap* kma
   tma_load_2d(stage + 24576, vmap, 64, row, bar);
 }
 
+// kAppend: the cache append is fused in (a separate instantiation, so the
+// plain step carries none of its code: this kernel's one-pass code is paced
+// by instruction fetch).
+template <bool kAppend>
 __global__ void __launch_bounds__(kDsThreads, 1)
     decode_step_kernel(const __grid_constant__ CUtensorMap kc_map, const __grid_constant__ CUtensorMap q_map,
                        const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
@@ -258,7 +262,7 @@ __global__ void __launch_bounds__(kDsThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kDsAWarps);
     }
-    mbar_init(qbar, p.q_src ? kDsAWarps : 1);   // the q tile: one TMA load, or the phase-A warps' stores
+    mbar_init(qbar, kAppend ? kDsAWarps : 1);   // the q tile: one TMA load, or the phase-A warps' stores
     for (int s = 0; s < kDsPairs; ++s) mbar_init(&kvfull[s], 1);
     mbar_init(lbar, 1);
     mbar_init(sbar, 1);
@@ -270,7 +274,7 @@ __global__ void __launch_bounds__(kDsThreads, 1)
   __syncthreads();
   pdl_wait();
   pdl_trigger();
-  if (p.q_src) {
+  if (kAppend) {
     // Fused append: the group's 16 q rows (4 KB) by the phase-A warps, one
     // 16-byte chunk per thread, into the layout the TMA load would give.
     if (warp < kDsAWarps) {
@@ -335,7 +339,7 @@ __global__ void __launch_bounds__(kDsThreads, 1)
     tma_load_2d(dst + 24576, &kc_map, 64, (bh * 2 + 1) * p.ncmax + row, &full[st]);
   };
   const int kv_row0 = bh * p.Lmax;
-  if (p.k_new && rank == 0 && warp == 10) {
+  if (kAppend && rank == 0 && warp == 10) {
     // Fused append: the token's key and value rows into the caches (row
     // L - 1).  Other CTAs' TMA loads read them only after the cluster barrier
     // that follows phase A (release here, acquire there); the newest kernel
@@ -383,8 +387,10 @@ __global__ void __launch_bounds__(kDsThreads, 1)
     const __nv_bfloat16* kbh = p.k + static_cast<size_t>(bh) * p.Lmax * kHeadDim;
     const int sub = lane & 15, half = lane >> 4;
     float acc[8], oth[8];
-    chunk_sum16(acc, kbh, (jn + half) * kStride, sub, p.k_new ? L - 1 : -1,
-                p.k_new ? p.k_new + static_cast<size_t>(bh) * 16 : nullptr);
+    if (kAppend)
+      chunk_sum16(acc, kbh, (jn + half) * kStride, sub, L - 1, p.k_new + static_cast<size_t>(bh) * 16);
+    else
+      chunk_sum16(acc, kbh, (jn + half) * kStride, sub);
 #pragma unroll
     for (int e = 0; e < 8; ++e) oth[e] = __shfl_down_sync(0xffffffffu, acc[e], 16);
     if (half == 0) {
@@ -526,7 +532,7 @@ __global__ void __launch_bounds__(kDsThreads, 1)
     st_dsmem_f32x2(dsmem_addr(&lse_in[rank * kGroup + (tid % kGroup)], tid / kGroup), cpart[tid % kGroup]);
   cluster_arrive();
   cluster_wait();
-  if (p.k_new) fence_proxy_async_global();   // the appended rows, before this CTA's TMA loads of them
+  if (kAppend) fence_proxy_async_global();   // the appended rows, before this CTA's TMA loads of them
   if (tid < kGroup * kDsMaxC) {   // head tid / 16, CTA tid % 16: a shuffle tree over the C partials
     const int q = tid % kDsMaxC, hd = tid / kDsMaxC;
     const float2 v = q < C ? lse_in[q * kGroup + hd] : make_float2(-INFINITY, 0.f);
@@ -999,10 +1005,10 @@ int ds_active_clusters(int C) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (!done[dev]) {
-    bool ok = cudaFuncSetAttribute(decode_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDsSmem) ==
-                  cudaSuccess &&
-              cudaFuncSetAttribute(decode_step_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
-                  cudaSuccess;
+    bool ok = true;
+    for (auto* fn : {decode_step_kernel<false>, decode_step_kernel<true>})
+      ok = ok && cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kDsSmem) == cudaSuccess &&
+           cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
     for (int c = 1; c <= kDsMaxC; ++c) {
       int n = 0;
       if (ok) {
@@ -1013,7 +1019,7 @@ int ds_active_clusters(int C) {
         cudaLaunchAttribute attrs[2];
         ds_config(s, c, &cfg, attrs, nullptr);
         cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&n, decode_step_kernel, &cfg) != cudaSuccess) n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, decode_step_kernel<false>, &cfg) != cudaSuccess) n = 0;
       }
       cache[dev][c] = n;
     }
@@ -1091,7 +1097,8 @@ cudaError_t launch_decode_step(const Shape& s, int cluster, const CUtensorMap& k
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attrs[2];
   ds_config(s, cluster, &cfg, attrs, st);
-  return cudaLaunchKernelEx(&cfg, decode_step_kernel, kc_map, q_map, k_map, v_map, p);
+  return append ? cudaLaunchKernelEx(&cfg, decode_step_kernel<true>, kc_map, q_map, k_map, v_map, p)
+                : cudaLaunchKernelEx(&cfg, decode_step_kernel<false>, kc_map, q_map, k_map, v_map, p);
 }
 
 }  // namespace infllmv2
