@@ -99,6 +99,10 @@ SELECT_CASES = [
     (2, 2, 40000, [40000, 9000], 5, 32, True, None),
     (1, 2, 30000, [30000], 12, 64, False, None),        # a partial second tile
     (1, 1, 20000, [20000], 40, 16, False, None),        # prefill-path n_q
+    # Short caches cap the cluster: 3 CTAs (each owning 3 tokens' score
+    # rows) and 2 CTAs (4 rows each).
+    (4, 2, 6000, [6000, 5000, 4100, 3000], 24, 16, True, None),
+    (2, 2, 4500, [4500, 2600], 20, 12, False, None),
     # 80 tiles (no cluster) with 1563 blocks of scores per token: too many for
     # two CTAs per SM, so one CTA per SM with a three-chunk ring.
     (1, 2, 100000, [100000], 320, 32, False, None),
