@@ -321,6 +321,32 @@ def test_decode_step_bad_kv_len(dev):
     assert run.nsel[0].eq(4).all().item()
 
 
+def test_append_decode_step_bad_kv_len(dev):
+    # A sequence whose kv_len lies past max_kv_len: status flagged, its caches
+    # untouched, an empty selection and a zero output; the other sequence's
+    # row is appended.
+    import torch
+    import trainable_block_sparse_infllm_gb300 as T
+    inp = S.make_random(batch=2, n_kv_heads=1, kv_len=1000, n_q=1, topk=4, seed=4, kv_lens=[1000, 900])
+    run = DeviceRun(inp, dev)
+    run.compress()
+    k0, v0 = run.k.clone(), run.v.clone()
+    k_new = torch.randn((2, 1, 1, 128), device=dev).to(torch.bfloat16)
+    v_new = torch.randn((2, 1, 1, 128), device=dev).to(torch.bfloat16)
+    run.lens[1] = 1001
+    out = torch.full_like(run.out, float("nan"))
+    T.append_decode_step(run.p, run.q, k_new, v_new, run.k, run.v, run.lens, run.kc, run.idx, run.nsel, out)
+    torch.cuda.synchronize()
+    assert T.get_device_status(clear=True) & T.DEVICE_BAD_KV_LEN
+    assert torch.equal(run.k[1].view(torch.int16), k0[1].view(torch.int16))
+    assert torch.equal(run.v[1].view(torch.int16), v0[1].view(torch.int16))
+    assert run.nsel[1].eq(0).all().item() and run.idx[1].eq(-1).all().item()
+    assert out[1].float().eq(0).all().item()
+    assert torch.equal(run.k[0, :, 999].view(torch.int16), k_new[0, :, 0].view(torch.int16))
+    assert torch.equal(run.v[0, :, 999].view(torch.int16), v_new[0, :, 0].view(torch.int16))
+    assert torch.isfinite(out[0].float()).all().item()
+
+
 # --------------------------------------------------------- full workloads ----
 
 @pytest.mark.parametrize("name", ["decode_4k", "decode_32k", "decode_128k", "verify_128k"])
