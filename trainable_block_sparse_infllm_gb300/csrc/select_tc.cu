@@ -48,7 +48,7 @@ namespace {
 
 constexpr int kStTokens = 8;
 constexpr int kStChunk = 64;               // kernels per chunk
-constexpr int kStMaxStages = 3;            // fewer when the block scores of a long cache need the room
+constexpr int kStMaxStages = 3;            // ring depth at one CTA per SM (two stages when two CTAs fit)
 constexpr int kStChunkBytes = 32768;       // hi then lo: 64 rows x 256 B each
 constexpr int kStRowWarps = 8;             // two per TMEM lane quadrant, 32 of a chunk's 64 kernels each
 constexpr int kStThreads = (kStRowWarps + 2) * 32;
@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(kStThreads, 2)
   pdl_wait();   // the previous kernel of the stream may still be writing the inputs
   pdl_trigger();
   // Block scores of the tile's 8 tokens: in shared memory, or past that
-  // capacity in this SM's slot of the global scratch (the kernel needs more
+  // capacity in this SM's slot of the global scratch (that form requests more
   // than half an SM's shared memory, so no two of its CTAs share an SM).
   const uint32_t slot = sm_id();
   if (p.r_scratch && slot >= static_cast<uint32_t>(p.r_slots)) {   // cannot happen with slots from %nsmid
