@@ -159,6 +159,29 @@ __global__ void __launch_bounds__(kStThreads, 2)
   const int seg_c = nch_a + (need_b ? nch_my : 0);
   const int total = nch_my > 0 ? seg_c + nch_my : 0;
 
+  // Each row thread's q (dims 64 hf .. 64 hf + 63 of row r = token r / 16,
+  // head r % 16; see the row warps below): loaded now, so that the loads
+  // land while the barriers and TMEM are set up, and stored to TMEM there.
+  uint32_t qw[32];
+  if (warp < kStRowWarps && total > 0) {
+    const int r = (warp & 3) * 32 + lane, tok = r >> 4, hf = warp >> 2;
+    if (tok < n_act) {
+      const size_t row = (static_cast<size_t>(b) * nq + t0 + tok) * (p.Hkv * kGroup) + h * kGroup + (r & 15);
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + row * 128 + 64 * hf);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 u = __ldg(src + i);
+        qw[4 * i] = u.x;
+        qw[4 * i + 1] = u.y;
+        qw[4 * i + 2] = u.z;
+        qw[4 * i + 3] = u.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) qw[i] = 0u;
+    }
+  }
+
   for (int e = tid; e < r_rows * p.nbmax; e += kStThreads) r_all[e] = -INFINITY;
   if (tid == 0) {
     prefetch_tensormap(&kc_map);
@@ -267,23 +290,7 @@ __global__ void __launch_bounds__(kStThreads, 2)
     // q of this row, dims 64 hf .. 64 hf + 63, into TMEM columns
     // kStColQ + 32 hf .. + 31 as bf16 pairs: the A operand of the products.
     if (total > 0) {
-      uint32_t w[32];
-      if (active) {
-        const size_t row = (static_cast<size_t>(b) * nq + t0 + tok) * (p.Hkv * kGroup) + h * kGroup + x;
-        const uint4* src = reinterpret_cast<const uint4*>(p.q + row * 128 + 64 * hf);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 u = __ldg(src + i);
-          w[4 * i] = u.x;
-          w[4 * i + 1] = u.y;
-          w[4 * i + 2] = u.z;
-          w[4 * i + 3] = u.w;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) w[i] = 0u;
-      }
-      tc::st32(lane_addr + kStColQ + 32 * hf, w);
+      tc::st32(lane_addr + kStColQ + 32 * hf, qw);
       tc::wait_st();
       tc::fence_before_sync();
       __syncwarp();
