@@ -596,19 +596,20 @@ __device__ void select_topk_smem(const float* r, int nb, int n_init, int n_local
   }
   // 3. mark the taken candidates and the forced blocks; collect the boundary.
   if (!take_none) {
+    // A warp's 32 consecutive blocks are one bitmask word: one OR per word.
 #pragma unroll 1
-    for (int j = tid; j < nb; j += NT) {
-      const float x = r[j];
-      if (!is_cand(j, x)) continue;
+    for (int j0 = warp * 32; j0 < nb; j0 += NT) {
+      const int j = j0 + lane;
+      const float x = j < nb ? r[j] : -INFINITY;
+      const bool cnd = j < nb && is_cand(j, x);
       const uint32_t key = float_to_ordered(x);
       const uint32_t d = top - (key >> kShift);
       int dd = static_cast<int>(min(255u, d));
       if (lvl == 2) dd = d < 255u ? -1 : static_cast<int>(min(255u, (d - 255u) >> 4));
-      if (lvl == 0 || dd < bnd) {
-        atomicOr(&bits[j >> 5], 1u << (j & 31));
-      } else if (dd == bnd) {
+      const uint32_t take = __ballot_sync(0xffffffffu, cnd && (lvl == 0 || dd < bnd));
+      if (lane == 0 && take) atomicOr(&bits[j0 >> 5], take);
+      if (cnd && lvl > 0 && dd == bnd)
         surv[atomicAdd(&sm.ctrl[2], 1)] = (static_cast<unsigned long long>(key) << 32) | static_cast<uint32_t>(~j);
-      }
     }
   }
   for (int j = tid; j < n_first; j += NT) atomicOr(&bits[j >> 5], 1u << (j & 31));
@@ -631,33 +632,39 @@ __device__ void select_topk_smem(const float* r, int nb, int n_init, int n_local
     }
     __syncthreads();
   }
-  // 5. ascending output from the bitmask (one warp, one 32-word slice per pass).
+  // 5. ascending output from the bitmask: warp 0 turns the words' bit counts
+  //    into output positions (over the boundary list, which is done), then
+  //    every warp expands words, one lane per bit.
+  int* wpos = reinterpret_cast<int*>(surv);
   if (warp == 0) {
     int base = 0;
 #pragma unroll 1
     for (int w0 = 0; w0 < n_words; w0 += 32) {
-      uint32_t bw = (w0 + lane < n_words) ? bits[w0 + lane] : 0u;
-      const int cnt = __popc(bw);
+      const int cnt = (w0 + lane < n_words) ? __popc(bits[w0 + lane]) : 0;
       const int incl = warp_inclusive_scan(cnt);
-      int pos = base + incl - cnt;
-      while (bw) {
-        const int j = (w0 + lane) * 32 + __ffs(bw) - 1;
-        bw &= bw - 1u;
-        if (pos < k_max) {
-          out_idx[pos] = j;
-          if (sorted_copy) sorted_copy[pos] = j;
-        }
-        ++pos;
-      }
+      if (w0 + lane < n_words) wpos[w0 + lane] = base + incl - cnt;
       base += __shfl_sync(0xffffffffu, incl, 31);
     }
-    const int total = min(base, k_max);
-    for (int x = total + lane; x < k_max; x += 32) {
-      out_idx[x] = -1;
-      if (sorted_copy) sorted_copy[x] = -1;
-    }
-    if (lane == 0) *out_n = total;
+    if (lane == 0) sm.ctrl[3] = base;
   }
+  __syncthreads();
+  const int total = min(sm.ctrl[3], k_max);
+#pragma unroll 1
+  for (int w = warp; w < n_words; w += NWARP) {
+    const uint32_t bw = bits[w];
+    if ((bw >> lane) & 1u) {
+      const int pos = wpos[w] + __popc(bw & ((1u << lane) - 1u));
+      if (pos < k_max) {
+        out_idx[pos] = w * 32 + lane;
+        if (sorted_copy) sorted_copy[pos] = w * 32 + lane;
+      }
+    }
+  }
+  for (int x = total + tid; x < k_max; x += NT) {
+    out_idx[x] = -1;
+    if (sorted_copy) sorted_copy[x] = -1;
+  }
+  if (tid == 0) *out_n = total;
 }
 
 
