@@ -27,6 +27,7 @@ for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import statistics
@@ -99,17 +100,29 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# Source file of each kernel whose DRAM traffic is recorded; its hash, with the
-# device headers every kernel includes, dates the recorded counters.
+# Source file of each kernel whose DRAM traffic is recorded; its hash, with
+# every header it includes from the same folder (transitively), dates the
+# recorded counters.
 _KERNEL_SRC = {"decode_step_kernel": "decode_step.cu", "attn_tc_kernel": "attn_tc.cu", "sel_tc_kernel": "select_tc.cu",
                "bwd_dq_kernel": "attn_bwd.cu", "bwd_dkdv_kernel": "attn_bwd.cu"}
-_DEVICE_HEADERS = ("common.cuh", "tc.cuh", "topk.cuh", "select_common.cuh", "compress.cuh")
 
 
 def _src_hash(kernel: str):
-    h = hashlib.sha256()
     csrc = os.path.join(ROOT, "trainable_block_sparse_infllm_gb300", "csrc")
-    for fn in (_KERNEL_SRC[kernel],) + _DEVICE_HEADERS:
+    order = []
+
+    def visit(fn):
+        if fn in order:
+            return
+        order.append(fn)
+        for line in open(os.path.join(csrc, fn)):
+            m = re.match(r'\s*#include "([^"]+)"', line)
+            if m and os.path.exists(os.path.join(csrc, m.group(1))):
+                visit(m.group(1))
+
+    visit(_KERNEL_SRC[kernel])
+    h = hashlib.sha256()
+    for fn in order:
         h.update(open(os.path.join(csrc, fn), "rb").read())
     return h.hexdigest()[:16]
 
