@@ -12,11 +12,13 @@
 // One CTA per 8 consecutive tokens of one (b, h_kv): their 8 x 16 heads are
 // the 128 rows of the tcgen05 tile and share every 64-kernel chunk of kernel
 // means (causality gives the 8 tokens the same kernels but for the last one
-// or two).  z = q . hi + q . lo accumulates in TMEM (M 128, N 64, K 128, hi and
-// lo as two products into one accumulator); q, the A operand, sits in TMEM
-// too (the row warps write it there), so shared memory holds only the chunk
-// ring and the block scores and two CTAs fit on an SM while the scores are
-// small.  The chunks are streamed twice:
+// or two).  z = q . hi + q . lo comes from one product per chunk (M 128,
+// N 128, K 128): the chunk's 64 hi rows and 64 lo rows are the 128 rows of B,
+// so TMEM receives q . hi and q . lo side by side and the row threads add
+// them (an N = 128 product issues at a higher rate than two of N = 64).
+// q, the A operand, sits in TMEM too (the row warps write it there), so
+// shared memory holds only the chunk ring and the block scores and two CTAs
+// fit on an SM while the scores are small.  The chunks are streamed twice:
 //   pass 1: each row thread keeps its head's running (max, sum of 2^z)
 //           (over coarse windows instead, for the LSE approximation);
 //   pass 2: each row thread forms 2^(z - lse) for its head, and the 16 lanes
@@ -49,11 +51,11 @@ namespace {
 constexpr int kStTokens = 8;
 constexpr int kStChunk = 64;               // kernels per chunk
 constexpr int kStMaxStages = 3;            // ring depth at one CTA per SM (two stages when two CTAs fit)
-constexpr int kStChunkBytes = 32768;       // hi then lo: 64 rows x 256 B each
+constexpr int kStChunkBytes = 32768;       // per 64-dim box: 64 hi rows then 64 lo rows (128 B each)
 constexpr int kStRowWarps = 8;             // two per TMEM lane quadrant, 32 of a chunk's 64 kernels each
 constexpr int kStThreads = (kStRowWarps + 2) * 32;
 constexpr int kStMmaWarp = kStRowWarps, kStTmaWarp = kStRowWarps + 1;
-constexpr uint32_t kStTmemCols = 256;      // two z buffers of 64 columns, then q
+constexpr uint32_t kStTmemCols = 256;      // z (q . hi | q . lo, 64 columns each), then q
 constexpr uint32_t kStColQ = 128;          // q: 128 rows x 128 dims as bf16 pairs (the A operand)
 constexpr int kStTwoPerSmSmem = 112 * 1024;   // a request this small leaves room for a second CTA on the SM
 
@@ -89,7 +91,7 @@ __host__ __device__ inline StLayout st_layout(int nbmax, int stages, bool cluste
 }
 
 enum StBar { kFull = 0, kEmpty = kFull + kStMaxStages, kQ = kEmpty + kStMaxStages, kZFull = kQ + 1,
-             kZFree = kZFull + 2, kLse = kZFree + 2, kStNumBars = kLse + 1 };
+             kZFree = kZFull + 1, kLse = kZFree + 1, kStNumBars = kLse + 1 };
 
 // Barrier of the two row warps of TMEM lane quadrant q (ids 1..4).
 __device__ __forceinline__ void quad_pair_sync(int q) {
@@ -191,10 +193,8 @@ __global__ void __launch_bounds__(kStThreads, 2)
       mbar_init(&bars[kEmpty + s], 1);
     }
     mbar_init(&bars[kQ], kStRowWarps);   // q written to TMEM by the row warps
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars[kZFull + s], 1);
-      mbar_init(&bars[kZFree + s], kStRowWarps);
-    }
+    mbar_init(&bars[kZFull], 1);
+    mbar_init(&bars[kZFree], kStRowWarps);   // z read out: the next chunk's product may overwrite it
     mbar_init(&bars[kLse], 1);
     // Cluster form: the C partials of 128 rows arrive by st.async.
     if (csize > 1) mbar_arrive_expect_tx(&bars[kLse], csize * 128 * 8);
@@ -229,8 +229,8 @@ __global__ void __launch_bounds__(kStThreads, 2)
         const int row_lo = (bh * 2 + 1) * rows + ch * kStChunk;
         mbar_arrive_expect_tx(&bars[kFull + st], kStChunkBytes);
         tma_load_2d(dst, map, 0, row_hi, &bars[kFull + st]);
-        tma_load_2d(dst + 8192, map, 64, row_hi, &bars[kFull + st]);
-        tma_load_2d(dst + 16384, map, 0, row_lo, &bars[kFull + st]);
+        tma_load_2d(dst + 8192, map, 0, row_lo, &bars[kFull + st]);
+        tma_load_2d(dst + 16384, map, 64, row_hi, &bars[kFull + st]);
         tma_load_2d(dst + 24576, map, 64, row_lo, &bars[kFull + st]);
       }
     }
@@ -238,26 +238,24 @@ __global__ void __launch_bounds__(kStThreads, 2)
   } else if (warp == kStMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0 && total > 0) {
-      constexpr uint32_t kId = tc::idesc_bf16(128, 64, 0, 0);
+      constexpr uint32_t kId = tc::idesc_bf16(128, 128, 0, 0);
       bool ok = mbar_wait(&bars[kQ], 0, p.status);
       for (int it = 0; it < total && ok; ++it) {
-        const int st = it % S, zb = it & 1;
+        const int st = it % S;
         ok = mbar_wait(&bars[kFull + st], (it / S) & 1, p.status);
-        if (ok && it >= 2) ok = mbar_wait(&bars[kZFree + zb], ((it >> 1) - 1) & 1, p.status);
+        if (ok && it >= 1) ok = mbar_wait(&bars[kZFree], (it - 1) & 1, p.status);
         if (!ok) break;
         tc::fence_after_sync();
         const uint32_t stage = base_s + lay.ring + st * kStChunkBytes;
-        const uint64_t hi_desc = tc::sdesc_sw128(stage, 16, 1024);
-        const uint64_t lo_desc = tc::sdesc_sw128(stage + 16384, 16, 1024);
+        const uint64_t b_desc = tc::sdesc_sw128(stage, 16, 1024);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          // A: q from TMEM (16 dims = 8 columns per step); B: the chunk's
-          // hi and lo rows, dims 16 k .. 16 k + 15 of the 64-dim boxes.
-          const uint64_t tb = static_cast<uint64_t>(((k >> 2) * 8192 + (k & 3) * 32) >> 4);
-          tc::mma_ts(tmem + zb * 64, tmem + kStColQ + 8 * k, hi_desc + tb, kId, k > 0 ? 1u : 0u);
-          tc::mma_ts(tmem + zb * 64, tmem + kStColQ + 8 * k, lo_desc + tb, kId, 1u);
+          // A: q from TMEM (16 dims = 8 columns per step); B: the chunk's 128
+          // rows (hi, then lo), dims 16 k .. 16 k + 15 of the 64-dim boxes.
+          const uint64_t tb = static_cast<uint64_t>(((k >> 2) * 16384 + (k & 3) * 32) >> 4);
+          tc::mma_ts(tmem, tmem + kStColQ + 8 * k, b_desc + tb, kId, k > 0 ? 1u : 0u);
         }
-        tc::commit(&bars[kZFull + zb]);
+        tc::commit(&bars[kZFull]);
         tc::commit(&bars[kEmpty + st]);
       }
     }
@@ -328,19 +326,24 @@ __global__ void __launch_bounds__(kStThreads, 2)
         st_dsmem_f32(dsmem_addr(r_tok + j, static_cast<uint32_t>(tok % csize)), v);
     };
     for (int it = 0; it < total; ++it) {
-      const int zb = it & 1;
       const bool pass2 = it >= seg_c;
       const int kbase = (it < nch_a ? it : ch0 + (pass2 ? it - seg_c : it - nch_a)) * kStChunk;
       if (it == seg_c) end_pass1();
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars[kZFull + zb], (it >> 1) & 1, p.status));
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars[kZFull], it & 1, p.status));
       tc::fence_after_sync();
       uint32_t v[32];
-      tc::ld32(lane_addr + zb * 64 + col0, v);
-      const uint32_t vx = pass2 ? tc::ld1(lane_addr + zb * 64 + xcol) : 0u;
+      uint32_t vl[32];   // q . lo of the same kernels, 64 columns on
+      tc::ld32(lane_addr + col0, v);
+      tc::ld32(lane_addr + 64 + col0, vl);
+      uint32_t vx = pass2 ? tc::ld1(lane_addr + xcol) : 0u;
+      const uint32_t vxl = pass2 ? tc::ld1(lane_addr + 64 + xcol) : 0u;
       tc::wait_ld();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kZFree + zb]);
+      if (lane == 0) mbar_arrive(&bars[kZFree]);
+#pragma unroll
+      for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) + __uint_as_float(vl[k]));
+      vx = __float_as_uint(__uint_as_float(vx) + __uint_as_float(vxl));
       // This row's visible rows of the chunk: coarse windows in segment A for
       // a token that has one, fine kernels in B for a token that has none,
       // fine kernels in C.
