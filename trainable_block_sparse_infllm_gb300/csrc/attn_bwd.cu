@@ -28,7 +28,8 @@
 //     selected j, so no work is spent on unselected pairs):
 //         S = Q K^T, dP = dO V^T            (M 128 rows, N 64 keys, K 128)
 //         P, dS per row                     (4 warps, one row per thread)
-//         dV^T += dO^T P, dK^T += Q^T dS    (M 128 dims, N 64 keys, K 128 rows)
+//         dV^T += dO^T P, dK^T += Q^T dS    (M 128 dims, N 128 = 64 keys of hi
+//                                           then lo parts, K 128 rows)
 //     with dV^T and dK^T accumulated in TMEM over the item and added to the
 //     fp32 dK / dV rows at the end.
 // P and dS enter every bf16 product as hi + lo parts (16 significant bits).
@@ -414,8 +415,9 @@ constexpr int kBkTileBytes = 65536;          // q 32 KB + dO 32 KB (two 64-colum
 constexpr int kBkThreads = 192;              // warps 0-3 rows, 4 MMA, 5 TMA
 constexpr int kBkMmaWarp = 4, kBkTmaWarp = 5;
 constexpr uint32_t kBkTmemCols = 512;
-// TMEM: two S buffers, two dP buffers (64 columns each), dV^T, dK^T.
-constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320;
+// TMEM: two S buffers, two dP buffers (64 columns each), dV^T and dK^T
+// (128 columns each: the products of the hi parts, then of the lo parts).
+constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
 
 // Shared memory (offsets from the 1024-aligned base).
 constexpr int kOffKV = 0;                                   // K block 16 KB, V block 16 KB
@@ -529,7 +531,7 @@ __global__ void __launch_bounds__(kBkThreads, 1)
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = tc::idesc_bf16(128, 64, 0, 0);   // rows x keys, both K-major
-      constexpr uint32_t kIdG = tc::idesc_bf16(128, 64, 1, 1);   // dims x keys, both MN-major
+      constexpr uint32_t kIdG = tc::idesc_bf16(128, 128, 1, 1);   // dims x (hi | lo keys), both MN-major
       const uint64_t k_desc = tc::sdesc_sw128(base_s + kOffKV, 16, 1024);
       const uint64_t v_desc = tc::sdesc_sw128(base_s + kOffKV + 16384, 16, 1024);
       const uint32_t ps = base_s + kOffPS;
@@ -570,17 +572,13 @@ __global__ void __launch_bounds__(kBkThreads, 1)
           const uint64_t qt_desc = tc::sdesc_sw128(tile, 16384, 1024);
           const uint64_t ot_desc = tc::sdesc_sw128(tile + 32768, 16384, 1024);
           const uint64_t ph_desc = tc::sdesc_sw128(ps, 16384, 1024);
-          const uint64_t pl_desc = tc::sdesc_sw128(ps + 16384, 16384, 1024);
           const uint64_t sh_desc = tc::sdesc_sw128(ps + 32768, 16384, 1024);
-          const uint64_t sl_desc = tc::sdesc_sw128(ps + 49152, 16384, 1024);
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const uint64_t kd = static_cast<uint64_t>((k * 2048) >> 4);
             const uint32_t first = (m > 0 || k > 0) ? 1u : 0u;
             tc::mma_ss(tmem + kColDV, ot_desc + kd, ph_desc + kd, kIdG, first);
-            tc::mma_ss(tmem + kColDV, ot_desc + kd, pl_desc + kd, kIdG, 1u);
             tc::mma_ss(tmem + kColDK, qt_desc + kd, sh_desc + kd, kIdG, first);
-            tc::mma_ss(tmem + kColDK, qt_desc + kd, sl_desc + kd, kIdG, 1u);
           }
           tc::commit(&bars[kBTEmpty + st]);
           tc::commit(&bars[kBPFree]);
@@ -687,18 +685,20 @@ __global__ void __launch_bounds__(kBkThreads, 1)
       float* dvp = p.dv + (static_cast<size_t>(bh) * p.Lmax + key0) * kHeadDim + d;
       float* dkp = p.dk + (static_cast<size_t>(bh) * p.Lmax + key0) * kHeadDim + d;
 #pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t gv[32], gk[32];
-        tc::ld32(lane_addr + kColDV + cc * 32, gv);
-        tc::ld32(lane_addr + kColDK + cc * 32, gk);
+      for (int cc = 0; cc < 4; ++cc) {   // dV then dK, 32 keys at a time: hi part + lo part
+        const uint32_t col = (cc < 2 ? kColDV : kColDK) + (cc & 1) * 32;
+        uint32_t gh[32], gl[32];
+        tc::ld32(lane_addr + col, gh);
+        tc::ld32(lane_addr + col + 64, gl);
         tc::wait_ld();
+        float* dst = cc < 2 ? dvp : dkp;
+        const float f = cc < 2 ? 1.f : p.scale;
 #pragma unroll
         for (int x = 0; x < 32; ++x) {
-          const int key = cc * 32 + x;
-          if (key < nkeys) {
-            atomicAdd(dvp + static_cast<size_t>(key) * kHeadDim, __uint_as_float(gv[x]));
-            atomicAdd(dkp + static_cast<size_t>(key) * kHeadDim, __uint_as_float(gk[x]) * p.scale);
-          }
+          const int key = (cc & 1) * 32 + x;
+          if (key < nkeys)
+            atomicAdd(dst + static_cast<size_t>(key) * kHeadDim,
+                      (__uint_as_float(gh[x]) + __uint_as_float(gl[x])) * f);
         }
       }
     }
