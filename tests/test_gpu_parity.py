@@ -321,6 +321,41 @@ def test_decode_step_bad_kv_len(dev):
     assert run.nsel[0].eq(4).all().item()
 
 
+def test_append_decode_step_one_launch_long_cache(dev):
+    # The same check on a 131,072-token cache, where the step runs as
+    # clusters of up to 16 CTAs: the appended key and value are stored by
+    # CTA 0 and read by whichever CTA attends the local block.  Pinned host
+    # inputs; the newest kernel ends on the appended key for the first
+    # sequence (131072) and not for the second (99999).
+    import torch
+    import trainable_block_sparse_infllm_gb300 as T
+    inp = S.make_random(batch=2, n_kv_heads=2, kv_len=131072, n_q=1, topk=64, seed=58,
+                        kv_lens=[131072, 99999])
+    run = DeviceRun(inp, dev)
+    full_k, full_v = run.k.clone(), run.v.clone()
+    kc_full = run.blank_step_kernels()
+    run.step()
+    torch.cuda.synchronize()
+    out_ref, idx_ref = run.out.clone(), run.idx.clone()
+    k_new = torch.stack([full_k[b, :, int(L) - 1:int(L)] for b, L in enumerate(inp.kv_lens)]).cpu().pin_memory()
+    v_new = torch.stack([full_v[b, :, int(L) - 1:int(L)] for b, L in enumerate(inp.kv_lens)]).cpu().pin_memory()
+    q = run.q.cpu().pin_memory()
+    out = torch.empty(run.out.shape, dtype=torch.bfloat16).pin_memory()
+    run.blank_step_kernels()
+    for b, L in enumerate(inp.kv_lens):
+        run.k[b, :, int(L) - 1].view(torch.int16).fill_(0x7FC0)
+        run.v[b, :, int(L) - 1].view(torch.int16).fill_(0x7FC0)
+    run.idx.fill_(-7)
+    T.append_decode_step(run.p, q, k_new, v_new, run.k, run.v, run.lens, run.kc, run.idx, run.nsel, out)
+    torch.cuda.synchronize()
+    assert T.get_device_status(clear=True) == 0
+    assert torch.equal(run.k.view(torch.int16), full_k.view(torch.int16))
+    assert torch.equal(run.v.view(torch.int16), full_v.view(torch.int16))
+    assert torch.equal(run.kc.view(torch.int16), kc_full.view(torch.int16))
+    assert torch.equal(run.idx, idx_ref)
+    assert torch.equal(out.to(dev).view(torch.int16), out_ref.view(torch.int16))
+
+
 def test_append_decode_step_bad_kv_len(dev):
     # A sequence whose kv_len lies past max_kv_len: status flagged, its caches
     # untouched, an empty selection and a zero output; the other sequence's
